@@ -1,0 +1,188 @@
+"""ctypes binding of the C oracle plus the fp64 GEMM reference (test infrastructure)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ufp4_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+E1M2, INT4, E2M1 = 0, 1, 2
+RTNE, SR = 0, 1
+SCALE_FP32, SCALE_UE8M0 = 0, 1
+GRID_NAMES = {"e1m2": E1M2, "int4": INT4, "e2m1": E2M1}
+
+CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction, no fast math)."""
+    with _lock:
+        if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+            tmp = _LIB + f".tmp{os.getpid()}"
+            subprocess.check_call(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"])
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        build()
+        L = ctypes.CDLL(_LIB)
+        P = ctypes.c_void_p
+        i64, u64, u32, i32 = ctypes.c_int64, ctypes.c_uint64, ctypes.c_uint32, ctypes.c_int
+        L.orc_philox4x32_10.argtypes = [P, P, P]
+        L.orc_signs.argtypes = [u64, i32, P]
+        L.orc_rht_rows.argtypes = [P, i64, i64, i64, i32, u64, P]
+        L.orc_rht_rows.restype = i32
+        L.orc_quantize_rows.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, u64, i32, u64, i32,
+                                        u32, u32, P, P]
+        L.orc_quantize_rows.restype = i32
+        L.orc_quantize_cols.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, u64, i32, u64, i32,
+                                        u32, P, P]
+        L.orc_quantize_cols.restype = i32
+        L.orc_dequantize.argtypes = [P, P, i64, i64, i32, i32, i32, i32, i32, u64, i32, P]
+        L.orc_dequantize.restype = i32
+        L.orc_dequantize_f64.argtypes = [P, P, i64, i64, i32, i32, i32, i32, P]
+        L.orc_dequantize_f64.restype = i32
+        L.orc_level.argtypes = [i32, i32]
+        L.orc_level.restype = ctypes.c_double
+        L.orc_qmax.argtypes = [i32]
+        L.orc_qmax.restype = ctypes.c_double
+        L.orc_po2_exponent.argtypes = [ctypes.c_float, i32]
+        L.orc_po2_exponent.restype = i32
+        L.orc_round_rtne.argtypes = [i32, ctypes.c_float]
+        L.orc_round_rtne.restype = i32
+        L.orc_round_sr.argtypes = [i32, ctypes.c_float, u32]
+        L.orc_round_sr.restype = i32
+        _lib = L
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _grid(g) -> int:
+    return GRID_NAMES[g] if isinstance(g, str) else int(g)
+
+
+# ---------------------------------------------------------------- primitives
+def philox4x32_10(ctr, key) -> np.ndarray:
+    c = np.asarray(ctr, dtype=np.uint32).copy()
+    k = np.asarray(key, dtype=np.uint32).copy()
+    out = np.zeros(4, dtype=np.uint32)
+    lib().orc_philox4x32_10(_ptr(c), _ptr(k), _ptr(out))
+    return out
+
+
+def signs(sign_seed: int, n: int) -> np.ndarray:
+    out = np.zeros(n, dtype=np.int8)
+    lib().orc_signs(sign_seed, n, _ptr(out))
+    return out
+
+
+def level(grid, idx: int) -> float:
+    return lib().orc_level(_grid(grid), idx)
+
+
+def qmax(grid) -> float:
+    return lib().orc_qmax(_grid(grid))
+
+
+def po2_exponent(M: float, grid) -> int:
+    return lib().orc_po2_exponent(M, _grid(grid))
+
+
+def round_rtne(grid, a: float) -> int:
+    return lib().orc_round_rtne(_grid(grid), a)
+
+
+def round_sr(grid, a: float, u16: int) -> int:
+    return lib().orc_round_sr(_grid(grid), a, u16)
+
+
+# ---------------------------------------------------------------- tensors
+def _as_bf16(x: np.ndarray) -> np.ndarray:
+    if x.dtype != np.uint16:
+        raise TypeError("oracle inputs are bf16 bit patterns held in uint16 arrays")
+    return np.ascontiguousarray(x)
+
+
+def rht_rows(x_bf16: np.ndarray, n: int, sign_seed: int) -> np.ndarray:
+    x = _as_bf16(x_bf16)
+    rows, cols = x.shape
+    z = np.zeros((rows, cols), dtype=np.float32)
+    if lib().orc_rht_rows(_ptr(x), rows, cols, cols, n, sign_seed, _ptr(z)):
+        raise ValueError("unsupported RHT arguments")
+    return z
+
+
+def quantize(x_bf16: np.ndarray, *, grid="e1m2", block=(1, 16), n=16, sign_seed=0, rounding=RTNE,
+             sr_seed=0, scale_fmt=SCALE_FP32, colwise=False, group=0):
+    """Quantize a bf16 matrix; returns (codes uint8, scales float32|uint8).
+
+    Row-wise: codes [rows x cols/2], scales [rows/br x cols/bc].
+    Column-wise: the quantization of x^T, in x^T's layout."""
+    x = _as_bf16(x_bf16)
+    rows, cols = x.shape
+    g = _grid(grid)
+    br, bc = block
+    orows, ocols = (cols, rows) if colwise else (rows, cols)
+    codes = np.zeros((orows, ocols // 2), dtype=np.uint8)
+    sdt = np.float32 if scale_fmt == SCALE_FP32 else np.uint8
+    scales = np.zeros((orows // br, ocols // bc), dtype=sdt)
+    if colwise:
+        rc = lib().orc_quantize_cols(_ptr(x), rows, cols, cols, g, br, bc, n, sign_seed, rounding,
+                                     sr_seed, scale_fmt, group, _ptr(codes), _ptr(scales))
+    else:
+        rc = lib().orc_quantize_rows(_ptr(x), rows, cols, cols, g, br, bc, n, sign_seed, rounding,
+                                     sr_seed, scale_fmt, 0, group, _ptr(codes), _ptr(scales))
+    if rc:
+        raise ValueError("unsupported quantize arguments")
+    return codes, scales
+
+
+def dequantize(codes, scales, *, grid="e1m2", block=(1, 16), scale_fmt=SCALE_FP32, n=16,
+               sign_seed=0, inverse_rht=False) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    rows, half = codes.shape
+    cols = 2 * half
+    out = np.zeros((rows, cols), dtype=np.float32)
+    if lib().orc_dequantize(_ptr(codes), _ptr(scales), rows, cols, _grid(grid), block[0], block[1],
+                            scale_fmt, n, sign_seed, int(inverse_rht), _ptr(out)):
+        raise ValueError("unsupported dequantize arguments")
+    return out
+
+
+def dequantize_f64(codes, scales, *, grid="e1m2", block=(1, 16), scale_fmt=SCALE_UE8M0) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    rows, half = codes.shape
+    cols = 2 * half
+    out = np.zeros((rows, cols), dtype=np.float64)
+    if lib().orc_dequantize_f64(_ptr(codes), _ptr(scales), rows, cols, _grid(grid), block[0],
+                                block[1], scale_fmt, _ptr(out)):
+        raise ValueError("unsupported dequantize arguments")
+    return out
+
+
+def gemm_reference(a_codes, a_scales, b_codes, b_scales, *, grid="e1m2", block=(1, 16),
+                   scale_fmt=SCALE_UE8M0, a_rows=None) -> np.ndarray:
+    """D = Q(A) Q(B)^T in fp64 [UFP4 summary, section 方法: the quantized GEMM
+    Y^ = Q_G(X H') Q_G(W H')^T with Q_G the dequantized operand].  a_rows
+    optionally selects a subset of A's rows (sampled check of large shapes)."""
+    A = dequantize_f64(a_codes, a_scales, grid=grid, block=block, scale_fmt=scale_fmt)
+    if a_rows is not None:
+        A = A[np.asarray(a_rows)]
+    B = dequantize_f64(b_codes, b_scales, grid=grid, block=block, scale_fmt=scale_fmt)
+    return A @ B.T
