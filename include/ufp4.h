@@ -1,0 +1,235 @@
+/*
+ * ufp4.h -- C ABI of the GB300 (sm_103a) library for the UFP4 recipe's
+ * data-parallel hot path: the fused Random Hadamard Transform (RHT) + block
+ * scaled 4-bit quantizer that prepares the operands of the three training
+ * GEMMs, and the quantized GEMM that consumes them.
+ *
+ * Sources, cited as page + section/equation:
+ *  [UFP4-data]   UFP4 summary (hyper.ai, arXiv 2606.20381), section 数据集:
+ *                codebooks G (E2M1, E1M2, INT4), contiguous blocks, block scale
+ *                s_B = block amax / largest level, RTNE and SR rounding, and
+ *                Q_G(T) meaning the dequantized tensor.
+ *  [UFP4-method] same page, section 方法: Eq. H_2n (Sylvester recursion),
+ *                H'_n = S_n H_n, Eq. Y = XW^T = (XH')(WH')^T, Eq. of the
+ *                quantized GEMM Y^ = Q_G(XH') Q_G(WH')^T, RHT on FPROP, DGRAD
+ *                and WGRAD, SR on dY only, free choice of the scale hierarchy.
+ *  [2D-block]    "Stable FP4 Training via Transposition-Invariant Block
+ *                Quantization" tutorial: b x b square blocks (Eq. S(B)=S(B^T)),
+ *                truncation-free scale S = 2^ceil(log2(2M/(Qp-Qn))), and the
+ *                transposes in dX = dY W, dW = dY^T X.
+ *
+ * General rules
+ *  - Ownership: the caller allocates and owns every buffer.  Only the entry
+ *    points documented as such read or write host memory; all other pointers
+ *    are device pointers on the current CUDA device.
+ *  - Asynchrony: device work is enqueued on `stream` and the call returns
+ *    without waiting.  Argument errors are detected on the host before any
+ *    launch and return an error code; nothing is launched then.
+ *  - Layouts are row-major.  A matrix of `rows x cols` elements with leading
+ *    dimension `ld` holds element (r, c) at offset r*ld + c.  Byte matrices
+ *    of codes hold two 4-bit codes per byte, the lower column index in the low
+ *    nibble.
+ *  - Inputs are bf16 bit patterns.  Non-finite inputs, and blocks whose
+ *    absolute maximum after the RHT is nonzero but below 2^-120 or above
+ *    2^120, are outside the contract (outputs are then unspecified but the
+ *    call stays memory-safe).
+ *  - Thread safety: calls keep no host state between calls and may be made
+ *    from several threads on different streams.
+ */
+#ifndef UFP4_H_
+#define UFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    UFP4_OK = 0,
+    UFP4_ERR_INVALID_ARG = 1, /* a null pointer, a bad size or an inconsistent shape */
+    UFP4_ERR_UNSUPPORTED = 2, /* a valid combination this library does not implement */
+    UFP4_ERR_ALIGNMENT = 3,   /* a pointer or leading dimension breaks the alignment rule */
+    UFP4_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed */
+    UFP4_ERR_TIMEOUT = 5      /* a bounded device-side wait gave up (see ufp4_device_error) */
+} ufp4_status;
+
+/* Codebooks [UFP4-data].  Levels (non-negative magnitudes, 3-bit index 0..7):
+ *   E1M2: 0, 0.25, 0.5, ..., 1.75 (uniform, largest level 1.75)
+ *   INT4: 0, 1, ..., 7            (uniform, signed range -7..7, -8 unused)
+ *   E2M1: 0, 0.5, 1, 1.5, 2, 3, 4, 6 (non-uniform, largest level 6)
+ * Nibble encodings: E1M2 and E2M1 are sign << 3 | index (a zero level is
+ * always written as 0x0); INT4 is the two's complement of the signed level. */
+typedef enum { UFP4_GRID_E1M2 = 0, UFP4_GRID_INT4 = 1, UFP4_GRID_E2M1 = 2 } ufp4_grid;
+
+/* Rounding [UFP4-data; UFP4-method: RTNE for X and W, SR for dY]:
+ *   RTNE: nearest level, exact ties to the even index.
+ *   SR:   with lo <= |t| <= hi the neighbouring levels and p = (|t|-lo)/(hi-lo),
+ *         the magnitude rounds up iff u < p * 65536, u a 16-bit Philox4x32-10
+ *         draw: key = sr_seed, counter = (g lo32, g hi32, stream, group) with
+ *         g = (row-major linear index of the element in the output tensor) / 8,
+ *         stream 0 for the row-wise output and 1 for the column-wise one;
+ *         element j = index % 8 takes the low 16 bits of word j/2 when j is
+ *         even and the high 16 bits when j is odd. */
+typedef enum { UFP4_ROUND_RTNE = 0, UFP4_ROUND_SR = 1 } ufp4_round;
+
+/* Scale formats.
+ *   FP32:  s = fp32(M / qmax) [UFP4-data]; elements are scaled as
+ *          t = z * fp32(1/s) (an all-zero block has s = 0 and t = 0).
+ *          Only for 1-D blocks.
+ *   UE8M0: S = 2^e with e the smallest integer such that M <= qmax * 2^e
+ *          [2D-block, truncation-free scale, with Qp = -Qn = qmax], clamped
+ *          to [-127, 127]; stored as the byte e + 127.  Required for b x b
+ *          blocks and for GEMM operands. */
+typedef enum { UFP4_SCALE_FP32 = 0, UFP4_SCALE_UE8M0 = 1 } ufp4_scale_fmt;
+
+/* Output selection bits for ufp4_rht_quantize. */
+enum { UFP4_OUT_ROWWISE = 1, UFP4_OUT_COLWISE = 2 };
+
+/* What to compute.
+ *   grid        ufp4_grid
+ *   block_rows, block_cols
+ *               1 x 16 or 1 x 32 (1-D blocks along the quantized dimension),
+ *               or b x b with b in {8, 16, 32, 64} (2-D square blocks,
+ *               [2D-block]); for the column-wise output the block shape applies
+ *               to the transposed tensor.
+ *   hadamard_n  n = 2^k in {1, 2, ..., 256}; the RHT acts on each length-n
+ *               segment of the quantized dimension with the same signs
+ *               [UFP4-method].  n = 1 switches the transform off.
+ *   sign_seed   eps_i = 1 - 2 b_i, b_i = bit (i % 32) of word (i % 128) / 32 of
+ *               Philox4x32-10(key = sign_seed, counter = (i/128, 0, 2, 0)).
+ *   round, sr_seed   see ufp4_round.
+ *   scale_fmt   ufp4_scale_fmt.
+ *   out_mask    UFP4_OUT_ROWWISE | UFP4_OUT_COLWISE.
+ *   group       fourth Philox counter word of SR draws (the expert id in the
+ *               grouped calls, which set it themselves; 0 otherwise). */
+typedef struct {
+    int32_t grid;
+    int32_t block_rows;
+    int32_t block_cols;
+    int32_t hadamard_n;
+    uint64_t sign_seed;
+    int32_t round;
+    int32_t scale_fmt;
+    uint64_t sr_seed;
+    int32_t out_mask;
+    int32_t group;
+} ufp4_quant_desc;
+
+/* A quantized matrix in device memory, described in its own layout: the
+ * row-wise output of an R x C input has rows = R, cols = C; the column-wise
+ * output (the quantization of the transpose) has rows = C, cols = R.
+ *   codes      rows x cols/2 bytes, leading dimension codes_ld bytes
+ *              (multiple of 8, and of 16 for GEMM operands; the pointer
+ *              16-byte aligned)
+ *   scales     (rows/block_rows) x (cols/block_cols) elements, float for FP32
+ *              scales and uint8 for UE8M0, leading dimension scales_ld
+ *              elements (the pointer 4-byte aligned for float) */
+typedef struct {
+    void* codes;
+    void* scales;
+    int64_t rows;
+    int64_t cols;
+    int64_t codes_ld;
+    int64_t scales_ld;
+} ufp4_qtensor;
+
+/* ufp4_rht_quantize -- fused RHT + block-scaled 4-bit quantization.
+ * [UFP4-data] blocks, scale, rounding; [UFP4-method] z = x S_n H_n along the
+ * GEMM's shared dimension; [2D-block] square blocks and the transposed copy.
+ *   x        device bf16 [rows x cols], leading dimension ld elements
+ *            (ld >= cols, ld multiple of 8, x 16-byte aligned)
+ *   rowwise  written when out_mask has UFP4_OUT_ROWWISE: quantization of each
+ *            row (RHT and blocks along cols); rows x cols
+ *   colwise  written when out_mask has UFP4_OUT_COLWISE: quantization of x^T
+ *            (RHT and blocks along rows); cols x rows
+ * Both outputs come from one read of x.  Requirements: cols divisible by n
+ * and by the block width for the row-wise output, rows divisible by n and by
+ * the block width for the column-wise one (2-D blocks: both dimensions by b).
+ * The qtensor's rows/cols must equal the shapes above. */
+ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                              const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
+                              const ufp4_qtensor* colwise, cudaStream_t stream);
+
+/* ufp4_rht_quantize_grouped -- the same for a stack of groups (MoE experts).
+ *   x             device bf16 [total_rows x cols], leading dimension ld, the
+ *                 rows of group g being offsets[g] .. offsets[g+1]-1
+ *   offsets       HOST int64 array of num_groups + 1 nondecreasing row offsets,
+ *                 offsets[0] = 0, offsets[num_groups] = total_rows
+ *   rowwise       total_rows x cols: each group's row-wise quantization in its
+ *                 own rows; SR draws use the group's id and the row index
+ *                 within the group
+ *   colwise       the column-wise quantization of each group, stacked: group g
+ *                 has padded length P_g = round_up(c_g, lcm(n, block width))
+ *                 (missing rows read as zero), and occupies a cols x P_g
+ *                 row-major matrix starting at codes + cols * (Poff_g / 2)
+ *                 bytes and scales + cols * Poff_g / block_width elements,
+ *                 Poff_g = P_0 + ... + P_{g-1}; its qtensor has rows = cols
+ *                 and cols = sum of P_g, its *_ld fields are ignored.
+ *   desc->group   ignored (each group uses its index)
+ * 1-D blocks only. */
+ufp4_status ufp4_rht_quantize_grouped(const void* x, int64_t cols, int64_t ld,
+                                      const int64_t* offsets, int32_t num_groups,
+                                      const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
+                                      const ufp4_qtensor* colwise, cudaStream_t stream);
+
+/* Padded length P_g used by the grouped column-wise output (host helper). */
+int64_t ufp4_grouped_padded_rows(int64_t rows, const ufp4_quant_desc* desc);
+
+/* ufp4_rht_transform -- the RHT alone: z = fp32 result of x S_n H_n on each
+ * length-n segment of every row [UFP4-method], with exactly the arithmetic of
+ * the quantizer (signs, butterfly strides 1..n/2, one multiply by
+ * fp32(1/sqrt n)).
+ *   x  device bf16 [rows x cols], ld elements; z device float [rows x cols], ldz */
+ufp4_status ufp4_rht_transform(const void* x, int64_t rows, int64_t cols, int64_t ld,
+                               int32_t hadamard_n, uint64_t sign_seed, float* z, int64_t ldz,
+                               cudaStream_t stream);
+
+/* ufp4_dequantize -- Q_G(T) = level(code) * scale as fp32 [UFP4-data], in the
+ * qtensor's own layout (rows x cols, leading dimension ld_out elements).
+ * With inverse_rht != 0 the rotation is undone on each length-n segment of a
+ * row: x = z H'^T = (z H) S, same butterfly, then the signs.
+ * desc supplies grid, block shape, scale format, hadamard_n and sign_seed. */
+ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc,
+                            int32_t inverse_rht, float* out, int64_t ld_out, cudaStream_t stream);
+
+/* ufp4_gemm_workspace_size -- device scratch bytes ufp4_gemm needs for
+ * operands A (M x K) and B (N x K) quantized with desc. */
+ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4_quant_desc* desc,
+                                     size_t* bytes);
+
+/* ufp4_gemm -- the quantized GEMM consumer [UFP4-method, Eq. Y^ = Q_G(XH')
+ * Q_G(WH')^T]: D[M x N] = Q(A) Q(B)^T in fp32 with fp32 accumulation, A and B
+ * both quantized along K (K-major): A = the M x K qtensor, B = the N x K
+ * qtensor, same desc (UE8M0 scales; 1 x 16, 1 x 32 or 32 x 32 blocks).
+ * FPROP uses (X rowwise, W rowwise); DGRAD (dY rowwise, W colwise); WGRAD
+ * (dY colwise, X colwise).  E2M1 runs on the native block-scaled FP4 tensor
+ * path; E1M2 and INT4 levels are integers times a power of two and are
+ * widened exactly into FP8 (E5M2) in the workspace first.
+ *   D          device float, leading dimension ldd (multiple of 4, D 16-byte aligned)
+ *   workspace  device scratch of at least ufp4_gemm_workspace_size bytes,
+ *              256-byte aligned; contents on entry are ignored. */
+ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
+                      float* D, int64_t ldd, void* workspace, size_t workspace_bytes,
+                      cudaStream_t stream);
+
+/* ufp4_sign_vector -- the n signs eps_i of the RHT (HOST output, int8 +-1),
+ * for consumers that apply the rotation themselves. */
+ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host);
+
+/* ufp4_device_error -- reads and clears the library's device error word on
+ * the current device (synchronizes the device).  *code = 0 when no bounded
+ * wait has given up since the last call. */
+ufp4_status ufp4_device_error(int32_t* code);
+
+/* ufp4_status_string -- static, human-readable name of a status code. */
+const char* ufp4_status_string(ufp4_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* UFP4_H_ */

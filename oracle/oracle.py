@@ -44,7 +44,7 @@ def lib():
         L.orc_rht_rows.argtypes = [P, i64, i64, i64, i32, u64, P]
         L.orc_rht_rows.restype = i32
         L.orc_quantize_rows.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, u64, i32, u64, i32,
-                                        u32, u32, P, P]
+                                        u32, u32, u64, P, P]
         L.orc_quantize_rows.restype = i32
         L.orc_quantize_cols.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, u64, i32, u64, i32,
                                         u32, P, P]
@@ -127,11 +127,13 @@ def rht_rows(x_bf16: np.ndarray, n: int, sign_seed: int) -> np.ndarray:
 
 
 def quantize(x_bf16: np.ndarray, *, grid="e1m2", block=(1, 16), n=16, sign_seed=0, rounding=RTNE,
-             sr_seed=0, scale_fmt=SCALE_FP32, colwise=False, group=0):
+             sr_seed=0, scale_fmt=SCALE_FP32, colwise=False, group=0, row0=0):
     """Quantize a bf16 matrix; returns (codes uint8, scales float32|uint8).
 
     Row-wise: codes [rows x cols/2], scales [rows/br x cols/bc].
-    Column-wise: the quantization of x^T, in x^T's layout."""
+    Column-wise: the quantization of x^T, in x^T's layout.
+    row0 (row-wise only): index of x's first row in the whole tensor, used by
+    the SR counters when a band of rows is checked on its own."""
     x = _as_bf16(x_bf16)
     rows, cols = x.shape
     g = _grid(grid)
@@ -145,7 +147,7 @@ def quantize(x_bf16: np.ndarray, *, grid="e1m2", block=(1, 16), n=16, sign_seed=
                                      sr_seed, scale_fmt, group, _ptr(codes), _ptr(scales))
     else:
         rc = lib().orc_quantize_rows(_ptr(x), rows, cols, cols, g, br, bc, n, sign_seed, rounding,
-                                     sr_seed, scale_fmt, 0, group, _ptr(codes), _ptr(scales))
+                                     sr_seed, scale_fmt, 0, group, row0, _ptr(codes), _ptr(scales))
     if rc:
         raise ValueError("unsupported quantize arguments")
     return codes, scales

@@ -247,11 +247,13 @@ static uint32_t sr_draw(uint64_t sr_seed, uint64_t lin, uint32_t stream, uint32_
  *   codes  [rows x cols/2] bytes, row-major;
  *   scales [rows/block_rows x cols/block_cols], float (fp32 mode) or uint8
  *          UE8M0 bytes (e + 127).
+ * row0 is the index of x's first row in the whole tensor; it only enters the
+ * SR counters, so a band of rows can be checked on its own.
  * Returns 0, or 1 on an unsupported argument. */
 int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int grid,
                       int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
                       uint64_t sr_seed, int scale_fmt, uint32_t stream, uint32_t group,
-                      uint8_t* codes, void* scales) {
+                      uint64_t row0, uint8_t* codes, void* scales) {
     if (grid < 0 || grid > 2 || block_rows < 1 || block_cols < 2 || cols % 2) return 1;
     if (rows % block_rows || cols % block_cols) return 1;
     float* z = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
@@ -293,7 +295,7 @@ int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                     if (round == ORC_RTNE) {
                         idx = orc_round_rtne(grid, a);
                     } else {
-                        uint64_t lin = (uint64_t)r * (uint64_t)cols + (uint64_t)c;
+                        uint64_t lin = (row0 + (uint64_t)r) * (uint64_t)cols + (uint64_t)c;
                         idx = orc_round_sr(grid, a, sr_draw(sr_seed, lin, stream, group));
                     }
                     uint8_t nib = encode(grid, signbit(t) ? 1 : 0, idx);
@@ -319,7 +321,7 @@ int orc_quantize_cols(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) xt[c * rows + r] = x[r * ld + c];
     int rc = orc_quantize_rows(xt, cols, rows, rows, grid, block_rows, block_cols, n, sign_seed,
-                               round, sr_seed, scale_fmt, 1u, group, codes, scales);
+                               round, sr_seed, scale_fmt, 1u, group, 0u, codes, scales);
     free(xt);
     return rc;
 }

@@ -1,0 +1,332 @@
+// C ABI of the UFP4 library (declared in include/ufp4.h): host-side argument
+// validation, the sign vector, and dispatch to the kernels.  Nothing here
+// allocates device memory and no host state survives a call.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <cuda_runtime.h>
+
+#include "../../include/ufp4.h"
+#include "internal.h"
+
+using namespace ufp4;
+
+namespace {
+
+// Host Philox4x32-10 (Salmon et al., SC'11) for the sign vector.
+void philox_host(const uint32_t ctr[4], uint32_t k0, uint32_t k1, uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    for (int i = 0; i < 10; ++i) {
+        if (i) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0;
+        const uint64_t p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        c1 = (uint32_t)p1;
+        c3 = (uint32_t)p0;
+        c0 = n0;
+        c2 = n2;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+// eps_i = 1 - 2 * (bit (i % 32) of word (i % 128) / 32 of Philox(sign_seed, (i/128, 0, 2, 0))).
+int sign_bit(uint64_t seed, int i) {
+    const uint32_t ctr[4] = {(uint32_t)(i / 128), 0u, 2u, 0u};
+    uint32_t w[4];
+    philox_host(ctr, (uint32_t)seed, (uint32_t)(seed >> 32), w);
+    return (int)((w[(i % 128) / 32] >> (i % 32)) & 1u);
+}
+
+// Bit i (0..255) set <=> eps_{i mod n} = -1.  n = 1 switches the transform off.
+void make_sign_bits(uint64_t seed, int n, uint32_t bits[8]) {
+    std::memset(bits, 0, 8 * sizeof(uint32_t));
+    if (n <= 1) return;
+    int base[256];
+    for (int i = 0; i < n; ++i) base[i] = sign_bit(seed, i);
+    for (int i = 0; i < 256; ++i)
+        if (base[i % n]) bits[i / 32] |= 1u << (i % 32);
+}
+
+bool is_pow2(int64_t v) { return v >= 1 && (v & (v - 1)) == 0; }
+
+float inv_sqrt_n(int n) { return (float)(1.0 / std::sqrt((double)n)); }
+
+int num_sms_current() {
+    int dev = 0, sms = 148;
+    if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    return sms;
+}
+
+bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
+
+struct BlockShape {
+    bool is2d;
+    int b2d;   // side of 2-D blocks
+    int bw;    // width along the quantized dimension
+};
+
+ufp4_status check_desc(const ufp4_quant_desc* d, BlockShape* bs) {
+    if (!d) return UFP4_ERR_INVALID_ARG;
+    if (d->grid < 0 || d->grid > 2 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 1)
+        return UFP4_ERR_INVALID_ARG;
+    if (!is_pow2(d->hadamard_n) || d->hadamard_n > 256) return UFP4_ERR_INVALID_ARG;
+    if (d->block_rows == 1 && (d->block_cols == 16 || d->block_cols == 32)) {
+        *bs = {false, 0, d->block_cols};
+    } else if (d->block_rows == d->block_cols &&
+               (d->block_rows == 8 || d->block_rows == 16 || d->block_rows == 32 || d->block_rows == 64)) {
+        if (d->scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_INVALID_ARG;  // 2-D blocks: power-of-two scale
+        *bs = {true, d->block_rows, d->block_rows};
+    } else {
+        return UFP4_ERR_INVALID_ARG;
+    }
+    return UFP4_OK;
+}
+
+ufp4_status check_out(const ufp4_qtensor* q, int64_t rows, int64_t cols, const BlockShape& bs,
+                      int scale_fmt, bool grouped) {
+    if (!q || !q->codes || !q->scales) return UFP4_ERR_INVALID_ARG;
+    if (q->rows != rows || q->cols != cols) return UFP4_ERR_INVALID_ARG;
+    if (!aligned(q->codes, 16)) return UFP4_ERR_ALIGNMENT;
+    if (!aligned(q->scales, scale_fmt == UFP4_SCALE_FP32 ? 4 : 1)) return UFP4_ERR_ALIGNMENT;
+    if (grouped) return UFP4_OK;
+    if (q->codes_ld % 8) return UFP4_ERR_ALIGNMENT;
+    if (q->codes_ld < cols / 2) return UFP4_ERR_INVALID_ARG;
+    const int64_t sc_cols = cols / bs.bw;
+    if (q->scales_ld < sc_cols) return UFP4_ERR_INVALID_ARG;
+    return UFP4_OK;
+}
+
+ufp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? UFP4_OK : UFP4_ERR_CUDA; }
+
+// Shared body of the plain and grouped quantizer calls.
+ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64_t* offsets, int ngroups,
+                            bool grouped, const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
+                            const ufp4_qtensor* colwise, cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!x || cols < 0 || ld < cols || ngroups < 1 || ngroups > kMaxGroups) return UFP4_ERR_INVALID_ARG;
+    if (desc->out_mask < 1 || desc->out_mask > 3) return UFP4_ERR_INVALID_ARG;
+    const bool do_row = desc->out_mask & UFP4_OUT_ROWWISE;
+    const bool do_col = desc->out_mask & UFP4_OUT_COLWISE;
+    const int n = desc->hadamard_n;
+    if (grouped && bs.is2d) return UFP4_ERR_UNSUPPORTED;
+    if (do_col && n > 128) return UFP4_ERR_UNSUPPORTED;  // column pass keeps n <= 128
+    if (!aligned(x, 16) || ld % 8) return UFP4_ERR_ALIGNMENT;
+    const int64_t total_rows = offsets[ngroups];
+    if (offsets[0] != 0 || total_rows < 0) return UFP4_ERR_INVALID_ARG;
+    for (int g = 0; g < ngroups; ++g)
+        if (offsets[g + 1] < offsets[g]) return UFP4_ERR_INVALID_ARG;
+    // shape rules
+    if (cols % 16) return UFP4_ERR_INVALID_ARG;
+    if (do_row && (cols % n || cols % bs.bw)) return UFP4_ERR_INVALID_ARG;
+    if (bs.is2d && (total_rows % bs.b2d || cols % bs.b2d)) return UFP4_ERR_INVALID_ARG;
+    const int64_t unit = grouped ? (int64_t)std::max<int>(std::max(n, bs.bw), 16) : 1;
+    int64_t padded_total = 0;
+    int64_t pad0[kMaxGroups + 1];
+    pad0[0] = 0;
+    for (int g = 0; g < ngroups; ++g) {
+        const int64_t c = offsets[g + 1] - offsets[g];
+        const int64_t pc = grouped ? ((c + unit - 1) / unit) * unit : c;
+        pad0[g + 1] = pad0[g] + pc;
+    }
+    padded_total = pad0[ngroups];
+    if (do_col && !grouped && (total_rows % 16 || total_rows % n || total_rows % bs.bw))
+        return UFP4_ERR_INVALID_ARG;
+    if (do_row) {
+        st = check_out(rowwise, total_rows, cols, bs, desc->scale_fmt, false);
+        if (st != UFP4_OK) return st;
+    }
+    if (do_col) {
+        st = check_out(colwise, cols, padded_total, bs, desc->scale_fmt, grouped);
+        if (st != UFP4_OK) return st;
+    }
+    if (total_rows == 0 || cols == 0) return UFP4_OK;
+
+    QuantParams p;
+    std::memset(&p, 0, sizeof(p));
+    const int tc = (n == 256) ? 256 : 128;
+    const int tr = (tc == 256) ? 64 : 128;
+    p.x = (const uint16_t*)x;
+    p.cols = cols;
+    p.ld = ld;
+    p.n = n;
+    p.inv_sqrt_n = inv_sqrt_n(n);
+    make_sign_bits(desc->sign_seed, n, p.sign_bits);
+    p.is2d = bs.is2d;
+    p.b2d = bs.b2d;
+    p.bw_row = bs.bw;
+    p.bw_col = bs.bw;
+    p.col_seg_lanes = (bs.is2d ? std::max(n, 16) : std::max(std::max(n, bs.bw), 16)) / 16;
+    p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
+    p.do_row = do_row;
+    p.do_col = do_col;
+    p.vec256 = aligned(x, 32) && (ld % 16 == 0);
+    p.col_grouped = grouped;
+    if (do_row) p.row = {rowwise->codes, rowwise->scales, rowwise->codes_ld, rowwise->scales_ld};
+    if (do_col) p.col = {colwise->codes, colwise->scales, colwise->codes_ld, colwise->scales_ld};
+    p.col_tiles = (int)((cols + tc - 1) / tc);
+    p.num_groups = ngroups;
+    int64_t tiles = 0;
+    for (int g = 0; g <= ngroups; ++g) {
+        p.grp_row0[g] = offsets[g];
+        p.grp_pad0[g] = pad0[g];
+        p.grp_tile0[g] = (int)tiles;
+        if (g < ngroups) {
+            // the tile walk covers the padded rows when the column pass needs them
+            const int64_t len = do_col ? pad0[g + 1] - pad0[g] : offsets[g + 1] - offsets[g];
+            tiles += (len + tr - 1) / tr;
+        }
+    }
+    const int64_t num_tiles = tiles * p.col_tiles;
+    if (num_tiles == 0) return UFP4_OK;
+    if (num_tiles > 0x7FFFFFFF) return UFP4_ERR_UNSUPPORTED;
+    p.group_base = grouped ? 0 : desc->group;
+    return cuda_status(launch_quantize(p, desc->grid, desc->round == UFP4_ROUND_SR,
+                                       desc->scale_fmt == UFP4_SCALE_UE8M0, tc, (int)num_tiles, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* ufp4_status_string(ufp4_status s) {
+    switch (s) {
+        case UFP4_OK: return "UFP4_OK";
+        case UFP4_ERR_INVALID_ARG: return "UFP4_ERR_INVALID_ARG";
+        case UFP4_ERR_UNSUPPORTED: return "UFP4_ERR_UNSUPPORTED";
+        case UFP4_ERR_ALIGNMENT: return "UFP4_ERR_ALIGNMENT";
+        case UFP4_ERR_CUDA: return "UFP4_ERR_CUDA";
+        case UFP4_ERR_TIMEOUT: return "UFP4_ERR_TIMEOUT";
+    }
+    return "UFP4_ERR_UNKNOWN";
+}
+
+ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host) {
+    if (!out_host || !is_pow2(n) || n > 256) return UFP4_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i) out_host[i] = (n == 1) ? 1 : (int8_t)(1 - 2 * sign_bit(sign_seed, i));
+    return UFP4_OK;
+}
+
+ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, const ufp4_quant_desc* desc,
+                              const ufp4_qtensor* rowwise, const ufp4_qtensor* colwise, cudaStream_t stream) {
+    if (rows < 0 || !desc) return UFP4_ERR_INVALID_ARG;
+    if (desc->group < 0) return UFP4_ERR_INVALID_ARG;
+    const int64_t offsets[2] = {0, rows};
+    return quantize_common(x, cols, ld, offsets, 1, false, desc, rowwise, colwise, stream);
+}
+
+int64_t ufp4_grouped_padded_rows(int64_t rows, const ufp4_quant_desc* desc) {
+    if (!desc || rows < 0) return -1;
+    int bw = desc->block_rows == 1 ? desc->block_cols : desc->block_rows;
+    const int64_t unit = std::max<int64_t>(std::max<int64_t>(desc->hadamard_n, bw), 16);
+    return ((rows + unit - 1) / unit) * unit;
+}
+
+ufp4_status ufp4_rht_quantize_grouped(const void* x, int64_t cols, int64_t ld, const int64_t* offsets,
+                                      int32_t num_groups, const ufp4_quant_desc* desc,
+                                      const ufp4_qtensor* rowwise, const ufp4_qtensor* colwise,
+                                      cudaStream_t stream) {
+    if (!offsets || num_groups < 1) return UFP4_ERR_INVALID_ARG;
+    return quantize_common(x, cols, ld, offsets, num_groups, true, desc, rowwise, colwise, stream);
+}
+
+ufp4_status ufp4_rht_transform(const void* x, int64_t rows, int64_t cols, int64_t ld, int32_t n,
+                               uint64_t sign_seed, float* z, int64_t ldz, cudaStream_t stream) {
+    if (!x || !z || rows < 0 || cols < 0 || ld < cols || ldz < cols) return UFP4_ERR_INVALID_ARG;
+    if (!is_pow2(n) || n > 256 || cols % 16 || cols % n) return UFP4_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || ld % 8 || !aligned(z, 16) || ldz % 4) return UFP4_ERR_ALIGNMENT;
+    if (rows == 0 || cols == 0) return UFP4_OK;
+    SignBits sb;
+    make_sign_bits(sign_seed, n, sb.bits);
+    return cuda_status(launch_rht((const uint16_t*)x, rows, cols, ld, n, inv_sqrt_n(n), sb, z, ldz,
+                                  num_sms_current(), stream));
+}
+
+ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc, int32_t inverse_rht, float* out,
+                            int64_t ld_out, cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!q || !out || q->rows < 0 || q->cols < 0 || ld_out < q->cols) return UFP4_ERR_INVALID_ARG;
+    if (q->cols % 16 || q->cols % bs.bw || (bs.is2d && q->rows % bs.b2d)) return UFP4_ERR_INVALID_ARG;
+    if (inverse_rht && q->cols % desc->hadamard_n) return UFP4_ERR_INVALID_ARG;
+    st = check_out(q, q->rows, q->cols, bs, desc->scale_fmt, false);
+    if (st != UFP4_OK) return st;
+    if (q->rows == 0 || q->cols == 0) return UFP4_OK;
+    DequantParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.codes = (const uint8_t*)q->codes;
+    p.scales = q->scales;
+    p.rows = q->rows;
+    p.cols = q->cols;
+    p.codes_ld = q->codes_ld;
+    p.scales_ld = q->scales_ld;
+    p.grid = desc->grid;
+    p.br = bs.is2d ? bs.b2d : 1;
+    p.bc = bs.bw;
+    p.po2 = desc->scale_fmt == UFP4_SCALE_UE8M0;
+    p.n = desc->hadamard_n;
+    p.inverse = inverse_rht ? 1 : 0;
+    p.inv_sqrt_n = inv_sqrt_n(desc->hadamard_n);
+    make_sign_bits(desc->sign_seed, desc->hadamard_n, p.sign_bits);
+    p.out = out;
+    p.ld_out = ld_out;
+    return cuda_status(launch_dequantize(p, num_sms_current(), stream));
+}
+
+ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4_quant_desc* desc, size_t* bytes) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!bytes || M < 0 || N < 0 || K < 0) return UFP4_ERR_INVALID_ARG;
+    *bytes = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
+    return UFP4_OK;
+}
+
+ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
+                      int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!A || !B || !D) return UFP4_ERR_INVALID_ARG;
+    if (desc->scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_UNSUPPORTED;
+    if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
+    if (K % 32 && !(bs.bw == 16 && K % 16 == 0)) return UFP4_ERR_INVALID_ARG;
+    st = check_out(A, M, K, bs, UFP4_SCALE_UE8M0, false);
+    if (st != UFP4_OK) return st;
+    st = check_out(B, N, K, bs, UFP4_SCALE_UE8M0, false);
+    if (st != UFP4_OK) return st;
+    if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
+    if (!aligned(D, 16) || ldd % 4) return UFP4_ERR_ALIGNMENT;
+    const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
+    if (workspace_bytes < need || (need && !workspace)) return UFP4_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return UFP4_ERR_ALIGNMENT;
+    if (M == 0 || N == 0) return UFP4_OK;
+    GemmArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.a = {(const uint8_t*)A->codes, (const uint8_t*)A->scales, M, A->codes_ld, A->scales_ld};
+    g.b = {(const uint8_t*)B->codes, (const uint8_t*)B->scales, N, B->codes_ld, B->scales_ld};
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.grid = desc->grid;
+    g.br = bs.is2d ? bs.b2d : 1;
+    g.bc = bs.bw;
+    g.D = D;
+    g.ldd = ldd;
+    g.workspace = workspace;
+    g.workspace_bytes = workspace_bytes;
+    const cudaError_t e = launch_gemm(g, num_sms_current(), stream);
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+}  // extern "C"

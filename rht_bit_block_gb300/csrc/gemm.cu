@@ -1,0 +1,598 @@
+// Quantized GEMM consumer D = Q(A) Q(B)^T (UFP4 summary, section 方法, the
+// quantized GEMM Y^ = Q_G(X H') Q_G(W H')^T) on the sm_103a tensor cores.
+//
+// Both operands are K-major 4-bit codes with UE8M0 (power-of-two) block
+// scales, so every product is exact in a block-scaled MMA:
+//  * E2M1 codes are native FP4: kind::mxf4nvf4 reads the packed nibbles
+//    straight from the quantizer's output (1 x 16 blocks: scale_vec::4X, one
+//    scale per 16 elements; 1 x 32 and 32 x 32 blocks: scale_vec::2X).
+//  * E1M2 / INT4 levels are integers k (|k| <= 7) times a power of two.  A
+//    prep kernel widens them into FP8 E5M2 (exact) in the workspace and folds
+//    the block scales into one UE8M0 scale per 32 elements (kind::mxf8f6f4,
+//    scale_vec::1X): for a pair of 1 x 16 blocks with exponents e0, e1 the
+//    hardware scale is max(e0, e1) and the elements of the smaller block are
+//    shifted down by the difference d (exact for d <= 16 in E5M2).
+//
+// Kernel: one CTA per 128 x BN output tile, 8 warps.  Warp 0 lane 0 drives
+// TMA (128B-swizzled 2-D tiles of A and B, 512-byte scale chunks) through a
+// ring of mbarriers; warp 1 lane 0 copies the scales into tensor memory
+// (tcgen05.cp) and issues the MMAs (tcgen05.mma, accumulator in TMEM);
+// warps 4..7 read the accumulator back (tcgen05.ld) and store fp32.  Every
+// wait is bounded: on expiry the kernel records an error code and returns.
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/ufp4.h"
+#include "internal.h"
+
+namespace ufp4 {
+
+__device__ int g_device_error;
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBKBytes = 128;          // bytes of K per stage per row (one 128B swizzle row)
+constexpr int kGemmThreads = 256;
+constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes, tcgen05.cp 32x128b layout
+constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr int kErrTimeout = 1;
+
+// ------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and records the error)
+// when the limit is reached.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    atomicExch(&g_device_error, kErrTimeout);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// K-major, 128-byte swizzle shared-memory matrix descriptor: 8-row groups
+// 1024 bytes apart (stride byte offset), fixed version bits 0b001 at 46..48,
+// swizzle mode 2 (128B) at 61..63.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(1024u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+// Plain (no swizzle) descriptor for a 32-row x 16-byte scale chunk quarter:
+// 8-row core matrices 128 bytes apart.
+__device__ __forceinline__ uint64_t plain_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+template <int KIND>  // 0: mxf8f6f4 scale_vec::1X, 1: mxf4 scale_vec::2X, 2: mxf4nvf4 scale_vec::4X
+__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                    uint32_t sfb, uint32_t accumulate) {
+    if (KIND == 0) {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    } else if (KIND == 1) {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    }
+}
+
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t r[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Instruction descriptor of the block-scaled kinds: B scale id at 4..5,
+// A/B formats at 7..9 / 10..12, N>>3 at 17..22, UE8M0 scale type at 23,
+// M>>4 at 24..28, A scale id at 29..30; both operands K-major.
+__host__ __device__ constexpr uint32_t make_idesc(int afmt, int bfmt, int M, int N, int sf_id) {
+    return ((uint32_t)sf_id << 4) | ((uint32_t)afmt << 7) | ((uint32_t)bfmt << 10) |
+           ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+}
+
+// --------------------------------------------------------------- kernel
+// KIND 0: FP8 E5M2 operands (4 MMAs of K=32 per stage, one scale chunk per
+// 128 rows); KIND 1/2: packed FP4 (4 MMAs of K=64 per stage; 2 or 4 scales per
+// MMA -> 2 or 4 chunks per 128 rows per stage).
+template <int KIND, int BN, int STAGES>
+struct GemmCfg {
+    static constexpr int kChunksPerStage = KIND == 0 ? 1 : (KIND == 1 ? 2 : 4);
+    static constexpr int kABytes = kBM * kBKBytes;    // 16 KB, multiple of 1024
+    static constexpr int kBBytes = BN * kBKBytes;     // 32 KB
+    static constexpr int kSfaBytes = kChunksPerStage * kChunkBytes;
+    static constexpr int kSfbBytes = (BN / 128) * kChunksPerStage * kChunkBytes;
+    static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes landing per stage
+    // shared memory: [A x STAGES][B x STAGES][SFA x STAGES][SFB x STAGES][barriers, flags]
+    static constexpr int kOffB = STAGES * kABytes;
+    static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
+    static constexpr int kOffSfb = kOffSfa + STAGES * kSfaBytes;
+    static constexpr int kOffBars = kOffSfb + STAGES * kSfbBytes;
+    static constexpr int kSmem = kOffBars + 8 * (2 * STAGES + 1) + 16 + 1024 /*alignment slack*/;
+    // tensor memory: accumulator (BN fp32 columns) then the scale rings;
+    // one 512-byte chunk occupies 4 columns (32 lanes, replicated 4x).
+    static constexpr int kSfaColsPerStage = kChunksPerStage * 4;
+    static constexpr int kSfbColsPerStage = kChunksPerStage * 4 * (BN / 128);
+    static constexpr int kTmemCols = 512;
+    static constexpr int kAccCol = 0;
+    static constexpr int kSfaCol = BN;
+    static constexpr int kSfbCol = BN + STAGES * kSfaColsPerStage;
+    static_assert(kSfbCol + STAGES * kSfbColsPerStage <= kTmemCols, "tensor memory overflow");
+    static_assert(kSmem <= 232448, "shared memory overflow");
+};
+
+struct GemmKParams {
+    const uint8_t* sfa;  // scale chunks of A: [ceil(M/128)][k chunks] x 512 B
+    const uint8_t* sfb;
+    int64_t sf_chunks_k;  // chunks along K per 128-row block
+    int M, N, k_tiles;
+    float* D;
+    int64_t ldd;
+    uint32_t idesc[4];  // per MMA within a stage (scale ids)
+};
+
+template <int KIND, int BN, int STAGES>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+            const GemmKParams p) {
+    using C = GemmCfg<KIND, BN, STAGES>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024-byte alignment
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + C::kOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    const uint32_t acc_bar = bars + 8u * (2 * STAGES);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * (2 * STAGES + 1));
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * (2 * STAGES + 1) + 4);
+
+    auto stage_a = [&](int s) { return base + s * C::kABytes; };
+    auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
+    auto stage_sfa = [&](int s) { return base + C::kOffSfa + s * C::kSfaBytes; };
+    auto stage_sfb = [&](int s) { return base + C::kOffSfb + s * C::kSfbBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int m0 = blockIdx.y * kBM;
+    const int n0 = blockIdx.x * BN;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(acc_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer
+        const uint8_t* sfa_blk = p.sfa + (int64_t)blockIdx.y * p.sf_chunks_k * kChunkBytes;
+        int issued = 0;
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+            const int s = kt % STAGES;
+            if (kt >= STAGES && !mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            mbar_expect_tx(full_bar(s), C::kTxBytes);
+            tma_load_2d(stage_a(s), &tmap_a, kt * kBKBytes, m0, full_bar(s));
+            tma_load_2d(stage_b(s), &tmap_b, kt * kBKBytes, n0, full_bar(s));
+            bulk_load(stage_sfa(s), sfa_blk + (int64_t)kt * C::kSfaBytes, C::kSfaBytes, full_bar(s));
+            for (int h = 0; h < BN / 128; ++h) {
+                const uint8_t* src =
+                    p.sfb + ((int64_t)(n0 / 128 + h) * p.sf_chunks_k + (int64_t)kt * C::kChunksPerStage) * kChunkBytes;
+                bulk_load(stage_sfb(s) + h * C::kChunksPerStage * kChunkBytes, src, C::kChunksPerStage * kChunkBytes,
+                          full_bar(s));
+            }
+            issued = kt + 1;
+        }
+        if (*abort_flag) {
+            // let the copies already issued land before the CTA leaves (bounded)
+            for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt)
+                mbar_wait(full_bar(kt % STAGES), (kt / STAGES) & 1);
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ----------------------------------------------------- MMA issuer
+        for (int kt = 0; kt < p.k_tiles; ++kt) {
+            const int s = kt % STAGES;
+            if (!mbar_wait(full_bar(s), (kt / STAGES) & 1)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            tc_fence_after();
+            const uint32_t sfa_t = tmem + C::kSfaCol + s * C::kSfaColsPerStage;
+            const uint32_t sfb_t = tmem + C::kSfbCol + s * C::kSfbColsPerStage;
+            // chunk c of A -> columns 4c; chunk c of B's row half h -> columns 4(c*(BN/128) + h)
+            for (int c = 0; c < C::kChunksPerStage; ++c)
+                tc_cp_scales(sfa_t + 4 * c, plain_desc(stage_sfa(s) + c * kChunkBytes));
+            for (int h = 0; h < BN / 128; ++h)
+                for (int c = 0; c < C::kChunksPerStage; ++c)
+                    tc_cp_scales(sfb_t + 4 * (c * (BN / 128) + h),
+                                 plain_desc(stage_sfb(s) + (h * C::kChunksPerStage + c) * kChunkBytes));
+            const uint64_t da = sw128_desc(stage_a(s));
+            const uint64_t db = sw128_desc(stage_b(s));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                // chunk holding MMA j's scales: FP8 1X -> 0 (byte j), FP4 2X -> j/2 (bytes 0-1 / 2-3), FP4 4X -> j
+                const int chunk = KIND == 0 ? 0 : (KIND == 1 ? j / 2 : j);
+                // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
+                mma<KIND>(tmem + C::kAccCol, da + 2 * j, db + 2 * j, p.idesc[j], sfa_t + 4 * chunk,
+                          sfb_t + 4 * chunk * (BN / 128), (kt > 0 || j > 0) ? 1u : 0u);
+            }
+            tc_commit(empty_bar(s));
+        }
+        tc_commit(acc_bar);  // arrives once every MMA issued above has completed
+    } else if (warp >= 4) {
+        // ------------------------------------------------------- epilogue
+        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0));  // warp-uniform before .sync.aligned loads
+        tc_fence_after();
+        if (ok && !*abort_flag) {
+            const int q = warp - 4;  // TMEM lane quadrant of this warp
+            const int row = m0 + q * 32 + lane;
+            for (int c = 0; c < BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol + c, r);
+                if (row < p.M) {
+                    float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
+                    if (n0 + c + 32 <= p.N) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4*>(dst + i) = make_float4(
+                                __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
+                                __uint_as_float(r[i + 3]));
+                    } else {
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + c + i < p.N) dst[i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+    }
+}
+
+// ------------------------------------------------------------- prep kernels
+// Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
+// elements.  One thread: one row, one 128-element K group (4 scale cells).
+__device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ int signed_level(int grid, uint32_t nib) {
+    if (grid == 1) return (nib & 8u) ? (int)nib - 16 : (int)nib;
+    return (nib & 8u) ? -(int)(nib & 7u) : (int)(nib & 7u);
+}
+
+__device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-149, 127]
+    if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+    if (e < -149) return 0.0f;
+    return __uint_as_float(1u << (e + 149));
+}
+
+struct PrepParams {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    int64_t rows, K, codes_ld, scales_ld;
+    int grid, br, bc;
+    uint8_t* out_fp8;      // rows x K (E1M2/INT4 only)
+    uint8_t* out_chunks;   // ceil(rows/128) x chunks_k x 512
+    int64_t chunks_k;
+    int hw_block;          // 16 (E2M1 1x16) or 32
+    int64_t rows_cover;    // chunk rows written: rows rounded up to the GEMM tile
+};
+
+__device__ __forceinline__ int64_t chunk_offset(int64_t row, int64_t cell, int64_t chunks_k) {
+    return ((row / 128) * chunks_k + cell) * kChunkBytes + (row % 32) * 16 + ((row % 128) / 32) * 4;
+}
+
+__device__ __forceinline__ int src_scale(const PrepParams& p, int64_t row, int64_t k_elem) {
+    // UE8M0 byte of the block holding (row, k_elem)
+    return p.scales[(row / p.br) * p.scales_ld + k_elem / p.bc];
+}
+
+__global__ void prep_widen_kernel(const PrepParams p) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= p.rows_cover * p.chunks_k) return;
+    const int64_t row = idx / p.chunks_k;
+    const int64_t cell = idx % p.chunks_k;  // 4 scale bytes = 128 K elements
+    uint32_t cellv = 0;
+    const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
+    for (int j = 0; j < 4; ++j) {
+        const int64_t k0 = cell * 128 + j * 32;
+        int hw = 0;
+        if (row < p.rows && k0 < p.K) {
+            int H = src_scale(p, row, k0);
+            if (p.bc == 16) H = max(H, src_scale(p, row, k0 + 16));
+            hw = max(H + step_log2, 0);
+            // 32 elements -> 32 bytes
+            uint32_t outw[8];
+            const uint8_t* cp = p.codes + row * p.codes_ld + k0 / 2;
+            const uint4 cw = *reinterpret_cast<const uint4*>(cp);
+            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            for (int h = 0; h < 2; ++h) {
+                const int e = (p.bc == 16) ? src_scale(p, row, k0 + 16 * h) : src_scale(p, row, k0);
+                const float mult = pow2f(e + step_log2 - hw);
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t w = words[2 * h + q / 2];
+                    const int sh = (q & 1) * 16;
+                    const float v0 = (float)signed_level(p.grid, (w >> sh) & 0xF) * mult;
+                    const float v1 = (float)signed_level(p.grid, (w >> (sh + 4)) & 0xF) * mult;
+                    const float v2 = (float)signed_level(p.grid, (w >> (sh + 8)) & 0xF) * mult;
+                    const float v3 = (float)signed_level(p.grid, (w >> (sh + 12)) & 0xF) * mult;
+                    outw[h * 4 + q] = cvt_e5m2x2(v1, v0) | (cvt_e5m2x2(v3, v2) << 16);
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(p.out_fp8 + row * p.K + k0);
+            dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+        }
+        cellv |= (uint32_t)hw << (8 * j);
+    }
+    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(row, cell, p.chunks_k)) = cellv;
+}
+
+// E2M1: only the scales move, into the chunk layout (hw_block 16 or 32).
+__global__ void prep_scales_kernel(const PrepParams p) {
+    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (idx >= p.rows_cover * p.chunks_k) return;
+    const int64_t row = idx / p.chunks_k;
+    const int64_t cell = idx % p.chunks_k;
+    uint32_t cellv = 0;
+    for (int j = 0; j < 4; ++j) {
+        const int64_t k0 = (cell * 4 + j) * p.hw_block;
+        int b = 0;
+        if (row < p.rows && k0 < p.K) b = src_scale(p, row, k0);
+        cellv |= (uint32_t)b << (8 * j);
+    }
+    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(row, cell, p.chunks_k)) = cellv;
+}
+
+// ------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiledFn)f;
+    }
+    return fn;
+}
+
+// 2-D byte tensor (rows x row_bytes, pitch bytes) read in boxes of 128 bytes x box_rows, 128B swizzle.
+bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes, int64_t pitch, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch};
+    const cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Plan {
+    int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X
+    int64_t k_bytes;   // bytes of K per row in the MMA operand
+    int64_t k_tiles;
+    int64_t chunks_k;  // scale chunks along K per 128 rows (multiple of chunks per stage)
+    size_t fp8_a, fp8_b, sfa, sfb;  // workspace offsets
+    size_t total;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
+    Plan pl{};
+    (void)br;
+    pl.kind = grid == 2 ? (bc == 16 ? 2 : 1) : 0;
+    pl.k_bytes = grid == 2 ? K / 2 : K;
+    pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
+    const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
+    pl.chunks_k = pl.k_tiles * cps;
+    const int64_t mb = (M + 127) / 128, nb = (N + 255) / 256 * 2;  // B chunks cover the 256-row tile
+    size_t off = 0;
+    if (pl.kind == 0) {
+        pl.fp8_a = off;
+        off = align256(off + (size_t)M * K);
+        pl.fp8_b = off;
+        off = align256(off + (size_t)N * K);
+    }
+    pl.sfa = off;
+    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes);
+    pl.sfb = off;
+    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes);
+    pl.total = off;
+    return pl;
+}
+
+template <int KIND, int BN, int STAGES>
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKParams& kp, cudaStream_t st) {
+    using C = GemmCfg<KIND, BN, STAGES>;
+    auto k = gemm_kernel<KIND, BN, STAGES>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    dim3 grid((kp.N + BN - 1) / BN, (kp.M + kBM - 1) / kBM);
+    k<<<grid, kGemmThreads, C::kSmem, st>>>(ma, mb, kp);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
+    return make_plan(M, N, K, grid, br, bc).total;
+}
+
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
+    (void)num_sms;
+    if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
+    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
+    if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+    uint8_t* ws = (uint8_t*)g.workspace;
+    // operand prep
+    for (int side = 0; side < 2; ++side) {
+        const GemmOperand& op = side ? g.b : g.a;
+        PrepParams pp{};
+        pp.codes = op.codes;
+        pp.scales = op.scales;
+        pp.rows = op.rows;
+        pp.K = g.K;
+        pp.codes_ld = op.codes_ld;
+        pp.scales_ld = op.scales_ld;
+        pp.grid = g.grid;
+        pp.br = g.br;
+        pp.bc = g.bc;
+        pp.out_fp8 = pl.kind == 0 ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
+        pp.out_chunks = ws + (side ? pl.sfb : pl.sfa);
+        pp.chunks_k = pl.chunks_k;
+        pp.hw_block = pl.kind == 2 ? 16 : 32;
+        // chunk rows cover whole output tiles (128 rows for A, 256 for B)
+        pp.rows_cover = side ? ((op.rows + 255) / 256) * 256 : ((op.rows + 127) / 128) * 128;
+        const int64_t threads = pp.rows_cover * pl.chunks_k;
+        const int tb = 256;
+        const unsigned blocks = (unsigned)((threads + tb - 1) / tb);
+        if (pl.kind == 0) prep_widen_kernel<<<blocks, tb, 0, st>>>(pp);
+        else prep_scales_kernel<<<blocks, tb, 0, st>>>(pp);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    CUtensorMap ma, mb;
+    const void* a_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
+    const void* b_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
+    const int64_t a_pitch = pl.kind == 0 ? g.K : g.a.codes_ld;
+    const int64_t b_pitch = pl.kind == 0 ? g.K : g.b.codes_ld;
+    constexpr int BN = 256;
+    if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, BN)) return cudaErrorInvalidValue;
+    GemmKParams kp{};
+    kp.sfa = ws + pl.sfa;
+    kp.sfb = ws + pl.sfb;
+    kp.sf_chunks_k = pl.chunks_k;
+    kp.M = (int)g.M;
+    kp.N = (int)g.N;
+    kp.k_tiles = (int)pl.k_tiles;
+    kp.D = g.D;
+    kp.ldd = g.ldd;
+    if (pl.kind == 0) {
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, j);  // E5M2 x E5M2
+        return run_gemm<0, BN, 4>(ma, mb, kp, st);
+    }
+    if (pl.kind == 1) {
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, (j % 2) * 2);  // E2M1
+        return run_gemm<1, BN, 4>(ma, mb, kp, st);
+    }
+    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, 0);
+    return run_gemm<2, BN, 3>(ma, mb, kp, st);
+}
+
+}  // namespace ufp4
+
+extern "C" ufp4_status ufp4_device_error(int32_t* code) {
+    if (!code) return UFP4_ERR_INVALID_ARG;
+    int v = 0;
+    if (cudaDeviceSynchronize() != cudaSuccess) return UFP4_ERR_CUDA;
+    if (cudaMemcpyFromSymbol(&v, ufp4::g_device_error, sizeof(int)) != cudaSuccess) return UFP4_ERR_CUDA;
+    const int zero = 0;
+    if (v && cudaMemcpyToSymbol(ufp4::g_device_error, &zero, sizeof(int)) != cudaSuccess) return UFP4_ERR_CUDA;
+    *code = v;
+    return UFP4_OK;
+}

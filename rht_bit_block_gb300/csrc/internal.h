@@ -1,0 +1,81 @@
+// Internal launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ufp4 {
+
+constexpr int kMaxGroups = 64;
+
+struct SignBits {
+    uint32_t bits[8];  // bit i set <=> eps_{i mod n} = -1, for i in 0..255
+};
+
+struct QOut {
+    void* codes;
+    void* scales;
+    int64_t codes_ld;   // bytes
+    int64_t scales_ld;  // elements
+};
+
+// Everything one quantizer launch needs (passed by value as the kernel parameter).
+struct QuantParams {
+    const uint16_t* x;
+    int64_t cols, ld;
+    int n;
+    float inv_sqrt_n;
+    uint32_t sign_bits[8];
+    int is2d, b2d;      // 2-D square blocks of side b2d
+    int bw_row, bw_col; // 1-D block widths (or b2d)
+    int col_seg_lanes;  // lanes sharing one column segment in the column pass
+    uint64_t sr_seed;
+    int do_row, do_col, vec256, col_grouped;
+    QOut row, col;
+    int col_tiles;
+    int group_base;  // SR counter group id of group 0 (the caller's id when not grouped)
+    int num_groups;
+    int64_t grp_row0[kMaxGroups + 1];  // input row offsets
+    int64_t grp_pad0[kMaxGroups + 1];  // padded row offsets (column-wise output)
+    int grp_tile0[kMaxGroups + 1];     // first row tile of each group
+};
+
+cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int num_tiles,
+                            cudaStream_t st);
+cudaError_t launch_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n,
+                       float inv_sqrt_n, const SignBits& sb, float* z, int64_t ldz, int num_sms,
+                       cudaStream_t st);
+
+struct DequantParams {
+    const uint8_t* codes;
+    const void* scales;
+    int64_t rows, cols, codes_ld, scales_ld;
+    int grid, br, bc, po2;
+    int n, inverse;
+    float inv_sqrt_n;
+    uint32_t sign_bits[8];
+    float* out;
+    int64_t ld_out;
+};
+cudaError_t launch_dequantize(const DequantParams& p, int num_sms, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMM
+struct GemmOperand {
+    const uint8_t* codes;
+    const uint8_t* scales;  // UE8M0
+    int64_t rows, codes_ld, scales_ld;
+};
+struct GemmArgs {
+    GemmOperand a, b;
+    int64_t M, N, K;
+    int grid, br, bc;
+    float* D;
+    int64_t ldd;
+    void* workspace;
+    size_t workspace_bytes;
+};
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc);
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st);
+
+}  // namespace ufp4

@@ -1,0 +1,256 @@
+// Device helpers of the UFP4 quantizer: Philox4x32-10, bf16 widening, the
+// per-chunk FWHT, block scales, rounding and 4-bit packing.
+//
+// Every floating-point step is written with explicit round-to-nearest
+// intrinsics (__fadd_rn/__fsub_rn/__fmul_rn/__fdiv_rn/__frcp_rn) so that no
+// multiply is fused with an add and results are reproducible bit for bit.
+//
+// Pages: UFP4 summary (hyper.ai, arXiv 2606.20381), sections 数据集 (codebooks,
+// blocks, s_B = amax / largest level, RTNE, SR) and 方法 (Sylvester H_2n,
+// H'_n = S_n H_n); "Stable FP4 Training via Transposition-Invariant Block
+// Quantization", truncation-free scale and 2D square blocks.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace ufp4 {
+
+constexpr int kChunk = 16;  // elements one thread carries along the quantized dimension
+
+// Largest level and its reciprocal step for each grid (E1M2 1.75, INT4 7, E2M1 6).
+__host__ __device__ constexpr float grid_qmax(int grid) {
+    return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : 6.0f);
+}
+
+// ------------------------------------------------------------- Philox4x32-10
+// Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
+// bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+    for (int i = 0; i < 10; ++i) {
+        if (i) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    }
+    return c;
+}
+
+// Sixteen 16-bit SR draws for output elements lin0 .. lin0+15 (lin0 % 8 == 0):
+// counter (g lo, g hi, stream, group) with g = lin / 8; element j of a group
+// of eight takes the low half of word j/2 when j is even, the high half when odd.
+__device__ __forceinline__ void sr_draws16(uint64_t seed, uint64_t lin0, uint32_t stream,
+                                           uint32_t group, uint32_t w[8]) {
+    const uint64_t g = lin0 >> 3;
+    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    const uint4 a = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, group), k0, k1);
+    const uint64_t g1 = g + 1;
+    const uint4 b = philox4x32_10(make_uint4((uint32_t)g1, (uint32_t)(g1 >> 32), stream, group), k0, k1);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+}
+
+// ------------------------------------------------------------------ loading
+// 16 bf16 (8 words) -> 16 fp32, with the RHT signs applied as sign-bit flips
+// (bit j of sgn set <=> eps_j = -1; exact, same as multiplying by -1).
+__device__ __forceinline__ void widen16(const uint32_t w[8], uint32_t sgn, float v[16]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t lo = (w[k] << 16) ^ (((sgn >> (2 * k)) & 1u) << 31);
+        const uint32_t hi = (w[k] & 0xFFFF0000u) ^ (((sgn >> (2 * k + 1)) & 1u) << 31);
+        v[2 * k] = __uint_as_float(lo);
+        v[2 * k + 1] = __uint_as_float(hi);
+    }
+}
+
+// ----------------------------------------------------------------- the FWHT
+// Sylvester order: strides 1, 2, 4, ... (the recursion H_2n = [[H_n, H_n],
+// [H_n, -H_n]]/sqrt 2 combines halves last), pair (i, i+h) -> (a+b, a-b).
+// Strides below 16 run inside the thread; strides 16..n/2 pair the thread
+// with lane ^ (h/16), which holds the elements h positions away.
+// `seg_lane` is this thread's chunk index inside its length-n segment.
+__device__ __forceinline__ void fwht16(float v[16], int n, int seg_lane) {
+#pragma unroll
+    for (int h = 1; h < kChunk; h <<= 1) {
+        if (h < n) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                if (i & h) continue;
+                const float a = v[i], b = v[i + h];
+                v[i] = __fadd_rn(a, b);
+                v[i + h] = __fsub_rn(a, b);
+            }
+        }
+    }
+    for (int h = kChunk; h < n; h <<= 1) {
+        const int lm = h / kChunk;
+        const bool upper = (seg_lane & lm) != 0;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const float o = __shfl_xor_sync(0xFFFFFFFFu, v[i], lm);
+            v[i] = upper ? __fsub_rn(o, v[i]) : __fadd_rn(v[i], o);
+        }
+    }
+}
+
+__device__ __forceinline__ float amax_range(const float v[16], int lo, int hi) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < kChunk; ++i)
+        if (i >= lo && i < hi) m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+// ------------------------------------------------------------------- scales
+// fp32 scale s = fp32(M / qmax); reciprocal r = fp32(1/s), 0 for s = 0.
+__device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float& r) {
+    s = __fdiv_rn(M, qmax);
+    r = (s == 0.0f) ? 0.0f : __frcp_rn(s);
+}
+
+// Power-of-two scale: smallest e with M <= qmax * 2^e, clamped to [-127, 127].
+// With M = m * 2^E (m in [1,2)) and qmax = mq * 2^Eq: e = E - Eq + (m > mq).
+// Returns e; r = 2^-e exactly.
+template <int GRID>
+__device__ __forceinline__ int scale_po2(float M, float& r) {
+    const uint32_t b = __float_as_uint(M);
+    constexpr int Eq = (GRID == 0) ? 0 : 2;
+    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : 0x600000u;  // 1.5 or 1.75
+    int e;
+    if (b < 0x00800000u) {
+        e = -127;  // zero (subnormal amax is outside the contract)
+    } else {
+        const int E = (int)(b >> 23) - 127;
+        e = E - Eq + (((b & 0x7FFFFFu) > mq) ? 1 : 0);
+        e = max(-127, min(127, e));
+    }
+    r = (e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : __uint_as_float(0x00400000u);
+    return e;
+}
+
+// ----------------------------------------------------------------- rounding
+__device__ __forceinline__ uint32_t cvt_e2m3x2(float hi, float lo) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
+    uint32_t r;
+    asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
+        : "=r"(r)
+        : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Four e2m3 bytes (s 0 0 k k k, k = |level index|) -> four sign-magnitude
+// nibbles in the low 16 bits (byte i -> nibble i).
+__device__ __forceinline__ uint32_t e2m3_bytes_to_nibbles(uint32_t w) {
+    uint32_t t = (w & 0x07070707u) | ((w >> 2) & 0x08080808u);
+    t = (t | (t >> 4)) & 0x00FF00FFu;
+    return (t | (t >> 8)) & 0xFFFFu;
+}
+
+// A zero level is written as +0: clear the sign of every nibble whose
+// magnitude bits are zero.
+__device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
+    const uint32_t mag = w & 0x77777777u;
+    const uint32_t nz = (mag + 0x77777777u) & 0x88888888u;
+    return mag | (w & nz);
+}
+
+// Sign-magnitude nibbles -> two's complement (INT4): for a negative nibble
+// s|k with k > 0 the result is 8 | ((8 - k) & 7); -0 becomes 0.
+__device__ __forceinline__ uint32_t signmag_to_twos(uint32_t w) {
+    const uint32_t neg = (w >> 3) & 0x11111111u;
+    const uint32_t mag = w & 0x77777777u;
+    const uint32_t negm = ((mag ^ (neg * 7u)) + neg) & 0x77777777u;
+    const uint32_t nz = (negm + 0x77777777u) & 0x88888888u;
+    return negm | ((neg << 3) & nz);
+}
+
+// RTNE of 16 scaled values t = z * r (r0 for elements 0..7, r1 for 8..15)
+// to packed codes (two 32-bit words, element 0 in the lowest nibble).
+// E1M2 / INT4: the level index k of |t| is the e2m3 conversion of t/2 or t/8
+// (values k/8 are exactly e2m3's subnormals, ties to even k); E2M1: the e2m1
+// conversion of t.  satfinite saturates |t| above the largest level.
+template <int GRID>
+__device__ __forceinline__ uint2 round_rtne16(const float z[16], float r0, float r1) {
+    uint32_t out[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const float r = h ? r1 : r0;
+        float t[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = __fmul_rn(z[8 * h + i], r);
+        uint32_t w;
+        if (GRID == 2) {
+            w = 0;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) w |= cvt_e2m1x2(t[2 * p + 1], t[2 * p]) << (8 * p);
+        } else {
+            const float q = (GRID == 0) ? 0.5f : 0.125f;
+            uint32_t b[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) b[p] = cvt_e2m3x2(__fmul_rn(t[2 * p + 1], q), __fmul_rn(t[2 * p], q));
+            const uint32_t lo = e2m3_bytes_to_nibbles(b[0] | (b[1] << 16));
+            const uint32_t hi = e2m3_bytes_to_nibbles(b[2] | (b[3] << 16));
+            w = lo | (hi << 16);
+        }
+        w = clear_negative_zero(w);
+        if (GRID == 1) w = signmag_to_twos(w);
+        out[h] = w;
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+// Stochastic rounding of one scaled value: with a = min(|t|, qmax) between
+// levels lo and hi, p = (a - lo)/(hi - lo), round up iff u < p * 65536.
+// Returns the sign-magnitude nibble (a zero level as +0).
+template <int GRID>
+__device__ __forceinline__ uint32_t round_sr1(float t, uint32_t u) {
+    constexpr float qmax = grid_qmax(GRID);
+    const float a = fminf(fabsf(t), qmax);
+    uint32_t idx;
+    if (GRID == 2) {
+        // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
+        const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+        const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+        const float v = __fmul_rn(a, inv);
+        const float fl = floorf(v);
+        const float frac = __fsub_rn(v, fl);
+        const float up = ((float)u < __fmul_rn(frac, 65536.0f)) ? 1.0f : 0.0f;
+        const float val = __fmul_rn(__fadd_rn(fl, up), gap);
+        idx = cvt_e2m1x2(0.0f, val) & 7u;
+    } else {
+        const float inv_step = (GRID == 0) ? 4.0f : 1.0f;
+        const float v = __fmul_rn(a, inv_step);
+        const float fl = floorf(v);
+        const float frac = __fsub_rn(v, fl);
+        idx = (uint32_t)fl + (((float)u < __fmul_rn(frac, 65536.0f)) ? 1u : 0u);
+    }
+    const uint32_t neg = (__float_as_uint(t) >> 31) & 1u;
+    return idx == 0 ? 0u : ((neg << 3) | idx);
+}
+
+template <int GRID>
+__device__ __forceinline__ uint2 round_sr16(const float z[16], float r0, float r1, const uint32_t w[8]) {
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float t = __fmul_rn(z[i], i < 8 ? r0 : r1);
+        const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        out[i >> 3] |= round_sr1<GRID>(t, u) << (4 * (i & 7));
+    }
+    if (GRID == 1) {
+        out[0] = signmag_to_twos(out[0]);
+        out[1] = signmag_to_twos(out[1]);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+}  // namespace ufp4

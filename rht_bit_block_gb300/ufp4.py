@@ -1,0 +1,196 @@
+"""Thin ctypes binding of libufp4.so (the C ABI in include/ufp4.h).
+
+Argument marshalling only: every step of the quantizer and the GEMM runs in
+the library's CUDA kernels.  Functions keep the C names; torch tensors supply
+device memory (``data_ptr``) and the current CUDA stream.  The library is
+required: importing this module on a machine without it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libufp4.so")
+
+UFP4_OK = 0
+STATUS_NAMES = {0: "UFP4_OK", 1: "UFP4_ERR_INVALID_ARG", 2: "UFP4_ERR_UNSUPPORTED",
+                3: "UFP4_ERR_ALIGNMENT", 4: "UFP4_ERR_CUDA", 5: "UFP4_ERR_TIMEOUT"}
+GRID_E1M2, GRID_INT4, GRID_E2M1 = 0, 1, 2
+GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1}
+ROUND_RTNE, ROUND_SR = 0, 1
+SCALE_FP32, SCALE_UE8M0 = 0, 1
+OUT_ROWWISE, OUT_COLWISE = 1, 2
+
+# Every symbol include/ufp4.h declares (checked by the tests).
+EXPORTED = (
+    "ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_grouped_padded_rows",
+    "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
+    "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string",
+)
+
+
+class QuantDesc(ctypes.Structure):
+    _fields_ = [("grid", ctypes.c_int32), ("block_rows", ctypes.c_int32), ("block_cols", ctypes.c_int32),
+                ("hadamard_n", ctypes.c_int32), ("sign_seed", ctypes.c_uint64), ("round", ctypes.c_int32),
+                ("scale_fmt", ctypes.c_int32), ("sr_seed", ctypes.c_uint64), ("out_mask", ctypes.c_int32),
+                ("group", ctypes.c_int32)]
+
+
+class QTensor(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("cols", ctypes.c_int64), ("codes_ld", ctypes.c_int64), ("scales_ld", ctypes.c_int64)]
+
+
+class Ufp4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+_lib = None
+
+
+def load(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libufp4.so (build it with rht_bit_block_gb300.build.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: run `python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(path)
+    P, i64, i32, u64 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
+    QD, QT = ctypes.POINTER(QuantDesc), ctypes.POINTER(QTensor)
+    L.ufp4_rht_quantize.argtypes = [P, i64, i64, i64, QD, QT, QT, P]
+    L.ufp4_rht_quantize_grouped.argtypes = [P, i64, i64, ctypes.POINTER(i64), i32, QD, QT, QT, P]
+    L.ufp4_grouped_padded_rows.argtypes = [i64, QD]
+    L.ufp4_grouped_padded_rows.restype = i64
+    L.ufp4_rht_transform.argtypes = [P, i64, i64, i64, i32, u64, P, i64, P]
+    L.ufp4_dequantize.argtypes = [QT, QD, i32, P, i64, P]
+    L.ufp4_gemm_workspace_size.argtypes = [i64, i64, i64, QD, ctypes.POINTER(ctypes.c_size_t)]
+    L.ufp4_gemm.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
+    L.ufp4_sign_vector.argtypes = [u64, i32, P]
+    L.ufp4_device_error.argtypes = [ctypes.POINTER(i32)]
+    L.ufp4_status_string.argtypes = [ctypes.c_int]
+    L.ufp4_status_string.restype = ctypes.c_char_p
+    for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
+                 "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(status: int, what: str):
+    if status != UFP4_OK:
+        raise Ufp4Error(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=0, rounding=ROUND_RTNE, sr_seed=0,
+              scale_fmt=SCALE_FP32, out_mask=OUT_ROWWISE, group=0) -> QuantDesc:
+    g = GRIDS[grid] if isinstance(grid, str) else int(grid)
+    return QuantDesc(g, block[0], block[1], n, sign_seed, rounding, scale_fmt, sr_seed, out_mask, group)
+
+
+def qtensor(codes, scales, rows: int, cols: int) -> QTensor:
+    """Describe a quantized matrix held in torch tensors codes [rows, cols/2]
+    (uint8) and scales [rows/br, cols/bc] (float32 or uint8)."""
+    return QTensor(codes.data_ptr(), scales.data_ptr(), rows, cols, codes.stride(0) * codes.element_size(),
+                   scales.stride(0))
+
+
+# ------------------------------------------------------------- C entry points
+def ufp4_rht_quantize(x, desc: QuantDesc, rowwise: QTensor | None, colwise: QTensor | None, stream=None):
+    rows, cols = x.shape
+    _check(load().ufp4_rht_quantize(x.data_ptr(), rows, cols, x.stride(0), ctypes.byref(desc),
+                                    ctypes.byref(rowwise) if rowwise is not None else None,
+                                    ctypes.byref(colwise) if colwise is not None else None,
+                                    _stream(stream)), "ufp4_rht_quantize")
+
+
+def ufp4_rht_quantize_grouped(x, offsets, desc: QuantDesc, rowwise: QTensor | None, colwise: QTensor | None,
+                              stream=None):
+    cols = x.shape[1]
+    arr = (ctypes.c_int64 * len(offsets))(*[int(o) for o in offsets])
+    _check(load().ufp4_rht_quantize_grouped(x.data_ptr(), cols, x.stride(0), arr, len(offsets) - 1,
+                                            ctypes.byref(desc),
+                                            ctypes.byref(rowwise) if rowwise is not None else None,
+                                            ctypes.byref(colwise) if colwise is not None else None,
+                                            _stream(stream)), "ufp4_rht_quantize_grouped")
+
+
+def ufp4_grouped_padded_rows(rows: int, desc: QuantDesc) -> int:
+    return int(load().ufp4_grouped_padded_rows(rows, ctypes.byref(desc)))
+
+
+def ufp4_rht_transform(x, n: int, sign_seed: int, z, stream=None):
+    rows, cols = x.shape
+    _check(load().ufp4_rht_transform(x.data_ptr(), rows, cols, x.stride(0), n, sign_seed, z.data_ptr(),
+                                     z.stride(0), _stream(stream)), "ufp4_rht_transform")
+
+
+def ufp4_dequantize(q: QTensor, desc: QuantDesc, inverse_rht: bool, out, stream=None):
+    _check(load().ufp4_dequantize(ctypes.byref(q), ctypes.byref(desc), int(inverse_rht), out.data_ptr(),
+                                  out.stride(0), _stream(stream)), "ufp4_dequantize")
+
+
+def ufp4_gemm_workspace_size(M: int, N: int, K: int, desc: QuantDesc) -> int:
+    out = ctypes.c_size_t(0)
+    _check(load().ufp4_gemm_workspace_size(M, N, K, ctypes.byref(desc), ctypes.byref(out)),
+           "ufp4_gemm_workspace_size")
+    return int(out.value)
+
+
+def ufp4_gemm(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace=None, stream=None):
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().ufp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(), D.stride(0),
+                            ws_ptr, ws_bytes, _stream(stream)), "ufp4_gemm")
+
+
+def ufp4_sign_vector(sign_seed: int, n: int):
+    buf = (ctypes.c_int8 * n)()
+    _check(load().ufp4_sign_vector(sign_seed, n, buf), "ufp4_sign_vector")
+    return list(buf)
+
+
+def ufp4_device_error() -> int:
+    code = ctypes.c_int32(0)
+    _check(load().ufp4_device_error(ctypes.byref(code)), "ufp4_device_error")
+    return int(code.value)
+
+
+def ufp4_status_string(status: int) -> str:
+    return load().ufp4_status_string(status).decode()
+
+
+# ------------------------------------------------------------- conveniences
+def alloc_quantized(rows: int, cols: int, desc: QuantDesc, device):
+    """torch buffers for one quantized matrix (rows x cols in its own layout)."""
+    import torch
+    br, bc = desc.block_rows, desc.block_cols
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    sdt = torch.float32 if desc.scale_fmt == SCALE_FP32 else torch.uint8
+    scales = torch.empty((rows // br, cols // bc), dtype=sdt, device=device)
+    return codes, scales
+
+
+def quantize(x, desc: QuantDesc, stream=None):
+    """Quantize a bf16 CUDA tensor; returns {"row": (codes, scales)?, "col": (codes, scales)?}."""
+    rows, cols = x.shape
+    out = {}
+    rq = cq = None
+    if desc.out_mask & OUT_ROWWISE:
+        out["row"] = alloc_quantized(rows, cols, desc, x.device)
+        rq = qtensor(*out["row"], rows, cols)
+    if desc.out_mask & OUT_COLWISE:
+        out["col"] = alloc_quantized(cols, rows, desc, x.device)
+        cq = qtensor(*out["col"], cols, rows)
+    ufp4_rht_quantize(x, desc, rq, cq, stream)
+    return out

@@ -1,0 +1,80 @@
+"""The C ABI library builds, loads and exports every symbol include/ufp4.h
+declares, and rejects bad arguments on the host (no GPU needed: nothing
+here launches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from rht_bit_block_gb300 import build, ufp4
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return ufp4.load()
+
+
+def declared_symbols():
+    with open(os.path.join(ROOT, "include", "ufp4.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z0-9_]+\*?\s+\**(ufp4_[a-z0-9_]+)\s*\(", text, re.M)))
+
+
+def test_header_declares_the_binding_names():
+    assert sorted(ufp4.EXPORTED) == declared_symbols()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in ufp4.STATUS_NAMES.items():
+        assert ufp4.ufp4_status_string(code) == name
+
+
+def test_sign_vector_matches_oracle(lib):
+    import oracle as orc
+    for n in (1, 2, 16, 256):
+        got = ufp4.ufp4_sign_vector(0x5EED0001, n)
+        exp = [1] if n == 1 else orc.signs(0x5EED0001, n).tolist()
+        assert got == exp
+
+
+def _call_quantize(lib, desc, rows=64, cols=64, ld=64, x=0x1000, codes=0x2000, scales=0x3000):
+    q = ufp4.QTensor(codes, scales, rows, cols, cols // 2, cols // 16)
+    return lib.ufp4_rht_quantize(ctypes.c_void_p(x), rows, cols, ld, ctypes.byref(desc), ctypes.byref(q), None,
+                                 None)
+
+
+def test_host_validation_rejects_bad_arguments(lib):
+    """Every rejection happens before a launch (fake device addresses are never touched)."""
+    ok = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)
+    bad_n = ufp4.make_desc(n=12)
+    bad_block = ufp4.make_desc(block=(2, 16))
+    fp32_2d = ufp4.make_desc(block=(32, 32), scale_fmt=ufp4.SCALE_FP32)
+    bad_grid = ufp4.make_desc(grid=7)
+    assert _call_quantize(lib, bad_n) == 1
+    assert _call_quantize(lib, bad_block) == 1
+    assert _call_quantize(lib, fp32_2d) == 1
+    assert _call_quantize(lib, bad_grid) == 1
+    assert _call_quantize(lib, ok, x=0x1001) == 3           # misaligned input
+    assert _call_quantize(lib, ok, cols=72, ld=72) == 1      # cols not a multiple of n/16
+    assert _call_quantize(lib, ok, ld=32) == 1               # ld < cols
+    assert lib.ufp4_rht_quantize(None, 16, 16, 16, ctypes.byref(ok), None, None, None) == 1
+    col256 = ufp4.make_desc(n=256, out_mask=ufp4.OUT_COLWISE)
+    q = ufp4.QTensor(0x2000, 0x3000, 256, 256, 128, 16)
+    assert lib.ufp4_rht_quantize(ctypes.c_void_p(0x1000), 256, 256, 256, ctypes.byref(col256), None,
+                                 ctypes.byref(q), None) == 2
+
+
+def test_gemm_rejects_fp32_scales(lib):
+    desc = ufp4.make_desc(scale_fmt=ufp4.SCALE_FP32)
+    A = ufp4.QTensor(0x2000, 0x3000, 128, 128, 64, 8)
+    D = ctypes.c_void_p(0x4000)
+    assert lib.ufp4_gemm(ctypes.byref(A), ctypes.byref(A), ctypes.byref(desc), D, 128, None, 0, None) == 2

@@ -1,0 +1,166 @@
+"""Parity of the quantized GEMM D = Q(A) Q(B)^T with the oracle's fp64 product
+of the dequantized operands (UFP4 summary, section 方法, Eq. of the quantized
+GEMM), called through the C ABI.  Bar: exact where every partial sum is an
+integer below 2^24, else relative Frobenius error <= 1e-5."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as orc
+from rht_bit_block_gb300 import inputs, ufp4
+from tests.gpu_util import gpu_quantize, to_dev
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-5
+BLOCKS = [(1, 16), (1, 32), (32, 32)]
+
+
+def _pack(nib):
+    return (nib[:, 0::2] | (nib[:, 1::2] << 4)).astype(np.uint8)
+
+
+def _rand_operand(rng, rows, K, grid, block, lo=127, hi=127):
+    nib = rng.integers(0, 16, size=(rows, K)).astype(np.uint8)
+    if grid == "int4":
+        nib[nib == 8] = 0  # -8 is not a level
+    sc = rng.integers(lo, hi + 1, size=(rows // block[0] if block[0] > 1 else rows, K // block[1])).astype(np.uint8)
+    if block[0] > 1:
+        sc = sc[: (rows + block[0] - 1) // block[0]]
+    return _pack(nib), sc
+
+
+def _gemm(ac, asc, bc, bsc, M, N, K, grid, block):
+    desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
+    dev = "cuda"
+    A = [torch.from_numpy(ac).to(dev), torch.from_numpy(asc).to(dev)]
+    B = [torch.from_numpy(bc).to(dev), torch.from_numpy(bsc).to(dev)]
+    D = torch.full((M, N), float("nan"), dtype=torch.float32, device=dev)
+    ws = torch.empty(max(1, ufp4.ufp4_gemm_workspace_size(M, N, K, desc)), dtype=torch.uint8, device=dev)
+    ufp4.ufp4_gemm(ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K), desc, D, ws)
+    torch.cuda.synchronize()
+    assert ufp4.ufp4_device_error() == 0
+    return D.cpu().numpy().astype(np.float64)
+
+
+def _rel(D, ref):
+    return np.linalg.norm(D - ref) / max(np.linalg.norm(ref), 1e-300)
+
+
+FP8_GRIDS = ("e1m2", "int4")
+
+
+@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
+@pytest.mark.parametrize("block", BLOCKS)
+@pytest.mark.parametrize("shape", [(128, 256, 128), (256, 512, 512), (200, 300, 384)])
+def test_gemm_exact_integer_case(grid, block, shape):
+    """Unit scales: every product and partial sum is an exact small dyadic,
+    so the tensor-core result equals the fp64 reference bit for bit."""
+    M, N, K = shape
+    if grid == "e2m1" and K % 64:
+        pytest.skip("FP4 operands need K % 64 == 0")
+    if block[0] > 1 and (M % 32 or N % 32):
+        M, N = (M + 31) // 32 * 32, (N + 31) // 32 * 32
+    rng = np.random.default_rng(M + N + K)
+    ac, asc = _rand_operand(rng, M, K, grid, block)
+    bc, bsc = _rand_operand(rng, N, K, grid, block)
+    D = _gemm(ac, asc, bc, bsc, M, N, K, grid, block)
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=block)
+    np.testing.assert_array_equal(D, ref)
+
+
+@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
+@pytest.mark.parametrize("block", BLOCKS)
+def test_gemm_random_scales(grid, block):
+    """Block scales spread over 2^-9 .. 2^7 (pairs of 1 x 16 blocks differ by up
+    to 16 binades, the exact range of the E5M2 fold)."""
+    M, N, K = 384, 512, 1024
+    rng = np.random.default_rng(31)
+    ac, asc = _rand_operand(rng, M, K, grid, block, lo=118, hi=134)
+    bc, bsc = _rand_operand(rng, N, K, grid, block, lo=118, hi=134)
+    D = _gemm(ac, asc, bc, bsc, M, N, K, grid, block)
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=block)
+    assert _rel(D, ref) <= TOL
+
+
+@pytest.mark.parametrize("grid", FP8_GRIDS)
+def test_gemm_wide_scale_gap(grid):
+    """Neighbouring 1 x 16 blocks 20-30 binades apart: the smaller block's
+    elements fall below E5M2's range and round; the error stays far below the bar."""
+    M, N, K = 256, 256, 512
+    rng = np.random.default_rng(5)
+    ac, asc = _rand_operand(rng, M, K, grid, (1, 16), lo=127, hi=127)
+    bc, bsc = _rand_operand(rng, N, K, grid, (1, 16), lo=127, hi=127)
+    asc[:, 1::2] = 100
+    D = _gemm(ac, asc, bc, bsc, M, N, K, grid, (1, 16))
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=(1, 16))
+    assert _rel(D, ref) <= TOL
+
+
+def _quantized(x, grid, block, colwise=False, rounding=orc.RTNE):
+    kw = dict(grid=grid, block=block, n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=orc.SCALE_UE8M0,
+              rounding=rounding, sr_seed=inputs.SR_SEED)
+    got = gpu_quantize(to_dev(x), out_mask=ufp4.OUT_COLWISE if colwise else ufp4.OUT_ROWWISE, **kw)
+    return got["col" if colwise else "row"]
+
+
+@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
+def test_fprop_dense_small(grid):
+    x, w = inputs.dense_fprop(m=1024, n=768, k=2048)
+    ac, asc = _quantized(x, grid, (1, 16))
+    bc, bsc = _quantized(w, grid, (1, 16))
+    D = _gemm(ac, asc, bc, bsc, 1024, 768, 2048, grid, (1, 16))
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=(1, 16))
+    assert _rel(D, ref) <= TOL
+
+
+def test_fprop_dense_full_size():
+    """Dense-1.5B-like FPROP Y = X W^T (8192 x 5632 x 2048), E1M2 1 x 16 RTNE."""
+    x, w = inputs.dense_fprop()
+    ac, asc = _quantized(x, "e1m2", (1, 16))
+    bc, bsc = _quantized(w, "e1m2", (1, 16))
+    D = _gemm(ac, asc, bc, bsc, 8192, 5632, 2048, "e1m2", (1, 16))
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid="e1m2", block=(1, 16))
+    assert _rel(D, ref) <= TOL
+
+
+def test_dgrad_and_wgrad_from_one_pass():
+    """dY (1e-3 Student-t, SR) row-wise feeds DGRAD dX = dY W (B = W column-wise);
+    its column-wise copy feeds WGRAD dW = dY^T X (B = X column-wise)."""
+    m, n, k = 2048, 1024, 768
+    dy = inputs.student_t_bf16(m, n, 301)
+    w = inputs.normal_bf16(n, k, 302, std=0.02)
+    x = inputs.normal_bf16(m, k, 303)
+    desc_sr = dict(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=orc.SCALE_UE8M0,
+                   rounding=orc.SR, sr_seed=inputs.SR_SEED)
+    both = gpu_quantize(to_dev(dy), out_mask=3, **desc_sr)
+    wc, wsc = _quantized(w, "e1m2", (1, 16), colwise=True)     # [k x n]
+    xc, xsc = _quantized(x, "e1m2", (1, 16), colwise=True)     # [k x m]
+    # DGRAD: [m x n] . [k x n]^T
+    D = _gemm(*both["row"], wc, wsc, m, k, n, "e1m2", (1, 16))
+    ref = orc.gemm_reference(*both["row"], wc, wsc, grid="e1m2", block=(1, 16))
+    assert _rel(D, ref) <= TOL
+    # WGRAD: [n x m] . [k x m]^T
+    D = _gemm(*both["col"], xc, xsc, n, k, m, "e1m2", (1, 16))
+    ref = orc.gemm_reference(*both["col"], xc, xsc, grid="e1m2", block=(1, 16))
+    assert _rel(D, ref) <= TOL
+
+
+@pytest.mark.parametrize("grid,block", [("e1m2", (1, 16)), ("int4", (32, 32)), ("e2m1", (1, 16)),
+                                        ("e2m1", (32, 32))])
+def test_large_fprop_sampled_rows(grid, block):
+    """MoE-124B-like FPROP 16384 x 7168 x 7168 checked on 256 seeded rows of D."""
+    x, w = inputs.large_sweep()
+    ac, asc = _quantized(x, grid, block)
+    bc, bsc = _quantized(w, grid, block)
+    D = torch.empty((16384, 7168), dtype=torch.float32, device="cuda")
+    desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
+    A = [torch.from_numpy(ac).cuda(), torch.from_numpy(asc).cuda()]
+    B = [torch.from_numpy(bc).cuda(), torch.from_numpy(bsc).cuda()]
+    ws = torch.empty(max(1, ufp4.ufp4_gemm_workspace_size(16384, 7168, 7168, desc)), dtype=torch.uint8, device="cuda")
+    ufp4.ufp4_gemm(ufp4.qtensor(*A, 16384, 7168), ufp4.qtensor(*B, 7168, 7168), desc, D, ws)
+    torch.cuda.synchronize()
+    rows = np.sort(np.random.default_rng(7).choice(16384, 256, replace=False))
+    got = D[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=block, a_rows=rows)
+    assert _rel(got, ref) <= TOL
