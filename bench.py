@@ -1,0 +1,347 @@
+#!/usr/bin/env python3
+"""Benchmark of the UFP4 hot path on GB300.
+
+One step = one pass of the hot path over one batch of the Dense-1.5B-like
+FPROP workload: fused RHT + E1M2 4-bit quantization (n = 16, 1 x 16 blocks,
+UE8M0 scales, RTNE) of X (8192 x 2048 bf16) and W (5632 x 2048 bf16), then
+the quantized GEMM Y = Q(X H') Q(W H')^T (8192 x 5632 x 2048, fp32 out).
+
+value  = fused quantizer throughput in GB/s of algorithmic bytes (bf16 read
+         + packed codes + scales written), from CUDA events around the
+         quantizer launches inside the timed steps.
+gemm   = quantized GEMM TFLOP/s (2 M N K per step, operand prep included).
+e2e    = the same quantizer metric through the C ABI with host buffers:
+         pinned H2D of X and W, quantize, GEMM and D2H of the codes, scales
+         and Y inside the timed region.
+Inputs rotate over 5 copies (270 MiB > 2 x L2), so every step reads cold data.
+
+--impl reference runs the oracle (plain C, one host core) as the reference
+arm on bounded row samples of the same workload.
+Multi-GPU (torchrun): every rank runs its own replica of the step (weak
+scaling, no collective on the data path); timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "fused RHT+4-bit quantize GB/s (% of HBM peak); quantized GEMM TFLOP/s (% peak)"
+M, N, K = 8192, 5632, 2048
+BLOCK = 16
+# algorithmic bytes per element: 2 (bf16 in) + 0.5 (codes) + 1/16 (UE8M0 scale)
+BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / BLOCK
+QUANT_ELEMS = (M + N) * K
+QUANT_BYTES = QUANT_ELEMS * BYTES_PER_ELEM
+GEMM_FLOPS = 2.0 * M * N * K
+ROTATE = 5
+WORKLOAD = "dense-1.5B FPROP operands: X 8192x2048, W 5632x2048 bf16; E1M2 1x16 UE8M0 RTNE, n=16; GEMM 8192x5632x2048"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "src": "measured"}
+    except Exception:
+        return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "src": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def aggregate(seconds: float, units: float, world: int, backend_device=None):
+    """Whole-job throughput: units summed over ranks / max time over ranks."""
+    if world == 1:
+        return seconds, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=backend_device)
+    u = torch.tensor([units], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------ CPU baseline
+def cpu_oracle_rate(rows_x: int, rows_w: int, min_seconds: float, max_reps: int):
+    """Oracle (single-threaded C) on a bounded row sample of X and W; returns
+    (GB/s of algorithmic bytes, elements, seconds, reps)."""
+    import oracle as orc
+    from rht_bit_block_gb300 import inputs
+    x, w = inputs.dense_fprop()
+    xs, ws = np.ascontiguousarray(x[:rows_x]), np.ascontiguousarray(w[:rows_w])
+    kw = dict(grid="e1m2", block=(1, BLOCK), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=orc.SCALE_UE8M0)
+    orc.quantize(xs[:16], **kw)  # build + load outside the timing
+    elems = 0
+    t0 = time.perf_counter()
+    reps = 0
+    while reps < max_reps:
+        orc.quantize(xs, **kw)
+        orc.quantize(ws, **kw)
+        elems += (xs.shape[0] + ws.shape[0]) * K
+        reps += 1
+        if time.perf_counter() - t0 >= min_seconds:
+            break
+    dt = time.perf_counter() - t0
+    return elems * BYTES_PER_ELEM / dt / 1e9, elems, dt, reps
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    rows = 64
+    for _ in range(args.warmup):
+        cpu_oracle_rate(rows, rows, 0.0, 1)
+    t0 = time.perf_counter()
+    elems = 0
+    for _ in range(args.steps):
+        _, e, _, _ = cpu_oracle_rate(rows, rows, 0.0, 1)
+        elems += e
+    dt = time.perf_counter() - t0
+    value = elems * BYTES_PER_ELEM / dt / 1e9
+    sample = f"each step: the first {rows} rows of X and of W ({2 * rows * K} elements), oracle quantizer only"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic", "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    from rht_bit_block_gb300 import inputs, ufp4
+    ufp4.load()
+    stream = torch.cuda.current_stream()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    x_np, w_np = inputs.dense_fprop()
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+    xs = [to_t(x_np).to(dev) for _ in range(ROTATE)]
+    wsrc = [to_t(w_np).to(dev) for _ in range(ROTATE)]
+    desc = ufp4.make_desc(grid="e1m2", block=(1, BLOCK), n=16, sign_seed=inputs.SIGN_SEED,
+                          scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+    qx = ufp4.alloc_quantized(M, K, desc, dev)
+    qw = ufp4.alloc_quantized(N, K, desc, dev)
+    tx, tw = ufp4.qtensor(*qx, M, K), ufp4.qtensor(*qw, N, K)
+    D = torch.empty((M, N), dtype=torch.float32, device=dev)
+    wsb = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+    n_ev = args.steps
+    e_q0, e_q1, e_g1 = [ev() for _ in range(n_ev)], [ev() for _ in range(n_ev)], [ev() for _ in range(n_ev)]
+
+    def step(i, timed):
+        xi, wi = xs[i % ROTATE], wsrc[i % ROTATE]
+        if timed:
+            e_q0[i].record(stream)
+        ufp4.ufp4_rht_quantize(xi, desc, tx, None, stream.cuda_stream)
+        ufp4.ufp4_rht_quantize(wi, desc, tw, None, stream.cuda_stream)
+        if timed:
+            e_q1[i].record(stream)
+        ufp4.ufp4_gemm(tx, tw, desc, D, wsb, stream.cuda_stream)
+        if timed:
+            e_g1[i].record(stream)
+
+    for i in range(args.warmup):
+        step(i, False)
+    barrier()
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.2)
+    barrier()
+    t0 = time.perf_counter()
+    start_all = ev()
+    end_all = ev()
+    start_all.record(stream)
+    for i in range(args.steps):
+        step(i, True)
+    end_all.record(stream)
+    barrier()
+    wall = time.perf_counter() - t0
+    clocks = sampler.stop()
+    assert ufp4.ufp4_device_error() == 0, "a bounded device wait gave up"
+    q_ms = [e_q0[i].elapsed_time(e_q1[i]) for i in range(args.steps)]
+    g_ms = [e_q1[i].elapsed_time(e_g1[i]) for i in range(args.steps)]
+    total_ms = start_all.elapsed_time(end_all)
+    q_s = sum(q_ms) / 1e3
+    g_s = sum(g_ms) / 1e3
+    q_time, q_units = aggregate(q_s, QUANT_BYTES * args.steps, world, dev)
+    g_time, g_units = aggregate(g_s, GEMM_FLOPS * args.steps, world, dev)
+    step_time, _ = aggregate(total_ms / 1e3, 0.0, world, dev)
+    value = q_units / q_time / 1e9
+    gemm_tflops = g_units / g_time / 1e12
+
+    # ------------------------------------------------------- e2e (host buffers)
+    xh = to_t(x_np).pin_memory()
+    whh = to_t(w_np).pin_memory()
+    xd, wd = xs[0], wsrc[0]
+    codes_h = [torch.empty_like(qx[0], device="cpu").pin_memory(), torch.empty_like(qx[1], device="cpu").pin_memory(),
+               torch.empty_like(qw[0], device="cpu").pin_memory(), torch.empty_like(qw[1], device="cpu").pin_memory()]
+    Dh = torch.empty((M, N), dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        wd.copy_(whh, non_blocking=True)
+        ufp4.ufp4_rht_quantize(xd, desc, tx, None, stream.cuda_stream)
+        ufp4.ufp4_rht_quantize(wd, desc, tw, None, stream.cuda_stream)
+        ufp4.ufp4_gemm(tx, tw, desc, D, wsb, stream.cuda_stream)
+        for hbuf, dbuf in zip(codes_h, (qx[0], qx[1], qw[0], qw[1])):
+            hbuf.copy_(dbuf, non_blocking=True)
+        Dh.copy_(D, non_blocking=True)
+
+    e2e_step()
+    barrier()
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    barrier()
+    e2e_s, e2e_units = aggregate(a.elapsed_time(b) / 1e3, QUANT_BYTES * e2e_steps, world, dev)
+    h2d = (xh.numel() + whh.numel()) * 2
+    d2h = sum(t.numel() * t.element_size() for t in codes_h) + Dh.numel() * 4
+
+    pk = peaks()
+    q_launch_ms = statistics.mean(q_ms) / 2  # two quantizer launches per step (X and W, same kernel)
+    q_gbs = (QUANT_BYTES / 2) / (q_launch_ms / 1e3) / 1e9
+    fp8_peak = 2.0 * pk["bf16"]  # dense FP8 = 2 x bf16 (nominal ratio)
+    gemm_frac = gemm_tflops / fp8_peak
+    rl_q = {"bound": "hbm", "achieved": q_gbs, "peak": pk["hbm"], "unit": "GB/s", "frac": q_gbs / pk["hbm"],
+            "traffic": None, "kernel": "quantize_kernel<E1M2,RTNE,UE8M0>", "peak_src": pk["src"] + " hbm_gbs"}
+    rl_g = {"bound": "tensor", "achieved": gemm_tflops, "peak": fp8_peak, "unit": "TFLOP/s", "frac": gemm_frac,
+            "traffic": None, "kernel": "gemm_kernel<FP8> + operand prep",
+            "peak_src": pk["src"] + " bf16_tflops x2 (FP8/bf16 nominal ratio)"}
+    dominant = rl_g if statistics.mean(g_ms) >= statistics.mean(q_ms) else rl_q
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        rate, elems, dt, reps = cpu_oracle_rate(1024, 1024, args.cpu_seconds, 64)
+        cpu = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first 1024 rows of X and of W ({2048 * K} elements) per rep, {reps} reps, {dt:.1f} s"}
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": step_time / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 in, 4-bit codes out)", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "l2": "inputs rotate over 5 copies (270 MiB > 2x L2)",
+                       "parallelism": f"replicas x{world}"},
+            "quant_frac_of_hbm": value / pk["hbm"],
+            "gemm": {"value": gemm_tflops, "unit": "TFLOP/s", "frac": gemm_frac, "peak": fp8_peak},
+            "roofline": dominant, "roofline_quantize": rl_q, "roofline_gemm": rl_g,
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_units / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 5 * args.steps, "clocks": clocks, "wall_s_timed": wall,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

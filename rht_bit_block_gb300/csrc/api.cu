@@ -110,8 +110,10 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     BlockShape bs;
     ufp4_status st = check_desc(desc, &bs);
     if (st != UFP4_OK) return st;
-    if (!x || cols < 0 || ld < cols || ngroups < 1 || ngroups > kMaxGroups) return UFP4_ERR_INVALID_ARG;
+    if (cols < 0 || ld < cols || ngroups < 1 || ngroups > kMaxGroups) return UFP4_ERR_INVALID_ARG;
     if (desc->out_mask < 1 || desc->out_mask > 3) return UFP4_ERR_INVALID_ARG;
+    if (offsets[ngroups] == 0 || cols == 0) return UFP4_OK;  // empty input: nothing to do (pointers may be null)
+    if (!x) return UFP4_ERR_INVALID_ARG;
     const bool do_row = desc->out_mask & UFP4_OUT_ROWWISE;
     const bool do_col = desc->out_mask & UFP4_OUT_COLWISE;
     const int n = desc->hadamard_n;
