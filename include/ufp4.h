@@ -216,6 +216,31 @@ ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_q
                       float* D, int64_t ldd, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
+/* Size of the fixed device scratch behind ufp4_gemm_noalloc: 32 MiB. */
+#define UFP4_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* ufp4_gemm_noalloc -- ufp4_gemm for callers that must not allocate device
+ * memory (no counterpart in the pages: it is an interface convenience).
+ * Some callers cannot call cudaMalloc at all: code inside a CUDA-graph
+ * capture, plugins or custom ops whose host framework owns every device
+ * allocation, and latency-critical loops where an allocation may synchronize
+ * the device.  This entry point takes the same A, B, desc, D and ldd as
+ * ufp4_gemm but no workspace: it uses one scratch array of
+ * UFP4_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library keeps until the process exits.
+ *   - It allocates nothing and calls no allocating routine.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Returns UFP4_ERR_UNSUPPORTED when ufp4_gemm_workspace_size for these
+ *     shapes exceeds UFP4_NOALLOC_SCRATCH_BYTES (E1M2/INT4 need about
+ *     (M + N) * K bytes; E2M1 needs only its scale chunks).
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it has to start at zero).  Calls whose GPU work overlaps,
+ *     for example on two streams at once, race on the array: serialize them. */
+ufp4_status ufp4_gemm_noalloc(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
+                              float* D, int64_t ldd, cudaStream_t stream);
+
 /* ufp4_sign_vector -- the n signs eps_i of the RHT (HOST output, int8 +-1),
  * for consumers that apply the rotation themselves. */
 ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host);

@@ -26,7 +26,7 @@ OUT_ROWWISE, OUT_COLWISE = 1, 2
 EXPORTED = (
     "ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_grouped_padded_rows",
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
-    "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string",
+    "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
 )
 
 
@@ -69,12 +69,14 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_dequantize.argtypes = [QT, QD, i32, P, i64, P]
     L.ufp4_gemm_workspace_size.argtypes = [i64, i64, i64, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
+    L.ufp4_gemm_noalloc.argtypes = [QT, QT, QD, P, i64, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
     L.ufp4_device_error.argtypes = [ctypes.POINTER(i32)]
     L.ufp4_status_string.argtypes = [ctypes.c_int]
     L.ufp4_status_string.restype = ctypes.c_char_p
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
-                 "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error"):
+                 "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error",
+                 "ufp4_gemm_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -152,6 +154,13 @@ def ufp4_gemm(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace=None, stream
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().ufp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(), D.stride(0),
                             ws_ptr, ws_bytes, _stream(stream)), "ufp4_gemm")
+
+
+def ufp4_gemm_noalloc(A: QTensor, B: QTensor, desc: QuantDesc, D, stream=None):
+    """ufp4_gemm without a workspace: the library's fixed device scratch is used
+    (for callers that cannot allocate device memory; calls must not overlap)."""
+    _check(load().ufp4_gemm_noalloc(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(),
+                                    D.stride(0), _stream(stream)), "ufp4_gemm_noalloc")
 
 
 def ufp4_sign_vector(sign_seed: int, n: int):
