@@ -153,7 +153,10 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     QuantParams p;
     std::memset(&p, 0, sizeof(p));
     const int tc = (n == 256) ? 256 : 128;
-    const int tr = (tc == 256) ? 64 : 128;
+    const int seg_lanes = (bs.is2d ? std::max(n, 16) : std::max(std::max(n, bs.bw), 16)) / 16;
+    // row-only work takes 128-row tiles (more elements per thread per tile);
+    // the column pass takes 64-row tiles unless a segment spans 8 row chunks
+    const int tr = (do_col && seg_lanes < 8) ? 64 : (n == 256 ? 64 : 128);
     p.x = (const uint16_t*)x;
     p.cols = cols;
     p.ld = ld;
@@ -164,7 +167,18 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     p.b2d = bs.b2d;
     p.bw_row = bs.bw;
     p.bw_col = bs.bw;
-    p.col_seg_lanes = (bs.is2d ? std::max(n, 16) : std::max(std::max(n, bs.bw), 16)) / 16;
+    p.col_seg_lanes = seg_lanes;
+    p.amax_slots = bs.is2d ? (tr / bs.b2d) * (tc / bs.b2d) : 0;
+    p.tile_rows = tr;
+    p.stages = std::max(2, std::min(6, (96 * 1024) / (tr * tc * 2)));  // about 96 KB of tiles in flight per CTA
+    auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
+    p.lbw_row = ilog2(bs.bw);
+    p.lbw_col = ilog2(bs.bw);
+    p.lb2d = bs.is2d ? ilog2(bs.b2d) : 0;
+    p.lseg = ilog2(seg_lanes);
+    p.log4n = 0;
+    while ((1 << (2 * p.log4n)) < n) ++p.log4n;
+    p.pow4 = (1 << (2 * p.log4n)) == n;
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
     p.do_row = do_row;
     p.do_col = do_col;
@@ -190,7 +204,8 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if (num_tiles > 0x7FFFFFFF) return UFP4_ERR_UNSUPPORTED;
     p.group_base = grouped ? 0 : desc->group;
     return cuda_status(launch_quantize(p, desc->grid, desc->round == UFP4_ROUND_SR,
-                                       desc->scale_fmt == UFP4_SCALE_UE8M0, tc, (int)num_tiles, stream));
+                                       desc->scale_fmt == UFP4_SCALE_UE8M0, tc, tr, (int)num_tiles, total_rows,
+                                       num_sms_current(), stream));
 }
 
 }  // namespace

@@ -37,7 +37,8 @@ constexpr int kBM = 128;
 constexpr int kBKBytes = 128;          // bytes of K per stage per row (one 128B swizzle row)
 constexpr int kGemmThreads = 256;
 constexpr int kChunkBytes = 512;       // 128 rows x 4 scale bytes, tcgen05.cp 32x128b layout
-constexpr uint32_t kWaitLimit = 1u << 24;
+constexpr uint32_t kWaitLimit = 1u << 22;  // bounded polling; each poll may sleep up to kSuspendNs
+constexpr uint32_t kSuspendNs = 1000;
 constexpr int kErrTimeout = 1;
 
 // ------------------------------------------------------------ PTX wrappers
@@ -59,9 +60,9 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < kWaitLimit; ++i) {
         uint32_t ok;
         asm volatile(
-            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+            "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3; selp.u32 %0, 1, 0, p; }"
             : "=r"(ok)
-            : "r"(bar), "r"(parity)
+            : "r"(bar), "r"(parity), "r"(kSuspendNs)
             : "memory");
         if (ok) return true;
     }
@@ -458,15 +459,8 @@ EncodeTiledFn encode_fn() {
 
 // 2-D byte tensor (rows x row_bytes, pitch bytes) read in boxes of 128 bytes x box_rows, 128B swizzle.
 bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes, int64_t pitch, int box_rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)pitch};
-    const cuuint32_t box[2] = {(cuuint32_t)kBKBytes, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return encode_map_2d(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, ptr, (uint64_t)row_bytes, (uint64_t)rows,
+                         (uint64_t)pitch, (uint32_t)kBKBytes, (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 struct Plan {
@@ -516,6 +510,18 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKPa
 }
 
 }  // namespace
+
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
+    const cuuint64_t strides[1] = {(cuuint64_t)pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dtype, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
     return make_plan(M, N, K, grid, br, bc).total;
@@ -593,6 +599,8 @@ extern "C" ufp4_status ufp4_device_error(int32_t* code) {
     if (cudaMemcpyFromSymbol(&v, ufp4::g_device_error, sizeof(int)) != cudaSuccess) return UFP4_ERR_CUDA;
     const int zero = 0;
     if (v && cudaMemcpyToSymbol(ufp4::g_device_error, &zero, sizeof(int)) != cudaSuccess) return UFP4_ERR_CUDA;
-    *code = v;
+    int q = 0;
+    if (ufp4::quant_error_read_clear(&q) != cudaSuccess) return UFP4_ERR_CUDA;
+    *code = v ? v : q;
     return UFP4_OK;
 }

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace ufp4 {
@@ -30,6 +31,11 @@ struct QuantParams {
     int is2d, b2d;      // 2-D square blocks of side b2d
     int bw_row, bw_col; // 1-D block widths (or b2d)
     int col_seg_lanes;  // lanes sharing one column segment in the column pass
+    int amax_slots;     // 2-D block amax slots per tile (0 for 1-D blocks)
+    int tile_rows;      // rows per tile: 64, or 128 when the column pass needs 8 lanes per segment
+    int stages;         // TMA ring depth
+    int lbw_row, lbw_col, lb2d, lseg;  // log2 of block widths, 2-D side and col_seg_lanes
+    int pow4, log4n;    // n = 4^log4n: 1/sqrt(n) is a power of two
     uint64_t sr_seed;
     int do_row, do_col, vec256, col_grouped;
     QOut row, col;
@@ -41,8 +47,14 @@ struct QuantParams {
     int grp_tile0[kMaxGroups + 1];     // first row tile of each group
 };
 
-cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int num_tiles,
-                            cudaStream_t st);
+cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
+                            int64_t total_rows, int num_sms, cudaStream_t st);
+cudaError_t quant_error_read_clear(int* value);
+
+// 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,
+// pitch bytes between rows, boxes of box_inner x box_outer elements.
+bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr, uint64_t inner, uint64_t outer,
+                   uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swizzle);
 cudaError_t launch_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n,
                        float inv_sqrt_n, const SignBits& sb, float* z, int64_t ldz, int num_sms,
                        cudaStream_t st);

@@ -1,22 +1,22 @@
 // Fused RHT + block-scaled 4-bit quantizer for sm_103a.
 //
-// One CTA owns a TR x TC tile of the bf16 input and produces, from a single
-// read of it, the row-wise quantization (RHT and blocks along the columns)
-// and the column-wise quantization of the transpose (RHT and blocks along the
-// rows), as required for FPROP, DGRAD and WGRAD (UFP4 summary, section 方法:
-// RHT on all three training GEMMs; 2D-block tutorial: dX = dY W and
-// dW = dY^T X need transposed operands).
+// Persistent CTAs walk TR x TC tiles of the bf16 input.  Each tile arrives by
+// one TMA copy into a 3-stage shared-memory ring, and from that single HBM
+// read the CTA produces the row-wise quantization (RHT and blocks along the
+// columns) and the column-wise quantization of the transpose (RHT and blocks
+// along the rows), as required for FPROP, DGRAD and WGRAD (UFP4 summary,
+// section 方法: RHT on all three training GEMMs; 2D-block tutorial: dX = dY W
+// and dW = dY^T X need transposed operands).
 //
-//  * row pass: each thread carries 16 consecutive elements of a row, loaded
-//    with one 256-bit (or two 128-bit) coalesced load, widened to fp32,
-//    transformed (in-register butterflies for strides < 16, warp shuffles
-//    above), scaled, rounded and packed straight from registers;
-//  * column pass: the same bf16 values are parked in shared memory with an
-//    XOR swizzle of 16-byte units by (row / 16), so that a warp reading 16
-//    consecutive rows of 32/S columns hits distinct banks; each thread then
-//    carries 16 consecutive rows of one column through the same steps;
+//  * row pass: a thread carries 16 consecutive elements of a row, widened to
+//    fp32 with the random signs folded into the widening, transformed with
+//    paired fp32 butterflies (shuffles for strides >= 16), scaled by one
+//    folded reciprocal per block, rounded and packed;
+//  * column pass: a thread gathers two adjacent columns, 16 rows each, with
+//    one 32-bit shared load per row, and runs them through the same steps;
 //  * 2-D b x b blocks reduce their amax through shared-memory atomics.
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -24,8 +24,12 @@
 
 namespace ufp4 {
 
+__device__ int g_quant_error;
+
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kMaxStages = 6;               // TMA ring depth (up to 96 KB of tiles in flight per CTA)
+constexpr uint32_t kWaitLimit = 1u << 24;   // bounded mbarrier polling
 
 __device__ __forceinline__ int find_group(const QuantParams& p, int row_tile) {
     int g = 0;
@@ -45,285 +49,506 @@ __device__ __forceinline__ uint32_t chunk_signs(const QuantParams& p, int pos) {
     return (p.sign_bits[pos >> 5] >> (pos & 31)) & 0xFFFFu;
 }
 
-// Scale, round, pack and store one 16-element chunk of transformed values z.
-// M0 is the amax of the block holding elements 0..7, M1 of 8..15 (equal
-// unless blocks are 8 wide).  w0 / w1: this thread writes the block's scale.
-template <int GRID, bool SR, bool PO2>
-__device__ __forceinline__ void emit_chunk(const float z[16], float M0, float M1, bool valid,
-                                           bool w0, bool w1, uint8_t* codes_ptr, void* scales,
-                                           int64_t si0, int64_t si1, uint64_t sr_seed,
-                                           uint64_t lin0, uint32_t stream, uint32_t group) {
+__device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
+    return (uint32_t)__cvta_generic_to_shared(ptr);
+}
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
+            : "=r"(ok)
+            : "r"(bar), "r"(parity)
+            : "memory");
+        if (ok) return true;
+    }
+    return false;
+}
+
+// Constants of a launch that the per-chunk code needs.
+struct Fold {
+    float inv_s;   // fp32(1/sqrt n)
+    bool pow4;     // n = 4^j: 1/sqrt n = 2^-j folds exactly into the block reciprocal
+    int j;         // log4 n when pow4
+};
+
+// Scale, round, pack and store two 16-element vectors a and b held as pairs
+// e[i] = (a_i, b_i) of transformed values before the 1/sqrt(n) multiply
+// (y = H S x).  MA0/MA1 (MB0/MB1): amax of |y| over the blocks holding
+// elements 0..7 / 8..15 of a (of b).  The block amax of z = y/sqrt n is
+// fp32(My * fp32(1/sqrt n)) (rounding is monotone), exact for n = 4^j.
+//
+// RTNE multiplies y by one folded reciprocal per block, rr = r * 2^-j * f,
+// where f = 2^-7 (E1M2: k/4 -> k * 2^-9) or 2^-9 (INT4: k -> k * 2^-9) puts
+// the uniform levels on e4m3's subnormals, and f = 1 for E2M1; every factor
+// is a power of two, so fp32(y * rr) = fp32(z * r) * f exactly.  SR uses
+// f = 1/step (E1M2 4, INT4 1, E2M1 1).  For other n, z = fp32(y * 1/sqrt n)
+// is formed first, as in the definition.
+template <int GRID, bool PO2>
+__device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, bool write, uint8_t* sptr) {
     constexpr float qmax = grid_qmax(GRID);
-    float r0, r1;
+    const float Mz = __fmul_rn(My, fd.inv_s);
+    const int lj = fd.pow4 ? -fd.j : 0;
     if (PO2) {
-        const int e0 = scale_po2<GRID>(M0, r0);
-        const int e1 = scale_po2<GRID>(M1, r1);
-        if (valid) {
-            uint8_t* sb = (uint8_t*)scales;
-            if (w0) sb[si0] = (uint8_t)(e0 + 127);
-            if (w1) sb[si1] = (uint8_t)(e1 + 127);
-        }
+        float r;
+        const int e = scale_po2<GRID>(Mz, r);
+        if (write) *sptr = (uint8_t)(e + 127);
+        return pow2_exact(-e + lf + lj);
     } else {
-        float s0, s1;
-        scale_fp32(M0, qmax, s0, r0);
-        scale_fp32(M1, qmax, s1, r1);
-        if (valid) {
-            float* sb = (float*)scales;
-            if (w0) sb[si0] = s0;
-            if (w1) sb[si1] = s1;
-        }
+        float sc, r;
+        scale_fp32(Mz, qmax, sc, r);
+        if (write) *reinterpret_cast<float*>(sptr) = sc;
+        return __fmul_rn(r, pow2_exact(lf + lj));
     }
-    uint2 packed;
+}
+
+template <int GRID>
+__device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uint64_t lin0, uint32_t stream,
+                                        uint32_t group) {
+    constexpr float qmax = grid_qmax(GRID);
+    uint32_t w[8];
+    sr_draws16(sr_seed, lin0, stream, group, w);
+    uint32_t out[2] = {0u, 0u};
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
+        const float ti = t[i];
+        uint32_t idx;
+        if (GRID == 2) {
+            const float a = fminf(fabsf(ti), qmax);
+            const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+            const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+            const float vv = __fmul_rn(a, inv);
+            const float fl = floorf(vv);
+            const float up = ((float)u < __fmul_rn(__fsub_rn(vv, fl), 65536.0f)) ? 1.0f : 0.0f;
+            idx = cvt_e2m1x2(0.0f, __fmul_rn(__fadd_rn(fl, up), gap)) & 7u;
+        } else {
+            const float vv = fminf(fabsf(ti), 7.0f);  // in steps of the uniform grid
+            const float fl = floorf(vv);
+            idx = (uint32_t)fl + (((float)u < __fmul_rn(__fsub_rn(vv, fl), 65536.0f)) ? 1u : 0u);
+        }
+        const uint32_t neg = __float_as_uint(ti) >> 31;
+        out[i >> 3] |= (idx == 0 ? 0u : ((neg << 3) | idx)) << (4 * (i & 7));
+    }
+    if (GRID == 1) {
+        out[0] = signmag_to_twos(out[0]);
+        out[1] = signmag_to_twos(out[1]);
+    }
+    return make_uint2(out[0], out[1]);
+}
+
+template <int GRID, bool SR, bool PO2>
+__device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
+                                          const Fold& fd, const Dest& A, const Dest& B,
+                                          uint64_t sr_seed, uint32_t stream, uint32_t group) {
+    constexpr int lf = SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0));  // log2 f
+    const float ra0 = block_recip<GRID, PO2>(MA0, fd, lf, A.valid && A.w0, A.s0);
+    const float rb0 = block_recip<GRID, PO2>(MB0, fd, lf, B.valid && B.w0, B.s0);
+    float ra1 = ra0, rb1 = rb0;
+    if (split) {
+        ra1 = block_recip<GRID, PO2>(MA1, fd, lf, A.valid && A.w1, A.s1);
+        rb1 = block_recip<GRID, PO2>(MB1, fd, lf, B.valid && B.w1, B.s1);
+    }
+    if (!fd.pow4) {
+        const uint64_t is2 = pk2(fd.inv_s, fd.inv_s);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) e[i] = mul2(e[i], is2);
+    }
+    const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
+    float ta[16], tb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) up2(mul2(e[i], i < 8 ? q0 : q1), ta[i], tb[i]);
+    uint2 ca, cb;
     if (SR) {
-        uint32_t w[8];
-        sr_draws16(sr_seed, lin0, stream, group, w);
-        packed = round_sr16<GRID>(z, r0, r1, w);
+        ca = sr_vec<GRID>(ta, sr_seed, A.lin0, stream, group);
+        cb = sr_vec<GRID>(tb, sr_seed, B.lin0, stream, group);
     } else {
-        packed = round_rtne16<GRID>(z, r0, r1);
+        ca = make_uint2(rtne8<GRID>(ta[0], ta[1], ta[2], ta[3], ta[4], ta[5], ta[6], ta[7]),
+                        rtne8<GRID>(ta[8], ta[9], ta[10], ta[11], ta[12], ta[13], ta[14], ta[15]));
+        cb = make_uint2(rtne8<GRID>(tb[0], tb[1], tb[2], tb[3], tb[4], tb[5], tb[6], tb[7]),
+                        rtne8<GRID>(tb[8], tb[9], tb[10], tb[11], tb[12], tb[13], tb[14], tb[15]));
     }
-    if (valid) *reinterpret_cast<uint2*>(codes_ptr) = packed;
+    if (A.valid) *reinterpret_cast<uint2*>(A.codes) = ca;
+    if (B.valid) *reinterpret_cast<uint2*>(B.codes) = cb;
 }
 
-// widen + signs + FWHT + 1/sqrt(n)
-__device__ __forceinline__ void build_z(const uint32_t w[8], uint32_t sgn, int n, int seg_lane,
-                                        float inv_sqrt_n, float z[16]) {
-    widen16(w, sgn, z);
-    fwht16(z, n, seg_lane);
-#pragma unroll
-    for (int i = 0; i < 16; ++i) z[i] = __fmul_rn(z[i], inv_sqrt_n);
+// 1-D block amax over bw/16 neighbouring lanes (bw >= 16), for both vectors.
+__device__ __forceinline__ void amax_1d_pair(const uint64_t e[16], int bw, float& ma, float& mb) {
+    amax_pair(e, 0, 16, ma, mb);
+    for (int k = 1; k < bw / kChunk; k <<= 1) {
+        ma = fmaxf(ma, __shfl_xor_sync(0xFFFFFFFFu, ma, k));
+        mb = fmaxf(mb, __shfl_xor_sync(0xFFFFFFFFu, mb, k));
+    }
 }
 
-// Amax of a 1-D block of width bw >= 16 spread over bw/16 neighbouring lanes.
-__device__ __forceinline__ float amax_1d(const float z[16], int bw) {
-    float m = amax_range(z, 0, 16);
-    for (int k = 1; k < bw / kChunk; k <<= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, k));
-    return m;
-}
-
-// Read 16 consecutive rows (rchunk*16 ..) of tile column tcol from the
-// swizzled tile (row r's 16-byte unit u lives at u ^ (((r/16) & 7) << 1)).
+// Row pass: 16 consecutive elements of tile row trow from shared memory.
 template <int TC>
-__device__ __forceinline__ void gather_column(const uint16_t* tile, int tcol, int rchunk, uint32_t w[8]) {
-    const int sw = (rchunk & 7) << 1;
-    const int u = (tcol >> 3) ^ sw;
-    const uint16_t* base = tile + (rchunk * kChunk) * TC + u * 8 + (tcol & 7);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t ea = base[(2 * j) * TC];
-        const uint32_t eb = base[(2 * j + 1) * TC];
-        w[j] = ea | (eb << 16);
-    }
+__device__ __forceinline__ void load_row_chunk(const uint16_t* tile, int trow, int cchunk, uint32_t w[8]) {
+    const uint4* src = reinterpret_cast<const uint4*>(tile + trow * TC + cchunk * kChunk);
+    const uint4 a = src[0], b = src[1];
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
 
-template <int GRID, bool SR, bool PO2, int TR, int TC>
-__global__ void __launch_bounds__(kThreads)
-quantize_kernel(const QuantParams p) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
-    uint16_t* tile = reinterpret_cast<uint16_t*>(smem_raw);
-    uint32_t* amax2d = reinterpret_cast<uint32_t*>(smem_raw + (p.do_col ? TR * TC * 2 : 0));
+// Column pass: rows rchunk*16 .. +15 of the column pair (tcol, tcol+1), one
+// 32-bit shared load per row (column tcol in the low half).
+template <int TC>
+__device__ __forceinline__ void gather_pair(const uint16_t* tile, int tcol, int rchunk, uint32_t g[16]) {
+    const uint32_t* src = reinterpret_cast<const uint32_t*>(tile + (rchunk * kChunk) * TC + tcol);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) g[i] = src[i * (TC / 2)];
+}
+
+template <int GRID, bool SR, bool PO2, int TC>
+__global__ void __launch_bounds__(kThreads, 2)
+quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, const int num_tiles) {
+    extern __shared__ uint8_t smem_raw[];
+    constexpr int SZ = PO2 ? 1 : 4;         // bytes per scale
+    const int TR = p.tile_rows;             // 64 or 128 (runtime)
+    const int tile_bytes = TR * TC * 2;
+    const int kStages = p.stages;           // ring depth (runtime, <= kMaxStages)
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+    uint8_t* base = smem_raw + pad;
+    uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * tile_bytes);
+    const uint32_t bars = smem_addr(base + kStages * tile_bytes + 4 * p.amax_slots);  // 8-byte aligned
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
-    const int row_tile = blockIdx.x / p.col_tiles;
-    const int col_tile = blockIdx.x % p.col_tiles;
-    const int g = find_group(p, row_tile);
-    const int64_t grow0 = p.grp_row0[g];                       // group's first input row
-    const int64_t cnt = p.grp_row0[g + 1] - grow0;             // real rows of the group
-    const int64_t padded = p.grp_pad0[g + 1] - p.grp_pad0[g];  // column-pass length
-    const int64_t lr0 = (int64_t)(row_tile - p.grp_tile0[g]) * TR;  // tile's first row in the group
-    const int64_t c0 = (int64_t)col_tile * TC;
     const int n = p.n;
-    const int nslot = p.is2d ? (TR / p.b2d) * (TC / p.b2d) : 0;
+    Fold fd;
+    fd.inv_s = p.inv_sqrt_n;
+    fd.pow4 = p.pow4;
+    fd.j = p.log4n;
 
+    auto issue = [&](int tile, int s) {
+        const int row_tile = tile / p.col_tiles;
+        const int g = find_group(p, row_tile);
+        const int64_t lr0 = (int64_t)(row_tile - p.grp_tile0[g]) * TR;
+        const int64_t c0 = (int64_t)(tile - row_tile * p.col_tiles) * TC;
+        const uint32_t bar = bars + 8u * s;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(tile_bytes)
+                     : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(smem_addr(base + s * tile_bytes)), "l"((uint64_t)&tmap), "r"((int)c0),
+            "r"((int)(p.grp_row0[g] + lr0)), "r"(bar)
+            : "memory");
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int tile = blockIdx.x + s * gridDim.x;
+            if (tile < num_tiles) issue(tile, s);
+        }
+
+    // row pass: a thread owns chunk column cchunk of the row pairs
+    // (r, r + kRPI), r = r0 + 2 * kRPI * it
     constexpr int kCPR = TC / kChunk;       // chunks per tile row
-    constexpr int kRPI = kThreads / kCPR;   // tile rows per iteration
-    constexpr int kIters = TR / kRPI;
-
-    // ------------------------------------------------ load (one HBM read)
+    constexpr int kRPI = kThreads / kCPR;   // tile rows per thread step
+    const int pairs = TR / (2 * kRPI);
     const int cchunk = tid % kCPR;
-    const int64_t col = c0 + cchunk * kChunk;
-    uint32_t w[kIters][8];
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-        const int trow = it * kRPI + tid / kCPR;
-        const int64_t lrow = lr0 + trow;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[it][j] = 0u;
-        if (lrow < cnt && col < p.cols) {
-            const uint16_t* src = p.x + (grow0 + lrow) * p.ld + col;
-            if (p.vec256) {
-                asm volatile("ld.global.nc.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                             : "=r"(w[it][0]), "=r"(w[it][1]), "=r"(w[it][2]), "=r"(w[it][3]),
-                               "=r"(w[it][4]), "=r"(w[it][5]), "=r"(w[it][6]), "=r"(w[it][7])
-                             : "l"(src));
-            } else {
-                const uint4 a = __ldg(reinterpret_cast<const uint4*>(src));
-                const uint4 b = __ldg(reinterpret_cast<const uint4*>(src) + 1);
-                w[it][0] = a.x; w[it][1] = a.y; w[it][2] = a.z; w[it][3] = a.w;
-                w[it][4] = b.x; w[it][5] = b.y; w[it][6] = b.z; w[it][7] = b.w;
-            }
-        }
-    }
-    if (p.do_col) {
-#pragma unroll
-        for (int it = 0; it < kIters; ++it) {
-            const int trow = it * kRPI + tid / kCPR;
-            const int sw = ((trow >> 4) & 7) << 1;
-            uint4* rowp = reinterpret_cast<uint4*>(tile + trow * TC);
-            const uint4 lo = make_uint4(w[it][0], w[it][1], w[it][2], w[it][3]);
-            const uint4 hi = make_uint4(w[it][4], w[it][5], w[it][6], w[it][7]);
-            // alternate the store order over lane quads to spread the banks
-            if ((cchunk >> 2) & 1) {
-                rowp[(2 * cchunk + 1) ^ sw] = hi;
-                rowp[(2 * cchunk) ^ sw] = lo;
-            } else {
-                rowp[(2 * cchunk) ^ sw] = lo;
-                rowp[(2 * cchunk + 1) ^ sw] = hi;
-            }
-        }
-    }
+    const int r0 = tid / kCPR;
+    const int seg_row = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
+    SignMasks mrow;
+    make_masks(chunk_signs(p, cchunk * kChunk), mrow);
+    const int lbw = p.lbw_row, lbwc = p.lbw_col, lb = p.lb2d;
+    // column pass: S = 2^lS lanes share one column segment; a warp task is
+    // 32/S column pairs x S row chunks
+    const int lS = p.lseg;
+    const int S = 1 << lS;
+    const int lncb = 1 + lS;                 // log2((TC/2) / (32/S)) for TC = 128
+    const int ncb_mask = (1 << lncb) - 1;
+    const int col_tasks = TR * TC / (kChunk * 64 * kWarps);  // per warp
+    const int nslot = p.amax_slots;
+    // tile coordinates advance by gridDim.x tiles per step, without division
+    const int step_r = gridDim.x / p.col_tiles, step_c = gridDim.x - step_r * p.col_tiles;
+    int row_tile = blockIdx.x / p.col_tiles, col_tile = blockIdx.x - row_tile * p.col_tiles;
+    int g = p.num_groups > 1 ? find_group(p, row_tile) : 0;
 
-    // ------------------------------------------------------------ row pass
-    if (p.do_row) {
-        const int seg_lane = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
-        const uint32_t sgn = chunk_signs(p, cchunk * kChunk);
-        const int bw = p.bw_row;
-        if (p.is2d) {
-            const int b = p.b2d;
-            const int nbc = TC / b;
-            for (int i = tid; i < nslot; i += kThreads) amax2d[i] = 0u;
+    int i = 0;
+    for (;; ++i) {
+        const int tile = blockIdx.x + i * gridDim.x;
+        if (tile >= num_tiles) break;
+        if (i) {
+            col_tile += step_c;
+            row_tile += step_r;
+            if (col_tile >= p.col_tiles) {
+                col_tile -= p.col_tiles;
+                ++row_tile;
+            }
+            if (p.num_groups > 1) g = find_group(p, row_tile);
+        }
+        const int s = i % kStages;
+        const bool landed = wait_phase(bars + 8u * s, (uint32_t)((i / kStages) & 1));
+        if (!__syncthreads_and(landed)) {
+            if (tid == 0) atomicExch(&g_quant_error, 1);
+            break;
+        }
+        const int64_t lr0 = (int64_t)(row_tile - p.grp_tile0[g]) * TR;
+        const int64_t c0 = (int64_t)col_tile * TC;
+        const int64_t grow0 = p.grp_row0[g];
+        const int64_t cnt = p.grp_row0[g + 1] - grow0;
+        const int64_t padded = p.grp_pad0[g + 1] - p.grp_pad0[g];
+        const uint32_t grp_id = (uint32_t)(p.group_base + g);
+        uint16_t* tile_s = reinterpret_cast<uint16_t*>(base + s * tile_bytes);
+        if (p.do_col && lr0 + TR > cnt) {
+            // rows past the group's end belong to the next group (or the
+            // padding): the column pass must see zeros there
+            const int first = cnt - lr0 > 0 ? (int)(cnt - lr0) : 0;
+            uint4* t4 = reinterpret_cast<uint4*>(tile_s + first * TC);
+            for (int q = tid; q < (TR - first) * TC / 8; q += kThreads) t4[q] = make_uint4(0, 0, 0, 0);
             __syncthreads();
-#pragma unroll
-            for (int it = 0; it < kIters; ++it) {
-                const int trow = it * kRPI + tid / kCPR;
-                float z[16];
-                build_z(w[it], sgn, n, seg_lane, p.inv_sqrt_n, z);
-                if (b == 8) {
-                    post_amax(&amax2d[(trow / b) * nbc + 2 * cchunk], amax_range(z, 0, 8));
-                    post_amax(&amax2d[(trow / b) * nbc + 2 * cchunk + 1], amax_range(z, 8, 16));
-                } else {
-                    post_amax(&amax2d[(trow / b) * nbc + (cchunk * kChunk) / b], amax_range(z, 0, 16));
+        }
+
+        // -------------------------------------------------------- row pass
+        if (p.do_row) {
+            const int64_t col = c0 + cchunk * kChunk;
+            const bool col_ok = col < p.cols;
+            // rows of this tile that exist, counted from this thread's first row
+            const int64_t left = cnt - lr0 - r0;
+            const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
+            if (p.is2d) {
+                const int lnbc = 7 + (TC == 256) - lb;  // log2(TC / b)
+                const int bmask = (1 << lb) - 1;
+                for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
+                __syncthreads();
+                for (int it = 0; it < pairs; ++it) {
+                    const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
+                    uint32_t wa[8], wb[8];
+                    uint64_t e[16];
+                    load_row_chunk<TC>(tile_s, ra, cchunk, wa);
+                    load_row_chunk<TC>(tile_s, rb, cchunk, wb);
+                    widen_rows(wa, wb, mrow, e);
+                    fwht_pair(e, n, seg_row);
+                    const int sa = (ra >> lb) << lnbc, sb = (rb >> lb) << lnbc;
+                    if (lb == 3) {
+                        float a0, b0, a1, b1;
+                        amax_pair(e, 0, 8, a0, b0);
+                        amax_pair(e, 8, 16, a1, b1);
+                        post_amax(&amax2d[sa + 2 * cchunk], a0);
+                        post_amax(&amax2d[sa + 2 * cchunk + 1], a1);
+                        post_amax(&amax2d[sb + 2 * cchunk], b0);
+                        post_amax(&amax2d[sb + 2 * cchunk + 1], b1);
+                    } else {
+                        float a0, b0;
+                        amax_pair(e, 0, 16, a0, b0);
+                        post_amax(&amax2d[sa + ((cchunk * kChunk) >> lb)], a0);
+                        post_amax(&amax2d[sb + ((cchunk * kChunk) >> lb)], b0);
+                    }
+                }
+                __syncthreads();
+                for (int it = 0; it < pairs; ++it) {
+                    const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
+                    uint32_t wa[8], wb[8];
+                    uint64_t e[16];
+                    load_row_chunk<TC>(tile_s, ra, cchunk, wa);
+                    load_row_chunk<TC>(tile_s, rb, cchunk, wb);
+                    widen_rows(wa, wb, mrow, e);
+                    fwht_pair(e, n, seg_row);
+                    const int off = lb == 3 ? 2 * cchunk : ((cchunk * kChunk) >> lb);
+                    const int sa = ((ra >> lb) << lnbc) + off, sb = ((rb >> lb) << lnbc) + off;
+                    const float MA0 = __uint_as_float(amax2d[sa]);
+                    const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
+                    const float MB0 = __uint_as_float(amax2d[sb]);
+                    const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                    Dest A, B;
+                    const int64_t la = lr0 + ra, lbr = lr0 + rb;
+                    const bool colfirst = lb == 3 || (col & bmask) == 0;
+                    uint8_t* sbase = (uint8_t*)p.row.scales;
+                    A.codes = (uint8_t*)p.row.codes + (grow0 + la) * p.row.codes_ld + (col >> 1);
+                    B.codes = (uint8_t*)p.row.codes + (grow0 + lbr) * p.row.codes_ld + (col >> 1);
+                    A.s0 = sbase + ((la >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
+                    B.s0 = sbase + ((lbr >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
+                    A.s1 = A.s0 + SZ;
+                    B.s1 = B.s0 + SZ;
+                    A.valid = la < cnt && col_ok;
+                    B.valid = lbr < cnt && col_ok;
+                    A.w0 = (la & bmask) == 0 && colfirst;
+                    B.w0 = (lbr & bmask) == 0 && colfirst;
+                    A.w1 = (la & bmask) == 0 && lb == 3;
+                    B.w1 = (lbr & bmask) == 0 && lb == 3;
+                    A.lin0 = (uint64_t)la * (uint64_t)p.cols + (uint64_t)col;
+                    B.lin0 = (uint64_t)lbr * (uint64_t)p.cols + (uint64_t)col;
+                    emit_pair<GRID, SR, PO2>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 0u, grp_id);
+                }
+            } else {
+                const bool wsc = (col & ((1 << lbw) - 1)) == 0;
+                // output pointers of this thread's first row, stepped per pair
+                const int64_t orow0 = grow0 + lr0 + r0;  // row-wise output rows follow the input rows
+                uint8_t* cp = (uint8_t*)p.row.codes + orow0 * p.row.codes_ld + (col >> 1);
+                uint8_t* sp = (uint8_t*)p.row.scales + (orow0 * p.row.scales_ld + (col >> lbw)) * SZ;
+                const int64_t cstep = (int64_t)kRPI * p.row.codes_ld;
+                const int64_t sstep = (int64_t)kRPI * p.row.scales_ld * SZ;
+                uint64_t lin = (uint64_t)(lr0 + r0) * (uint64_t)p.cols + (uint64_t)col;
+                const uint64_t lstep = (uint64_t)kRPI * (uint64_t)p.cols;
+                for (int it = 0; it < pairs; ++it) {
+                    const int ra = 2 * kRPI * it;
+                    uint32_t wa[8], wb[8];
+                    uint64_t e[16];
+                    const uint4* pa = reinterpret_cast<const uint4*>(src + ra * TC);
+                    const uint4* pb = reinterpret_cast<const uint4*>(src + (ra + kRPI) * TC);
+                    const uint4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
+                    wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
+                    wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+                    wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
+                    wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+                    widen_rows(wa, wb, mrow, e);
+                    fwht_pair(e, n, seg_row);
+                    float Ma, Mb;
+                    amax_1d_pair(e, 1 << lbw, Ma, Mb);
+                    Dest A, B;
+                    A.codes = cp + (2 * it) * cstep;
+                    B.codes = A.codes + cstep;
+                    A.s0 = A.s1 = sp + (2 * it) * sstep;
+                    B.s0 = B.s1 = A.s0 + sstep;
+                    A.valid = ra < left && col_ok;
+                    B.valid = ra + kRPI < left && col_ok;
+                    A.w0 = B.w0 = wsc;
+                    A.w1 = B.w1 = false;
+                    A.lin0 = lin + (uint64_t)(2 * it) * lstep;
+                    B.lin0 = A.lin0 + lstep;
+                    emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, grp_id);
                 }
             }
-            __syncthreads();
-#pragma unroll
-            for (int it = 0; it < kIters; ++it) {
-                const int trow = it * kRPI + tid / kCPR;
-                const int64_t lrow = lr0 + trow;
-                float z[16];
-                build_z(w[it], sgn, n, seg_lane, p.inv_sqrt_n, z);
-                const int s0 = (trow / b) * nbc + (b == 8 ? 2 * cchunk : (cchunk * kChunk) / b);
-                const float M0 = __uint_as_float(amax2d[s0]);
-                const float M1 = __uint_as_float(amax2d[b == 8 ? s0 + 1 : s0]);
-                const int64_t sidx = (lrow / b) * p.row.scales_ld + col / b;
-                const bool first_row = (lrow % b) == 0;
-                const bool w0 = first_row && (b == 8 || (col % b) == 0);
-                const bool w1 = first_row && b == 8;
-                uint8_t* cp = (uint8_t*)p.row.codes + (grow0 + lrow) * p.row.codes_ld + col / 2;
-                const uint64_t lin0 = (uint64_t)lrow * (uint64_t)p.cols + (uint64_t)col;
-                emit_chunk<GRID, SR, PO2>(z, M0, M1, lrow < cnt && col < p.cols, w0, w1, cp,
-                                          p.row.scales, sidx, sidx + 1, p.sr_seed, lin0, 0u, (uint32_t)(p.group_base + g));
-            }
-        } else {
-#pragma unroll
-            for (int it = 0; it < kIters; ++it) {
-                const int trow = it * kRPI + tid / kCPR;
-                const int64_t lrow = lr0 + trow;
-                const int64_t orow = grow0 + lrow;  // row-wise output rows follow the input rows
-                float z[16];
-                build_z(w[it], sgn, n, seg_lane, p.inv_sqrt_n, z);
-                const float M = amax_1d(z, bw);
-                const int64_t sidx = orow * p.row.scales_ld + col / bw;
-                uint8_t* cp = (uint8_t*)p.row.codes + orow * p.row.codes_ld + col / 2;
-                const uint64_t lin0 = (uint64_t)lrow * (uint64_t)p.cols + (uint64_t)col;
-                emit_chunk<GRID, SR, PO2>(z, M, M, lrow < cnt && col < p.cols, (col % bw) == 0, false,
-                                          cp, p.row.scales, sidx, sidx, p.sr_seed, lin0, 0u, (uint32_t)(p.group_base + g));
-            }
         }
-    }
-    if (!p.do_col) return;
 
-    // --------------------------------------------------------- column pass
-    __syncthreads();
-    // S lanes share one column segment (S consecutive 16-row chunks of one
-    // column); a warp task covers 32/S columns x S chunks.
-    const int S = p.col_seg_lanes;
-    const int cpw = 32 / S;
-    const int ncb = TC / cpw;
-    constexpr int kTasks = (TR / kChunk) * TC / 32 / kWarps;  // tasks per warp
-    const int bwc = p.bw_col;
-    const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
-    const int sdiv = p.is2d ? p.b2d : bwc;
-    const int64_t sc_ld = p.col_grouped ? padded / sdiv : p.col.scales_ld;
-    uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
-    uint8_t* gscales = (uint8_t*)p.col.scales +
-                       (p.col_grouped ? p.cols * (p.grp_pad0[g] / sdiv) * (PO2 ? 1 : 4) : 0);
-    if (p.is2d) {
-        const int b = p.b2d;
-        const int nbq = TR / b;  // blocks along the quantized dimension (tile rows)
-        for (int i = tid; i < nslot; i += kThreads) amax2d[i] = 0u;
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kTasks; ++k) {
-            const int t = warp + kWarps * k;
-            const int tcol = (t % ncb) * cpw + lane / S;
-            const int rchunk = (t / ncb) * S + lane % S;
-            uint32_t wc[8];
-            gather_column<TC>(tile, tcol, rchunk, wc);
-            float z[16];
-            build_z(wc, chunk_signs(p, rchunk * kChunk), n, rchunk % S, p.inv_sqrt_n, z);
-            if (b == 8) {
-                post_amax(&amax2d[(tcol / b) * nbq + 2 * rchunk], amax_range(z, 0, 8));
-                post_amax(&amax2d[(tcol / b) * nbq + 2 * rchunk + 1], amax_range(z, 8, 16));
+        // ----------------------------------------------------- column pass
+        if (p.do_col) {
+            const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
+            const int lsd = p.is2d ? lb : lbwc;
+            const int64_t sc_ld = p.col_grouped ? (padded >> lsd) : p.col.scales_ld;
+            uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
+            uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lsd) * SZ : 0);
+            if (p.is2d) {
+                const int lnbq = (TR == 128 ? 7 : 6) - lb;  // log2(TR / b)
+                const int bmask = (1 << lb) - 1;
+                for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
+                __syncthreads();
+                for (int k = 0; k < col_tasks; ++k) {
+                    const int t = warp + kWarps * k;
+                    const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
+                    const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
+                    SignMasks mc;
+                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
+                    uint32_t gw[16];
+                    uint64_t e[16];
+                    gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                    widen_cols(gw, mc, e);
+                    fwht_pair(e, n, rchunk & (S - 1));
+                    const int sa = (tcol >> lb) << lnbq, sb = ((tcol + 1) >> lb) << lnbq;
+                    if (lb == 3) {
+                        float a0, b0, a1, b1;
+                        amax_pair(e, 0, 8, a0, b0);
+                        amax_pair(e, 8, 16, a1, b1);
+                        post_amax(&amax2d[sa + 2 * rchunk], a0);
+                        post_amax(&amax2d[sa + 2 * rchunk + 1], a1);
+                        post_amax(&amax2d[sb + 2 * rchunk], b0);
+                        post_amax(&amax2d[sb + 2 * rchunk + 1], b1);
+                    } else {
+                        float a0, b0;
+                        amax_pair(e, 0, 16, a0, b0);
+                        post_amax(&amax2d[sa + ((rchunk * kChunk) >> lb)], a0);
+                        post_amax(&amax2d[sb + ((rchunk * kChunk) >> lb)], b0);
+                    }
+                }
+                __syncthreads();
+                for (int k = 0; k < col_tasks; ++k) {
+                    const int t = warp + kWarps * k;
+                    const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
+                    const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
+                    SignMasks mc;
+                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
+                    uint32_t gw[16];
+                    uint64_t e[16];
+                    gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                    widen_cols(gw, mc, e);
+                    fwht_pair(e, n, rchunk & (S - 1));
+                    const int off = lb == 3 ? 2 * rchunk : ((rchunk * kChunk) >> lb);
+                    const int sa = ((tcol >> lb) << lnbq) + off, sb = (((tcol + 1) >> lb) << lnbq) + off;
+                    const float MA0 = __uint_as_float(amax2d[sa]);
+                    const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
+                    const float MB0 = __uint_as_float(amax2d[sb]);
+                    const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                    const int64_t lrow = lr0 + rchunk * kChunk;
+                    const int64_t ca = c0 + tcol, cb = ca + 1;
+                    const bool rowfirst = lb == 3 || (lrow & bmask) == 0;
+                    Dest A, B;
+                    A.codes = gcodes + ca * out_ld + (lrow >> 1);
+                    B.codes = gcodes + cb * out_ld + (lrow >> 1);
+                    A.s0 = gscales + ((ca >> lb) * sc_ld + (lrow >> lb)) * SZ;
+                    B.s0 = gscales + ((cb >> lb) * sc_ld + (lrow >> lb)) * SZ;
+                    A.s1 = A.s0 + SZ;
+                    B.s1 = B.s0 + SZ;
+                    A.valid = lrow < padded && ca < p.cols;
+                    B.valid = lrow < padded && cb < p.cols;
+                    A.w0 = (ca & bmask) == 0 && rowfirst;
+                    B.w0 = (cb & bmask) == 0 && rowfirst;
+                    A.w1 = (ca & bmask) == 0 && lb == 3;
+                    B.w1 = (cb & bmask) == 0 && lb == 3;
+                    A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
+                    B.lin0 = A.lin0 + (uint64_t)padded;
+                    emit_pair<GRID, SR, PO2>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 1u, grp_id);
+                }
             } else {
-                post_amax(&amax2d[(tcol / b) * nbq + (rchunk * kChunk) / b], amax_range(z, 0, 16));
+                const int bwc = 1 << lbwc;
+                for (int k = 0; k < col_tasks; ++k) {
+                    const int t = warp + kWarps * k;
+                    const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
+                    const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
+                    SignMasks mc;
+                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
+                    uint32_t gw[16];
+                    uint64_t e[16];
+                    gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                    widen_cols(gw, mc, e);
+                    fwht_pair(e, n, rchunk & (S - 1));
+                    float Ma, Mb;
+                    amax_1d_pair(e, bwc, Ma, Mb);
+                    const int64_t lrow = lr0 + rchunk * kChunk;
+                    const bool wsc = (lrow & (bwc - 1)) == 0;
+                    const int64_t ca = c0 + tcol, cb = ca + 1;
+                    Dest A, B;
+                    A.codes = gcodes + ca * out_ld + (lrow >> 1);
+                    B.codes = A.codes + out_ld;
+                    A.s0 = A.s1 = gscales + (ca * sc_ld + (lrow >> lbwc)) * SZ;
+                    B.s0 = B.s1 = A.s0 + sc_ld * SZ;
+                    A.valid = lrow < padded && ca < p.cols;
+                    B.valid = lrow < padded && cb < p.cols;
+                    A.w0 = B.w0 = wsc;
+                    A.w1 = B.w1 = false;
+                    A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
+                    B.lin0 = A.lin0 + (uint64_t)padded;
+                    emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 1u, grp_id);
+                }
             }
         }
+        // everyone is done with stage s: refill it (the fence orders this
+        // CTA's generic shared-memory accesses before the async-proxy write)
         __syncthreads();
-#pragma unroll
-        for (int k = 0; k < kTasks; ++k) {
-            const int t = warp + kWarps * k;
-            const int tcol = (t % ncb) * cpw + lane / S;
-            const int rchunk = (t / ncb) * S + lane % S;
-            uint32_t wc[8];
-            gather_column<TC>(tile, tcol, rchunk, wc);
-            float z[16];
-            build_z(wc, chunk_signs(p, rchunk * kChunk), n, rchunk % S, p.inv_sqrt_n, z);
-            const int s0 = (tcol / b) * nbq + (b == 8 ? 2 * rchunk : (rchunk * kChunk) / b);
-            const float M0 = __uint_as_float(amax2d[s0]);
-            const float M1 = __uint_as_float(amax2d[b == 8 ? s0 + 1 : s0]);
-            const int64_t colg = c0 + tcol;
-            const int64_t lrow = lr0 + rchunk * kChunk;
-            const int64_t sidx = (colg / b) * sc_ld + lrow / b;
-            const bool first_col = (colg % b) == 0;
-            const bool w0 = first_col && (b == 8 || (lrow % b) == 0);
-            const bool w1 = first_col && b == 8;
-            uint8_t* cp = gcodes + colg * out_ld + lrow / 2;
-            const uint64_t lin0 = (uint64_t)colg * (uint64_t)padded + (uint64_t)lrow;
-            emit_chunk<GRID, SR, PO2>(z, M0, M1, lrow < padded && colg < p.cols, w0, w1, cp, gscales,
-                                      sidx, sidx + 1, p.sr_seed, lin0, 1u, (uint32_t)(p.group_base + g));
-        }
-    } else {
-#pragma unroll
-        for (int k = 0; k < kTasks; ++k) {
-            const int t = warp + kWarps * k;
-            const int tcol = (t % ncb) * cpw + lane / S;
-            const int rchunk = (t / ncb) * S + lane % S;
-            uint32_t wc[8];
-            gather_column<TC>(tile, tcol, rchunk, wc);
-            float z[16];
-            build_z(wc, chunk_signs(p, rchunk * kChunk), n, rchunk % S, p.inv_sqrt_n, z);
-            const float M = amax_1d(z, bwc);
-            const int64_t colg = c0 + tcol;
-            const int64_t lrow = lr0 + rchunk * kChunk;
-            const int64_t sidx = colg * sc_ld + lrow / bwc;
-            uint8_t* cp = gcodes + colg * out_ld + lrow / 2;
-            const uint64_t lin0 = (uint64_t)colg * (uint64_t)padded + (uint64_t)lrow;
-            emit_chunk<GRID, SR, PO2>(z, M, M, lrow < padded && colg < p.cols, (lrow % bwc) == 0, false,
-                                      cp, gscales, sidx, sidx, p.sr_seed, lin0, 1u, (uint32_t)(p.group_base + g));
+        if (tid == 0) {
+            const int next = tile + kStages * gridDim.x;
+            if (next < num_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, s);
+            }
         }
     }
+    // a broken-off loop leaves copies in flight: let them land (bounded)
+    if (tid == 0)
+        for (int k = i; k < i + kStages; ++k) {
+            const int tile = blockIdx.x + k * gridDim.x;
+            if (tile >= num_tiles) break;
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1));
+        }
 }
 
 // ------------------------------------------------------------- RHT only
@@ -349,7 +574,10 @@ rht_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, flo
         const uint32_t sgn = (sb.bits[pos / 32] >> (pos % 32)) & 0xFFFFu;
         float v[16];
         const int seg_lane = (int)((cc * kChunk) % (n > kChunk ? n : kChunk)) / kChunk;
-        build_z(w, sgn, n, seg_lane, inv_sqrt_n, v);
+        widen16(w, sgn, v);
+        fwht16(v, n, seg_lane);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __fmul_rn(v[k], inv_sqrt_n);
         if (valid) {
             float4* dst = reinterpret_cast<float4*>(z + r * ldz + cc * kChunk);
 #pragma unroll
@@ -359,39 +587,55 @@ rht_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, flo
 }
 
 // ------------------------------------------------------------- launchers
-template <int GRID, bool SR, bool PO2, int TR, int TC>
-static cudaError_t launch_q(const QuantParams& p, int num_tiles, cudaStream_t st) {
-    const int amax_bytes = p.is2d ? (TR / p.b2d) * (TC / p.b2d) * 4 : 0;
-    const size_t smem = (p.do_col ? (size_t)TR * TC * 2 : 0) + amax_bytes;
-    auto k = quantize_kernel<GRID, SR, PO2, TR, TC>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-    }
-    k<<<num_tiles, kThreads, smem, st>>>(p);
+template <int GRID, bool SR, bool PO2, int TC>
+static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int num_tiles, int num_sms,
+                            cudaStream_t st) {
+    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 4 * (size_t)p.amax_slots + 8 * p.stages + 128;
+    auto k = quantize_kernel<GRID, SR, PO2, TC>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = num_tiles < 2 * num_sms ? num_tiles : 2 * num_sms;
+    k<<<grid, kThreads, smem, st>>>(map, p, num_tiles);
     return cudaGetLastError();
 }
 
 template <int GRID, bool SR, bool PO2>
-static cudaError_t launch_q_tiles(const QuantParams& p, int tc, int num_tiles, cudaStream_t st) {
-    if (tc == 256) return launch_q<GRID, SR, PO2, 64, 256>(p, num_tiles, st);
-    return launch_q<GRID, SR, PO2, 128, 128>(p, num_tiles, st);
+static cudaError_t launch_q_tiles(const CUtensorMap& map, const QuantParams& p, int tc, int num_tiles, int num_sms,
+                                  cudaStream_t st) {
+    if (tc == 256) return launch_q<GRID, SR, PO2, 256>(map, p, num_tiles, num_sms, st);
+    return launch_q<GRID, SR, PO2, 128>(map, p, num_tiles, num_sms, st);
 }
 
-cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int num_tiles,
-                            cudaStream_t st) {
-#define UFP4_Q(G)                                                                  \
-    if (grid == G) {                                                               \
-        if (sr) return po2 ? launch_q_tiles<G, true, true>(p, tc, num_tiles, st)   \
-                           : launch_q_tiles<G, true, false>(p, tc, num_tiles, st); \
-        return po2 ? launch_q_tiles<G, false, true>(p, tc, num_tiles, st)          \
-                   : launch_q_tiles<G, false, false>(p, tc, num_tiles, st);        \
+cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
+                            int64_t total_rows, int num_sms, cudaStream_t st) {
+    CUtensorMap map;
+    if (!encode_map_2d(&map, CU_TENSOR_MAP_DATA_TYPE_UINT16, p.x, (uint64_t)p.cols, (uint64_t)total_rows,
+                       (uint64_t)p.ld * 2, (uint32_t)tc, (uint32_t)tr, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+#define UFP4_Q(G)                                                                                   \
+    if (grid == G) {                                                                                \
+        if (sr) return po2 ? launch_q_tiles<G, true, true>(map, p, tc, num_tiles, num_sms, st)      \
+                           : launch_q_tiles<G, true, false>(map, p, tc, num_tiles, num_sms, st);    \
+        return po2 ? launch_q_tiles<G, false, true>(map, p, tc, num_tiles, num_sms, st)             \
+                   : launch_q_tiles<G, false, false>(map, p, tc, num_tiles, num_sms, st);           \
     }
     UFP4_Q(0)
     UFP4_Q(1)
     UFP4_Q(2)
 #undef UFP4_Q
     return cudaErrorInvalidValue;
+}
+
+cudaError_t quant_error_read_clear(int* value) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_quant_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_quant_error, &zero, sizeof(int));
+    }
+    *value = v;
+    return e;
 }
 
 cudaError_t launch_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n,

@@ -158,9 +158,9 @@ __device__ __forceinline__ uint32_t e2m3_bytes_to_nibbles(uint32_t w) {
 // A zero level is written as +0: clear the sign of every nibble whose
 // magnitude bits are zero.
 __device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
-    const uint32_t mag = w & 0x77777777u;
-    const uint32_t nz = (mag + 0x77777777u) & 0x88888888u;
-    return mag | (w & nz);
+    // per nibble, (mag + 7) has bit 3 set iff mag >= 1 (no carry leaves the nibble)
+    const uint32_t y = (w & 0x77777777u) + 0x77777777u;
+    return w & (y | 0x77777777u);
 }
 
 // Sign-magnitude nibbles -> two's complement (INT4): for a negative nibble
@@ -251,6 +251,251 @@ __device__ __forceinline__ uint2 round_sr16(const float z[16], float r0, float r
         out[1] = signmag_to_twos(out[1]);
     }
     return make_uint2(out[0], out[1]);
+}
+
+}  // namespace ufp4
+
+// ======================================================================
+// Paired-lane helpers (sm_100+ add/sub/mul.rn.f32x2: two independent IEEE
+// binary32 operations, round to nearest even, per instruction).
+namespace ufp4 {
+
+__device__ __forceinline__ uint64_t pk2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void up2(uint64_t v, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
+// Sign masks of a 16-element chunk: bit j of sgn set <=> eps_j = -1.
+struct SignMasks {
+    uint32_t lo[8], hi[8];  // 0 or 0x80000000 for elements 2k and 2k+1
+};
+__device__ __forceinline__ void make_masks(uint32_t sgn, SignMasks& m) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        m.lo[k] = ((sgn >> (2 * k)) & 1u) << 31;
+        m.hi[k] = ((sgn >> (2 * k + 1)) & 1u) << 31;
+    }
+}
+
+// 8 words of bf16 pairs -> 8 packed fp32 pairs with the RHT signs: the low
+// bf16 of a word becomes w * 65536 (+ 2^31 flips the sign bit exactly like
+// an xor, because the low 16 bits are zero), the high one w & 0xffff0000.
+__device__ __forceinline__ void widen16_x2(const uint32_t w[8], const SignMasks& m, uint64_t v[8]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t lo = w[k] * 65536u + m.lo[k];
+        const uint32_t hi = (w[k] & 0xFFFF0000u) ^ m.hi[k];
+        v[k] = pk2(__uint_as_float(lo), __uint_as_float(hi));
+    }
+}
+
+// Sylvester FWHT on a chunk held as 8 pairs (2k, 2k+1): stride 1 inside each
+// pair (scalar add/sub), strides 2, 4, 8 between pairs k and k + h/2
+// (paired adds), strides 16..n/2 with the lane holding the chunk h/16 away.
+// Same operations, in the same order, as the scalar butterfly.
+__device__ __forceinline__ void fwht16_x2(uint64_t v[8], int n, int seg_lane) {
+    if (n > 1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            float a, b;
+            up2(v[k], a, b);
+            v[k] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+    }
+#pragma unroll
+    for (int hp = 1; hp < 8; hp <<= 1) {  // pair stride hp <-> element stride 2*hp
+        if (2 * hp < n) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (k & hp) continue;
+                const uint64_t a = v[k], b = v[k + hp];
+                v[k] = add2(a, b);
+                v[k + hp] = sub2(a, b);
+            }
+        }
+    }
+    for (int h = kChunk; h < n; h <<= 1) {
+        const int lm = h / kChunk;
+        const bool upper = (seg_lane & lm) != 0;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)v[k], lm);
+            v[k] = upper ? sub2(o, v[k]) : add2(v[k], o);
+        }
+    }
+}
+
+__device__ __forceinline__ float amax_pairs(const uint64_t v[8], int k0, int k1) {
+    float m = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        if (k < k0 || k >= k1) continue;
+        float a, b;
+        up2(v[k], a, b);
+        m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
+    }
+    return m;
+}
+
+__device__ __forceinline__ float pow2_exact(int e) {  // 2^e, e in [-149, 127]
+    if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
+    return __uint_as_float(1u << (e + 149));
+}
+
+// Four e4m3 conversions packed into one word of bytes.
+__device__ __forceinline__ uint32_t cvt_e4m3x4(float b0, float b1, float b2, float b3) {
+    uint32_t r;
+    asm("{ .reg .b16 lo, hi;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n"
+        "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n"
+        "mov.b32 %0, {lo, hi}; }"
+        : "=r"(r)
+        : "f"(b0), "f"(b1), "f"(b2), "f"(b3));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float t0, float t1, float t2, float t3, float t4, float t5,
+                                               float t6, float t7) {
+    uint32_t r;
+    asm("{ .reg .b8 b0, b1, b2, b3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n"
+        "mov.b32 %0, {b0, b1, b2, b3}; }"
+        : "=r"(r)
+        : "f"(t0), "f"(t1), "f"(t2), "f"(t3), "f"(t4), "f"(t5), "f"(t6), "f"(t7));
+    return r;
+}
+
+// RTNE of 8 scaled values (already multiplied by the folded reciprocal) to one
+// word of packed sign-magnitude codes.  Uniform grids: the values are k * 2^-9
+// with |k| <= 7 exactly on e4m3's subnormals, so an e4m3 conversion rounds to
+// nearest with ties to even k; the even-indexed elements land in word E and
+// the odd ones in word O, and each byte of E | O becomes one packed byte.
+template <int GRID>
+__device__ __forceinline__ uint32_t rtne8(float t0, float t1, float t2, float t3, float t4, float t5, float t6,
+                                          float t7) {
+    uint32_t w;
+    if (GRID == 2) {
+        w = cvt_e2m1x8(t0, t1, t2, t3, t4, t5, t6, t7);
+    } else {
+        const uint32_t E = cvt_e4m3x4(t0, t2, t4, t6);  // bytes: s000 0kkk
+        const uint32_t O = cvt_e4m3x4(t1, t3, t5, t7);
+        w = ((E | (E >> 4)) & 0x0F0F0F0Fu) | ((O | (O << 4)) & 0xF0F0F0F0u);
+    }
+    w = clear_negative_zero(w);
+    if (GRID == 1) w = signmag_to_twos(w);
+    return w;
+}
+
+}  // namespace ufp4
+
+// ======================================================================
+// Two independent 16-element vectors a and b carried together: e[i] holds
+// (a_i, b_i) in one 64-bit register pair, so every butterfly stage, the
+// 1/sqrt(n) multiply and the scaling are paired fp32 operations.
+namespace ufp4 {
+
+struct Dest {
+    uint8_t* codes;    // 8 bytes of packed codes
+    uint8_t* s0;       // scale of elements 0..7 (byte address)
+    uint8_t* s1;       // scale of elements 8..15
+    bool valid, w0, w1;
+    uint64_t lin0;     // SR: linear index of element 0 in the output tensor
+};
+
+// Rows: two chunks (8 words each) sharing the same sign masks.
+__device__ __forceinline__ void widen_rows(const uint32_t wa[8], const uint32_t wb[8], const SignMasks& m,
+                                           uint64_t e[16]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        e[2 * k] = pk2(__uint_as_float(wa[k] * 65536u + m.lo[k]), __uint_as_float(wb[k] * 65536u + m.lo[k]));
+        e[2 * k + 1] = pk2(__uint_as_float((wa[k] & 0xFFFF0000u) ^ m.hi[k]),
+                           __uint_as_float((wb[k] & 0xFFFF0000u) ^ m.hi[k]));
+    }
+}
+
+// Columns: word g[i] holds row i of column a (low half) and column b (high half).
+__device__ __forceinline__ void widen_cols(const uint32_t g[16], const SignMasks& m, uint64_t e[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t mi = (i & 1) ? m.hi[i >> 1] : m.lo[i >> 1];
+        e[i] = pk2(__uint_as_float(g[i] * 65536u + mi), __uint_as_float((g[i] & 0xFFFF0000u) ^ mi));
+    }
+}
+
+// Sylvester butterfly, strides 1, 2, ..., n/2 in that order (strides >= 16
+// with the lane holding the chunk h/16 away).
+__device__ __forceinline__ void fwht_pair(uint64_t e[16], int n, int seg_lane) {
+#pragma unroll
+    for (int h = 1; h < kChunk; h <<= 1) {
+        if (h < n) {
+#pragma unroll
+            for (int i = 0; i < kChunk; ++i) {
+                if (i & h) continue;
+                const uint64_t a = e[i], b = e[i + h];
+                e[i] = add2(a, b);
+                e[i + h] = sub2(a, b);
+            }
+        }
+    }
+    for (int h = kChunk; h < n; h <<= 1) {
+        const int lm = h / kChunk;
+        const bool upper = (seg_lane & lm) != 0;
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)e[i], lm);
+            e[i] = upper ? sub2(o, e[i]) : add2(e[i], o);
+        }
+    }
+}
+
+// max(|x|, |y|) with the xor of the signs: the magnitude is what a block
+// amax needs, and chained calls keep it, so |.| is taken once at the end.
+__device__ __forceinline__ float maxabs(float x, float y) {
+    float r;
+    asm("max.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(y));
+    return r;
+}
+
+// Tree amax of |a_i| and |b_i| over i in [lo, hi) (lo, hi multiples of 8).
+__device__ __forceinline__ void amax_pair(const uint64_t e[16], int lo, int hi, float& ma, float& mb) {
+    float ta[16], tb[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) up2(e[i], ta[i], tb[i]);
+    float ra = 0.0f, rb = 0.0f;
+#pragma unroll
+    for (int h8 = 0; h8 < 16; h8 += 8) {
+        if (h8 < lo || h8 >= hi) continue;
+        const float a01 = maxabs(ta[h8 + 0], ta[h8 + 1]), a23 = maxabs(ta[h8 + 2], ta[h8 + 3]);
+        const float a45 = maxabs(ta[h8 + 4], ta[h8 + 5]), a67 = maxabs(ta[h8 + 6], ta[h8 + 7]);
+        const float b01 = maxabs(tb[h8 + 0], tb[h8 + 1]), b23 = maxabs(tb[h8 + 2], tb[h8 + 3]);
+        const float b45 = maxabs(tb[h8 + 4], tb[h8 + 5]), b67 = maxabs(tb[h8 + 6], tb[h8 + 7]);
+        ra = maxabs(ra, maxabs(maxabs(a01, a23), maxabs(a45, a67)));
+        rb = maxabs(rb, maxabs(maxabs(b01, b23), maxabs(b45, b67)));
+    }
+    ma = fabsf(ra);
+    mb = fabsf(rb);
 }
 
 }  // namespace ufp4
