@@ -13,12 +13,14 @@
 //    hardware scale is max(e0, e1) and the elements of the smaller block are
 //    shifted down by the difference d (exact for d <= 16 in E5M2).
 //
-// Kernel: one CTA per 128 x BN output tile, 8 warps.  Warp 0 lane 0 drives
-// TMA (128B-swizzled 2-D tiles of A and B, 512-byte scale chunks) through a
-// ring of mbarriers; warp 1 lane 0 copies the scales into tensor memory
-// (tcgen05.cp) and issues the MMAs (tcgen05.mma, accumulator in TMEM);
-// warps 4..7 read the accumulator back (tcgen05.ld) and store fp32.  Every
-// wait is bounded: on expiry the kernel records an error code and returns.
+// Kernel: persistent, one CTA (8 warps) per SM walking 128 x BN output tiles.
+// Warp 0 lane 0 drives TMA (128B-swizzled 2-D tiles of A and B, 512-byte
+// scale chunks) through a ring of mbarriers; warp 1 lane 0 copies the scales
+// into tensor memory (tcgen05.cp) and issues the MMAs (tcgen05.mma) into one
+// of two tensor-memory accumulators; warps 4..7 read the other accumulator
+// back (tcgen05.ld) and store fp32, so a tile's epilogue overlaps the next
+// tile's main loop.  Every wait is bounded: on expiry the kernel records an
+// error code, lets its copies and MMAs finish and returns.
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -54,6 +56,10 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 // Bounded wait on an mbarrier phase.  Returns false (and records the error)
 // when the limit is reached.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
@@ -70,11 +76,40 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
     return false;
 }
 
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+// L2 policies: operand tiles are re-read by many CTAs (keep them), the fp32
+// output is written once (let it leave first).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar,
+                                            uint64_t pol) {
     asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-        ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar)
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(bar), "l"(pol)
         : "memory");
+}
+
+__device__ __forceinline__ void st_out4(float* dst, const uint32_t* r, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;"
+                 ::"l"(dst), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "l"(pol)
+                 : "memory");
+}
+
+// 32-byte store: one whole L2 sector per instruction (needs a 32-byte aligned address).
+__device__ __forceinline__ void st_out8(float* dst, const uint32_t* r, uint64_t pol) {
+    asm volatile("st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+                 ::"l"(dst), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                   "r"(r[7]), "l"(pol)
+                 : "memory");
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
@@ -169,36 +204,41 @@ __host__ __device__ constexpr uint32_t make_idesc(int afmt, int bfmt, int M, int
 template <int KIND, int BN, int STAGES>
 struct GemmCfg {
     static constexpr int kChunksPerStage = KIND == 0 ? 1 : (KIND == 1 ? 2 : 4);
-    static constexpr int kABytes = kBM * kBKBytes;    // 16 KB, multiple of 1024
-    static constexpr int kBBytes = BN * kBKBytes;     // 32 KB
+    static constexpr int kHalvesB = (BN + 127) / 128;  // 128-row chunk blocks per B tile
+    static constexpr int kABytes = kBM * kBKBytes;      // 16 KB, multiple of 1024
+    static constexpr int kBBytes = BN * kBKBytes;       // multiple of 1024
     static constexpr int kSfaBytes = kChunksPerStage * kChunkBytes;
-    static constexpr int kSfbBytes = (BN / 128) * kChunksPerStage * kChunkBytes;
+    static constexpr int kSfbBytes = kHalvesB * kChunksPerStage * kChunkBytes;
     static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes landing per stage
     // shared memory: [A x STAGES][B x STAGES][SFA x STAGES][SFB x STAGES][barriers, flags]
     static constexpr int kOffB = STAGES * kABytes;
     static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
     static constexpr int kOffSfb = kOffSfa + STAGES * kSfaBytes;
     static constexpr int kOffBars = kOffSfb + STAGES * kSfbBytes;
-    static constexpr int kSmem = kOffBars + 8 * (2 * STAGES + 1) + 16 + 1024 /*alignment slack*/;
-    // tensor memory: accumulator (BN fp32 columns) then the scale rings;
-    // one 512-byte chunk occupies 4 columns (32 lanes, replicated 4x).
-    static constexpr int kSfaColsPerStage = kChunksPerStage * 4;
-    static constexpr int kSfbColsPerStage = kChunksPerStage * 4 * (BN / 128);
+    static constexpr int kNumBars = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
+    static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024 /*alignment slack*/;
+    // tensor memory: two accumulators of BN fp32 columns, then two sets of
+    // scale columns (one 512-byte chunk = 4 columns, replicated over the 4
+    // lane quadrants); k-tiles alternate between the sets
+    static constexpr int kSfaCols = kChunksPerStage * 4;
+    static constexpr int kSfbCols = kChunksPerStage * 4 * kHalvesB;
     static constexpr int kTmemCols = 512;
-    static constexpr int kAccCol = 0;
-    static constexpr int kSfaCol = BN;
-    static constexpr int kSfbCol = BN + STAGES * kSfaColsPerStage;
-    static_assert(kSfbCol + STAGES * kSfbColsPerStage <= kTmemCols, "tensor memory overflow");
+    static constexpr int kSfaCol = 2 * BN;
+    static __device__ __forceinline__ int kAccCol(int buf) { return buf * BN; }
+    static constexpr int kSfbCol = 2 * BN + 2 * kSfaCols;
+    static_assert(kSfbCol + 2 * kSfbCols <= kTmemCols, "tensor memory overflow");
     static_assert(kSmem <= 232448, "shared memory overflow");
+    static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
 };
 
 struct GemmKParams {
     const uint8_t* sfa;  // scale chunks of A: [ceil(M/128)][k chunks] x 512 B
-    const uint8_t* sfb;
+    const uint8_t* sfb;  // scale chunks of B: [ceil(N/BN) * halves][k chunks] x 512 B
     int64_t sf_chunks_k;  // chunks along K per 128-row block
-    int M, N, k_tiles;
+    int M, N, k_tiles, m_tiles, n_tiles;
     float* D;
     int64_t ldd;
+    int vec8;           // D and ldd allow 32-byte stores
     uint32_t idesc[4];  // per MMA within a stage (scale ids)
 };
 
@@ -214,9 +254,11 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     const uint32_t bars = base + C::kOffBars;
     auto full_bar = [&](int s) { return bars + 8u * s; };
     auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
-    const uint32_t acc_bar = bars + 8u * (2 * STAGES);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * (2 * STAGES + 1));
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * (2 * STAGES + 1) + 4);
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * C::kNumBars + 4);
 
     auto stage_a = [&](int s) { return base + s * C::kABytes; };
     auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
@@ -225,15 +267,18 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int m0 = blockIdx.y * kBM;
-    const int n0 = blockIdx.x * BN;
+    const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        mbar_init(acc_bar, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);
+            mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
+        }
+        mbar_init(drain_bar, 1);
         *abort_flag = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -249,88 +294,115 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- TMA producer
-        const uint8_t* sfa_blk = p.sfa + (int64_t)blockIdx.y * p.sf_chunks_k * kChunkBytes;
-        int issued = 0;
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-            const int s = kt % STAGES;
-            if (kt >= STAGES && !mbar_wait(empty_bar(s), ((kt / STAGES) - 1) & 1)) {
-                *abort_flag = 1;
-                break;
+        int it = 0;
+        const uint64_t keep = policy_evict_last();
+        for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+            const uint8_t* sfa_blk = p.sfa + (int64_t)mb * p.sf_chunks_k * kChunkBytes;
+            for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(empty_bar(s), ((it / STAGES) & 1) ^ 1)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_expect_tx(full_bar(s), C::kTxBytes);
+                tma_load_2d(stage_a(s), &tmap_a, kt * kBKBytes, mb * kBM, full_bar(s), keep);
+                tma_load_2d(stage_b(s), &tmap_b, kt * kBKBytes, nb * BN, full_bar(s), keep);
+                bulk_load(stage_sfa(s), sfa_blk + (int64_t)kt * C::kSfaBytes, C::kSfaBytes, full_bar(s));
+                for (int h = 0; h < C::kHalvesB; ++h) {
+                    const uint8_t* src = p.sfb + ((int64_t)(nb * C::kHalvesB + h) * p.sf_chunks_k +
+                                                  (int64_t)kt * C::kChunksPerStage) * kChunkBytes;
+                    bulk_load(stage_sfb(s) + h * C::kChunksPerStage * kChunkBytes, src,
+                              C::kChunksPerStage * kChunkBytes, full_bar(s));
+                }
             }
-            if (*abort_flag) break;
-            mbar_expect_tx(full_bar(s), C::kTxBytes);
-            tma_load_2d(stage_a(s), &tmap_a, kt * kBKBytes, m0, full_bar(s));
-            tma_load_2d(stage_b(s), &tmap_b, kt * kBKBytes, n0, full_bar(s));
-            bulk_load(stage_sfa(s), sfa_blk + (int64_t)kt * C::kSfaBytes, C::kSfaBytes, full_bar(s));
-            for (int h = 0; h < BN / 128; ++h) {
-                const uint8_t* src =
-                    p.sfb + ((int64_t)(n0 / 128 + h) * p.sf_chunks_k + (int64_t)kt * C::kChunksPerStage) * kChunkBytes;
-                bulk_load(stage_sfb(s) + h * C::kChunksPerStage * kChunkBytes, src, C::kChunksPerStage * kChunkBytes,
-                          full_bar(s));
-            }
-            issued = kt + 1;
         }
         if (*abort_flag) {
-            // let the copies already issued land before the CTA leaves (bounded)
-            for (int kt = issued > STAGES ? issued - STAGES : 0; kt < issued; ++kt)
-                mbar_wait(full_bar(kt % STAGES), (kt / STAGES) & 1);
+            // let every issued copy land before the CTA leaves (bounded)
+            for (int k = it > STAGES ? it - STAGES : 0; k < it; ++k) mbar_wait(full_bar(k % STAGES), (k / STAGES) & 1);
         }
     } else if (warp == 1 && lane == 0) {
         // ----------------------------------------------------- MMA issuer
-        for (int kt = 0; kt < p.k_tiles; ++kt) {
-            const int s = kt % STAGES;
-            if (!mbar_wait(full_bar(s), (kt / STAGES) & 1)) {
-                *abort_flag = 1;
+        int it = 0, tc = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tc) {
+            const int buf = tc & 1;
+            if (!mbar_wait(acce_bar(buf), ((tc >> 1) & 1) ^ 1)) {
+                ok = false;
                 break;
             }
-            if (*abort_flag) break;
             tc_fence_after();
-            const uint32_t sfa_t = tmem + C::kSfaCol + s * C::kSfaColsPerStage;
-            const uint32_t sfb_t = tmem + C::kSfbCol + s * C::kSfbColsPerStage;
-            // chunk c of A -> columns 4c; chunk c of B's row half h -> columns 4(c*(BN/128) + h)
-            for (int c = 0; c < C::kChunksPerStage; ++c)
-                tc_cp_scales(sfa_t + 4 * c, plain_desc(stage_sfa(s) + c * kChunkBytes));
-            for (int h = 0; h < BN / 128; ++h)
+            const uint32_t acc = tmem + C::kAccCol(buf);
+            for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
+                const int s = it % STAGES;
+                if (!mbar_wait(full_bar(s), (it / STAGES) & 1) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int set = it & 1;
+                const uint32_t sfa_t = tmem + C::kSfaCol + set * C::kSfaCols;
+                const uint32_t sfb_t = tmem + C::kSfbCol + set * C::kSfbCols;
+                // chunk c of A -> columns 4c; chunk c of B's half h -> columns 4(c*halves + h)
                 for (int c = 0; c < C::kChunksPerStage; ++c)
-                    tc_cp_scales(sfb_t + 4 * (c * (BN / 128) + h),
-                                 plain_desc(stage_sfb(s) + (h * C::kChunksPerStage + c) * kChunkBytes));
-            const uint64_t da = sw128_desc(stage_a(s));
-            const uint64_t db = sw128_desc(stage_b(s));
+                    tc_cp_scales(sfa_t + 4 * c, plain_desc(stage_sfa(s) + c * kChunkBytes));
+                for (int h = 0; h < C::kHalvesB; ++h)
+                    for (int c = 0; c < C::kChunksPerStage; ++c)
+                        tc_cp_scales(sfb_t + 4 * (c * C::kHalvesB + h),
+                                     plain_desc(stage_sfb(s) + (h * C::kChunksPerStage + c) * kChunkBytes));
+                const uint64_t da = sw128_desc(stage_a(s));
+                const uint64_t db = sw128_desc(stage_b(s));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                // chunk holding MMA j's scales: FP8 1X -> 0 (byte j), FP4 2X -> j/2 (bytes 0-1 / 2-3), FP4 4X -> j
-                const int chunk = KIND == 0 ? 0 : (KIND == 1 ? j / 2 : j);
-                // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
-                mma<KIND>(tmem + C::kAccCol, da + 2 * j, db + 2 * j, p.idesc[j], sfa_t + 4 * chunk,
-                          sfb_t + 4 * chunk * (BN / 128), (kt > 0 || j > 0) ? 1u : 0u);
+                for (int j = 0; j < 4; ++j) {
+                    // chunk holding MMA j's scales: FP8 1X -> 0 (byte j), FP4 2X -> j/2 (bytes 0-1 / 2-3), FP4 4X -> j
+                    const int chunk = KIND == 0 ? 0 : (KIND == 1 ? j / 2 : j);
+                    // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
+                    mma<KIND>(acc, da + 2 * j, db + 2 * j, p.idesc[j], sfa_t + 4 * chunk,
+                              sfb_t + 4 * chunk * C::kHalvesB, (kt > 0 || j > 0) ? 1u : 0u);
+                }
+                tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
             }
-            tc_commit(empty_bar(s));
+            if (ok) tc_commit(accf_bar(buf));  // the accumulator is complete once every MMA above is
         }
-        tc_commit(acc_bar);  // arrives once every MMA issued above has completed
+        if (!ok) *abort_flag = 1;
+        tc_commit(drain_bar);  // arrives when every MMA issued by this thread has completed
+        mbar_wait(drain_bar, 0);
     } else if (warp >= 4) {
         // ------------------------------------------------------- epilogue
-        const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(acc_bar, 0));  // warp-uniform before .sync.aligned loads
-        tc_fence_after();
-        if (ok && !*abort_flag) {
-            const int q = warp - 4;  // TMEM lane quadrant of this warp
-            const int row = m0 + q * 32 + lane;
+        const int q = warp - 4;  // TMEM lane quadrant of this warp
+        const uint64_t stream_out = policy_evict_first();
+        int tc = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
+            const int buf = tc & 1;
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), (tc >> 1) & 1));
+            if (!ok || *abort_flag) break;
+            tc_fence_after();
+            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+            const int row = mb * kBM + q * 32 + lane;
+            const int n0 = nb * BN;
             for (int c = 0; c < BN; c += 32) {
                 uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol + c, r);
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol(buf) + c, r);
                 if (row < p.M) {
                     float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
                     if (n0 + c + 32 <= p.N) {
+                        if (p.vec8) {
 #pragma unroll
-                        for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4*>(dst + i) = make_float4(
-                                __uint_as_float(r[i]), __uint_as_float(r[i + 1]), __uint_as_float(r[i + 2]),
-                                __uint_as_float(r[i + 3]));
+                            for (int i = 0; i < 32; i += 8) st_out8(dst + i, r + i, stream_out);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) st_out4(dst + i, r + i, stream_out);
+                        }
                     } else {
                         for (int i = 0; i < 32; ++i)
                             if (n0 + c + i < p.N) dst[i] = __uint_as_float(r[i]);
                     }
                 }
             }
+            // the accumulator has been read: hand it back to the MMA issuer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(acce_bar(buf));
         }
     }
     tc_fence_before();
@@ -350,10 +422,6 @@ __device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
     return r;
 }
 
-__device__ __forceinline__ int signed_level(int grid, uint32_t nib) {
-    if (grid == 1) return (nib & 8u) ? (int)nib - 16 : (int)nib;
-    return (nib & 8u) ? -(int)(nib & 7u) : (int)(nib & 7u);
-}
 
 __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-149, 127]
     if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
@@ -371,10 +439,19 @@ struct PrepParams {
     int64_t chunks_k;
     int hw_block;          // 16 (E2M1 1x16) or 32
     int64_t rows_cover;    // chunk rows written: rows rounded up to the GEMM tile
+    int tile_rows;         // rows of one GEMM tile of this operand (128 for A, BN for B)
 };
 
-__device__ __forceinline__ int64_t chunk_offset(int64_t row, int64_t cell, int64_t chunks_k) {
-    return ((row / 128) * chunks_k + cell) * kChunkBytes + (row % 32) * 16 + ((row % 128) / 32) * 4;
+// Scale chunks are grouped per GEMM tile: tile t = row / tile_rows holds
+// ceil(tile_rows / 128) blocks of 128 rows; inside a block, row w and scale
+// cell j sit at (w % 32) * 16 + (w / 32) * 4 + j (the tcgen05.cp 32x128b layout).
+__device__ __forceinline__ int64_t chunk_offset(const PrepParams& p, int64_t row, int64_t cell) {
+    const int halves = (p.tile_rows + 127) / 128;
+    const int64_t t = row / p.tile_rows;
+    const int64_t rr = row - t * p.tile_rows;
+    const int64_t cb = t * halves + rr / 128;
+    const int64_t w = rr % 128;
+    return (cb * p.chunks_k + cell) * kChunkBytes + (w % 32) * 16 + (w / 32) * 4;
 }
 
 __device__ __forceinline__ int src_scale(const PrepParams& p, int64_t row, int64_t k_elem) {
@@ -382,45 +459,83 @@ __device__ __forceinline__ int src_scale(const PrepParams& p, int64_t row, int64
     return p.scales[(row / p.br) * p.scales_ld + k_elem / p.bc];
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t r;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+    return r;
+}
+
+// Four sign-magnitude codes (16 bits) -> four E5M2 bytes of k * 2^-d, d <= 14:
+// the magnitudes 0..7 index the E5M2 bytes of 0, 1, 2, ..., 7 (byte permute),
+// the shift subtracts d from the exponent field of the nonzero bytes, and the
+// sign goes to bit 7.  Exact: every k * 2^-d with |k| <= 7, d <= 14 is an E5M2
+// normal number.
+__device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
+    const uint32_t mag = c16 & 0x7777u;
+    const uint32_t v = prmt(0x42403C00u, 0x47464544u, mag);  // 0, 1.0, 2.0, 3.0 | 4.0, 5.0, 6.0, 7.0
+    const uint32_t nz = prmt(0xFFFFFF00u, 0xFFFFFFFFu, mag);  // 0xff where k != 0
+    const uint32_t sg = prmt(0x00008000u, 0u, (c16 >> 3) & 0x1111u);
+    return (v - (sub4 & nz)) | sg;
+}
+
+// Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
+// elements.  One thread: one row, one 32-element group (16 code bytes in,
+// 32 FP8 bytes and one scale byte out); consecutive threads walk along K.
 __global__ void prep_widen_kernel(const PrepParams p) {
+    const int64_t groups = (p.K + 31) / 32;
+    const int64_t gpad = p.chunks_k * 4;  // groups covered by the chunk layout
     const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= p.rows_cover * p.chunks_k) return;
-    const int64_t row = idx / p.chunks_k;
-    const int64_t cell = idx % p.chunks_k;  // 4 scale bytes = 128 K elements
-    uint32_t cellv = 0;
+    if (idx >= p.rows_cover * gpad) return;
+    const int64_t row = idx / gpad;
+    const int64_t grp = idx - row * gpad;
+    const int64_t k0 = grp * 32;
     const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
-    for (int j = 0; j < 4; ++j) {
-        const int64_t k0 = cell * 128 + j * 32;
-        int hw = 0;
-        if (row < p.rows && k0 < p.K) {
-            int H = src_scale(p, row, k0);
-            if (p.bc == 16) H = max(H, src_scale(p, row, k0 + 16));
-            hw = max(H + step_log2, 0);
-            // 32 elements -> 32 bytes
-            uint32_t outw[8];
-            const uint8_t* cp = p.codes + row * p.codes_ld + k0 / 2;
-            const uint4 cw = *reinterpret_cast<const uint4*>(cp);
-            const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-            for (int h = 0; h < 2; ++h) {
-                const int e = (p.bc == 16) ? src_scale(p, row, k0 + 16 * h) : src_scale(p, row, k0);
-                const float mult = pow2f(e + step_log2 - hw);
-                for (int q = 0; q < 4; ++q) {
-                    const uint32_t w = words[2 * h + q / 2];
-                    const int sh = (q & 1) * 16;
-                    const float v0 = (float)signed_level(p.grid, (w >> sh) & 0xF) * mult;
-                    const float v1 = (float)signed_level(p.grid, (w >> (sh + 4)) & 0xF) * mult;
-                    const float v2 = (float)signed_level(p.grid, (w >> (sh + 8)) & 0xF) * mult;
-                    const float v3 = (float)signed_level(p.grid, (w >> (sh + 12)) & 0xF) * mult;
-                    outw[h * 4 + q] = cvt_e5m2x2(v1, v0) | (cvt_e5m2x2(v3, v2) << 16);
-                }
+    int hw = 0;
+    if (row < p.rows && grp < groups) {
+        const int e0 = src_scale(p, row, k0);
+        const int e1 = (p.bc == 16) ? src_scale(p, row, k0 + 16) : e0;
+        hw = max(max(e0, e1) + step_log2, 0);
+        const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
+        const uint4 cw = *reinterpret_cast<const uint4*>(p.codes + row * p.codes_ld + k0 / 2);
+        uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        if (p.grid == 1) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
+                const uint32_t w = words[q];
+                const uint32_t neg = (w >> 3) & 0x11111111u;
+                const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
+                words[q] = mag | (neg << 3);
             }
-            uint4* dst = reinterpret_cast<uint4*>(p.out_fp8 + row * p.K + k0);
-            dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-            dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
         }
-        cellv |= (uint32_t)hw << (8 * j);
+        uint32_t outw[8];
+        if (d0 <= 14 && d1 <= 14) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
+                outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
+            }
+        } else {
+            // shifts beyond E5M2's normal range: exact float path, rounding to
+            // nearest only below E5M2's smallest subnormal
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float mult = pow2f(-(q < 4 ? d0 : d1));
+                const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+                float v[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t nib = (w >> (4 * t)) & 0xFu;
+                    const float k = (float)(int)(nib & 7u);
+                    v[t] = ((nib & 8u) ? -k : k) * mult;
+                }
+                outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(p.out_fp8 + row * p.K + k0);
+        dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(row, cell, p.chunks_k)) = cellv;
+    p.out_chunks[chunk_offset(p, row, grp >> 2) + (grp & 3)] = (uint8_t)hw;
 }
 
 // E2M1: only the scales move, into the chunk layout (hw_block 16 or 32).
@@ -436,7 +551,7 @@ __global__ void prep_scales_kernel(const PrepParams p) {
         if (row < p.rows && k0 < p.K) b = src_scale(p, row, k0);
         cellv |= (uint32_t)b << (8 * j);
     }
-    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(row, cell, p.chunks_k)) = cellv;
+    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(p, row, cell)) = cellv;
 }
 
 // ------------------------------------------------------------ host side
@@ -465,6 +580,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes
 
 struct Plan {
     int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X
+    int bn;            // B tile rows (output tile columns)
     int64_t k_bytes;   // bytes of K per row in the MMA operand
     int64_t k_tiles;
     int64_t chunks_k;  // scale chunks along K per 128 rows (multiple of chunks per stage)
@@ -474,15 +590,22 @@ struct Plan {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+// Output tiles are 128 x 192: two accumulators and two scale sets fit in the
+// 512 tensor-memory columns, and a 5-stage ring (4 for FP4 with 16-element
+// scales) fits in shared memory.
+constexpr int kBnFp8 = 192, kBnFp4x2 = 192, kBnFp4x4 = 192;
+
 Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
     Plan pl{};
     (void)br;
     pl.kind = grid == 2 ? (bc == 16 ? 2 : 1) : 0;
+    pl.bn = pl.kind == 0 ? kBnFp8 : (pl.kind == 1 ? kBnFp4x2 : kBnFp4x4);
     pl.k_bytes = grid == 2 ? K / 2 : K;
     pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
     const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
     pl.chunks_k = pl.k_tiles * cps;
-    const int64_t mb = (M + 127) / 128, nb = (N + 255) / 256 * 2;  // B chunks cover the 256-row tile
+    const int64_t mb = (M + 127) / 128;
+    const int64_t nb = (N + pl.bn - 1) / pl.bn * ((pl.bn + 127) / 128);  // chunk blocks of B
     size_t off = 0;
     if (pl.kind == 0) {
         pl.fp8_a = off;
@@ -499,12 +622,14 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
 }
 
 template <int KIND, int BN, int STAGES>
-cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKParams& kp, cudaStream_t st) {
+cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKParams& kp, int num_sms,
+                     cudaStream_t st) {
     using C = GemmCfg<KIND, BN, STAGES>;
     auto k = gemm_kernel<KIND, BN, STAGES>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
-    dim3 grid((kp.N + BN - 1) / BN, (kp.M + kBM - 1) / kBM);
+    const int tiles = kp.m_tiles * kp.n_tiles;
+    const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
     k<<<grid, kGemmThreads, C::kSmem, st>>>(ma, mb, kp);
     return cudaGetLastError();
 }
@@ -528,7 +653,6 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, i
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
-    (void)num_sms;
     if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
     if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
@@ -551,9 +675,10 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
         pp.out_chunks = ws + (side ? pl.sfb : pl.sfa);
         pp.chunks_k = pl.chunks_k;
         pp.hw_block = pl.kind == 2 ? 16 : 32;
-        // chunk rows cover whole output tiles (128 rows for A, 256 for B)
-        pp.rows_cover = side ? ((op.rows + 255) / 256) * 256 : ((op.rows + 127) / 128) * 128;
-        const int64_t threads = pp.rows_cover * pl.chunks_k;
+        pp.tile_rows = side ? pl.bn : kBM;
+        // chunk rows cover whole output tiles
+        pp.rows_cover = ((op.rows + pp.tile_rows - 1) / pp.tile_rows) * pp.tile_rows;
+        const int64_t threads = pp.rows_cover * pl.chunks_k * (pl.kind == 0 ? 4 : 1);
         const int tb = 256;
         const unsigned blocks = (unsigned)((threads + tb - 1) / tb);
         if (pl.kind == 0) prep_widen_kernel<<<blocks, tb, 0, st>>>(pp);
@@ -566,9 +691,8 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
     const void* b_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
     const int64_t a_pitch = pl.kind == 0 ? g.K : g.a.codes_ld;
     const int64_t b_pitch = pl.kind == 0 ? g.K : g.b.codes_ld;
-    constexpr int BN = 256;
     if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, BN)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn)) return cudaErrorInvalidValue;
     GemmKParams kp{};
     kp.sfa = ws + pl.sfa;
     kp.sfb = ws + pl.sfb;
@@ -576,18 +700,21 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
     kp.M = (int)g.M;
     kp.N = (int)g.N;
     kp.k_tiles = (int)pl.k_tiles;
+    kp.m_tiles = (int)((g.M + kBM - 1) / kBM);
+    kp.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
     kp.D = g.D;
     kp.ldd = g.ldd;
+    kp.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
     if (pl.kind == 0) {
-        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, j);  // E5M2 x E5M2
-        return run_gemm<0, BN, 4>(ma, mb, kp, st);
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp8, j);  // E5M2 x E5M2
+        return run_gemm<0, kBnFp8, 5>(ma, mb, kp, num_sms, st);
     }
     if (pl.kind == 1) {
-        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, (j % 2) * 2);  // E2M1
-        return run_gemm<1, BN, 4>(ma, mb, kp, st);
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x2, (j % 2) * 2);  // E2M1
+        return run_gemm<1, kBnFp4x2, 5>(ma, mb, kp, num_sms, st);
     }
-    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, BN, 0);
-    return run_gemm<2, BN, 3>(ma, mb, kp, st);
+    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x4, 0);
+    return run_gemm<2, kBnFp4x4, 4>(ma, mb, kp, num_sms, st);
 }
 
 }  // namespace ufp4
