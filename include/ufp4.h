@@ -163,8 +163,9 @@ ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t
  *                 own rows; SR draws use the group's id and the row index
  *                 within the group
  *   colwise       the column-wise quantization of each group, stacked: group g
- *                 has padded length P_g = round_up(c_g, lcm(n, block width))
- *                 (missing rows read as zero), and occupies a cols x P_g
+ *                 has padded length P_g = round_up(c_g, max(n, block width, 64))
+ *                 (missing rows read as zero; 64 makes P_g a valid GEMM K for
+ *                 WGRAD), and occupies a cols x P_g
  *                 row-major matrix starting at codes + cols * (Poff_g / 2)
  *                 bytes and scales + cols * Poff_g / block_width elements,
  *                 Poff_g = P_0 + ... + P_{g-1}; its qtensor has rows = cols
@@ -215,6 +216,31 @@ ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4
 ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
                       float* D, int64_t ldd, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
+
+/* ufp4_gemm_grouped_workspace_size -- scratch bytes ufp4_gemm_grouped needs:
+ * the largest ufp4_gemm_workspace_size over the groups (A, B: HOST arrays of
+ * num_groups qtensors). */
+ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
+                                             const ufp4_quant_desc* desc, size_t* bytes);
+
+/* ufp4_gemm_grouped -- the quantized GEMM over a set of independent groups
+ * (MoE experts) [UFP4-method: the same quantized GEMM on every expert's
+ * linear layer]: D_g = Q(A_g) Q(B_g)^T for g = 0 .. num_groups-1, each group
+ * with its own shapes, as in ufp4_gemm.
+ *   A, B   HOST arrays of num_groups qtensors describing device buffers.  The
+ *          grouped quantizer's outputs slot in directly: FPROP uses the
+ *          row-wise X slab of expert g and W_g; DGRAD the row-wise dY slab and
+ *          W_g column-wise; WGRAD the column-wise dY_g and X_g (K = P_g, the
+ *          padded token count).
+ *   D, ldd HOST arrays of num_groups device output pointers and leading
+ *          dimensions.
+ *   workspace  device scratch of at least ufp4_gemm_grouped_workspace_size
+ *          bytes; the groups run one after another on `stream` and share it.
+ * A group with no rows (M_g = 0 or N_g = 0) is skipped; a group with K_g = 0
+ * writes D_g = 0.  Every group is checked before anything is launched. */
+ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
+                              const ufp4_quant_desc* desc, float* const* D, const int64_t* ldd, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream);
 
 /* Size of the fixed device scratch behind ufp4_gemm_noalloc: 32 MiB. */
 #define UFP4_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)

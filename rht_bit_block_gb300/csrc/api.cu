@@ -3,6 +3,7 @@
 // allocates device memory and no host state survives a call.
 #include <algorithm>
 #include <cmath>
+#include <new>
 #include <cstdint>
 #include <cstring>
 #include <cuda_runtime.h>
@@ -128,7 +129,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if (cols % 16) return UFP4_ERR_INVALID_ARG;
     if (do_row && (cols % n || cols % bs.bw)) return UFP4_ERR_INVALID_ARG;
     if (bs.is2d && (total_rows % bs.b2d || cols % bs.b2d)) return UFP4_ERR_INVALID_ARG;
-    const int64_t unit = grouped ? (int64_t)std::max<int>(std::max(n, bs.bw), 16) : 1;
+    const int64_t unit = grouped ? (int64_t)std::max<int>(std::max(n, bs.bw), 64) : 1;
     int64_t padded_total = 0;
     int64_t pad0[kMaxGroups + 1];
     pad0[0] = 0;
@@ -208,6 +209,56 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
                                        num_sms_current(), stream));
 }
 
+// Checks one GEMM call and fills its launch arguments (nothing is launched).
+ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
+                         int64_t ldd, void* workspace, size_t workspace_bytes, GemmArgs* out) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!A || !B) return UFP4_ERR_INVALID_ARG;
+    if (desc->scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_UNSUPPORTED;
+    if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
+    if (M > 0 && N > 0 && !D) return UFP4_ERR_INVALID_ARG;
+    if (K % 32 && !(bs.bw == 16 && K % 16 == 0)) return UFP4_ERR_INVALID_ARG;
+    std::memset(out, 0, sizeof(*out));
+    out->M = M;
+    out->N = N;
+    out->K = K;
+    out->D = D;
+    out->ldd = ldd;
+    if (M == 0 || N == 0) return UFP4_OK;  // nothing to compute
+    if (!aligned(D, 16) || ldd % 4) return UFP4_ERR_ALIGNMENT;
+    if (K == 0) return UFP4_OK;  // D = 0 (written by run_prepared_gemm)
+    st = check_out(A, M, K, bs, UFP4_SCALE_UE8M0, false);
+    if (st != UFP4_OK) return st;
+    st = check_out(B, N, K, bs, UFP4_SCALE_UE8M0, false);
+    if (st != UFP4_OK) return st;
+    if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
+    const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
+    if (workspace_bytes < need || (need && !workspace)) return UFP4_ERR_INVALID_ARG;
+    if (workspace && !aligned(workspace, 256)) return UFP4_ERR_ALIGNMENT;
+    out->a = {(const uint8_t*)A->codes, (const uint8_t*)A->scales, M, A->codes_ld, A->scales_ld};
+    out->b = {(const uint8_t*)B->codes, (const uint8_t*)B->scales, N, B->codes_ld, B->scales_ld};
+    out->grid = desc->grid;
+    out->br = bs.is2d ? bs.b2d : 1;
+    out->bc = bs.bw;
+    out->workspace = workspace;
+    out->workspace_bytes = workspace_bytes;
+    return UFP4_OK;
+}
+
+ufp4_status run_prepared_gemm(const GemmArgs& g, cudaStream_t stream) {
+    if (g.M == 0 || g.N == 0) return UFP4_OK;
+    if (g.K == 0)  // an empty sum: D = 0
+        return cuda_status(cudaMemset2DAsync(g.D, (size_t)g.ldd * sizeof(float), 0, (size_t)g.N * sizeof(float),
+                                             (size_t)g.M, stream));
+    const cudaError_t e = launch_gemm(g, num_sms_current(), stream);
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
 }  // namespace
 
 extern "C" {
@@ -241,7 +292,7 @@ ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t
 int64_t ufp4_grouped_padded_rows(int64_t rows, const ufp4_quant_desc* desc) {
     if (!desc || rows < 0) return -1;
     int bw = desc->block_rows == 1 ? desc->block_cols : desc->block_rows;
-    const int64_t unit = std::max<int64_t>(std::max<int64_t>(desc->hadamard_n, bw), 16);
+    const int64_t unit = std::max<int64_t>(std::max<int64_t>(desc->hadamard_n, bw), 64);
     return ((rows + unit - 1) / unit) * unit;
 }
 
@@ -308,42 +359,45 @@ ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4
 
 ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
                       int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
-    BlockShape bs;
-    ufp4_status st = check_desc(desc, &bs);
-    if (st != UFP4_OK) return st;
-    if (!A || !B || !D) return UFP4_ERR_INVALID_ARG;
-    if (desc->scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_UNSUPPORTED;
-    if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
-    const int64_t M = A->rows, N = B->rows, K = A->cols;
-    if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
-    if (K % 32 && !(bs.bw == 16 && K % 16 == 0)) return UFP4_ERR_INVALID_ARG;
-    st = check_out(A, M, K, bs, UFP4_SCALE_UE8M0, false);
-    if (st != UFP4_OK) return st;
-    st = check_out(B, N, K, bs, UFP4_SCALE_UE8M0, false);
-    if (st != UFP4_OK) return st;
-    if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
-    if (!aligned(D, 16) || ldd % 4) return UFP4_ERR_ALIGNMENT;
-    const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
-    if (workspace_bytes < need || (need && !workspace)) return UFP4_ERR_INVALID_ARG;
-    if (workspace && !aligned(workspace, 256)) return UFP4_ERR_ALIGNMENT;
-    if (M == 0 || N == 0) return UFP4_OK;
     GemmArgs g;
-    std::memset(&g, 0, sizeof(g));
-    g.a = {(const uint8_t*)A->codes, (const uint8_t*)A->scales, M, A->codes_ld, A->scales_ld};
-    g.b = {(const uint8_t*)B->codes, (const uint8_t*)B->scales, N, B->codes_ld, B->scales_ld};
-    g.M = M;
-    g.N = N;
-    g.K = K;
-    g.grid = desc->grid;
-    g.br = bs.is2d ? bs.b2d : 1;
-    g.bc = bs.bw;
-    g.D = D;
-    g.ldd = ldd;
-    g.workspace = workspace;
-    g.workspace_bytes = workspace_bytes;
-    const cudaError_t e = launch_gemm(g, num_sms_current(), stream);
-    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
-    return cuda_status(e);
+    const ufp4_status st = prepare_gemm(A, B, desc, D, ldd, workspace, workspace_bytes, &g);
+    if (st != UFP4_OK) return st;
+    return run_prepared_gemm(g, stream);
+}
+
+ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
+                                             const ufp4_quant_desc* desc, size_t* bytes) {
+    if (num_groups < 0 || (num_groups && (!A || !B)) || !bytes) return UFP4_ERR_INVALID_ARG;
+    size_t need = 0;
+    for (int32_t i = 0; i < num_groups; ++i) {
+        size_t b = 0;
+        const ufp4_status st = ufp4_gemm_workspace_size(A[i].rows, B[i].rows, A[i].cols, desc, &b);
+        if (st != UFP4_OK) return st;
+        need = std::max(need, b);
+    }
+    *bytes = need;
+    return UFP4_OK;
+}
+
+ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
+                              const ufp4_quant_desc* desc, float* const* D, const int64_t* ldd, void* workspace,
+                              size_t workspace_bytes, cudaStream_t stream) {
+    if (num_groups < 0 || (num_groups && (!A || !B || !D || !ldd))) return UFP4_ERR_INVALID_ARG;
+    // every group is checked before anything is launched
+    GemmArgs* args = new (std::nothrow) GemmArgs[num_groups > 0 ? num_groups : 1];
+    if (!args) return UFP4_ERR_INVALID_ARG;
+    for (int32_t i = 0; i < num_groups; ++i) {
+        const ufp4_status st = prepare_gemm(&A[i], &B[i], desc, D[i], ldd[i], workspace, workspace_bytes, &args[i]);
+        if (st != UFP4_OK) {
+            delete[] args;
+            return st;
+        }
+    }
+    // the groups run one after another on the stream, so they share the workspace
+    ufp4_status st = UFP4_OK;
+    for (int32_t i = 0; i < num_groups && st == UFP4_OK; ++i) st = run_prepared_gemm(args[i], stream);
+    delete[] args;
+    return st;
 }
 
 }  // extern "C"

@@ -27,6 +27,7 @@ EXPORTED = (
     "ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_grouped_padded_rows",
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
+    "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped",
 )
 
 
@@ -70,13 +71,15 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_gemm_workspace_size.argtypes = [i64, i64, i64, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
     L.ufp4_gemm_noalloc.argtypes = [QT, QT, QD, P, i64, P]
+    L.ufp4_gemm_grouped_workspace_size.argtypes = [i32, QT, QT, QD, ctypes.POINTER(ctypes.c_size_t)]
+    L.ufp4_gemm_grouped.argtypes = [i32, QT, QT, QD, ctypes.POINTER(P), ctypes.POINTER(i64), P, ctypes.c_size_t, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
     L.ufp4_device_error.argtypes = [ctypes.POINTER(i32)]
     L.ufp4_status_string.argtypes = [ctypes.c_int]
     L.ufp4_status_string.restype = ctypes.c_char_p
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
                  "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error",
-                 "ufp4_gemm_noalloc"):
+                 "ufp4_gemm_noalloc", "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -154,6 +157,27 @@ def ufp4_gemm(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace=None, stream
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().ufp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(), D.stride(0),
                             ws_ptr, ws_bytes, _stream(stream)), "ufp4_gemm")
+
+
+def ufp4_gemm_grouped_workspace_size(A, B, desc: QuantDesc) -> int:
+    n = len(A)
+    arrA, arrB = (QTensor * max(n, 1))(*A), (QTensor * max(n, 1))(*B)
+    out = ctypes.c_size_t(0)
+    _check(load().ufp4_gemm_grouped_workspace_size(n, arrA, arrB, ctypes.byref(desc), ctypes.byref(out)),
+           "ufp4_gemm_grouped_workspace_size")
+    return int(out.value)
+
+
+def ufp4_gemm_grouped(A, B, desc: QuantDesc, D, workspace=None, stream=None):
+    """A, B: lists of QTensor; D: list of float32 CUDA tensors (one per group)."""
+    n = len(A)
+    arrA, arrB = (QTensor * max(n, 1))(*A), (QTensor * max(n, 1))(*B)
+    dptr = (ctypes.c_void_p * max(n, 1))(*[d.data_ptr() for d in D])
+    ldd = (ctypes.c_int64 * max(n, 1))(*[d.stride(0) if d.dim() == 2 else 1 for d in D])
+    ws_ptr = workspace.data_ptr() if workspace is not None else None
+    ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(load().ufp4_gemm_grouped(n, arrA, arrB, ctypes.byref(desc), dptr, ldd, ws_ptr, ws_bytes,
+                                    _stream(stream)), "ufp4_gemm_grouped")
 
 
 def ufp4_gemm_noalloc(A: QTensor, B: QTensor, desc: QuantDesc, D, stream=None):
