@@ -217,6 +217,19 @@ ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_q
                       float* D, int64_t ldd, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);
 
+/* ufp4_gemm_prepare / ufp4_gemm_prepared -- the two stages of ufp4_gemm,
+ * for callers that reuse prepared operands or time the stages apart.
+ * ufp4_gemm_prepare writes the tensor-core form of A and B into the workspace
+ * (E1M2/INT4: FP8 E5M2 copies with one UE8M0 scale per 32 elements; all
+ * grids: the scales in the tensor-memory copy layout).  ufp4_gemm_prepared
+ * then computes D from that workspace; it must get the same A, B (shapes and
+ * scales), desc and workspace as the ufp4_gemm_prepare call before it on the
+ * stream.  ufp4_gemm(...) == ufp4_gemm_prepare(...) + ufp4_gemm_prepared(...). */
+ufp4_status ufp4_gemm_prepare(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream);
+ufp4_status ufp4_gemm_prepared(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
+                               int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ufp4_gemm_grouped_workspace_size -- scratch bytes ufp4_gemm_grouped needs:
  * the largest ufp4_gemm_workspace_size over the groups (A, B: HOST arrays of
  * num_groups qtensors). */

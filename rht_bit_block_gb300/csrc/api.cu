@@ -365,6 +365,30 @@ ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_q
     return run_prepared_gemm(g, stream);
 }
 
+ufp4_status ufp4_gemm_prepare(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
+                              void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    GemmArgs g;
+    float dummy_d[4] __attribute__((aligned(16)));  // shape checks only; D is not touched here
+    const ufp4_status st = prepare_gemm(A, B, desc, dummy_d, B ? B->rows : 0, workspace, workspace_bytes, &g);
+    if (st != UFP4_OK) return st;
+    if (g.M == 0 || g.N == 0 || g.K == 0) return UFP4_OK;
+    const cudaError_t e = launch_gemm_prep(g, stream);
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
+ufp4_status ufp4_gemm_prepared(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
+                               int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    GemmArgs g;
+    const ufp4_status st = prepare_gemm(A, B, desc, D, ldd, workspace, workspace_bytes, &g);
+    if (st != UFP4_OK) return st;
+    if (g.M == 0 || g.N == 0) return UFP4_OK;
+    if (g.K == 0) return run_prepared_gemm(g, stream);
+    const cudaError_t e = launch_gemm_main(g, num_sms_current(), stream);
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    return cuda_status(e);
+}
+
 ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
                                              const ufp4_quant_desc* desc, size_t* bytes) {
     if (num_groups < 0 || (num_groups && (!A || !B)) || !bytes) return UFP4_ERR_INVALID_ARG;

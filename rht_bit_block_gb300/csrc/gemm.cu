@@ -652,13 +652,13 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, i
     return make_plan(M, N, K, grid, br, bc).total;
 }
 
-cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
+// Operand preparation: FP8 widening (E1M2/INT4) and scale chunks into the workspace.
+cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
     if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
     if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
-    // operand prep
     for (int side = 0; side < 2; ++side) {
         const GemmOperand& op = side ? g.b : g.a;
         PrepParams pp{};
@@ -686,6 +686,16 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
+    return cudaSuccess;
+}
+
+// The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.
+cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
+    if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;
+    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
+    if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+    uint8_t* ws = (uint8_t*)g.workspace;
     CUtensorMap ma, mb;
     const void* a_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
     const void* b_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
@@ -715,6 +725,12 @@ cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
     }
     for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x4, 0);
     return run_gemm<2, kBnFp4x4, 4>(ma, mb, kp, num_sms, st);
+}
+
+cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
+    const cudaError_t e = launch_gemm_prep(g, st);
+    if (e != cudaSuccess) return e;
+    return launch_gemm_main(g, num_sms, st);
 }
 
 }  // namespace ufp4

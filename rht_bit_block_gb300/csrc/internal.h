@@ -89,5 +89,7 @@ struct GemmArgs {
 };
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc);
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st);
+cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st);
+cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st);
 
 }  // namespace ufp4

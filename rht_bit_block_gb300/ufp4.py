@@ -27,7 +27,7 @@ EXPORTED = (
     "ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_grouped_padded_rows",
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
-    "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped",
+    "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
 )
 
 
@@ -71,6 +71,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_gemm_workspace_size.argtypes = [i64, i64, i64, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
     L.ufp4_gemm_noalloc.argtypes = [QT, QT, QD, P, i64, P]
+    L.ufp4_gemm_prepare.argtypes = [QT, QT, QD, P, ctypes.c_size_t, P]
+    L.ufp4_gemm_prepared.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
     L.ufp4_gemm_grouped_workspace_size.argtypes = [i32, QT, QT, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm_grouped.argtypes = [i32, QT, QT, QD, ctypes.POINTER(P), ctypes.POINTER(i64), P, ctypes.c_size_t, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
@@ -79,7 +81,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_status_string.restype = ctypes.c_char_p
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
                  "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error",
-                 "ufp4_gemm_noalloc", "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped"):
+                 "ufp4_gemm_noalloc", "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped",
+                 "ufp4_gemm_prepare", "ufp4_gemm_prepared"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -157,6 +160,18 @@ def ufp4_gemm(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace=None, stream
     ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
     _check(load().ufp4_gemm(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(), D.stride(0),
                             ws_ptr, ws_bytes, _stream(stream)), "ufp4_gemm")
+
+
+def ufp4_gemm_prepare(A: QTensor, B: QTensor, desc: QuantDesc, workspace, stream=None):
+    _check(load().ufp4_gemm_prepare(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), workspace.data_ptr(),
+                                    workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ufp4_gemm_prepare")
+
+
+def ufp4_gemm_prepared(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace, stream=None):
+    _check(load().ufp4_gemm_prepared(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), D.data_ptr(),
+                                     D.stride(0), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                     _stream(stream)), "ufp4_gemm_prepared")
 
 
 def ufp4_gemm_grouped_workspace_size(A, B, desc: QuantDesc) -> int:

@@ -164,3 +164,27 @@ def test_large_fprop_sampled_rows(grid, block):
     got = D[torch.from_numpy(rows).cuda()].cpu().numpy().astype(np.float64)
     ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=block, a_rows=rows)
     assert _rel(got, ref) <= TOL
+
+
+@pytest.mark.parametrize("grid", ["e1m2", "e2m1"])
+def test_prepare_then_prepared_equals_gemm(grid):
+    """ufp4_gemm = ufp4_gemm_prepare + ufp4_gemm_prepared, bit for bit, and a
+    prepared workspace can serve a second call."""
+    M, N, K = 256, 384, 512
+    rng = np.random.default_rng(77)
+    ac, asc = _rand_operand(rng, M, K, grid, (1, 16), lo=120, hi=132)
+    bc, bsc = _rand_operand(rng, N, K, grid, (1, 16), lo=120, hi=132)
+    desc = ufp4.make_desc(grid=grid, block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+    A = [torch.from_numpy(ac).cuda(), torch.from_numpy(asc).cuda()]
+    B = [torch.from_numpy(bc).cuda(), torch.from_numpy(bsc).cuda()]
+    qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+    ws = torch.empty(max(1, ufp4.ufp4_gemm_workspace_size(M, N, K, desc)), dtype=torch.uint8, device="cuda")
+    D1 = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    D2 = torch.empty_like(D1)
+    D3 = torch.empty_like(D1)
+    ufp4.ufp4_gemm(qa, qb, desc, D1, ws)
+    ufp4.ufp4_gemm_prepare(qa, qb, desc, ws)
+    ufp4.ufp4_gemm_prepared(qa, qb, desc, D2, ws)
+    ufp4.ufp4_gemm_prepared(qa, qb, desc, D3, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(D1, D2) and torch.equal(D1, D3)
