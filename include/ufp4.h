@@ -149,7 +149,9 @@ typedef struct {
  * Both outputs come from one read of x.  Requirements: cols divisible by n
  * and by the block width for the row-wise output, rows divisible by n and by
  * the block width for the column-wise one (2-D blocks: both dimensions by b).
- * The qtensor's rows/cols must equal the shapes above. */
+ * The qtensor's rows/cols must equal the shapes above.  On a non-default
+ * stream the kernel is launched as a programmatic dependent of the previous
+ * kernel; it waits for that kernel to finish before it reads or writes. */
 ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld,
                               const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
                               const ufp4_qtensor* colwise, cudaStream_t stream);
@@ -212,7 +214,11 @@ ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4
  * widened exactly into FP8 (E5M2) in the workspace first.
  *   D          device float, leading dimension ldd (multiple of 4, D 16-byte aligned)
  *   workspace  device scratch of at least ufp4_gemm_workspace_size bytes,
- *              256-byte aligned; contents on entry are ignored. */
+ *              256-byte aligned; contents on entry are ignored.
+ * M, N and K up to 2^30 (UFP4_ERR_UNSUPPORTED beyond).  On a non-default
+ * stream the kernels are launched as programmatic dependents: each one waits
+ * for the previous kernel of the stream to finish before it touches memory,
+ * so stream order is kept exactly as with plain launches. */
 ufp4_status ufp4_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc,
                       float* D, int64_t ldd, void* workspace, size_t workspace_bytes,
                       cudaStream_t stream);

@@ -220,6 +220,7 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
     const int64_t M = A->rows, N = B->rows, K = A->cols;
     if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
+    if (M > (1LL << 30) || N > (1LL << 30) || K > (1LL << 30)) return UFP4_ERR_UNSUPPORTED;  // 32-bit indexing
     if (M > 0 && N > 0 && !D) return UFP4_ERR_INVALID_ARG;
     if (K % 32 && !(bs.bw == 16 && K % 16 == 0)) return UFP4_ERR_INVALID_ARG;
     std::memset(out, 0, sizeof(*out));

@@ -21,6 +21,7 @@
 // back (tcgen05.ld) and store fp32, so a tile's epilogue overlaps the next
 // tile's main loop.  Every wait is bounded: on expiry the kernel records an
 // error code, lets its copies and MMAs finish and returns.
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
@@ -291,6 +292,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // operands come from the prep kernel; D may still be read by the kernel before
+    griddep_wait();
+    griddep_launch();
 
     if (warp == 0 && lane == 0) {
         // ---------------------------------------------------- TMA producer
@@ -429,34 +433,39 @@ __device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-149, 127]
     return __uint_as_float(1u << (e + 149));
 }
 
-struct PrepParams {
+// One operand of the prep launch.
+struct PrepSide {
     const uint8_t* codes;
     const uint8_t* scales;
-    int64_t rows, K, codes_ld, scales_ld;
-    int grid, br, bc;
-    uint8_t* out_fp8;      // rows x K (E1M2/INT4 only)
-    uint8_t* out_chunks;   // ceil(rows/128) x chunks_k x 512
-    int64_t chunks_k;
-    int hw_block;          // 16 (E2M1 1x16) or 32
-    int64_t rows_cover;    // chunk rows written: rows rounded up to the GEMM tile
-    int tile_rows;         // rows of one GEMM tile of this operand (128 for A, BN for B)
+    int64_t codes_ld, scales_ld;
+    int rows;          // rows of the operand
+    int rows_cover;    // chunk rows written: rows rounded up to whole GEMM tiles
+    int tile_rows;     // rows of one GEMM tile of this operand (128 for A, BN for B)
+    uint8_t* out_fp8;  // rows x K bytes (E1M2/INT4 only)
+    uint8_t* out_chunks;
+};
+
+// Both operands in one launch (blockIdx.z picks the side).
+struct PrepParams {
+    PrepSide side[2];
+    int K;
+    int chunks_k;      // chunk cells along K per 128 rows
+    int grid;          // codebook
+    int lbr, lbc;      // log2 of the block rows and columns
+    int lhw;           // log2 of the hardware scale block: 4 (E2M1 1x16) or 5
 };
 
 // Scale chunks are grouped per GEMM tile: tile t = row / tile_rows holds
 // ceil(tile_rows / 128) blocks of 128 rows; inside a block, row w and scale
-// cell j sit at (w % 32) * 16 + (w / 32) * 4 + j (the tcgen05.cp 32x128b layout).
-__device__ __forceinline__ int64_t chunk_offset(const PrepParams& p, int64_t row, int64_t cell) {
-    const int halves = (p.tile_rows + 127) / 128;
-    const int64_t t = row / p.tile_rows;
-    const int64_t rr = row - t * p.tile_rows;
-    const int64_t cb = t * halves + rr / 128;
-    const int64_t w = rr % 128;
-    return (cb * p.chunks_k + cell) * kChunkBytes + (w % 32) * 16 + (w / 32) * 4;
-}
-
-__device__ __forceinline__ int src_scale(const PrepParams& p, int64_t row, int64_t k_elem) {
-    // UE8M0 byte of the block holding (row, k_elem)
-    return p.scales[(row / p.br) * p.scales_ld + k_elem / p.bc];
+// cell j sit at (w % 32) * 16 + (w / 32) * 4 + j (the tcgen05.cp 32x128b
+// layout).  Returns the byte offset of cell 0 of this row.
+__device__ __forceinline__ int64_t chunk_row_offset(const PrepSide& s, int chunks_k, int row) {
+    const int halves = (s.tile_rows + 127) >> 7;
+    const int t = row / s.tile_rows;
+    const int rr = row - t * s.tile_rows;
+    const int64_t cb = (int64_t)t * halves + (rr >> 7);
+    const int w = rr & 127;
+    return cb * chunks_k * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -479,79 +488,94 @@ __device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
 }
 
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
-// elements.  One thread: one row, one 32-element group (16 code bytes in,
-// 32 FP8 bytes and one scale byte out); consecutive threads walk along K.
-__global__ void prep_widen_kernel(const PrepParams p) {
-    const int64_t groups = (p.K + 31) / 32;
-    const int64_t gpad = p.chunks_k * 4;  // groups covered by the chunk layout
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= p.rows_cover * gpad) return;
-    const int64_t row = idx / gpad;
-    const int64_t grp = idx - row * gpad;
-    const int64_t k0 = grp * 32;
-    const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
-    int hw = 0;
-    if (row < p.rows && grp < groups) {
-        const int e0 = src_scale(p, row, k0);
-        const int e1 = (p.bc == 16) ? src_scale(p, row, k0 + 16) : e0;
-        hw = max(max(e0, e1) + step_log2, 0);
-        const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
-        const uint4 cw = *reinterpret_cast<const uint4*>(p.codes + row * p.codes_ld + k0 / 2);
-        uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
-        if (p.grid == 1) {
+// elements.  A CTA of 128 threads covers 128 rows of one operand (blockIdx.x)
+// and one 128-element K tile (blockIdx.y); a thread owns one row of it: 64
+// code bytes in, 128 FP8 bytes and one 4-byte chunk cell (the four scales of
+// the tile) out.
+__global__ void __launch_bounds__(128) prep_widen_kernel(const PrepParams p) {
+    griddep_wait();
+    griddep_launch();
+    const PrepSide& s = p.side[blockIdx.z];
+    const int row = blockIdx.x * 128 + threadIdx.x;
+    if (row >= s.rows_cover) return;
+    const int kt = blockIdx.y;
+    uint32_t cell = 0;
+    if (row < s.rows) {
+        const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
+        const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+        const uint4* crow = reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld) + kt * 4;
+        uint4* orow = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * p.K) + kt * 8;
+#pragma unroll 1
+        for (int j = 0; j < 4; ++j) {
+            const int k0 = kt * 128 + j * 32;
+            if (k0 >= p.K) break;
+            const int e0 = srow[k0 >> p.lbc];
+            const int e1 = p.lbc == 4 ? srow[(k0 + 16) >> 4] : e0;
+            const int hw = max(max(e0, e1) + step_log2, 0);
+            const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
+            const uint4 cw = crow[j];
+            uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            if (p.grid == 1) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
-                const uint32_t w = words[q];
-                const uint32_t neg = (w >> 3) & 0x11111111u;
-                const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
-                words[q] = mag | (neg << 3);
-            }
-        }
-        uint32_t outw[8];
-        if (d0 <= 14 && d1 <= 14) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
-                outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
-            }
-        } else {
-            // shifts beyond E5M2's normal range: exact float path, rounding to
-            // nearest only below E5M2's smallest subnormal
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float mult = pow2f(-(q < 4 ? d0 : d1));
-                const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                float v[4];
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t nib = (w >> (4 * t)) & 0xFu;
-                    const float k = (float)(int)(nib & 7u);
-                    v[t] = ((nib & 8u) ? -k : k) * mult;
+                for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
+                    const uint32_t w = words[q];
+                    const uint32_t neg = (w >> 3) & 0x11111111u;
+                    const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
+                    words[q] = mag | (neg << 3);
                 }
-                outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
             }
+            uint32_t outw[8];
+            if (d0 <= 14 && d1 <= 14) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
+                    outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
+                }
+            } else {
+                // shifts beyond E5M2's normal range: exact float path, rounding to
+                // nearest only below E5M2's smallest subnormal
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float mult = pow2f(-(q < 4 ? d0 : d1));
+                    const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+                    float v[4];
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t nib = (w >> (4 * t)) & 0xFu;
+                        const float k = (float)(int)(nib & 7u);
+                        v[t] = ((nib & 8u) ? -k : k) * mult;
+                    }
+                    outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
+                }
+            }
+            orow[2 * j] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+            orow[2 * j + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
+            cell |= (uint32_t)hw << (8 * j);
         }
-        uint4* dst = reinterpret_cast<uint4*>(p.out_fp8 + row * p.K + k0);
-        dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-        dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    p.out_chunks[chunk_offset(p, row, grp >> 2) + (grp & 3)] = (uint8_t)hw;
+    *reinterpret_cast<uint32_t*>(s.out_chunks + chunk_row_offset(s, p.chunks_k, row) + (int64_t)kt * kChunkBytes) =
+        cell;
 }
 
-// E2M1: only the scales move, into the chunk layout (hw_block 16 or 32).
-__global__ void prep_scales_kernel(const PrepParams p) {
-    const int64_t idx = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (idx >= p.rows_cover * p.chunks_k) return;
-    const int64_t row = idx / p.chunks_k;
-    const int64_t cell = idx % p.chunks_k;
-    uint32_t cellv = 0;
-    for (int j = 0; j < 4; ++j) {
-        const int64_t k0 = (cell * 4 + j) * p.hw_block;
-        int b = 0;
-        if (row < p.rows && k0 < p.K) b = src_scale(p, row, k0);
-        cellv |= (uint32_t)b << (8 * j);
+// E2M1: only the scales move, into the chunk layout (hardware blocks of 16 or
+// 32 elements).  One thread: one row, one 4-byte chunk cell.
+__global__ void __launch_bounds__(128) prep_scales_kernel(const PrepParams p) {
+    griddep_wait();
+    griddep_launch();
+    const PrepSide& s = p.side[blockIdx.z];
+    const int row = blockIdx.x * 128 + threadIdx.x;
+    if (row >= s.rows_cover) return;
+    const int c = blockIdx.y;
+    uint32_t cell = 0;
+    if (row < s.rows) {
+        const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+        for (int j = 0; j < 4; ++j) {
+            const int k0 = (c * 4 + j) << p.lhw;
+            if (k0 < p.K) cell |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
+        }
     }
-    *reinterpret_cast<uint32_t*>(p.out_chunks + chunk_offset(p, row, cell)) = cellv;
+    *reinterpret_cast<uint32_t*>(s.out_chunks + chunk_row_offset(s, p.chunks_k, row) + (int64_t)c * kChunkBytes) =
+        cell;
 }
 
 // ------------------------------------------------------------ host side
@@ -589,6 +613,12 @@ struct Plan {
 };
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+int ilog2(int v) {  // v a power of two
+    int l = 0;
+    while ((1 << l) < v) ++l;
+    return l;
+}
 
 // Output tiles are 128 x 192: two accumulators and two scale sets fit in the
 // 512 tensor-memory columns, and a 5-stage ring (4 for FP4 with 16-element
@@ -630,8 +660,7 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKPa
     if (e != cudaSuccess) return e;
     const int tiles = kp.m_tiles * kp.n_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
-    k<<<grid, kGemmThreads, C::kSmem, st>>>(ma, mb, kp);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kGemmThreads), (size_t)C::kSmem, st, ma, mb, kp);
 }
 
 }  // namespace
@@ -659,34 +688,32 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
+    PrepParams pp{};
+    int row_blocks = 0;
     for (int side = 0; side < 2; ++side) {
         const GemmOperand& op = side ? g.b : g.a;
-        PrepParams pp{};
-        pp.codes = op.codes;
-        pp.scales = op.scales;
-        pp.rows = op.rows;
-        pp.K = g.K;
-        pp.codes_ld = op.codes_ld;
-        pp.scales_ld = op.scales_ld;
-        pp.grid = g.grid;
-        pp.br = g.br;
-        pp.bc = g.bc;
-        pp.out_fp8 = pl.kind == 0 ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
-        pp.out_chunks = ws + (side ? pl.sfb : pl.sfa);
-        pp.chunks_k = pl.chunks_k;
-        pp.hw_block = pl.kind == 2 ? 16 : 32;
-        pp.tile_rows = side ? pl.bn : kBM;
-        // chunk rows cover whole output tiles
-        pp.rows_cover = ((op.rows + pp.tile_rows - 1) / pp.tile_rows) * pp.tile_rows;
-        const int64_t threads = pp.rows_cover * pl.chunks_k * (pl.kind == 0 ? 4 : 1);
-        const int tb = 256;
-        const unsigned blocks = (unsigned)((threads + tb - 1) / tb);
-        if (pl.kind == 0) prep_widen_kernel<<<blocks, tb, 0, st>>>(pp);
-        else prep_scales_kernel<<<blocks, tb, 0, st>>>(pp);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        PrepSide& ps = pp.side[side];
+        ps.codes = op.codes;
+        ps.scales = op.scales;
+        ps.codes_ld = op.codes_ld;
+        ps.scales_ld = op.scales_ld;
+        ps.rows = (int)op.rows;
+        ps.tile_rows = side ? pl.bn : kBM;
+        ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;  // whole output tiles
+        ps.out_fp8 = pl.kind == 0 ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
+        ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
+        row_blocks = std::max(row_blocks, (ps.rows_cover + 127) / 128);
     }
-    return cudaSuccess;
+    pp.K = (int)g.K;
+    pp.chunks_k = (int)pl.chunks_k;
+    pp.grid = g.grid;
+    pp.lbr = ilog2(g.br);
+    pp.lbc = ilog2(g.bc);
+    pp.lhw = pl.kind == 2 ? 4 : 5;
+    if (pl.chunks_k > 65535) return cudaErrorNotSupported;  // grid y limit: K up to 8.3 M elements
+    const dim3 grid((unsigned)row_blocks, (unsigned)pl.chunks_k, 2);
+    if (pl.kind == 0) return launch_pdl(prep_widen_kernel, grid, dim3(128), 0, st, pp);
+    return launch_pdl(prep_scales_kernel, grid, dim3(128), 0, st, pp);
 }
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.

@@ -10,6 +10,35 @@ namespace ufp4 {
 
 constexpr int kMaxGroups = 64;
 
+// Programmatic dependent launch.  Kernels launched through launch_pdl may
+// start while the previous kernel of the stream is still running; each of
+// them executes griddep_wait() before it touches global memory that the
+// previous kernel may write or read (the wait returns once that kernel has
+// completed and its writes are visible), and griddep_launch() to let the
+// next kernel start early.  Without the launch attribute both are no-ops.
+#ifdef __CUDACC__
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+#endif
+
+// The attribute is set on non-default streams only; launches on the legacy
+// default stream stay plain.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = st ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 struct SignBits {
     uint32_t bits[8];  // bit i set <=> eps_{i mod n} = -1, for i in 0..255
 };

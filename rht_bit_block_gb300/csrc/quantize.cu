@@ -244,6 +244,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // the input may come from the previous kernel, and that kernel may still
+    // read buffers this one writes: wait for it before the first copy
+    griddep_wait();
+    griddep_launch();
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
@@ -595,8 +599,7 @@ static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int nu
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = num_tiles < 2 * num_sms ? num_tiles : 2 * num_sms;
-    k<<<grid, kThreads, smem, st>>>(map, p, num_tiles);
-    return cudaGetLastError();
+    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, map, p, num_tiles);
 }
 
 template <int GRID, bool SR, bool PO2>
