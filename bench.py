@@ -221,7 +221,10 @@ def run_gpu(args):
         dist.init_process_group("nccl", device_id=dev)
     from rht_bit_block_gb300 import inputs, ufp4
     ufp4.load()
-    stream = torch.cuda.current_stream()
+    # a stream of its own: on non-default streams the library launches its
+    # kernels as programmatic dependents of the previous kernel
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
 
     def barrier():
         if world > 1:

@@ -505,16 +505,25 @@ __global__ void __launch_bounds__(128) prep_widen_kernel(const PrepParams p) {
         const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
         const uint4* crow = reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld) + kt * 4;
         uint4* orow = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * p.K) + kt * 8;
-#pragma unroll 1
+        const int ng = min(4, (p.K - kt * 128) >> 5);  // 32-element groups of this tile (K % 32 == 0)
+        // issue every load of the tile before converting
+        uint4 cw[4];
+        int e0[4], e1[4];
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int k0 = kt * 128 + j * 32;
-            if (k0 >= p.K) break;
-            const int e0 = srow[k0 >> p.lbc];
-            const int e1 = p.lbc == 4 ? srow[(k0 + 16) >> 4] : e0;
-            const int hw = max(max(e0, e1) + step_log2, 0);
-            const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
-            const uint4 cw = crow[j];
-            uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+            if (j < ng) {
+                const int k0 = kt * 128 + j * 32;
+                cw[j] = crow[j];
+                e0[j] = srow[k0 >> p.lbc];
+                e1[j] = p.lbc == 4 ? srow[(k0 + 16) >> 4] : e0[j];
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            if (j >= ng) break;
+            const int hw = max(max(e0[j], e1[j]) + step_log2, 0);
+            const int d0 = hw - step_log2 - e0[j], d1 = hw - step_log2 - e1[j];  // >= 0
+            uint32_t words[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
             if (p.grid == 1) {
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
