@@ -488,96 +488,84 @@ __device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
 }
 
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
-// elements.  A CTA of 128 threads covers 128 rows of one operand (blockIdx.x)
-// and one 128-element K tile (blockIdx.y); a thread owns one row of it: 64
-// code bytes in, 128 FP8 bytes and one 4-byte chunk cell (the four scales of
-// the tile) out.
-__global__ void __launch_bounds__(128) prep_widen_kernel(const PrepParams p) {
+// elements.  A CTA is 32 x 8 threads: each warp (threadIdx.y) owns one row,
+// each lane one 32-element group of it (16 code bytes in, 32 FP8 bytes and one
+// scale byte of a 4-byte chunk cell out), so that every load and store of a
+// warp is contiguous.  blockIdx.x: 8-row slab, blockIdx.y: 32-group slab,
+// blockIdx.z: operand.
+__global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
     griddep_wait();
     griddep_launch();
     const PrepSide& s = p.side[blockIdx.z];
-    const int row = blockIdx.x * 128 + threadIdx.x;
+    const int row = blockIdx.x * 8 + threadIdx.y;
     if (row >= s.rows_cover) return;
-    const int kt = blockIdx.y;
-    uint32_t cell = 0;
-    if (row < s.rows) {
+    const int grp = blockIdx.y * 32 + threadIdx.x;  // 32-element group along K
+    if (grp >= p.chunks_k * 4) return;               // groups covered by the chunk cells
+    const int k0 = grp * 32;
+    int hw = 0;
+    if (row < s.rows && k0 < p.K) {
         const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
         const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
-        const uint4* crow = reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld) + kt * 4;
-        uint4* orow = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * p.K) + kt * 8;
-        const int ng = min(4, (p.K - kt * 128) >> 5);  // 32-element groups of this tile (K % 32 == 0)
-        // issue every load of the tile before converting
-        uint4 cw[4];
-        int e0[4], e1[4];
+        const uint4 cw = *reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld + grp * 16);
+        const int e0 = srow[k0 >> p.lbc];
+        const int e1 = p.lbc == 4 ? srow[(k0 >> 4) + 1] : e0;
+        hw = max(max(e0, e1) + step_log2, 0);
+        const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
+        uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+        if (p.grid == 1) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j < ng) {
-                const int k0 = kt * 128 + j * 32;
-                cw[j] = crow[j];
-                e0[j] = srow[k0 >> p.lbc];
-                e1[j] = p.lbc == 4 ? srow[(k0 + 16) >> 4] : e0[j];
+            for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
+                const uint32_t w = words[q];
+                const uint32_t neg = (w >> 3) & 0x11111111u;
+                const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
+                words[q] = mag | (neg << 3);
             }
         }
+        uint32_t outw[8];
+        if (d0 <= 14 && d1 <= 14) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            if (j >= ng) break;
-            const int hw = max(max(e0[j], e1[j]) + step_log2, 0);
-            const int d0 = hw - step_log2 - e0[j], d1 = hw - step_log2 - e1[j];  // >= 0
-            uint32_t words[4] = {cw[j].x, cw[j].y, cw[j].z, cw[j].w};
-            if (p.grid == 1) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
-                    const uint32_t w = words[q];
-                    const uint32_t neg = (w >> 3) & 0x11111111u;
-                    const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
-                    words[q] = mag | (neg << 3);
-                }
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
+                outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
             }
-            uint32_t outw[8];
-            if (d0 <= 14 && d1 <= 14) {
+        } else {
+            // shifts beyond E5M2's normal range: exact float path, rounding to
+            // nearest only below E5M2's smallest subnormal
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
-                    outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
+            for (int q = 0; q < 8; ++q) {
+                const float mult = pow2f(-(q < 4 ? d0 : d1));
+                const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
+                float v[4];
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t nib = (w >> (4 * t)) & 0xFu;
+                    const float k = (float)(int)(nib & 7u);
+                    v[t] = ((nib & 8u) ? -k : k) * mult;
                 }
-            } else {
-                // shifts beyond E5M2's normal range: exact float path, rounding to
-                // nearest only below E5M2's smallest subnormal
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const float mult = pow2f(-(q < 4 ? d0 : d1));
-                    const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                    float v[4];
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t nib = (w >> (4 * t)) & 0xFu;
-                        const float k = (float)(int)(nib & 7u);
-                        v[t] = ((nib & 8u) ? -k : k) * mult;
-                    }
-                    outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
-                }
+                outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
             }
-            orow[2 * j] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
-            orow[2 * j + 1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
-            cell |= (uint32_t)hw << (8 * j);
         }
+        uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * p.K + k0);
+        dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
+        dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    *reinterpret_cast<uint32_t*>(s.out_chunks + chunk_row_offset(s, p.chunks_k, row) + (int64_t)kt * kChunkBytes) =
-        cell;
+    s.out_chunks[chunk_row_offset(s, p.chunks_k, row) + (int64_t)(grp >> 2) * kChunkBytes + (grp & 3)] = (uint8_t)hw;
 }
 
 // E2M1: only the scales move, into the chunk layout (hardware blocks of 16 or
-// 32 elements).  One thread: one row, one 4-byte chunk cell.
-__global__ void __launch_bounds__(128) prep_scales_kernel(const PrepParams p) {
+// 32 elements).  Same CTA shape as above; a lane owns one 4-byte chunk cell.
+__global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
     griddep_wait();
     griddep_launch();
     const PrepSide& s = p.side[blockIdx.z];
-    const int row = blockIdx.x * 128 + threadIdx.x;
+    const int row = blockIdx.x * 8 + threadIdx.y;
     if (row >= s.rows_cover) return;
-    const int c = blockIdx.y;
+    const int c = blockIdx.y * 32 + threadIdx.x;
+    if (c >= p.chunks_k) return;
     uint32_t cell = 0;
     if (row < s.rows) {
         const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+#pragma unroll
         for (int j = 0; j < 4; ++j) {
             const int k0 = (c * 4 + j) << p.lhw;
             if (k0 < p.K) cell |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
@@ -711,7 +699,7 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
         ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;  // whole output tiles
         ps.out_fp8 = pl.kind == 0 ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
         ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
-        row_blocks = std::max(row_blocks, (ps.rows_cover + 127) / 128);
+        row_blocks = std::max(row_blocks, (ps.rows_cover + 7) / 8);
     }
     pp.K = (int)g.K;
     pp.chunks_k = (int)pl.chunks_k;
@@ -719,10 +707,12 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
     pp.lbr = ilog2(g.br);
     pp.lbc = ilog2(g.bc);
     pp.lhw = pl.kind == 2 ? 4 : 5;
-    if (pl.chunks_k > 65535) return cudaErrorNotSupported;  // grid y limit: K up to 8.3 M elements
-    const dim3 grid((unsigned)row_blocks, (unsigned)pl.chunks_k, 2);
-    if (pl.kind == 0) return launch_pdl(prep_widen_kernel, grid, dim3(128), 0, st, pp);
-    return launch_pdl(prep_scales_kernel, grid, dim3(128), 0, st, pp);
+    // 32 groups (FP8) or 32 chunk cells (FP4) per CTA along K
+    const int64_t kslabs = pl.kind == 0 ? (pl.chunks_k * 4 + 31) / 32 : (pl.chunks_k + 31) / 32;
+    if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
+    const dim3 grid((unsigned)row_blocks, (unsigned)kslabs, 2);
+    if (pl.kind == 0) return launch_pdl(prep_widen_kernel, grid, dim3(32, 8), 0, st, pp);
+    return launch_pdl(prep_scales_kernel, grid, dim3(32, 8), 0, st, pp);
 }
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.

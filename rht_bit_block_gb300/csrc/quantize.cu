@@ -28,7 +28,8 @@ __device__ int g_quant_error;
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kMaxStages = 6;               // TMA ring depth (up to 96 KB of tiles in flight per CTA)
+constexpr int kMaxStages = 6;               // TMA ring depth
+constexpr int kCtasPerSm = 3;               // 24 warps per SM; the ring holds about 64 KB per CTA
 constexpr uint32_t kWaitLimit = 1u << 24;   // bounded mbarrier polling
 
 __device__ __forceinline__ int find_group(const QuantParams& p, int row_tile) {
@@ -201,7 +202,7 @@ __device__ __forceinline__ void gather_pair(const uint16_t* tile, int tcol, int 
 }
 
 template <int GRID, bool SR, bool PO2, int TC>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
 quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, const int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int SZ = PO2 ? 1 : 4;         // bytes per scale
@@ -279,6 +280,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     int g = p.num_groups > 1 ? find_group(p, row_tile) : 0;
 
     int i = 0;
+    int s = 0;            // ring stage of tile i
+    uint32_t phase = 0;   // parity of that stage's current use
     for (;; ++i) {
         const int tile = blockIdx.x + i * gridDim.x;
         if (tile >= num_tiles) break;
@@ -291,8 +294,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             }
             if (p.num_groups > 1) g = find_group(p, row_tile);
         }
-        const int s = i % kStages;
-        const bool landed = wait_phase(bars + 8u * s, (uint32_t)((i / kStages) & 1));
+        const bool landed = wait_phase(bars + 8u * s, phase);
         if (!__syncthreads_and(landed)) {
             if (tid == 0) atomicExch(&g_quant_error, 1);
             break;
@@ -545,6 +547,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 issue(next, s);
             }
         }
+        if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+        }
     }
     // a broken-off loop leaves copies in flight: let them land (bounded)
     if (tid == 0)
@@ -598,7 +604,7 @@ static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int nu
     auto k = quantize_kernel<GRID, SR, PO2, TC>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int grid = num_tiles < 2 * num_sms ? num_tiles : 2 * num_sms;
+    const int grid = num_tiles < kCtasPerSm * num_sms ? num_tiles : kCtasPerSm * num_sms;
     return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, map, p, num_tiles);
 }
 

@@ -479,23 +479,25 @@ __device__ __forceinline__ float maxabs(float x, float y) {
 }
 
 // Tree amax of |a_i| and |b_i| over i in [lo, hi) (lo, hi multiples of 8).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void amax_pair(const uint64_t e[16], int lo, int hi, float& ma, float& mb) {
     float ta[16], tb[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) up2(e[i], ta[i], tb[i]);
     float ra = 0.0f, rb = 0.0f;
 #pragma unroll
-    for (int h8 = 0; h8 < 16; h8 += 8) {
-        if (h8 < lo || h8 >= hi) continue;
-        const float a01 = maxabs(ta[h8 + 0], ta[h8 + 1]), a23 = maxabs(ta[h8 + 2], ta[h8 + 3]);
-        const float a45 = maxabs(ta[h8 + 4], ta[h8 + 5]), a67 = maxabs(ta[h8 + 6], ta[h8 + 7]);
-        const float b01 = maxabs(tb[h8 + 0], tb[h8 + 1]), b23 = maxabs(tb[h8 + 2], tb[h8 + 3]);
-        const float b45 = maxabs(tb[h8 + 4], tb[h8 + 5]), b67 = maxabs(tb[h8 + 6], tb[h8 + 7]);
-        ra = maxabs(ra, maxabs(maxabs(a01, a23), maxabs(a45, a67)));
-        rb = maxabs(rb, maxabs(maxabs(b01, b23), maxabs(b45, b67)));
+    for (int i = 0; i < 16; i += 2) {
+        if (i < lo || i >= hi) continue;
+        ra = max3(ra, fabsf(ta[i]), fabsf(ta[i + 1]));
+        rb = max3(rb, fabsf(tb[i]), fabsf(tb[i + 1]));
     }
-    ma = fabsf(ra);
-    mb = fabsf(rb);
+    ma = ra;
+    mb = rb;
 }
 
 }  // namespace ufp4
