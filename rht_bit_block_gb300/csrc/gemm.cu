@@ -44,6 +44,15 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // bounded polling; each poll may sle
 constexpr uint32_t kSuspendNs = 1000;
 constexpr int kErrTimeout = 1;
 
+// Output tile widths.  FP8 runs on CTA pairs with 256 x 224 tiles: two
+// 224-column accumulators plus two sets of scale columns fit the 512
+// tensor-memory columns, and the wider tile gives each MMA instruction more
+// work (issuing a tcgen05 instruction costs a fixed time).  FP4 runs 128 x 192
+// tiles on single CTAs.
+constexpr int kBnFp8 = 224, kBnFp4x2 = 192, kBnFp4x4 = 192;
+// FP8 CTA-pair ring: kPairStages stages of kPairKps K tiles each
+constexpr int kPairKps = 2, kPairStages = 3;
+
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return (uint32_t)__cvta_generic_to_shared(p);
@@ -417,6 +426,310 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
     }
 }
 
+// ------------------------------------------------- CTA-pair FP8 kernel
+// The FP8 path (E1M2 / INT4 widened to E5M2) on CTA pairs: a cluster of two
+// CTAs on two SMs computes a 256 x 192 output tile with tcgen05.mma
+// .cta_group::2.  Each CTA holds its own 128 rows of A and half (96 rows) of
+// B, so per SM the shared-memory and L2 traffic per MMA FLOP drops by about
+// 30 % against the single-CTA 128 x 192 tile; the accumulator rows of a CTA
+// sit in its own tensor memory.  Both CTAs hold the full 192-row scale chunks
+// of B.  The even CTA ("leader") issues the MMAs for both; both CTAs' copies
+// complete on the leader's stage barrier, and the leader's commits arrive on
+// the barriers of both CTAs.
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// shared::cluster address of the same shared-memory offset in CTA `rank`
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// arrive on an mbarrier given by its shared::cluster address (own or peer CTA)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+
+// TMA tile load into this CTA's shared memory whose completion is counted on
+// an mbarrier of either CTA of the pair (shared::cluster address).
+__device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t cbar,
+                                              uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(dst), "l"((uint64_t)map), "r"(x), "r"(y), "r"(cbar), "l"(pol)
+        : "memory");
+}
+
+// nk consecutive 512-byte chunk rows: the chunk maps are encoded with a box
+// of KPS rows; with nk < KPS (last stage of an odd K) the box still lands
+// KPS rows, so the byte count expected is that of the full box.
+__device__ __forceinline__ void tma_load_pair_rows(uint32_t dst, const CUtensorMap* map, int row, int nk, uint32_t cbar,
+                                                   uint64_t pol) {
+    (void)nk;
+    tma_load_pair(dst, map, 0, row, cbar, pol);
+}
+
+__device__ __forceinline__ void mma_pair_fp8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                             uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+        : "memory");
+}
+
+// arrives on the mbarrier at this offset in both CTAs once every MMA / copy
+// issued so far by this thread has completed
+__device__ __forceinline__ void tc_commit_pair_both(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+        "h"((uint16_t)3)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tc_cp_scales_pair(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// A stage holds KPS consecutive 128-byte K tiles ("atoms") of each operand.
+template <int STAGES, int KPS>
+struct PairCfg {
+    static constexpr int BN = kBnFp8;                    // output columns of a pair tile
+    static constexpr int kBRows = BN / 2;                // B rows held per CTA
+    static constexpr int kAAtom = kBM * kBKBytes;        // 16 KB
+    static constexpr int kBAtom = kBRows * kBKBytes;     // 14 KB
+    static constexpr int kABytes = KPS * kAAtom;
+    static constexpr int kBBytes = KPS * kBAtom;
+    static constexpr int kSfaBytes = KPS * kChunkBytes;      // KPS chunks of this CTA's 128 rows
+    static constexpr int kSfbBytes = 2 * KPS * kChunkBytes;  // KPS chunks of each 128-row part of the BN B rows
+    static constexpr int kTxPerAtom = kAAtom + kBAtom;              // operand bytes per CTA per K tile
+    static constexpr int kTxScales = 3 * KPS * kChunkBytes;        // scale bytes per CTA per stage (full boxes)
+    static constexpr int kOffB = STAGES * kABytes;
+    static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
+    static constexpr int kOffSfb = kOffSfa + STAGES * kSfaBytes;
+    static constexpr int kOffBars = kOffSfb + STAGES * kSfbBytes;
+    static constexpr int kNumBars = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
+    static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024;
+    static constexpr int kTmemCols = 512;
+    static constexpr int kSfaCol = 2 * BN;               // two sets of 4 columns
+    static constexpr int kSfbCol = 2 * BN + 8;           // two sets of 8 columns
+    static_assert(kSfbCol + 16 <= kTmemCols, "tensor memory overflow");
+    static_assert(kSmem <= 232448, "shared memory overflow");
+    static_assert(kBAtom % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
+    static_assert(BN % 32 == 0 && BN > 128 && BN <= 256, "two scale chunks of B; 32-column epilogue reads");
+};
+
+struct PairKParams {
+    int M, N, k_tiles, m_pairs, n_tiles;
+    int64_t sf_chunks_k;  // chunk rows per 128-row block along K
+    float* D;
+    int64_t ldd;
+    int vec8;
+    uint32_t idesc[4];
+};
+
+template <int STAGES, int KPS>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                 const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
+                 const PairKParams p) {
+    using C = PairCfg<STAGES, KPS>;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + C::kOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
+    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
+    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
+    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * C::kNumBars + 4);
+    auto stage_a = [&](int s) { return base + s * C::kABytes; };
+    auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
+    auto stage_sfa = [&](int s) { return base + C::kOffSfa + s * C::kSfaBytes; };
+    auto stage_sfb = [&](int s) { return base + C::kOffSfb + s * C::kSfbBytes; };
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const uint32_t peer = rank & 1u;       // 0: leader (even CTA), 1: the other CTA of the pair
+    const uint32_t leader = rank & ~1u;
+    const int num_tiles = p.m_pairs * p.n_tiles;
+    const int cluster_id = blockIdx.x >> 1;
+    const int num_clusters = gridDim.x >> 1;
+    const int k_stages = (p.k_tiles + KPS - 1) / KPS;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full_bar(s), 1);   // the leader's expect_tx arrival (both CTAs' bytes)
+            mbar_init(empty_bar(s), 1);  // the leader's commit
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(accf_bar(b), 1);   // the leader's commit
+            mbar_init(acce_bar(b), 8);   // four epilogue warps of each CTA
+        }
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        // one warp of each CTA of the pair allocates, collectively
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(C::kTmemCols));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any copy or commit targets them
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_wait();
+    griddep_launch();
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer (both CTAs)
+        int s = 0;
+        uint32_t ph = 0;
+        const uint64_t keep = policy_evict_last();
+        for (int tile = cluster_id; tile < num_tiles && !*abort_flag; tile += num_clusters) {
+            const int mp = tile % p.m_pairs, nb = tile / p.m_pairs;
+            const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
+            const int arow = ablk * kBM;
+            const int brow = nb * C::BN + (int)peer * C::kBRows;
+            const int sfa_row = ablk * (int)p.sf_chunks_k;
+            const int sfb_row0 = (2 * nb) * (int)p.sf_chunks_k, sfb_row1 = (2 * nb + 1) * (int)p.sf_chunks_k;
+            for (int ks = 0; ks < k_stages; ++ks) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                const int kt0 = ks * KPS;
+                const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
+                const uint32_t fb = map_to_rank(full_bar(s), leader);
+                if (peer == 0) mbar_expect_tx(full_bar(s), 2 * (nk * C::kTxPerAtom + C::kTxScales));
+                for (int j = 0; j < nk; ++j) {
+                    tma_load_pair(stage_a(s) + j * C::kAAtom, &tmap_a, (kt0 + j) * kBKBytes, arow, fb, keep);
+                    tma_load_pair(stage_b(s) + j * C::kBAtom, &tmap_b, (kt0 + j) * kBKBytes, brow, fb, keep);
+                }
+                // chunks of consecutive K tiles are contiguous: one box of nk chunk rows each
+                tma_load_pair_rows(stage_sfa(s), &tmap_sfa, sfa_row + kt0, nk, fb, keep);
+                tma_load_pair_rows(stage_sfb(s), &tmap_sfb, sfb_row0 + kt0, nk, fb, keep);
+                tma_load_pair_rows(stage_sfb(s) + KPS * kChunkBytes, &tmap_sfb, sfb_row1 + kt0, nk, fb, keep);
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0 && peer == 0) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        int s = 0, tc = 0;
+        uint32_t ph = 0;
+        int it = 0;  // K tiles issued so far (alternates the scale sets)
+        bool ok = true;
+        for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++tc) {
+            const int buf = tc & 1;
+            if (!mbar_wait(acce_bar(buf), ((tc >> 1) & 1) ^ 1)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t acc = tmem + buf * C::BN;
+            for (int ks = 0; ks < k_stages; ++ks) {
+                if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const int kt0 = ks * KPS;
+                const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
+                for (int j = 0; j < nk; ++j, ++it) {
+                    const int set = it & 1;
+                    const uint32_t sfa_t = tmem + C::kSfaCol + set * 4;
+                    const uint32_t sfb_t = tmem + C::kSfbCol + set * 8;
+                    tc_cp_scales_pair(sfa_t, plain_desc(stage_sfa(s) + j * kChunkBytes));
+                    tc_cp_scales_pair(sfb_t, plain_desc(stage_sfb(s) + j * kChunkBytes));
+                    tc_cp_scales_pair(sfb_t + 4, plain_desc(stage_sfb(s) + (KPS + j) * kChunkBytes));
+                    const uint64_t da = sw128_desc(stage_a(s) + j * C::kAAtom);
+                    const uint64_t db = sw128_desc(stage_b(s) + j * C::kBAtom);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        mma_pair_fp8(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t, sfb_t,
+                                     (kt0 + j > 0 || q > 0) ? 1u : 0u);
+                }
+                tc_commit_pair_both(empty_bar(s));  // frees stage s in both CTAs
+                if (++s == STAGES) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (ok) tc_commit_pair_both(accf_bar(buf));
+        }
+        if (!ok) *abort_flag = 1;
+        tc_commit_pair_local(drain_bar);
+        mbar_wait(drain_bar, 0);
+    } else if (warp >= 4) {
+        // ------------------------------------------------- epilogue (both CTAs)
+        const int q = warp - 4;
+        const uint64_t stream_out = policy_evict_first();
+        int tc = 0;
+        for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++tc) {
+            const int buf = tc & 1;
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), (tc >> 1) & 1));
+            if (!ok || *abort_flag) break;
+            tc_fence_after();
+            const int mp = tile % p.m_pairs, nb = tile / p.m_pairs;
+            const int row = (2 * mp + (int)peer) * kBM + q * 32 + lane;
+            const int n0 = nb * C::BN;
+            for (int c = 0; c < C::BN; c += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * C::BN + c, r);
+                if (row < p.M) {
+                    float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
+                    if (n0 + c + 32 <= p.N) {
+                        if (p.vec8) {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 8) st_out8(dst + i, r + i, stream_out);
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; i += 4) st_out4(dst + i, r + i, stream_out);
+                        }
+                    } else {
+                        for (int i = 0; i < 32; ++i)
+                            if (n0 + c + i < p.N) dst[i] = __uint_as_float(r[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(acce_bar(buf), leader));
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the other may still use its memory or barriers
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
+    }
+}
+
 // ------------------------------------------------------------- prep kernels
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
 // elements.  One thread: one row, one 128-element K group (4 scale cells).
@@ -617,10 +930,10 @@ int ilog2(int v) {  // v a power of two
     return l;
 }
 
-// Output tiles are 128 x 192: two accumulators and two scale sets fit in the
-// 512 tensor-memory columns, and a 5-stage ring (4 for FP4 with 16-element
-// scales) fits in shared memory.
-constexpr int kBnFp8 = 192, kBnFp4x2 = 192, kBnFp4x4 = 192;
+// FP4 tiles are 128 x 192 on single CTAs with a 5-stage ring (4 for 16-element
+// scales); FP8 tiles are 256 x kBnFp8 on CTA pairs (the tile widths are set
+// at the top of this file).
+
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
     Plan pl{};
@@ -658,6 +971,48 @@ cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKPa
     const int tiles = kp.m_tiles * kp.n_tiles;
     const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
     return launch_pdl(k, dim3(grid), dim3(kGemmThreads), (size_t)C::kSmem, st, ma, mb, kp);
+}
+
+// Co-resident two-CTA clusters of the pair kernel on this device (cached).
+template <int STAGES, int KPS>
+int pair_clusters(const cudaLaunchConfig_t& cfg) {
+    static int cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (cached[dev] > 0) return cached[dev];
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<STAGES, KPS>, &cfg) != cudaSuccess) return 0;
+    cached[dev] = n;
+    return n;
+}
+
+template <int STAGES, int KPS>
+cudaError_t run_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
+                          const PairKParams& kp, cudaStream_t st) {
+    using C = PairCfg<STAGES, KPS>;
+    auto k = gemm_pair_kernel<STAGES, KPS>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(kGemmThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const int max_clusters = pair_clusters<STAGES, KPS>(cfg);
+    if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
+    const int tiles = kp.m_pairs * kp.n_tiles;
+    cfg.gridDim = dim3(2 * (tiles < max_clusters ? tiles : max_clusters));  // persistent: one pair per two SMs
+    cfg.numAttrs = st ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, kp);
 }
 
 }  // namespace
@@ -729,6 +1084,35 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     const int64_t b_pitch = pl.kind == 0 ? g.K : g.b.codes_ld;
     if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
     if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn)) return cudaErrorInvalidValue;
+    if (pl.kind == 0) {
+        // FP8: CTA pairs, 256 x 192 tiles (A: 128 rows per CTA, B: 96 rows per CTA)
+        CUtensorMap ma, mb, msa, msb;
+        const int64_t a_blocks = (g.M + kBM - 1) / kBM;
+        const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
+        if (!make_map(&ma, ws + pl.fp8_a, g.M, pl.k_bytes, g.K, kBM)) return cudaErrorInvalidValue;
+        if (!make_map(&mb, ws + pl.fp8_b, g.N, pl.k_bytes, g.K, pl.bn / 2)) return cudaErrorInvalidValue;
+        // scale chunks as rows of 128 x 32-bit words (one 512-byte chunk per row)
+        // (boxes of kPairKps rows: the chunks of the K tiles of one stage)
+        if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k),
+                           kChunkBytes, 128, kPairKps, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k),
+                           kChunkBytes, 128, kPairKps, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        PairKParams pk{};
+        pk.M = (int)g.M;
+        pk.N = (int)g.N;
+        pk.k_tiles = (int)pl.k_tiles;
+        pk.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
+        pk.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
+        pk.sf_chunks_k = pl.chunks_k;
+        pk.D = g.D;
+        pk.ldd = g.ldd;
+        pk.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
+        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp8, j);  // E5M2 x E5M2, M = 256
+        (void)num_sms;
+        return run_gemm_pair<kPairStages, kPairKps>(ma, mb, msa, msb, pk, st);
+    }
     GemmKParams kp{};
     kp.sfa = ws + pl.sfa;
     kp.sfb = ws + pl.sfb;
@@ -741,10 +1125,6 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     kp.D = g.D;
     kp.ldd = g.ldd;
     kp.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
-    if (pl.kind == 0) {
-        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp8, j);  // E5M2 x E5M2
-        return run_gemm<0, kBnFp8, 5>(ma, mb, kp, num_sms, st);
-    }
     if (pl.kind == 1) {
         for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x2, (j % 2) * 2);  // E2M1
         return run_gemm<1, kBnFp4x2, 5>(ma, mb, kp, num_sms, st);
