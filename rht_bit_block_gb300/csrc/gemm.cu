@@ -470,15 +470,6 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
         : "memory");
 }
 
-// nk consecutive 512-byte chunk rows: the chunk maps are encoded with a box
-// of KPS rows; with nk < KPS (last stage of an odd K) the box still lands
-// KPS rows, so the byte count expected is that of the full box.
-__device__ __forceinline__ void tma_load_pair_rows(uint32_t dst, const CUtensorMap* map, int row, int nk, uint32_t cbar,
-                                                   uint64_t pol) {
-    (void)nk;
-    tma_load_pair(dst, map, 0, row, cbar, pol);
-}
-
 __device__ __forceinline__ void mma_pair_fp8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                              uint32_t sfb, uint32_t accumulate) {
     asm volatile(
@@ -501,11 +492,30 @@ __device__ __forceinline__ void tc_commit_pair_local(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void tc_cp_scales_pair(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+// 128 lanes x 32 bytes (8 columns) from a 4 KB replicated-chunk block:
+// lane L reads 16-byte line L of the first 2 KB and of the second 2 KB.
+__device__ __forceinline__ void tc_cp_scales_pair_256(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// A stage holds KPS consecutive 128-byte K tiles ("atoms") of each operand.
+// No-swizzle K-major descriptor of that block: 8-row core matrices (128 B)
+// 128 bytes apart, the second 16-byte column 2048 bytes after the first.
+__device__ __forceinline__ uint64_t sf256_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(2048u >> 4) << 16;
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
+// A stage holds KPS consecutive 128-byte K tiles ("atoms") of each operand,
+// and the scale chunks of those K tiles in the replicated layout the prep
+// kernel writes for this path (each 512-byte chunk four times, so that one
+// tcgen05.cp .128x256b fills 8 tensor-memory columns of all 128 lanes): A's
+// chunks of K tiles kt, kt+1 side by side (one copy per two K tiles), B's two
+// 128-row parts of one K tile side by side (one copy per K tile).  The scale
+// stages come first in shared memory, the 1024-aligned operand stages after.
 template <int STAGES, int KPS>
 struct PairCfg {
     static constexpr int BN = kBnFp8;                    // output columns of a pair tile
@@ -514,23 +524,27 @@ struct PairCfg {
     static constexpr int kBAtom = kBRows * kBKBytes;     // 14 KB
     static constexpr int kABytes = KPS * kAAtom;
     static constexpr int kBBytes = KPS * kBAtom;
-    static constexpr int kSfaBytes = KPS * kChunkBytes;      // KPS chunks of this CTA's 128 rows
-    static constexpr int kSfbBytes = 2 * KPS * kChunkBytes;  // KPS chunks of each 128-row part of the BN B rows
-    static constexpr int kTxPerAtom = kAAtom + kBAtom;              // operand bytes per CTA per K tile
-    static constexpr int kTxScales = 3 * KPS * kChunkBytes;        // scale bytes per CTA per stage (full boxes)
-    static constexpr int kOffB = STAGES * kABytes;
-    static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
-    static constexpr int kOffSfb = kOffSfa + STAGES * kSfaBytes;
-    static constexpr int kOffBars = kOffSfb + STAGES * kSfbBytes;
+    static constexpr int kRep = 4 * kChunkBytes;             // one replicated chunk: 2 KB
+    static constexpr int kSfaBytes = KPS * kRep;             // this CTA's 128 rows, KPS K tiles
+    static constexpr int kSfbBytes = 2 * KPS * kRep;         // both 128-row parts of B, KPS K tiles
+    static constexpr int kTxPerAtom = kAAtom + kBAtom;       // operand bytes per CTA per K tile
+    static constexpr int kTxScales = kSfaBytes + kSfbBytes;  // scale bytes per CTA per stage (full boxes)
+    static constexpr int kOffSfa = 0;
+    static constexpr int kOffSfb = STAGES * kSfaBytes;
+    static constexpr int kOffA = kOffSfb + STAGES * kSfbBytes;
+    static constexpr int kOffB = kOffA + STAGES * kABytes;
+    static constexpr int kOffBars = kOffB + STAGES * kBBytes;
     static constexpr int kNumBars = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
     static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr int kSfaCol = 2 * BN;               // two sets of 4 columns
-    static constexpr int kSfbCol = 2 * BN + 8;           // two sets of 8 columns
+    static constexpr int kSfaCol = 2 * BN;               // two sets of 8 columns (K tiles kt, kt+1)
+    static constexpr int kSfbCol = 2 * BN + 16;          // two sets of 8 columns (parts 0, 1 of one K tile)
     static_assert(kSfbCol + 16 <= kTmemCols, "tensor memory overflow");
     static_assert(kSmem <= 232448, "shared memory overflow");
-    static_assert(kBAtom % 1024 == 0, "128B-swizzled tiles need 1024-byte alignment");
-    static_assert(BN % 32 == 0 && BN > 128 && BN <= 256, "two scale chunks of B; 32-column epilogue reads");
+    static_assert(kOffA % 1024 == 0 && kAAtom % 1024 == 0 && kBAtom % 1024 == 0,
+                  "128B-swizzled tiles need 1024-byte alignment");
+    static_assert(BN % 32 == 0 && BN > 128 && BN <= 256, "two scale parts of B; 32-column epilogue reads");
+    static_assert(KPS == 2, "one scale copy of A covers two K tiles");
 };
 
 struct PairKParams {
@@ -560,7 +574,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * C::kNumBars + 4);
-    auto stage_a = [&](int s) { return base + s * C::kABytes; };
+    auto stage_a = [&](int s) { return base + C::kOffA + s * C::kABytes; };
     auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
     auto stage_sfa = [&](int s) { return base + C::kOffSfa + s * C::kSfaBytes; };
     auto stage_sfb = [&](int s) { return base + C::kOffSfb + s * C::kSfbBytes; };
@@ -612,8 +626,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
             const int arow = ablk * kBM;
             const int brow = nb * C::BN + (int)peer * C::kBRows;
-            const int sfa_row = ablk * (int)p.sf_chunks_k;
-            const int sfb_row0 = (2 * nb) * (int)p.sf_chunks_k, sfb_row1 = (2 * nb + 1) * (int)p.sf_chunks_k;
+            // 512-byte rows of the replicated chunk arrays: 4 per K tile for A, 8 for B
+            const int sfa_row = ablk * p.k_tiles * 4;
+            const int sfb_row = nb * p.k_tiles * 8;
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
                     *abort_flag = 1;
@@ -627,10 +642,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     tma_load_pair(stage_a(s) + j * C::kAAtom, &tmap_a, (kt0 + j) * kBKBytes, arow, fb, keep);
                     tma_load_pair(stage_b(s) + j * C::kBAtom, &tmap_b, (kt0 + j) * kBKBytes, brow, fb, keep);
                 }
-                // chunks of consecutive K tiles are contiguous: one box of nk chunk rows each
-                tma_load_pair_rows(stage_sfa(s), &tmap_sfa, sfa_row + kt0, nk, fb, keep);
-                tma_load_pair_rows(stage_sfb(s), &tmap_sfb, sfb_row0 + kt0, nk, fb, keep);
-                tma_load_pair_rows(stage_sfb(s) + KPS * kChunkBytes, &tmap_sfb, sfb_row1 + kt0, nk, fb, keep);
+                // the scales of the stage's K tiles are contiguous: one box each
+                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * 4, fb, keep);
+                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * 8, fb, keep);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -641,7 +655,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // ------------------------------------------------ MMA issuer (leader only)
         int s = 0, tc = 0;
         uint32_t ph = 0;
-        int it = 0;  // K tiles issued so far (alternates the scale sets)
+        int it = 0;  // K tiles issued so far (alternates B's scale sets)
+        int sc = 0;  // stages issued so far (alternates A's scale sets)
         bool ok = true;
         for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++tc) {
             const int buf = tc & 1;
@@ -659,18 +674,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 tc_fence_after();
                 const int kt0 = ks * KPS;
                 const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
+                // A's scales of both K tiles of the stage: columns sfa_t (kt0) and sfa_t + 4 (kt0 + 1)
+                const uint32_t sfa_t = tmem + C::kSfaCol + (sc++ & 1) * 8;
+                tc_cp_scales_pair_256(sfa_t, sf256_desc(stage_sfa(s)));
                 for (int j = 0; j < nk; ++j, ++it) {
-                    const int set = it & 1;
-                    const uint32_t sfa_t = tmem + C::kSfaCol + set * 4;
-                    const uint32_t sfb_t = tmem + C::kSfbCol + set * 8;
-                    tc_cp_scales_pair(sfa_t, plain_desc(stage_sfa(s) + j * kChunkBytes));
-                    tc_cp_scales_pair(sfb_t, plain_desc(stage_sfb(s) + j * kChunkBytes));
-                    tc_cp_scales_pair(sfb_t + 4, plain_desc(stage_sfb(s) + (KPS + j) * kChunkBytes));
+                    // B's scales of this K tile: part 0 at sfb_t, part 1 at sfb_t + 4
+                    const uint32_t sfb_t = tmem + C::kSfbCol + (it & 1) * 8;
+                    tc_cp_scales_pair_256(sfb_t, sf256_desc(stage_sfb(s) + j * 2 * C::kRep));
                     const uint64_t da = sw128_desc(stage_a(s) + j * C::kAAtom);
                     const uint64_t db = sw128_desc(stage_b(s) + j * C::kBAtom);
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        mma_pair_fp8(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t, sfb_t,
+                        mma_pair_fp8(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t + 4 * j, sfb_t,
                                      (kt0 + j > 0 || q > 0) ? 1u : 0u);
                 }
                 tc_commit_pair_both(empty_bar(s));  // frees stage s in both CTAs
@@ -781,6 +796,19 @@ __device__ __forceinline__ int64_t chunk_row_offset(const PrepSide& s, int chunk
     return cb * chunks_k * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
 }
 
+// FP8 path: replicated chunks.  GEMM tile t (tile_rows rows), K tile kt and
+// 128-row part h of the tile own four copies of the 512-byte chunk at
+// (((t * k_tiles + kt) * parts + h) * 4 + copy) * 512, with row w and scale
+// cell j at (w % 32) * 16 + (w / 32) * 4 + j in each copy.  Returns the offset
+// of copy 0 for this row.
+__device__ __forceinline__ int64_t rep_chunk_offset(const PrepSide& s, int k_tiles, int row, int kt) {
+    const int parts = (s.tile_rows + 127) >> 7;
+    const int t = row / s.tile_rows;
+    const int rr = row - t * s.tile_rows;
+    const int h = rr >> 7, w = rr & 127;
+    return ((((int64_t)t * k_tiles + kt) * parts + h) * 4) * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
+}
+
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
     asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -801,7 +829,7 @@ __device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
 }
 
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
-// elements.  A CTA is 32 x 8 threads: each warp (threadIdx.y) owns one row,
+// elements (replicated chunk layout above).  A CTA is 32 x 8 threads: each warp (threadIdx.y) owns one row,
 // each lane one 32-element group of it (16 code bytes in, 32 FP8 bytes and one
 // scale byte of a 4-byte chunk cell out), so that every load and store of a
 // warp is contiguous.  blockIdx.x: 8-row slab, blockIdx.y: 32-group slab,
@@ -862,7 +890,9 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
         dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    s.out_chunks[chunk_row_offset(s, p.chunks_k, row) + (int64_t)(grp >> 2) * kChunkBytes + (grp & 3)] = (uint8_t)hw;
+    uint8_t* cell = s.out_chunks + rep_chunk_offset(s, p.chunks_k, row, grp >> 2) + (grp & 3);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) cell[r * kChunkBytes] = (uint8_t)hw;
 }
 
 // E2M1: only the scales move, into the chunk layout (hardware blocks of 16 or
@@ -953,10 +983,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
         pl.fp8_b = off;
         off = align256(off + (size_t)N * K);
     }
+    const size_t copies = pl.kind == 0 ? 4 : 1;  // FP8: replicated chunks
     pl.sfa = off;
-    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes);
+    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes * copies);
     pl.sfb = off;
-    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes);
+    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes * copies);
     pl.total = off;
     return pl;
 }
@@ -1092,12 +1123,14 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
         if (!make_map(&ma, ws + pl.fp8_a, g.M, pl.k_bytes, g.K, kBM)) return cudaErrorInvalidValue;
         if (!make_map(&mb, ws + pl.fp8_b, g.N, pl.k_bytes, g.K, pl.bn / 2)) return cudaErrorInvalidValue;
         // scale chunks as rows of 128 x 32-bit words (one 512-byte chunk per row)
-        // (boxes of kPairKps rows: the chunks of the K tiles of one stage)
-        if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k),
-                           kChunkBytes, 128, kPairKps, CU_TENSOR_MAP_SWIZZLE_NONE))
+        // (boxes: the replicated chunks of the K tiles of one stage, 4 rows per K tile for A, 8 for B)
+        if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128,
+                           (uint64_t)(a_blocks * pl.chunks_k * 4), kChunkBytes, 128, 4 * kPairKps,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
-        if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k),
-                           kChunkBytes, 128, kPairKps, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128,
+                           (uint64_t)(b_blocks * pl.chunks_k * 4), kChunkBytes, 128, 8 * kPairKps,
+                           CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
         PairKParams pk{};
         pk.M = (int)g.M;
