@@ -156,6 +156,23 @@ ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t
                               const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
                               const ufp4_qtensor* colwise, cudaStream_t stream);
 
+/* ufp4_rht_quantize_batch -- the row-wise ufp4_rht_quantize of `count`
+ * independent tensors that share one descriptor, in a single launch, e.g. the
+ * X and W operands of one FPROP GEMM [UFP4-method, quantized GEMM Y^ =
+ * Q_G(XH') Q_G(WH')^T: both operands are quantized along K].  Element i of
+ * each host array describes tensor i exactly as the arguments of
+ * ufp4_rht_quantize do (x: device bf16 rows[i] x cols[i], leading dimension
+ * ld[i]; rowwise[i]: its row-wise output).  Requirements: 0 <= count <=
+ * UFP4_MAX_BATCH, desc->out_mask == UFP4_OUT_ROWWISE, 1-D blocks, hadamard_n
+ * <= 128 (UFP4_ERR_UNSUPPORTED otherwise), and per tensor the shape and
+ * alignment rules of ufp4_rht_quantize.  The results are bit-identical to
+ * `count` separate ufp4_rht_quantize calls.  Nothing is written when any
+ * argument is rejected. */
+#define UFP4_MAX_BATCH 4
+ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const* x, const int64_t* rows, const int64_t* cols,
+                                    const int64_t* ld, const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
+                                    cudaStream_t stream);
+
 /* ufp4_rht_quantize_grouped -- the same for a stack of groups (MoE experts).
  *   x             device bf16 [total_rows x cols], leading dimension ld, the
  *                 rows of group g being offsets[g] .. offsets[g+1]-1

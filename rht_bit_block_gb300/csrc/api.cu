@@ -105,6 +105,51 @@ ufp4_status check_out(const ufp4_qtensor* q, int64_t rows, int64_t cols, const B
 ufp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? UFP4_OK : UFP4_ERR_CUDA; }
 
 // Shared body of the plain and grouped quantizer calls.
+// Row-wise quantization of `count` tensors in one launch of the lean kernel
+// (arguments already validated).
+ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* rows, const int64_t* cols,
+                                const int64_t* ld, const ufp4_quant_desc* desc, const BlockShape& bs,
+                                const ufp4_qtensor* rowwise, cudaStream_t stream) {
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
+    const int n = desc->hadamard_n;
+    int64_t tiles = 0;
+    int k = 0;
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] == 0 || cols[i] == 0) continue;  // empty tensors take no tiles
+        RowsTensor& T = p.t[k++];
+        T.x = (const uint16_t*)x[i];
+        T.ld = ld[i];
+        T.codes = (uint8_t*)rowwise[i].codes;
+        T.scales = (uint8_t*)rowwise[i].scales;
+        T.codes_ld = rowwise[i].codes_ld;
+        T.scales_ld = rowwise[i].scales_ld;
+        T.rows = (int)rows[i];
+        T.cols = (int)cols[i];
+        T.col_tiles = (int)((cols[i] + 127) / 128);
+        T.row_tiles = (int)((rows[i] + 127) / 128);
+        T.tile0 = (int)tiles;
+        tiles += (int64_t)T.col_tiles * T.row_tiles;
+    }
+    if (k == 0) return UFP4_OK;
+    if (tiles > 0x7FFFFFFF) return UFP4_ERR_UNSUPPORTED;
+    p.count = k;
+    p.num_tiles = (int)tiles;
+    p.n = n;
+    p.lbw = ilog2(bs.bw);
+    p.log4n = 0;
+    while ((1 << (2 * p.log4n)) < n) ++p.log4n;
+    p.pow4 = (1 << (2 * p.log4n)) == n;
+    p.stages = 2;  // 2 x 32 KB tiles per CTA, 3 CTAs per SM
+    p.inv_sqrt_n = inv_sqrt_n(n);
+    make_sign_bits(desc->sign_seed, n, p.sign_bits);
+    p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
+    p.group = desc->group;
+    return cuda_status(launch_quantize_rows(p, desc->grid, desc->round == UFP4_ROUND_SR,
+                                            desc->scale_fmt == UFP4_SCALE_UE8M0, num_sms_current(), stream));
+}
+
 ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64_t* offsets, int ngroups,
                             bool grouped, const ufp4_quant_desc* desc, const ufp4_qtensor* rowwise,
                             const ufp4_qtensor* colwise, cudaStream_t stream) {
@@ -150,6 +195,11 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
         if (st != UFP4_OK) return st;
     }
     if (total_rows == 0 || cols == 0) return UFP4_OK;
+
+    if (do_row && !do_col && !bs.is2d && !grouped && n <= 128 && total_rows < (1LL << 31) && cols < (1LL << 31)) {
+        const ufp4_qtensor* rw = rowwise;
+        return quantize_rows_batch(1, &x, &total_rows, &cols, &ld, desc, bs, rw, stream);
+    }
 
     QuantParams p;
     std::memset(&p, 0, sizeof(p));
@@ -288,6 +338,31 @@ ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t
     if (desc->group < 0) return UFP4_ERR_INVALID_ARG;
     const int64_t offsets[2] = {0, rows};
     return quantize_common(x, cols, ld, offsets, 1, false, desc, rowwise, colwise, stream);
+}
+
+extern "C" ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const* x, const int64_t* rows,
+                                               const int64_t* cols, const int64_t* ld, const ufp4_quant_desc* desc,
+                                               const ufp4_qtensor* rowwise, cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (count < 0 || count > UFP4_MAX_BATCH) return UFP4_ERR_INVALID_ARG;
+    if (count == 0) return UFP4_OK;
+    if (!x || !rows || !cols || !ld || !rowwise) return UFP4_ERR_INVALID_ARG;
+    if (desc->out_mask != UFP4_OUT_ROWWISE) return UFP4_ERR_INVALID_ARG;
+    if (bs.is2d || desc->hadamard_n > 128) return UFP4_ERR_UNSUPPORTED;
+    const int n = desc->hadamard_n;
+    for (int i = 0; i < count; ++i) {
+        if (rows[i] < 0 || cols[i] < 0 || ld[i] < cols[i]) return UFP4_ERR_INVALID_ARG;
+        if (rows[i] >= (1LL << 31) || cols[i] >= (1LL << 31)) return UFP4_ERR_UNSUPPORTED;
+        if (rows[i] == 0 || cols[i] == 0) continue;
+        if (!x[i]) return UFP4_ERR_INVALID_ARG;
+        if (!aligned(x[i], 16) || ld[i] % 8) return UFP4_ERR_ALIGNMENT;
+        if (cols[i] % 16 || cols[i] % n || cols[i] % bs.bw) return UFP4_ERR_INVALID_ARG;
+        st = check_out(&rowwise[i], rows[i], cols[i], bs, desc->scale_fmt, false);
+        if (st != UFP4_OK) return st;
+    }
+    return quantize_rows_batch(count, x, rows, cols, ld, desc, bs, rowwise, stream);
 }
 
 int64_t ufp4_grouped_padded_rows(int64_t rows, const ufp4_quant_desc* desc) {

@@ -839,12 +839,13 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
     griddep_launch();
     const PrepSide& s = p.side[blockIdx.z];
     const int row = blockIdx.x * 8 + threadIdx.y;
-    if (row >= s.rows_cover) return;
-    const int grp = blockIdx.y * 32 + threadIdx.x;  // 32-element group along K
-    if (grp >= p.chunks_k * 4) return;               // groups covered by the chunk cells
+    if (row >= s.rows_cover) return;                 // whole warps
+    const int lane = threadIdx.x;
+    const int grp = blockIdx.y * 32 + lane;          // 32-element group along K
+    const bool in_cells = grp < p.chunks_k * 4;      // groups covered by the chunk cells (whole 4-lane sets)
     const int k0 = grp * 32;
     int hw = 0;
-    if (row < s.rows && k0 < p.K) {
+    if (in_cells && row < s.rows && k0 < p.K) {
         const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
         const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
         const uint4 cw = *reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld + grp * 16);
@@ -890,9 +891,14 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
         dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    uint8_t* cell = s.out_chunks + rep_chunk_offset(s, p.chunks_k, row, grp >> 2) + (grp & 3);
-#pragma unroll
-    for (int r = 0; r < 4; ++r) cell[r * kChunkBytes] = (uint8_t)hw;
+    // lanes 4c .. 4c+3 hold the four scale bytes of one chunk cell: gather
+    // the word, then lane 4c + r writes copy r of it
+    const uint32_t v = (uint32_t)hw << (8 * (lane & 3));
+    uint32_t word = v | __shfl_xor_sync(0xFFFFFFFFu, v, 1);
+    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
+    if (in_cells)
+        *reinterpret_cast<uint32_t*>(s.out_chunks + rep_chunk_offset(s, p.chunks_k, row, grp >> 2) +
+                                     (lane & 3) * kChunkBytes) = word;
 }
 
 // E2M1: only the scales move, into the chunk layout (hardware blocks of 16 or

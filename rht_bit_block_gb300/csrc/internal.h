@@ -78,6 +78,31 @@ struct QuantParams {
 
 cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
                             int64_t total_rows, int num_sms, cudaStream_t st);
+
+// Row-wise only, 1-D blocks, n <= 128: the lean kernel, over up to
+// kMaxBatch independent tensors in one launch.
+constexpr int kMaxBatch = 4;
+struct RowsTensor {
+    const uint16_t* x;  // host side only (the kernel reads through its tensor map)
+    int64_t ld;         // elements
+    uint8_t* codes;
+    uint8_t* scales;
+    int64_t codes_ld;   // bytes
+    int64_t scales_ld;  // elements
+    int rows, cols;
+    int col_tiles, row_tiles;
+    int tile0;          // first tile of this tensor in the launch
+};
+struct RowsParams {
+    RowsTensor t[kMaxBatch];
+    int count, num_tiles;
+    int n, lbw, pow4, log4n, stages;
+    float inv_sqrt_n;
+    uint32_t sign_bits[8];
+    uint64_t sr_seed;
+    int group;
+};
+cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int num_sms, cudaStream_t st);
 cudaError_t quant_error_read_clear(int* value);
 
 // 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,

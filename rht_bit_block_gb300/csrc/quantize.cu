@@ -16,6 +16,7 @@
 //    one 32-bit shared load per row, and runs them through the same steps;
 //  * 2-D b x b blocks reduce their amax through shared-memory atomics.
 #include <cstdint>
+#include <cstring>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -561,6 +562,169 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         }
 }
 
+// ------------------------------------------------------ row-wise (lean)
+// Row-wise quantization with 1-D blocks and n <= 128, the FPROP operands'
+// case, over up to kMaxBatch independent tensors in one launch (their tiles
+// are numbered one after the other).  Same steps as the row pass above, with
+// 128 x 128 tiles fixed at compile time, tile coordinates and output pointers
+// advanced without division, and per-row bounds checks only on ragged tiles.
+struct RowsMaps {
+    CUtensorMap m[kMaxBatch];
+};
+
+template <int GRID, bool SR, bool PO2>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
+    constexpr int TC = 128, TR = 128;
+    constexpr int kTileBytes = TR * TC * 2;
+    constexpr int SZ = PO2 ? 1 : 4;
+    constexpr int kCPR = TC / kChunk;      // 16-element chunks per tile row
+    constexpr int kRPI = kThreads / kCPR;  // tile rows per thread step
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+    uint8_t* base = smem_raw + pad;
+    const int kStages = p.stages;
+    const uint32_t bars = smem_addr(base + kStages * kTileBytes);
+    const int tid = threadIdx.x;
+    const int cchunk = tid % kCPR;
+    const int r0 = tid / kCPR;
+    const int n = p.n;
+    Fold fd;
+    fd.inv_s = p.inv_sqrt_n;
+    fd.pow4 = p.pow4;
+    fd.j = p.log4n;
+    const int seg_row = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
+    SignMasks mrow;
+    {
+        const int pos = (cchunk * kChunk) & 255;
+        make_masks((p.sign_bits[pos >> 5] >> (pos & 31)) & 0xFFFFu, mrow);
+    }
+    const int lbw = p.lbw;
+
+    // tensor and tile coordinates of a tile index
+    auto locate = [&](int tile, int& t, int& rt, int& ct) {
+        t = 0;
+        while (t + 1 < p.count && tile >= p.t[t + 1].tile0) ++t;
+        const int local = tile - p.t[t].tile0;
+        rt = local / p.t[t].col_tiles;
+        ct = local - rt * p.t[t].col_tiles;
+    };
+    auto issue = [&](int tile, int s) {
+        int t, rt, ct;
+        locate(tile, t, rt, ct);
+        const uint32_t bar = bars + 8u * s;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(smem_addr(base + s * kTileBytes)), "l"((uint64_t)&maps.m[t]), "r"(ct * TC), "r"(rt * TR), "r"(bar)
+            : "memory");
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    griddep_wait();
+    griddep_launch();
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int tile = blockIdx.x + s * gridDim.x;
+            if (tile < p.num_tiles) issue(tile, s);
+        }
+
+    int t = 0, rt = 0, ct = 0, step_r = 0, step_c = 0;
+    auto relocate = [&](int tile) {
+        locate(tile, t, rt, ct);
+        step_r = (int)gridDim.x / p.t[t].col_tiles;
+        step_c = (int)gridDim.x - step_r * p.t[t].col_tiles;
+    };
+    if ((int)blockIdx.x < p.num_tiles) relocate(blockIdx.x);
+    int s = 0;
+    uint32_t phase = 0;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++i) {
+        if (i) {
+            ct += step_c;
+            rt += step_r;
+            if (ct >= p.t[t].col_tiles) {
+                ct -= p.t[t].col_tiles;
+                ++rt;
+            }
+            if (rt >= p.t[t].row_tiles) relocate(tile);  // into the next tensor
+        }
+        const bool landed = wait_phase(bars + 8u * s, phase);
+        if (!__syncthreads_and(landed)) {
+            if (tid == 0) atomicExch(&g_quant_error, 1);
+            break;
+        }
+        const RowsTensor& T = p.t[t];
+        const uint16_t* tile_s = reinterpret_cast<const uint16_t*>(base + s * kTileBytes);
+        const int row0 = rt * TR;
+        const int col = ct * TC + cchunk * kChunk;
+        const bool col_ok = col < T.cols;
+        const int left = T.rows - row0 - r0;  // rows of this thread's first row onward
+        const bool full = T.rows - row0 >= TR;
+        uint8_t* cp = T.codes + (int64_t)(row0 + r0) * T.codes_ld + (col >> 1);
+        uint8_t* sp = T.scales + ((int64_t)(row0 + r0) * T.scales_ld + (col >> lbw)) * SZ;
+        const int64_t cstep = (int64_t)kRPI * T.codes_ld;
+        const int64_t sstep = (int64_t)kRPI * T.scales_ld * SZ;
+        const bool wsc = (col & ((1 << lbw) - 1)) == 0;
+        const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
+#pragma unroll
+        for (int it = 0; it < TR / (2 * kRPI); ++it) {
+            const int ra = 2 * kRPI * it;
+            uint32_t wa[8], wb[8];
+            uint64_t e[16];
+            const uint4* pa = reinterpret_cast<const uint4*>(src + ra * TC);
+            const uint4* pb = reinterpret_cast<const uint4*>(src + (ra + kRPI) * TC);
+            const uint4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
+            wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
+            wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+            wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
+            wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+            widen_rows(wa, wb, mrow, e);
+            fwht_pair(e, n, seg_row);
+            float Ma, Mb;
+            amax_1d_pair(e, 1 << lbw, Ma, Mb);
+            Dest A, B;
+            A.codes = cp + (2 * it) * cstep;
+            B.codes = A.codes + cstep;
+            A.s0 = A.s1 = sp + (2 * it) * sstep;
+            B.s0 = B.s1 = A.s0 + sstep;
+            A.valid = col_ok && (full || ra < left);
+            B.valid = col_ok && (full || ra + kRPI < left);
+            A.w0 = B.w0 = wsc;
+            A.w1 = B.w1 = false;
+            A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
+            B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
+            emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, (uint32_t)p.group);
+        }
+        // everyone is done with stage s: refill it
+        __syncthreads();
+        if (tid == 0) {
+            const int next = tile + kStages * gridDim.x;
+            if (next < p.num_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, s);
+            }
+        }
+        if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+    // a broken-off loop leaves copies in flight: let them land (bounded)
+    if (tid == 0)
+        for (int k = i; k < i + kStages; ++k) {
+            const int tile = blockIdx.x + k * gridDim.x;
+            if (tile >= p.num_tiles) break;
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1));
+        }
+}
+
 // ------------------------------------------------------------- RHT only
 __global__ void __launch_bounds__(kThreads)
 rht_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, float inv_sqrt_n,
@@ -632,6 +796,39 @@ cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, i
     UFP4_Q(1)
     UFP4_Q(2)
 #undef UFP4_Q
+    return cudaErrorInvalidValue;
+}
+
+template <int GRID, bool SR, bool PO2>
+static cudaError_t launch_rows(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
+    const size_t smem = (size_t)p.stages * 128 * 128 * 2 + 8 * p.stages + 128;
+    auto k = quantize_rows_kernel<GRID, SR, PO2>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < kCtasPerSm * num_sms ? p.num_tiles : kCtasPerSm * num_sms;
+    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
+}
+
+cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int num_sms, cudaStream_t st) {
+    RowsMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int t = 0; t < p.count; ++t) {
+        const RowsTensor& T = p.t[t];
+        if (!encode_map_2d(&maps.m[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, T.x, (uint64_t)T.cols, (uint64_t)T.rows,
+                           (uint64_t)T.ld * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+#define UFP4_R(G)                                                                              \
+    if (grid == G) {                                                                           \
+        if (sr) return po2 ? launch_rows<G, true, true>(maps, p, num_sms, st)                  \
+                           : launch_rows<G, true, false>(maps, p, num_sms, st);                \
+        return po2 ? launch_rows<G, false, true>(maps, p, num_sms, st)                         \
+                   : launch_rows<G, false, false>(maps, p, num_sms, st);                       \
+    }
+    UFP4_R(0)
+    UFP4_R(1)
+    UFP4_R(2)
+#undef UFP4_R
     return cudaErrorInvalidValue;
 }
 

@@ -28,7 +28,9 @@ EXPORTED = (
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
     "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
+    "ufp4_rht_quantize_batch",
 )
+MAX_BATCH = 4
 
 
 class QuantDesc(ctypes.Structure):
@@ -64,6 +66,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     QD, QT = ctypes.POINTER(QuantDesc), ctypes.POINTER(QTensor)
     L.ufp4_rht_quantize.argtypes = [P, i64, i64, i64, QD, QT, QT, P]
     L.ufp4_rht_quantize_grouped.argtypes = [P, i64, i64, ctypes.POINTER(i64), i32, QD, QT, QT, P]
+    L.ufp4_rht_quantize_batch.argtypes = [i32, ctypes.POINTER(P), ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                          ctypes.POINTER(i64), QD, QT, P]
     L.ufp4_grouped_padded_rows.argtypes = [i64, QD]
     L.ufp4_grouped_padded_rows.restype = i64
     L.ufp4_rht_transform.argtypes = [P, i64, i64, i64, i32, u64, P, i64, P]
@@ -120,6 +124,19 @@ def ufp4_rht_quantize(x, desc: QuantDesc, rowwise: QTensor | None, colwise: QTen
                                     ctypes.byref(rowwise) if rowwise is not None else None,
                                     ctypes.byref(colwise) if colwise is not None else None,
                                     _stream(stream)), "ufp4_rht_quantize")
+
+
+def ufp4_rht_quantize_batch(xs, desc: QuantDesc, rowwise, stream=None):
+    """Row-wise quantization of several 2-D bf16 tensors sharing `desc`, one launch."""
+    k = len(xs)
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    ptrs = (P * max(k, 1))(*[x.data_ptr() for x in xs])
+    rows = (I64 * max(k, 1))(*[x.shape[0] for x in xs])
+    cols = (I64 * max(k, 1))(*[x.shape[1] for x in xs])
+    lds = (I64 * max(k, 1))(*[x.stride(0) for x in xs])
+    outs = (QTensor * max(k, 1))(*rowwise)
+    _check(load().ufp4_rht_quantize_batch(k, ptrs, rows, cols, lds, ctypes.byref(desc), outs, _stream(stream)),
+           "ufp4_rht_quantize_batch")
 
 
 def ufp4_rht_quantize_grouped(x, offsets, desc: QuantDesc, rowwise: QTensor | None, colwise: QTensor | None,

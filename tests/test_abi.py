@@ -78,3 +78,21 @@ def test_gemm_rejects_fp32_scales(lib):
     A = ufp4.QTensor(0x2000, 0x3000, 128, 128, 64, 8)
     D = ctypes.c_void_p(0x4000)
     assert lib.ufp4_gemm(ctypes.byref(A), ctypes.byref(A), ctypes.byref(desc), D, 128, None, 0, None) == 2
+
+
+def test_batch_validation_rejects_bad_arguments(lib):
+    """ufp4_rht_quantize_batch checks every tensor before anything is launched."""
+    P, I64 = ctypes.c_void_p, ctypes.c_int64
+    def call(desc, count=2, xs=(0x1000, 0x9000), rows=(64, 64), cols=(64, 64), lds=(64, 64)):
+        q = (ufp4.QTensor * 2)(*[ufp4.QTensor(0x2000, 0x3000, r, c, c // 2, c // 16) for r, c in zip(rows, cols)])
+        return lib.ufp4_rht_quantize_batch(count, (P * 2)(*xs), (I64 * 2)(*rows), (I64 * 2)(*cols),
+                                           (I64 * 2)(*lds), ctypes.byref(desc), q, None)
+    ok = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)
+    assert call(ok, count=0) == 0                                          # nothing to do
+    assert call(ok, count=ufp4.MAX_BATCH + 1) == 1                          # too many tensors
+    assert call(ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)) == 1  # row-wise only
+    assert call(ufp4.make_desc(n=256, out_mask=ufp4.OUT_ROWWISE)) == 2     # n > 128
+    assert call(ufp4.make_desc(block=(32, 32), scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)) == 2
+    assert call(ok, xs=(0x1000, 0x9001)) == 3                              # second input misaligned
+    assert call(ok, cols=(64, 72), lds=(64, 72)) == 1                      # cols not a multiple of 16
+    assert call(ok, lds=(64, 32)) == 1                                     # ld < cols

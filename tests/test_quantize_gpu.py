@@ -250,3 +250,45 @@ def test_large_sweep_sampled_rows(n):
             assert_bitwise(got["row"][0][r0:r0 + 64], c, f"{grid} {block} band {b} codes")
             br = block[0]
             assert_bitwise(got["row"][1][r0 // br:(r0 + 64) // br], s, f"{grid} {block} band {b} scales")
+
+
+# ----------------------------------------- row-wise kernel and batched calls
+# Row-wise calls with 1-D blocks and n <= 128 run the lean row kernel; these
+# cover its ragged row and column tiles, padded leading dimensions and every
+# rounding and scale mode.
+@pytest.mark.parametrize("grid", GRIDS)
+@pytest.mark.parametrize("rounding", [RTNE, SR])
+@pytest.mark.parametrize("block,n,cols", [((1, 16), 16, 576), ((1, 32), 64, 576), ((1, 16), 128, 640),
+                                          ((1, 32), 1, 544)])
+def test_rowwise_ragged_tiles(grid, rounding, block, n, cols):
+    x = inputs.tiny_check(300, cols)
+    fmt = PO2 if grid == "e2m1" else FP32
+    _check(x, grid=grid, block=block, n=n, sign_seed=21, rounding=rounding, sr_seed=8, scale_fmt=fmt,
+           ld=cols + 64, group=2)
+
+
+@pytest.mark.parametrize("rounding", [RTNE, SR])
+@pytest.mark.parametrize("grid", ["e1m2", "e2m1"])
+def test_batch_matches_oracle_and_single_calls(rounding, grid):
+    """ufp4_rht_quantize_batch over tensors of different shapes (one empty)
+    equals the oracle per tensor and the separate single calls, bit for bit."""
+    shapes = [(300, 576), (128, 1024), (0, 64), (1000, 192)]
+    xs = [inputs.tiny_check(r, c) if r else np.zeros((0, c), np.uint16) for r, c in shapes]
+    kw = dict(grid=grid, block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, rounding=rounding,
+              sr_seed=inputs.SR_SEED, scale_fmt=PO2, group=3)
+    desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE, **kw)
+    devs = [to_dev(x) for x in xs]
+    bufs = [ufp4.alloc_quantized(r, c, desc, "cuda") for r, c in shapes]
+    qts = [ufp4.qtensor(cb, sb, r, c) for (cb, sb), (r, c) in zip(bufs, shapes)]
+    ufp4.ufp4_rht_quantize_batch(devs, desc, qts)
+    torch.cuda.synchronize()
+    assert ufp4.ufp4_device_error() == 0
+    for x, dv, (cb, sb), (r, c) in zip(xs, devs, bufs, shapes):
+        if r == 0:
+            continue
+        oc, osc = orc.quantize(x, **kw)
+        assert_bitwise(cb.cpu().numpy(), oc, f"batch codes {r}x{c}")
+        assert_bitwise(sb.cpu().numpy(), osc, f"batch scales {r}x{c}")
+        single = gpu_quantize(dv, out_mask=ufp4.OUT_ROWWISE, **kw)["row"]
+        assert_bitwise(cb.cpu().numpy(), single[0], "batch vs single codes")
+        assert_bitwise(sb.cpu().numpy(), single[1], "batch vs single scales")
