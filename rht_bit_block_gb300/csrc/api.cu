@@ -156,9 +156,10 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     BlockShape bs;
     ufp4_status st = check_desc(desc, &bs);
     if (st != UFP4_OK) return st;
-    if (cols < 0 || ld < cols || ngroups < 1 || ngroups > kMaxGroups) return UFP4_ERR_INVALID_ARG;
+    if (cols < 0 || ngroups < 1 || ngroups > kMaxGroups) return UFP4_ERR_INVALID_ARG;
     if (desc->out_mask < 1 || desc->out_mask > 3) return UFP4_ERR_INVALID_ARG;
-    if (offsets[ngroups] == 0 || cols == 0) return UFP4_OK;  // empty input: nothing to do (pointers may be null)
+    if (offsets[ngroups] == 0 || cols == 0) return UFP4_OK;  // empty input: nothing to do (pointers, ld unused)
+    if (ld < cols) return UFP4_ERR_INVALID_ARG;
     if (!x) return UFP4_ERR_INVALID_ARG;
     const bool do_row = desc->out_mask & UFP4_OUT_ROWWISE;
     const bool do_col = desc->out_mask & UFP4_OUT_COLWISE;
@@ -353,9 +354,10 @@ extern "C" ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const*
     if (bs.is2d || desc->hadamard_n > 128) return UFP4_ERR_UNSUPPORTED;
     const int n = desc->hadamard_n;
     for (int i = 0; i < count; ++i) {
-        if (rows[i] < 0 || cols[i] < 0 || ld[i] < cols[i]) return UFP4_ERR_INVALID_ARG;
+        if (rows[i] < 0 || cols[i] < 0) return UFP4_ERR_INVALID_ARG;
         if (rows[i] >= (1LL << 31) || cols[i] >= (1LL << 31)) return UFP4_ERR_UNSUPPORTED;
-        if (rows[i] == 0 || cols[i] == 0) continue;
+        if (rows[i] == 0 || cols[i] == 0) continue;  // empty: its pointers and leading dimension are not used
+        if (ld[i] < cols[i]) return UFP4_ERR_INVALID_ARG;
         if (!x[i]) return UFP4_ERR_INVALID_ARG;
         if (!aligned(x[i], 16) || ld[i] % 8) return UFP4_ERR_ALIGNMENT;
         if (cols[i] % 16 || cols[i] % n || cols[i] % bs.bw) return UFP4_ERR_INVALID_ARG;

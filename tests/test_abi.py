@@ -96,3 +96,5 @@ def test_batch_validation_rejects_bad_arguments(lib):
     assert call(ok, xs=(0x1000, 0x9001)) == 3                              # second input misaligned
     assert call(ok, cols=(64, 72), lds=(64, 72)) == 1                      # cols not a multiple of 16
     assert call(ok, lds=(64, 32)) == 1                                     # ld < cols
+    # an empty tensor's pointer and leading dimension are not looked at
+    assert call(ok, count=1, xs=(0, 0), rows=(0, 0), lds=(1, 1)) == 0
