@@ -63,7 +63,12 @@ typedef enum {
  *   E2M1: 0, 0.5, 1, 1.5, 2, 3, 4, 6 (non-uniform, largest level 6)
  * Nibble encodings: E1M2 and E2M1 are sign << 3 | index (a zero level is
  * always written as 0x0); INT4 is the two's complement of the signed level. */
-typedef enum { UFP4_GRID_E1M2 = 0, UFP4_GRID_INT4 = 1, UFP4_GRID_E2M1 = 2 } ufp4_grid;
+/* UFP4_GRID_E2M1_R2: range-limited E2M1 -- blocks scaled so that amax maps to
+ * 2 and rounded to E2M1's uniform levels 0, 0.5, 1, 1.5, 2 only; the codes
+ * are E2M1 codes, so the GEMM runs on the native FP4 path (a reading of the
+ * UFP4 summary, section 实验: a uniform grid cannot simply be substituted on
+ * FP4 hardware). */
+typedef enum { UFP4_GRID_E1M2 = 0, UFP4_GRID_INT4 = 1, UFP4_GRID_E2M1 = 2, UFP4_GRID_E2M1_R2 = 3 } ufp4_grid;
 
 /* Rounding [UFP4-data; UFP4-method: RTNE for X and W, SR for dY]:
  *   RTNE: nearest level, exact ties to the even index.

@@ -14,10 +14,10 @@ _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
 
-E1M2, INT4, E2M1 = 0, 1, 2
+E1M2, INT4, E2M1, E2M1_R2 = 0, 1, 2, 3
 RTNE, SR = 0, 1
 SCALE_FP32, SCALE_UE8M0 = 0, 1
-GRID_NAMES = {"e1m2": E1M2, "int4": INT4, "e2m1": E2M1}
+GRID_NAMES = {"e1m2": E1M2, "int4": INT4, "e2m1": E2M1, "e2m1r2": E2M1_R2}
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
 
@@ -57,6 +57,8 @@ def lib():
         L.orc_level.restype = ctypes.c_double
         L.orc_qmax.argtypes = [i32]
         L.orc_qmax.restype = ctypes.c_double
+        L.orc_num_levels.argtypes = [i32]
+        L.orc_num_levels.restype = i32
         L.orc_po2_exponent.argtypes = [ctypes.c_float, i32]
         L.orc_po2_exponent.restype = i32
         L.orc_round_rtne.argtypes = [i32, ctypes.c_float]
@@ -96,6 +98,11 @@ def level(grid, idx: int) -> float:
 
 def qmax(grid) -> float:
     return lib().orc_qmax(_grid(grid))
+
+
+def num_levels(grid) -> int:
+    """Number of non-negative levels the grid rounds to (qmax is the last)."""
+    return lib().orc_num_levels(_grid(grid))
 
 
 def po2_exponent(M: float, grid) -> int:

@@ -41,7 +41,7 @@
 #include <stdlib.h>
 #include <string.h>
 
-enum { ORC_E1M2 = 0, ORC_INT4 = 1, ORC_E2M1 = 2 };
+enum { ORC_E1M2 = 0, ORC_INT4 = 1, ORC_E2M1 = 2, ORC_E2M1_R2 = 3 };
 enum { ORC_RTNE = 0, ORC_SR = 1 };
 enum { ORC_SCALE_FP32 = 0, ORC_SCALE_UE8M0 = 1 };
 
@@ -51,15 +51,24 @@ enum { ORC_SCALE_FP32 = 0, ORC_SCALE_UE8M0 = 1 };
  *  E1M2: 1 exponent bit, 2 mantissa bits -> 0, 0.25, ..., 1.75 (uniform).
  *  INT4: integers 0..7 (symmetric range -7..7; -8 is not used).
  *  E2M1: 2 exponent bits, 1 mantissa bit -> 0,0.5,1,1.5,2,3,4,6 (non-uniform).
+ *  E2M1_R2: the range-limited use of E2M1 -- only its levels up to 2, i.e. the
+ *  uniform sub-grid 0, 0.5, 1, 1.5, 2 (blocks scaled so that amax maps to 2),
+ *  so the codes stay native E2M1 codes.  A reading of the UFP4 summary,
+ *  section "实验" (a uniform grid cannot simply be substituted on native FP4
+ *  hardware): the uniform part of E2M1 is what such a substitution can use.
+ * NLEV is the number of levels a grid rounds to; the last one is qmax.
  */
-static const double LEVELS[3][8] = {
+static const double LEVELS[4][8] = {
     {0.0, 0.25, 0.5, 0.75, 1.0, 1.25, 1.5, 1.75},
     {0.0, 1.0, 2.0, 3.0, 4.0, 5.0, 6.0, 7.0},
     {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0},
+    {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0},
 };
+static const int NLEV[4] = {8, 8, 8, 5};
 
 double orc_level(int grid, int idx) { return LEVELS[grid][idx]; }
-double orc_qmax(int grid) { return LEVELS[grid][7]; }
+double orc_qmax(int grid) { return LEVELS[grid][NLEV[grid] - 1]; }
+int orc_num_levels(int grid) { return NLEV[grid]; }
 
 /* ----------------------------------------------------------- Philox4x32-10
  * Counter-based generator of Salmon, Moraes, Dror, Shaw, "Parallel random
@@ -188,7 +197,7 @@ int orc_round_rtne(int grid, float a) {
     double x = (double)a;
     int best = 0;
     double best_d = fabs(x - LEVELS[grid][0]);
-    for (int i = 1; i < 8; ++i) {
+    for (int i = 1; i < NLEV[grid]; ++i) {
         double d = fabs(x - LEVELS[grid][i]);
         if (d < best_d || (d == best_d && (i % 2) == 0 && (best % 2) != 0)) {
             best = i;
@@ -205,9 +214,9 @@ int orc_round_rtne(int grid, float a) {
 int orc_round_sr(int grid, float a, uint32_t u16) {
     double x = (double)a;
     int lo = 0;
-    for (int i = 0; i < 8; ++i)
+    for (int i = 0; i < NLEV[grid]; ++i)
         if (LEVELS[grid][i] <= x) lo = i;
-    if (lo == 7) return 7;
+    if (lo == NLEV[grid] - 1) return lo;
     double p = (x - LEVELS[grid][lo]) / (LEVELS[grid][lo + 1] - LEVELS[grid][lo]);
     return ((double)u16 < p * 65536.0) ? lo + 1 : lo;
 }
@@ -254,7 +263,7 @@ int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                       int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
                       uint64_t sr_seed, int scale_fmt, uint32_t stream, uint32_t group,
                       uint64_t row0, uint8_t* codes, void* scales) {
-    if (grid < 0 || grid > 2 || block_rows < 1 || block_cols < 2 || cols % 2) return 1;
+    if (grid < 0 || grid > 3 || block_rows < 1 || block_cols < 2 || cols % 2) return 1;
     if (rows % block_rows || cols % block_cols) return 1;
     float* z = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
     if (!z) return 1;

@@ -73,7 +73,7 @@ struct BlockShape {
 
 ufp4_status check_desc(const ufp4_quant_desc* d, BlockShape* bs) {
     if (!d) return UFP4_ERR_INVALID_ARG;
-    if (d->grid < 0 || d->grid > 2 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 1)
+    if (d->grid < 0 || d->grid > 3 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 1)
         return UFP4_ERR_INVALID_ARG;
     if (!is_pow2(d->hadamard_n) || d->hadamard_n > 256) return UFP4_ERR_INVALID_ARG;
     if (d->block_rows == 1 && (d->block_cols == 16 || d->block_cols == 32)) {

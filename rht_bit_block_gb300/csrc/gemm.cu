@@ -974,9 +974,9 @@ int ilog2(int v) {  // v a power of two
 Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
     Plan pl{};
     (void)br;
-    pl.kind = grid == 2 ? (bc == 16 ? 2 : 1) : 0;
+    pl.kind = grid >= 2 ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
     pl.bn = pl.kind == 0 ? kBnFp8 : (pl.kind == 1 ? kBnFp4x2 : kBnFp4x4);
-    pl.k_bytes = grid == 2 ? K / 2 : K;
+    pl.k_bytes = grid >= 2 ? K / 2 : K;
     pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
     const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
     pl.chunks_k = pl.k_tiles * cps;
@@ -1072,8 +1072,8 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, i
 
 // Operand preparation: FP8 widening (E1M2/INT4) and scale chunks into the workspace.
 cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
-    if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
+    if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
@@ -1109,8 +1109,8 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.
 cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
-    if (g.K % 32 && !(g.grid == 2 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && g.grid == 2) return cudaErrorNotSupported;
+    if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;

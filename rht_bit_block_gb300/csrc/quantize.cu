@@ -117,7 +117,7 @@ __device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uin
         const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
         const float ti = t[i];
         uint32_t idx;
-        if (GRID == 2) {
+        if (GRID >= 2) {
             const float a = fminf(fabsf(ti), qmax);
             const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
             const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
@@ -795,6 +795,7 @@ cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, i
     UFP4_Q(0)
     UFP4_Q(1)
     UFP4_Q(2)
+    UFP4_Q(3)
 #undef UFP4_Q
     return cudaErrorInvalidValue;
 }
@@ -828,6 +829,7 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int
     UFP4_R(0)
     UFP4_R(1)
     UFP4_R(2)
+    UFP4_R(3)
 #undef UFP4_R
     return cudaErrorInvalidValue;
 }

@@ -20,7 +20,7 @@ constexpr int kChunk = 16;  // elements one thread carries along the quantized d
 
 // Largest level and its reciprocal step for each grid (E1M2 1.75, INT4 7, E2M1 6).
 __host__ __device__ constexpr float grid_qmax(int grid) {
-    return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : 6.0f);
+    return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : (grid == 2 ? 6.0f : 2.0f));
 }
 
 // ------------------------------------------------------------- Philox4x32-10
@@ -118,8 +118,8 @@ __device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float&
 template <int GRID>
 __device__ __forceinline__ int scale_po2(float M, float& r) {
     const uint32_t b = __float_as_uint(M);
-    constexpr int Eq = (GRID == 0) ? 0 : 2;
-    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : 0x600000u;  // 1.5 or 1.75
+    constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : 2);
+    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : 0x600000u);  // 1.5, 1.0 or 1.75
     int e;
     if (b < 0x00800000u) {
         e = -127;  // zero (subnormal amax is outside the contract)
@@ -188,7 +188,7 @@ __device__ __forceinline__ uint2 round_rtne16(const float z[16], float r0, float
 #pragma unroll
         for (int i = 0; i < 8; ++i) t[i] = __fmul_rn(z[8 * h + i], r);
         uint32_t w;
-        if (GRID == 2) {
+        if (GRID >= 2) {
             w = 0;
 #pragma unroll
             for (int p = 0; p < 4; ++p) w |= cvt_e2m1x2(t[2 * p + 1], t[2 * p]) << (8 * p);
@@ -216,7 +216,7 @@ __device__ __forceinline__ uint32_t round_sr1(float t, uint32_t u) {
     constexpr float qmax = grid_qmax(GRID);
     const float a = fminf(fabsf(t), qmax);
     uint32_t idx;
-    if (GRID == 2) {
+    if (GRID >= 2) {
         // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
         const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
         const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
@@ -396,7 +396,7 @@ template <int GRID>
 __device__ __forceinline__ uint32_t rtne8(float t0, float t1, float t2, float t3, float t4, float t5, float t6,
                                           float t7) {
     uint32_t w;
-    if (GRID == 2) {
+    if (GRID >= 2) {
         w = cvt_e2m1x8(t0, t1, t2, t3, t4, t5, t6, t7);
     } else {
         const uint32_t E = cvt_e4m3x4(t0, t2, t4, t6);  // bytes: s000 0kkk

@@ -17,7 +17,8 @@ UFP4_OK = 0
 STATUS_NAMES = {0: "UFP4_OK", 1: "UFP4_ERR_INVALID_ARG", 2: "UFP4_ERR_UNSUPPORTED",
                 3: "UFP4_ERR_ALIGNMENT", 4: "UFP4_ERR_CUDA", 5: "UFP4_ERR_TIMEOUT"}
 GRID_E1M2, GRID_INT4, GRID_E2M1 = 0, 1, 2
-GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1}
+GRID_E2M1_R2 = 3
+GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1, "e2m1r2": GRID_E2M1_R2}
 ROUND_RTNE, ROUND_SR = 0, 1
 SCALE_FP32, SCALE_UE8M0 = 0, 1
 OUT_ROWWISE, OUT_COLWISE = 1, 2

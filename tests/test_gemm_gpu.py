@@ -50,14 +50,14 @@ def _rel(D, ref):
 FP8_GRIDS = ("e1m2", "int4")
 
 
-@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
+@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1", "e2m1r2"))
 @pytest.mark.parametrize("block", BLOCKS)
 @pytest.mark.parametrize("shape", [(128, 256, 128), (256, 512, 512), (200, 300, 384)])
 def test_gemm_exact_integer_case(grid, block, shape):
     """Unit scales: every product and partial sum is an exact small dyadic,
     so the tensor-core result equals the fp64 reference bit for bit."""
     M, N, K = shape
-    if grid == "e2m1" and K % 64:
+    if grid.startswith("e2m1") and K % 64:
         pytest.skip("FP4 operands need K % 64 == 0")
     if block[0] > 1 and (M % 32 or N % 32):
         M, N = (M + 31) // 32 * 32, (N + 31) // 32 * 32
@@ -104,7 +104,7 @@ def _quantized(x, grid, block, colwise=False, rounding=orc.RTNE):
     return got["col" if colwise else "row"]
 
 
-@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
+@pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1", "e2m1r2"))
 def test_fprop_dense_small(grid):
     x, w = inputs.dense_fprop(m=1024, n=768, k=2048)
     ac, asc = _quantized(x, grid, (1, 16))

@@ -17,7 +17,7 @@ import oracle as orc
 from rht_bit_block_gb300 import inputs
 from tests.conftest import read_golden
 
-GRIDS = ("e1m2", "int4", "e2m1")
+GRIDS = ("e1m2", "int4", "e2m1", "e2m1r2")
 
 
 # ------------------------------------------------------------------ Philox
@@ -167,7 +167,7 @@ def test_rht_preserves_gemm():
 @pytest.mark.parametrize("grid", GRIDS)
 def test_rtne_is_nearest_level_dense_sweep(grid):
     """RTNE picks a nearest level (brute force over the level list)."""
-    levels = np.array([orc.level(grid, i) for i in range(8)])
+    levels = np.array([orc.level(grid, i) for i in range(orc.num_levels(grid))])
     qm = orc.qmax(grid)
     for a in np.linspace(0.0, qm, 4001, dtype=np.float32):
         idx = orc.round_rtne(grid, float(a))
@@ -183,10 +183,11 @@ def test_rtne_ties_go_to_even_code():
 
 def test_uniform_rtne_matches_numpy_rint():
     """On the uniform grids RTNE is numpy's round-half-even of a / step."""
-    for grid, step in (("e1m2", 0.25), ("int4", 1.0)):
+    for grid, step in (("e1m2", 0.25), ("int4", 1.0), ("e2m1r2", 0.5)):
         qm = orc.qmax(grid)
         a = np.random.default_rng(8).uniform(0, qm, 20000).astype(np.float32)
-        a = np.concatenate([a, (np.arange(0, 15) * 0.5 * step).astype(np.float32)])
+        halves = int(round(2 * qm / step)) + 1  # every level and midpoint in [0, qmax]
+        a = np.concatenate([a, (np.arange(0, halves) * 0.5 * step).astype(np.float32)])
         for v in a:
             assert orc.round_rtne(grid, float(v)) == int(np.rint(np.float64(v) / step))
 
@@ -195,7 +196,7 @@ def test_uniform_rtne_matches_numpy_rint():
 def test_bin_bias_law(grid, q, expect):
     """UFP4 summary, 方法, bin-bias law: for t uniform on the RTNE bin of an
     interior level q_i, E[rho(t) - t] = (2 q_i - q_{i-1} - q_{i+1}) / 4."""
-    levels = [orc.level(grid, i) for i in range(8)]
+    levels = [orc.level(grid, i) for i in range(orc.num_levels(grid))]
     i = levels.index(q)
     lo, hi = (levels[i - 1] + q) / 2, (q + levels[i + 1]) / 2
     t = np.random.default_rng(int(q * 1000) + len(grid)).uniform(lo, hi, 200_000).astype(np.float32)
@@ -209,7 +210,7 @@ def test_bin_bias_law(grid, q, expect):
 def test_sr_is_unbiased(grid, p):
     """2D-block page (stochastic rounding) and UFP4 summary (数据集): E[SR(x)] = x.
     10^6 draws at adversarial points, within 4 sigma."""
-    levels = [orc.level(grid, i) for i in range(8)]
+    levels = [orc.level(grid, i) for i in range(orc.num_levels(grid))]
     lo, hi = levels[3], levels[4]
     x = np.float32(lo + p * (hi - lo))
     u = np.random.default_rng(17).integers(0, 65536, 1_000_000)
@@ -226,13 +227,14 @@ def test_sr_is_unbiased(grid, p):
 
 @pytest.mark.parametrize("grid", GRIDS)
 def test_sr_only_picks_neighbours(grid):
-    levels = np.array([orc.level(grid, i) for i in range(8)])
+    levels = np.array([orc.level(grid, i) for i in range(orc.num_levels(grid))])
+    top = len(levels) - 1
     rng = np.random.default_rng(5)
     for a in rng.uniform(0, orc.qmax(grid), 3000).astype(np.float32):
         idx = orc.round_sr(grid, float(a), int(rng.integers(0, 65536)))
-        assert levels[idx] >= a or idx == 7 or levels[idx + 1] > a
+        assert levels[idx] >= a or idx == top or levels[idx + 1] > a
         lo = np.max(np.nonzero(levels <= a)[0])
-        assert idx in (lo, min(lo + 1, 7))
+        assert idx in (lo, min(lo + 1, top))
 
 
 def test_sr_through_quantizer_is_unbiased():
@@ -263,7 +265,7 @@ def test_fp32_scale_maps_amax_to_qmax(grid):
     else:
         m = mags & 7
     blockmax = m.reshape(64, 16, 16).max(axis=2)
-    assert (blockmax[sc > 0] == 7).all()
+    assert (blockmax[sc > 0] == orc.num_levels(grid) - 1).all()
 
 
 @pytest.mark.parametrize("grid", GRIDS)
@@ -355,7 +357,7 @@ def test_dequantize_inverse_rht_undoes_rotation(grid):
     # and the reconstruction error is within the grid's resolution
     xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
     seg_err = np.linalg.norm((inv - xf).reshape(32, -1, 16), axis=2)
-    step = {"e1m2": 0.25, "int4": 1.0, "e2m1": 2.0}[grid]
+    step = {"e1m2": 0.25, "int4": 1.0, "e2m1": 2.0, "e2m1r2": 0.5}[grid]
     s = np.repeat(sc.astype(np.float64), 1, axis=1)
     assert (seg_err <= np.sqrt(16) * step / 2 * s.max() * 1.01 + 1e-6).all()
 
@@ -384,3 +386,37 @@ def test_gemm_reference_exact_integer_case():
     sb = np.full((N, K // 16), 127, dtype=np.uint8)
     D = orc.gemm_reference(pack(ka), sa, pack(kb), sb, grid="int4", block=(1, 16))
     np.testing.assert_array_equal(D, (ka @ kb.T).astype(np.float64))
+
+
+# ------------------------------------------------ range-limited E2M1 (E2M1_R2)
+def test_range_limited_e2m1_uses_the_uniform_part_of_e2m1():
+    """The range-limited grid rounds to E2M1's levels up to 2 and writes plain
+    E2M1 codes: its level table is the first five entries of the E2M1
+    codebook printed on the UFP4 summary (数据集: E2M1 = {0, 0.5, 1, 1.5, 2,
+    3, 4, 6}), and no code above 4 (the level 2) ever appears."""
+    e2m1_pages = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+    assert orc.num_levels("e2m1r2") == 5 and orc.qmax("e2m1r2") == 2.0
+    assert [orc.level("e2m1r2", i) for i in range(5)] == e2m1_pages[:5]
+    x = inputs.tiny_check(128, 512)
+    for kw in (dict(), dict(scale_fmt=orc.SCALE_UE8M0), dict(rounding=orc.SR, sr_seed=4)):
+        codes, _ = orc.quantize(x, grid="e2m1r2", n=16, sign_seed=2, **kw)
+        nib = np.stack([codes & 0xF, codes >> 4], -1)
+        assert int((nib & 7).max()) == 4
+
+
+def test_range_limited_e2m1_has_no_bin_bias_where_e2m1_does():
+    """UFP4 summary, 方法 (bin-bias law): E2M1 is biased at q = 2 (its spacing
+    changes there); on the range-limited grid the same level sits on a uniform
+    run and the bias is zero.  Measured on locally uniform samples."""
+    def bias(grid, q):
+        levels = [orc.level(grid, i) for i in range(orc.num_levels(grid))]
+        i = levels.index(q)
+        lo, hi = (levels[i - 1] + q) / 2, (q + levels[i + 1]) / 2
+        t = np.random.default_rng(44).uniform(lo, hi, 100_000).astype(np.float32)
+        err = np.array([orc.level(grid, orc.round_rtne(grid, float(v))) for v in t]) - t.astype(np.float64)
+        return err.mean(), (hi - lo) / np.sqrt(12) / np.sqrt(t.size)
+    m, sig = bias("e2m1", 2.0)
+    assert abs(m + 0.125) < 5 * sig
+    for q in (0.5, 1.0, 1.5):
+        m, sig = bias("e2m1r2", q)
+        assert abs(m) < 5 * sig

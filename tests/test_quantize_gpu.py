@@ -14,7 +14,7 @@ from tests.gpu_util import assert_bitwise, gpu_quantize, to_dev
 
 pytestmark = pytest.mark.gpu
 
-GRIDS = ("e1m2", "int4", "e2m1")
+GRIDS = ("e1m2", "int4", "e2m1", "e2m1r2")
 SR = orc.SR
 RTNE = orc.RTNE
 PO2 = orc.SCALE_UE8M0
@@ -262,7 +262,7 @@ def test_large_sweep_sampled_rows(n):
                                           ((1, 32), 1, 544)])
 def test_rowwise_ragged_tiles(grid, rounding, block, n, cols):
     x = inputs.tiny_check(300, cols)
-    fmt = PO2 if grid == "e2m1" else FP32
+    fmt = PO2 if grid.startswith("e2m1") else FP32
     _check(x, grid=grid, block=block, n=n, sign_seed=21, rounding=rounding, sr_seed=8, scale_fmt=fmt,
            ld=cols + 64, group=2)
 
