@@ -221,6 +221,26 @@ ufp4_status ufp4_rht_transform(const void* x, int64_t rows, int64_t cols, int64_
 ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc,
                             int32_t inverse_rht, float* out, int64_t ld_out, cudaStream_t stream);
 
+/* ufp4_quant_error_stats -- diagnostics of one row-wise quantization
+ * [UFP4-data: Q_G(T) is the dequantized tensor; UFP4-method: RTNE on a
+ * non-uniform grid shrinks values bin by bin].  From x (device bf16 rows x
+ * cols, ld elements) and its row-wise quantization `rowwise` made with desc,
+ * the library recomputes z = RHT(x) with the quantizer's arithmetic and q =
+ * level * scale, and writes to stats (device, 4 doubles, 8-byte aligned):
+ *   stats[0] = sum z^2, stats[1] = sum (q - z)^2, stats[2] = sum q z,
+ *   stats[3] = sum q^2, accumulated in fp64 (the order of the additions is
+ * unspecified).  SQNR = stats[0] / stats[1]; the shrinkage factor
+ * E[Q(t) t] / E[t^2] = stats[2] / stats[0]. */
+ufp4_status ufp4_quant_error_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, const ufp4_quant_desc* desc,
+                                   const ufp4_qtensor* rowwise, double* stats, cudaStream_t stream);
+
+/* ufp4_error_stats -- the same four fp64 sums for two device fp32 matrices
+ * (rows x cols): stats[0] = sum ref^2, stats[1] = sum (approx - ref)^2,
+ * stats[2] = sum ref * approx, stats[3] = sum approx^2; e.g. a quantized GEMM
+ * output against a reference product. */
+ufp4_status ufp4_error_stats(const float* ref, int64_t ld_ref, const float* approx, int64_t ld_approx, int64_t rows,
+                             int64_t cols, double* stats, cudaStream_t stream);
+
 /* ufp4_gemm_workspace_size -- device scratch bytes ufp4_gemm needs for
  * operands A (M x K) and B (N x K) quantized with desc. */
 ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4_quant_desc* desc,

@@ -195,3 +195,15 @@ def gemm_reference(a_codes, a_scales, b_codes, b_scales, *, grid="e1m2", block=(
         A = A[np.asarray(a_rows)]
     B = dequantize_f64(b_codes, b_scales, grid=grid, block=block, scale_fmt=scale_fmt)
     return A @ B.T
+
+
+def quant_error_stats(x_bf16: np.ndarray, codes, scales, *, grid="e1m2", block=(1, 16), scale_fmt=SCALE_FP32, n=16,
+                      sign_seed=0) -> np.ndarray:
+    """Diagnostics of one row-wise quantization (UFP4 summary, 数据集: Q_G(T) is
+    the dequantized tensor; 方法: RTNE shrinkage bin by bin).  z = the RHT of x
+    with the quantizer's fp32 arithmetic, q = level * scale (fp32); returns the
+    fp64 sums [sum z^2, sum (q - z)^2, sum q z, sum q^2]."""
+    z = rht_rows(x_bf16, n, sign_seed).astype(np.float64)
+    q = dequantize(codes, scales, grid=grid, block=block, scale_fmt=scale_fmt, n=n).astype(np.float64)
+    d = q - z
+    return np.array([(z * z).sum(), (d * d).sum(), (q * z).sum(), (q * q).sum()])

@@ -426,6 +426,50 @@ ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc, 
     return cuda_status(launch_dequantize(p, num_sms_current(), stream));
 }
 
+ufp4_status ufp4_quant_error_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, const ufp4_quant_desc* desc,
+                                   const ufp4_qtensor* rowwise, double* stats, cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!rowwise || !stats || rows < 0 || cols < 0) return UFP4_ERR_INVALID_ARG;
+    if (!aligned(stats, 8)) return UFP4_ERR_ALIGNMENT;
+    const int n = desc->hadamard_n;
+    if (cols % 16 || cols % n || cols % bs.bw || (bs.is2d && rows % bs.b2d)) return UFP4_ERR_INVALID_ARG;
+    st = check_out(rowwise, rows, cols, bs, desc->scale_fmt, false);
+    if (st != UFP4_OK) return st;
+    if (rows > 0 && cols > 0) {
+        if (!x || ld < cols) return UFP4_ERR_INVALID_ARG;
+        if (!aligned(x, 16) || ld % 8) return UFP4_ERR_ALIGNMENT;
+    }
+    QStatsParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = (const uint16_t*)x;
+    p.ld = ld;
+    p.rows = rows;
+    p.cols = cols;
+    p.codes = (const uint8_t*)rowwise->codes;
+    p.scales = rowwise->scales;
+    p.codes_ld = rowwise->codes_ld;
+    p.scales_ld = rowwise->scales_ld;
+    p.grid = desc->grid;
+    p.br = bs.is2d ? bs.b2d : 1;
+    p.bc = bs.bw;
+    p.po2 = desc->scale_fmt == UFP4_SCALE_UE8M0;
+    p.n = n;
+    p.inv_sqrt_n = inv_sqrt_n(n);
+    make_sign_bits(desc->sign_seed, n, p.sign_bits);
+    p.stats = stats;
+    return cuda_status(launch_qstats(p, num_sms_current(), stream));
+}
+
+ufp4_status ufp4_error_stats(const float* ref, int64_t ld_ref, const float* approx, int64_t ld_approx, int64_t rows,
+                             int64_t cols, double* stats, cudaStream_t stream) {
+    if (!stats || rows < 0 || cols < 0) return UFP4_ERR_INVALID_ARG;
+    if (!aligned(stats, 8)) return UFP4_ERR_ALIGNMENT;
+    if (rows > 0 && cols > 0 && (!ref || !approx || ld_ref < cols || ld_approx < cols)) return UFP4_ERR_INVALID_ARG;
+    return cuda_status(launch_dstats(ref, ld_ref, approx, ld_approx, rows, cols, stats, num_sms_current(), stream));
+}
+
 ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4_quant_desc* desc, size_t* bytes) {
     BlockShape bs;
     ufp4_status st = check_desc(desc, &bs);

@@ -10,18 +10,6 @@
 
 namespace ufp4 {
 
-__device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
-    if (grid == 1) return (float)((nib & 8u) ? (int)nib - 16 : (int)nib);
-    const uint32_t k = nib & 7u;
-    float v;
-    if (grid == 0) {
-        v = (float)k * 0.25f;
-    } else {
-        // E2M1 levels 0, .5, 1, 1.5, 2, 3, 4, 6
-        v = k < 4 ? (float)k * 0.5f : (k == 4 ? 2.0f : (k == 5 ? 3.0f : (k == 6 ? 4.0f : 6.0f)));
-    }
-    return (nib & 8u) ? -v : v;
-}
 
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
     const int64_t cpr = p.cols / kChunk;

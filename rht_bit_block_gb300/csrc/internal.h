@@ -126,6 +126,23 @@ struct DequantParams {
 };
 cudaError_t launch_dequantize(const DequantParams& p, int num_sms, cudaStream_t st);
 
+// Diagnostics (stats.cu): fp64 sums over a row-wise quantization and its input,
+// and over two fp32 matrices.
+struct QStatsParams {
+    const uint16_t* x;
+    int64_t ld, rows, cols;
+    const uint8_t* codes;
+    const void* scales;
+    int64_t codes_ld, scales_ld;
+    int grid, br, bc, po2, n;
+    float inv_sqrt_n;
+    uint32_t sign_bits[8];
+    double* stats;  // device, 4 doubles
+};
+cudaError_t launch_qstats(const QStatsParams& p, int num_sms, cudaStream_t st);
+cudaError_t launch_dstats(const float* a, int64_t lda, const float* b, int64_t ldb, int64_t rows, int64_t cols,
+                          double* stats, int num_sms, cudaStream_t st);
+
 // ---------------------------------------------------------------- GEMM
 struct GemmOperand {
     const uint8_t* codes;

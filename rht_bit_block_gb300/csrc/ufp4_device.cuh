@@ -26,6 +26,20 @@ __host__ __device__ constexpr float grid_qmax(int grid) {
 // ------------------------------------------------------------- Philox4x32-10
 // Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
 // bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.
+// Value of a 4-bit code on the grid's level scale (before the block scale).
+__device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
+    if (grid == 1) return (float)((nib & 8u) ? (int)nib - 16 : (int)nib);
+    const uint32_t k = nib & 7u;
+    float v;
+    if (grid == 0) {
+        v = (float)k * 0.25f;
+    } else {
+        // E2M1 levels 0, .5, 1, 1.5, 2, 3, 4, 6
+        v = k < 4 ? (float)k * 0.5f : (k == 4 ? 2.0f : (k == 5 ? 3.0f : (k == 6 ? 4.0f : 6.0f)));
+    }
+    return (nib & 8u) ? -v : v;
+}
+
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {

@@ -29,7 +29,7 @@ EXPORTED = (
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
     "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
-    "ufp4_rht_quantize_batch",
+    "ufp4_rht_quantize_batch", "ufp4_quant_error_stats", "ufp4_error_stats",
 )
 MAX_BATCH = 4
 
@@ -67,6 +67,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     QD, QT = ctypes.POINTER(QuantDesc), ctypes.POINTER(QTensor)
     L.ufp4_rht_quantize.argtypes = [P, i64, i64, i64, QD, QT, QT, P]
     L.ufp4_rht_quantize_grouped.argtypes = [P, i64, i64, ctypes.POINTER(i64), i32, QD, QT, QT, P]
+    L.ufp4_quant_error_stats.argtypes = [P, i64, i64, i64, QD, QT, P, P]
+    L.ufp4_error_stats.argtypes = [P, i64, P, i64, i64, i64, P, P]
     L.ufp4_rht_quantize_batch.argtypes = [i32, ctypes.POINTER(P), ctypes.POINTER(i64), ctypes.POINTER(i64),
                                           ctypes.POINTER(i64), QD, QT, P]
     L.ufp4_grouped_padded_rows.argtypes = [i64, QD]
@@ -138,6 +140,21 @@ def ufp4_rht_quantize_batch(xs, desc: QuantDesc, rowwise, stream=None):
     outs = (QTensor * max(k, 1))(*rowwise)
     _check(load().ufp4_rht_quantize_batch(k, ptrs, rows, cols, lds, ctypes.byref(desc), outs, _stream(stream)),
            "ufp4_rht_quantize_batch")
+
+
+def ufp4_quant_error_stats(x, desc: QuantDesc, rowwise: QTensor, stats, stream=None):
+    """fp64 sums [sum z^2, sum (q-z)^2, sum q z, sum q^2] of a row-wise quantization, into `stats` (4 doubles)."""
+    rows, cols = x.shape
+    _check(load().ufp4_quant_error_stats(x.data_ptr(), rows, cols, x.stride(0), ctypes.byref(desc),
+                                         ctypes.byref(rowwise), stats.data_ptr(), _stream(stream)),
+           "ufp4_quant_error_stats")
+
+
+def ufp4_error_stats(ref, approx, stats, stream=None):
+    """fp64 sums [sum ref^2, sum (approx-ref)^2, sum ref*approx, sum approx^2] of two fp32 matrices."""
+    rows, cols = ref.shape
+    _check(load().ufp4_error_stats(ref.data_ptr(), ref.stride(0), approx.data_ptr(), approx.stride(0), rows, cols,
+                                   stats.data_ptr(), _stream(stream)), "ufp4_error_stats")
 
 
 def ufp4_rht_quantize_grouped(x, offsets, desc: QuantDesc, rowwise: QTensor | None, colwise: QTensor | None,

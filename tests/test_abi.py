@@ -98,3 +98,17 @@ def test_batch_validation_rejects_bad_arguments(lib):
     assert call(ok, lds=(64, 32)) == 1                                     # ld < cols
     # an empty tensor's pointer and leading dimension are not looked at
     assert call(ok, count=1, xs=(0, 0), rows=(0, 0), lds=(1, 1)) == 0
+
+
+def test_diagnostics_validation(lib):
+    desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)
+    q = ufp4.QTensor(0x2000, 0x3000, 64, 64, 32, 4)
+    x = ctypes.c_void_p(0x1000)
+    assert lib.ufp4_quant_error_stats(x, 64, 64, 64, ctypes.byref(desc), ctypes.byref(q), None, None) == 1
+    assert lib.ufp4_quant_error_stats(x, 64, 64, 64, ctypes.byref(desc), ctypes.byref(q),
+                                      ctypes.c_void_p(0x4004), None) == 3       # stats not 8-byte aligned
+    assert lib.ufp4_quant_error_stats(x, 64, 72, 72, ctypes.byref(desc), ctypes.byref(q),
+                                      ctypes.c_void_p(0x4000), None) == 1       # cols not a multiple of 16
+    assert lib.ufp4_error_stats(None, 8, None, 8, 4, 8, None, None) == 1
+    assert lib.ufp4_error_stats(ctypes.c_void_p(0x1000), 4, ctypes.c_void_p(0x2000), 8, 4, 8,
+                                ctypes.c_void_p(0x4000), None) == 1            # ld < cols

@@ -420,3 +420,27 @@ def test_range_limited_e2m1_has_no_bin_bias_where_e2m1_does():
     for q in (0.5, 1.0, 1.5):
         m, sig = bias("e2m1r2", q)
         assert abs(m) < 5 * sig
+
+
+# ----------------------------------------------------------- diagnostics
+def test_shrinkage_follows_the_bin_bias_law():
+    """UFP4 summary, 方法: with RTNE, E[Q(t) (Q(t) - t)] = sum_i q_i * bias_i
+    over the bins.  On a uniform grid the interior biases vanish (E[Q^2] =
+    E[Q t] up to sampling noise); E2M1's negative biases at 2 and 4 make
+    E[Q^2] < E[Q t]: the values shrink toward zero.  Measured with n = 1 on
+    magnitudes uniform up to a bin edge (so every bin is sampled evenly on
+    both sides of its level) and one element per 1 x 16 block at amax."""
+    edge = {"e1m2": 1.375, "int4": 6.5, "e2m1": 5.0, "e2m1r2": 1.75}  # bin edges below qmax
+    res = {}
+    for grid, e in edge.items():
+        rng = np.random.default_rng(12)
+        a = rng.uniform(0.0, e / orc.qmax(grid), (512, 1024)).astype(np.float32)
+        a[:, ::16] = 1.0  # amax = 1 in every block: t = a * qmax
+        x = inputs.f32_to_bf16_bits(a)
+        codes, sc = orc.quantize(x, grid=grid, n=1)
+        zz, dd, qz, qq = orc.quant_error_stats(x, codes, sc, grid=grid, n=1)
+        res[grid] = ((qq - qz) / dd, qz / zz)
+    for grid in ("e1m2", "int4", "e2m1r2"):
+        assert abs(res[grid][0]) < 0.2, (grid, res[grid])
+    assert res["e2m1"][0] < -1.0
+    assert res["e2m1"][1] < min(res[g][1] for g in ("e1m2", "int4", "e2m1r2"))  # stronger shrinkage
