@@ -372,6 +372,137 @@ def run_gpu(args):
     return 0
 
 
+# ------------------------------------------------------------- suite mode
+def run_suite(args):
+    """Further measurements, one JSON line each (not the headline): the other
+    workloads of the configuration list and the widened rows.  CUDA events on
+    the launching stream, 3 warm-ups, median of the timed repetitions; inputs
+    larger than L2 or rotated over 5 copies."""
+    import torch
+    from rht_bit_block_gb300 import inputs, ufp4
+    ufp4.load()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.Stream()
+    torch.cuda.set_stream(stream)
+    pk = peaks()
+    to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
+
+    def timed(fn, reps=20, warm=3):
+        for i in range(warm):
+            fn(i)
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for i, (a, b) in enumerate(ev):
+            a.record(stream)
+            fn(i)
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+    def emit(name, workload, value, unit, frac=None, peak=None, **extra):
+        line = {"suite": name, "workload": workload, "value": value, "unit": unit}
+        if frac is not None:
+            line.update({"frac": frac, "peak": peak})
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    def scale_bytes(desc):
+        per = 1 if desc.scale_fmt == ufp4.SCALE_UE8M0 else 4
+        return per / (desc.block_rows * desc.block_cols)
+
+    # 1. large-shape sweep operand, row-wise (X 16384 x 7168, > L2)
+    x5, _ = inputs.large_sweep(k=7168, n=128)
+    xs5 = [to_t(x5).to(dev) for _ in range(2)]
+    rows, cols = x5.shape
+    cases = [("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_RTNE), ("int4", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
+             ("e2m1", (1, 16), 16, ufp4.SCALE_UE8M0, 0), ("e2m1r2", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
+             ("e1m2", (1, 16), 16, ufp4.SCALE_FP32, 0), ("e1m2", (1, 32), 64, ufp4.SCALE_UE8M0, 0),
+             ("e1m2", (1, 16), 256, ufp4.SCALE_UE8M0, 0), ("e2m1", (32, 32), 16, ufp4.SCALE_UE8M0, 0),
+             ("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_SR)]
+    for grid, block, n, fmt, rnd in cases:
+        desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt, rounding=rnd,
+                              sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
+        out = ufp4.alloc_quantized(rows, cols, desc, dev)
+        q = ufp4.qtensor(*out, rows, cols)
+        ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
+        gbs = rows * cols * (2.5 + scale_bytes(desc)) / (ms / 1e3) / 1e9
+        emit("quantize_rowwise", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
+             f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs, "GB/s", gbs / pk["hbm"], pk["hbm"],
+             ms=ms)
+    del xs5
+
+    # 2. dY stochastic-rounding path: row-wise and column-wise from one read
+    dy, _ = inputs.dy_sr()
+    dys = [to_t(dy).to(dev) for _ in range(5)]
+    r3, c3 = dy.shape
+    for fmt in (ufp4.SCALE_FP32, ufp4.SCALE_UE8M0):
+        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
+                              rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED,
+                              out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
+        ro = ufp4.alloc_quantized(r3, c3, desc, dev)
+        co = ufp4.alloc_quantized(c3, r3, desc, dev)
+        rq, cq = ufp4.qtensor(*ro, r3, c3), ufp4.qtensor(*co, c3, r3)
+        ms = timed(lambda i: ufp4.ufp4_rht_quantize(dys[i % 5], desc, rq, cq, stream.cuda_stream))
+        gbs = r3 * c3 * (2 + 2 * (0.5 + scale_bytes(desc))) / (ms / 1e3) / 1e9
+        emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 SR row+col", gbs,
+             "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
+
+    # 3. diagnostics on the dense FPROP X
+    x2, _ = inputs.dense_fprop(n=128)
+    x2s = [to_t(x2).to(dev) for _ in range(5)]
+    r2, c2 = x2.shape
+    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
+                          scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+    qout = [ufp4.alloc_quantized(r2, c2, desc, dev) for _ in range(5)]
+    for i in range(5):
+        ufp4.ufp4_rht_quantize(x2s[i], desc, ufp4.qtensor(*qout[i], r2, c2), None, stream.cuda_stream)
+    st = torch.zeros(4, dtype=torch.float64, device=dev)
+    ms = timed(lambda i: ufp4.ufp4_quant_error_stats(x2s[i % 5], desc, ufp4.qtensor(*qout[i % 5], r2, c2), st,
+                                                     stream.cuda_stream))
+    gbs = r2 * c2 * (2 + 0.5 + 1 / 16) / (ms / 1e3) / 1e9
+    s = st.cpu().numpy()
+    emit("diagnostics", f"quant_error_stats X {r2}x{c2} e1m2 1x16 UE8M0 n=16", gbs, "GB/s", gbs / pk["hbm"],
+         pk["hbm"], ms=ms, sqnr_db=float(10 * np.log10(s[0] / s[1])), shrinkage=float(s[2] / s[0]))
+    del x2s, qout
+
+    # 4. GEMMs per grid on the dense FPROP shape (tensor-core kernel alone, prep timed apart)
+    M, N, K = 8192, 5632, 2048
+    g = torch.Generator().manual_seed(7)
+    for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 32), 2.0), ("e2m1", (1, 16), 6.0),
+                                   ("e2m1", (1, 32), 6.0), ("e2m1r2", (1, 16), 6.0)):
+        desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
+        def operand(rows):
+            c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8)
+            c = c & 0x77 if grid != "int4" else c & 0x77  # valid codes in every grid, no -0 / -8
+            sc = torch.randint(120, 132, (rows, K // block[1]), generator=g, dtype=torch.uint8)
+            return c.to(dev), sc.to(dev)
+        A, B = operand(M), operand(N)
+        qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+        D = torch.empty((M, N), dtype=torch.float32, device=dev)
+        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+        peak = kind_peak * pk["bf16"]
+        emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
+             kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
+        del A, B, ws, D
+    # the large-sweep FPROP GEMM
+    M5, N5, K5 = 16384, 7168, 7168
+    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+    A = (torch.randint(0, 256, (M5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+         torch.randint(120, 132, (M5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
+    B = (torch.randint(0, 256, (N5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+         torch.randint(120, 132, (N5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
+    qa, qb = ufp4.qtensor(*A, M5, K5), ufp4.qtensor(*B, N5, K5)
+    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M5, N5, K5, desc), dtype=torch.uint8, device=dev)
+    D = torch.empty((M5, N5), dtype=torch.float32, device=dev)
+    ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream)
+    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream), reps=10)
+    tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
+    emit("gemm", f"{M5}x{N5}x{K5} e1m2 1x16 UE8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
+         kernel_ms=kms)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -380,9 +511,14 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--suite", action="store_true",
+                    help="further measurements (other workloads, widened rows), one JSON line each")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.suite:
+        run_suite(args)
+        return
     if args.impl == "reference":
         return run_reference(args)
     return run_gpu(args)

@@ -228,8 +228,9 @@ ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc,
  * the library recomputes z = RHT(x) with the quantizer's arithmetic and q =
  * level * scale, and writes to stats (device, 4 doubles, 8-byte aligned):
  *   stats[0] = sum z^2, stats[1] = sum (q - z)^2, stats[2] = sum q z,
- *   stats[3] = sum q^2, accumulated in fp64 (the order of the additions is
- * unspecified).  SQNR = stats[0] / stats[1]; the shrinkage factor
+ *   stats[3] = sum q^2, accumulated in fp64 over 16-element fp32 partial
+ * sums (relative difference from an exact sum of order 1e-6; the order of
+ * the additions is unspecified).  SQNR = stats[0] / stats[1]; the shrinkage factor
  * E[Q(t) t] / E[t^2] = stats[2] / stats[0]. */
 ufp4_status ufp4_quant_error_stats(const void* x, int64_t rows, int64_t cols, int64_t ld, const ufp4_quant_desc* desc,
                                    const ufp4_qtensor* rowwise, double* stats, cudaStream_t stream);

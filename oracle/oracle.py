@@ -16,7 +16,7 @@ _lib = None
 
 E1M2, INT4, E2M1, E2M1_R2 = 0, 1, 2, 3
 RTNE, SR = 0, 1
-SCALE_FP32, SCALE_UE8M0 = 0, 1
+SCALE_FP32, SCALE_UE8M0, SCALE_E4M3 = 0, 1, 2
 GRID_NAMES = {"e1m2": E1M2, "int4": INT4, "e2m1": E2M1, "e2m1r2": E2M1_R2}
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-shared", "-fPIC"]
@@ -59,6 +59,19 @@ def lib():
         L.orc_qmax.restype = ctypes.c_double
         L.orc_num_levels.argtypes = [i32]
         L.orc_num_levels.restype = i32
+        L.orc_e4m3_encode.argtypes = [ctypes.c_double]
+        L.orc_e4m3_encode.restype = ctypes.c_uint8
+        L.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
+        L.orc_e4m3_decode.restype = ctypes.c_double
+        L.orc_tensor_scale.argtypes = [ctypes.c_float, i32]
+        L.orc_tensor_scale.restype = ctypes.c_float
+        L.orc_quantize_rows_2level.argtypes = [P, i64, i64, i64, i32, i32, i32, i32, u64, i32, u64, ctypes.c_uint32,
+                                               u64, ctypes.c_float, P, P, P]
+        L.orc_quantize_rows_2level.restype = i32
+        L.orc_dequantize_2level.argtypes = [P, P, i64, i64, i32, i32, i32, ctypes.c_float, i32, u64, i32, P]
+        L.orc_dequantize_2level.restype = i32
+        L.orc_dequantize_f64_2level.argtypes = [P, P, i64, i64, i32, i32, i32, ctypes.c_float, P]
+        L.orc_dequantize_f64_2level.restype = i32
         L.orc_po2_exponent.argtypes = [ctypes.c_float, i32]
         L.orc_po2_exponent.restype = i32
         L.orc_round_rtne.argtypes = [i32, ctypes.c_float]
@@ -207,3 +220,62 @@ def quant_error_stats(x_bf16: np.ndarray, codes, scales, *, grid="e1m2", block=(
     q = dequantize(codes, scales, grid=grid, block=block, scale_fmt=scale_fmt, n=n).astype(np.float64)
     d = q - z
     return np.array([(z * z).sum(), (d * d).sum(), (q * z).sum(), (q * q).sum()])
+
+
+# ------------------------------------------------------ two-level scale
+def e4m3_encode(a: float) -> int:
+    """E4M3 byte of a >= 0, rounded to nearest even, saturated at 448."""
+    return int(lib().orc_e4m3_encode(float(a)))
+
+
+def e4m3_decode(b: int) -> float:
+    return float(lib().orc_e4m3_decode(int(b)))
+
+
+def tensor_scale(tensor_amax: float, grid) -> float:
+    """g = fp32(T / fp32(qmax * 448))."""
+    return float(lib().orc_tensor_scale(tensor_amax, _grid(grid)))
+
+
+def quantize_2level(x_bf16: np.ndarray, *, grid="e2m1", block=(1, 16), n=16, sign_seed=0, rounding=RTNE,
+                    sr_seed=0, group=0, row0=0, tensor_amax=-1.0):
+    """Row-wise quantization with the two-level scale (E4M3 block scales x the
+    fp32 tensor scale g): returns (codes, E4M3 scale bytes, tensor amax T).
+    tensor_amax < 0 takes T from this call's rows."""
+    x = _as_bf16(x_bf16)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.zeros((rows // block[0], cols // block[1]), dtype=np.uint8)
+    t_out = np.zeros(1, dtype=np.float32)
+    if lib().orc_quantize_rows_2level(_ptr(x), rows, cols, cols, _grid(grid), block[0], block[1], n, sign_seed,
+                                      rounding, sr_seed, group, row0, tensor_amax, _ptr(codes), _ptr(scales),
+                                      _ptr(t_out)):
+        raise ValueError("unsupported quantizer arguments")
+    return codes, scales, float(t_out[0])
+
+
+def dequantize_2level(codes, scales, tensor_amax: float, *, grid="e2m1", block=(1, 16), n=16, sign_seed=0,
+                      inverse_rht=False) -> np.ndarray:
+    codes = np.ascontiguousarray(codes)
+    scales = np.ascontiguousarray(scales)
+    rows, half = codes.shape
+    out = np.zeros((rows, 2 * half), dtype=np.float32)
+    if lib().orc_dequantize_2level(_ptr(codes), _ptr(scales), rows, 2 * half, _grid(grid), block[0], block[1],
+                                   tensor_amax, n, sign_seed, int(inverse_rht), _ptr(out)):
+        raise ValueError("unsupported dequantize arguments")
+    return out
+
+
+def gemm_reference_2level(a_codes, a_scales, a_amax, b_codes, b_scales, b_amax, *, grid="e2m1",
+                          block=(1, 16)) -> np.ndarray:
+    """fp64 product of the two-level dequantized operands (level * e4m3 * g)."""
+    def deq(c, sc, t):
+        c = np.ascontiguousarray(c)
+        sc = np.ascontiguousarray(sc)
+        rows, half = c.shape
+        out = np.zeros((rows, 2 * half), dtype=np.float64)
+        if lib().orc_dequantize_f64_2level(_ptr(c), _ptr(sc), rows, 2 * half, _grid(grid), block[0], block[1],
+                                           t, _ptr(out)):
+            raise ValueError("unsupported arguments")
+        return out
+    return deq(a_codes, a_scales, a_amax) @ deq(b_codes, b_scales, b_amax).T

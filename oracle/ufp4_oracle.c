@@ -43,7 +43,7 @@
 
 enum { ORC_E1M2 = 0, ORC_INT4 = 1, ORC_E2M1 = 2, ORC_E2M1_R2 = 3 };
 enum { ORC_RTNE = 0, ORC_SR = 1 };
-enum { ORC_SCALE_FP32 = 0, ORC_SCALE_UE8M0 = 1 };
+enum { ORC_SCALE_FP32 = 0, ORC_SCALE_UE8M0 = 1, ORC_SCALE_E4M3 = 2 };
 
 /* ---------------------------------------------------------------- codebooks
  * [UFP4-data]: each format has a normalized codebook G of fixed levels.  The
@@ -189,6 +189,52 @@ int orc_po2_exponent(float M, int grid) {
     return e;
 }
 
+/* ---------------------------------------------------- two-level scale
+ * The "two-level" option of the scale hierarchy [UFP4-method: the scale
+ * hierarchy is chosen for hardware efficiency]: a per-tensor fp32 scale g
+ * times a per-block scale stored as an E4M3 byte.  E4M3 (the OCP FP8 format
+ * without infinities): 1 sign, 4 exponent bits with bias 7, 3 mantissa bits;
+ * normal values (1 + m/8) 2^(e-7), e = 1..15 (e = 15 with m = 7 is NaN, so the
+ * largest finite value is 448 = 1.75 * 2^8); subnormals m * 2^-9.
+ * Reading of the definition:
+ *   T = max |z| over the whole tensor (z = the RHT output),
+ *   g = fp32(T / fp32(qmax * 448))  (the block scale of amax lands on 448),
+ *   per block: b = fp32(fp32(M / qmax) / g), stored as the E4M3 byte of b
+ *   rounded to nearest even and saturated at 448 (0 when g = 0),
+ *   s = fp32(e4m3(b) * g), elements scaled by fp32(1 / s) (0 when s = 0). */
+uint8_t orc_e4m3_encode(double a) {
+    if (!(a > 0.0)) return 0;
+    if (a >= 448.0) return 0x7E;
+    int e2;
+    frexp(a, &e2);
+    int E = e2 - 1;          /* a in [2^E, 2^(E+1)) */
+    if (E < -6) E = -6;      /* subnormals share the step of the smallest binade */
+    double step = ldexp(1.0, E - 3);
+    double k = a / step;     /* exact: scaling by a power of two */
+    double fl = floor(k), rem = k - fl;
+    double m = (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) ? fl + 1.0 : fl;
+    double v = m * step;
+    if (v > 448.0) v = 448.0;
+    if (v < ldexp(1.0, -6)) return (uint8_t)(v / ldexp(1.0, -9));  /* subnormal: m * 2^-9 */
+    int f2;
+    frexp(v, &f2);
+    int VE = f2 - 1;
+    int mant = (int)((v / ldexp(1.0, VE) - 1.0) * 8.0);
+    return (uint8_t)(((VE + 7) << 3) | mant);
+}
+
+double orc_e4m3_decode(uint8_t b) {
+    int e = (b >> 3) & 15, m = b & 7;
+    double v = e == 0 ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+    return (b & 0x80) ? -v : v;
+}
+
+/* g from the tensor amax T (fp32 arithmetic as written above). */
+float orc_tensor_scale(float T, int grid) {
+    float d = (float)orc_qmax(grid) * 448.0f;
+    return T / d;
+}
+
 /* ---------------------------------------------------------------- rounding
  * [UFP4-data]: RTNE maps a scaled magnitude to the nearest level of G; an exact
  * tie goes to the level with the even index (the even mantissa / integer LSB,
@@ -259,11 +305,13 @@ static uint32_t sr_draw(uint64_t sr_seed, uint64_t lin, uint32_t stream, uint32_
  * row0 is the index of x's first row in the whole tensor; it only enters the
  * SR counters, so a band of rows can be checked on its own.
  * Returns 0, or 1 on an unsupported argument. */
-int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int grid,
-                      int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
-                      uint64_t sr_seed, int scale_fmt, uint32_t stream, uint32_t group,
-                      uint64_t row0, uint8_t* codes, void* scales) {
+static int quantize_rows_impl(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int grid,
+                              int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
+                              uint64_t sr_seed, int scale_fmt, uint32_t stream, uint32_t group,
+                              uint64_t row0, float tensor_amax, uint8_t* codes, void* scales,
+                              float* tensor_amax_out) {
     if (grid < 0 || grid > 3 || block_rows < 1 || block_cols < 2 || cols % 2) return 1;
+    if (scale_fmt < 0 || scale_fmt > 2) return 1;
     if (rows % block_rows || cols % block_cols) return 1;
     float* z = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
     if (!z) return 1;
@@ -274,6 +322,17 @@ int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
     float qmax = (float)orc_qmax(grid);
     int64_t nbr = rows / block_rows, nbc = cols / block_cols;
     memset(codes, 0, (size_t)(rows * cols / 2));
+    /* two-level: the tensor amax (of this call's rows unless given) and g */
+    float T = tensor_amax, g = 0.0f;
+    if (scale_fmt == ORC_SCALE_E4M3) {
+        if (T < 0.0f) {
+            T = 0.0f;
+            for (int64_t i = 0; i < rows * cols; ++i)
+                if (fabsf(z[i]) > T) T = fabsf(z[i]);
+        }
+        g = orc_tensor_scale(T, grid);
+        if (tensor_amax_out) *tensor_amax_out = T;
+    }
     for (int64_t bi = 0; bi < nbr; ++bi) {
         for (int64_t bj = 0; bj < nbc; ++bj) {
             /* block amax [UFP4-data] */
@@ -289,6 +348,12 @@ int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
                 float s;
                 scale_fp32(M, grid, &s, &rcp);
                 ((float*)scales)[bi * nbc + bj] = s;
+            } else if (scale_fmt == ORC_SCALE_E4M3) {
+                float sb = M / qmax;
+                uint8_t b8 = (g == 0.0f) ? 0 : orc_e4m3_encode((double)(sb / g));
+                float s = (float)orc_e4m3_decode(b8) * g;
+                rcp = (s == 0.0f) ? 0.0f : 1.0f / s;
+                ((uint8_t*)scales)[bi * nbc + bj] = b8;
             } else {
                 int e = orc_po2_exponent(M, grid);
                 ((uint8_t*)scales)[bi * nbc + bj] = (uint8_t)(e + 127);
@@ -314,6 +379,26 @@ int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
     }
     free(z);
     return 0;
+}
+
+int orc_quantize_rows(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int grid,
+                      int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
+                      uint64_t sr_seed, int scale_fmt, uint32_t stream, uint32_t group,
+                      uint64_t row0, uint8_t* codes, void* scales) {
+    if (scale_fmt == ORC_SCALE_E4M3) return 1;  /* needs the tensor amax: orc_quantize_rows_2level */
+    return quantize_rows_impl(x, rows, cols, ld, grid, block_rows, block_cols, n, sign_seed, round, sr_seed,
+                              scale_fmt, stream, group, row0, -1.0f, codes, scales, NULL);
+}
+
+/* Two-level scale (E4M3 block scales x fp32 tensor scale).  tensor_amax < 0:
+ * T is the amax of this call's z; else T is given (a band of a larger tensor).
+ * T is written to *tensor_amax_out. */
+int orc_quantize_rows_2level(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int grid,
+                             int block_rows, int block_cols, int n, uint64_t sign_seed, int round,
+                             uint64_t sr_seed, uint32_t group, uint64_t row0, float tensor_amax,
+                             uint8_t* codes, uint8_t* scales, float* tensor_amax_out) {
+    return quantize_rows_impl(x, rows, cols, ld, grid, block_rows, block_cols, n, sign_seed, round, sr_seed,
+                              ORC_SCALE_E4M3, 0u, group, row0, tensor_amax, codes, scales, tensor_amax_out);
 }
 
 /* Column-wise quantization [2D-block, the transposition problem; UFP4-method,
@@ -349,19 +434,24 @@ static double decode(int grid, uint8_t nib) {
     return (nib & 8) ? -v : v;
 }
 
-int orc_dequantize(const uint8_t* codes, const void* scales, int64_t rows, int64_t cols, int grid,
-                   int block_rows, int block_cols, int scale_fmt, int n, uint64_t sign_seed,
-                   int inverse_rht, float* out) {
+static int dequantize_impl(const uint8_t* codes, const void* scales, int64_t rows, int64_t cols, int grid,
+                           int block_rows, int block_cols, int scale_fmt, float tensor_amax, int n,
+                           uint64_t sign_seed, int inverse_rht, float* out) {
     if (rows % block_rows || cols % block_cols || cols % 2) return 1;
+    const float g = scale_fmt == ORC_SCALE_E4M3 ? orc_tensor_scale(tensor_amax, grid) : 0.0f;
     int64_t nbc = cols / block_cols;
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < cols; ++c) {
             uint8_t nib = (uint8_t)((codes[r * (cols / 2) + c / 2] >> (4 * (c % 2))) & 0xF);
             int64_t b = (r / block_rows) * nbc + (c / block_cols);
             float lv = (float)decode(grid, nib);
-            float s = (scale_fmt == ORC_SCALE_FP32)
-                          ? ((const float*)scales)[b]
-                          : (float)ldexp(1.0, (int)((const uint8_t*)scales)[b] - 127);
+            float s;
+            if (scale_fmt == ORC_SCALE_FP32)
+                s = ((const float*)scales)[b];
+            else if (scale_fmt == ORC_SCALE_E4M3)
+                s = (float)orc_e4m3_decode(((const uint8_t*)scales)[b]) * g;  /* the quantizer's s */
+            else
+                s = (float)ldexp(1.0, (int)((const uint8_t*)scales)[b] - 127);
             out[r * cols + c] = lv * s;
         }
     if (inverse_rht && n > 1) {
@@ -382,6 +472,38 @@ int orc_dequantize(const uint8_t* codes, const void* scales, int64_t rows, int64
                 for (int i = 0; i < n; ++i) v[i] = (v[i] * inv_s) * (float)eps[i];
             }
     }
+    return 0;
+}
+
+int orc_dequantize(const uint8_t* codes, const void* scales, int64_t rows, int64_t cols, int grid,
+                   int block_rows, int block_cols, int scale_fmt, int n, uint64_t sign_seed,
+                   int inverse_rht, float* out) {
+    if (scale_fmt == ORC_SCALE_E4M3) return 1;  /* needs the tensor amax: orc_dequantize_2level */
+    return dequantize_impl(codes, scales, rows, cols, grid, block_rows, block_cols, scale_fmt, 0.0f, n,
+                           sign_seed, inverse_rht, out);
+}
+
+int orc_dequantize_2level(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols, int grid,
+                          int block_rows, int block_cols, float tensor_amax, int n, uint64_t sign_seed,
+                          int inverse_rht, float* out) {
+    return dequantize_impl(codes, scales, rows, cols, grid, block_rows, block_cols, ORC_SCALE_E4M3, tensor_amax,
+                           n, sign_seed, inverse_rht, out);
+}
+
+/* Two-level exact fp64 values for the GEMM reference: level * e4m3(b) * g,
+ * the product the block-scaled MMA forms (level * e4m3 block scale) times the
+ * tensor scales applied to its output. */
+int orc_dequantize_f64_2level(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols, int grid,
+                              int block_rows, int block_cols, float tensor_amax, double* out) {
+    if (rows % block_rows || cols % block_cols || cols % 2) return 1;
+    const double g = (double)orc_tensor_scale(tensor_amax, grid);
+    int64_t nbc = cols / block_cols;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            uint8_t nib = (uint8_t)((codes[r * (cols / 2) + c / 2] >> (4 * (c % 2))) & 0xF);
+            int64_t b = (r / block_rows) * nbc + (c / block_cols);
+            out[r * cols + c] = decode(grid, nib) * orc_e4m3_decode(scales[b]) * g;
+        }
     return 0;
 }
 

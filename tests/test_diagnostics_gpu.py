@@ -1,6 +1,8 @@
 """Diagnostics (single-tensor and GEMM-output error figures): the library's
-fp64 sums against the oracle's, through the C ABI.  The sums add exact fp64
-terms in a different order, so the bar is a relative difference of 1e-9."""
+sums against the oracle's exact fp64 sums, through the C ABI.  The library
+adds 16-element fp32 partial sums (fused multiply-adds) in fp64, so the bar
+is a relative difference of 1e-5; the two-matrix sums use fp32 products
+(exact to 2^-24 relative) and the bar there is 1e-6."""
 import numpy as np
 import pytest
 import torch
@@ -12,7 +14,7 @@ from tests.gpu_util import gpu_quantize, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _close(a, b, tol=1e-9):
+def _close(a, b, tol=1e-5):
     a, b = np.asarray(a, np.float64), np.asarray(b, np.float64)
     assert (np.abs(a - b) <= tol * np.maximum(np.abs(b), 1e-300)).all(), (a, b)
 
@@ -53,7 +55,7 @@ def test_error_stats_of_two_matrices():
     torch.cuda.synchronize()
     a64, b64 = a.astype(np.float64), b.astype(np.float64)
     _close(stats.cpu().numpy(), [(a64 * a64).sum(), ((b64 - a64) ** 2).sum(), (a64 * b64).sum(), (b64 * b64).sum()],
-           1e-12)
+           1e-6)
 
 
 def test_gemm_output_error_against_the_fp64_reference():

@@ -444,3 +444,55 @@ def test_shrinkage_follows_the_bin_bias_law():
         assert abs(res[grid][0]) < 0.2, (grid, res[grid])
     assert res["e2m1"][0] < -1.0
     assert res["e2m1"][1] < min(res[g][1] for g in ("e1m2", "int4", "e2m1r2"))  # stronger shrinkage
+
+
+# ------------------------------------------------ two-level scale (E4M3 x fp32)
+def test_e4m3_rounding_matches_torch_float8():
+    """The oracle's E4M3 rounding (written from the format's definition) equals
+    torch's float8_e4m3fn conversion (a library routine) on [0, 448]: dense
+    random values, every midpoint between neighbouring codes, subnormals."""
+    torch = pytest.importorskip("torch")
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    vals = [orc.e4m3_decode(b) for b in range(0, 0x7F)]
+    mids = [(a + b) / 2 for a, b in zip(vals[:-1], vals[1:])]
+    rng = np.random.default_rng(9)
+    xs = np.concatenate([rng.uniform(0, 448, 5000), 2.0 ** rng.uniform(-12, 8.8, 5000), mids, vals])
+    xs = xs.astype(np.float32)
+    ref = torch.from_numpy(xs).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([orc.e4m3_encode(float(v)) for v in xs], dtype=np.uint8)
+    np.testing.assert_array_equal(got, ref)
+    dec = torch.arange(0, 0x7F, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(np.array(vals), dec)
+
+
+def test_e4m3_is_the_nearest_code_brute_force():
+    vals = np.array([orc.e4m3_decode(b) for b in range(0, 0x7F)])  # all finite non-negative codes
+    rng = np.random.default_rng(10)
+    for a in rng.uniform(0, 448, 3000).astype(np.float32):
+        b = orc.e4m3_encode(float(a))
+        d = np.abs(vals - np.float64(a))
+        assert d[b] == d.min()
+
+
+def test_two_level_scale_properties():
+    """The block holding the tensor amax gets the largest E4M3 scale (448); a
+    band quantized with the whole tensor's T equals the same rows of the full
+    run; every element is scaled by s = e4m3(b) * g."""
+    x = inputs.tiny_check(128, 512)
+    for grid in ("e2m1", "e1m2"):
+        c, s, T = orc.quantize_2level(x, grid=grid, n=16, sign_seed=4)
+        z = orc.rht_rows(x, 16, 4)
+        assert T == np.abs(z).max()
+        assert s.max() == 0x7E
+        cb, sb, Tb = orc.quantize_2level(x[32:64], grid=grid, n=16, sign_seed=4, row0=32, tensor_amax=T)
+        np.testing.assert_array_equal(cb, c[32:64])
+        np.testing.assert_array_equal(sb, s[32:64])
+        deq = orc.dequantize_2level(c, s, T, grid=grid, n=16)
+        g = np.float32(orc.tensor_scale(T, grid))
+        s_el = np.repeat(np.array([[np.float32(orc.e4m3_decode(b)) * g for b in row] for row in s],
+                                  dtype=np.float32), 16, axis=1)
+        nib = np.stack([c & 0xF, c >> 4], -1).reshape(c.shape[0], -1).astype(int)
+        lev = np.array([orc.level(grid, k) for k in range(8)], dtype=np.float32)[nib & 7]
+        lev = np.where(nib & 8, -lev, lev).astype(np.float32)
+        np.testing.assert_array_equal(deq, lev * s_el)
