@@ -88,8 +88,17 @@ typedef enum { UFP4_ROUND_RTNE = 0, UFP4_ROUND_SR = 1 } ufp4_round;
  *   UE8M0: S = 2^e with e the smallest integer such that M <= qmax * 2^e
  *          [2D-block, truncation-free scale, with Qp = -Qn = qmax], clamped
  *          to [-127, 127]; stored as the byte e + 127.  Required for b x b
- *          blocks and for GEMM operands. */
-typedef enum { UFP4_SCALE_FP32 = 0, UFP4_SCALE_UE8M0 = 1 } ufp4_scale_fmt;
+ *          blocks and for GEMM operands.
+ *   E4M3:  two-level [UFP4-method: the scale hierarchy is free to follow the
+ *          hardware]: a per-tensor fp32 scale g = fp32(T / fp32(qmax * 448)),
+ *          T = amax of the whole RHT output, times a per-block E4M3 byte
+ *          b = E4M3 round-to-nearest-even, saturated at 448, of
+ *          fp32(fp32(M / qmax) / g) (0 when g = 0); elements are scaled by
+ *          fp32(1/s), s = fp32(e4m3(b) * g) (0 when s = 0).  T is stored in
+ *          the qtensor's tensor_amax.  Row-wise only, 1-D blocks, n <= 128;
+ *          the GEMM takes it for E2M1 codes with 1 x 16 blocks (native
+ *          block-scaled FP4 with E4M3 scales, g_A * g_B applied to D). */
+typedef enum { UFP4_SCALE_FP32 = 0, UFP4_SCALE_UE8M0 = 1, UFP4_SCALE_E4M3 = 2 } ufp4_scale_fmt;
 
 /* Output selection bits for ufp4_rht_quantize. */
 enum { UFP4_OUT_ROWWISE = 1, UFP4_OUT_COLWISE = 2 };
@@ -131,8 +140,11 @@ typedef struct {
  *              (multiple of 8, and of 16 for GEMM operands; the pointer
  *              16-byte aligned)
  *   scales     (rows/block_rows) x (cols/block_cols) elements, float for FP32
- *              scales and uint8 for UE8M0, leading dimension scales_ld
- *              elements (the pointer 4-byte aligned for float) */
+ *              scales and uint8 for UE8M0 and E4M3, leading dimension
+ *              scales_ld elements (the pointer 4-byte aligned for float)
+ *   tensor_amax  device float: T of the two-level scale (UFP4_SCALE_E4M3),
+ *              written by the quantizer, read by dequantize, the GEMM and the
+ *              diagnostics; unused (may be NULL) for the other formats */
 typedef struct {
     void* codes;
     void* scales;
@@ -140,6 +152,7 @@ typedef struct {
     int64_t cols;
     int64_t codes_ld;
     int64_t scales_ld;
+    float* tensor_amax;
 } ufp4_qtensor;
 
 /* ufp4_rht_quantize -- fused RHT + block-scaled 4-bit quantization.

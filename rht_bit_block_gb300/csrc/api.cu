@@ -73,7 +73,7 @@ struct BlockShape {
 
 ufp4_status check_desc(const ufp4_quant_desc* d, BlockShape* bs) {
     if (!d) return UFP4_ERR_INVALID_ARG;
-    if (d->grid < 0 || d->grid > 3 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 1)
+    if (d->grid < 0 || d->grid > 3 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 2)
         return UFP4_ERR_INVALID_ARG;
     if (!is_pow2(d->hadamard_n) || d->hadamard_n > 256) return UFP4_ERR_INVALID_ARG;
     if (d->block_rows == 1 && (d->block_cols == 16 || d->block_cols == 32)) {
@@ -94,6 +94,8 @@ ufp4_status check_out(const ufp4_qtensor* q, int64_t rows, int64_t cols, const B
     if (q->rows != rows || q->cols != cols) return UFP4_ERR_INVALID_ARG;
     if (!aligned(q->codes, 16)) return UFP4_ERR_ALIGNMENT;
     if (!aligned(q->scales, scale_fmt == UFP4_SCALE_FP32 ? 4 : 1)) return UFP4_ERR_ALIGNMENT;
+    if (scale_fmt == UFP4_SCALE_E4M3 && !q->tensor_amax) return UFP4_ERR_INVALID_ARG;
+    if (scale_fmt == UFP4_SCALE_E4M3 && !aligned(q->tensor_amax, 4)) return UFP4_ERR_ALIGNMENT;
     if (grouped) return UFP4_OK;
     if (q->codes_ld % 8) return UFP4_ERR_ALIGNMENT;
     if (q->codes_ld < cols / 2) return UFP4_ERR_INVALID_ARG;
@@ -130,6 +132,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
         T.col_tiles = (int)((cols[i] + 127) / 128);
         T.row_tiles = (int)((rows[i] + 127) / 128);
         T.tile0 = (int)tiles;
+        T.amax = rowwise[i].tensor_amax;
         tiles += (int64_t)T.col_tiles * T.row_tiles;
     }
     if (k == 0) return UFP4_OK;
@@ -146,8 +149,15 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     make_sign_bits(desc->sign_seed, n, p.sign_bits);
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
     p.group = desc->group;
-    return cuda_status(launch_quantize_rows(p, desc->grid, desc->round == UFP4_ROUND_SR,
-                                            desc->scale_fmt == UFP4_SCALE_UE8M0, num_sms_current(), stream));
+    if (desc->scale_fmt == UFP4_SCALE_E4M3)  // two-level: the tensor amax pre-pass first
+        for (int i = 0; i < k; ++i) {
+            const RowsTensor& T = p.t[i];
+            const cudaError_t e = launch_tensor_amax(T.x, T.rows, T.cols, T.ld, n, p.inv_sqrt_n, p.sign_bits,
+                                                     const_cast<float*>(T.amax), num_sms_current(), stream);
+            if (e != cudaSuccess) return UFP4_ERR_CUDA;
+        }
+    return cuda_status(launch_quantize_rows(p, desc->grid, desc->round == UFP4_ROUND_SR, desc->scale_fmt,
+                                            num_sms_current(), stream));
 }
 
 ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64_t* offsets, int ngroups,
@@ -197,6 +207,9 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     }
     if (total_rows == 0 || cols == 0) return UFP4_OK;
 
+    if (desc->scale_fmt == UFP4_SCALE_E4M3 && (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) ||
+                                               cols >= (1LL << 31)))
+        return UFP4_ERR_UNSUPPORTED;  // two-level scale: row-wise, 1-D blocks, n <= 128
     if (do_row && !do_col && !bs.is2d && !grouped && n <= 128 && total_rows < (1LL << 31) && cols < (1LL << 31)) {
         const ufp4_qtensor* rw = rowwise;
         return quantize_rows_batch(1, &x, &total_rows, &cols, &ld, desc, bs, rw, stream);
@@ -267,7 +280,10 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     ufp4_status st = check_desc(desc, &bs);
     if (st != UFP4_OK) return st;
     if (!A || !B) return UFP4_ERR_INVALID_ARG;
-    if (desc->scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_UNSUPPORTED;
+    const bool two_level = desc->scale_fmt == UFP4_SCALE_E4M3;
+    // UE8M0 block scales; the two-level scale only for E2M1 codes in 1 x 16 blocks (native FP4 with E4M3 scales)
+    if (desc->scale_fmt != UFP4_SCALE_UE8M0 && !(two_level && desc->grid >= UFP4_GRID_E2M1 && !bs.is2d && bs.bw == 16))
+        return UFP4_ERR_UNSUPPORTED;
     if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
     const int64_t M = A->rows, N = B->rows, K = A->cols;
     if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
@@ -283,9 +299,9 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     if (M == 0 || N == 0) return UFP4_OK;  // nothing to compute
     if (!aligned(D, 16) || ldd % 4) return UFP4_ERR_ALIGNMENT;
     if (K == 0) return UFP4_OK;  // D = 0 (written by run_prepared_gemm)
-    st = check_out(A, M, K, bs, UFP4_SCALE_UE8M0, false);
+    st = check_out(A, M, K, bs, desc->scale_fmt, false);
     if (st != UFP4_OK) return st;
-    st = check_out(B, N, K, bs, UFP4_SCALE_UE8M0, false);
+    st = check_out(B, N, K, bs, desc->scale_fmt, false);
     if (st != UFP4_OK) return st;
     if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
     const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
@@ -296,6 +312,9 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     out->grid = desc->grid;
     out->br = bs.is2d ? bs.b2d : 1;
     out->bc = bs.bw;
+    out->sf = desc->scale_fmt;
+    out->amax_a = A->tensor_amax;
+    out->amax_b = B->tensor_amax;
     out->workspace = workspace;
     out->workspace_bytes = workspace_bytes;
     return UFP4_OK;
@@ -416,7 +435,8 @@ ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc, 
     p.grid = desc->grid;
     p.br = bs.is2d ? bs.b2d : 1;
     p.bc = bs.bw;
-    p.po2 = desc->scale_fmt == UFP4_SCALE_UE8M0;
+    p.sf = desc->scale_fmt;
+    p.amax = q->tensor_amax;
     p.n = desc->hadamard_n;
     p.inverse = inverse_rht ? 1 : 0;
     p.inv_sqrt_n = inv_sqrt_n(desc->hadamard_n);
@@ -454,7 +474,8 @@ ufp4_status ufp4_quant_error_stats(const void* x, int64_t rows, int64_t cols, in
     p.grid = desc->grid;
     p.br = bs.is2d ? bs.b2d : 1;
     p.bc = bs.bw;
-    p.po2 = desc->scale_fmt == UFP4_SCALE_UE8M0;
+    p.sf = desc->scale_fmt;
+    p.amax = rowwise->tensor_amax;
     p.n = n;
     p.inv_sqrt_n = inv_sqrt_n(n);
     make_sign_bits(desc->sign_seed, n, p.sign_bits);

@@ -12,6 +12,8 @@ namespace ufp4 {
 
 
 __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
+    // two-level scale: g = fp32(T / fp32(qmax * 448))
+    const float g = p.sf == 2 ? __fdiv_rn(*p.amax, grid_qmax(p.grid) * 448.0f) : 0.0f;
     const int64_t cpr = p.cols / kChunk;
     const int64_t total = p.rows * cpr;
     for (int64_t base = (int64_t)blockIdx.x * blockDim.x; base < total; base += (int64_t)gridDim.x * blockDim.x) {
@@ -30,10 +32,12 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
             float s = 0.0f;
             if (valid) {
                 const int64_t si = (r / p.br) * p.scales_ld + (c + i) / p.bc;
-                if (p.po2) {
+                if (p.sf == 1) {
                     const int e = (int)((const uint8_t*)p.scales)[si] - 127;
                     s = (e >= -126) ? __uint_as_float((uint32_t)(e + 127) << 23)
                                     : __uint_as_float(0x00400000u >> (-127 - e));
+                } else if (p.sf == 2) {
+                    s = __fmul_rn(e4m3_value(((const uint8_t*)p.scales)[si]), g);
                 } else {
                     s = ((const float*)p.scales)[si];
                 }

@@ -202,9 +202,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t r[32]) {
 // Instruction descriptor of the block-scaled kinds: B scale id at 4..5,
 // A/B formats at 7..9 / 10..12, N>>3 at 17..22, UE8M0 scale type at 23,
 // M>>4 at 24..28, A scale id at 29..30; both operands K-major.
-__host__ __device__ constexpr uint32_t make_idesc(int afmt, int bfmt, int M, int N, int sf_id) {
+__host__ __device__ constexpr uint32_t make_idesc(int afmt, int bfmt, int M, int N, int sf_id, bool ue8m0 = true) {
     return ((uint32_t)sf_id << 4) | ((uint32_t)afmt << 7) | ((uint32_t)bfmt << 10) |
-           ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24) | ((uint32_t)sf_id << 29);
+           ((uint32_t)(N >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) | ((uint32_t)(M >> 4) << 24) |
+           ((uint32_t)sf_id << 29);
 }
 
 // --------------------------------------------------------------- kernel
@@ -250,6 +251,11 @@ struct GemmKParams {
     int64_t ldd;
     int vec8;           // D and ldd allow 32-byte stores
     uint32_t idesc[4];  // per MMA within a stage (scale ids)
+    // two-level scale: D = acc * g_A * g_B, g = fp32(T / den), den = fp32(qmax * 448)
+    const float* amax_a;
+    const float* amax_b;
+    float den;
+    int two_level;
 };
 
 template <int KIND, int BN, int STAGES>
@@ -384,6 +390,8 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
         // ------------------------------------------------------- epilogue
         const int q = warp - 4;  // TMEM lane quadrant of this warp
         const uint64_t stream_out = policy_evict_first();
+        // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
+        const float gab = p.two_level ? __fmul_rn(__fdiv_rn(*p.amax_a, p.den), __fdiv_rn(*p.amax_b, p.den)) : 1.0f;
         int tc = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
             const int buf = tc & 1;
@@ -396,6 +404,9 @@ gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ 
             for (int c = 0; c < BN; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol(buf) + c, r);
+                if (p.two_level)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), gab));
                 if (row < p.M) {
                     float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
                     if (n0 + c + 32 <= p.N) {
@@ -960,6 +971,8 @@ struct Plan {
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+float grid_qmax_host(int grid) { return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : (grid == 2 ? 6.0f : 2.0f)); }
+
 int ilog2(int v) {  // v a power of two
     int l = 0;
     while ((1 << l) < v) ++l;
@@ -1168,7 +1181,13 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
         for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x2, (j % 2) * 2);  // E2M1
         return run_gemm<1, kBnFp4x2, 5>(ma, mb, kp, num_sms, st);
     }
-    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x4, 0);
+    // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
+    const bool two_level = g.sf == 2;
+    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x4, 0, !two_level);
+    kp.two_level = two_level;
+    kp.amax_a = g.amax_a;
+    kp.amax_b = g.amax_b;
+    kp.den = grid_qmax_host(g.grid) * 448.0f;
     return run_gemm<2, kBnFp4x4, 4>(ma, mb, kp, num_sms, st);
 }
 

@@ -92,6 +92,7 @@ struct RowsTensor {
     int rows, cols;
     int col_tiles, row_tiles;
     int tile0;          // first tile of this tensor in the launch
+    const float* amax;  // two-level scale: the tensor amax T (device)
 };
 struct RowsParams {
     RowsTensor t[kMaxBatch];
@@ -102,7 +103,10 @@ struct RowsParams {
     uint64_t sr_seed;
     int group;
 };
-cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int num_sms, cudaStream_t st);
+cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st);
+// Two-level scale pre-pass: *amax = max |RHT(x)| over the tensor (zeroed first).
+cudaError_t launch_tensor_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, float inv_sqrt_n,
+                               const uint32_t sign_bits[8], float* amax, int num_sms, cudaStream_t st);
 cudaError_t quant_error_read_clear(int* value);
 
 // 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,
@@ -117,7 +121,9 @@ struct DequantParams {
     const uint8_t* codes;
     const void* scales;
     int64_t rows, cols, codes_ld, scales_ld;
-    int grid, br, bc, po2;
+    int grid, br, bc;
+    int sf;             // scale format: 0 fp32, 1 UE8M0, 2 two-level E4M3
+    const float* amax;  // two-level: tensor amax T
     int n, inverse;
     float inv_sqrt_n;
     uint32_t sign_bits[8];
@@ -134,7 +140,8 @@ struct QStatsParams {
     const uint8_t* codes;
     const void* scales;
     int64_t codes_ld, scales_ld;
-    int grid, br, bc, po2, n;
+    int grid, br, bc, sf, n;  // sf: 0 fp32, 1 UE8M0, 2 two-level E4M3
+    const float* amax;        // two-level: tensor amax T
     float inv_sqrt_n;
     uint32_t sign_bits[8];
     double* stats;  // device, 4 doubles
@@ -153,6 +160,9 @@ struct GemmArgs {
     GemmOperand a, b;
     int64_t M, N, K;
     int grid, br, bc;
+    int sf;                              // 1 UE8M0 block scales, 2 two-level (E4M3 x tensor scale)
+    const float* amax_a;                 // two-level: tensor amax of A and of B
+    const float* amax_b;
     float* D;
     int64_t ldd;
     void* workspace;

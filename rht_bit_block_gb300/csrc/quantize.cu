@@ -70,6 +70,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
 
 // Constants of a launch that the per-chunk code needs.
 struct Fold {
+    float g;       // two-level scale: the tensor scale fp32(T / fp32(qmax * 448))
     float inv_s;   // fp32(1/sqrt n)
     bool pow4;     // n = 4^j: 1/sqrt n = 2^-j folds exactly into the block reciprocal
     int j;         // log4 n when pow4
@@ -87,12 +88,21 @@ struct Fold {
 // is a power of two, so fp32(y * rr) = fp32(z * r) * f exactly.  SR uses
 // f = 1/step (E1M2 4, INT4 1, E2M1 1).  For other n, z = fp32(y * 1/sqrt n)
 // is formed first, as in the definition.
-template <int GRID, bool PO2>
+// SF: 0 fp32 scale, 1 UE8M0, 2 two-level (E4M3 block byte x tensor scale g).
+template <int GRID, int SF>
 __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, bool write, uint8_t* sptr) {
     constexpr float qmax = grid_qmax(GRID);
     const float Mz = __fmul_rn(My, fd.inv_s);
     const int lj = fd.pow4 ? -fd.j : 0;
-    if (PO2) {
+    if (SF == 2) {
+        // b = E4M3(fp32(fp32(M / qmax) / g)), s = fp32(e4m3(b) * g), r = fp32(1 / s)
+        const float sb = __fdiv_rn(Mz, qmax);
+        const uint32_t b8 = fd.g == 0.0f ? 0u : e4m3_byte(__fdiv_rn(sb, fd.g));
+        const float s = __fmul_rn(e4m3_value(b8), fd.g);
+        if (write) *sptr = (uint8_t)b8;
+        const float r = s == 0.0f ? 0.0f : __frcp_rn(s);
+        return __fmul_rn(r, pow2_exact(lf + lj));
+    } else if (SF == 1) {
         float r;
         const int e = scale_po2<GRID>(Mz, r);
         if (write) *sptr = (uint8_t)(e + 127);
@@ -140,17 +150,17 @@ __device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uin
     return make_uint2(out[0], out[1]);
 }
 
-template <int GRID, bool SR, bool PO2>
+template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B,
                                           uint64_t sr_seed, uint32_t stream, uint32_t group) {
     constexpr int lf = SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0));  // log2 f
-    const float ra0 = block_recip<GRID, PO2>(MA0, fd, lf, A.valid && A.w0, A.s0);
-    const float rb0 = block_recip<GRID, PO2>(MB0, fd, lf, B.valid && B.w0, B.s0);
+    const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0);
+    const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0);
     float ra1 = ra0, rb1 = rb0;
     if (split) {
-        ra1 = block_recip<GRID, PO2>(MA1, fd, lf, A.valid && A.w1, A.s1);
-        rb1 = block_recip<GRID, PO2>(MB1, fd, lf, B.valid && B.w1, B.s1);
+        ra1 = block_recip<GRID, SF>(MA1, fd, lf, A.valid && A.w1, A.s1);
+        rb1 = block_recip<GRID, SF>(MB1, fd, lf, B.valid && B.w1, B.s1);
     }
     if (!fd.pow4) {
         const uint64_t is2 = pk2(fd.inv_s, fd.inv_s);
@@ -221,6 +231,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     const int warp = tid >> 5;
     const int n = p.n;
     Fold fd;
+    fd.g = 0.0f;
     fd.inv_s = p.inv_sqrt_n;
     fd.pow4 = p.pow4;
     fd.j = p.log4n;
@@ -385,7 +396,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     B.w1 = (lbr & bmask) == 0 && lb == 3;
                     A.lin0 = (uint64_t)la * (uint64_t)p.cols + (uint64_t)col;
                     B.lin0 = (uint64_t)lbr * (uint64_t)p.cols + (uint64_t)col;
-                    emit_pair<GRID, SR, PO2>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 0u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 0u, grp_id);
                 }
             } else {
                 const bool wsc = (col & ((1 << lbw) - 1)) == 0;
@@ -423,7 +434,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     A.w1 = B.w1 = false;
                     A.lin0 = lin + (uint64_t)(2 * it) * lstep;
                     B.lin0 = A.lin0 + lstep;
-                    emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, grp_id);
                 }
             }
         }
@@ -503,7 +514,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     B.w1 = (cb & bmask) == 0 && lb == 3;
                     A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
                     B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 1u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 1u, grp_id);
                 }
             } else {
                 const int bwc = 1 << lbwc;
@@ -534,7 +545,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     A.w1 = B.w1 = false;
                     A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
                     B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 1u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 1u, grp_id);
                 }
             }
         }
@@ -572,12 +583,12 @@ struct RowsMaps {
     CUtensorMap m[kMaxBatch];
 };
 
-template <int GRID, bool SR, bool PO2>
+template <int GRID, bool SR, int SF>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
     constexpr int TC = 128, TR = 128;
     constexpr int kTileBytes = TR * TC * 2;
-    constexpr int SZ = PO2 ? 1 : 4;
+    constexpr int SZ = SF == 0 ? 4 : 1;
     constexpr int kCPR = TC / kChunk;      // 16-element chunks per tile row
     constexpr int kRPI = kThreads / kCPR;  // tile rows per thread step
     extern __shared__ uint8_t smem_raw[];
@@ -594,6 +605,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     fd.inv_s = p.inv_sqrt_n;
     fd.pow4 = p.pow4;
     fd.j = p.log4n;
+    fd.g = 0.0f;
     const int seg_row = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
     SignMasks mrow;
     {
@@ -640,6 +652,8 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
         locate(tile, t, rt, ct);
         step_r = (int)gridDim.x / p.t[t].col_tiles;
         step_c = (int)gridDim.x - step_r * p.t[t].col_tiles;
+        // two-level scale: the tensor amax was written by the pre-pass (before this launch)
+        if (SF == 2) fd.g = __fdiv_rn(*p.t[t].amax, grid_qmax(GRID) * 448.0f);
     };
     if ((int)blockIdx.x < p.num_tiles) relocate(blockIdx.x);
     int s = 0;
@@ -700,7 +714,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             A.w1 = B.w1 = false;
             A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
             B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
-            emit_pair<GRID, SR, PO2>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, (uint32_t)p.group);
+            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, (uint32_t)p.group);
         }
         // everyone is done with stage s: refill it
         __syncthreads();
@@ -800,17 +814,17 @@ cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, i
     return cudaErrorInvalidValue;
 }
 
-template <int GRID, bool SR, bool PO2>
+template <int GRID, bool SR, int SF>
 static cudaError_t launch_rows(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
     const size_t smem = (size_t)p.stages * 128 * 128 * 2 + 8 * p.stages + 128;
-    auto k = quantize_rows_kernel<GRID, SR, PO2>;
+    auto k = quantize_rows_kernel<GRID, SR, SF>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < kCtasPerSm * num_sms ? p.num_tiles : kCtasPerSm * num_sms;
     return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
 }
 
-cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int num_sms, cudaStream_t st) {
+cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
     RowsMaps maps;
     memset(&maps, 0, sizeof(maps));
     for (int t = 0; t < p.count; ++t) {
@@ -821,10 +835,12 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, bool po2, int
     }
 #define UFP4_R(G)                                                                              \
     if (grid == G) {                                                                           \
-        if (sr) return po2 ? launch_rows<G, true, true>(maps, p, num_sms, st)                  \
-                           : launch_rows<G, true, false>(maps, p, num_sms, st);                \
-        return po2 ? launch_rows<G, false, true>(maps, p, num_sms, st)                         \
-                   : launch_rows<G, false, false>(maps, p, num_sms, st);                       \
+        if (sr) return sf == 2 ? launch_rows<G, true, 2>(maps, p, num_sms, st)                 \
+                     : sf == 1 ? launch_rows<G, true, 1>(maps, p, num_sms, st)                 \
+                               : launch_rows<G, true, 0>(maps, p, num_sms, st);                \
+        return sf == 2 ? launch_rows<G, false, 2>(maps, p, num_sms, st)                        \
+             : sf == 1 ? launch_rows<G, false, 1>(maps, p, num_sms, st)                        \
+                       : launch_rows<G, false, 0>(maps, p, num_sms, st);                       \
     }
     UFP4_R(0)
     UFP4_R(1)

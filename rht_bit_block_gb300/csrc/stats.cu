@@ -46,6 +46,7 @@ __device__ __forceinline__ void reduce_add4(double v[4], double* out) {
 }
 
 __global__ void __launch_bounds__(kStatThreads) qstats_kernel(const QStatsParams p) {
+    const float g = p.sf == 2 ? __fdiv_rn(*p.amax, grid_qmax(p.grid) * 448.0f) : 0.0f;
     const int64_t cpr = p.cols / kChunk;
     const int64_t total = p.rows * cpr;
     double acc[4] = {0.0, 0.0, 0.0, 0.0};
@@ -82,9 +83,11 @@ __global__ void __launch_bounds__(kStatThreads) qstats_kernel(const QStatsParams
                 const int64_t c = cc * kChunk + i;
                 const int64_t sidx = (r / p.br) * p.scales_ld + c / p.bc;
                 float s;
-                if (p.po2) {
+                if (p.sf == 1) {
                     const int b = reinterpret_cast<const uint8_t*>(p.scales)[sidx];
                     s = b >= 1 ? __uint_as_float((uint32_t)b << 23) : __uint_as_float(0x00400000u);
+                } else if (p.sf == 2) {
+                    s = __fmul_rn(e4m3_value(reinterpret_cast<const uint8_t*>(p.scales)[sidx]), g);
                 } else {
                     s = reinterpret_cast<const float*>(p.scales)[sidx];
                 }
@@ -120,7 +123,64 @@ __global__ void __launch_bounds__(kStatThreads) dstats_kernel(const float* a, in
     reduce_add4(acc, stats);
 }
 
+// Two-level scale pre-pass: T = max |z| over the tensor, z = RHT(x) with the
+// quantizer's arithmetic (non-negative floats order like their bits, so the
+// maximum is an integer atomicMax on the bit patterns).
+__global__ void __launch_bounds__(kStatThreads) amax_kernel(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld,
+                                                            int n, float inv_sqrt_n, SignBits sb, float* amax) {
+    __shared__ unsigned int part[kStatThreads / 32];
+    const int64_t cpr = cols / kChunk;
+    const int64_t total = rows * cpr;
+    float m = 0.0f;
+    for (int64_t base = (int64_t)blockIdx.x * kStatThreads; base < total;
+         base += (int64_t)gridDim.x * kStatThreads) {
+        const int64_t qi = base + threadIdx.x;
+        const bool valid = qi < total;
+        const int64_t r = valid ? qi / cpr : 0;
+        const int64_t cc = valid ? qi % cpr : 0;
+        uint32_t w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if (valid) {
+            const uint4* src = reinterpret_cast<const uint4*>(x + r * ld + cc * kChunk);
+            const uint4 a = __ldg(src), b = __ldg(src + 1);
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+            w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        }
+        const int pos = (int)((cc * kChunk) % 256);
+        const uint32_t sgn = (sb.bits[pos / 32] >> (pos % 32)) & 0xFFFFu;
+        const int seg_lane = (int)((cc * kChunk) % (n > kChunk ? n : kChunk)) / kChunk;
+        float z[16];
+        widen16(w, sgn, z);
+        fwht16(z, n, seg_lane);
+        if (valid)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) m = fmaxf(m, fabsf(__fmul_rn(z[k], inv_sqrt_n)));
+    }
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) part[warp] = __float_as_uint(m);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        unsigned int v = 0;
+        for (int i = 0; i < kStatThreads / 32; ++i) v = v > part[i] ? v : part[i];
+        atomicMax(reinterpret_cast<unsigned int*>(amax), v);
+    }
+}
+
 }  // namespace
+
+cudaError_t launch_tensor_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, float inv_sqrt_n,
+                               const uint32_t sign_bits[8], float* amax, int num_sms, cudaStream_t st) {
+    cudaError_t e = cudaMemsetAsync(amax, 0, sizeof(float), st);
+    if (e != cudaSuccess) return e;
+    SignBits sb;
+    for (int i = 0; i < 8; ++i) sb.bits[i] = sign_bits[i];
+    const int64_t total = rows * (cols / kChunk);
+    int64_t blocks = (total + kStatThreads - 1) / kStatThreads;
+    if (blocks > (int64_t)num_sms * 8) blocks = (int64_t)num_sms * 8;
+    if (blocks < 1) blocks = 1;
+    amax_kernel<<<(unsigned)blocks, kStatThreads, 0, st>>>(x, rows, cols, ld, n, inv_sqrt_n, sb, amax);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_qstats(const QStatsParams& p, int num_sms, cudaStream_t st) {
     cudaError_t e = cudaMemsetAsync(p.stats, 0, 4 * sizeof(double), st);

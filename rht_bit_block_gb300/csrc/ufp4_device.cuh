@@ -12,6 +12,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 namespace ufp4 {
@@ -26,6 +27,19 @@ __host__ __device__ constexpr float grid_qmax(int grid) {
 // ------------------------------------------------------------- Philox4x32-10
 // Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
 // bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.
+// E4M3 byte of a >= 0, rounded to nearest even and saturated at 448 (the
+// hardware conversion), and its value.
+__device__ __forceinline__ uint32_t e4m3_byte(float a) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(a));
+    return r & 0xFFu;
+}
+__device__ __forceinline__ float e4m3_value(uint32_t b) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)(b & 0xFFu)));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+}
+
 // Value of a 4-bit code on the grid's level scale (before the block scale).
 __device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
     if (grid == 1) return (float)((nib & 8u) ? (int)nib - 16 : (int)nib);

@@ -20,7 +20,7 @@ GRID_E1M2, GRID_INT4, GRID_E2M1 = 0, 1, 2
 GRID_E2M1_R2 = 3
 GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1, "e2m1r2": GRID_E2M1_R2}
 ROUND_RTNE, ROUND_SR = 0, 1
-SCALE_FP32, SCALE_UE8M0 = 0, 1
+SCALE_FP32, SCALE_UE8M0, SCALE_E4M3 = 0, 1, 2
 OUT_ROWWISE, OUT_COLWISE = 1, 2
 
 # Every symbol include/ufp4.h declares (checked by the tests).
@@ -43,7 +43,8 @@ class QuantDesc(ctypes.Structure):
 
 class QTensor(ctypes.Structure):
     _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("rows", ctypes.c_int64),
-                ("cols", ctypes.c_int64), ("codes_ld", ctypes.c_int64), ("scales_ld", ctypes.c_int64)]
+                ("cols", ctypes.c_int64), ("codes_ld", ctypes.c_int64), ("scales_ld", ctypes.c_int64),
+                ("tensor_amax", ctypes.c_void_p)]
 
 
 class Ufp4Error(RuntimeError):
@@ -113,11 +114,12 @@ def make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=0, rounding=ROUND_RTNE
     return QuantDesc(g, block[0], block[1], n, sign_seed, rounding, scale_fmt, sr_seed, out_mask, group)
 
 
-def qtensor(codes, scales, rows: int, cols: int) -> QTensor:
+def qtensor(codes, scales, rows: int, cols: int, tensor_amax=None) -> QTensor:
     """Describe a quantized matrix held in torch tensors codes [rows, cols/2]
-    (uint8) and scales [rows/br, cols/bc] (float32 or uint8)."""
+    (uint8) and scales [rows/br, cols/bc] (float32 or uint8); tensor_amax: a
+    1-element float32 tensor for the two-level scale format."""
     return QTensor(codes.data_ptr(), scales.data_ptr(), rows, cols, codes.stride(0) * codes.element_size(),
-                   scales.stride(0))
+                   scales.stride(0), tensor_amax.data_ptr() if tensor_amax is not None else None)
 
 
 # ------------------------------------------------------------- C entry points
@@ -265,13 +267,19 @@ def alloc_quantized(rows: int, cols: int, desc: QuantDesc, device):
 
 
 def quantize(x, desc: QuantDesc, stream=None):
-    """Quantize a bf16 CUDA tensor; returns {"row": (codes, scales)?, "col": (codes, scales)?}."""
+    """Quantize a bf16 CUDA tensor; returns {"row": (codes, scales)?, "col": (codes, scales)?}
+    (and "row_amax", the tensor amax, for the two-level scale format)."""
     rows, cols = x.shape
     out = {}
     rq = cq = None
     if desc.out_mask & OUT_ROWWISE:
         out["row"] = alloc_quantized(rows, cols, desc, x.device)
-        rq = qtensor(*out["row"], rows, cols)
+        amax = None
+        if desc.scale_fmt == SCALE_E4M3:
+            import torch
+            amax = torch.zeros(1, dtype=torch.float32, device=x.device)
+            out["row_amax"] = amax
+        rq = qtensor(*out["row"], rows, cols, amax)
     if desc.out_mask & OUT_COLWISE:
         out["col"] = alloc_quantized(cols, rows, desc, x.device)
         cq = qtensor(*out["col"], cols, rows)

@@ -20,7 +20,10 @@ def gpu_quantize(x_dev: torch.Tensor, **kw):
     desc = ufp4.make_desc(**kw)
     out = ufp4.quantize(x_dev, desc)
     torch.cuda.synchronize()
-    return {k: (c.cpu().numpy(), s.cpu().numpy()) for k, (c, s) in out.items()}
+    res = {k: (v[0].cpu().numpy(), v[1].cpu().numpy()) for k, v in out.items() if k != "row_amax"}
+    if "row_amax" in out:
+        res["row_amax"] = float(out["row_amax"].cpu().item())
+    return res
 
 
 def assert_bitwise(a: np.ndarray, b: np.ndarray, what: str):

@@ -112,3 +112,20 @@ def test_diagnostics_validation(lib):
     assert lib.ufp4_error_stats(None, 8, None, 8, 4, 8, None, None) == 1
     assert lib.ufp4_error_stats(ctypes.c_void_p(0x1000), 4, ctypes.c_void_p(0x2000), 8, 4, 8,
                                 ctypes.c_void_p(0x4000), None) == 1            # ld < cols
+
+
+def test_two_level_validation(lib):
+    """The two-level scale is row-wise only, needs the tensor-amax slot, and the
+    GEMM takes it only for E2M1 codes with 1 x 16 blocks."""
+    two = ufp4.make_desc(grid="e2m1", scale_fmt=ufp4.SCALE_E4M3, out_mask=ufp4.OUT_ROWWISE)
+    q = ufp4.QTensor(0x2000, 0x3000, 64, 64, 32, 4)  # no tensor_amax
+    assert lib.ufp4_rht_quantize(ctypes.c_void_p(0x1000), 64, 64, 64, ctypes.byref(two), ctypes.byref(q), None,
+                                 None) == 1
+    both = ufp4.make_desc(grid="e2m1", scale_fmt=ufp4.SCALE_E4M3, out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
+    qa = ufp4.QTensor(0x2000, 0x3000, 64, 64, 32, 4, 0x5000)
+    assert lib.ufp4_rht_quantize(ctypes.c_void_p(0x1000), 64, 64, 64, ctypes.byref(both), ctypes.byref(qa),
+                                 ctypes.byref(qa), None) == 2
+    e1m2 = ufp4.make_desc(grid="e1m2", scale_fmt=ufp4.SCALE_E4M3)
+    A = ufp4.QTensor(0x2000, 0x3000, 128, 128, 64, 8, 0x5000)
+    assert lib.ufp4_gemm(ctypes.byref(A), ctypes.byref(A), ctypes.byref(e1m2), ctypes.c_void_p(0x4000), 128, None, 0,
+                         None) == 2
