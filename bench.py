@@ -486,6 +486,21 @@ def run_suite(args):
         emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
              kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
         del A, B, ws, D
+    # fp32 block scales (the two-scale path: bf16 partials rescaled on the CUDA cores)
+    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
+    A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+         torch.rand((M, K // 16), generator=g).add(0.5).to(dev))
+    B = (torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+         torch.rand((N, K // 16), generator=g).add(0.5).to(dev))
+    qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+    D = torch.empty((M, N), dtype=torch.float32, device=dev)
+    pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+    tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+    emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
+         2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
+    del A, B, ws, D
     # the large-sweep FPROP GEMM
     M5, N5, K5 = 16384, 7168, 7168
     desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)

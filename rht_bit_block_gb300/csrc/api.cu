@@ -282,8 +282,11 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     if (!A || !B) return UFP4_ERR_INVALID_ARG;
     const bool two_level = desc->scale_fmt == UFP4_SCALE_E4M3;
     // UE8M0 block scales; the two-level scale only for E2M1 codes in 1 x 16 blocks (native FP4 with E4M3 scales)
-    if (desc->scale_fmt != UFP4_SCALE_UE8M0 && !(two_level && desc->grid >= UFP4_GRID_E2M1 && !bs.is2d && bs.bw == 16))
+    const bool fp32_scales = desc->scale_fmt == UFP4_SCALE_FP32;  // 1-D blocks only (check_desc)
+    if (desc->scale_fmt != UFP4_SCALE_UE8M0 && !fp32_scales &&
+        !(two_level && desc->grid >= UFP4_GRID_E2M1 && !bs.is2d && bs.bw == 16))
         return UFP4_ERR_UNSUPPORTED;
+    if (fp32_scales && A->cols % 128) return UFP4_ERR_UNSUPPORTED;  // the fp32-scale path walks 128-element K tiles
     if (bs.is2d && bs.b2d != 32) return UFP4_ERR_UNSUPPORTED;
     const int64_t M = A->rows, N = B->rows, K = A->cols;
     if (B->cols != K || M < 0 || N < 0 || K < 0 || ldd < N) return UFP4_ERR_INVALID_ARG;
@@ -304,7 +307,7 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     st = check_out(B, N, K, bs, desc->scale_fmt, false);
     if (st != UFP4_OK) return st;
     if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
-    const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
+    const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw, desc->scale_fmt);
     if (workspace_bytes < need || (need && !workspace)) return UFP4_ERR_INVALID_ARG;
     if (workspace && !aligned(workspace, 256)) return UFP4_ERR_ALIGNMENT;
     out->a = {(const uint8_t*)A->codes, (const uint8_t*)A->scales, M, A->codes_ld, A->scales_ld};
@@ -496,7 +499,7 @@ ufp4_status ufp4_gemm_workspace_size(int64_t M, int64_t N, int64_t K, const ufp4
     ufp4_status st = check_desc(desc, &bs);
     if (st != UFP4_OK) return st;
     if (!bytes || M < 0 || N < 0 || K < 0) return UFP4_ERR_INVALID_ARG;
-    *bytes = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw);
+    *bytes = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw, desc->scale_fmt);
     return UFP4_OK;
 }
 

@@ -25,6 +25,7 @@
 #include <cstdint>
 #include <cstring>
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "../../include/ufp4.h"
@@ -206,6 +207,12 @@ __host__ __device__ constexpr uint32_t make_idesc(int afmt, int bfmt, int M, int
     return ((uint32_t)sf_id << 4) | ((uint32_t)afmt << 7) | ((uint32_t)bfmt << 10) |
            ((uint32_t)(N >> 3) << 17) | ((ue8m0 ? 1u : 0u) << 23) | ((uint32_t)(M >> 4) << 24) |
            ((uint32_t)sf_id << 29);
+}
+
+// kind::f16 instruction descriptor: fp32 accumulator (bits 4..5 = 1), bf16 A
+// and B (bits 7..9, 10..12 = 1), both K-major, N>>3 at 17..22, M>>4 at 24..28.
+__host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
 // --------------------------------------------------------------- kernel
@@ -756,6 +763,255 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     }
 }
 
+// ------------------------------------------- fp32-scale GEMM (two-scale)
+// D = sum over K blocks b of s_A[m,b] s_B[n,b] P_b[m,n], P_b = the block's
+// product of the plain grid levels (UFP4 summary, 数据集: s_B = amax / qmax in
+// fp32; 方法: the quantized GEMM Y^ = Q_G(XH') Q_G(WH')^T).  Plain fp32 block
+// scales cannot be folded into a block-scaled MMA exactly, so each 16- or
+// 32-element block runs as its own bf16 MMA (tcgen05.mma kind::f16, the
+// levels are exact in bf16) into one of four tensor-memory partial buffers,
+// and eight rescaler warps fold s_A s_B P_b into fp32 register accumulators.
+// The CUDA-core multiply-adds bound it (two per output element and block).
+constexpr int kF32sBN = 128;        // output tile 128 x 128
+constexpr int kF32sStages = 3;
+constexpr int kF32sThreads = 384;   // warps 0-3: TMA, MMA, idle; warps 4-11: rescalers
+constexpr int kF32sPBufs = 4;       // 128-column partial buffers in tensor memory
+
+struct F32sCfg {
+    static constexpr int kAtom = kBM * kBKBytes;                 // 128 rows x 64 bf16 = 16 KB
+    static constexpr int kABytes = 2 * kAtom;                    // a stage holds 128 K elements
+    static constexpr int kBBytes = 2 * kAtom;
+    static constexpr int kSaBytes = 128 * 8 * 4;                 // s_A: 128 rows x up to 8 blocks
+    static constexpr int kSbBytes = 8 * kF32sBN * 4;             // s_B: up to 8 blocks x 128 columns
+    static constexpr int kOffB = kF32sStages * kABytes;
+    static constexpr int kOffSa = kOffB + kF32sStages * kBBytes;
+    static constexpr int kOffSb = kOffSa + kF32sStages * kSaBytes;
+    static constexpr int kOffBars = kOffSb + kF32sStages * kSbBytes;
+    static constexpr int kNumBars = 2 * kF32sStages + 2 * kF32sPBufs;
+    static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024;
+    static_assert(kSmem <= 232448, "shared memory overflow");
+};
+
+struct F32sKParams {
+    int M, N, k_tiles, kb_per_tile;  // k_tiles: 128-element K tiles; blocks per K tile (8 or 4)
+    int m_tiles, n_tiles;
+    int kb_pad;                       // s_A row length (floats) in the workspace
+    float* D;
+    int64_t ldd;
+    uint32_t idesc;                   // kind::f16, bf16 x bf16 -> fp32, M = 128, N = 128
+    int mmas_per_block;               // 1 (16-element blocks) or 2 (32)
+};
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }"
+        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__global__ void __launch_bounds__(kF32sThreads, 1)
+gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
+                 const __grid_constant__ CUtensorMap tmap_sa, const __grid_constant__ CUtensorMap tmap_sb,
+                 const F32sKParams p) {
+    using C = F32sCfg;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* gbase = smem_raw + (base - raw);
+    const uint32_t bars = base + C::kOffBars;
+    auto full_bar = [&](int s) { return bars + 8u * s; };
+    auto empty_bar = [&](int s) { return bars + 8u * (kF32sStages + s); };
+    auto pfull_bar = [&](int b) { return bars + 8u * (2 * kF32sStages + b); };
+    auto pempty_bar = [&](int b) { return bars + 8u * (2 * kF32sStages + kF32sPBufs + b); };
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * C::kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * C::kNumBars + 4);
+    auto stage_a = [&](int s) { return base + s * C::kABytes; };
+    auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
+    const float* sa_s = reinterpret_cast<const float*>(gbase + C::kOffSa);
+    const float* sb_s = reinterpret_cast<const float*>(gbase + C::kOffSb);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_tiles = p.m_tiles * p.n_tiles;
+    const int kb = p.kb_per_tile;
+    constexpr int kRescalers = 8;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kF32sStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1 + kRescalers);  // the MMA commit and every rescaler warp
+        }
+        for (int b = 0; b < kF32sPBufs; ++b) {
+            mbar_init(pfull_bar(b), 1);
+            mbar_init(pempty_bar(b), kRescalers);
+        }
+        *abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
+                     "r"(512));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    griddep_wait();
+    griddep_launch();
+
+    if (warp == 0 && lane == 0) {
+        // ---------------------------------------------------- TMA producer
+        int s = 0;
+        uint32_t ph = 0;
+        const uint64_t keep = policy_evict_last();
+        for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
+            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+            for (int kt = 0; kt < p.k_tiles; ++kt) {
+                if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                mbar_expect_tx(full_bar(s), C::kABytes + C::kBBytes + 128 * kb * 4 + kb * kF32sBN * 4);
+                for (int j = 0; j < 2; ++j) {
+                    tma_load_2d(stage_a(s) + j * C::kAtom, &tmap_a, (2 * kt + j) * kBKBytes, mb * kBM, full_bar(s),
+                                keep);
+                    tma_load_2d(stage_b(s) + j * C::kAtom, &tmap_b, (2 * kt + j) * kBKBytes, nb * kF32sBN,
+                                full_bar(s), keep);
+                }
+                tma_load_2d(base + C::kOffSa + s * C::kSaBytes, &tmap_sa, kt * kb, mb * kBM, full_bar(s), keep);
+                tma_load_2d(base + C::kOffSb + s * C::kSbBytes, &tmap_sb, 0, nb * p.k_tiles * kb + kt * kb,
+                            full_bar(s), keep);
+                if (++s == kF32sStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1 && lane == 0) {
+        // ----------------------------------------------------- MMA issuer
+        int s = 0, pb = 0;
+        uint32_t ph = 0, pph = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int kt = 0; kt < p.k_tiles && ok; ++kt) {
+                if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int j = 0; j < kb; ++j) {
+                    if (!mbar_wait(pempty_bar(pb), pph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // block j covers 16 * mmas_per_block K elements: 32-byte steps inside 128-byte atoms
+                    for (int q = 0; q < p.mmas_per_block; ++q) {
+                        const int step = j * p.mmas_per_block + q;  // 16-element step within the stage
+                        const uint64_t da = sw128_desc(stage_a(s) + (step >> 2) * C::kAtom) + 2 * (step & 3);
+                        const uint64_t db = sw128_desc(stage_b(s) + (step >> 2) * C::kAtom) + 2 * (step & 3);
+                        mma_f16(tmem + pb * kF32sBN, da, db, p.idesc, q > 0 ? 1u : 0u);
+                    }
+                    tc_commit(pfull_bar(pb));
+                    if (++pb == kF32sPBufs) {
+                        pb = 0;
+                        pph ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(empty_bar(s));  // the operand tiles may be refilled once these MMAs are done
+                if (++s == kF32sStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+        }
+        if (!ok) *abort_flag = 1;
+    } else if (warp >= 4) {
+        // -------------------------------------------------------- rescalers
+        const int q = warp & 3;               // tensor-memory lane quadrant (rows 32q .. 32q+31)
+        const int half = (warp - 4) >> 2;      // columns 64 half .. +63
+        const int row_in_tile = q * 32 + lane;
+        int s = 0, pb = 0;
+        uint32_t ph = 0, pph = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
+            float acc[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+            bool ok = true;
+            for (int kt = 0; kt < p.k_tiles && ok; ++kt) {
+                if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), ph)) || *abort_flag) {
+                    ok = false;
+                    break;
+                }
+                const float* sa = sa_s + s * (C::kSaBytes / 4) + row_in_tile * kb;  // this row's block scales
+                const float* sb = sb_s + s * (C::kSbBytes / 4);                      // [block][128 columns]
+                for (int j = 0; j < kb; ++j) {
+                    if (!__all_sync(0xFFFFFFFFu, mbar_wait(pfull_bar(pb), pph))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    uint32_t r0[32], r1[32];
+                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + pb * kF32sBN + half * 64;
+                    tmem_ld32(taddr, r0);
+                    tmem_ld32(taddr + 32, r1);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(pempty_bar(pb));  // the partial buffer may be refilled
+                    if (++pb == kF32sPBufs) {
+                        pb = 0;
+                        pph ^= 1u;
+                    }
+                    const float a = sa[j];
+                    const float4* sbv = reinterpret_cast<const float4*>(sb + j * kF32sBN + half * 64);
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 b = sbv[c4];
+                        acc[4 * c4 + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 0]), b.x), a, acc[4 * c4 + 0]);
+                        acc[4 * c4 + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 1]), b.y), a, acc[4 * c4 + 1]);
+                        acc[4 * c4 + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 2]), b.z), a, acc[4 * c4 + 2]);
+                        acc[4 * c4 + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 3]), b.w), a, acc[4 * c4 + 3]);
+                    }
+#pragma unroll
+                    for (int c4 = 0; c4 < 8; ++c4) {
+                        const float4 b = sbv[8 + c4];
+                        acc[32 + 4 * c4 + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 0]), b.x), a, acc[32 + 4 * c4 + 0]);
+                        acc[32 + 4 * c4 + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 1]), b.y), a, acc[32 + 4 * c4 + 1]);
+                        acc[32 + 4 * c4 + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 2]), b.z), a, acc[32 + 4 * c4 + 2]);
+                        acc[32 + 4 * c4 + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 3]), b.w), a, acc[32 + 4 * c4 + 3]);
+                    }
+                }
+                if (!ok) break;
+                // this stage's scales have been read: release it (with the MMA's commit)
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty_bar(s));
+                if (++s == kF32sStages) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+            const int row = mb * kBM + row_in_tile;
+            const int n0 = nb * kF32sBN + half * 64;
+            if (row < p.M) {
+                float* dst = p.D + (int64_t)row * p.ldd + n0;
+                for (int c = 0; c < 64; ++c)
+                    if (n0 + c < p.N) dst[c] = acc[c];
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(512));
+    }
+}
+
 // ------------------------------------------------------------- prep kernels
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
 // elements.  One thread: one row, one 128-element K group (4 scale cells).
@@ -935,6 +1191,71 @@ __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
         cell;
 }
 
+// Level value of a 4-bit code (E1M2 k/4, INT4 two's complement k, E2M1 codes
+// for grids 2 and 3).
+__device__ __forceinline__ float decode_level_gemm(int grid, uint32_t nib) {
+    if (grid == 1) return (float)((nib & 8u) ? (int)nib - 16 : (int)nib);
+    const uint32_t k = nib & 7u;
+    float v;
+    if (grid == 0) v = (float)k * 0.25f;
+    else v = k < 4 ? (float)k * 0.5f : (k == 4 ? 2.0f : (k == 5 ? 3.0f : (k == 6 ? 4.0f : 6.0f)));
+    return (nib & 8u) ? -v : v;
+}
+
+// fp32 block scales: bf16 copies of the levels (exact) and the scales in the
+// two-scale kernel's layout (A: [row][block]; B: [tile][block][128 columns]).
+// One thread: one row, one 16-element chunk.
+struct F32sSide {
+    const uint8_t* codes;
+    const float* scales;
+    int64_t codes_ld, scales_ld;
+    int rows, rows_cover, tile_rows, transposed;
+    uint16_t* levels;
+    float* scales_out;
+};
+struct F32sPrep {
+    F32sSide side[2];
+    int K, bc, grid;
+};
+
+__global__ void __launch_bounds__(256) prep_f32s_kernel(const F32sPrep p) {
+    griddep_wait();
+    griddep_launch();
+    const F32sSide& s = p.side[blockIdx.z];
+    const int64_t cpr = p.K / 16;
+    const int64_t idx = (int64_t)blockIdx.x * 256 + threadIdx.x;
+    if (idx >= (int64_t)s.rows_cover * cpr) return;
+    const int row = (int)(idx / cpr);
+    const int ch = (int)(idx - (int64_t)row * cpr);
+    const bool live = row < s.rows;
+    if (live) {
+        const uint2 code = *reinterpret_cast<const uint2*>(s.codes + (int64_t)row * s.codes_ld + ch * 8);
+        uint32_t out[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t word = i < 4 ? code.x : code.y;
+            const float lo = decode_level_gemm(p.grid, (word >> (8 * (i & 3))) & 0xFu);
+            const float hi = decode_level_gemm(p.grid, (word >> (8 * (i & 3) + 4)) & 0xFu);
+            out[i] = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(lo)) |
+                     ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(hi)) << 16);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(s.levels + (int64_t)row * p.K + ch * 16);
+        dst[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        dst[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    }
+    if ((ch * 16) % p.bc == 0) {  // the first chunk of a block moves its scale (0 on padding rows)
+        const int64_t kbt = p.K / p.bc;
+        const int b = ch * 16 / p.bc;
+        const float v = live ? s.scales[(int64_t)row * s.scales_ld + b] : 0.0f;
+        if (s.transposed) {
+            const int t = row / s.tile_rows, c = row - t * s.tile_rows;
+            s.scales_out[((int64_t)t * kbt + b) * s.tile_rows + c] = v;
+        } else {
+            s.scales_out[(int64_t)row * kbt + b] = v;
+        }
+    }
+}
+
 // ------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -960,7 +1281,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes
 }
 
 struct Plan {
-    int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X
+    int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X, 3 fp32 block scales (bf16 partials rescaled)
     int bn;            // B tile rows (output tile columns)
     int64_t k_bytes;   // bytes of K per row in the MMA operand
     int64_t k_tiles;
@@ -984,9 +1305,29 @@ int ilog2(int v) {  // v a power of two
 // at the top of this file).
 
 
-Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
+Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf) {
     Plan pl{};
     (void)br;
+    if (sf == 0) {
+        // fp32 block scales: bf16 level copies and the scales, laid out for the two-scale kernel
+        pl.kind = 3;
+        pl.bn = kF32sBN;
+        pl.k_bytes = K * 2;
+        pl.k_tiles = K / 128;
+        const int64_t kbt = K / bc;  // blocks along K
+        const int64_t mt = (M + kBM - 1) / kBM, nt = (N + kF32sBN - 1) / kF32sBN;
+        size_t off = 0;
+        pl.fp8_a = off;  // bf16 levels of A
+        off = align256(off + (size_t)M * K * 2);
+        pl.fp8_b = off;  // bf16 levels of B
+        off = align256(off + (size_t)N * K * 2);
+        pl.sfa = off;    // s_A [mt * 128][kbt]
+        off = align256(off + (size_t)mt * kBM * kbt * 4);
+        pl.sfb = off;    // s_B [nt][kbt][128]
+        off = align256(off + (size_t)nt * kbt * kF32sBN * 4);
+        pl.total = off;
+        return pl;
+    }
     pl.kind = grid >= 2 ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
     pl.bn = pl.kind == 0 ? kBnFp8 : (pl.kind == 1 ? kBnFp4x2 : kBnFp4x4);
     pl.k_bytes = grid >= 2 ? K / 2 : K;
@@ -1079,15 +1420,43 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc) {
-    return make_plan(M, N, K, grid, br, bc).total;
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf) {
+    return make_plan(M, N, K, grid, br, bc, sf).total;
 }
 
 // Operand preparation: FP8 widening (E1M2/INT4) and scale chunks into the workspace.
 cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
+    if (g.sf == 0) {
+        if (g.K % 128) return cudaErrorNotSupported;
+        const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
+        if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+        uint8_t* ws = (uint8_t*)g.workspace;
+        F32sPrep pp{};
+        pp.K = (int)g.K;
+        pp.bc = g.bc;
+        pp.grid = g.grid;
+        for (int side = 0; side < 2; ++side) {
+            const GemmOperand& op = side ? g.b : g.a;
+            F32sSide& ps = pp.side[side];
+            ps.codes = op.codes;
+            ps.scales = reinterpret_cast<const float*>(op.scales);
+            ps.codes_ld = op.codes_ld;
+            ps.scales_ld = op.scales_ld;
+            ps.rows = (int)op.rows;
+            ps.tile_rows = side ? kF32sBN : kBM;
+            ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;
+            ps.levels = reinterpret_cast<uint16_t*>(ws + (side ? pl.fp8_b : pl.fp8_a));
+            ps.scales_out = reinterpret_cast<float*>(ws + (side ? pl.sfb : pl.sfa));
+            ps.transposed = side;
+        }
+        const int64_t chunks = (int64_t)std::max(pp.side[0].rows_cover, pp.side[1].rows_cover) * (g.K / 16);
+        const int64_t blocks = (chunks + 255) / 256;
+        if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
+        return launch_pdl(prep_f32s_kernel, dim3((unsigned)blocks, 1, 2), dim3(256), 0, st, pp);
+    }
     if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
     if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
-    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
+    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
     PrepParams pp{};
@@ -1122,9 +1491,45 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.
 cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
+    if (g.sf == 0) {
+        if (g.K % 128) return cudaErrorNotSupported;
+        const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
+        if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+        uint8_t* ws = (uint8_t*)g.workspace;
+        const int64_t kbt = g.K / g.bc;
+        const int kb = (int)(128 / g.bc);
+        const int64_t mt = (g.M + kBM - 1) / kBM, nt = (g.N + kF32sBN - 1) / kF32sBN;
+        CUtensorMap ma, mb, msa, msb;
+        if (!make_map(&ma, ws + pl.fp8_a, g.M, g.K * 2, g.K * 2, kBM)) return cudaErrorInvalidValue;
+        if (!make_map(&mb, ws + pl.fp8_b, g.N, g.K * 2, g.K * 2, kF32sBN)) return cudaErrorInvalidValue;
+        if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + pl.sfa, (uint64_t)kbt, (uint64_t)(mt * kBM),
+                           (uint64_t)kbt * 4, (uint32_t)kb, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws + pl.sfb, kF32sBN, (uint64_t)(nt * kbt),
+                           kF32sBN * 4, kF32sBN, (uint32_t)kb, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+        F32sKParams kp{};
+        kp.M = (int)g.M;
+        kp.N = (int)g.N;
+        kp.k_tiles = (int)(g.K / 128);
+        kp.kb_per_tile = kb;
+        kp.m_tiles = (int)mt;
+        kp.n_tiles = (int)nt;
+        kp.kb_pad = (int)kbt;
+        kp.D = g.D;
+        kp.ldd = g.ldd;
+        kp.idesc = make_idesc_f16(kBM, kF32sBN);
+        kp.mmas_per_block = g.bc / 16;
+        auto k = gemm_f32s_kernel;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, F32sCfg::kSmem);
+        if (e != cudaSuccess) return e;
+        const int tiles = kp.m_tiles * kp.n_tiles;
+        const int grid = tiles < num_sms ? tiles : num_sms;
+        return launch_pdl(k, dim3(grid), dim3(kF32sThreads), (size_t)F32sCfg::kSmem, st, ma, mb, msa, msb, kp);
+    }
     if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
     if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;
-    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc);
+    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
     CUtensorMap ma, mb;

@@ -160,7 +160,7 @@ struct GemmArgs {
     GemmOperand a, b;
     int64_t M, N, K;
     int grid, br, bc;
-    int sf;                              // 1 UE8M0 block scales, 2 two-level (E4M3 x tensor scale)
+    int sf;                              // 0 fp32 block scales, 1 UE8M0, 2 two-level (E4M3 x tensor scale)
     const float* amax_a;                 // two-level: tensor amax of A and of B
     const float* amax_b;
     float* D;
@@ -168,7 +168,7 @@ struct GemmArgs {
     void* workspace;
     size_t workspace_bytes;
 };
-size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc);
+size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf);
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st);
 cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st);

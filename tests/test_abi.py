@@ -73,9 +73,10 @@ def test_host_validation_rejects_bad_arguments(lib):
                                  ctypes.byref(q), None) == 2
 
 
-def test_gemm_rejects_fp32_scales(lib):
+def test_gemm_fp32_scales_need_128_element_k_tiles(lib):
+    """fp32 block scales run the two-scale path, which walks 128-element K tiles."""
     desc = ufp4.make_desc(scale_fmt=ufp4.SCALE_FP32)
-    A = ufp4.QTensor(0x2000, 0x3000, 128, 128, 64, 8)
+    A = ufp4.QTensor(0x2000, 0x3000, 128, 96, 48, 6)
     D = ctypes.c_void_p(0x4000)
     assert lib.ufp4_gemm(ctypes.byref(A), ctypes.byref(A), ctypes.byref(desc), D, 128, None, 0, None) == 2
 
