@@ -770,11 +770,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 // scales cannot be folded into a block-scaled MMA exactly, so each 16- or
 // 32-element block runs as its own bf16 MMA (tcgen05.mma kind::f16, the
 // levels are exact in bf16) into one of four tensor-memory partial buffers,
-// and eight rescaler warps fold s_A s_B P_b into fp32 register accumulators.
+// and sixteen rescaler warps (4 lane quadrants x 4 groups of 32 columns) fold
+// s_A s_B P_b into fp32 register accumulators.
 // The CUDA-core multiply-adds bound it (two per output element and block).
 constexpr int kF32sBN = 128;        // output tile 128 x 128
 constexpr int kF32sStages = 3;
-constexpr int kF32sThreads = 384;   // warps 0-3: TMA, MMA, idle; warps 4-11: rescalers
+constexpr int kF32sThreads = 640;   // warps 0-3: TMA, MMA, idle; warps 4-19: rescalers
 constexpr int kF32sPBufs = 4;       // 128-column partial buffers in tensor memory
 
 struct F32sCfg {
@@ -835,7 +836,7 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     const int lane = threadIdx.x & 31;
     const int num_tiles = p.m_tiles * p.n_tiles;
     const int kb = p.kb_per_tile;
-    constexpr int kRescalers = 8;
+    constexpr int kRescalers = 16;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kF32sStages; ++s) {
@@ -932,15 +933,15 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     } else if (warp >= 4) {
         // -------------------------------------------------------- rescalers
         const int q = warp & 3;               // tensor-memory lane quadrant (rows 32q .. 32q+31)
-        const int half = (warp - 4) >> 2;      // columns 64 half .. +63
+        const int grp = (warp - 4) >> 2;       // columns 32 grp .. +31
         const int row_in_tile = q * 32 + lane;
         int s = 0, pb = 0;
         uint32_t ph = 0, pph = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
             const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
-            float acc[64];
+            float acc[32];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) acc[c] = 0.0f;
+            for (int c = 0; c < 32; ++c) acc[c] = 0.0f;
             bool ok = true;
             for (int kt = 0; kt < p.k_tiles && ok; ++kt) {
                 if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_bar(s), ph)) || *abort_flag) {
@@ -955,10 +956,8 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         break;
                     }
                     tc_fence_after();
-                    uint32_t r0[32], r1[32];
-                    const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + pb * kF32sBN + half * 64;
-                    tmem_ld32(taddr, r0);
-                    tmem_ld32(taddr + 32, r1);
+                    uint32_t r[32];
+                    tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + pb * kF32sBN + grp * 32, r);
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(pempty_bar(pb));  // the partial buffer may be refilled
@@ -967,22 +966,14 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         pph ^= 1u;
                     }
                     const float a = sa[j];
-                    const float4* sbv = reinterpret_cast<const float4*>(sb + j * kF32sBN + half * 64);
+                    const float4* sbv = reinterpret_cast<const float4*>(sb + j * kF32sBN + grp * 32);
 #pragma unroll
                     for (int c4 = 0; c4 < 8; ++c4) {
                         const float4 b = sbv[c4];
-                        acc[4 * c4 + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 0]), b.x), a, acc[4 * c4 + 0]);
-                        acc[4 * c4 + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 1]), b.y), a, acc[4 * c4 + 1]);
-                        acc[4 * c4 + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 2]), b.z), a, acc[4 * c4 + 2]);
-                        acc[4 * c4 + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(r0[4 * c4 + 3]), b.w), a, acc[4 * c4 + 3]);
-                    }
-#pragma unroll
-                    for (int c4 = 0; c4 < 8; ++c4) {
-                        const float4 b = sbv[8 + c4];
-                        acc[32 + 4 * c4 + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 0]), b.x), a, acc[32 + 4 * c4 + 0]);
-                        acc[32 + 4 * c4 + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 1]), b.y), a, acc[32 + 4 * c4 + 1]);
-                        acc[32 + 4 * c4 + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 2]), b.z), a, acc[32 + 4 * c4 + 2]);
-                        acc[32 + 4 * c4 + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(r1[4 * c4 + 3]), b.w), a, acc[32 + 4 * c4 + 3]);
+                        acc[4 * c4 + 0] = __fmaf_rn(__fmul_rn(__uint_as_float(r[4 * c4 + 0]), b.x), a, acc[4 * c4 + 0]);
+                        acc[4 * c4 + 1] = __fmaf_rn(__fmul_rn(__uint_as_float(r[4 * c4 + 1]), b.y), a, acc[4 * c4 + 1]);
+                        acc[4 * c4 + 2] = __fmaf_rn(__fmul_rn(__uint_as_float(r[4 * c4 + 2]), b.z), a, acc[4 * c4 + 2]);
+                        acc[4 * c4 + 3] = __fmaf_rn(__fmul_rn(__uint_as_float(r[4 * c4 + 3]), b.w), a, acc[4 * c4 + 3]);
                     }
                 }
                 if (!ok) break;
@@ -996,11 +987,17 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             }
             if (!ok) break;
             const int row = mb * kBM + row_in_tile;
-            const int n0 = nb * kF32sBN + half * 64;
+            const int n0 = nb * kF32sBN + grp * 32;
             if (row < p.M) {
                 float* dst = p.D + (int64_t)row * p.ldd + n0;
-                for (int c = 0; c < 64; ++c)
-                    if (n0 + c < p.N) dst[c] = acc[c];
+                if (n0 + 32 <= p.N) {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4)
+                        *reinterpret_cast<float4*>(dst + c) = make_float4(acc[c], acc[c + 1], acc[c + 2], acc[c + 3]);
+                } else {
+                    for (int c = 0; c < 32; ++c)
+                        if (n0 + c < p.N) dst[c] = acc[c];
+                }
             }
         }
     }
