@@ -12,15 +12,23 @@
 //    scale_vec::1X): for a pair of 1 x 16 blocks with exponents e0, e1 the
 //    hardware scale is max(e0, e1) and the elements of the smaller block are
 //    shifted down by the difference d (exact for d <= 16 in E5M2).
+//  * The two-level format's E4M3 block scales (E2M1, 1 x 16) ride in
+//    kind::mxf4nvf4 as UE4M3 (never negative); the product of the two fp32
+//    tensor scales multiplies the accumulator in the epilogue.
 //
-// Kernel: persistent, one CTA (8 warps) per SM walking 128 x BN output tiles.
-// Warp 0 lane 0 drives TMA (128B-swizzled 2-D tiles of A and B, 512-byte
-// scale chunks) through a ring of mbarriers; warp 1 lane 0 copies the scales
-// into tensor memory (tcgen05.cp) and issues the MMAs (tcgen05.mma) into one
-// of two tensor-memory accumulators; warps 4..7 read the other accumulator
-// back (tcgen05.ld) and store fp32, so a tile's epilogue overlaps the next
-// tile's main loop.  Every wait is bounded: on expiry the kernel records an
-// error code, lets its copies and MMAs finish and returns.
+// Kernel: persistent CTA pairs (clusters of two CTAs on two SMs, 8 warps
+// each) walking 256 x BN output tiles with tcgen05.mma .cta_group::2.  Warp 0
+// lane 0 of each CTA drives TMA (128B-swizzled 2-D tiles of A and B, boxes of
+// replicated scale chunks) through a ring of mbarriers; warp 1 lane 0 of the
+// even CTA copies the scales into tensor memory (tcgen05.cp) and issues the
+// MMAs for both CTAs into one of two tensor-memory accumulators; warps 4..7
+// of both CTAs read the other accumulator back (tcgen05.ld) and store fp32,
+// so a tile's epilogue overlaps the next tile's main loop.  Every wait is
+// bounded: on expiry the kernel records an error code, lets its copies and
+// MMAs finish and returns.
+//
+// Plain fp32 block scales cannot ride in a block-scaled MMA; they take the
+// two-scale kernel at the end of this file.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -45,14 +53,16 @@ constexpr uint32_t kWaitLimit = 1u << 22;  // bounded polling; each poll may sle
 constexpr uint32_t kSuspendNs = 1000;
 constexpr int kErrTimeout = 1;
 
-// Output tile widths.  FP8 runs on CTA pairs with 256 x 224 tiles: two
+// Output tile widths.  Both paths run on CTA pairs.  FP8: 256 x 224 tiles, two
 // 224-column accumulators plus two sets of scale columns fit the 512
 // tensor-memory columns, and the wider tile gives each MMA instruction more
-// work (issuing a tcgen05 instruction costs a fixed time).  FP4 runs 128 x 192
-// tiles on single CTAs.
-constexpr int kBnFp8 = 224, kBnFp4x2 = 192, kBnFp4x4 = 192;
-// FP8 CTA-pair ring: kPairStages stages of kPairKps K tiles each
-constexpr int kPairKps = 2, kPairStages = 3;
+// work (issuing a tcgen05 instruction costs a fixed time).  FP4 needs two to
+// four times the scale columns per K tile, so its tiles are 256 x 192.
+constexpr int kBnFp8 = 224, kBnFp4 = 192;
+// CTA-pair rings: stages of KPS K tiles each (FP4 stages hold one K tile of
+// 256 elements, as much MMA work as two FP8 K tiles of 128)
+constexpr int kPairKps = 2, kPairStages = 3;          // FP8
+constexpr int kPairStagesFp4x2 = 5, kPairStagesFp4x4 = 4;
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -123,12 +133,6 @@ __device__ __forceinline__ void st_out8(float* dst, const uint32_t* r, uint64_t 
                  : "memory");
 }
 
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-                 ::"r"(dst), "l"((uint64_t)src), "r"(bytes), "r"(bar)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
@@ -144,47 +148,9 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return d;
 }
 
-// Plain (no swizzle) descriptor for a 32-row x 16-byte scale chunk quarter:
-// 8-row core matrices 128 bytes apart.
-__device__ __forceinline__ uint64_t plain_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
-    d |= (uint64_t)(128u >> 4) << 32;
-    d |= (uint64_t)1 << 46;
-    return d;
-}
-
-template <int KIND>  // 0: mxf8f6f4 scale_vec::1X, 1: mxf4 scale_vec::2X, 2: mxf4nvf4 scale_vec::4X
-__device__ __forceinline__ void mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                    uint32_t sfb, uint32_t accumulate) {
-    if (KIND == 0) {
-        asm volatile(
-            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
-            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-            : "memory");
-    } else if (KIND == 1) {
-        asm volatile(
-            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
-            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-            : "memory");
-    } else {
-        asm volatile(
-            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-            "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
-            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-            : "memory");
-    }
-}
-
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void tc_cp_scales(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t r[32]) {
@@ -215,245 +181,17 @@ __host__ __device__ constexpr uint32_t make_idesc_f16(int M, int N) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// --------------------------------------------------------------- kernel
-// KIND 0: FP8 E5M2 operands (4 MMAs of K=32 per stage, one scale chunk per
-// 128 rows); KIND 1/2: packed FP4 (4 MMAs of K=64 per stage; 2 or 4 scales per
-// MMA -> 2 or 4 chunks per 128 rows per stage).
-template <int KIND, int BN, int STAGES>
-struct GemmCfg {
-    static constexpr int kChunksPerStage = KIND == 0 ? 1 : (KIND == 1 ? 2 : 4);
-    static constexpr int kHalvesB = (BN + 127) / 128;  // 128-row chunk blocks per B tile
-    static constexpr int kABytes = kBM * kBKBytes;      // 16 KB, multiple of 1024
-    static constexpr int kBBytes = BN * kBKBytes;       // multiple of 1024
-    static constexpr int kSfaBytes = kChunksPerStage * kChunkBytes;
-    static constexpr int kSfbBytes = kHalvesB * kChunksPerStage * kChunkBytes;
-    static constexpr int kTxBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;  // bytes landing per stage
-    // shared memory: [A x STAGES][B x STAGES][SFA x STAGES][SFB x STAGES][barriers, flags]
-    static constexpr int kOffB = STAGES * kABytes;
-    static constexpr int kOffSfa = kOffB + STAGES * kBBytes;
-    static constexpr int kOffSfb = kOffSfa + STAGES * kSfaBytes;
-    static constexpr int kOffBars = kOffSfb + STAGES * kSfbBytes;
-    static constexpr int kNumBars = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
-    static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024 /*alignment slack*/;
-    // tensor memory: two accumulators of BN fp32 columns, then two sets of
-    // scale columns (one 512-byte chunk = 4 columns, replicated over the 4
-    // lane quadrants); k-tiles alternate between the sets
-    static constexpr int kSfaCols = kChunksPerStage * 4;
-    static constexpr int kSfbCols = kChunksPerStage * 4 * kHalvesB;
-    static constexpr int kTmemCols = 512;
-    static constexpr int kSfaCol = 2 * BN;
-    static __device__ __forceinline__ int kAccCol(int buf) { return buf * BN; }
-    static constexpr int kSfbCol = 2 * BN + 2 * kSfaCols;
-    static_assert(kSfbCol + 2 * kSfbCols <= kTmemCols, "tensor memory overflow");
-    static_assert(kSmem <= 232448, "shared memory overflow");
-    static_assert(BN % 32 == 0 && BN <= 256, "epilogue reads 32 columns at a time");
-};
-
-struct GemmKParams {
-    const uint8_t* sfa;  // scale chunks of A: [ceil(M/128)][k chunks] x 512 B
-    const uint8_t* sfb;  // scale chunks of B: [ceil(N/BN) * halves][k chunks] x 512 B
-    int64_t sf_chunks_k;  // chunks along K per 128-row block
-    int M, N, k_tiles, m_tiles, n_tiles;
-    float* D;
-    int64_t ldd;
-    int vec8;           // D and ldd allow 32-byte stores
-    uint32_t idesc[4];  // per MMA within a stage (scale ids)
-    // two-level scale: D = acc * g_A * g_B, g = fp32(T / den), den = fp32(qmax * 448)
-    const float* amax_a;
-    const float* amax_b;
-    float den;
-    int two_level;
-};
-
-template <int KIND, int BN, int STAGES>
-__global__ void __launch_bounds__(kGemmThreads, 1)
-gemm_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-            const GemmKParams p) {
-    using C = GemmCfg<KIND, BN, STAGES>;
-    extern __shared__ uint8_t smem_raw[];
-    const uint32_t raw = smem_u32(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;  // 128B-swizzled tiles need 1024-byte alignment
-    uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t bars = base + C::kOffBars;
-    auto full_bar = [&](int s) { return bars + 8u * s; };
-    auto empty_bar = [&](int s) { return bars + 8u * (STAGES + s); };
-    auto accf_bar = [&](int b) { return bars + 8u * (2 * STAGES + b); };
-    auto acce_bar = [&](int b) { return bars + 8u * (2 * STAGES + 2 + b); };
-    const uint32_t drain_bar = bars + 8u * (2 * STAGES + 4);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffBars + 8 * C::kNumBars);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + C::kOffBars + 8 * C::kNumBars + 4);
-
-    auto stage_a = [&](int s) { return base + s * C::kABytes; };
-    auto stage_b = [&](int s) { return base + C::kOffB + s * C::kBBytes; };
-    auto stage_sfa = [&](int s) { return base + C::kOffSfa + s * C::kSfaBytes; };
-    auto stage_sfb = [&](int s) { return base + C::kOffSfb + s * C::kSfbBytes; };
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int num_tiles = p.m_tiles * p.n_tiles;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(accf_bar(b), 1);
-            mbar_init(acce_bar(b), 4);  // one arrival per epilogue warp
-        }
-        mbar_init(drain_bar, 1);
-        *abort_flag = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_slot)),
-                     "r"(C::kTmemCols));
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // operands come from the prep kernel; D may still be read by the kernel before
-    griddep_wait();
-    griddep_launch();
-
-    if (warp == 0 && lane == 0) {
-        // ---------------------------------------------------- TMA producer
-        int it = 0;
-        const uint64_t keep = policy_evict_last();
-        for (int tile = blockIdx.x; tile < num_tiles && !*abort_flag; tile += gridDim.x) {
-            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
-            const uint8_t* sfa_blk = p.sfa + (int64_t)mb * p.sf_chunks_k * kChunkBytes;
-            for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-                const int s = it % STAGES;
-                if (!mbar_wait(empty_bar(s), ((it / STAGES) & 1) ^ 1)) {
-                    *abort_flag = 1;
-                    break;
-                }
-                mbar_expect_tx(full_bar(s), C::kTxBytes);
-                tma_load_2d(stage_a(s), &tmap_a, kt * kBKBytes, mb * kBM, full_bar(s), keep);
-                tma_load_2d(stage_b(s), &tmap_b, kt * kBKBytes, nb * BN, full_bar(s), keep);
-                bulk_load(stage_sfa(s), sfa_blk + (int64_t)kt * C::kSfaBytes, C::kSfaBytes, full_bar(s));
-                for (int h = 0; h < C::kHalvesB; ++h) {
-                    const uint8_t* src = p.sfb + ((int64_t)(nb * C::kHalvesB + h) * p.sf_chunks_k +
-                                                  (int64_t)kt * C::kChunksPerStage) * kChunkBytes;
-                    bulk_load(stage_sfb(s) + h * C::kChunksPerStage * kChunkBytes, src,
-                              C::kChunksPerStage * kChunkBytes, full_bar(s));
-                }
-            }
-        }
-        if (*abort_flag) {
-            // let every issued copy land before the CTA leaves (bounded)
-            for (int k = it > STAGES ? it - STAGES : 0; k < it; ++k) mbar_wait(full_bar(k % STAGES), (k / STAGES) & 1);
-        }
-    } else if (warp == 1 && lane == 0) {
-        // ----------------------------------------------------- MMA issuer
-        int it = 0, tc = 0;
-        bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tc) {
-            const int buf = tc & 1;
-            if (!mbar_wait(acce_bar(buf), ((tc >> 1) & 1) ^ 1)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t acc = tmem + C::kAccCol(buf);
-            for (int kt = 0; kt < p.k_tiles; ++kt, ++it) {
-                const int s = it % STAGES;
-                if (!mbar_wait(full_bar(s), (it / STAGES) & 1) || *abort_flag) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const int set = it & 1;
-                const uint32_t sfa_t = tmem + C::kSfaCol + set * C::kSfaCols;
-                const uint32_t sfb_t = tmem + C::kSfbCol + set * C::kSfbCols;
-                // chunk c of A -> columns 4c; chunk c of B's half h -> columns 4(c*halves + h)
-                for (int c = 0; c < C::kChunksPerStage; ++c)
-                    tc_cp_scales(sfa_t + 4 * c, plain_desc(stage_sfa(s) + c * kChunkBytes));
-                for (int h = 0; h < C::kHalvesB; ++h)
-                    for (int c = 0; c < C::kChunksPerStage; ++c)
-                        tc_cp_scales(sfb_t + 4 * (c * C::kHalvesB + h),
-                                     plain_desc(stage_sfb(s) + (h * C::kChunksPerStage + c) * kChunkBytes));
-                const uint64_t da = sw128_desc(stage_a(s));
-                const uint64_t db = sw128_desc(stage_b(s));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    // chunk holding MMA j's scales: FP8 1X -> 0 (byte j), FP4 2X -> j/2 (bytes 0-1 / 2-3), FP4 4X -> j
-                    const int chunk = KIND == 0 ? 0 : (KIND == 1 ? j / 2 : j);
-                    // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
-                    mma<KIND>(acc, da + 2 * j, db + 2 * j, p.idesc[j], sfa_t + 4 * chunk,
-                              sfb_t + 4 * chunk * C::kHalvesB, (kt > 0 || j > 0) ? 1u : 0u);
-                }
-                tc_commit(empty_bar(s));  // frees the stage once these MMAs have read it
-            }
-            if (ok) tc_commit(accf_bar(buf));  // the accumulator is complete once every MMA above is
-        }
-        if (!ok) *abort_flag = 1;
-        tc_commit(drain_bar);  // arrives when every MMA issued by this thread has completed
-        mbar_wait(drain_bar, 0);
-    } else if (warp >= 4) {
-        // ------------------------------------------------------- epilogue
-        const int q = warp - 4;  // TMEM lane quadrant of this warp
-        const uint64_t stream_out = policy_evict_first();
-        // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
-        const float gab = p.two_level ? __fmul_rn(__fdiv_rn(*p.amax_a, p.den), __fdiv_rn(*p.amax_b, p.den)) : 1.0f;
-        int tc = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
-            const int buf = tc & 1;
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), (tc >> 1) & 1));
-            if (!ok || *abort_flag) break;
-            tc_fence_after();
-            const int mb = tile % p.m_tiles, nb = tile / p.m_tiles;
-            const int row = mb * kBM + q * 32 + lane;
-            const int n0 = nb * BN;
-            for (int c = 0; c < BN; c += 32) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + C::kAccCol(buf) + c, r);
-                if (p.two_level)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), gab));
-                if (row < p.M) {
-                    float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
-                    if (n0 + c + 32 <= p.N) {
-                        if (p.vec8) {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 8) st_out8(dst + i, r + i, stream_out);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 32; i += 4) st_out4(dst + i, r + i, stream_out);
-                        }
-                    } else {
-                        for (int i = 0; i < 32; ++i)
-                            if (n0 + c + i < p.N) dst[i] = __uint_as_float(r[i]);
-                    }
-                }
-            }
-            // the accumulator has been read: hand it back to the MMA issuer
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acce_bar(buf));
-        }
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols));
-    }
-}
-
-// ------------------------------------------------- CTA-pair FP8 kernel
-// The FP8 path (E1M2 / INT4 widened to E5M2) on CTA pairs: a cluster of two
-// CTAs on two SMs computes a 256 x 192 output tile with tcgen05.mma
-// .cta_group::2.  Each CTA holds its own 128 rows of A and half (96 rows) of
-// B, so per SM the shared-memory and L2 traffic per MMA FLOP drops by about
-// 30 % against the single-CTA 128 x 192 tile; the accumulator rows of a CTA
-// sit in its own tensor memory.  Both CTAs hold the full 192-row scale chunks
-// of B.  The even CTA ("leader") issues the MMAs for both; both CTAs' copies
-// complete on the leader's stage barrier, and the leader's commits arrive on
-// the barriers of both CTAs.
+// ------------------------------------------------------ CTA-pair kernel
+// A cluster of two CTAs on two SMs computes a 256 x BN output tile with
+// tcgen05.mma .cta_group::2: the FP8 path (E1M2 / INT4 widened to E5M2) and
+// the native FP4 kinds (E2M1 codes straight from the quantizer).  Each CTA
+// holds its own 128 rows of A and half (BN/2 rows) of B, so per SM the
+// shared-memory and L2 traffic per MMA FLOP drops by about 30 % against a
+// single-CTA 128 x BN tile; the accumulator rows of a CTA sit in its own
+// tensor memory.  Both CTAs hold the scale chunks of all BN rows of B.  The
+// even CTA ("leader") issues the MMAs for both; both CTAs' copies complete on
+// the leader's stage barrier, and the leader's commits arrive on the barriers
+// of both CTAs.
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -488,13 +226,28 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
         : "memory");
 }
 
-__device__ __forceinline__ void mma_pair_fp8(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                             uint32_t sfb, uint32_t accumulate) {
-    asm volatile(
-        "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
-        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
-        ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
-        : "memory");
+template <int KIND>  // 0: mxf8f6f4 scale_vec::1X, 1: mxf4 scale_vec::2X, 2: mxf4nvf4 scale_vec::4X
+__device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                         uint32_t sfb, uint32_t accumulate) {
+    if (KIND == 0) {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    } else if (KIND == 1) {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    } else {
+        asm volatile(
+            "{ .reg .pred p; setp.ne.b32 p, %6, 0;\n"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p; }"
+            ::"r"(d_tmem), "l"(a), "l"(b), "r"(idesc), "r"(sfa), "r"(sfb), "r"(accumulate)
+            : "memory");
+    }
 }
 
 // arrives on the mbarrier at this offset in both CTAs once every MMA / copy
@@ -529,22 +282,28 @@ __device__ __forceinline__ uint64_t sf256_desc(uint32_t saddr) {
 
 // A stage holds KPS consecutive 128-byte K tiles ("atoms") of each operand,
 // and the scale chunks of those K tiles in the replicated layout the prep
-// kernel writes for this path (each 512-byte chunk four times, so that one
-// tcgen05.cp .128x256b fills 8 tensor-memory columns of all 128 lanes): A's
-// chunks of K tiles kt, kt+1 side by side (one copy per two K tiles), B's two
-// 128-row parts of one K tile side by side (one copy per K tile).  The scale
-// stages come first in shared memory, the 1024-aligned operand stages after.
-template <int STAGES, int KPS>
+// kernels write for this path: each 512-byte chunk (128 rows x 4 scale bytes)
+// stored four times, so that one tcgen05.cp .128x256b fills 8 tensor-memory
+// columns of all 128 lanes from two chunks.  A K tile has CPK chunks per 128
+// rows (FP8 1X: 1; FP4 2X: 2, one per two MMAs; FP4 4X: 4, one per MMA);
+// chunk u = j * CPK + c of the stage (K tile j, chunk c):
+//  * A: chunks 2v and 2v+1 side by side in copy v (columns 4u of the A set);
+//  * B: its two 128-row parts side by side in copy u (columns 8u, 8u + 4).
+// The scale stages come first in shared memory, the 1024-aligned operand
+// stages after; stages alternate between two sets of scale columns.
+template <int KIND, int STAGES, int KPS>
 struct PairCfg {
-    static constexpr int BN = kBnFp8;                    // output columns of a pair tile
+    static constexpr int CPK = KIND == 0 ? 1 : (KIND == 1 ? 2 : 4);
+    static constexpr int BN = KIND == 0 ? kBnFp8 : kBnFp4;  // output columns of a pair tile
     static constexpr int kBRows = BN / 2;                // B rows held per CTA
     static constexpr int kAAtom = kBM * kBKBytes;        // 16 KB
-    static constexpr int kBAtom = kBRows * kBKBytes;     // 14 KB
+    static constexpr int kBAtom = kBRows * kBKBytes;
     static constexpr int kABytes = KPS * kAAtom;
     static constexpr int kBBytes = KPS * kBAtom;
+    static constexpr int kChunks = KPS * CPK;                // chunks per 128 rows per stage
     static constexpr int kRep = 4 * kChunkBytes;             // one replicated chunk: 2 KB
-    static constexpr int kSfaBytes = KPS * kRep;             // this CTA's 128 rows, KPS K tiles
-    static constexpr int kSfbBytes = 2 * KPS * kRep;         // both 128-row parts of B, KPS K tiles
+    static constexpr int kSfaBytes = kChunks * kRep;         // this CTA's 128 rows
+    static constexpr int kSfbBytes = 2 * kChunks * kRep;     // both 128-row parts of B
     static constexpr int kTxPerAtom = kAAtom + kBAtom;       // operand bytes per CTA per K tile
     static constexpr int kTxScales = kSfaBytes + kSfbBytes;  // scale bytes per CTA per stage (full boxes)
     static constexpr int kOffSfa = 0;
@@ -555,31 +314,38 @@ struct PairCfg {
     static constexpr int kNumBars = 2 * STAGES + 4 + 1;  // full, empty, acc_full x2, acc_empty x2, drain
     static constexpr int kSmem = kOffBars + 8 * kNumBars + 16 + 1024;
     static constexpr int kTmemCols = 512;
-    static constexpr int kSfaCol = 2 * BN;               // two sets of 8 columns (K tiles kt, kt+1)
-    static constexpr int kSfbCol = 2 * BN + 16;          // two sets of 8 columns (parts 0, 1 of one K tile)
-    static_assert(kSfbCol + 16 <= kTmemCols, "tensor memory overflow");
+    static constexpr int kASet = 4 * kChunks;            // scale columns of A per set
+    static constexpr int kBSet = 8 * kChunks;            // scale columns of B per set
+    static constexpr int kSfaCol = 2 * BN;
+    static constexpr int kSfbCol = 2 * BN + 2 * kASet;
+    static_assert(kSfbCol + 2 * kBSet <= kTmemCols, "tensor memory overflow");
     static_assert(kSmem <= 232448, "shared memory overflow");
     static_assert(kOffA % 1024 == 0 && kAAtom % 1024 == 0 && kBAtom % 1024 == 0,
                   "128B-swizzled tiles need 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN > 128 && BN <= 256, "two scale parts of B; 32-column epilogue reads");
-    static_assert(KPS == 2, "one scale copy of A covers two K tiles");
+    static_assert(kChunks % 2 == 0, "A's scale copies hold two chunks");
 };
 
 struct PairKParams {
     int M, N, k_tiles, m_pairs, n_tiles;
-    int64_t sf_chunks_k;  // chunk rows per 128-row block along K
+    int64_t sf_chunks_k;  // chunks along K per 128-row block
     float* D;
     int64_t ldd;
     int vec8;
     uint32_t idesc[4];
+    // two-level scale: D = acc * g_A * g_B, g = fp32(T / den), den = fp32(qmax * 448)
+    const float* amax_a;
+    const float* amax_b;
+    float den;
+    int two_level;
 };
 
-template <int STAGES, int KPS>
+template <int KIND, int STAGES, int KPS>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
                  const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
                  const PairKParams p) {
-    using C = PairCfg<STAGES, KPS>;
+    using C = PairCfg<KIND, STAGES, KPS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -644,9 +410,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
             const int arow = ablk * kBM;
             const int brow = nb * C::BN + (int)peer * C::kBRows;
-            // 512-byte rows of the replicated chunk arrays: 4 per K tile for A, 8 for B
-            const int sfa_row = ablk * p.k_tiles * 4;
-            const int sfb_row = nb * p.k_tiles * 8;
+            // 512-byte rows of the replicated chunk arrays: 4 per chunk for A, 8 for B
+            const int sfa_row = ablk * (int)p.sf_chunks_k * 4;
+            const int sfb_row = nb * (int)p.sf_chunks_k * 8;
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
                     *abort_flag = 1;
@@ -661,8 +427,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     tma_load_pair(stage_b(s) + j * C::kBAtom, &tmap_b, (kt0 + j) * kBKBytes, brow, fb, keep);
                 }
                 // the scales of the stage's K tiles are contiguous: one box each
-                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * 4, fb, keep);
-                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * 8, fb, keep);
+                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * C::CPK * 4, fb, keep);
+                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * C::CPK * 8, fb, keep);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -673,8 +439,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // ------------------------------------------------ MMA issuer (leader only)
         int s = 0, tc = 0;
         uint32_t ph = 0;
-        int it = 0;  // K tiles issued so far (alternates B's scale sets)
-        int sc = 0;  // stages issued so far (alternates A's scale sets)
+        int sc = 0;  // stages issued so far (alternates the scale sets)
         bool ok = true;
         for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++tc) {
             const int buf = tc & 1;
@@ -692,19 +457,27 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 tc_fence_after();
                 const int kt0 = ks * KPS;
                 const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
-                // A's scales of both K tiles of the stage: columns sfa_t (kt0) and sfa_t + 4 (kt0 + 1)
-                const uint32_t sfa_t = tmem + C::kSfaCol + (sc++ & 1) * 8;
-                tc_cp_scales_pair_256(sfa_t, sf256_desc(stage_sfa(s)));
-                for (int j = 0; j < nk; ++j, ++it) {
-                    // B's scales of this K tile: part 0 at sfb_t, part 1 at sfb_t + 4
-                    const uint32_t sfb_t = tmem + C::kSfbCol + (it & 1) * 8;
-                    tc_cp_scales_pair_256(sfb_t, sf256_desc(stage_sfb(s) + j * 2 * C::kRep));
+                const uint32_t sfa_t = tmem + C::kSfaCol + (sc & 1) * C::kASet;
+                const uint32_t sfb_t = tmem + C::kSfbCol + (sc & 1) * C::kBSet;
+                ++sc;
+                for (int j = 0; j < nk; ++j) {
                     const uint64_t da = sw128_desc(stage_a(s) + j * C::kAAtom);
                     const uint64_t db = sw128_desc(stage_b(s) + j * C::kBAtom);
 #pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        mma_pair_fp8(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t + 4 * j, sfb_t,
-                                     (kt0 + j > 0 || q > 0) ? 1u : 0u);
+                    for (int q = 0; q < 4; ++q) {
+                        // chunk of MMA q: FP8 1X -> 0 (byte q), FP4 2X -> q/2 (bytes 0-1 / 2-3), FP4 4X -> q
+                        const int cq = C::CPK == 1 ? 0 : (C::CPK == 2 ? q >> 1 : q);
+                        const int u = j * C::CPK + cq;
+                        if (C::CPK == 4 || q == 0 || (C::CPK == 2 && q == 2)) {
+                            // first MMA of chunk u: A's copy of chunks u, u+1 (u even), B's copy of chunk u
+                            if ((u & 1) == 0)
+                                tc_cp_scales_pair_256(sfa_t + 4 * u, sf256_desc(stage_sfa(s) + (u >> 1) * 2 * C::kRep));
+                            tc_cp_scales_pair_256(sfb_t + 8 * u, sf256_desc(stage_sfb(s) + u * 2 * C::kRep));
+                        }
+                        // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
+                        mma_pair<KIND>(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t + 4 * u, sfb_t + 8 * u,
+                                       (kt0 + j > 0 || q > 0) ? 1u : 0u);
+                    }
                 }
                 tc_commit_pair_both(empty_bar(s));  // frees stage s in both CTAs
                 if (++s == STAGES) {
@@ -721,6 +494,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // ------------------------------------------------- epilogue (both CTAs)
         const int q = warp - 4;
         const uint64_t stream_out = policy_evict_first();
+        // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
+        const float gab = p.two_level ? __fmul_rn(__fdiv_rn(*p.amax_a, p.den), __fdiv_rn(*p.amax_b, p.den)) : 1.0f;
         int tc = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++tc) {
             const int buf = tc & 1;
@@ -733,6 +508,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             for (int c = 0; c < C::BN; c += 32) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + buf * C::BN + c, r);
+                if (p.two_level)
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), gab));
                 if (row < p.M) {
                     float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
                     if (n0 + c + 32 <= p.N) {
@@ -1047,30 +825,19 @@ struct PrepParams {
     int lhw;           // log2 of the hardware scale block: 4 (E2M1 1x16) or 5
 };
 
-// Scale chunks are grouped per GEMM tile: tile t = row / tile_rows holds
-// ceil(tile_rows / 128) blocks of 128 rows; inside a block, row w and scale
-// cell j sit at (w % 32) * 16 + (w / 32) * 4 + j (the tcgen05.cp 32x128b
-// layout).  Returns the byte offset of cell 0 of this row.
-__device__ __forceinline__ int64_t chunk_row_offset(const PrepSide& s, int chunks_k, int row) {
-    const int halves = (s.tile_rows + 127) >> 7;
-    const int t = row / s.tile_rows;
-    const int rr = row - t * s.tile_rows;
-    const int64_t cb = (int64_t)t * halves + (rr >> 7);
-    const int w = rr & 127;
-    return cb * chunks_k * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
-}
-
-// FP8 path: replicated chunks.  GEMM tile t (tile_rows rows), K tile kt and
-// 128-row part h of the tile own four copies of the 512-byte chunk at
-// (((t * k_tiles + kt) * parts + h) * 4 + copy) * 512, with row w and scale
-// cell j at (w % 32) * 16 + (w / 32) * 4 + j in each copy.  Returns the offset
-// of copy 0 for this row.
-__device__ __forceinline__ int64_t rep_chunk_offset(const PrepSide& s, int k_tiles, int row, int kt) {
+// Replicated scale chunks of the CTA-pair kernel.  Chunk g along K (g = K
+// tile * chunks per K tile + c) of the 128-row part h of GEMM tile t
+// (tile_rows rows) is stored four times, at
+// ((((t * chunks_k + g) * parts + h) * 4 + copy) * 512, with row w of the part
+// and scale cell byte j at (w % 32) * 16 + (w / 32) * 4 + j in each copy
+// (the tcgen05.cp 32x128b chunk layout).  Returns the offset of copy 0 for
+// this row.
+__device__ __forceinline__ int64_t rep_chunk_offset(const PrepSide& s, int chunks_k, int row, int g) {
     const int parts = (s.tile_rows + 127) >> 7;
     const int t = row / s.tile_rows;
     const int rr = row - t * s.tile_rows;
     const int h = rr >> 7, w = rr & 127;
-    return ((((int64_t)t * k_tiles + kt) * parts + h) * 4) * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
+    return ((((int64_t)t * chunks_k + g) * parts + h) * 4) * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -1165,27 +932,44 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
                                      (lane & 3) * kChunkBytes) = word;
 }
 
-// E2M1: only the scales move, into the chunk layout (hardware blocks of 16 or
-// 32 elements).  Same CTA shape as above; a lane owns one 4-byte chunk cell.
+// E2M1: only the scales move, into the replicated chunk layout (hardware
+// blocks of 16 or 32 elements, one scale byte each: UE8M0, or E4M3 for the
+// two-level format).  A warp writes one chunk: lane i builds the chunk's
+// 16-byte line i (cells of rows i, i + 32, i + 64, i + 96 of the part) and
+// stores it into the four copies, so every store of the warp covers 512
+// contiguous bytes.  blockIdx.x: 8 chunks (one per warp), blockIdx.z: operand.
 __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
     griddep_wait();
     griddep_launch();
     const PrepSide& s = p.side[blockIdx.z];
-    const int row = blockIdx.x * 8 + threadIdx.y;
-    if (row >= s.rows_cover) return;
-    const int c = blockIdx.y * 32 + threadIdx.x;
-    if (c >= p.chunks_k) return;
-    uint32_t cell = 0;
-    if (row < s.rows) {
-        const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+    const int parts = (s.tile_rows + 127) >> 7;
+    const int64_t blocks = (int64_t)(s.rows_cover / s.tile_rows) * parts;  // 128-row parts
+    const int64_t item = (int64_t)blockIdx.x * 8 + threadIdx.y;            // (part block, chunk) pair
+    if (item >= blocks * p.chunks_k) return;                               // whole warps
+    const int g = (int)(item % p.chunks_k);
+    const int64_t pb = item / p.chunks_k;
+    const int t = (int)(pb / parts), h = (int)(pb % parts);
+    const int i = threadIdx.x;
+    uint32_t cell[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const int k0 = (c * 4 + j) << p.lhw;
-            if (k0 < p.K) cell |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
+    for (int c = 0; c < 4; ++c) {
+        const int rr = h * 128 + i + 32 * c;  // row within the tile
+        const int row = t * s.tile_rows + rr;
+        uint32_t v = 0;
+        if (rr < s.tile_rows && row < s.rows) {
+            const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int k0 = (g * 4 + j) << p.lhw;
+                if (k0 < p.K) v |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
+            }
         }
+        cell[c] = v;
     }
-    *reinterpret_cast<uint32_t*>(s.out_chunks + chunk_row_offset(s, p.chunks_k, row) + (int64_t)c * kChunkBytes) =
-        cell;
+    const uint4 line = make_uint4(cell[0], cell[1], cell[2], cell[3]);
+    uint8_t* dst = s.out_chunks + ((((int64_t)t * p.chunks_k + g) * parts + h) * 4) * kChunkBytes + i * 16;
+#pragma unroll
+    for (int copy = 0; copy < 4; ++copy) *reinterpret_cast<uint4*>(dst + copy * kChunkBytes) = line;
 }
 
 // Level value of a 4-bit code (E1M2 k/4, INT4 two's complement k, E2M1 codes
@@ -1297,9 +1081,6 @@ int ilog2(int v) {  // v a power of two
     return l;
 }
 
-// FP4 tiles are 128 x 192 on single CTAs with a 5-stage ring (4 for 16-element
-// scales); FP8 tiles are 256 x kBnFp8 on CTA pairs (the tile widths are set
-// at the top of this file).
 
 
 Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf) {
@@ -1326,7 +1107,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
         return pl;
     }
     pl.kind = grid >= 2 ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
-    pl.bn = pl.kind == 0 ? kBnFp8 : (pl.kind == 1 ? kBnFp4x2 : kBnFp4x4);
+    pl.bn = pl.kind == 0 ? kBnFp8 : kBnFp4;
     pl.k_bytes = grid >= 2 ? K / 2 : K;
     pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
     const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
@@ -1340,45 +1121,32 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
         pl.fp8_b = off;
         off = align256(off + (size_t)N * K);
     }
-    const size_t copies = pl.kind == 0 ? 4 : 1;  // FP8: replicated chunks
-    pl.sfa = off;
-    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes * copies);
+    pl.sfa = off;  // replicated chunks: four copies of each
+    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes * 4);
     pl.sfb = off;
-    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes * copies);
+    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes * 4);
     pl.total = off;
     return pl;
 }
 
-template <int KIND, int BN, int STAGES>
-cudaError_t run_gemm(const CUtensorMap& ma, const CUtensorMap& mb, const GemmKParams& kp, int num_sms,
-                     cudaStream_t st) {
-    using C = GemmCfg<KIND, BN, STAGES>;
-    auto k = gemm_kernel<KIND, BN, STAGES>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-    if (e != cudaSuccess) return e;
-    const int tiles = kp.m_tiles * kp.n_tiles;
-    const int grid = tiles < num_sms ? tiles : num_sms;  // persistent: one CTA per SM
-    return launch_pdl(k, dim3(grid), dim3(kGemmThreads), (size_t)C::kSmem, st, ma, mb, kp);
-}
-
 // Co-resident two-CTA clusters of the pair kernel on this device (cached).
-template <int STAGES, int KPS>
+template <int KIND, int STAGES, int KPS>
 int pair_clusters(const cudaLaunchConfig_t& cfg) {
     static int cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] > 0) return cached[dev];
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<STAGES, KPS>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<KIND, STAGES, KPS>, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
     return n;
 }
 
-template <int STAGES, int KPS>
+template <int KIND, int STAGES, int KPS>
 cudaError_t run_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
                           const PairKParams& kp, cudaStream_t st) {
-    using C = PairCfg<STAGES, KPS>;
-    auto k = gemm_pair_kernel<STAGES, KPS>;
+    using C = PairCfg<KIND, STAGES, KPS>;
+    auto k = gemm_pair_kernel<KIND, STAGES, KPS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1395,7 +1163,7 @@ cudaError_t run_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int max_clusters = pair_clusters<STAGES, KPS>(cfg);
+    const int max_clusters = pair_clusters<KIND, STAGES, KPS>(cfg);
     if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
     const int tiles = kp.m_pairs * kp.n_tiles;
     cfg.gridDim = dim3(2 * (tiles < max_clusters ? tiles : max_clusters));  // persistent: one pair per two SMs
@@ -1478,12 +1246,21 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
     pp.lbr = ilog2(g.br);
     pp.lbc = ilog2(g.bc);
     pp.lhw = pl.kind == 2 ? 4 : 5;
-    // 32 groups (FP8) or 32 chunk cells (FP4) per CTA along K
-    const int64_t kslabs = pl.kind == 0 ? (pl.chunks_k * 4 + 31) / 32 : (pl.chunks_k + 31) / 32;
-    if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
-    const dim3 grid((unsigned)row_blocks, (unsigned)kslabs, 2);
-    if (pl.kind == 0) return launch_pdl(prep_widen_kernel, grid, dim3(32, 8), 0, st, pp);
-    return launch_pdl(prep_scales_kernel, grid, dim3(32, 8), 0, st, pp);
+    if (pl.kind == 0) {
+        // 32 groups of 32 elements per CTA along K, 8 rows per CTA
+        const int64_t kslabs = (pl.chunks_k * 4 + 31) / 32;
+        if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
+        return launch_pdl(prep_widen_kernel, dim3((unsigned)row_blocks, (unsigned)kslabs, 2), dim3(32, 8), 0, st, pp);
+    }
+    // FP4: one warp per (128-row part, chunk)
+    int64_t items = 0;
+    for (int side = 0; side < 2; ++side) {
+        const PrepSide& ps = pp.side[side];
+        items = std::max(items, (int64_t)(ps.rows_cover / ps.tile_rows) * ((ps.tile_rows + 127) / 128) * pl.chunks_k);
+    }
+    const int64_t blocks = (items + 7) / 8;
+    if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
+    return launch_pdl(prep_scales_kernel, dim3((unsigned)blocks, 1, 2), dim3(32, 8), 0, st, pp);
 }
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.
@@ -1529,68 +1306,54 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
-    CUtensorMap ma, mb;
+    (void)num_sms;
+    // CTA pairs, 256 x bn tiles: A 128 rows per CTA, B bn/2 rows per CTA.
+    // FP8 reads the widened copies in the workspace, FP4 the codes themselves.
     const void* a_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
     const void* b_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
     const int64_t a_pitch = pl.kind == 0 ? g.K : g.a.codes_ld;
     const int64_t b_pitch = pl.kind == 0 ? g.K : g.b.codes_ld;
+    CUtensorMap ma, mb, msa, msb;
     if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn)) return cudaErrorInvalidValue;
+    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn / 2)) return cudaErrorInvalidValue;
+    // scale chunks as rows of 128 x 32-bit words (one 512-byte copy of a chunk
+    // per row); boxes: one stage's chunks, 4 rows per chunk for A, 8 for B
+    const int cpk = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
+    const int kps = pl.kind == 0 ? kPairKps : 1;
+    const int64_t a_blocks = (g.M + kBM - 1) / kBM;
+    const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
+    if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k * 4),
+                       kChunkBytes, 128, (uint32_t)(4 * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k * 4),
+                       kChunkBytes, 128, (uint32_t)(8 * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    PairKParams pk{};
+    pk.M = (int)g.M;
+    pk.N = (int)g.N;
+    pk.k_tiles = (int)pl.k_tiles;
+    pk.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
+    pk.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
+    pk.sf_chunks_k = pl.chunks_k;
+    pk.D = g.D;
+    pk.ldd = g.ldd;
+    pk.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
     if (pl.kind == 0) {
-        // FP8: CTA pairs, 256 x 192 tiles (A: 128 rows per CTA, B: 96 rows per CTA)
-        CUtensorMap ma, mb, msa, msb;
-        const int64_t a_blocks = (g.M + kBM - 1) / kBM;
-        const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
-        if (!make_map(&ma, ws + pl.fp8_a, g.M, pl.k_bytes, g.K, kBM)) return cudaErrorInvalidValue;
-        if (!make_map(&mb, ws + pl.fp8_b, g.N, pl.k_bytes, g.K, pl.bn / 2)) return cudaErrorInvalidValue;
-        // scale chunks as rows of 128 x 32-bit words (one 512-byte chunk per row)
-        // (boxes: the replicated chunks of the K tiles of one stage, 4 rows per K tile for A, 8 for B)
-        if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128,
-                           (uint64_t)(a_blocks * pl.chunks_k * 4), kChunkBytes, 128, 4 * kPairKps,
-                           CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-        if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128,
-                           (uint64_t)(b_blocks * pl.chunks_k * 4), kChunkBytes, 128, 8 * kPairKps,
-                           CU_TENSOR_MAP_SWIZZLE_NONE))
-            return cudaErrorInvalidValue;
-        PairKParams pk{};
-        pk.M = (int)g.M;
-        pk.N = (int)g.N;
-        pk.k_tiles = (int)pl.k_tiles;
-        pk.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
-        pk.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
-        pk.sf_chunks_k = pl.chunks_k;
-        pk.D = g.D;
-        pk.ldd = g.ldd;
-        pk.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
         for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp8, j);  // E5M2 x E5M2, M = 256
-        (void)num_sms;
-        return run_gemm_pair<kPairStages, kPairKps>(ma, mb, msa, msb, pk, st);
+        return run_gemm_pair<0, kPairStages, kPairKps>(ma, mb, msa, msb, pk, st);
     }
-    GemmKParams kp{};
-    kp.sfa = ws + pl.sfa;
-    kp.sfb = ws + pl.sfb;
-    kp.sf_chunks_k = pl.chunks_k;
-    kp.M = (int)g.M;
-    kp.N = (int)g.N;
-    kp.k_tiles = (int)pl.k_tiles;
-    kp.m_tiles = (int)((g.M + kBM - 1) / kBM);
-    kp.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
-    kp.D = g.D;
-    kp.ldd = g.ldd;
-    kp.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
     if (pl.kind == 1) {
-        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x2, (j % 2) * 2);  // E2M1
-        return run_gemm<1, kBnFp4x2, 5>(ma, mb, kp, num_sms, st);
+        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, (j % 2) * 2);  // E2M1
+        return run_gemm_pair<1, kPairStagesFp4x2, 1>(ma, mb, msa, msb, pk, st);
     }
     // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
     const bool two_level = g.sf == 2;
-    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, kBM, kBnFp4x4, 0, !two_level);
-    kp.two_level = two_level;
-    kp.amax_a = g.amax_a;
-    kp.amax_b = g.amax_b;
-    kp.den = grid_qmax_host(g.grid) * 448.0f;
-    return run_gemm<2, kBnFp4x4, 4>(ma, mb, kp, num_sms, st);
+    for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, 0, !two_level);
+    pk.two_level = two_level;
+    pk.amax_a = g.amax_a;
+    pk.amax_b = g.amax_b;
+    pk.den = grid_qmax_host(g.grid) * 448.0f;
+    return run_gemm_pair<2, kPairStagesFp4x4, 1>(ma, mb, msa, msb, pk, st);
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {
