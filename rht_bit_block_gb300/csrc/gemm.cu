@@ -63,6 +63,11 @@ constexpr int kBnFp8 = 224, kBnFp4 = 192;
 // 256 elements, as much MMA work as two FP8 K tiles of 128)
 constexpr int kPairKps = 2, kPairStages = 3;          // FP8
 constexpr int kPairStagesFp4x2 = 5, kPairStagesFp4x4 = 4;
+// Scale chunks of the FP4 kinds: stored once and copied to tensor memory
+// with one .32x128b.warpx4 per 512-byte chunk (false), or stored four times
+// and copied two chunks per .128x256b (true, the FP8 layout)
+constexpr bool kFp4Replicated = true;
+__host__ __device__ constexpr bool pair_replicated(int kind) { return kind == 0 || kFp4Replicated; }
 
 // ------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -269,6 +274,20 @@ __device__ __forceinline__ void tc_cp_scales_pair_256(uint32_t taddr, uint64_t s
     asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// 32 lanes x 16 bytes of one 512-byte chunk, to all four lane quadrants
+__device__ __forceinline__ void tc_cp_scales_pair_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// No-swizzle descriptor of one 512-byte chunk: 8-row core matrices 128 bytes apart
+__device__ __forceinline__ uint64_t sf512_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+    d |= (uint64_t)(128u >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    return d;
+}
+
 // No-swizzle K-major descriptor of that block: 8-row core matrices (128 B)
 // 128 bytes apart, the second 16-byte column 2048 bytes after the first.
 __device__ __forceinline__ uint64_t sf256_desc(uint32_t saddr) {
@@ -301,7 +320,8 @@ struct PairCfg {
     static constexpr int kABytes = KPS * kAAtom;
     static constexpr int kBBytes = KPS * kBAtom;
     static constexpr int kChunks = KPS * CPK;                // chunks per 128 rows per stage
-    static constexpr int kRep = 4 * kChunkBytes;             // one replicated chunk: 2 KB
+    static constexpr bool kRepl = pair_replicated(KIND);
+    static constexpr int kRep = (kRepl ? 4 : 1) * kChunkBytes;  // one stored chunk: 2 KB replicated, else 512 B
     static constexpr int kSfaBytes = kChunks * kRep;         // this CTA's 128 rows
     static constexpr int kSfbBytes = 2 * kChunks * kRep;     // both 128-row parts of B
     static constexpr int kTxPerAtom = kAAtom + kBAtom;       // operand bytes per CTA per K tile
@@ -410,9 +430,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
             const int arow = ablk * kBM;
             const int brow = nb * C::BN + (int)peer * C::kBRows;
-            // 512-byte rows of the replicated chunk arrays: 4 per chunk for A, 8 for B
-            const int sfa_row = ablk * (int)p.sf_chunks_k * 4;
-            const int sfb_row = nb * (int)p.sf_chunks_k * 8;
+            // 512-byte rows of the chunk arrays: R per chunk for A, 2R for B (R = 4 replicated, else 1)
+            constexpr int R = C::kRep / kChunkBytes;
+            const int sfa_row = ablk * (int)p.sf_chunks_k * R;
+            const int sfb_row = nb * (int)p.sf_chunks_k * 2 * R;
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
                     *abort_flag = 1;
@@ -427,8 +448,8 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                     tma_load_pair(stage_b(s) + j * C::kBAtom, &tmap_b, (kt0 + j) * kBKBytes, brow, fb, keep);
                 }
                 // the scales of the stage's K tiles are contiguous: one box each
-                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * C::CPK * 4, fb, keep);
-                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * C::CPK * 8, fb, keep);
+                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * C::CPK * R, fb, keep);
+                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * C::CPK * 2 * R, fb, keep);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -469,10 +490,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         const int cq = C::CPK == 1 ? 0 : (C::CPK == 2 ? q >> 1 : q);
                         const int u = j * C::CPK + cq;
                         if (C::CPK == 4 || q == 0 || (C::CPK == 2 && q == 2)) {
-                            // first MMA of chunk u: A's copy of chunks u, u+1 (u even), B's copy of chunk u
-                            if ((u & 1) == 0)
-                                tc_cp_scales_pair_256(sfa_t + 4 * u, sf256_desc(stage_sfa(s) + (u >> 1) * 2 * C::kRep));
-                            tc_cp_scales_pair_256(sfb_t + 8 * u, sf256_desc(stage_sfb(s) + u * 2 * C::kRep));
+                            if (C::kRepl) {
+                                // first MMA of chunk u: A's copy of chunks u, u+1 (u even), B's copy of chunk u
+                                if ((u & 1) == 0)
+                                    tc_cp_scales_pair_256(sfa_t + 4 * u,
+                                                          sf256_desc(stage_sfa(s) + (u >> 1) * 2 * C::kRep));
+                                tc_cp_scales_pair_256(sfb_t + 8 * u, sf256_desc(stage_sfb(s) + u * 2 * C::kRep));
+                            } else {
+                                // one copy per 512-byte chunk: A's chunk u, B's chunk u of parts 0 and 1
+                                tc_cp_scales_pair_x4(sfa_t + 4 * u, sf512_desc(stage_sfa(s) + u * C::kRep));
+                                tc_cp_scales_pair_x4(sfb_t + 8 * u, sf512_desc(stage_sfb(s) + 2 * u * C::kRep));
+                                tc_cp_scales_pair_x4(sfb_t + 8 * u + 4, sf512_desc(stage_sfb(s) + (2 * u + 1) * C::kRep));
+                            }
                         }
                         // each MMA consumes 32 bytes of K: advance the start address by two 16-byte units
                         mma_pair<KIND>(acc, da + 2 * q, db + 2 * q, p.idesc[q], sfa_t + 4 * u, sfb_t + 8 * u,
@@ -932,12 +961,12 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
                                      (lane & 3) * kChunkBytes) = word;
 }
 
-// E2M1: only the scales move, into the replicated chunk layout (hardware
-// blocks of 16 or 32 elements, one scale byte each: UE8M0, or E4M3 for the
-// two-level format).  A warp writes one chunk: lane i builds the chunk's
-// 16-byte line i (cells of rows i, i + 32, i + 64, i + 96 of the part) and
-// stores it into the four copies, so every store of the warp covers 512
-// contiguous bytes.  blockIdx.x: 8 chunks (one per warp), blockIdx.z: operand.
+// E2M1: only the scales move, into the chunk layout of the pair kernel
+// (hardware blocks of 16 or 32 elements, one scale byte each: UE8M0, or E4M3
+// for the two-level format), replicated or not as pair_replicated says.  A
+// warp writes one chunk: lane i builds the chunk's 16-byte line i (cells of
+// rows i, i + 32, i + 64, i + 96 of the part) and stores it into each copy,
+// so every store of the warp covers 512 contiguous bytes.  blockIdx.x: 8 chunks (one per warp), blockIdx.z: operand.
 __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
     griddep_wait();
     griddep_launch();
@@ -967,9 +996,10 @@ __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
         cell[c] = v;
     }
     const uint4 line = make_uint4(cell[0], cell[1], cell[2], cell[3]);
-    uint8_t* dst = s.out_chunks + ((((int64_t)t * p.chunks_k + g) * parts + h) * 4) * kChunkBytes + i * 16;
+    constexpr int copies = pair_replicated(1) ? 4 : 1;
+    uint8_t* dst = s.out_chunks + ((((int64_t)t * p.chunks_k + g) * parts + h) * copies) * kChunkBytes + i * 16;
 #pragma unroll
-    for (int copy = 0; copy < 4; ++copy) *reinterpret_cast<uint4*>(dst + copy * kChunkBytes) = line;
+    for (int copy = 0; copy < copies; ++copy) *reinterpret_cast<uint4*>(dst + copy * kChunkBytes) = line;
 }
 
 // Level value of a 4-bit code (E1M2 k/4, INT4 two's complement k, E2M1 codes
@@ -1121,10 +1151,11 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
         pl.fp8_b = off;
         off = align256(off + (size_t)N * K);
     }
-    pl.sfa = off;  // replicated chunks: four copies of each
-    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes * 4);
+    const size_t copies = pair_replicated(pl.kind) ? 4 : 1;
+    pl.sfa = off;
+    off = align256(off + (size_t)mb * pl.chunks_k * kChunkBytes * copies);
     pl.sfb = off;
-    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes * 4);
+    off = align256(off + (size_t)nb * pl.chunks_k * kChunkBytes * copies);
     pl.total = off;
     return pl;
 }
@@ -1320,13 +1351,14 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     // per row); boxes: one stage's chunks, 4 rows per chunk for A, 8 for B
     const int cpk = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
     const int kps = pl.kind == 0 ? kPairKps : 1;
+    const int rpc = pair_replicated(pl.kind) ? 4 : 1;  // 512-byte rows per chunk
     const int64_t a_blocks = (g.M + kBM - 1) / kBM;
     const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
-    if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k * 4),
-                       kChunkBytes, 128, (uint32_t)(4 * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k * rpc),
+                       kChunkBytes, 128, (uint32_t)(rpc * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k * 4),
-                       kChunkBytes, 128, (uint32_t)(8 * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
+    if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k * rpc),
+                       kChunkBytes, 128, (uint32_t)(2 * rpc * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     PairKParams pk{};
     pk.M = (int)g.M;

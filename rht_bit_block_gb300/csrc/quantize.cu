@@ -103,10 +103,11 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
         const float r = s == 0.0f ? 0.0f : __frcp_rn(s);
         return __fmul_rn(r, pow2_exact(lf + lj));
     } else if (SF == 1) {
-        float r;
-        const int e = scale_po2<GRID>(Mz, r);
-        if (write) *sptr = (uint8_t)(e + 127);
-        return pow2_exact(-e + lf + lj);
+        const int eb = scale_po2_byte<GRID>(Mz);  // e + 127
+        if (write) *sptr = (uint8_t)eb;
+        // 2^(-e + lf + lj) from its biased exponent (a subnormal below 1)
+        const int kb = 254 - eb + lf + lj;
+        return __uint_as_float(kb >= 1 ? (uint32_t)kb << 23 : 1u << (kb + 22));
     } else {
         float sc, r;
         scale_fp32(Mz, qmax, sc, r);

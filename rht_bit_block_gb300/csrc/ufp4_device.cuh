@@ -140,24 +140,19 @@ __device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float&
     r = (s == 0.0f) ? 0.0f : __frcp_rn(s);
 }
 
-// Power-of-two scale: smallest e with M <= qmax * 2^e, clamped to [-127, 127].
-// With M = m * 2^E (m in [1,2)) and qmax = mq * 2^Eq: e = E - Eq + (m > mq).
-// Returns e; r = 2^-e exactly.
+// Power-of-two scale: smallest e with M <= qmax * 2^e, clamped to
+// [-127, 127], returned as its UE8M0 byte e + 127.  With M = m * 2^E (m in
+// [1,2)) and qmax = mq * 2^Eq: e = E - Eq + (m > mq).  The comparison is the
+// carry of M's mantissa + (2^23 - 1 - mq) into the exponent field, so the
+// byte is one add and one shift of M's bits.  Zero (and a subnormal M,
+// outside the contract) gives byte 0.
 template <int GRID>
-__device__ __forceinline__ int scale_po2(float M, float& r) {
-    const uint32_t b = __float_as_uint(M);
+__device__ __forceinline__ int scale_po2_byte(float M) {
     constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : 2);
     constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : 0x600000u);  // 1.5, 1.0 or 1.75
-    int e;
-    if (b < 0x00800000u) {
-        e = -127;  // zero (subnormal amax is outside the contract)
-    } else {
-        const int E = (int)(b >> 23) - 127;
-        e = E - Eq + (((b & 0x7FFFFFu) > mq) ? 1 : 0);
-        e = max(-127, min(127, e));
-    }
-    r = (e <= 126) ? __uint_as_float((uint32_t)(127 - e) << 23) : __uint_as_float(0x00400000u);
-    return e;
+    const uint32_t b = __float_as_uint(M);
+    const int eb = (int)((b + (0x7FFFFFu - mq)) >> 23) - Eq;
+    return b < 0x00800000u ? 0 : min(max(eb, 0), 254);
 }
 
 // ----------------------------------------------------------------- rounding
