@@ -116,6 +116,13 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
     }
 }
 
+// Stochastic rounding of 16 scaled values to packed codes.  With a =
+// min(|t|, qmax) in units of the local level gap g (v = a / g, between the
+// levels floor(v) and floor(v) + 1), round up iff u < (v - floor(v)) * 2^16,
+// u the element's 16 random bits.  For integer u that is u < ceil(v * 2^16) -
+// floor(v) * 2^16, so the level index is k = (ceil(v * 2^16) + 2^16 - 1 - u)
+// >> 16 (floor(v) or floor(v) + 1), and ceil(v * 2^16) is the low mantissa
+// bits of one fma rounded upward, v * 2^16 + 2^23 (exact: v * 2^16 < 2^23).
 template <int GRID>
 __device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uint64_t lin0, uint32_t stream,
                                         uint32_t group) {
@@ -127,19 +134,20 @@ __device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uin
     for (int i = 0; i < 16; ++i) {
         const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
         const float ti = t[i];
+        // E2M1 values are in level units (largest qmax), uniform ones in steps (largest 7)
+        const float a = fminf(fabsf(ti), GRID >= 2 ? qmax : 7.0f);
         uint32_t idx;
         if (GRID >= 2) {
-            const float a = fminf(fabsf(ti), qmax);
+            // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
             const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
             const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-            const float vv = __fmul_rn(a, inv);
-            const float fl = floorf(vv);
-            const float up = ((float)u < __fmul_rn(__fsub_rn(vv, fl), 65536.0f)) ? 1.0f : 0.0f;
-            idx = cvt_e2m1x2(0.0f, __fmul_rn(__fadd_rn(fl, up), gap)) & 7u;
+            const uint32_t vb = __float_as_uint(__fmaf_ru(__fmul_rn(a, inv), 65536.0f, 8388608.0f));
+            const uint32_t k = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
+            idx = cvt_e2m1x2(0.0f, __fmul_rn((float)k, gap)) & 7u;
         } else {
-            const float vv = fminf(fabsf(ti), 7.0f);  // in steps of the uniform grid
-            const float fl = floorf(vv);
-            idx = (uint32_t)fl + (((float)u < __fmul_rn(__fsub_rn(vv, fl), 65536.0f)) ? 1u : 0u);
+            // uniform grids: t is already in units of the step
+            const uint32_t vb = __float_as_uint(__fmaf_ru(a, 65536.0f, 8388608.0f));
+            idx = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
         }
         const uint32_t neg = __float_as_uint(ti) >> 31;
         out[i >> 3] |= (idx == 0 ? 0u : ((neg << 3) | idx)) << (4 * (i & 7));

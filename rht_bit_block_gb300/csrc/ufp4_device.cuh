@@ -24,9 +24,6 @@ __host__ __device__ constexpr float grid_qmax(int grid) {
     return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : (grid == 2 ? 6.0f : 2.0f));
 }
 
-// ------------------------------------------------------------- Philox4x32-10
-// Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
-// bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.
 // E4M3 byte of a >= 0, rounded to nearest even and saturated at 448 (the
 // hardware conversion), and its value.
 __device__ __forceinline__ uint32_t e4m3_byte(float a) {
@@ -54,6 +51,10 @@ __device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
     return (nib & 8u) ? -v : v;
 }
 
+// ------------------------------------------------------------- Philox4x32-10
+// Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
+// bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.  Each product is one
+// 32 x 32 -> 64-bit multiply (both halves at once).
 __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
@@ -61,9 +62,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
             k0 += 0x9E3779B9u;
             k1 += 0xBB67AE85u;
         }
-        const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
-        const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        uint64_t p0, p1;
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
+        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
     }
     return c;
 }
@@ -125,14 +127,6 @@ __device__ __forceinline__ void fwht16(float v[16], int n, int seg_lane) {
     }
 }
 
-__device__ __forceinline__ float amax_range(const float v[16], int lo, int hi) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kChunk; ++i)
-        if (i >= lo && i < hi) m = fmaxf(m, fabsf(v[i]));
-    return m;
-}
-
 // ------------------------------------------------------------------- scales
 // fp32 scale s = fp32(M / qmax); reciprocal r = fp32(1/s), 0 for s = 0.
 __device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float& r) {
@@ -155,27 +149,12 @@ __device__ __forceinline__ int scale_po2_byte(float M) {
     return b < 0x00800000u ? 0 : min(max(eb, 0), 254);
 }
 
-// ----------------------------------------------------------------- rounding
-__device__ __forceinline__ uint32_t cvt_e2m3x2(float hi, float lo) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e2m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
     uint32_t r;
     asm("{ .reg .b8 t; cvt.rn.satfinite.e2m1x2.f32 t, %1, %2; cvt.u32.u8 %0, t; }"
         : "=r"(r)
         : "f"(hi), "f"(lo));
     return r;
-}
-
-// Four e2m3 bytes (s 0 0 k k k, k = |level index|) -> four sign-magnitude
-// nibbles in the low 16 bits (byte i -> nibble i).
-__device__ __forceinline__ uint32_t e2m3_bytes_to_nibbles(uint32_t w) {
-    uint32_t t = (w & 0x07070707u) | ((w >> 2) & 0x08080808u);
-    t = (t | (t >> 4)) & 0x00FF00FFu;
-    return (t | (t >> 8)) & 0xFFFFu;
 }
 
 // A zero level is written as +0: clear the sign of every nibble whose
@@ -196,91 +175,13 @@ __device__ __forceinline__ uint32_t signmag_to_twos(uint32_t w) {
     return negm | ((neg << 3) & nz);
 }
 
-// RTNE of 16 scaled values t = z * r (r0 for elements 0..7, r1 for 8..15)
-// to packed codes (two 32-bit words, element 0 in the lowest nibble).
-// E1M2 / INT4: the level index k of |t| is the e2m3 conversion of t/2 or t/8
-// (values k/8 are exactly e2m3's subnormals, ties to even k); E2M1: the e2m1
-// conversion of t.  satfinite saturates |t| above the largest level.
-template <int GRID>
-__device__ __forceinline__ uint2 round_rtne16(const float z[16], float r0, float r1) {
-    uint32_t out[2];
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const float r = h ? r1 : r0;
-        float t[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) t[i] = __fmul_rn(z[8 * h + i], r);
-        uint32_t w;
-        if (GRID >= 2) {
-            w = 0;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) w |= cvt_e2m1x2(t[2 * p + 1], t[2 * p]) << (8 * p);
-        } else {
-            const float q = (GRID == 0) ? 0.5f : 0.125f;
-            uint32_t b[4];
-#pragma unroll
-            for (int p = 0; p < 4; ++p) b[p] = cvt_e2m3x2(__fmul_rn(t[2 * p + 1], q), __fmul_rn(t[2 * p], q));
-            const uint32_t lo = e2m3_bytes_to_nibbles(b[0] | (b[1] << 16));
-            const uint32_t hi = e2m3_bytes_to_nibbles(b[2] | (b[3] << 16));
-            w = lo | (hi << 16);
-        }
-        w = clear_negative_zero(w);
-        if (GRID == 1) w = signmag_to_twos(w);
-        out[h] = w;
-    }
-    return make_uint2(out[0], out[1]);
-}
-
-// Stochastic rounding of one scaled value: with a = min(|t|, qmax) between
-// levels lo and hi, p = (a - lo)/(hi - lo), round up iff u < p * 65536.
-// Returns the sign-magnitude nibble (a zero level as +0).
-template <int GRID>
-__device__ __forceinline__ uint32_t round_sr1(float t, uint32_t u) {
-    constexpr float qmax = grid_qmax(GRID);
-    const float a = fminf(fabsf(t), qmax);
-    uint32_t idx;
-    if (GRID >= 2) {
-        // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
-        const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-        const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-        const float v = __fmul_rn(a, inv);
-        const float fl = floorf(v);
-        const float frac = __fsub_rn(v, fl);
-        const float up = ((float)u < __fmul_rn(frac, 65536.0f)) ? 1.0f : 0.0f;
-        const float val = __fmul_rn(__fadd_rn(fl, up), gap);
-        idx = cvt_e2m1x2(0.0f, val) & 7u;
-    } else {
-        const float inv_step = (GRID == 0) ? 4.0f : 1.0f;
-        const float v = __fmul_rn(a, inv_step);
-        const float fl = floorf(v);
-        const float frac = __fsub_rn(v, fl);
-        idx = (uint32_t)fl + (((float)u < __fmul_rn(frac, 65536.0f)) ? 1u : 0u);
-    }
-    const uint32_t neg = (__float_as_uint(t) >> 31) & 1u;
-    return idx == 0 ? 0u : ((neg << 3) | idx);
-}
-
-template <int GRID>
-__device__ __forceinline__ uint2 round_sr16(const float z[16], float r0, float r1, const uint32_t w[8]) {
-    uint32_t out[2] = {0u, 0u};
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float t = __fmul_rn(z[i], i < 8 ? r0 : r1);
-        const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
-        out[i >> 3] |= round_sr1<GRID>(t, u) << (4 * (i & 7));
-    }
-    if (GRID == 1) {
-        out[0] = signmag_to_twos(out[0]);
-        out[1] = signmag_to_twos(out[1]);
-    }
-    return make_uint2(out[0], out[1]);
-}
-
 }  // namespace ufp4
 
 // ======================================================================
-// Paired-lane helpers (sm_100+ add/sub/mul.rn.f32x2: two independent IEEE
-// binary32 operations, round to nearest even, per instruction).
+// Paired-lane helpers (PTX add/sub/mul.rn.f32x2: two independent IEEE
+// binary32 operations, round to nearest even).  On sm_103a each issues as two
+// scalar operations (instruction counters); the pairing keeps two vectors in
+// step through the same code.
 namespace ufp4 {
 
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
@@ -317,66 +218,6 @@ __device__ __forceinline__ void make_masks(uint32_t sgn, SignMasks& m) {
         m.lo[k] = ((sgn >> (2 * k)) & 1u) << 31;
         m.hi[k] = ((sgn >> (2 * k + 1)) & 1u) << 31;
     }
-}
-
-// 8 words of bf16 pairs -> 8 packed fp32 pairs with the RHT signs: the low
-// bf16 of a word becomes w * 65536 (+ 2^31 flips the sign bit exactly like
-// an xor, because the low 16 bits are zero), the high one w & 0xffff0000.
-__device__ __forceinline__ void widen16_x2(const uint32_t w[8], const SignMasks& m, uint64_t v[8]) {
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t lo = w[k] * 65536u + m.lo[k];
-        const uint32_t hi = (w[k] & 0xFFFF0000u) ^ m.hi[k];
-        v[k] = pk2(__uint_as_float(lo), __uint_as_float(hi));
-    }
-}
-
-// Sylvester FWHT on a chunk held as 8 pairs (2k, 2k+1): stride 1 inside each
-// pair (scalar add/sub), strides 2, 4, 8 between pairs k and k + h/2
-// (paired adds), strides 16..n/2 with the lane holding the chunk h/16 away.
-// Same operations, in the same order, as the scalar butterfly.
-__device__ __forceinline__ void fwht16_x2(uint64_t v[8], int n, int seg_lane) {
-    if (n > 1) {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            float a, b;
-            up2(v[k], a, b);
-            v[k] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
-        }
-    }
-#pragma unroll
-    for (int hp = 1; hp < 8; hp <<= 1) {  // pair stride hp <-> element stride 2*hp
-        if (2 * hp < n) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (k & hp) continue;
-                const uint64_t a = v[k], b = v[k + hp];
-                v[k] = add2(a, b);
-                v[k + hp] = sub2(a, b);
-            }
-        }
-    }
-    for (int h = kChunk; h < n; h <<= 1) {
-        const int lm = h / kChunk;
-        const bool upper = (seg_lane & lm) != 0;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)v[k], lm);
-            v[k] = upper ? sub2(o, v[k]) : add2(v[k], o);
-        }
-    }
-}
-
-__device__ __forceinline__ float amax_pairs(const uint64_t v[8], int k0, int k1) {
-    float m = 0.0f;
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        if (k < k0 || k >= k1) continue;
-        float a, b;
-        up2(v[k], a, b);
-        m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
-    }
-    return m;
 }
 
 __device__ __forceinline__ float pow2_exact(int e) {  // 2^e, e in [-149, 127]
@@ -491,14 +332,6 @@ __device__ __forceinline__ void fwht_pair(uint64_t e[16], int n, int seg_lane) {
             e[i] = upper ? sub2(o, e[i]) : add2(e[i], o);
         }
     }
-}
-
-// max(|x|, |y|) with the xor of the signs: the magnitude is what a block
-// amax needs, and chained calls keep it, so |.| is taken once at the end.
-__device__ __forceinline__ float maxabs(float x, float y) {
-    float r;
-    asm("max.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(y));
-    return r;
 }
 
 // Tree amax of |a_i| and |b_i| over i in [lo, hi) (lo, hi multiples of 8).
