@@ -78,6 +78,10 @@ def lib():
         L.orc_round_rtne.restype = i32
         L.orc_round_sr.argtypes = [i32, ctypes.c_float, u32]
         L.orc_round_sr.restype = i32
+        L.orc_quantize_rows_mxfp8.argtypes = [P, i64, i64, i64, i32, u64, P, P]
+        L.orc_quantize_rows_mxfp8.restype = i32
+        L.orc_dequantize_f64_mxfp8.argtypes = [P, P, i64, i64, P]
+        L.orc_dequantize_f64_mxfp8.restype = i32
         _lib = L
     return _lib
 
@@ -279,3 +283,38 @@ def gemm_reference_2level(a_codes, a_scales, a_amax, b_codes, b_scales, b_amax, 
             raise ValueError("unsupported arguments")
         return out
     return deq(a_codes, a_scales, a_amax) @ deq(b_codes, b_scales, b_amax).T
+
+
+def quantize_mxfp8(x_bf16: np.ndarray, *, n=1, sign_seed=0):
+    """MXFP8 (E4M3 elements, one E8M0 scale per 32 along the row) of the
+    row-wise RHT of x, the format the 2D-block page keeps for the Query and
+    Key projections (mixed-precision section), read as the OCP MX
+    definition.  Returns (codes [rows x cols] E4M3 bytes, scales [rows x
+    cols/32] E8M0 bytes)."""
+    x = _as_bf16(x_bf16)
+    rows, cols = x.shape
+    codes = np.zeros((rows, cols), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    if lib().orc_quantize_rows_mxfp8(_ptr(x), rows, cols, x.strides[0] // 2, n, sign_seed, _ptr(codes),
+                                     _ptr(scales)):
+        raise ValueError("unsupported arguments")
+    return codes, scales
+
+
+def dequantize_mxfp8(codes, scales) -> np.ndarray:
+    """Exact fp64 values e4m3(code) * 2^(scale byte - 127)."""
+    c = np.ascontiguousarray(codes)
+    sc = np.ascontiguousarray(scales)
+    rows, cols = c.shape
+    out = np.zeros((rows, cols), dtype=np.float64)
+    if lib().orc_dequantize_f64_mxfp8(_ptr(c), _ptr(sc), rows, cols, _ptr(out)):
+        raise ValueError("unsupported arguments")
+    return out
+
+
+def gemm_reference_mxfp8(a_codes, a_scales, b_codes, b_scales, a_rows=None) -> np.ndarray:
+    """fp64 product of two dequantized MXFP8 operands (both K-major)."""
+    a = dequantize_mxfp8(a_codes, a_scales)
+    if a_rows is not None:
+        a = a[np.asarray(a_rows)]
+    return a @ dequantize_mxfp8(b_codes, b_scales).T

@@ -524,3 +524,64 @@ int orc_dequantize_f64(const uint8_t* codes, const void* scales, int64_t rows, i
         }
     return 0;
 }
+
+/* ------------------------------------------------------------------ MXFP8
+ * [2D-block, section on mixed precision]: the Query and Key projections keep
+ * MXFP8, a format with more precision and a wider dynamic range than FP4.
+ * The page names the format and nothing more, so its definition is read as
+ * the OCP Microscaling format MXFP8 (E4M3): blocks of 32 consecutive
+ * elements along a row share one power-of-two scale X = 2^e stored as the
+ * E8M0 byte e + 127, with e = floor(log2(max |z|)) - 8 (8 = the exponent of
+ * E4M3's largest normal, 448 = 1.75 * 2^8), clamped to [-127, 127]; each
+ * element is z / X rounded to E4M3 to nearest even, saturated at 448.  A
+ * zero block has byte 0 and codes 0, and a value that rounds to zero is
+ * written as +0 (byte 0x00), as for the 4-bit formats.  z is the row-wise
+ * RHT of x (n = 1: x itself).  Outputs: codes [rows x cols] E4M3 bytes,
+ * scales [rows x cols/32] E8M0 bytes. */
+int orc_quantize_rows_mxfp8(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n,
+                            uint64_t sign_seed, uint8_t* codes, uint8_t* scales) {
+    if (cols % 32) return 1;
+    float* z = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
+    if (!z) return 1;
+    if (orc_rht_rows(x, rows, cols, ld, n, sign_seed, z)) {
+        free(z);
+        return 1;
+    }
+    const int64_t nbc = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t bj = 0; bj < nbc; ++bj) {
+            const float* zb = &z[r * cols + bj * 32];
+            float M = 0.0f;
+            for (int i = 0; i < 32; ++i)
+                if (fabsf(zb[i]) > M) M = fabsf(zb[i]);
+            int e = -127;
+            if (M > 0.0f) {
+                int e2;
+                frexp((double)M, &e2); /* M in [2^(e2-1), 2^e2) */
+                e = (e2 - 1) - 8;
+                if (e < -127) e = -127;
+                if (e > 127) e = 127;
+            }
+            scales[r * nbc + bj] = (uint8_t)(e + 127);
+            for (int i = 0; i < 32; ++i) {
+                double t = ldexp((double)zb[i], -e); /* exact */
+                uint8_t b = orc_e4m3_encode(fabs(t));
+                if (b != 0 && t < 0.0) b |= 0x80;
+                codes[r * cols + bj * 32 + i] = b;
+            }
+        }
+    free(z);
+    return 0;
+}
+
+/* Exact fp64 values e4m3(code) * 2^(byte - 127) of an MXFP8 tensor. */
+int orc_dequantize_f64_mxfp8(const uint8_t* codes, const uint8_t* scales, int64_t rows, int64_t cols,
+                             double* out) {
+    if (cols % 32) return 1;
+    const int64_t nbc = cols / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[r * cols + c] = orc_e4m3_decode(codes[r * cols + c]) *
+                                ldexp(1.0, (int)scales[r * nbc + c / 32] - 127);
+    return 0;
+}

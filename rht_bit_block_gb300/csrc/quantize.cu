@@ -84,8 +84,9 @@ struct Fold {
 //
 // RTNE multiplies y by one folded reciprocal per block, rr = r * 2^-j * f,
 // where f = 2^-7 (E1M2: k/4 -> k * 2^-9) or 2^-9 (INT4: k -> k * 2^-9) puts
-// the uniform levels on e4m3's subnormals, and f = 1 for E2M1; every factor
-// is a power of two, so fp32(y * rr) = fp32(z * r) * f exactly.  SR uses
+// the uniform levels on e4m3's subnormals, and f = 1 for E2M1 and for INT4
+// with UE8M0 scales (rounded by an fma instead); every factor is a power of
+// two, so fp32(y * rr) = fp32(z * r) * f exactly.  SR uses
 // f = 1/step (E1M2 4, INT4 1, E2M1 1).  For other n, z = fp32(y * 1/sqrt n)
 // is formed first, as in the definition.
 // SF: 0 fp32 scale, 1 UE8M0, 2 two-level (E4M3 block byte x tensor scale g).
@@ -163,7 +164,9 @@ template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B,
                                           uint64_t sr_seed, uint32_t stream, uint32_t group) {
-    constexpr int lf = SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0));  // log2 f
+    // INT4 with power-of-two scales rounds by adding 1.5 * 2^23 + 8 (below)
+    constexpr bool kMagic = GRID == 1 && !SR && SF == 1;
+    constexpr int lf = kMagic ? 0 : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
     const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0);
     const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0);
     float ra1 = ra0, rb1 = rb0;
@@ -175,6 +178,33 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         const uint64_t is2 = pk2(fd.inv_s, fd.inv_s);
 #pragma unroll
         for (int i = 0; i < 16; ++i) e[i] = mul2(e[i], is2);
+    }
+    if (kMagic) {
+        // t = z r is exact (r a power of two), so one fma t + (1.5 * 2^23 + 8)
+        // rounds t to the nearest integer k, ties to even (the addend is even
+        // and the result's unit is 1), and its low nibble is k + 8 (|k| <= 7):
+        // the two's complement nibble of k after flipping bit 3.  Pairs of
+        // nibbles merge with one multiply-add (bits 4..7 of k + 8 are clear).
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float a, b;
+            up2(e[i], a, b);
+            va[i] = __float_as_uint(__fmaf_rn(a, i < 8 ? ra0 : ra1, 12582920.0f));
+            vb[i] = __float_as_uint(__fmaf_rn(b, i < 8 ? rb0 : rb1, 12582920.0f));
+        }
+        auto pack8 = [](const uint32_t* v) {
+            const uint32_t p0 = v[1] * 16u + v[0], p1 = v[3] * 16u + v[2];
+            const uint32_t p2 = v[5] * 16u + v[4], p3 = v[7] * 16u + v[6];
+            uint32_t x, y, w;
+            asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(x) : "r"(p0), "r"(p1));
+            asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(y) : "r"(p2), "r"(p3));
+            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(x), "r"(y));
+            return w ^ 0x88888888u;
+        };
+        if (A.valid) *reinterpret_cast<uint2*>(A.codes) = make_uint2(pack8(va), pack8(va + 8));
+        if (B.valid) *reinterpret_cast<uint2*>(B.codes) = make_uint2(pack8(vb), pack8(vb + 8));
+        return;
     }
     const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
     float ta[16], tb[16];

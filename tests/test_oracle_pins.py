@@ -496,3 +496,69 @@ def test_two_level_scale_properties():
         lev = np.array([orc.level(grid, k) for k in range(8)], dtype=np.float32)[nib & 7]
         lev = np.where(nib & 8, -lev, lev).astype(np.float32)
         np.testing.assert_array_equal(deq, lev * s_el)
+
+
+# ------------------------------------------------------------------ MXFP8
+# The 2D-block page keeps MXFP8 for the Query and Key projections (section on
+# mixed precision); the oracle reads it as the OCP MX format: 32-element
+# blocks, E8M0 scale 2^(floor(log2 amax) - 8), E4M3 elements, nearest-even,
+# saturated at 448.
+
+def _bf16_bits(values):
+    return inputs.f32_to_bf16_bits(np.asarray(values, dtype=np.float32))
+
+
+def test_mxfp8_scale_puts_the_block_amax_in_the_top_binade():
+    """floor(log2 amax) - 8: the amax divided by the scale lies in [256, 512),
+    the binade of E4M3's largest normal (checked with frexp in fp64)."""
+    x = inputs.normal_bf16(64, 256, 11)
+    codes, scales = orc.quantize_mxfp8(x)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    amax = np.abs(xf.reshape(64, 8, 32)).max(axis=2)
+    ratio = amax / np.ldexp(1.0, scales.astype(np.int64) - 127)
+    assert np.all((ratio >= 256.0) & (ratio < 512.0))
+
+
+def test_mxfp8_elements_match_torch_float8_rounding():
+    """Each element is z / X rounded by torch's float8_e4m3fn cast (a library
+    routine), saturated at 448; zero stays +0."""
+    import torch
+    if not hasattr(torch, "float8_e4m3fn"):
+        pytest.skip("torch without float8_e4m3fn")
+    x = inputs.with_element_outliers(inputs.normal_bf16(32, 512, 12), 0.001, 50.0, 14)
+    codes, scales = orc.quantize_mxfp8(x)
+    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
+    t = xf / np.repeat(np.ldexp(1.0, scales.astype(np.int64) - 127), 32, axis=1)
+    tc = np.clip(t, -448.0, 448.0)
+    ref = torch.from_numpy(tc).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = np.where((ref & 0x7F) == 0, 0, ref).astype(np.uint8)
+    assert np.array_equal(codes, ref)
+
+
+def test_mxfp8_is_exact_on_representable_blocks():
+    """Blocks built from E4M3 values times 2^k, with the block amax in
+    [256, 448] * 2^k, come back unchanged through quantize + dequantize."""
+    rng = np.random.default_rng(13)
+    e4m3 = np.array([orc.e4m3_decode(b) for b in range(0, 0x7F)])
+    rows = []
+    for k in (-20, -3, 0, 5, 30):
+        vals = rng.choice(e4m3, size=32) * rng.choice([-1.0, 1.0], size=32)
+        vals[rng.integers(32)] = rng.choice(e4m3[e4m3 >= 256.0])
+        rows.append(np.ldexp(vals, k))
+    x = _bf16_bits(np.array(rows))
+    codes, scales = orc.quantize_mxfp8(x)
+    back = orc.dequantize_mxfp8(codes, scales)
+    assert np.array_equal(back, np.array(rows))
+
+
+def test_mxfp8_saturates_and_keeps_zero_positive():
+    """amax / X in (448, 512): the largest element becomes 448 * X; a zero
+    block has scale byte 0 and zero codes; -tiny rounds to +0."""
+    row = np.zeros(64, dtype=np.float32)
+    row[0] = 480.0
+    row[1] = -1e-6
+    x = _bf16_bits(row[None, :])
+    codes, scales = orc.quantize_mxfp8(x)
+    assert scales[0, 0] == 127 + 0 and codes[0, 0] == 0x7E
+    assert codes[0, 1] == 0x00
+    assert scales[0, 1] == 0 and not codes[0, 32:].any()
