@@ -417,16 +417,19 @@ def run_suite(args):
              ("e2m1", (1, 16), 16, ufp4.SCALE_UE8M0, 0), ("e2m1r2", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
              ("e1m2", (1, 16), 16, ufp4.SCALE_FP32, 0), ("e1m2", (1, 32), 64, ufp4.SCALE_UE8M0, 0),
              ("e1m2", (1, 16), 256, ufp4.SCALE_UE8M0, 0), ("e2m1", (32, 32), 16, ufp4.SCALE_UE8M0, 0),
-             ("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_SR)]
+             ("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_SR),
+             ("mxfp8", (1, 32), 1, ufp4.SCALE_UE8M0, 0), ("mxfp8", (1, 32), 16, ufp4.SCALE_UE8M0, 0)]
     for grid, block, n, fmt, rnd in cases:
         desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt, rounding=rnd,
                               sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
         out = ufp4.alloc_quantized(rows, cols, desc, dev)
         q = ufp4.qtensor(*out, rows, cols)
         ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
-        gbs = rows * cols * (2.5 + scale_bytes(desc)) / (ms / 1e3) / 1e9
+        code_bytes = 1.0 if grid == "mxfp8" else 0.5
+        gbs = rows * cols * (2 + code_bytes + scale_bytes(desc)) / (ms / 1e3) / 1e9
         emit("quantize_rowwise", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
-             f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs, "GB/s", gbs / pk["hbm"], pk["hbm"],
+             f"{('E8M0' if grid == 'mxfp8' else 'UE8M0') if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs,
+             "GB/s", gbs / pk["hbm"], pk["hbm"],
              ms=ms)
     del xs5
 
@@ -486,6 +489,23 @@ def run_suite(args):
         emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
              kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
         del A, B, ws, D
+    # MXFP8 operands (E4M3 codes read in place by the FP8 kernel)
+    desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
+    def e4m3_operand(rows):
+        c = torch.randint(0, 0x7F, (rows, K), generator=g, dtype=torch.uint8)  # finite magnitudes
+        c = c | (torch.randint(0, 2, (rows, K), generator=g, dtype=torch.uint8) << 7)
+        sc = torch.randint(120, 132, (rows, K // 32), generator=g, dtype=torch.uint8)
+        return c.to(dev), sc.to(dev)
+    A, B = e4m3_operand(M), e4m3_operand(N)
+    qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+    D = torch.empty((M, N), dtype=torch.float32, device=dev)
+    pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+    tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+    emit("gemm", f"{M}x{N}x{K} mxfp8 1x32 E8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
+         kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (nominal ratio)")
+    del A, B, ws, D
     # fp32 block scales (the two-scale path: bf16 partials rescaled on the CUDA cores)
     desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
     A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),

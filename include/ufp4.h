@@ -68,7 +68,24 @@ typedef enum {
  * are E2M1 codes, so the GEMM runs on the native FP4 path (a reading of the
  * UFP4 summary, section 实验: a uniform grid cannot simply be substituted on
  * FP4 hardware). */
-typedef enum { UFP4_GRID_E1M2 = 0, UFP4_GRID_INT4 = 1, UFP4_GRID_E2M1 = 2, UFP4_GRID_E2M1_R2 = 3 } ufp4_grid;
+/* UFP4_GRID_MXFP8: the format the 2D-block page keeps for the Query and Key
+ * projections (section on mixed precision: more precision and a wider
+ * dynamic range than FP4), read as the OCP Microscaling MXFP8 format with
+ * E4M3 elements.  Codes are E4M3 bytes, ONE BYTE PER ELEMENT (codes_ld >=
+ * cols bytes, a multiple of 16); blocks are 1 x 32 with an E8M0 scale byte
+ * e + 127, e = floor(log2 M) - 8 clamped to [-127, 127] (M the block amax of
+ * the RHT output; 8 is the exponent of E4M3's largest normal 448), and each
+ * element is z * 2^-e rounded to E4M3, nearest even, saturated at 448; a
+ * zero code is written as +0.  Requires block 1 x 32, UFP4_SCALE_UE8M0 (the
+ * E8M0 byte; the rule above replaces the truncation-free one), RTNE and the
+ * row-wise output; the GEMM runs it on the FP8 tensor cores in place. */
+typedef enum {
+    UFP4_GRID_E1M2 = 0,
+    UFP4_GRID_INT4 = 1,
+    UFP4_GRID_E2M1 = 2,
+    UFP4_GRID_E2M1_R2 = 3,
+    UFP4_GRID_MXFP8 = 4
+} ufp4_grid;
 
 /* Rounding [UFP4-data; UFP4-method: RTNE for X and W, SR for dY]:
  *   RTNE: nearest level, exact ties to the even index.
@@ -136,9 +153,9 @@ typedef struct {
 /* A quantized matrix in device memory, described in its own layout: the
  * row-wise output of an R x C input has rows = R, cols = C; the column-wise
  * output (the quantization of the transpose) has rows = C, cols = R.
- *   codes      rows x cols/2 bytes, leading dimension codes_ld bytes
- *              (multiple of 8, and of 16 for GEMM operands; the pointer
- *              16-byte aligned)
+ *   codes      rows x cols/2 bytes (rows x cols for UFP4_GRID_MXFP8),
+ *              leading dimension codes_ld bytes (multiple of 8; of 16 for
+ *              GEMM operands and for MXFP8; the pointer 16-byte aligned)
  *   scales     (rows/block_rows) x (cols/block_cols) elements, float for FP32
  *              scales and uint8 for UE8M0 and E4M3, leading dimension
  *              scales_ld elements (the pointer 4-byte aligned for float)

@@ -73,9 +73,13 @@ struct BlockShape {
 
 ufp4_status check_desc(const ufp4_quant_desc* d, BlockShape* bs) {
     if (!d) return UFP4_ERR_INVALID_ARG;
-    if (d->grid < 0 || d->grid > 3 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 2)
+    if (d->grid < 0 || d->grid > 4 || d->round < 0 || d->round > 1 || d->scale_fmt < 0 || d->scale_fmt > 2)
         return UFP4_ERR_INVALID_ARG;
     if (!is_pow2(d->hadamard_n) || d->hadamard_n > 256) return UFP4_ERR_INVALID_ARG;
+    // MXFP8: 1 x 32 blocks with E8M0 scales, rounded to nearest
+    if (d->grid == UFP4_GRID_MXFP8 && (d->block_rows != 1 || d->block_cols != 32 ||
+                                       d->scale_fmt != UFP4_SCALE_UE8M0 || d->round != UFP4_ROUND_RTNE))
+        return UFP4_ERR_UNSUPPORTED;
     if (d->block_rows == 1 && (d->block_cols == 16 || d->block_cols == 32)) {
         *bs = {false, 0, d->block_cols};
     } else if (d->block_rows == d->block_cols &&
@@ -89,7 +93,7 @@ ufp4_status check_desc(const ufp4_quant_desc* d, BlockShape* bs) {
 }
 
 ufp4_status check_out(const ufp4_qtensor* q, int64_t rows, int64_t cols, const BlockShape& bs,
-                      int scale_fmt, bool grouped) {
+                      int scale_fmt, bool grouped, int grid) {
     if (!q || !q->codes || !q->scales) return UFP4_ERR_INVALID_ARG;
     if (q->rows != rows || q->cols != cols) return UFP4_ERR_INVALID_ARG;
     if (!aligned(q->codes, 16)) return UFP4_ERR_ALIGNMENT;
@@ -97,8 +101,9 @@ ufp4_status check_out(const ufp4_qtensor* q, int64_t rows, int64_t cols, const B
     if (scale_fmt == UFP4_SCALE_E4M3 && !q->tensor_amax) return UFP4_ERR_INVALID_ARG;
     if (scale_fmt == UFP4_SCALE_E4M3 && !aligned(q->tensor_amax, 4)) return UFP4_ERR_ALIGNMENT;
     if (grouped) return UFP4_OK;
-    if (q->codes_ld % 8) return UFP4_ERR_ALIGNMENT;
-    if (q->codes_ld < cols / 2) return UFP4_ERR_INVALID_ARG;
+    const bool bytes = grid == UFP4_GRID_MXFP8;  // one byte per code
+    if (q->codes_ld % (bytes ? 16 : 8)) return UFP4_ERR_ALIGNMENT;
+    if (q->codes_ld < (bytes ? cols : cols / 2)) return UFP4_ERR_INVALID_ARG;
     const int64_t sc_cols = cols / bs.bw;
     if (q->scales_ld < sc_cols) return UFP4_ERR_INVALID_ARG;
     return UFP4_OK;
@@ -198,18 +203,18 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if (do_col && !grouped && (total_rows % 16 || total_rows % n || total_rows % bs.bw))
         return UFP4_ERR_INVALID_ARG;
     if (do_row) {
-        st = check_out(rowwise, total_rows, cols, bs, desc->scale_fmt, false);
+        st = check_out(rowwise, total_rows, cols, bs, desc->scale_fmt, false, desc->grid);
         if (st != UFP4_OK) return st;
     }
     if (do_col) {
-        st = check_out(colwise, cols, padded_total, bs, desc->scale_fmt, grouped);
+        st = check_out(colwise, cols, padded_total, bs, desc->scale_fmt, grouped, desc->grid);
         if (st != UFP4_OK) return st;
     }
     if (total_rows == 0 || cols == 0) return UFP4_OK;
 
-    if (desc->scale_fmt == UFP4_SCALE_E4M3 && (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) ||
-                                               cols >= (1LL << 31)))
-        return UFP4_ERR_UNSUPPORTED;  // two-level scale: row-wise, 1-D blocks, n <= 128
+    if ((desc->scale_fmt == UFP4_SCALE_E4M3 || desc->grid == UFP4_GRID_MXFP8) &&
+        (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) || cols >= (1LL << 31)))
+        return UFP4_ERR_UNSUPPORTED;  // two-level scale and MXFP8: row-wise, 1-D blocks, n <= 128
     if (do_row && !do_col && !bs.is2d && !grouped && n <= 128 && total_rows < (1LL << 31) && cols < (1LL << 31)) {
         const ufp4_qtensor* rw = rowwise;
         return quantize_rows_batch(1, &x, &total_rows, &cols, &ld, desc, bs, rw, stream);
@@ -302,9 +307,9 @@ ufp4_status prepare_gemm(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp
     if (M == 0 || N == 0) return UFP4_OK;  // nothing to compute
     if (!aligned(D, 16) || ldd % 4) return UFP4_ERR_ALIGNMENT;
     if (K == 0) return UFP4_OK;  // D = 0 (written by run_prepared_gemm)
-    st = check_out(A, M, K, bs, desc->scale_fmt, false);
+    st = check_out(A, M, K, bs, desc->scale_fmt, false, desc->grid);
     if (st != UFP4_OK) return st;
-    st = check_out(B, N, K, bs, desc->scale_fmt, false);
+    st = check_out(B, N, K, bs, desc->scale_fmt, false, desc->grid);
     if (st != UFP4_OK) return st;
     if (A->codes_ld % 16 || B->codes_ld % 16) return UFP4_ERR_ALIGNMENT;  // TMA row pitch
     const size_t need = gemm_workspace_bytes(M, N, K, desc->grid, bs.is2d ? bs.b2d : 1, bs.bw, desc->scale_fmt);
@@ -383,7 +388,7 @@ extern "C" ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const*
         if (!x[i]) return UFP4_ERR_INVALID_ARG;
         if (!aligned(x[i], 16) || ld[i] % 8) return UFP4_ERR_ALIGNMENT;
         if (cols[i] % 16 || cols[i] % n || cols[i] % bs.bw) return UFP4_ERR_INVALID_ARG;
-        st = check_out(&rowwise[i], rows[i], cols[i], bs, desc->scale_fmt, false);
+        st = check_out(&rowwise[i], rows[i], cols[i], bs, desc->scale_fmt, false, desc->grid);
         if (st != UFP4_OK) return st;
     }
     return quantize_rows_batch(count, x, rows, cols, ld, desc, bs, rowwise, stream);
@@ -424,7 +429,7 @@ ufp4_status ufp4_dequantize(const ufp4_qtensor* q, const ufp4_quant_desc* desc, 
     if (!q || !out || q->rows < 0 || q->cols < 0 || ld_out < q->cols) return UFP4_ERR_INVALID_ARG;
     if (q->cols % 16 || q->cols % bs.bw || (bs.is2d && q->rows % bs.b2d)) return UFP4_ERR_INVALID_ARG;
     if (inverse_rht && q->cols % desc->hadamard_n) return UFP4_ERR_INVALID_ARG;
-    st = check_out(q, q->rows, q->cols, bs, desc->scale_fmt, false);
+    st = check_out(q, q->rows, q->cols, bs, desc->scale_fmt, false, desc->grid);
     if (st != UFP4_OK) return st;
     if (q->rows == 0 || q->cols == 0) return UFP4_OK;
     DequantParams p;
@@ -456,9 +461,10 @@ ufp4_status ufp4_quant_error_stats(const void* x, int64_t rows, int64_t cols, in
     if (st != UFP4_OK) return st;
     if (!rowwise || !stats || rows < 0 || cols < 0) return UFP4_ERR_INVALID_ARG;
     if (!aligned(stats, 8)) return UFP4_ERR_ALIGNMENT;
+    if (desc->grid == UFP4_GRID_MXFP8) return UFP4_ERR_UNSUPPORTED;  // the statistics decode 4-bit codes
     const int n = desc->hadamard_n;
     if (cols % 16 || cols % n || cols % bs.bw || (bs.is2d && rows % bs.b2d)) return UFP4_ERR_INVALID_ARG;
-    st = check_out(rowwise, rows, cols, bs, desc->scale_fmt, false);
+    st = check_out(rowwise, rows, cols, bs, desc->scale_fmt, false, desc->grid);
     if (st != UFP4_OK) return st;
     if (rows > 0 && cols > 0) {
         if (!x || ld < cols) return UFP4_ERR_INVALID_ARG;

@@ -1,7 +1,8 @@
 // Dequantization Q_G(T) = level(code) * scale (UFP4 summary, section 数据集:
 // inside arithmetic the quantized tensor stands for its dequantized values),
 // with an optional inverse RHT x = (z H) S (H'_n = S_n H_n is orthogonal,
-// section 方法).  A check and diagnostics path, off the hot path.
+// section 方法).  MXFP8 codes are E4M3 bytes, one per element.  A check and
+// diagnostics path, off the hot path.
 #include <cstdint>
 #include <cuda_runtime.h>
 
@@ -23,12 +24,20 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
         const int64_t cc = valid ? q % cpr : 0;
         const int64_t c = cc * kChunk;
         float v[16];
-        uint2 code = make_uint2(0u, 0u);
-        if (valid) code = *reinterpret_cast<const uint2*>(p.codes + r * p.codes_ld + c / 2);
+        const bool bytes = p.grid == 4;  // MXFP8: one E4M3 byte per element
+        uint4 code = make_uint4(0u, 0u, 0u, 0u);
+        if (valid && bytes) code = *reinterpret_cast<const uint4*>(p.codes + r * p.codes_ld + c);
+        if (valid && !bytes) {
+            const uint2 c2 = *reinterpret_cast<const uint2*>(p.codes + r * p.codes_ld + c / 2);
+            code.x = c2.x;
+            code.y = c2.y;
+        }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             const uint32_t word = i < 8 ? code.x : code.y;
             const uint32_t nib = (word >> (4 * (i & 7))) & 0xFu;
+            const uint32_t w4 = i < 4 ? code.x : (i < 8 ? code.y : (i < 12 ? code.z : code.w));
+            const uint32_t byte = (w4 >> (8 * (i & 3))) & 0xFFu;
             float s = 0.0f;
             if (valid) {
                 const int64_t si = (r / p.br) * p.scales_ld + (c + i) / p.bc;
@@ -42,7 +51,9 @@ __global__ void __launch_bounds__(256) dequant_kernel(const DequantParams p) {
                     s = ((const float*)p.scales)[si];
                 }
             }
-            v[i] = __fmul_rn(decode_level(p.grid, nib), s);
+            const float lv = bytes ? ((byte & 0x80u) ? -e4m3_value(byte & 0x7Fu) : e4m3_value(byte))
+                                   : decode_level(p.grid, nib);
+            v[i] = __fmul_rn(lv, s);
         }
         if (p.inverse && p.n > 1) {
             const int seg_lane = (int)((c % (p.n > kChunk ? p.n : kChunk)) / kChunk);

@@ -852,6 +852,7 @@ struct PrepParams {
     int grid;          // codebook
     int lbr, lbc;      // log2 of the block rows and columns
     int lhw;           // log2 of the hardware scale block: 4 (E2M1 1x16) or 5
+    int copies;        // stored copies of each chunk (4: replicated)
 };
 
 // Replicated scale chunks of the CTA-pair kernel.  Chunk g along K (g = K
@@ -961,7 +962,7 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
                                      (lane & 3) * kChunkBytes) = word;
 }
 
-// E2M1: only the scales move, into the chunk layout of the pair kernel
+// E2M1 and MXFP8: only the scales move, into the chunk layout of the pair kernel
 // (hardware blocks of 16 or 32 elements, one scale byte each: UE8M0, or E4M3
 // for the two-level format), replicated or not as pair_replicated says.  A
 // warp writes one chunk: lane i builds the chunk's 16-byte line i (cells of
@@ -996,7 +997,7 @@ __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
         cell[c] = v;
     }
     const uint4 line = make_uint4(cell[0], cell[1], cell[2], cell[3]);
-    constexpr int copies = pair_replicated(1) ? 4 : 1;
+    const int copies = p.copies;
     uint8_t* dst = s.out_chunks + ((((int64_t)t * p.chunks_k + g) * parts + h) * copies) * kChunkBytes + i * 16;
 #pragma unroll
     for (int copy = 0; copy < copies; ++copy) *reinterpret_cast<uint4*>(dst + copy * kChunkBytes) = line;
@@ -1093,6 +1094,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes
 
 struct Plan {
     int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X, 3 fp32 block scales (bf16 partials rescaled)
+    bool native;       // kind 0 on MXFP8 codes: E4M3 operands used in place (no widening)
     int bn;            // B tile rows (output tile columns)
     int64_t k_bytes;   // bytes of K per row in the MMA operand
     int64_t k_tiles;
@@ -1136,16 +1138,17 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
         pl.total = off;
         return pl;
     }
-    pl.kind = grid >= 2 ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
+    pl.kind = (grid == 2 || grid == 3) ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
+    pl.native = grid == 4;                                          // MXFP8: E4M3 bytes
     pl.bn = pl.kind == 0 ? kBnFp8 : kBnFp4;
-    pl.k_bytes = grid >= 2 ? K / 2 : K;
+    pl.k_bytes = (grid == 2 || grid == 3) ? K / 2 : K;
     pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
     const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
     pl.chunks_k = pl.k_tiles * cps;
     const int64_t mb = (M + 127) / 128;
     const int64_t nb = (N + pl.bn - 1) / pl.bn * ((pl.bn + 127) / 128);  // chunk blocks of B
     size_t off = 0;
-    if (pl.kind == 0) {
+    if (pl.kind == 0 && !pl.native) {
         pl.fp8_a = off;
         off = align256(off + (size_t)M * K);
         pl.fp8_b = off;
@@ -1250,8 +1253,9 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
         if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
         return launch_pdl(prep_f32s_kernel, dim3((unsigned)blocks, 1, 2), dim3(256), 0, st, pp);
     }
-    if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
+    const bool fp4 = g.grid == 2 || g.grid == 3;
+    if (g.K % 32 && !(fp4 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && fp4) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
@@ -1267,7 +1271,7 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
         ps.rows = (int)op.rows;
         ps.tile_rows = side ? pl.bn : kBM;
         ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;  // whole output tiles
-        ps.out_fp8 = pl.kind == 0 ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
+        ps.out_fp8 = (pl.kind == 0 && !pl.native) ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
         ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
         row_blocks = std::max(row_blocks, (ps.rows_cover + 7) / 8);
     }
@@ -1277,13 +1281,14 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
     pp.lbr = ilog2(g.br);
     pp.lbc = ilog2(g.bc);
     pp.lhw = pl.kind == 2 ? 4 : 5;
-    if (pl.kind == 0) {
+    pp.copies = pair_replicated(pl.kind) ? 4 : 1;
+    if (pl.kind == 0 && !pl.native) {
         // 32 groups of 32 elements per CTA along K, 8 rows per CTA
         const int64_t kslabs = (pl.chunks_k * 4 + 31) / 32;
         if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
         return launch_pdl(prep_widen_kernel, dim3((unsigned)row_blocks, (unsigned)kslabs, 2), dim3(32, 8), 0, st, pp);
     }
-    // FP4: one warp per (128-row part, chunk)
+    // FP4 and MXFP8: only the scales move, one warp per (128-row part, chunk)
     int64_t items = 0;
     for (int side = 0; side < 2; ++side) {
         const PrepSide& ps = pp.side[side];
@@ -1332,18 +1337,21 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
         const int grid = tiles < num_sms ? tiles : num_sms;
         return launch_pdl(k, dim3(grid), dim3(kF32sThreads), (size_t)F32sCfg::kSmem, st, ma, mb, msa, msb, kp);
     }
-    if (g.K % 32 && !(g.grid >= 2 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && g.grid >= 2) return cudaErrorNotSupported;
+    const bool fp4 = g.grid == 2 || g.grid == 3;
+    if (g.K % 32 && !(fp4 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && fp4) return cudaErrorNotSupported;
     const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
     uint8_t* ws = (uint8_t*)g.workspace;
     (void)num_sms;
     // CTA pairs, 256 x bn tiles: A 128 rows per CTA, B bn/2 rows per CTA.
-    // FP8 reads the widened copies in the workspace, FP4 the codes themselves.
-    const void* a_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
-    const void* b_ptr = pl.kind == 0 ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
-    const int64_t a_pitch = pl.kind == 0 ? g.K : g.a.codes_ld;
-    const int64_t b_pitch = pl.kind == 0 ? g.K : g.b.codes_ld;
+    // E1M2 / INT4 read the widened copies in the workspace; FP4 and MXFP8
+    // the codes themselves.
+    const bool widened = pl.kind == 0 && !pl.native;
+    const void* a_ptr = widened ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
+    const void* b_ptr = widened ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
+    const int64_t a_pitch = widened ? g.K : g.a.codes_ld;
+    const int64_t b_pitch = widened ? g.K : g.b.codes_ld;
     CUtensorMap ma, mb, msa, msb;
     if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
     if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn / 2)) return cudaErrorInvalidValue;
@@ -1371,7 +1379,9 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     pk.ldd = g.ldd;
     pk.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
     if (pl.kind == 0) {
-        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp8, j);  // E5M2 x E5M2, M = 256
+        // E5M2 x E5M2 (format 1) for the widened codes, E4M3 x E4M3 (format 0) for MXFP8; M = 256
+        const int fmt = pl.native ? 0 : 1;
+        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(fmt, fmt, 2 * kBM, kBnFp8, j);
         return run_gemm_pair<0, kPairStages, kPairKps>(ma, mb, msa, msb, pk, st);
     }
     if (pl.kind == 1) {

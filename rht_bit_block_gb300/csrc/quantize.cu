@@ -166,7 +166,7 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
                                           uint64_t sr_seed, uint32_t stream, uint32_t group) {
     // INT4 with power-of-two scales rounds by adding 1.5 * 2^23 + 8 (below)
     constexpr bool kMagic = GRID == 1 && !SR && SF == 1;
-    constexpr int lf = kMagic ? 0 : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
+    constexpr int lf = (kMagic || GRID == 4) ? 0 : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
     const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0);
     const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0);
     float ra1 = ra0, rb1 = rb0;
@@ -178,6 +178,26 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         const uint64_t is2 = pk2(fd.inv_s, fd.inv_s);
 #pragma unroll
         for (int i = 0; i < 16; ++i) e[i] = mul2(e[i], is2);
+    }
+    if (GRID == 4) {
+        // MXFP8: t = z * 2^-e (exact), one E4M3 byte per element, nearest
+        // even, saturated at 448; a zero byte keeps no sign
+        const uint64_t q = pk2(ra0, rb0);
+        float ta[16], tb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) up2(mul2(e[i], q), ta[i], tb[i]);
+        uint32_t wa[4], wb[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const uint32_t va = cvt_e4m3x4(ta[4 * k], ta[4 * k + 1], ta[4 * k + 2], ta[4 * k + 3]);
+            const uint32_t vb = cvt_e4m3x4(tb[4 * k], tb[4 * k + 1], tb[4 * k + 2], tb[4 * k + 3]);
+            // per byte: keep bit 7 only where the magnitude bits are nonzero
+            wa[k] = va & (((va & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | 0x7F7F7F7Fu);
+            wb[k] = vb & (((vb & 0x7F7F7F7Fu) + 0x7F7F7F7Fu) | 0x7F7F7F7Fu);
+        }
+        if (A.valid) *reinterpret_cast<uint4*>(A.codes) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+        if (B.valid) *reinterpret_cast<uint4*>(B.codes) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+        return;
     }
     if (kMagic) {
         // t = z r is exact (r a power of two), so one fma t + (1.5 * 2^23 + 8)
@@ -720,7 +740,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
         const bool col_ok = col < T.cols;
         const int left = T.rows - row0 - r0;  // rows of this thread's first row onward
         const bool full = T.rows - row0 >= TR;
-        uint8_t* cp = T.codes + (int64_t)(row0 + r0) * T.codes_ld + (col >> 1);
+        uint8_t* cp = T.codes + (int64_t)(row0 + r0) * T.codes_ld + (GRID == 4 ? col : col >> 1);
         uint8_t* sp = T.scales + ((int64_t)(row0 + r0) * T.scales_ld + (col >> lbw)) * SZ;
         const int64_t cstep = (int64_t)kRPI * T.codes_ld;
         const int64_t sstep = (int64_t)kRPI * T.scales_ld * SZ;
@@ -886,6 +906,7 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int n
     UFP4_R(2)
     UFP4_R(3)
 #undef UFP4_R
+    if (grid == 4 && !sr && sf == 1) return launch_rows<4, false, 1>(maps, p, num_sms, st);  // MXFP8
     return cudaErrorInvalidValue;
 }
 

@@ -21,7 +21,7 @@ constexpr int kChunk = 16;  // elements one thread carries along the quantized d
 
 // Largest level and its reciprocal step for each grid (E1M2 1.75, INT4 7, E2M1 6).
 __host__ __device__ constexpr float grid_qmax(int grid) {
-    return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : (grid == 2 ? 6.0f : 2.0f));
+    return grid == 0 ? 1.75f : (grid == 1 ? 7.0f : (grid == 2 ? 6.0f : (grid == 3 ? 2.0f : 448.0f)));
 }
 
 // E4M3 byte of a >= 0, rounded to nearest even and saturated at 448 (the
@@ -140,10 +140,12 @@ __device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float&
 // carry of M's mantissa + (2^23 - 1 - mq) into the exponent field, so the
 // byte is one add and one shift of M's bits.  Zero (and a subnormal M,
 // outside the contract) gives byte 0.
+// MXFP8 (GRID 4) takes e = floor(log2 M) - 8 instead: the same formula with
+// Eq = 8 and mq = 2^23 - 1 (no carry).
 template <int GRID>
 __device__ __forceinline__ int scale_po2_byte(float M) {
-    constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : 2);
-    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : 0x600000u);  // 1.5, 1.0 or 1.75
+    constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : (GRID == 4 ? 8 : 2));
+    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : (GRID == 4 ? 0x7FFFFFu : 0x600000u));
     const uint32_t b = __float_as_uint(M);
     const int eb = (int)((b + (0x7FFFFFu - mq)) >> 23) - Eq;
     return b < 0x00800000u ? 0 : min(max(eb, 0), 254);

@@ -18,7 +18,8 @@ STATUS_NAMES = {0: "UFP4_OK", 1: "UFP4_ERR_INVALID_ARG", 2: "UFP4_ERR_UNSUPPORTE
                 3: "UFP4_ERR_ALIGNMENT", 4: "UFP4_ERR_CUDA", 5: "UFP4_ERR_TIMEOUT"}
 GRID_E1M2, GRID_INT4, GRID_E2M1 = 0, 1, 2
 GRID_E2M1_R2 = 3
-GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1, "e2m1r2": GRID_E2M1_R2}
+GRID_MXFP8 = 4  # E4M3 byte codes, 1 x 32 blocks with E8M0 scales
+GRIDS = {"e1m2": GRID_E1M2, "int4": GRID_INT4, "e2m1": GRID_E2M1, "e2m1r2": GRID_E2M1_R2, "mxfp8": GRID_MXFP8}
 ROUND_RTNE, ROUND_SR = 0, 1
 SCALE_FP32, SCALE_UE8M0, SCALE_E4M3 = 0, 1, 2
 OUT_ROWWISE, OUT_COLWISE = 1, 2
@@ -116,7 +117,7 @@ def make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=0, rounding=ROUND_RTNE
 
 def qtensor(codes, scales, rows: int, cols: int, tensor_amax=None) -> QTensor:
     """Describe a quantized matrix held in torch tensors codes [rows, cols/2]
-    (uint8) and scales [rows/br, cols/bc] (float32 or uint8); tensor_amax: a
+    (uint8; [rows, cols] for MXFP8) and scales [rows/br, cols/bc] (float32 or uint8); tensor_amax: a
     1-element float32 tensor for the two-level scale format."""
     return QTensor(codes.data_ptr(), scales.data_ptr(), rows, cols, codes.stride(0) * codes.element_size(),
                    scales.stride(0), tensor_amax.data_ptr() if tensor_amax is not None else None)
@@ -260,7 +261,8 @@ def alloc_quantized(rows: int, cols: int, desc: QuantDesc, device):
     """torch buffers for one quantized matrix (rows x cols in its own layout)."""
     import torch
     br, bc = desc.block_rows, desc.block_cols
-    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=device)
+    code_cols = cols if desc.grid == GRID_MXFP8 else cols // 2
+    codes = torch.empty((rows, code_cols), dtype=torch.uint8, device=device)
     sdt = torch.float32 if desc.scale_fmt == SCALE_FP32 else torch.uint8
     scales = torch.empty((rows // br, cols // bc), dtype=sdt, device=device)
     return codes, scales

@@ -130,3 +130,28 @@ def test_two_level_validation(lib):
     A = ufp4.QTensor(0x2000, 0x3000, 128, 128, 64, 8, 0x5000)
     assert lib.ufp4_gemm(ctypes.byref(A), ctypes.byref(A), ctypes.byref(e1m2), ctypes.c_void_p(0x4000), 128, None, 0,
                          None) == 2
+
+
+def test_mxfp8_validation(lib):
+    """MXFP8 takes 1 x 32 blocks, E8M0 (UE8M0) scales, RTNE and the row-wise
+    output only, with byte codes (codes_ld >= cols, a multiple of 16)."""
+    UNS, INV, ALN = 2, 1, 3
+    mk = lambda **kw: ufp4.make_desc(grid="mxfp8", block=kw.pop("block", (1, 32)),
+                                     scale_fmt=kw.pop("scale_fmt", ufp4.SCALE_UE8M0), **kw)
+    x, codes, scales = 0x1000, 0x2000, 0x3000
+
+    def call(desc, codes_ld=64, colwise=False, rows=64, cols=64):
+        q = ufp4.QTensor(codes, scales, rows, cols, codes_ld, cols // 32)
+        c = ufp4.QTensor(codes, scales, cols, rows, rows, rows // 32)
+        return lib.ufp4_rht_quantize(ctypes.c_void_p(x), rows, cols, cols, ctypes.byref(desc), ctypes.byref(q),
+                                     ctypes.byref(c) if colwise else None, None)
+    assert call(mk(block=(1, 16))) == UNS
+    assert call(mk(scale_fmt=ufp4.SCALE_FP32)) == UNS
+    assert call(mk(rounding=ufp4.ROUND_SR)) == UNS
+    assert call(mk(out_mask=3), colwise=True) == UNS
+    assert call(mk(), codes_ld=32) == INV      # half-byte leading dimension is too small for byte codes
+    assert call(mk(), codes_ld=72) == ALN      # not a multiple of 16
+    stats = (ctypes.c_double * 4)()
+    q = ufp4.QTensor(codes, scales, 64, 64, 64, 2)
+    assert lib.ufp4_quant_error_stats(ctypes.c_void_p(x), 64, 64, 64, ctypes.byref(mk()), ctypes.byref(q),
+                                      stats, None) == UNS
