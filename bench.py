@@ -545,6 +545,73 @@ def run_suite(args):
     tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
     emit("gemm", f"{M5}x{N5}x{K5} e1m2 1x16 UE8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
          kernel_ms=kms)
+    del A, B, ws, D
+
+    # 5. MoE-7.9B-like expert FFN step: seeded top-2 routing of 16384 tokens
+    # over 8 experts (hidden 2048, ffn 1408); grouped row+col quantization of
+    # X (RTNE) and dY (SR), per-expert W_e row+col (RTNE), then the grouped
+    # FPROP, DGRAD and WGRAD GEMMs (prep included)
+    lists, x_all, w_all, dy_np = inputs.moe_step()
+    experts, hidden, ffn = w_all.shape[0], w_all.shape[2], w_all.shape[1]
+    counts = [len(l) for l in lists]
+    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    total = int(off[-1])
+    xs = to_t(np.ascontiguousarray(np.concatenate([x_all[l] for l in lists]))).to(dev)
+    dys = to_t(dy_np).to(dev)
+    ws_e = [to_t(np.ascontiguousarray(w_all[e])).to(dev) for e in range(experts)]
+    kw = dict(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0, out_mask=3)
+    x_desc = ufp4.make_desc(**kw)
+    dy_desc = ufp4.make_desc(rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED, **kw)
+    gdesc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+    pads = [ufp4.ufp4_grouped_padded_rows(c, x_desc) for c in counts]
+    poff = np.concatenate([[0], np.cumsum(pads)]).astype(np.int64)
+    ptot = int(poff[-1])
+
+    def grouped_bufs(cols):
+        rc = torch.empty((total, cols // 2), dtype=torch.uint8, device=dev)
+        rs = torch.empty((total, cols // 16), dtype=torch.uint8, device=dev)
+        cc = torch.empty((cols * ptot // 2,), dtype=torch.uint8, device=dev)
+        cs = torch.empty((cols * ptot // 16,), dtype=torch.uint8, device=dev)
+        row_q = ufp4.qtensor(rc, rs, total, cols)
+        col_q = ufp4.QTensor(cc.data_ptr(), cs.data_ptr(), cols, ptot, 0, 0)
+        rows = [ufp4.qtensor(rc[off[g]:off[g + 1]], rs[off[g]:off[g + 1]], counts[g], cols) for g in range(experts)]
+        colsq = [ufp4.qtensor(cc[cols * poff[g] // 2: cols * poff[g + 1] // 2].view(cols, pads[g] // 2),
+                              cs[cols * poff[g] // 16: cols * poff[g + 1] // 16].view(cols, pads[g] // 16),
+                              cols, pads[g]) for g in range(experts)]
+        return (rc, rs, cc, cs), row_q, col_q, rows, colsq
+    xb, xrq, xcq, xrow, xcol = grouped_bufs(hidden)
+    yb, yrq, ycq, yrow, ycol = grouped_bufs(ffn)
+    wbufs = [(ufp4.alloc_quantized(ffn, hidden, x_desc, dev), ufp4.alloc_quantized(hidden, ffn, x_desc, dev))
+             for _ in range(experts)]
+    wrow = [ufp4.qtensor(*r, ffn, hidden) for r, _ in wbufs]
+    wcol = [ufp4.qtensor(*c, hidden, ffn) for _, c in wbufs]
+    gemms = {"FPROP": (xrow, wrow, [(c, ffn) for c in counts]),
+             "DGRAD": (yrow, wcol, [(c, hidden) for c in counts]),
+             "WGRAD": (ycol, xcol, [(ffn, hidden)] * experts)}
+    outs = {k: [torch.empty((m, n), dtype=torch.float32, device=dev) for m, n in v[2]] for k, v in gemms.items()}
+    wsz = max(ufp4.ufp4_gemm_grouped_workspace_size(a, b, gdesc) for a, b, _ in gemms.values())
+    gws = torch.empty(max(1, wsz), dtype=torch.uint8, device=dev)
+
+    def quantize_all(i):
+        ufp4.ufp4_rht_quantize_grouped(xs, off.tolist(), x_desc, xrq, xcq, stream.cuda_stream)
+        ufp4.ufp4_rht_quantize_grouped(dys, off.tolist(), dy_desc, yrq, ycq, stream.cuda_stream)
+        for e in range(experts):
+            ufp4.ufp4_rht_quantize(ws_e[e], x_desc, wrow[e], wcol[e], stream.cuda_stream)
+
+    def gemm_all(i):
+        for k, (a, b, _) in gemms.items():
+            ufp4.ufp4_gemm_grouped(a, b, gdesc, outs[k], gws, stream.cuda_stream)
+
+    qms = timed(quantize_all, reps=10)
+    gms = timed(gemm_all, reps=10)
+    flops = 3 * 2.0 * total * ffn * hidden
+    qbytes = (total * hidden + total * ffn + experts * ffn * hidden) * (2 + 2 * (0.5 + 1 / 16))
+    emit("moe_step", f"MoE-7.9B-like step, {total} routed rows, 8 experts, hidden {hidden}, ffn {ffn}: "
+         "grouped row+col quantize of X (RTNE), dY (SR) and W_e (RTNE)", qbytes / (qms / 1e3) / 1e9, "GB/s",
+         qbytes / (qms / 1e3) / 1e9 / pk["hbm"], pk["hbm"], ms=qms)
+    emit("moe_step", f"MoE-7.9B-like step: grouped FPROP + DGRAD + WGRAD GEMMs, e1m2 1x16 UE8M0, prep included",
+         flops / (gms / 1e3) / 1e12, "TFLOP/s", flops / (gms / 1e3) / 1e12 / (2 * pk["bf16"]), 2 * pk["bf16"],
+         ms=gms, step_ms=qms + gms)
 
 
 def main():
