@@ -382,7 +382,7 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------- suite mode
-def run_suite(args):
+def run_suite(args, sections=("rowwise", "rowcol", "diag", "gemm", "moe")):
     """Further measurements, one JSON line each (not the headline): the other
     workloads of the configuration list and the widened rows.  CUDA events on
     the launching stream, 3 warm-ups, median of the timed repetitions; inputs
@@ -418,200 +418,212 @@ def run_suite(args):
         per = 1 if desc.scale_fmt == ufp4.SCALE_UE8M0 else 4
         return per / (desc.block_rows * desc.block_cols)
 
-    # 1. large-shape sweep operand, row-wise (X 16384 x 7168, > L2)
-    x5, _ = inputs.large_sweep(k=7168, n=128)
-    xs5 = [to_t(x5).to(dev) for _ in range(2)]
-    rows, cols = x5.shape
-    cases = [("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_RTNE), ("int4", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
-             ("e2m1", (1, 16), 16, ufp4.SCALE_UE8M0, 0), ("e2m1r2", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
-             ("e1m2", (1, 16), 16, ufp4.SCALE_FP32, 0), ("e1m2", (1, 32), 64, ufp4.SCALE_UE8M0, 0),
-             ("e1m2", (1, 16), 256, ufp4.SCALE_UE8M0, 0), ("e2m1", (32, 32), 16, ufp4.SCALE_UE8M0, 0),
-             ("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_SR),
-             ("mxfp8", (1, 32), 1, ufp4.SCALE_UE8M0, 0), ("mxfp8", (1, 32), 16, ufp4.SCALE_UE8M0, 0)]
-    for grid, block, n, fmt, rnd in cases:
-        desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt, rounding=rnd,
-                              sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
-        out = ufp4.alloc_quantized(rows, cols, desc, dev)
-        q = ufp4.qtensor(*out, rows, cols)
-        ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
-        code_bytes = 1.0 if grid == "mxfp8" else 0.5
-        gbs = rows * cols * (2 + code_bytes + scale_bytes(desc)) / (ms / 1e3) / 1e9
-        emit("quantize_rowwise", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
-             f"{('E8M0' if grid == 'mxfp8' else 'UE8M0') if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs,
-             "GB/s", gbs / pk["hbm"], pk["hbm"],
-             ms=ms)
-    del xs5
+    if "rowwise" in sections:
+        # 1. large-shape sweep operand, row-wise (X 16384 x 7168, > L2)
+        x5, _ = inputs.large_sweep(k=7168, n=128)
+        xs5 = [to_t(x5).to(dev) for _ in range(2)]
+        rows, cols = x5.shape
+        cases = [("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_RTNE), ("int4", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
+                 ("e2m1", (1, 16), 16, ufp4.SCALE_UE8M0, 0), ("e2m1r2", (1, 16), 16, ufp4.SCALE_UE8M0, 0),
+                 ("e1m2", (1, 16), 16, ufp4.SCALE_FP32, 0), ("e1m2", (1, 32), 64, ufp4.SCALE_UE8M0, 0),
+                 ("e1m2", (1, 16), 256, ufp4.SCALE_UE8M0, 0), ("e2m1", (32, 32), 16, ufp4.SCALE_UE8M0, 0),
+                 ("e1m2", (1, 16), 16, ufp4.SCALE_UE8M0, ufp4.ROUND_SR),
+                 ("mxfp8", (1, 32), 1, ufp4.SCALE_UE8M0, 0), ("mxfp8", (1, 32), 16, ufp4.SCALE_UE8M0, 0)]
+        for grid, block, n, fmt, rnd in cases:
+            desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt, rounding=rnd,
+                                  sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
+            out = ufp4.alloc_quantized(rows, cols, desc, dev)
+            q = ufp4.qtensor(*out, rows, cols)
+            ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
+            code_bytes = 1.0 if grid == "mxfp8" else 0.5
+            gbs = rows * cols * (2 + code_bytes + scale_bytes(desc)) / (ms / 1e3) / 1e9
+            emit("quantize_rowwise", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
+                 f"{('E8M0' if grid == 'mxfp8' else 'UE8M0') if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs,
+                 "GB/s", gbs / pk["hbm"], pk["hbm"],
+                 ms=ms)
+        del xs5
 
-    # 2. dY stochastic-rounding path: row-wise and column-wise from one read
-    dy, _ = inputs.dy_sr()
-    dys = [to_t(dy).to(dev) for _ in range(5)]
-    r3, c3 = dy.shape
-    for fmt in (ufp4.SCALE_FP32, ufp4.SCALE_UE8M0):
-        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
-                              rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED,
-                              out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
-        ro = ufp4.alloc_quantized(r3, c3, desc, dev)
-        co = ufp4.alloc_quantized(c3, r3, desc, dev)
-        rq, cq = ufp4.qtensor(*ro, r3, c3), ufp4.qtensor(*co, c3, r3)
-        ms = timed(lambda i: ufp4.ufp4_rht_quantize(dys[i % 5], desc, rq, cq, stream.cuda_stream))
-        gbs = r3 * c3 * (2 + 2 * (0.5 + scale_bytes(desc))) / (ms / 1e3) / 1e9
-        emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 SR row+col", gbs,
-             "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
+    if "rowcol" in sections:
+        # 2. dY stochastic-rounding path: row-wise and column-wise from one read
+        dy, _ = inputs.dy_sr()
+        dys = [to_t(dy).to(dev) for _ in range(5)]
+        r3, c3 = dy.shape
+        for fmt in (ufp4.SCALE_FP32, ufp4.SCALE_UE8M0):
+            desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
+                                  rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED,
+                                  out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
+            ro = ufp4.alloc_quantized(r3, c3, desc, dev)
+            co = ufp4.alloc_quantized(c3, r3, desc, dev)
+            rq, cq = ufp4.qtensor(*ro, r3, c3), ufp4.qtensor(*co, c3, r3)
+            ms = timed(lambda i: ufp4.ufp4_rht_quantize(dys[i % 5], desc, rq, cq, stream.cuda_stream))
+            gbs = r3 * c3 * (2 + 2 * (0.5 + scale_bytes(desc))) / (ms / 1e3) / 1e9
+            emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 SR row+col", gbs,
+                 "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
 
-    # 3. diagnostics on the dense FPROP X
-    x2, _ = inputs.dense_fprop(n=128)
-    x2s = [to_t(x2).to(dev) for _ in range(5)]
-    r2, c2 = x2.shape
-    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
-                          scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
-    qout = [ufp4.alloc_quantized(r2, c2, desc, dev) for _ in range(5)]
-    for i in range(5):
-        ufp4.ufp4_rht_quantize(x2s[i], desc, ufp4.qtensor(*qout[i], r2, c2), None, stream.cuda_stream)
-    st = torch.zeros(4, dtype=torch.float64, device=dev)
-    ms = timed(lambda i: ufp4.ufp4_quant_error_stats(x2s[i % 5], desc, ufp4.qtensor(*qout[i % 5], r2, c2), st,
-                                                     stream.cuda_stream))
-    gbs = r2 * c2 * (2 + 0.5 + 1 / 16) / (ms / 1e3) / 1e9
-    s = st.cpu().numpy()
-    emit("diagnostics", f"quant_error_stats X {r2}x{c2} e1m2 1x16 UE8M0 n=16", gbs, "GB/s", gbs / pk["hbm"],
-         pk["hbm"], ms=ms, sqnr_db=float(10 * np.log10(s[0] / s[1])), shrinkage=float(s[2] / s[0]))
-    del x2s, qout
+    if "diag" in sections:
+        # 3. diagnostics on the dense FPROP X
+        x2, _ = inputs.dense_fprop(n=128)
+        x2s = [to_t(x2).to(dev) for _ in range(5)]
+        r2, c2 = x2.shape
+        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
+                              scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+        qout = [ufp4.alloc_quantized(r2, c2, desc, dev) for _ in range(5)]
+        for i in range(5):
+            ufp4.ufp4_rht_quantize(x2s[i], desc, ufp4.qtensor(*qout[i], r2, c2), None, stream.cuda_stream)
+        st = torch.zeros(4, dtype=torch.float64, device=dev)
+        ms = timed(lambda i: ufp4.ufp4_quant_error_stats(x2s[i % 5], desc, ufp4.qtensor(*qout[i % 5], r2, c2), st,
+                                                         stream.cuda_stream))
+        gbs = r2 * c2 * (2 + 0.5 + 1 / 16) / (ms / 1e3) / 1e9
+        s = st.cpu().numpy()
+        emit("diagnostics", f"quant_error_stats X {r2}x{c2} e1m2 1x16 UE8M0 n=16", gbs, "GB/s", gbs / pk["hbm"],
+             pk["hbm"], ms=ms, sqnr_db=float(10 * np.log10(s[0] / s[1])), shrinkage=float(s[2] / s[0]))
+        del x2s, qout
 
-    # 4. GEMMs per grid on the dense FPROP shape (tensor-core kernel alone, prep timed apart)
-    M, N, K = 8192, 5632, 2048
-    g = torch.Generator().manual_seed(7)
-    for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 32), 2.0), ("e2m1", (1, 16), 6.0),
-                                   ("e2m1", (1, 32), 6.0), ("e2m1r2", (1, 16), 6.0)):
-        desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
-        def operand(rows):
-            c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8)
-            c = c & 0x77 if grid != "int4" else c & 0x77  # valid codes in every grid, no -0 / -8
-            sc = torch.randint(120, 132, (rows, K // block[1]), generator=g, dtype=torch.uint8)
+    if "gemm" in sections:
+        # 4. GEMMs per grid on the dense FPROP shape (tensor-core kernel alone, prep timed apart)
+        M, N, K = 8192, 5632, 2048
+        g = torch.Generator().manual_seed(7)
+        for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 32), 2.0), ("e2m1", (1, 16), 6.0),
+                                       ("e2m1", (1, 32), 6.0), ("e2m1r2", (1, 16), 6.0)):
+            desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
+            def operand(rows):
+                c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8)
+                c = c & 0x77 if grid != "int4" else c & 0x77  # valid codes in every grid, no -0 / -8
+                sc = torch.randint(120, 132, (rows, K // block[1]), generator=g, dtype=torch.uint8)
+                return c.to(dev), sc.to(dev)
+            A, B = operand(M), operand(N)
+            qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+            ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+            D = torch.empty((M, N), dtype=torch.float32, device=dev)
+            pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+            kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+            tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+            peak = kind_peak * pk["bf16"]
+            emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
+                 kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
+            del A, B, ws, D
+        # MXFP8 operands (E4M3 codes read in place by the FP8 kernel)
+        desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
+        def e4m3_operand(rows):
+            c = torch.randint(0, 0x7F, (rows, K), generator=g, dtype=torch.uint8)  # finite magnitudes
+            c = c | (torch.randint(0, 2, (rows, K), generator=g, dtype=torch.uint8) << 7)
+            sc = torch.randint(120, 132, (rows, K // 32), generator=g, dtype=torch.uint8)
             return c.to(dev), sc.to(dev)
-        A, B = operand(M), operand(N)
+        A, B = e4m3_operand(M), e4m3_operand(N)
         qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
         ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
         D = torch.empty((M, N), dtype=torch.float32, device=dev)
         pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
         kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
         tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-        peak = kind_peak * pk["bf16"]
-        emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
-             kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
+        emit("gemm", f"{M}x{N}x{K} mxfp8 1x32 E8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
+             kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (nominal ratio)")
         del A, B, ws, D
-    # MXFP8 operands (E4M3 codes read in place by the FP8 kernel)
-    desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
-    def e4m3_operand(rows):
-        c = torch.randint(0, 0x7F, (rows, K), generator=g, dtype=torch.uint8)  # finite magnitudes
-        c = c | (torch.randint(0, 2, (rows, K), generator=g, dtype=torch.uint8) << 7)
-        sc = torch.randint(120, 132, (rows, K // 32), generator=g, dtype=torch.uint8)
-        return c.to(dev), sc.to(dev)
-    A, B = e4m3_operand(M), e4m3_operand(N)
-    qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
-    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
-    D = torch.empty((M, N), dtype=torch.float32, device=dev)
-    pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
-    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
-    tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-    emit("gemm", f"{M}x{N}x{K} mxfp8 1x32 E8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
-         kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (nominal ratio)")
-    del A, B, ws, D
-    # fp32 block scales (the two-scale path: bf16 partials rescaled on the CUDA cores)
-    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
-    A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-         torch.rand((M, K // 16), generator=g).add(0.5).to(dev))
-    B = (torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-         torch.rand((N, K // 16), generator=g).add(0.5).to(dev))
-    qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
-    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
-    D = torch.empty((M, N), dtype=torch.float32, device=dev)
-    pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
-    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
-    tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-    emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
-         2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
-    del A, B, ws, D
-    # the large-sweep FPROP GEMM
-    M5, N5, K5 = 16384, 7168, 7168
-    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
-    A = (torch.randint(0, 256, (M5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-         torch.randint(120, 132, (M5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
-    B = (torch.randint(0, 256, (N5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-         torch.randint(120, 132, (N5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
-    qa, qb = ufp4.qtensor(*A, M5, K5), ufp4.qtensor(*B, N5, K5)
-    ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M5, N5, K5, desc), dtype=torch.uint8, device=dev)
-    D = torch.empty((M5, N5), dtype=torch.float32, device=dev)
-    ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream)
-    kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream), reps=10)
-    tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
-    emit("gemm", f"{M5}x{N5}x{K5} e1m2 1x16 UE8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
-         kernel_ms=kms)
-    del A, B, ws, D
+        # fp32 block scales (the two-scale path: bf16 partials rescaled on the CUDA cores)
+        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
+        A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+             torch.rand((M, K // 16), generator=g).add(0.5).to(dev))
+        B = (torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+             torch.rand((N, K // 16), generator=g).add(0.5).to(dev))
+        qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+        D = torch.empty((M, N), dtype=torch.float32, device=dev)
+        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+        emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
+             2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
+        del A, B, ws, D
+        # the large-sweep FPROP GEMM
+        M5, N5, K5 = 16384, 7168, 7168
+        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+        A = (torch.randint(0, 256, (M5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+             torch.randint(120, 132, (M5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
+        B = (torch.randint(0, 256, (N5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+             torch.randint(120, 132, (N5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
+        qa, qb = ufp4.qtensor(*A, M5, K5), ufp4.qtensor(*B, N5, K5)
+        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M5, N5, K5, desc), dtype=torch.uint8, device=dev)
+        D = torch.empty((M5, N5), dtype=torch.float32, device=dev)
+        ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream)
+        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream), reps=10)
+        tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
+        emit("gemm", f"{M5}x{N5}x{K5} e1m2 1x16 UE8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
+             kernel_ms=kms)
+        del A, B, ws, D
 
-    # 5. MoE-7.9B-like expert FFN step: seeded top-2 routing of 16384 tokens
-    # over 8 experts (hidden 2048, ffn 1408); grouped row+col quantization of
-    # X (RTNE) and dY (SR), per-expert W_e row+col (RTNE), then the grouped
-    # FPROP, DGRAD and WGRAD GEMMs (prep included)
-    lists, x_all, w_all, dy_np = inputs.moe_step()
-    experts, hidden, ffn = w_all.shape[0], w_all.shape[2], w_all.shape[1]
-    counts = [len(l) for l in lists]
-    off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
-    total = int(off[-1])
-    xs = to_t(np.ascontiguousarray(np.concatenate([x_all[l] for l in lists]))).to(dev)
-    dys = to_t(dy_np).to(dev)
-    ws_e = [to_t(np.ascontiguousarray(w_all[e])).to(dev) for e in range(experts)]
-    kw = dict(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0, out_mask=3)
-    x_desc = ufp4.make_desc(**kw)
-    dy_desc = ufp4.make_desc(rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED, **kw)
-    gdesc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
-    pads = [ufp4.ufp4_grouped_padded_rows(c, x_desc) for c in counts]
-    poff = np.concatenate([[0], np.cumsum(pads)]).astype(np.int64)
-    ptot = int(poff[-1])
+    if "moe" in sections:
+        # 5. MoE-7.9B-like expert FFN step: seeded top-2 routing of 16384 tokens
+        # over 8 experts (hidden 2048, ffn 1408); grouped row+col quantization of
+        # X (RTNE) and dY (SR), per-expert W_e row+col (RTNE), then the grouped
+        # FPROP, DGRAD and WGRAD GEMMs (prep included)
+        lists, x_all, w_all, dy_np = inputs.moe_step()
+        experts, hidden, ffn = w_all.shape[0], w_all.shape[2], w_all.shape[1]
+        counts = [len(l) for l in lists]
+        off = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+        total = int(off[-1])
+        xs = to_t(np.ascontiguousarray(np.concatenate([x_all[l] for l in lists]))).to(dev)
+        dys = to_t(dy_np).to(dev)
+        w_stack = to_t(np.ascontiguousarray(w_all.reshape(experts * ffn, hidden))).to(dev)
+        w_off = [e * ffn for e in range(experts + 1)]
+        kw = dict(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0, out_mask=3)
+        x_desc = ufp4.make_desc(**kw)
+        dy_desc = ufp4.make_desc(rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED, **kw)
+        gdesc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+        pads = [ufp4.ufp4_grouped_padded_rows(c, x_desc) for c in counts]
+        poff = np.concatenate([[0], np.cumsum(pads)]).astype(np.int64)
+        ptot = int(poff[-1])
 
-    def grouped_bufs(cols):
-        rc = torch.empty((total, cols // 2), dtype=torch.uint8, device=dev)
-        rs = torch.empty((total, cols // 16), dtype=torch.uint8, device=dev)
-        cc = torch.empty((cols * ptot // 2,), dtype=torch.uint8, device=dev)
-        cs = torch.empty((cols * ptot // 16,), dtype=torch.uint8, device=dev)
-        row_q = ufp4.qtensor(rc, rs, total, cols)
-        col_q = ufp4.QTensor(cc.data_ptr(), cs.data_ptr(), cols, ptot, 0, 0)
-        rows = [ufp4.qtensor(rc[off[g]:off[g + 1]], rs[off[g]:off[g + 1]], counts[g], cols) for g in range(experts)]
-        colsq = [ufp4.qtensor(cc[cols * poff[g] // 2: cols * poff[g + 1] // 2].view(cols, pads[g] // 2),
-                              cs[cols * poff[g] // 16: cols * poff[g + 1] // 16].view(cols, pads[g] // 16),
-                              cols, pads[g]) for g in range(experts)]
-        return (rc, rs, cc, cs), row_q, col_q, rows, colsq
-    xb, xrq, xcq, xrow, xcol = grouped_bufs(hidden)
-    yb, yrq, ycq, yrow, ycol = grouped_bufs(ffn)
-    wbufs = [(ufp4.alloc_quantized(ffn, hidden, x_desc, dev), ufp4.alloc_quantized(hidden, ffn, x_desc, dev))
-             for _ in range(experts)]
-    wrow = [ufp4.qtensor(*r, ffn, hidden) for r, _ in wbufs]
-    wcol = [ufp4.qtensor(*c, hidden, ffn) for _, c in wbufs]
-    gemms = {"FPROP": (xrow, wrow, [(c, ffn) for c in counts]),
-             "DGRAD": (yrow, wcol, [(c, hidden) for c in counts]),
-             "WGRAD": (ycol, xcol, [(ffn, hidden)] * experts)}
-    outs = {k: [torch.empty((m, n), dtype=torch.float32, device=dev) for m, n in v[2]] for k, v in gemms.items()}
-    wsz = max(ufp4.ufp4_gemm_grouped_workspace_size(a, b, gdesc) for a, b, _ in gemms.values())
-    gws = torch.empty(max(1, wsz), dtype=torch.uint8, device=dev)
+        def grouped_bufs(cols):
+            rc = torch.empty((total, cols // 2), dtype=torch.uint8, device=dev)
+            rs = torch.empty((total, cols // 16), dtype=torch.uint8, device=dev)
+            cc = torch.empty((cols * ptot // 2,), dtype=torch.uint8, device=dev)
+            cs = torch.empty((cols * ptot // 16,), dtype=torch.uint8, device=dev)
+            row_q = ufp4.qtensor(rc, rs, total, cols)
+            col_q = ufp4.QTensor(cc.data_ptr(), cs.data_ptr(), cols, ptot, 0, 0)
+            rows = [ufp4.qtensor(rc[off[g]:off[g + 1]], rs[off[g]:off[g + 1]], counts[g], cols) for g in range(experts)]
+            colsq = [ufp4.qtensor(cc[cols * poff[g] // 2: cols * poff[g + 1] // 2].view(cols, pads[g] // 2),
+                                  cs[cols * poff[g] // 16: cols * poff[g + 1] // 16].view(cols, pads[g] // 16),
+                                  cols, pads[g]) for g in range(experts)]
+            return (rc, rs, cc, cs), row_q, col_q, rows, colsq
+        xb, xrq, xcq, xrow, xcol = grouped_bufs(hidden)
+        yb, yrq, ycq, yrow, ycol = grouped_bufs(ffn)
+        # W_e: one grouped call over the stacked experts (ffn is a multiple of the
+        # grouped padding unit, so each expert's column-wise slab is its own W_e^T)
+        assert ufp4.ufp4_grouped_padded_rows(ffn, x_desc) == ffn
+        wrc = torch.empty((experts * ffn, hidden // 2), dtype=torch.uint8, device=dev)
+        wrs = torch.empty((experts * ffn, hidden // 16), dtype=torch.uint8, device=dev)
+        wcc = torch.empty((experts, hidden, ffn // 2), dtype=torch.uint8, device=dev)
+        wcs = torch.empty((experts, hidden, ffn // 16), dtype=torch.uint8, device=dev)
+        w_rq = ufp4.qtensor(wrc, wrs, experts * ffn, hidden)
+        w_cq = ufp4.QTensor(wcc.data_ptr(), wcs.data_ptr(), hidden, experts * ffn, 0, 0)
+        wrow = [ufp4.qtensor(wrc[e * ffn:(e + 1) * ffn], wrs[e * ffn:(e + 1) * ffn], ffn, hidden) for e in range(experts)]
+        wcol = [ufp4.qtensor(wcc[e], wcs[e], hidden, ffn) for e in range(experts)]
+        gemms = {"FPROP": (xrow, wrow, [(c, ffn) for c in counts]),
+                 "DGRAD": (yrow, wcol, [(c, hidden) for c in counts]),
+                 "WGRAD": (ycol, xcol, [(ffn, hidden)] * experts)}
+        outs = {k: [torch.empty((m, n), dtype=torch.float32, device=dev) for m, n in v[2]] for k, v in gemms.items()}
+        wsz = max(ufp4.ufp4_gemm_grouped_workspace_size(a, b, gdesc) for a, b, _ in gemms.values())
+        gws = torch.empty(max(1, wsz), dtype=torch.uint8, device=dev)
 
-    def quantize_all(i):
-        ufp4.ufp4_rht_quantize_grouped(xs, off.tolist(), x_desc, xrq, xcq, stream.cuda_stream)
-        ufp4.ufp4_rht_quantize_grouped(dys, off.tolist(), dy_desc, yrq, ycq, stream.cuda_stream)
-        for e in range(experts):
-            ufp4.ufp4_rht_quantize(ws_e[e], x_desc, wrow[e], wcol[e], stream.cuda_stream)
+        def quantize_all(i):
+            ufp4.ufp4_rht_quantize_grouped(xs, off.tolist(), x_desc, xrq, xcq, stream.cuda_stream)
+            ufp4.ufp4_rht_quantize_grouped(dys, off.tolist(), dy_desc, yrq, ycq, stream.cuda_stream)
+            ufp4.ufp4_rht_quantize_grouped(w_stack, w_off, x_desc, w_rq, w_cq, stream.cuda_stream)
 
-    def gemm_all(i):
-        for k, (a, b, _) in gemms.items():
-            ufp4.ufp4_gemm_grouped(a, b, gdesc, outs[k], gws, stream.cuda_stream)
+        def gemm_all(i):
+            for k, (a, b, _) in gemms.items():
+                ufp4.ufp4_gemm_grouped(a, b, gdesc, outs[k], gws, stream.cuda_stream)
 
-    qms = timed(quantize_all, reps=10)
-    gms = timed(gemm_all, reps=10)
-    flops = 3 * 2.0 * total * ffn * hidden
-    qbytes = (total * hidden + total * ffn + experts * ffn * hidden) * (2 + 2 * (0.5 + 1 / 16))
-    emit("moe_step", f"MoE-7.9B-like step, {total} routed rows, 8 experts, hidden {hidden}, ffn {ffn}: "
-         "grouped row+col quantize of X (RTNE), dY (SR) and W_e (RTNE)", qbytes / (qms / 1e3) / 1e9, "GB/s",
-         qbytes / (qms / 1e3) / 1e9 / pk["hbm"], pk["hbm"], ms=qms)
-    emit("moe_step", f"MoE-7.9B-like step: grouped FPROP + DGRAD + WGRAD GEMMs, e1m2 1x16 UE8M0, prep included",
-         flops / (gms / 1e3) / 1e12, "TFLOP/s", flops / (gms / 1e3) / 1e12 / (2 * pk["bf16"]), 2 * pk["bf16"],
-         ms=gms, step_ms=qms + gms)
+        qms = timed(quantize_all, reps=10)
+        gms = timed(gemm_all, reps=10)
+        flops = 3 * 2.0 * total * ffn * hidden
+        qbytes = (total * hidden + total * ffn + experts * ffn * hidden) * (2 + 2 * (0.5 + 1 / 16))
+        emit("moe_step", f"MoE-7.9B-like step, {total} routed rows, 8 experts, hidden {hidden}, ffn {ffn}: "
+             "grouped row+col quantize of X (RTNE), dY (SR) and W_e (RTNE)", qbytes / (qms / 1e3) / 1e9, "GB/s",
+             qbytes / (qms / 1e3) / 1e9 / pk["hbm"], pk["hbm"], ms=qms)
+        emit("moe_step", f"MoE-7.9B-like step: grouped FPROP + DGRAD + WGRAD GEMMs, e1m2 1x16 UE8M0, prep included",
+             flops / (gms / 1e3) / 1e12, "TFLOP/s", flops / (gms / 1e3) / 1e12 / (2 * pk["bf16"]), 2 * pk["bf16"],
+             ms=gms, step_ms=qms + gms)
 
 
 def main():
@@ -624,11 +636,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="further measurements (other workloads, widened rows), one JSON line each")
+    ap.add_argument("--suite-sections", default="rowwise,rowcol,diag,gemm,moe",
+                    help="comma-separated subset of the suite: rowwise, rowcol, diag, gemm, moe")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.suite:
-        run_suite(args)
+        run_suite(args, tuple(args.suite_sections.split(",")))
         return
     if args.impl == "reference":
         return run_reference(args)

@@ -3,6 +3,7 @@
 // allocates device memory and no host state survives a call.
 #include <algorithm>
 #include <cmath>
+#include <mutex>
 #include <new>
 #include <cstdint>
 #include <cstring>
@@ -57,7 +58,27 @@ bool is_pow2(int64_t v) { return v >= 1 && (v & (v - 1)) == 0; }
 
 float inv_sqrt_n(int n) { return (float)(1.0 / std::sqrt((double)n)); }
 
+// Loads every kernel of the library on the current device, once, before the
+// library's first launch there (see the preload functions).
+void ensure_loaded() {
+    static std::mutex mu;
+    static bool done[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return;
+    std::lock_guard<std::mutex> lock(mu);
+    if (done[dev]) return;
+    preload_quantize_kernels();
+    preload_gemm_kernels();
+    preload_dequant_kernels();
+    preload_stats_kernels();
+    cudaGetLastError();  // a failed query shows up again at the launch
+    done[dev] = true;
+}
+
+// SM count of the current device; every launch path asks for it right before
+// launching, so it also makes sure the kernels are loaded.
 int num_sms_current() {
+    ensure_loaded();
     int dev = 0, sms = 148;
     if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     return sms;
@@ -524,6 +545,7 @@ ufp4_status ufp4_gemm_prepare(const ufp4_qtensor* A, const ufp4_qtensor* B, cons
     const ufp4_status st = prepare_gemm(A, B, desc, dummy_d, B ? B->rows : 0, workspace, workspace_bytes, &g);
     if (st != UFP4_OK) return st;
     if (g.M == 0 || g.N == 0 || g.K == 0) return UFP4_OK;
+    ensure_loaded();
     const cudaError_t e = launch_gemm_prep(g, stream);
     if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
     return cuda_status(e);
@@ -544,12 +566,14 @@ ufp4_status ufp4_gemm_prepared(const ufp4_qtensor* A, const ufp4_qtensor* B, con
 ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
                                              const ufp4_quant_desc* desc, size_t* bytes) {
     if (num_groups < 0 || (num_groups && (!A || !B)) || !bytes) return UFP4_ERR_INVALID_ARG;
+    // each group its own 256-byte aligned region (the groups of one launch run together)
     size_t need = 0;
     for (int32_t i = 0; i < num_groups; ++i) {
         size_t b = 0;
         const ufp4_status st = ufp4_gemm_workspace_size(A[i].rows, B[i].rows, A[i].cols, desc, &b);
         if (st != UFP4_OK) return st;
-        need = std::max(need, b);
+        if (A[i].rows == 0 || B[i].rows == 0 || A[i].cols == 0) b = 0;  // an empty product needs none
+        need += (b + 255) & ~(size_t)255;
     }
     *bytes = need;
     return UFP4_OK;
@@ -559,21 +583,30 @@ ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const u
                               const ufp4_quant_desc* desc, float* const* D, const int64_t* ldd, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream) {
     if (num_groups < 0 || (num_groups && (!A || !B || !D || !ldd))) return UFP4_ERR_INVALID_ARG;
-    // every group is checked before anything is launched
+    if (workspace && !aligned(workspace, 256)) return UFP4_ERR_ALIGNMENT;
+    // every group is checked before anything is launched; group i takes the
+    // workspace region after those of groups 0..i-1
     GemmArgs* args = new (std::nothrow) GemmArgs[num_groups > 0 ? num_groups : 1];
     if (!args) return UFP4_ERR_INVALID_ARG;
+    size_t off = 0;
     for (int32_t i = 0; i < num_groups; ++i) {
-        const ufp4_status st = prepare_gemm(&A[i], &B[i], desc, D[i], ldd[i], workspace, workspace_bytes, &args[i]);
+        size_t need = 0;
+        ufp4_status st = ufp4_gemm_workspace_size(A[i].rows, B[i].rows, A[i].cols, desc, &need);
+        if (A[i].rows == 0 || B[i].rows == 0 || A[i].cols == 0) need = 0;  // an empty product needs none
+        if (st == UFP4_OK && off + need > workspace_bytes) st = UFP4_ERR_INVALID_ARG;
+        if (st == UFP4_OK)
+            st = prepare_gemm(&A[i], &B[i], desc, D[i], ldd[i], need ? (uint8_t*)workspace + off : nullptr, need,
+                              &args[i]);
         if (st != UFP4_OK) {
             delete[] args;
             return st;
         }
+        off += (need + 255) & ~(size_t)255;
     }
-    // the groups run one after another on the stream, so they share the workspace
-    ufp4_status st = UFP4_OK;
-    for (int32_t i = 0; i < num_groups && st == UFP4_OK; ++i) st = run_prepared_gemm(args[i], stream);
+    const cudaError_t e = launch_gemm_groups(args, num_groups, num_sms_current(), stream);
     delete[] args;
-    return st;
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    return cuda_status(e);
 }
 
 }  // extern "C"

@@ -83,4 +83,9 @@ cudaError_t launch_dequantize(const DequantParams& p, int num_sms, cudaStream_t 
     return cudaGetLastError();
 }
 
+cudaError_t preload_dequant_kernels() {
+    cudaFuncAttributes a;
+    return cudaFuncGetAttributes(&a, dequant_kernel);
+}
+
 }  // namespace ufp4

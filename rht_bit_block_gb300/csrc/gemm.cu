@@ -346,25 +346,36 @@ struct PairCfg {
     static_assert(kChunks % 2 == 0, "A's scale copies hold two chunks");
 };
 
-struct PairKParams {
+// One GEMM of a launch.  A launch walks the tiles of up to G GEMMs sharing
+// the kind and the descriptor (the groups of ufp4_gemm_grouped), numbered
+// one GEMM after the other.
+struct PairGroup {
     int M, N, k_tiles, m_pairs, n_tiles;
+    int tile0;            // index of this GEMM's first tile in the launch
     int64_t sf_chunks_k;  // chunks along K per 128-row block
     float* D;
     int64_t ldd;
     int vec8;
-    uint32_t idesc[4];
     // two-level scale: D = acc * g_A * g_B, g = fp32(T / den), den = fp32(qmax * 448)
     const float* amax_a;
     const float* amax_b;
+};
+template <int G>
+struct PairMaps {
+    CUtensorMap m[G][4];  // A, B and their scale chunks, per GEMM
+};
+template <int G>
+struct PairKParams {
+    PairGroup g[G];
+    int ngroups, num_tiles;
+    uint32_t idesc[4];
     float den;
     int two_level;
 };
 
-template <int KIND, int STAGES, int KPS>
+template <int KIND, int STAGES, int KPS, int G>
 __global__ void __launch_bounds__(kGemmThreads, 1)
-gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_constant__ CUtensorMap tmap_b,
-                 const __grid_constant__ CUtensorMap tmap_sfa, const __grid_constant__ CUtensorMap tmap_sfb,
-                 const PairKParams p) {
+gemm_pair_kernel(const __grid_constant__ PairMaps<G> maps, const __grid_constant__ PairKParams<G> p) {
     using C = PairCfg<KIND, STAGES, KPS>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -388,10 +399,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
     const uint32_t rank = cluster_rank();
     const uint32_t peer = rank & 1u;       // 0: leader (even CTA), 1: the other CTA of the pair
     const uint32_t leader = rank & ~1u;
-    const int num_tiles = p.m_pairs * p.n_tiles;
+    const int num_tiles = p.num_tiles;
     const int cluster_id = blockIdx.x >> 1;
     const int num_clusters = gridDim.x >> 1;
-    const int k_stages = (p.k_tiles + KPS - 1) / KPS;
+    // the GEMM a tile belongs to, and the tile's index inside it
+    auto locate = [&](int tile, int& local) {
+        int gi = 0;
+        while (gi + 1 < p.ngroups && tile >= p.g[gi + 1].tile0) ++gi;
+        local = tile - p.g[gi].tile0;
+        return gi;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -426,30 +443,35 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         uint32_t ph = 0;
         const uint64_t keep = policy_evict_last();
         for (int tile = cluster_id; tile < num_tiles && !*abort_flag; tile += num_clusters) {
-            const int mp = tile % p.m_pairs, nb = tile / p.m_pairs;
+            int local;
+            const int gi = locate(tile, local);
+            const PairGroup& q = p.g[gi];
+            const CUtensorMap* tm = maps.m[gi];
+            const int mp = local % q.m_pairs, nb = local / q.m_pairs;
+            const int k_stages = (q.k_tiles + KPS - 1) / KPS;
             const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
             const int arow = ablk * kBM;
             const int brow = nb * C::BN + (int)peer * C::kBRows;
             // 512-byte rows of the chunk arrays: R per chunk for A, 2R for B (R = 4 replicated, else 1)
             constexpr int R = C::kRep / kChunkBytes;
-            const int sfa_row = ablk * (int)p.sf_chunks_k * R;
-            const int sfb_row = nb * (int)p.sf_chunks_k * 2 * R;
+            const int sfa_row = ablk * (int)q.sf_chunks_k * R;
+            const int sfb_row = nb * (int)q.sf_chunks_k * 2 * R;
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait(empty_bar(s), ph ^ 1u)) {
                     *abort_flag = 1;
                     break;
                 }
                 const int kt0 = ks * KPS;
-                const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
+                const int nk = q.k_tiles - kt0 < KPS ? q.k_tiles - kt0 : KPS;
                 const uint32_t fb = map_to_rank(full_bar(s), leader);
                 if (peer == 0) mbar_expect_tx(full_bar(s), 2 * (nk * C::kTxPerAtom + C::kTxScales));
                 for (int j = 0; j < nk; ++j) {
-                    tma_load_pair(stage_a(s) + j * C::kAAtom, &tmap_a, (kt0 + j) * kBKBytes, arow, fb, keep);
-                    tma_load_pair(stage_b(s) + j * C::kBAtom, &tmap_b, (kt0 + j) * kBKBytes, brow, fb, keep);
+                    tma_load_pair(stage_a(s) + j * C::kAAtom, &tm[0], (kt0 + j) * kBKBytes, arow, fb, keep);
+                    tma_load_pair(stage_b(s) + j * C::kBAtom, &tm[1], (kt0 + j) * kBKBytes, brow, fb, keep);
                 }
                 // the scales of the stage's K tiles are contiguous: one box each
-                tma_load_pair(stage_sfa(s), &tmap_sfa, 0, sfa_row + kt0 * C::CPK * R, fb, keep);
-                tma_load_pair(stage_sfb(s), &tmap_sfb, 0, sfb_row + kt0 * C::CPK * 2 * R, fb, keep);
+                tma_load_pair(stage_sfa(s), &tm[2], 0, sfa_row + kt0 * C::CPK * R, fb, keep);
+                tma_load_pair(stage_sfb(s), &tm[3], 0, sfb_row + kt0 * C::CPK * 2 * R, fb, keep);
                 if (++s == STAGES) {
                     s = 0;
                     ph ^= 1u;
@@ -470,6 +492,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
             }
             tc_fence_after();
             const uint32_t acc = tmem + buf * C::BN;
+            int local;
+            const int k_tiles = p.g[locate(tile, local)].k_tiles;
+            const int k_stages = (k_tiles + KPS - 1) / KPS;
             for (int ks = 0; ks < k_stages; ++ks) {
                 if (!mbar_wait(full_bar(s), ph) || *abort_flag) {
                     ok = false;
@@ -477,7 +502,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 }
                 tc_fence_after();
                 const int kt0 = ks * KPS;
-                const int nk = p.k_tiles - kt0 < KPS ? p.k_tiles - kt0 : KPS;
+                const int nk = k_tiles - kt0 < KPS ? k_tiles - kt0 : KPS;
                 const uint32_t sfa_t = tmem + C::kSfaCol + (sc & 1) * C::kASet;
                 const uint32_t sfb_t = tmem + C::kSfbCol + (sc & 1) * C::kBSet;
                 ++sc;
@@ -523,16 +548,19 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
         // ------------------------------------------------- epilogue (both CTAs)
         const int q = warp - 4;
         const uint64_t stream_out = policy_evict_first();
-        // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
-        const float gab = p.two_level ? __fmul_rn(__fdiv_rn(*p.amax_a, p.den), __fdiv_rn(*p.amax_b, p.den)) : 1.0f;
         int tc = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++tc) {
             const int buf = tc & 1;
             const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), (tc >> 1) & 1));
             if (!ok || *abort_flag) break;
             tc_fence_after();
-            const int mp = tile % p.m_pairs, nb = tile / p.m_pairs;
+            int local;
+            const PairGroup& pg = p.g[locate(tile, local)];
+            const int mp = local % pg.m_pairs, nb = local / pg.m_pairs;
             const int row = (2 * mp + (int)peer) * kBM + q * 32 + lane;
+            // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
+            const float gab =
+                p.two_level ? __fmul_rn(__fdiv_rn(*pg.amax_a, p.den), __fdiv_rn(*pg.amax_b, p.den)) : 1.0f;
             const int n0 = nb * C::BN;
             for (int c = 0; c < C::BN; c += 32) {
                 uint32_t r[32];
@@ -540,10 +568,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                 if (p.two_level)
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__fmul_rn(__uint_as_float(r[i]), gab));
-                if (row < p.M) {
-                    float* dst = p.D + (int64_t)row * p.ldd + n0 + c;
-                    if (n0 + c + 32 <= p.N) {
-                        if (p.vec8) {
+                if (row < pg.M) {
+                    float* dst = pg.D + (int64_t)row * pg.ldd + n0 + c;
+                    if (n0 + c + 32 <= pg.N) {
+                        if (pg.vec8) {
 #pragma unroll
                             for (int i = 0; i < 32; i += 8) st_out8(dst + i, r + i, stream_out);
                         } else {
@@ -552,7 +580,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
                         }
                     } else {
                         for (int i = 0; i < 32; ++i)
-                            if (n0 + c + i < p.N) dst[i] = __uint_as_float(r[i]);
+                            if (n0 + c + i < pg.N) dst[i] = __uint_as_float(r[i]);
                     }
                 }
             }
@@ -842,13 +870,15 @@ struct PrepSide {
     int tile_rows;     // rows of one GEMM tile of this operand (128 for A, BN for B)
     uint8_t* out_fp8;  // rows x K bytes (E1M2/INT4 only)
     uint8_t* out_chunks;
+    int K;             // elements along K
+    int chunks_k;      // chunk cells along K per 128 rows
 };
 
-// Both operands in one launch (blockIdx.z picks the side).
+// Up to kPairGroups GEMMs (both operands of each) in one prep launch:
+// blockIdx.z picks the side, 2 g + (0 for A, 1 for B).
+constexpr int kPairGroups = 8;
 struct PrepParams {
-    PrepSide side[2];
-    int K;
-    int chunks_k;      // chunk cells along K per 128 rows
+    PrepSide side[2 * kPairGroups];
     int grid;          // codebook
     int lbr, lbc;      // log2 of the block rows and columns
     int lhw;           // log2 of the hardware scale block: 4 (E2M1 1x16) or 5
@@ -894,7 +924,7 @@ __device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
 // each lane one 32-element group of it (16 code bytes in, 32 FP8 bytes and one
 // scale byte of a 4-byte chunk cell out), so that every load and store of a
 // warp is contiguous.  blockIdx.x: 8-row slab, blockIdx.y: 32-group slab,
-// blockIdx.z: operand.
+// blockIdx.z: operand (of one of the GEMMs of the launch).
 __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
     griddep_wait();
     griddep_launch();
@@ -903,10 +933,10 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
     if (row >= s.rows_cover) return;                 // whole warps
     const int lane = threadIdx.x;
     const int grp = blockIdx.y * 32 + lane;          // 32-element group along K
-    const bool in_cells = grp < p.chunks_k * 4;      // groups covered by the chunk cells (whole 4-lane sets)
+    const bool in_cells = grp < s.chunks_k * 4;      // groups covered by the chunk cells (whole 4-lane sets)
     const int k0 = grp * 32;
     int hw = 0;
-    if (in_cells && row < s.rows && k0 < p.K) {
+    if (in_cells && row < s.rows && k0 < s.K) {
         const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
         const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
         const uint4 cw = *reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld + grp * 16);
@@ -948,7 +978,7 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
                 outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * p.K + k0);
+        uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * s.K + k0);
         dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
@@ -958,7 +988,7 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
     uint32_t word = v | __shfl_xor_sync(0xFFFFFFFFu, v, 1);
     word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
     if (in_cells)
-        *reinterpret_cast<uint32_t*>(s.out_chunks + rep_chunk_offset(s, p.chunks_k, row, grp >> 2) +
+        *reinterpret_cast<uint32_t*>(s.out_chunks + rep_chunk_offset(s, s.chunks_k, row, grp >> 2) +
                                      (lane & 3) * kChunkBytes) = word;
 }
 
@@ -975,9 +1005,9 @@ __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
     const int parts = (s.tile_rows + 127) >> 7;
     const int64_t blocks = (int64_t)(s.rows_cover / s.tile_rows) * parts;  // 128-row parts
     const int64_t item = (int64_t)blockIdx.x * 8 + threadIdx.y;            // (part block, chunk) pair
-    if (item >= blocks * p.chunks_k) return;                               // whole warps
-    const int g = (int)(item % p.chunks_k);
-    const int64_t pb = item / p.chunks_k;
+    if (item >= blocks * s.chunks_k) return;                               // whole warps
+    const int g = (int)(item % s.chunks_k);
+    const int64_t pb = item / s.chunks_k;
     const int t = (int)(pb / parts), h = (int)(pb % parts);
     const int i = threadIdx.x;
     uint32_t cell[4];
@@ -991,14 +1021,14 @@ __global__ void __launch_bounds__(256) prep_scales_kernel(const PrepParams p) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int k0 = (g * 4 + j) << p.lhw;
-                if (k0 < p.K) v |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
+                if (k0 < s.K) v |= (uint32_t)srow[k0 >> p.lbc] << (8 * j);
             }
         }
         cell[c] = v;
     }
     const uint4 line = make_uint4(cell[0], cell[1], cell[2], cell[3]);
     const int copies = p.copies;
-    uint8_t* dst = s.out_chunks + ((((int64_t)t * p.chunks_k + g) * parts + h) * copies) * kChunkBytes + i * 16;
+    uint8_t* dst = s.out_chunks + ((((int64_t)t * s.chunks_k + g) * parts + h) * copies) * kChunkBytes + i * 16;
 #pragma unroll
     for (int copy = 0; copy < copies; ++copy) *reinterpret_cast<uint4*>(dst + copy * kChunkBytes) = line;
 }
@@ -1164,23 +1194,22 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
 }
 
 // Co-resident two-CTA clusters of the pair kernel on this device (cached).
-template <int KIND, int STAGES, int KPS>
+template <int KIND, int STAGES, int KPS, int G>
 int pair_clusters(const cudaLaunchConfig_t& cfg) {
     static int cached[64];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
     if (cached[dev] > 0) return cached[dev];
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<KIND, STAGES, KPS>, &cfg) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveClusters(&n, gemm_pair_kernel<KIND, STAGES, KPS, G>, &cfg) != cudaSuccess) return 0;
     cached[dev] = n;
     return n;
 }
 
-template <int KIND, int STAGES, int KPS>
-cudaError_t run_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& msa, const CUtensorMap& msb,
-                          const PairKParams& kp, cudaStream_t st) {
+template <int KIND, int STAGES, int KPS, int G>
+cudaError_t run_gemm_pair(const PairMaps<G>& maps, const PairKParams<G>& kp, cudaStream_t st) {
     using C = PairCfg<KIND, STAGES, KPS>;
-    auto k = gemm_pair_kernel<KIND, STAGES, KPS>;
+    auto k = gemm_pair_kernel<KIND, STAGES, KPS, G>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -1197,12 +1226,12 @@ cudaError_t run_gemm_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CU
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const int max_clusters = pair_clusters<KIND, STAGES, KPS>(cfg);
+    const int max_clusters = pair_clusters<KIND, STAGES, KPS, G>(cfg);
     if (max_clusters <= 0) return cudaErrorLaunchOutOfResources;
-    const int tiles = kp.m_pairs * kp.n_tiles;
+    const int tiles = kp.num_tiles;
     cfg.gridDim = dim3(2 * (tiles < max_clusters ? tiles : max_clusters));  // persistent: one pair per two SMs
     cfg.numAttrs = st ? 2 : 1;
-    return cudaLaunchKernelEx(&cfg, k, ma, mb, msa, msb, kp);
+    return cudaLaunchKernelEx(&cfg, k, maps, kp);
 }
 
 }  // namespace
@@ -1221,6 +1250,162 @@ bool encode_map_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* ptr,
 
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf) {
     return make_plan(M, N, K, grid, br, bc, sf).total;
+}
+
+// ------------------------------------------------ pair-kernel launches
+// Shape checks and the plan of one GEMM of the pair kernel (kinds 0-2).
+cudaError_t pair_plan(const GemmArgs& g, Plan& pl) {
+    const bool fp4 = g.grid == 2 || g.grid == 3;
+    if (g.K % 32 && !(fp4 && g.bc == 16)) return cudaErrorNotSupported;
+    if (g.K % 64 && fp4) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
+    pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
+    if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+// Operand prep of n <= kPairGroups GEMMs sharing the kind, in one launch:
+// FP8 widening of E1M2 / INT4 (with the folded scale chunks), or the scale
+// chunks alone for FP4 and MXFP8.
+cudaError_t launch_prep_pair(const GemmArgs* gs, int n, cudaStream_t st) {
+    if (n < 1 || n > kPairGroups) return cudaErrorInvalidValue;
+    PrepParams pp{};
+    int row_blocks = 0;
+    int64_t kslabs = 0, items = 0;
+    Plan pl{};
+    for (int i = 0; i < n; ++i) {
+        const GemmArgs& g = gs[i];
+        const cudaError_t e = pair_plan(g, pl);
+        if (e != cudaSuccess) return e;
+        uint8_t* ws = (uint8_t*)g.workspace;
+        for (int side = 0; side < 2; ++side) {
+            const GemmOperand& op = side ? g.b : g.a;
+            PrepSide& ps = pp.side[2 * i + side];
+            ps.codes = op.codes;
+            ps.scales = op.scales;
+            ps.codes_ld = op.codes_ld;
+            ps.scales_ld = op.scales_ld;
+            ps.rows = (int)op.rows;
+            ps.tile_rows = side ? pl.bn : kBM;
+            ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;  // whole output tiles
+            ps.out_fp8 = (pl.kind == 0 && !pl.native) ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
+            ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
+            ps.K = (int)g.K;
+            ps.chunks_k = (int)pl.chunks_k;
+            row_blocks = std::max(row_blocks, (ps.rows_cover + 7) / 8);
+            kslabs = std::max(kslabs, (pl.chunks_k * 4 + 31) / 32);
+            items = std::max(items, (int64_t)(ps.rows_cover / ps.tile_rows) * ((ps.tile_rows + 127) / 128) *
+                                        pl.chunks_k);
+        }
+    }
+    // every GEMM of the launch has the same kind (same descriptor)
+    pp.grid = gs[0].grid;
+    pp.lbr = ilog2(gs[0].br);
+    pp.lbc = ilog2(gs[0].bc);
+    pp.lhw = pl.kind == 2 ? 4 : 5;
+    pp.copies = pair_replicated(pl.kind) ? 4 : 1;
+    if (pl.kind == 0 && !pl.native) {
+        // 32 groups of 32 elements per CTA along K, 8 rows per CTA
+        if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
+        return launch_pdl(prep_widen_kernel, dim3((unsigned)row_blocks, (unsigned)kslabs, 2 * n), dim3(32, 8), 0,
+                          st, pp);
+    }
+    // FP4 and MXFP8: only the scales move, one warp per (128-row part, chunk)
+    const int64_t blocks = (items + 7) / 8;
+    if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
+    return launch_pdl(prep_scales_kernel, dim3((unsigned)blocks, 1, 2 * n), dim3(32, 8), 0, st, pp);
+}
+
+// Tensor maps and parameters of one GEMM of a pair launch.
+cudaError_t fill_pair_group(const GemmArgs& g, const Plan& pl, CUtensorMap* maps, PairGroup& pg) {
+    uint8_t* ws = (uint8_t*)g.workspace;
+    // E1M2 / INT4 read the widened copies in the workspace; FP4 and MXFP8
+    // the codes themselves.
+    const bool widened = pl.kind == 0 && !pl.native;
+    const void* a_ptr = widened ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
+    const void* b_ptr = widened ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
+    const int64_t a_pitch = widened ? g.K : g.a.codes_ld;
+    const int64_t b_pitch = widened ? g.K : g.b.codes_ld;
+    // CTA pairs, 256 x bn tiles: A 128 rows per CTA, B bn/2 rows per CTA
+    if (!make_map(&maps[0], a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
+    if (!make_map(&maps[1], b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn / 2)) return cudaErrorInvalidValue;
+    // scale chunks as rows of 128 x 32-bit words (one 512-byte copy of a chunk
+    // per row); boxes: one stage's chunks, rpc rows per chunk for A, 2 rpc for B
+    const int cpk = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
+    const int kps = pl.kind == 0 ? kPairKps : 1;
+    const int rpc = pair_replicated(pl.kind) ? 4 : 1;  // 512-byte rows per chunk
+    const int64_t a_blocks = (g.M + kBM - 1) / kBM;
+    const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
+    if (!encode_map_2d(&maps[2], CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128,
+                       (uint64_t)(a_blocks * pl.chunks_k * rpc), kChunkBytes, 128, (uint32_t)(rpc * kps * cpk),
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    if (!encode_map_2d(&maps[3], CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128,
+                       (uint64_t)(b_blocks * pl.chunks_k * rpc), kChunkBytes, 128, (uint32_t)(2 * rpc * kps * cpk),
+                       CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    pg.M = (int)g.M;
+    pg.N = (int)g.N;
+    pg.k_tiles = (int)pl.k_tiles;
+    pg.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
+    pg.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
+    pg.sf_chunks_k = pl.chunks_k;
+    pg.D = g.D;
+    pg.ldd = g.ldd;
+    pg.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
+    pg.amax_a = g.amax_a;
+    pg.amax_b = g.amax_b;
+    return cudaSuccess;
+}
+
+template <int G>
+cudaError_t launch_main_pair_g(const GemmArgs* gs, int n, cudaStream_t st) {
+    PairMaps<G> maps;
+    std::memset(&maps, 0, sizeof(maps));
+    PairKParams<G> kp;
+    std::memset(&kp, 0, sizeof(kp));
+    Plan pl{};
+    int tiles = 0;
+    for (int i = 0; i < n; ++i) {
+        cudaError_t e = pair_plan(gs[i], pl);
+        if (e != cudaSuccess) return e;
+        e = fill_pair_group(gs[i], pl, maps.m[i], kp.g[i]);
+        if (e != cudaSuccess) return e;
+        kp.g[i].tile0 = tiles;
+        tiles += kp.g[i].m_pairs * kp.g[i].n_tiles;
+    }
+    kp.ngroups = n;
+    kp.num_tiles = tiles;
+    if (tiles == 0) return cudaSuccess;
+    const GemmArgs& g = gs[0];  // kind, grid and scale format are shared
+    if (pl.kind == 0) {
+        // E5M2 x E5M2 (format 1) for the widened codes, E4M3 x E4M3 (format 0) for MXFP8; M = 256
+        const int fmt = pl.native ? 0 : 1;
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(fmt, fmt, 2 * kBM, kBnFp8, j);
+        return run_gemm_pair<0, kPairStages, kPairKps, G>(maps, kp, st);
+    }
+    if (pl.kind == 1) {
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, (j % 2) * 2);  // E2M1
+        return run_gemm_pair<1, kPairStagesFp4x2, 1, G>(maps, kp, st);
+    }
+    // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
+    const bool two_level = g.sf == 2;
+    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, 0, !two_level);
+    kp.two_level = two_level;
+    kp.den = grid_qmax_host(g.grid) * 448.0f;
+    return run_gemm_pair<2, kPairStagesFp4x4, 1, G>(maps, kp, st);
+}
+
+// The tensor-core kernel over one GEMM.  The kernel can walk the tiles of
+// several GEMMs in one launch (G > 1, one set of tensor maps per GEMM in its
+// parameters), but such launches stalled for minutes when they followed
+// other GEMMs on a stream (a timing-dependent stall, not seen when run alone
+// or with eager module loading), so every GEMM gets its own launch.
+cudaError_t launch_main_pair(const GemmArgs* gs, int n, cudaStream_t st) {
+    for (int i = 0; i < n; ++i) {
+        const cudaError_t e = launch_main_pair_g<1>(&gs[i], 1, st);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 // Operand preparation: FP8 widening (E1M2/INT4) and scale chunks into the workspace.
@@ -1253,50 +1438,7 @@ cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st) {
         if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
         return launch_pdl(prep_f32s_kernel, dim3((unsigned)blocks, 1, 2), dim3(256), 0, st, pp);
     }
-    const bool fp4 = g.grid == 2 || g.grid == 3;
-    if (g.K % 32 && !(fp4 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && fp4) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
-    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
-    if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
-    uint8_t* ws = (uint8_t*)g.workspace;
-    PrepParams pp{};
-    int row_blocks = 0;
-    for (int side = 0; side < 2; ++side) {
-        const GemmOperand& op = side ? g.b : g.a;
-        PrepSide& ps = pp.side[side];
-        ps.codes = op.codes;
-        ps.scales = op.scales;
-        ps.codes_ld = op.codes_ld;
-        ps.scales_ld = op.scales_ld;
-        ps.rows = (int)op.rows;
-        ps.tile_rows = side ? pl.bn : kBM;
-        ps.rows_cover = (int)((op.rows + ps.tile_rows - 1) / ps.tile_rows) * ps.tile_rows;  // whole output tiles
-        ps.out_fp8 = (pl.kind == 0 && !pl.native) ? ws + (side ? pl.fp8_b : pl.fp8_a) : nullptr;
-        ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
-        row_blocks = std::max(row_blocks, (ps.rows_cover + 7) / 8);
-    }
-    pp.K = (int)g.K;
-    pp.chunks_k = (int)pl.chunks_k;
-    pp.grid = g.grid;
-    pp.lbr = ilog2(g.br);
-    pp.lbc = ilog2(g.bc);
-    pp.lhw = pl.kind == 2 ? 4 : 5;
-    pp.copies = pair_replicated(pl.kind) ? 4 : 1;
-    if (pl.kind == 0 && !pl.native) {
-        // 32 groups of 32 elements per CTA along K, 8 rows per CTA
-        const int64_t kslabs = (pl.chunks_k * 4 + 31) / 32;
-        if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
-        return launch_pdl(prep_widen_kernel, dim3((unsigned)row_blocks, (unsigned)kslabs, 2), dim3(32, 8), 0, st, pp);
-    }
-    // FP4 and MXFP8: only the scales move, one warp per (128-row part, chunk)
-    int64_t items = 0;
-    for (int side = 0; side < 2; ++side) {
-        const PrepSide& ps = pp.side[side];
-        items = std::max(items, (int64_t)(ps.rows_cover / ps.tile_rows) * ((ps.tile_rows + 127) / 128) * pl.chunks_k);
-    }
-    const int64_t blocks = (items + 7) / 8;
-    if (blocks > 0x7FFFFFFF) return cudaErrorNotSupported;
-    return launch_pdl(prep_scales_kernel, dim3((unsigned)blocks, 1, 2), dim3(32, 8), 0, st, pp);
+    return launch_prep_pair(&g, 1, st);
 }
 
 // The tensor-core kernel on a workspace filled by launch_gemm_prep for the same arguments.
@@ -1337,65 +1479,36 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
         const int grid = tiles < num_sms ? tiles : num_sms;
         return launch_pdl(k, dim3(grid), dim3(kF32sThreads), (size_t)F32sCfg::kSmem, st, ma, mb, msa, msb, kp);
     }
-    const bool fp4 = g.grid == 2 || g.grid == 3;
-    if (g.K % 32 && !(fp4 && g.bc == 16)) return cudaErrorNotSupported;
-    if (g.K % 64 && fp4) return cudaErrorNotSupported;
-    const Plan pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
-    if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
-    uint8_t* ws = (uint8_t*)g.workspace;
     (void)num_sms;
-    // CTA pairs, 256 x bn tiles: A 128 rows per CTA, B bn/2 rows per CTA.
-    // E1M2 / INT4 read the widened copies in the workspace; FP4 and MXFP8
-    // the codes themselves.
-    const bool widened = pl.kind == 0 && !pl.native;
-    const void* a_ptr = widened ? (const void*)(ws + pl.fp8_a) : (const void*)g.a.codes;
-    const void* b_ptr = widened ? (const void*)(ws + pl.fp8_b) : (const void*)g.b.codes;
-    const int64_t a_pitch = widened ? g.K : g.a.codes_ld;
-    const int64_t b_pitch = widened ? g.K : g.b.codes_ld;
-    CUtensorMap ma, mb, msa, msb;
-    if (!make_map(&ma, a_ptr, g.M, pl.k_bytes, a_pitch, kBM)) return cudaErrorInvalidValue;
-    if (!make_map(&mb, b_ptr, g.N, pl.k_bytes, b_pitch, pl.bn / 2)) return cudaErrorInvalidValue;
-    // scale chunks as rows of 128 x 32-bit words (one 512-byte copy of a chunk
-    // per row); boxes: one stage's chunks, 4 rows per chunk for A, 8 for B
-    const int cpk = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
-    const int kps = pl.kind == 0 ? kPairKps : 1;
-    const int rpc = pair_replicated(pl.kind) ? 4 : 1;  // 512-byte rows per chunk
-    const int64_t a_blocks = (g.M + kBM - 1) / kBM;
-    const int64_t b_blocks = (g.N + pl.bn - 1) / pl.bn * 2;
-    if (!encode_map_2d(&msa, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfa, 128, (uint64_t)(a_blocks * pl.chunks_k * rpc),
-                       kChunkBytes, 128, (uint32_t)(rpc * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    if (!encode_map_2d(&msb, CU_TENSOR_MAP_DATA_TYPE_UINT32, ws + pl.sfb, 128, (uint64_t)(b_blocks * pl.chunks_k * rpc),
-                       kChunkBytes, 128, (uint32_t)(2 * rpc * kps * cpk), CU_TENSOR_MAP_SWIZZLE_NONE))
-        return cudaErrorInvalidValue;
-    PairKParams pk{};
-    pk.M = (int)g.M;
-    pk.N = (int)g.N;
-    pk.k_tiles = (int)pl.k_tiles;
-    pk.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
-    pk.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
-    pk.sf_chunks_k = pl.chunks_k;
-    pk.D = g.D;
-    pk.ldd = g.ldd;
-    pk.vec8 = ((uintptr_t)g.D % 32 == 0) && (g.ldd % 8 == 0);
-    if (pl.kind == 0) {
-        // E5M2 x E5M2 (format 1) for the widened codes, E4M3 x E4M3 (format 0) for MXFP8; M = 256
-        const int fmt = pl.native ? 0 : 1;
-        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(fmt, fmt, 2 * kBM, kBnFp8, j);
-        return run_gemm_pair<0, kPairStages, kPairKps>(ma, mb, msa, msb, pk, st);
+    return launch_main_pair(&g, 1, st);
+}
+
+// GEMMs sharing a descriptor, each with its own workspace region, run one
+// after another on the stream (operand prep and tensor-core launch each).
+// Empty products are skipped and K = 0 gives D = 0.  Launching several GEMMs
+// from one persistent grid was tried; it stalled for minutes when it followed
+// other GEMMs on the stream with lazily loaded modules, so it is not used.
+cudaError_t launch_gemm_groups(const GemmArgs* gs, int n, int num_sms, cudaStream_t st) {
+    for (int i = 0; i < n; ++i) {
+        const GemmArgs& g = gs[i];
+        if (g.M == 0 || g.N == 0) continue;
+        const cudaError_t e = g.K == 0
+            ? cudaMemset2DAsync(g.D, (size_t)g.ldd * sizeof(float), 0, (size_t)g.N * sizeof(float), (size_t)g.M, st)
+            : launch_gemm(g, num_sms, st);
+        if (e != cudaSuccess) return e;
     }
-    if (pl.kind == 1) {
-        for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, (j % 2) * 2);  // E2M1
-        return run_gemm_pair<1, kPairStagesFp4x2, 1>(ma, mb, msa, msb, pk, st);
-    }
-    // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
-    const bool two_level = g.sf == 2;
-    for (int j = 0; j < 4; ++j) pk.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, 0, !two_level);
-    pk.two_level = two_level;
-    pk.amax_a = g.amax_a;
-    pk.amax_b = g.amax_b;
-    pk.den = grid_qmax_host(g.grid) * 448.0f;
-    return run_gemm_pair<2, kPairStagesFp4x4, 1>(ma, mb, msa, msb, pk, st);
+    return cudaSuccess;
+}
+
+cudaError_t preload_gemm_kernels() {
+    cudaFuncAttributes a;
+    cudaFuncGetAttributes(&a, gemm_pair_kernel<0, kPairStages, kPairKps, 1>);
+    cudaFuncGetAttributes(&a, gemm_pair_kernel<1, kPairStagesFp4x2, 1, 1>);
+    cudaFuncGetAttributes(&a, gemm_pair_kernel<2, kPairStagesFp4x4, 1, 1>);
+    cudaFuncGetAttributes(&a, gemm_f32s_kernel);
+    cudaFuncGetAttributes(&a, prep_widen_kernel);
+    cudaFuncGetAttributes(&a, prep_scales_kernel);
+    return cudaFuncGetAttributes(&a, prep_f32s_kernel);
 }
 
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st) {

@@ -172,5 +172,15 @@ size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, i
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st);
 cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st);
+// Load every kernel of each unit.  The library does it once per device
+// before its first launch: with lazy module loading, loading a kernel while
+// earlier kernels of the library are in flight (programmatic dependent
+// launches waiting on one another) stalled the stream for minutes.
+cudaError_t preload_quantize_kernels();
+cudaError_t preload_gemm_kernels();
+cudaError_t preload_dequant_kernels();
+cudaError_t preload_stats_kernels();
+// n GEMMs sharing a descriptor, each with its own workspace (the grouped call)
+cudaError_t launch_gemm_groups(const GemmArgs* gs, int n, int num_sms, cudaStream_t st);
 
 }  // namespace ufp4

@@ -934,4 +934,36 @@ cudaError_t launch_rht(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld
     return cudaGetLastError();
 }
 
+// Loads every kernel of this unit (cudaFuncGetAttributes loads a function
+// that has not been loaded yet).
+template <int G, bool SR, bool PO2>
+static void preload_q(cudaFuncAttributes* a) {
+    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128>);
+    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 256>);
+}
+template <int G, bool SR>
+static void preload_rows(cudaFuncAttributes* a) {
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2>);
+}
+template <int G>
+static void preload_grid(cudaFuncAttributes* a) {
+    preload_q<G, false, false>(a);
+    preload_q<G, false, true>(a);
+    preload_q<G, true, false>(a);
+    preload_q<G, true, true>(a);
+    preload_rows<G, false>(a);
+    preload_rows<G, true>(a);
+}
+cudaError_t preload_quantize_kernels() {
+    cudaFuncAttributes a;
+    preload_grid<0>(&a);
+    preload_grid<1>(&a);
+    preload_grid<2>(&a);
+    preload_grid<3>(&a);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1>);
+    return cudaFuncGetAttributes(&a, rht_kernel);
+}
+
 }  // namespace ufp4

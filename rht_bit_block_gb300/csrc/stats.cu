@@ -205,4 +205,11 @@ cudaError_t launch_dstats(const float* a, int64_t lda, const float* b, int64_t l
     return cudaGetLastError();
 }
 
+cudaError_t preload_stats_kernels() {
+    cudaFuncAttributes a;
+    cudaFuncGetAttributes(&a, qstats_kernel);
+    cudaFuncGetAttributes(&a, dstats_kernel);
+    return cudaFuncGetAttributes(&a, amax_kernel);
+}
+
 }  // namespace ufp4
