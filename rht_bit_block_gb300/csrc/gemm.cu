@@ -845,8 +845,6 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 }
 
 // ------------------------------------------------------------- prep kernels
-// Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
-// elements.  One thread: one row, one 128-element K group (4 scale cells).
 __device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
     uint16_t r;
     asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
@@ -890,15 +888,7 @@ struct PrepParams {
 // (tile_rows rows) is stored four times, at
 // ((((t * chunks_k + g) * parts + h) * 4 + copy) * 512, with row w of the part
 // and scale cell byte j at (w % 32) * 16 + (w / 32) * 4 + j in each copy
-// (the tcgen05.cp 32x128b chunk layout).  Returns the offset of copy 0 for
-// this row.
-__device__ __forceinline__ int64_t rep_chunk_offset(const PrepSide& s, int chunks_k, int row, int g) {
-    const int parts = (s.tile_rows + 127) >> 7;
-    const int t = row / s.tile_rows;
-    const int rr = row - t * s.tile_rows;
-    const int h = rr >> 7, w = rr & 127;
-    return ((((int64_t)t * chunks_k + g) * parts + h) * 4) * kChunkBytes + (w & 31) * 16 + (w >> 5) * 4;
-}
+// (the tcgen05.cp 32x128b chunk layout).
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     uint32_t r;
@@ -906,90 +896,142 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return r;
 }
 
-// Four sign-magnitude codes (16 bits) -> four E5M2 bytes of k * 2^-d, d <= 14:
-// the magnitudes 0..7 index the E5M2 bytes of 0, 1, 2, ..., 7 (byte permute),
-// the shift subtracts d from the exponent field of the nonzero bytes, and the
-// sign goes to bit 7.  Exact: every k * 2^-d with |k| <= 7, d <= 14 is an E5M2
-// normal number.
-__device__ __forceinline__ uint32_t e5m2x4(uint32_t c16, uint32_t sub4) {
-    const uint32_t mag = c16 & 0x7777u;
-    const uint32_t v = prmt(0x42403C00u, 0x47464544u, mag);  // 0, 1.0, 2.0, 3.0 | 4.0, 5.0, 6.0, 7.0
-    const uint32_t nz = prmt(0xFFFFFF00u, 0xFFFFFFFFu, mag);  // 0xff where k != 0
-    const uint32_t sg = prmt(0x00008000u, 0u, (c16 >> 3) & 0x1111u);
-    return (v - (sub4 & nz)) | sg;
+// Eight sign-magnitude codes (one 32-bit word) -> eight E5M2 bytes of
+// k * 2^-d, d <= 14 (two words).  lo and hi hold the E5M2 bytes of 0, 1, ..., 7
+// with d already subtracted from the exponent field of the nonzero ones
+// (e5m2_tables); the magnitudes select from them and the sign bits select
+// 0x80 or 0 (byte permutes).  Exact: every k * 2^-d with |k| <= 7, d <= 14 is
+// an E5M2 normal number.
+__device__ __forceinline__ void e5m2x8(uint32_t w, uint32_t lo, uint32_t hi, uint32_t& o0, uint32_t& o1) {
+    const uint32_t mw = w & 0x77777777u;
+    const uint32_t sw = (w >> 3) & 0x11111111u;  // each nibble: its sign bit
+    o0 = prmt(lo, hi, mw) | prmt(0x00008000u, 0u, sw);
+    o1 = prmt(lo, hi, mw >> 16) | prmt(0x00008000u, 0u, sw >> 16);
+}
+
+// E5M2 bytes of 0, 1.0, 2.0, 3.0 (lo) and 4.0 .. 7.0 (hi), each nonzero one
+// scaled by 2^-d (d <= 14: every byte stays >= 4 d, so no borrow crosses bytes).
+__device__ __forceinline__ void e5m2_tables(int d, uint32_t& lo, uint32_t& hi) {
+    const uint32_t sub = (uint32_t)d * 0x04040404u;
+    lo = 0x42403C00u - (sub & 0xFFFFFF00u);
+    hi = 0x47464544u - sub;
 }
 
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
-// elements (replicated chunk layout above).  A CTA is 32 x 8 threads: each warp (threadIdx.y) owns one row,
-// each lane one 32-element group of it (16 code bytes in, 32 FP8 bytes and one
-// scale byte of a 4-byte chunk cell out), so that every load and store of a
-// warp is contiguous.  blockIdx.x: 8-row slab, blockIdx.y: 32-group slab,
+// elements (replicated chunk layout above).  A CTA is 32 x 8 threads and
+// covers, in one 128-row part of a GEMM tile, the rows w = 32 q + 2 j + e
+// (q = 0..3, e = 0..1; warp 2 q + e) for its j = blockIdx.x % 16: the rows
+// whose chunk cells make up two whole 16-byte lines of every chunk.  Each warp
+// owns its row, each lane two adjacent 32-element groups of it (32 code bytes
+// in, 64 FP8 bytes out, contiguous across the warp); the scale bytes are
+// gathered in shared memory and leave as whole 32-byte sectors, four copies
+// per chunk.  blockIdx.x: (part, j), blockIdx.y: 64-group slab along K,
 // blockIdx.z: operand (of one of the GEMMs of the launch).
 __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
+    __shared__ __align__(16) uint8_t cells[16][32];  // per chunk of the slab: lines 2 j and 2 j + 1
     griddep_wait();
     griddep_launch();
     const PrepSide& s = p.side[blockIdx.z];
-    const int row = blockIdx.x * 8 + threadIdx.y;
-    if (row >= s.rows_cover) return;                 // whole warps
-    const int lane = threadIdx.x;
-    const int grp = blockIdx.y * 32 + lane;          // 32-element group along K
-    const bool in_cells = grp < s.chunks_k * 4;      // groups covered by the chunk cells (whole 4-lane sets)
-    const int k0 = grp * 32;
-    int hw = 0;
-    if (in_cells && row < s.rows && k0 < s.K) {
-        const int step_log2 = p.grid == 0 ? -2 : 0;  // E1M2 levels are k/4, INT4 levels k
-        const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
-        const uint4 cw = *reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld + grp * 16);
-        const int e0 = srow[k0 >> p.lbc];
-        const int e1 = p.lbc == 4 ? srow[(k0 >> 4) + 1] : e0;
-        hw = max(max(e0, e1) + step_log2, 0);
-        const int d0 = hw - step_log2 - e0, d1 = hw - step_log2 - e1;  // >= 0
-        uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+    const int parts = (s.tile_rows + 127) >> 7;
+    const int part = blockIdx.x >> 4, jj = blockIdx.x & 15;
+    if (part >= (s.rows_cover / s.tile_rows) * parts) return;  // whole CTAs
+    const int t = part / parts, h = part - t * parts;
+    const int part_rows = min(128, s.tile_rows - h * 128);
+    const int y = threadIdx.y, lane = threadIdx.x;
+    const int w = 32 * (y >> 1) + 2 * jj + (y & 1);
+    const bool has_row = w < part_rows;            // rows past a 224-row tile's end do not exist
+    const int row = t * s.tile_rows + h * 128 + w;
+    const bool live = has_row && row < s.rows;     // rows up to rows_cover get zero cells
+    const int g0 = blockIdx.y * 64 + 2 * lane;     // groups g0, g0 + 1 along K
+    const int step_log2 = p.grid == 0 ? -2 : 0;    // E1M2 levels are k/4, INT4 levels k
+    const uint8_t* srow = s.scales + (int64_t)(row >> p.lbr) * s.scales_ld;
+    uint4 cw[2];
+    int e0[2] = {0, 0}, e1[2] = {0, 0};
+    bool ok[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        ok[q] = live && (g0 + q) * 32 < s.K;
+        cw[q] = make_uint4(0u, 0u, 0u, 0u);
+        if (ok[q]) cw[q] = *reinterpret_cast<const uint4*>(s.codes + (int64_t)row * s.codes_ld + (g0 + q) * 16);
+    }
+    // the scale bytes of both groups: one aligned word (1 x 16) or half word (1 x 32) where possible
+    const uintptr_t sa = reinterpret_cast<uintptr_t>(srow);
+    if (ok[1] && p.lbc == 4 && (sa & 3) == 0) {
+        const uint32_t v = *reinterpret_cast<const uint32_t*>(srow + 2 * g0);
+        e0[0] = v & 0xFF; e1[0] = (v >> 8) & 0xFF; e0[1] = (v >> 16) & 0xFF; e1[1] = v >> 24;
+    } else if (ok[1] && p.lbc == 5 && (sa & 1) == 0) {
+        const uint32_t v = *reinterpret_cast<const uint16_t*>(srow + g0);
+        e0[0] = e1[0] = v & 0xFF; e0[1] = e1[1] = v >> 8;
+    } else {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+            if (ok[q]) {
+                const int k0 = (g0 + q) * 32;
+                e0[q] = srow[k0 >> p.lbc];
+                e1[q] = p.lbc == 4 ? srow[(k0 >> 4) + 1] : e0[q];
+            }
+    }
+    int hw[2];
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+        hw[q] = ok[q] ? max(max(e0[q], e1[q]) + step_log2, 0) : 0;
+        if (!ok[q]) continue;
+        const int d0 = hw[q] - step_log2 - e0[q], d1 = hw[q] - step_log2 - e1[q];  // >= 0
+        uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
         if (p.grid == 1) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {  // two's complement -> sign-magnitude (no -8 code occurs)
-                const uint32_t w = words[q];
-                const uint32_t neg = (w >> 3) & 0x11111111u;
-                const uint32_t mag = ((w ^ (neg * 15u)) + neg) & 0x77777777u;
-                words[q] = mag | (neg << 3);
+            for (int k = 0; k < 4; ++k) {  // two's complement -> sign-magnitude (no -8 code occurs)
+                const uint32_t v = words[k];
+                const uint32_t neg = (v >> 3) & 0x11111111u;
+                const uint32_t mag = ((v ^ (neg * 15u)) + neg) & 0x77777777u;
+                words[k] = mag | (neg << 3);
             }
         }
         uint32_t outw[8];
         if (d0 <= 14 && d1 <= 14) {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t sub4 = (uint32_t)(4 * (q < 4 ? d0 : d1)) * 0x01010101u;
-                outw[q] = e5m2x4((words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu, sub4);
-            }
+            uint32_t lo0, hi0, lo1, hi1;
+            e5m2_tables(d0, lo0, hi0);
+            e5m2_tables(d1, lo1, hi1);
+            e5m2x8(words[0], lo0, hi0, outw[0], outw[1]);  // elements 0-15: the first 16-element block
+            e5m2x8(words[1], lo0, hi0, outw[2], outw[3]);
+            e5m2x8(words[2], lo1, hi1, outw[4], outw[5]);
+            e5m2x8(words[3], lo1, hi1, outw[6], outw[7]);
         } else {
             // shifts beyond E5M2's normal range: exact float path, rounding to
             // nearest only below E5M2's smallest subnormal
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const float mult = pow2f(-(q < 4 ? d0 : d1));
-                const uint32_t w = (words[q >> 1] >> (16 * (q & 1))) & 0xFFFFu;
-                float v[4];
+            for (int k = 0; k < 8; ++k) {
+                const float mult = pow2f(-(k < 4 ? d0 : d1));
+                const uint32_t v = (words[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
+                float f[4];
 #pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const uint32_t nib = (w >> (4 * t)) & 0xFu;
-                    const float k = (float)(int)(nib & 7u);
-                    v[t] = ((nib & 8u) ? -k : k) * mult;
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t nib = (v >> (4 * u)) & 0xFu;
+                    const float m = (float)(int)(nib & 7u);
+                    f[u] = ((nib & 8u) ? -m : m) * mult;
                 }
-                outw[q] = cvt_e5m2x2(v[1], v[0]) | (cvt_e5m2x2(v[3], v[2]) << 16);
+                outw[k] = cvt_e5m2x2(f[1], f[0]) | (cvt_e5m2x2(f[3], f[2]) << 16);
             }
         }
-        uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * s.K + k0);
+        uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * s.K + (g0 + q) * 32);
         dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
     }
-    // lanes 4c .. 4c+3 hold the four scale bytes of one chunk cell: gather
-    // the word, then lane 4c + r writes copy r of it
-    const uint32_t v = (uint32_t)hw << (8 * (lane & 3));
-    uint32_t word = v | __shfl_xor_sync(0xFFFFFFFFu, v, 1);
-    word |= __shfl_xor_sync(0xFFFFFFFFu, word, 2);
-    if (in_cells)
-        *reinterpret_cast<uint32_t*>(s.out_chunks + rep_chunk_offset(s, s.chunks_k, row, grp >> 2) +
-                                     (lane & 3) * kChunkBytes) = word;
+    // the cell of row w in chunk c: bytes (w % 32) * 16 + (w / 32) * 4 + (group % 4) of each copy;
+    // here line e = w % 2 of the CTA's two, bytes (w / 32) * 4 + 2 (lane % 2) + {0, 1}
+    *reinterpret_cast<uint16_t*>(&cells[lane >> 1][(y & 1) * 16 + (y >> 1) * 4 + 2 * (lane & 1)]) =
+        (uint16_t)(hw[0] | (hw[1] << 8));
+    __syncthreads();
+    const int tid = y * 32 + lane;
+    if (tid < 128) {
+        const int c = tid >> 3, copy = (tid >> 1) & 3, e = tid & 1;
+        const int g = blockIdx.y * 16 + c;  // chunk along K
+        if (g < s.chunks_k) {
+            const int64_t off =
+                ((((int64_t)t * s.chunks_k + g) * parts + h) * 4 + copy) * kChunkBytes + (2 * jj + e) * 16;
+            *reinterpret_cast<uint4*>(s.out_chunks + off) = *reinterpret_cast<const uint4*>(&cells[c][e * 16]);
+        }
+    }
 }
 
 // E2M1 and MXFP8: only the scales move, into the chunk layout of the pair kernel
@@ -1291,8 +1333,8 @@ cudaError_t launch_prep_pair(const GemmArgs* gs, int n, cudaStream_t st) {
             ps.out_chunks = ws + (side ? pl.sfb : pl.sfa);
             ps.K = (int)g.K;
             ps.chunks_k = (int)pl.chunks_k;
-            row_blocks = std::max(row_blocks, (ps.rows_cover + 7) / 8);
-            kslabs = std::max(kslabs, (pl.chunks_k * 4 + 31) / 32);
+            row_blocks = std::max(row_blocks, 16 * (ps.rows_cover / ps.tile_rows) * ((ps.tile_rows + 127) / 128));
+            kslabs = std::max(kslabs, (pl.chunks_k * 4 + 63) / 64);
             items = std::max(items, (int64_t)(ps.rows_cover / ps.tile_rows) * ((ps.tile_rows + 127) / 128) *
                                         pl.chunks_k);
         }
@@ -1304,7 +1346,7 @@ cudaError_t launch_prep_pair(const GemmArgs* gs, int n, cudaStream_t st) {
     pp.lhw = pl.kind == 2 ? 4 : 5;
     pp.copies = pair_replicated(pl.kind) ? 4 : 1;
     if (pl.kind == 0 && !pl.native) {
-        // 32 groups of 32 elements per CTA along K, 8 rows per CTA
+        // 64 groups of 32 elements per CTA along K; 16 CTAs per 128-row part of a GEMM tile
         if (kslabs > 65535) return cudaErrorNotSupported;  // grid y limit
         return launch_pdl(prep_widen_kernel, dim3((unsigned)row_blocks, (unsigned)kslabs, 2 * n), dim3(32, 8), 0,
                           st, pp);
