@@ -52,10 +52,12 @@ FP8_GRIDS = ("e1m2", "int4")
 
 @pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1", "e2m1r2"))
 @pytest.mark.parametrize("block", BLOCKS)
-@pytest.mark.parametrize("shape", [(128, 256, 128), (256, 512, 512), (200, 300, 384)])
+@pytest.mark.parametrize("shape", [(128, 256, 128), (256, 512, 512), (200, 300, 384), (200, 300, 160)])
 def test_gemm_exact_integer_case(grid, block, shape):
     """Unit scales: every product and partial sum is an exact small dyadic,
-    so the tensor-core result equals the fp64 reference bit for bit."""
+    so the tensor-core result equals the fp64 reference bit for bit.  K = 160
+    gives 5 or 10 scale bytes per row (odd rows start unaligned) and a partly
+    filled last 128-element scale chunk."""
     M, N, K = shape
     if grid.startswith("e2m1") and K % 64:
         pytest.skip("FP4 operands need K % 64 == 0")
@@ -71,10 +73,16 @@ def test_gemm_exact_integer_case(grid, block, shape):
 
 @pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1",))
 @pytest.mark.parametrize("block", BLOCKS)
-def test_gemm_random_scales(grid, block):
+@pytest.mark.parametrize("shape", [(384, 512, 1024), (200, 300, 160)])
+def test_gemm_random_scales(grid, block, shape):
     """Block scales spread over 2^-9 .. 2^7 (pairs of 1 x 16 blocks differ by up
-    to 16 binades, the exact range of the E5M2 fold)."""
-    M, N, K = 384, 512, 1024
+    to 16 binades, the exact range of the E5M2 fold).  K = 160: rows of 5 or 10
+    scale bytes, so the scale bytes of odd rows start unaligned."""
+    M, N, K = shape
+    if grid.startswith("e2m1") and K % 64:
+        pytest.skip("FP4 operands need K % 64 == 0")
+    if block[0] > 1 and (M % 32 or N % 32):
+        M, N = (M + 31) // 32 * 32, (N + 31) // 32 * 32
     rng = np.random.default_rng(31)
     ac, asc = _rand_operand(rng, M, K, grid, block, lo=118, hi=134)
     bc, bsc = _rand_operand(rng, N, K, grid, block, lo=118, hi=134)
