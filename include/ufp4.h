@@ -310,8 +310,9 @@ ufp4_status ufp4_gemm_prepared(const ufp4_qtensor* A, const ufp4_qtensor* B, con
                                int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /* ufp4_gemm_grouped_workspace_size -- scratch bytes ufp4_gemm_grouped needs:
- * the largest ufp4_gemm_workspace_size over the groups (A, B: HOST arrays of
- * num_groups qtensors). */
+ * the sum over the groups of ufp4_gemm_workspace_size, each rounded up to 256
+ * bytes (0 for a group with an empty product); A, B: HOST arrays of
+ * num_groups qtensors. */
 ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
                                              const ufp4_quant_desc* desc, size_t* bytes);
 
@@ -327,9 +328,19 @@ ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qten
  *   D, ldd HOST arrays of num_groups device output pointers and leading
  *          dimensions.
  *   workspace  device scratch of at least ufp4_gemm_grouped_workspace_size
- *          bytes; the groups run one after another on `stream` and share it.
+ *          bytes; group g uses its own region of it (after those of groups
+ *          0 .. g-1).
  * A group with no rows (M_g = 0 or N_g = 0) is skipped; a group with K_g = 0
- * writes D_g = 0.  Every group is checked before anything is launched. */
+ * writes D_g = 0.  Every group is checked before anything is launched.
+ * Streams: with two or more non-empty groups, the groups are dealt
+ * round-robin to `stream` and two internal non-blocking streams of the
+ * current device (created on the first such call, kept for the process), so
+ * that small groups run side by side.  The internal streams start after the
+ * work already enqueued on `stream`, and `stream` waits for them before any
+ * later work, so the call is ordered on `stream` like a single launch.  The
+ * enqueue sequence is serialized by a lock (safe from several host threads).
+ * Inside a CUDA-graph capture of `stream` the internal streams join the
+ * capture and are joined back before the call returns. */
 ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
                               const ufp4_quant_desc* desc, float* const* D, const int64_t* ldd, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);

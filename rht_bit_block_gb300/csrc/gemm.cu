@@ -32,6 +32,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -1525,21 +1526,82 @@ cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st) {
     return launch_main_pair(&g, 1, st);
 }
 
-// GEMMs sharing a descriptor, each with its own workspace region, run one
-// after another on the stream (operand prep and tensor-core launch each).
-// Empty products are skipped and K = 0 gives D = 0.  Launching several GEMMs
-// from one persistent grid was tried; it stalled for minutes when it followed
-// other GEMMs on the stream with lazily loaded modules, so it is not used.
+// One group of a grouped call: operand prep and tensor-core launch, or
+// D = 0 for K = 0.
+static cudaError_t launch_one_group(const GemmArgs& g, int num_sms, cudaStream_t st) {
+    if (g.K == 0)
+        return cudaMemset2DAsync(g.D, (size_t)g.ldd * sizeof(float), 0, (size_t)g.N * sizeof(float), (size_t)g.M, st);
+    return launch_gemm(g, num_sms, st);
+}
+
+// Two streams per device that grouped calls spread their groups over, with
+// the caller's stream; created on first use and kept for the process.
+constexpr int kLanes = 2;
+struct GroupLanes {
+    cudaStream_t s[kLanes];
+    bool ready;
+};
+static std::mutex g_lanes_mu;
+static GroupLanes g_lanes[64];
+
+// GEMMs sharing a descriptor, each with its own workspace region.  Every
+// group on its own is a small GEMM whose last wave of tiles leaves much of the
+// GPU idle, so the groups are dealt round-robin to the caller's stream and
+// two internal streams: an event recorded on the caller's stream orders them
+// after the caller's earlier work, and the caller's stream waits for events
+// recorded on the internal streams after their last group.  The kernels of
+// different groups never wait on one another; the whole fork, launch and join
+// sequence of a call is enqueued under one lock, so every wait refers to work
+// already enqueued.  Empty products are skipped and K = 0 gives D = 0.
+// (Launching several GEMMs from one persistent grid was tried; it stalled for
+// minutes when it followed other GEMMs with lazily loaded modules.)
 cudaError_t launch_gemm_groups(const GemmArgs* gs, int n, int num_sms, cudaStream_t st) {
-    for (int i = 0; i < n; ++i) {
-        const GemmArgs& g = gs[i];
-        if (g.M == 0 || g.N == 0) continue;
-        const cudaError_t e = g.K == 0
-            ? cudaMemset2DAsync(g.D, (size_t)g.ldd * sizeof(float), 0, (size_t)g.N * sizeof(float), (size_t)g.M, st)
-            : launch_gemm(g, num_sms, st);
-        if (e != cudaSuccess) return e;
+    int live = 0;
+    for (int i = 0; i < n; ++i) live += gs[i].M > 0 && gs[i].N > 0;
+    int dev = 0;
+    if (live < 2 || cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+        for (int i = 0; i < n; ++i) {
+            if (gs[i].M == 0 || gs[i].N == 0) continue;
+            const cudaError_t e = launch_one_group(gs[i], num_sms, st);
+            if (e != cudaSuccess) return e;
+        }
+        return cudaSuccess;
     }
-    return cudaSuccess;
+    std::lock_guard<std::mutex> lock(g_lanes_mu);
+    GroupLanes& L = g_lanes[dev];
+    if (!L.ready) {
+        for (int j = 0; j < kLanes; ++j) {
+            const cudaError_t e = cudaStreamCreateWithFlags(&L.s[j], cudaStreamNonBlocking);
+            if (e != cudaSuccess) {
+                for (int k = 0; k < j; ++k) cudaStreamDestroy(L.s[k]);
+                return e;
+            }
+        }
+        L.ready = true;
+    }
+    cudaEvent_t fork = nullptr, join[kLanes] = {};
+    cudaError_t e = cudaEventCreateWithFlags(&fork, cudaEventDisableTiming);
+    for (int j = 0; j < kLanes && e == cudaSuccess; ++j) e = cudaEventCreateWithFlags(&join[j], cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(fork, st);
+    for (int j = 0; j < kLanes && e == cudaSuccess; ++j) e = cudaStreamWaitEvent(L.s[j], fork, 0);
+    if (e == cudaSuccess) {
+        const cudaStream_t lanes[kLanes + 1] = {st, L.s[0], L.s[1]};
+        int k = 0;
+        for (int i = 0; i < n && e == cudaSuccess; ++i) {
+            if (gs[i].M == 0 || gs[i].N == 0) continue;
+            e = launch_one_group(gs[i], num_sms, lanes[k++ % (kLanes + 1)]);
+        }
+        // join even after a failed launch, so that the caller's stream stays ordered after the lanes
+        for (int j = 0; j < kLanes; ++j) {
+            cudaError_t r = cudaEventRecord(join[j], L.s[j]);
+            if (r == cudaSuccess) r = cudaStreamWaitEvent(st, join[j], 0);
+            if (e == cudaSuccess) e = r;
+        }
+    }
+    if (fork) cudaEventDestroy(fork);  // released once the recorded work completes
+    for (int j = 0; j < kLanes; ++j)
+        if (join[j]) cudaEventDestroy(join[j]);
+    return e;
 }
 
 cudaError_t preload_gemm_kernels() {
