@@ -441,6 +441,16 @@ def run_suite(args, sections=("rowwise", "rowcol", "diag", "gemm", "moe")):
                  f"{('E8M0' if grid == 'mxfp8' else 'UE8M0') if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs,
                  "GB/s", gbs / pk["hbm"], pk["hbm"],
                  ms=ms)
+        # two-level scale: the tensor amax pre-pass reads x once more before the quantizer reads it
+        desc = ufp4.make_desc(grid="e2m1", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
+                              scale_fmt=ufp4.SCALE_E4M3, out_mask=ufp4.OUT_ROWWISE)
+        out = ufp4.alloc_quantized(rows, cols, desc, dev)
+        t_amax = torch.zeros(1, dtype=torch.float32, device=dev)
+        q = ufp4.qtensor(*out, rows, cols, t_amax)
+        ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
+        gbs = rows * cols * (2 * 2 + 0.5 + 1 / 16) / (ms / 1e3) / 1e9
+        emit("quantize_rowwise", f"X {rows}x{cols} e2m1 1x16 two-level (E4M3 x fp32) n=16 RTNE: tensor amax "
+             "pre-pass + quantize, x read twice", gbs, "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
         del xs5
 
     if "rowcol" in sections:
@@ -502,6 +512,22 @@ def run_suite(args, sections=("rowwise", "rowcol", "diag", "gemm", "moe")):
             emit("gemm", f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
                  kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
             del A, B, ws, D
+        # two-level scales: UE4M3 block bytes on the native FP4 kind, g_A g_B in the epilogue
+        desc = ufp4.make_desc(grid="e2m1", block=(1, 16), scale_fmt=ufp4.SCALE_E4M3)
+        def two_level_operand(rows):
+            c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8) & 0x77
+            sc = torch.randint(0x30, 0x48, (rows, K // 16), generator=g, dtype=torch.uint8)  # E4M3 0.5 .. 4
+            return c.to(dev), sc.to(dev), torch.full((1,), 100.0, dtype=torch.float32, device=dev)
+        A, B = two_level_operand(M), two_level_operand(N)
+        qa, qb = ufp4.qtensor(A[0], A[1], M, K, A[2]), ufp4.qtensor(B[0], B[1], N, K, B[2])
+        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+        D = torch.empty((M, N), dtype=torch.float32, device=dev)
+        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+        emit("gemm", f"{M}x{N}x{K} e2m1 1x16 two-level (UE4M3 x fp32)", tf, "TFLOP/s", tf / (6 * pk["bf16"]),
+             6 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x6 (nominal ratio)")
+        del A, B, ws, D
         # MXFP8 operands (E4M3 codes read in place by the FP8 kernel)
         desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
         def e4m3_operand(rows):
