@@ -155,3 +155,28 @@ def test_mxfp8_validation(lib):
     q = ufp4.QTensor(codes, scales, 64, 64, 64, 2)
     assert lib.ufp4_quant_error_stats(ctypes.c_void_p(x), 64, 64, 64, ctypes.byref(mk()), ctypes.byref(q),
                                       stats, None) == UNS
+
+
+def test_grouped_workspace_is_the_sum_of_aligned_group_sizes(lib):
+    """Each group takes its own 256-byte aligned region (groups may run side by
+    side); a group with an empty product needs none.  A workspace smaller than
+    the first group's share is rejected before anything is launched (fake
+    device addresses: the first group alone needs its 200 x 160 FP8 copy)."""
+    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
+    shapes = [(200, 300, 160), (0, 64, 128), (512, 256, 2048), (128, 0, 64), (64, 96, 0)]
+    A = [ufp4.QTensor(0x10000, 0x20000, m, k, max(16, k // 2), max(1, k // 16)) for m, n, k in shapes]
+    B = [ufp4.QTensor(0x30000, 0x40000, n, k, max(16, k // 2), max(1, k // 16)) for m, n, k in shapes]
+    each = []
+    for m, n, k in shapes:
+        b = ufp4.ufp4_gemm_workspace_size(m, n, k, desc) if m and n and k else 0
+        each.append((b + 255) // 256 * 256)
+    need = ufp4.ufp4_gemm_grouped_workspace_size(A, B, desc)
+    assert need == sum(each) and need > 0
+    n = len(shapes)
+    arrA, arrB = (ufp4.QTensor * n)(*A), (ufp4.QTensor * n)(*B)
+    dptr = (ctypes.c_void_p * n)(*[0x50000] * n)
+    ldd = (ctypes.c_int64 * n)(*[max(1, s[1]) for s in shapes])
+    assert each[0] > 200 * 160
+    rc = lib.ufp4_gemm_grouped(n, arrA, arrB, ctypes.byref(desc), dptr, ldd, ctypes.c_void_p(0x100000),
+                               ctypes.c_size_t(256), None)
+    assert rc == 1  # UFP4_ERR_INVALID_ARG
