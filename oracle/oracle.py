@@ -78,6 +78,10 @@ def lib():
         L.orc_round_rtne.restype = i32
         L.orc_round_sr.argtypes = [i32, ctypes.c_float, u32]
         L.orc_round_sr.restype = i32
+        L.orc_round_sr_array.argtypes = [i32, P, P, i64, P]
+        L.orc_round_sr_array.restype = None
+        L.orc_round_sr_philox.argtypes = [i32, ctypes.c_float, u64, u64, i64, u32, u32, P]
+        L.orc_round_sr_philox.restype = None
         L.orc_quantize_rows_mxfp8.argtypes = [P, i64, i64, i64, i32, u64, P, P]
         L.orc_quantize_rows_mxfp8.restype = i32
         L.orc_dequantize_f64_mxfp8.argtypes = [P, P, i64, i64, P]
@@ -132,6 +136,25 @@ def round_rtne(grid, a: float) -> int:
 
 def round_sr(grid, a: float, u16: int) -> int:
     return lib().orc_round_sr(_grid(grid), a, u16)
+
+
+def round_sr_array(grid, a: np.ndarray, u16: np.ndarray) -> np.ndarray:
+    """orc_round_sr over arrays of magnitudes and 16-bit draws (level indices)."""
+    a = np.ascontiguousarray(a, dtype=np.float32)
+    u = np.ascontiguousarray(u16, dtype=np.uint16)
+    assert a.shape == u.shape
+    idx = np.empty(a.shape, dtype=np.uint8)
+    lib().orc_round_sr_array(_grid(grid), _ptr(a), _ptr(u), a.size, _ptr(idx))
+    return idx
+
+
+def round_sr_philox(grid, a: float, sr_seed: int, lin0: int, count: int, stream: int = 0,
+                    group: int = 0) -> np.ndarray:
+    """orc_round_sr of one magnitude with the quantizer's Philox draws of output
+    elements lin0 .. lin0 + count - 1 (level indices)."""
+    idx = np.empty(count, dtype=np.uint8)
+    lib().orc_round_sr_philox(_grid(grid), a, sr_seed, lin0, count, stream, group, _ptr(idx))
+    return idx
 
 
 # ---------------------------------------------------------------- tensors

@@ -294,6 +294,20 @@ static uint32_t sr_draw(uint64_t sr_seed, uint64_t lin, uint32_t stream, uint32_
     return (j % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);
 }
 
+/* Test entries of the SR rule above, over many draws at once.
+ *  orc_round_sr_array:  idx[i] = orc_round_sr(grid, a[i], u16[i]);
+ *  orc_round_sr_philox: idx[i] = orc_round_sr(grid, a, draw of output element
+ *                       lin0 + i), with the quantizer's counter layout. */
+void orc_round_sr_array(int grid, const float* a, const uint16_t* u16, int64_t count, uint8_t* idx) {
+    for (int64_t i = 0; i < count; ++i) idx[i] = (uint8_t)orc_round_sr(grid, a[i], u16[i]);
+}
+
+void orc_round_sr_philox(int grid, float a, uint64_t sr_seed, uint64_t lin0, int64_t count, uint32_t stream,
+                         uint32_t group, uint8_t* idx) {
+    for (int64_t i = 0; i < count; ++i)
+        idx[i] = (uint8_t)orc_round_sr(grid, a, sr_draw(sr_seed, lin0 + (uint64_t)i, stream, group));
+}
+
 /* --------------------------------------------------------- the quantizer
  * Quantize the bf16 matrix x (rows x cols, leading dimension ld) along its
  * rows: RHT on each length-n segment of a row, then blocks of

@@ -205,24 +205,63 @@ def test_bin_bias_law(grid, q, expect):
     assert abs(err.mean() - expect) < 5 * sigma + 1e-9
 
 
-@pytest.mark.parametrize("grid", GRIDS)
-@pytest.mark.parametrize("p", [0.5 + 1e-6, 1e-3, 1 - 1e-3, 0.3141])
-def test_sr_is_unbiased(grid, p):
-    """2D-block page (stochastic rounding) and UFP4 summary (数据集): E[SR(x)] = x.
-    10^6 draws at adversarial points, within 4 sigma."""
+def _sr_bins(grid):
+    """The lowest and the highest bin of the grid, and one in the middle."""
     levels = [orc.level(grid, i) for i in range(orc.num_levels(grid))]
-    lo, hi = levels[3], levels[4]
-    x = np.float32(lo + p * (hi - lo))
-    u = np.random.default_rng(17).integers(0, 65536, 1_000_000)
-    # orc_round_sr rounds up iff u < p*65536, so count the draws below the threshold
-    thr = np.float64(x - lo) / (hi - lo) * 65536.0
-    ups = int((u < thr).sum())
-    # one direct call per distinct outcome to check the rule itself
-    assert orc.round_sr(grid, float(x), 0) == 4
-    assert orc.round_sr(grid, float(x), 65535) == (4 if thr > 65535 else 3)
-    mean = lo + (hi - lo) * ups / u.size
-    sigma = (hi - lo) * np.sqrt(p * (1 - p) / u.size)
-    assert abs(mean - np.float64(x)) < 4 * sigma + (hi - lo) * 2.0 ** -16
+    m = len(levels) // 2
+    return levels, [(0, 1), (m - 1, m), (len(levels) - 2, len(levels) - 1)]
+
+
+def _sr_mean_check(grid, idx, levels, i_lo, x):
+    lo, hi = levels[i_lo], levels[i_lo + 1]
+    assert set(np.unique(idx).tolist()) <= {i_lo, i_lo + 1}, "SR left the two neighbouring levels"
+    p = (np.float64(x) - lo) / (hi - lo)
+    mean = np.asarray(levels, dtype=np.float64)[idx].mean()
+    sigma = (hi - lo) * np.sqrt(p * (1 - p) / idx.size)
+    # 16-bit draws: P(up) = ceil(65536 p) / 65536, a bias of at most 2^-16 of the gap
+    assert abs(mean - np.float64(x)) < 4 * sigma + (hi - lo) * 2.0 ** -16, (grid, p, mean, np.float64(x))
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+@pytest.mark.parametrize("p", [0.5 + 1e-6, 1e-3, 1 - 1e-3])
+def test_sr_is_unbiased(grid, p):
+    """2D-block page (stochastic rounding, E[roundS(x)] = x) and UFP4 summary
+    (数据集, SR): the oracle's own SR function, applied to 10^6 uniform 16-bit
+    draws at adversarial points of three bins per grid, averages to x within
+    4 sigma (plus the 2^-16 resolution of the draws).  An 8-bit draw, a wrong
+    threshold or a wrong neighbour would miss by far more at p = 1e-3."""
+    levels, bins = _sr_bins(grid)
+    u = np.random.default_rng(17).integers(0, 65536, 1_000_000).astype(np.uint16)
+    for i_lo, i_hi in bins:
+        x = np.float32(levels[i_lo] + p * (levels[i_hi] - levels[i_lo]))
+        idx = orc.round_sr_array(grid, np.full(u.size, x, dtype=np.float32), u)
+        _sr_mean_check(grid, idx, levels, i_lo, x)
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+@pytest.mark.parametrize("p", [0.5 + 1e-6, 1e-3, 1 - 1e-3])
+def test_sr_is_unbiased_with_the_quantizer_draws(grid, p):
+    """The same law with the draws the quantizer itself uses (Philox4x32-10,
+    the 16-bit halves of consecutive output elements), 10^6 elements in both
+    the row-wise and the column-wise stream."""
+    levels, bins = _sr_bins(grid)
+    i_lo = bins[1][0]
+    x = np.float32(levels[i_lo] + p * (levels[i_lo + 1] - levels[i_lo]))
+    for stream in (0, 1):
+        idx = orc.round_sr_philox(grid, float(x), inputs.SR_SEED, 12345 * 8, 1_000_000, stream=stream, group=3)
+        _sr_mean_check(grid, idx, levels, i_lo, x)
+
+
+def test_sr_draw_cross_check():
+    """Cross-check of the rule on its own: counting u < p * 65536 over the same
+    draws gives the same number of round-ups as the oracle."""
+    u = np.random.default_rng(3).integers(0, 65536, 200_000).astype(np.uint16)
+    for grid in GRIDS:
+        levels = [orc.level(grid, i) for i in range(orc.num_levels(grid))]
+        x = np.float32(levels[1] + 0.3141 * (levels[2] - levels[1]))
+        thr = (np.float64(x) - levels[1]) / (levels[2] - levels[1]) * 65536.0
+        idx = orc.round_sr_array(grid, np.full(u.size, x, dtype=np.float32), u)
+        assert int((idx == 2).sum()) == int((u < thr).sum())
 
 
 @pytest.mark.parametrize("grid", GRIDS)
@@ -237,19 +276,23 @@ def test_sr_only_picks_neighbours(grid):
         assert idx in (lo, min(lo + 1, top))
 
 
-def test_sr_through_quantizer_is_unbiased():
-    """Whole quantizer with SR: the mean dequantized value of a constant block
-    pattern equals the rotated input within 4 sigma."""
-    rows, cols = 4096, 64
-    base = np.tile(np.array([7.0] + [1.3] * 15, dtype=np.float32), (rows, cols // 16))
+@pytest.mark.parametrize("v", [1.296875, 1.0078125, 1.9921875])
+def test_sr_through_quantizer_is_unbiased(v):
+    """Whole quantizer with SR (n = 1, E1M2, fp32 scales): blocks [7, v, ..., v]
+    have s = 4, so v / 4 falls between the levels 0.25 and 0.5 at p = 0.297,
+    2^-7 and 1 - 2^-7; the mean dequantized v over about 10^6 elements equals
+    v within 4 sigma."""
+    rows, cols = 1024, 1024
+    base = np.tile(np.array([7.0] + [v] * 15, dtype=np.float32), (rows, cols // 16))
     x = inputs.f32_to_bf16_bits(base)
     codes, sc = orc.quantize(x, grid="e1m2", n=1, rounding=orc.SR, sr_seed=9)
+    assert (sc == 4.0).all()
     deq = orc.dequantize(codes, sc, grid="e1m2", n=1).astype(np.float64)
-    xf = inputs.bf16_bits_to_f32(x).astype(np.float64)
-    s = np.float64(sc[0, 0])
-    col = deq[:, 1::16].ravel()  # the 1.3 entries
-    sigma = 0.25 * s / 2 / np.sqrt(col.size)
-    assert abs(col.mean() - xf[0, 1]) < 4 * sigma + 0.25 * s * 2.0 ** -16 + 1e-6 * xf[0, 1]
+    vals = deq.reshape(rows, cols // 16, 16)[:, :, 1:].ravel()
+    assert set(np.unique(vals).tolist()) <= {1.0, 2.0}
+    p = (v / 4 - 0.25) / 0.25
+    sigma = 1.0 * np.sqrt(p * (1 - p) / vals.size)
+    assert abs(vals.mean() - v) < 4 * sigma + 2.0 ** -16
 
 
 # -------------------------------------------------------------------- scale
