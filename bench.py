@@ -1,22 +1,25 @@
 #!/usr/bin/env python3
 """Benchmark of the UFP4 hot path on GB300.
 
-One step = one pass of the hot path over one batch of the Dense-1.5B-like
-FPROP workload: fused RHT + E1M2 4-bit quantization (n = 16, 1 x 16 blocks,
-UE8M0 scales, RTNE) of X (8192 x 2048 bf16) and W (5632 x 2048 bf16), then
-the quantized GEMM Y = Q(X H') Q(W H')^T (8192 x 5632 x 2048, fp32 out).
+One step = one pass of the hot path over one batch of the MoE-124B-like FPROP
+workload (the largest single-GPU configuration): fused RHT + E1M2 4-bit
+quantization (n = 16, 1 x 16 blocks, UE8M0 scales, RTNE) of X (16384 x 7168
+bf16) and W (7168 x 7168 bf16), both N(0,1) with 0.1 % element outliers x50,
+then the quantized GEMM Y = Q(X H') Q(W H')^T (16384 x 7168 x 7168, fp32 out).
 
 value  = fused quantizer throughput in GB/s of algorithmic bytes (bf16 read
          + packed codes + scales written), from CUDA events around the
-         quantizer launches inside the timed steps.
+         quantizer launch inside the timed steps.
 gemm   = quantized GEMM TFLOP/s (2 M N K per step, operand prep included).
 e2e    = the same quantizer metric through the C ABI with host buffers:
          pinned H2D of X and W, quantize, GEMM and D2H of the codes, scales
          and Y inside the timed region.
-Inputs rotate over 5 copies (270 MiB > 2 x L2), so every step reads cold data.
+Inputs rotate over 2 copies (each copy 322 MiB > 2 x L2), so every step reads
+cold data.
 
 --impl reference runs the oracle (plain C, one host core) as the reference
 arm on bounded row samples of the same workload.
+--suite prints further lines (the other workloads and modes), not the headline.
 Multi-GPU (torchrun): every rank runs its own replica of the step (weak
 scaling, no collective on the data path); timing is the max over ranks.
 """
@@ -37,15 +40,17 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 
 METRIC = "fused RHT+4-bit quantize GB/s (% of HBM peak); quantized GEMM TFLOP/s (% peak)"
-M, N, K = 8192, 5632, 2048
+M, N, K = 16384, 7168, 7168
 BLOCK = 16
 # algorithmic bytes per element: 2 (bf16 in) + 0.5 (codes) + 1/16 (UE8M0 scale)
 BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / BLOCK
 QUANT_ELEMS = (M + N) * K
 QUANT_BYTES = QUANT_ELEMS * BYTES_PER_ELEM
 GEMM_FLOPS = 2.0 * M * N * K
-ROTATE = 5
-WORKLOAD = "dense-1.5B FPROP operands: X 8192x2048, W 5632x2048 bf16; E1M2 1x16 UE8M0 RTNE, n=16; GEMM 8192x5632x2048"
+ROTATE = 2
+WORKLOAD = ("MoE-124B-like FPROP operands: X 16384x7168, W 7168x7168 bf16 (N(0,1), 0.1% element outliers x50); "
+            "E1M2 1x16 UE8M0 RTNE, n=16; GEMM Y = Q(X)Q(W)^T 16384x7168x7168")
+L2_NOTE = "inputs rotate over 2 copies (each 322 MiB > 2x L2); the 470 MB fp32 Y is written every step"
 
 
 # library kernel launches per step: quantize X and W (one batched launch),
@@ -169,8 +174,9 @@ def oracle_sample(rows_x: int, rows_w: int):
     arguments, generated once, outside any timed region."""
     import oracle as orc
     from rht_bit_block_gb300 import inputs
-    x, w = inputs.dense_fprop()
+    x, w = inputs.large_sweep(M, K, N)
     xs, ws = np.ascontiguousarray(x[:rows_x]), np.ascontiguousarray(w[:rows_w])
+    del x, w
     kw = dict(grid="e1m2", block=(1, BLOCK), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=orc.SCALE_UE8M0)
     orc.quantize(xs[:16], **kw)  # build + load outside the timing
     return xs, ws, kw
@@ -243,7 +249,7 @@ def run_gpu(args):
             dist.barrier()
         torch.cuda.synchronize()
 
-    x_np, w_np = inputs.dense_fprop()
+    x_np, w_np = inputs.large_sweep(M, K, N)
     to_t = lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)
     xs = [to_t(x_np).to(dev) for _ in range(ROTATE)]
     wsrc = [to_t(w_np).to(dev) for _ in range(ROTATE)]
@@ -356,13 +362,13 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         rate, elems, dt, reps = cpu_oracle_rate(oracle_sample(1024, 1024), args.cpu_seconds, 64)
         cpu = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first 1024 rows of X and of W ({2048 * K} elements) per rep, {reps} reps, {dt:.1f} s"}
+               "sample": f"first 1024 rows of X and of W ({2 * 1024 * K} elements) per rep, {reps} reps, {dt:.1f} s"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_time / args.steps * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32 (bf16 in, 4-bit codes out)", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "l2": "inputs rotate over 5 copies (270 MiB > 2x L2)",
+            "config": {"workload": WORKLOAD, "l2": L2_NOTE,
                        "parallelism": f"replicas x{world}"},
             "quant_frac_of_hbm": value / pk["hbm"],
             "gemm": {"value": gemm_tflops, "unit": "TFLOP/s", "frac": gemm_frac, "peak": fp8_peak,
@@ -382,7 +388,7 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------- suite mode
-def run_suite(args, sections=("rowwise", "rowcol", "diag", "gemm", "moe")):
+def run_suite(args, sections=("dense", "rowwise", "rowcol", "diag", "gemm", "moe")):
     """Further measurements, one JSON line each (not the headline): the other
     workloads of the configuration list and the widened rows.  CUDA events on
     the launching stream, 3 warm-ups, median of the timed repetitions; inputs
@@ -417,6 +423,32 @@ def run_suite(args, sections=("rowwise", "rowcol", "diag", "gemm", "moe")):
     def scale_bytes(desc):
         per = 1 if desc.scale_fmt == ufp4.SCALE_UE8M0 else 4
         return per / (desc.block_rows * desc.block_cols)
+
+    if "dense" in sections:
+        # the Dense-1.5B-like FPROP step: X 8192 x 2048 and W 5632 x 2048 quantized
+        # in one launch, then the GEMM 8192 x 5632 x 2048 (prep and kernel timed apart)
+        xd_np, wd_np = inputs.dense_fprop()
+        (m2, k2), n2 = xd_np.shape, wd_np.shape[0]
+        xs2 = [to_t(xd_np).to(dev) for _ in range(5)]
+        ws2 = [to_t(wd_np).to(dev) for _ in range(5)]
+        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
+                              scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+        qx2, qw2 = ufp4.alloc_quantized(m2, k2, desc, dev), ufp4.alloc_quantized(n2, k2, desc, dev)
+        tx2, tw2 = ufp4.qtensor(*qx2, m2, k2), ufp4.qtensor(*qw2, n2, k2)
+        D2 = torch.empty((m2, n2), dtype=torch.float32, device=dev)
+        wsb2 = torch.empty(ufp4.ufp4_gemm_workspace_size(m2, n2, k2, desc), dtype=torch.uint8, device=dev)
+        qms = timed(lambda i: ufp4.ufp4_rht_quantize_batch([xs2[i % 5], ws2[i % 5]], desc, [tx2, tw2],
+                                                           stream.cuda_stream))
+        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(tx2, tw2, desc, wsb2, stream.cuda_stream))
+        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(tx2, tw2, desc, D2, wsb2, stream.cuda_stream))
+        qb = (m2 + n2) * k2 * BYTES_PER_ELEM
+        emit("dense_step", f"Dense-1.5B-like FPROP operands X {m2}x{k2} + W {n2}x{k2}, e1m2 1x16 UE8M0 n=16 RTNE, "
+             "one batched launch", qb / (qms / 1e3) / 1e9, "GB/s", qb / (qms / 1e3) / 1e9 / pk["hbm"], pk["hbm"],
+             ms=qms)
+        tf = 2.0 * m2 * n2 * k2 / (kms / 1e3) / 1e12
+        emit("dense_step", f"Dense-1.5B-like FPROP GEMM {m2}x{n2}x{k2} e1m2 1x16 UE8M0 (tensor-core kernel; "
+             "prep timed apart)", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"], kernel_ms=kms, prep_ms=pms)
+        del xs2, ws2, D2, wsb2
 
     if "rowwise" in sections:
         # 1. large-shape sweep operand, row-wise (X 16384 x 7168, > L2)
@@ -662,8 +694,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="further measurements (other workloads, widened rows), one JSON line each")
-    ap.add_argument("--suite-sections", default="rowwise,rowcol,diag,gemm,moe",
-                    help="comma-separated subset of the suite: rowwise, rowcol, diag, gemm, moe")
+    ap.add_argument("--suite-sections", default="dense,rowwise,rowcol,diag,gemm,moe",
+                    help="comma-separated subset of the suite: dense, rowwise, rowcol, diag, gemm, moe")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -33,8 +33,15 @@
  *    absolute maximum after the RHT is nonzero but below 2^-120 or above
  *    2^120, are outside the contract (outputs are then unspecified but the
  *    call stays memory-safe).
- *  - Thread safety: calls keep no host state between calls and may be made
- *    from several threads on different streams.
+ *  - Host state: calls may be made from several threads on different
+ *    streams.  The library keeps a little process-lifetime state per device,
+ *    set up on first use and guarded by locks: a flag that its kernels have
+ *    been loaded (done once, before its first launch on the device), the
+ *    cached co-residency figures of the GEMM launch, the two internal streams
+ *    of ufp4_gemm_grouped (created on its first call with two or more
+ *    groups) and the device address of the ufp4_gemm_noalloc scratch.  After
+ *    cudaDeviceReset that state is stale: do not call the library on that
+ *    device again in the same process.
  */
 #ifndef UFP4_H_
 #define UFP4_H_
@@ -350,9 +357,9 @@ ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const u
 
 /* ufp4_gemm_noalloc -- ufp4_gemm for callers that must not allocate device
  * memory (no counterpart in the pages: it is an interface convenience).
- * Some callers cannot call cudaMalloc at all: code inside a CUDA-graph
- * capture, plugins or custom ops whose host framework owns every device
- * allocation, and latency-critical loops where an allocation may synchronize
+ * Some callers cannot call cudaMalloc at all: plugins or custom ops whose
+ * host framework owns every device allocation and hands out none for
+ * scratch, and latency-critical loops where an allocation may synchronize
  * the device.  This entry point takes the same A, B, desc, D and ldd as
  * ufp4_gemm but no workspace: it uses one scratch array of
  * UFP4_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that

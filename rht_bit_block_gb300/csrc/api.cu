@@ -1,6 +1,7 @@
 // C ABI of the UFP4 library (declared in include/ufp4.h): host-side argument
 // validation, the sign vector, and dispatch to the kernels.  Nothing here
-// allocates device memory and no host state survives a call.
+// allocates device memory; the only host state kept between calls is the
+// per-device kernels-loaded flag below.
 #include <algorithm>
 #include <cmath>
 #include <mutex>

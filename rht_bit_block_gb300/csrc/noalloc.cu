@@ -3,9 +3,9 @@
 // scratch array that lives in this library's device image.
 //
 // Who needs it: code that runs where cudaMalloc is off limits -- inside a
-// region being captured into a CUDA graph, inside a plugin or custom op whose
-// host framework owns every allocation, or in a latency-critical loop where
-// an allocation (which can synchronize the whole device) is not acceptable.
+// plugin or custom op whose host framework owns every allocation and hands
+// out none for scratch, or in a latency-critical loop where an allocation
+// (which can synchronize the whole device) is not acceptable.
 // Such callers still own and pass A, B and D; only the scratch moves here.
 #include <cstdint>
 #include <mutex>

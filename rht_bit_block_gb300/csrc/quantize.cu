@@ -84,8 +84,9 @@ struct Fold {
 //
 // RTNE multiplies y by one folded reciprocal per block, rr = r * 2^-j * f,
 // where f = 2^-7 (E1M2: k/4 -> k * 2^-9) or 2^-9 (INT4: k -> k * 2^-9) puts
-// the uniform levels on e4m3's subnormals, and f = 1 for E2M1 and for INT4
-// with UE8M0 scales (rounded by an fma instead); every factor is a power of
+// the uniform levels on e4m3's subnormals, and f = 1 for E2M1; with UE8M0
+// scales the uniform grids are rounded by an fma instead, with f = 1/step
+// (E1M2 4, INT4 1); every factor is a power of
 // two, so fp32(y * rr) = fp32(z * r) * f exactly.  SR uses
 // f = 1/step (E1M2 4, INT4 1, E2M1 1).  For other n, z = fp32(y * 1/sqrt n)
 // is formed first, as in the definition.
@@ -106,8 +107,9 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
     } else if (SF == 1) {
         const int eb = scale_po2_byte<GRID>(Mz);  // e + 127
         if (write) *sptr = (uint8_t)eb;
-        // 2^(-e + lf + lj) from its biased exponent (a subnormal below 1)
-        const int kb = 254 - eb + lf + lj;
+        // 2^(-e + lf + lj) from its biased exponent (a subnormal below 1;
+        // capped at 2^127, reached only by blocks outside the input contract)
+        const int kb = min(254 - eb + lf + lj, 254);
         return __uint_as_float(kb >= 1 ? (uint32_t)kb << 23 : 1u << (kb + 22));
     } else {
         float sc, r;
@@ -164,9 +166,12 @@ template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B,
                                           uint64_t sr_seed, uint32_t stream, uint32_t group) {
-    // INT4 with power-of-two scales rounds by adding 1.5 * 2^23 + 8 (below)
-    constexpr bool kMagic = GRID == 1 && !SR && SF == 1;
-    constexpr int lf = (kMagic || GRID == 4) ? 0 : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
+    // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
+    // to the value in units of the grid step (below): INT4 k, E1M2 4 t
+    constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
+    constexpr int lf = GRID == 4 ? 0
+                     : kMagic    ? (GRID == 0 ? 2 : 0)
+                                 : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
     const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0);
     const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0);
     float ra1 = ra0, rb1 = rb0;
@@ -200,11 +205,15 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         return;
     }
     if (kMagic) {
-        // t = z r is exact (r a power of two), so one fma t + (1.5 * 2^23 + 8)
-        // rounds t to the nearest integer k, ties to even (the addend is even
-        // and the result's unit is 1), and its low nibble is k + 8 (|k| <= 7):
-        // the two's complement nibble of k after flipping bit 3.  Pairs of
-        // nibbles merge with one multiply-add (bits 4..7 of k + 8 are clear).
+        // t = z r is exact (r a power of two; for E1M2 r also carries the
+        // factor 4 = 1 / step), so one fma t + (1.5 * 2^23 + 8) rounds t to the
+        // nearest integer k, ties to even (the addend is even and the result's
+        // unit is 1), and its low nibble is o = k + 8 (|k| <= 7: the
+        // truncation-free scale keeps |t| <= 7).  Pairs of nibbles merge with
+        // one multiply-add (bits 4..7 of k + 8 are clear).  INT4: flipping
+        // bit 3 of o gives the two's complement nibble of k.  E1M2: o >= 8
+        // (k >= 0) becomes o - 8 = k; o < 8 (k < 0) becomes (o ^ 15) + 1 =
+        // 8 + |k|, the sign-magnitude nibble, and k = 0 is +0.
         uint32_t va[16], vb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -220,7 +229,9 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
             asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(x) : "r"(p0), "r"(p1));
             asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(y) : "r"(p2), "r"(p3));
             asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(x), "r"(y));
-            return w ^ 0x88888888u;
+            if (GRID == 1) return w ^ 0x88888888u;
+            const uint32_t neg = ((w >> 3) & 0x11111111u) ^ 0x11111111u;  // per nibble: 1 iff o < 8
+            return (w ^ (neg * 7u + 0x88888888u)) + neg;
         };
         if (A.valid) *reinterpret_cast<uint2*>(A.codes) = make_uint2(pack8(va), pack8(va + 8));
         if (B.valid) *reinterpret_cast<uint2*>(B.codes) = make_uint2(pack8(vb), pack8(vb + 8));

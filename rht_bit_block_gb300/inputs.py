@@ -19,10 +19,20 @@ SR_SEED = 1234
 
 
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
-    """fp32 -> bf16 bit patterns, round to nearest even (finite inputs)."""
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    """fp32 -> bf16 bit patterns, round to nearest even (finite inputs: the
+    largest finite pattern plus the rounding increment stays below 2^32, so
+    32-bit arithmetic does not wrap)."""
+    a = np.asarray(a, dtype=np.float32)
+    flat = np.ascontiguousarray(a).reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint16)
+    step = 1 << 20  # in slices that stay in cache (whole-array temporaries are much slower)
+    for i in range(0, flat.size, step):
+        u = flat[i:i + step].view(np.uint32).copy()
+        u += (u >> 16) & 1
+        u += 0x7FFF
+        u >>= 16
+        out[i:i + step] = u
+    return out.reshape(a.shape)
 
 
 def bf16_bits_to_f32(h: np.ndarray) -> np.ndarray:
@@ -36,13 +46,14 @@ def normal_bf16(rows: int, cols: int, seed: int, std: float = 1.0) -> np.ndarray
 
 def with_element_outliers(x_bf16: np.ndarray, frac: float, factor: float, seed: int) -> np.ndarray:
     """Multiply round(frac * size) distinct, seeded positions by `factor`."""
-    x = bf16_bits_to_f32(x_bf16).copy()
     rng = np.random.Generator(np.random.PCG64(seed))
-    k = int(round(frac * x.size))
-    pos = rng.choice(x.size, size=k, replace=False)
-    flat = x.reshape(-1)
-    flat[pos] *= np.float32(factor)
-    return f32_to_bf16_bits(x)
+    k = int(round(frac * x_bf16.size))
+    pos = rng.choice(x_bf16.size, size=k, replace=False)
+    # only the chosen entries change (bf16 -> fp32 -> bf16 is the identity elsewhere)
+    out = np.array(x_bf16, dtype=np.uint16, copy=True)
+    flat = out.reshape(-1)
+    flat[pos] = f32_to_bf16_bits(bf16_bits_to_f32(flat[pos]) * np.float32(factor))
+    return out
 
 
 def with_column_outliers(x_bf16: np.ndarray, frac: float, factor: float, seed: int) -> np.ndarray:
