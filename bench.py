@@ -388,7 +388,7 @@ def run_gpu(args):
 
 
 # ------------------------------------------------------------- suite mode
-def run_suite(args, sections=("dense", "rowwise", "rowcol", "diag", "gemm", "moe")):
+def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "gemm", "moe")):
     """Further measurements, one JSON line each (not the headline): the other
     workloads of the configuration list and the widened rows.  CUDA events on
     the launching stream, 3 warm-ups, median of the timed repetitions; inputs
@@ -483,6 +483,30 @@ def run_suite(args, sections=("dense", "rowwise", "rowcol", "diag", "gemm", "moe
         gbs = rows * cols * (2 * 2 + 0.5 + 1 / 16) / (ms / 1e3) / 1e9
         emit("quantize_rowwise", f"X {rows}x{cols} e2m1 1x16 two-level (E4M3 x fp32) n=16 RTNE: tensor amax "
              "pre-pass + quantize, x read twice", gbs, "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
+        del xs5
+
+    if "sweep" in sections:
+        # the large-shape quantizer sweep on X 16384 x 7168, row-wise: n in {16, 64,
+        # 256} x grid {E1M2, INT4, E2M1} x block {1x16 fp32, 1x32 fp32, 32x32 UE8M0}
+        # x {RTNE, SR}, 54 cells
+        x5, _ = inputs.large_sweep(k=7168, n=128)
+        xs5 = [to_t(x5).to(dev) for _ in range(2)]
+        rows, cols = x5.shape
+        for n in (16, 64, 256):
+            for grid in ("e1m2", "int4", "e2m1"):
+                for block, fmt in (((1, 16), ufp4.SCALE_FP32), ((1, 32), ufp4.SCALE_FP32),
+                                   ((32, 32), ufp4.SCALE_UE8M0)):
+                    for rnd in (ufp4.ROUND_RTNE, ufp4.ROUND_SR):
+                        desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
+                                              rounding=rnd, sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
+                        out = ufp4.alloc_quantized(rows, cols, desc, dev)
+                        q = ufp4.qtensor(*out, rows, cols)
+                        ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
+                        gbs = rows * cols * (2 + 0.5 + scale_bytes(desc)) / (ms / 1e3) / 1e9
+                        emit("quantize_sweep", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
+                             f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs, "GB/s",
+                             gbs / pk["hbm"], pk["hbm"], ms=ms)
+                        del out, q
         del xs5
 
     if "rowcol" in sections:
@@ -694,8 +718,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--suite", action="store_true",
                     help="further measurements (other workloads, widened rows), one JSON line each")
-    ap.add_argument("--suite-sections", default="dense,rowwise,rowcol,diag,gemm,moe",
-                    help="comma-separated subset of the suite: dense, rowwise, rowcol, diag, gemm, moe")
+    ap.add_argument("--suite-sections", default="dense,rowwise,sweep,rowcol,diag,gemm,moe",
+                    help="comma-separated subset of the suite: dense, rowwise, sweep, rowcol, diag, gemm, moe")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

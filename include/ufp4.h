@@ -381,10 +381,27 @@ ufp4_status ufp4_gemm_noalloc(const ufp4_qtensor* A, const ufp4_qtensor* B, cons
  * for consumers that apply the rotation themselves. */
 ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host);
 
-/* ufp4_device_error -- reads and clears the library's device error word on
- * the current device (synchronizes the device).  *code = 0 when no bounded
- * wait has given up since the last call. */
+/* ufp4_device_error -- reads and clears the library's device error words on
+ * the current device (synchronizes the device first).  Every device-side wait
+ * of the library is bounded: a kernel whose wait gives up records the event,
+ * lets its copies in flight land, releases what it holds and returns, leaving
+ * its outputs unspecified.  Returns UFP4_ERR_TIMEOUT, with *code = 1, when
+ * such a wait has given up since the last call, and UFP4_OK with *code = 0
+ * otherwise (UFP4_ERR_CUDA if the device cannot be read).  The library does
+ * not check the words on its other calls, which never synchronize. */
 ufp4_status ufp4_device_error(int32_t* code);
+
+/* ufp4_set_quantize_wait_limit -- failure-detection hook (no counterpart in
+ * the pages).  Sets how many times the quantizer kernels poll for a tile's
+ * arrival before they give up, on the current device, for later launches;
+ * polls < 0 restores the default (2^24 polls, seconds).  With polls = 0 the
+ * first wait of every quantizer CTA gives up at once: the kernel records the
+ * timeout, waits (with the default limit) for the copies it has started and
+ * returns, so tests can exercise the timeout path without hanging or faulting
+ * the GPU; ufp4_device_error then returns UFP4_ERR_TIMEOUT.  Synchronizes the
+ * device; do not call it while quantizer work is in flight on another
+ * thread. */
+ufp4_status ufp4_set_quantize_wait_limit(int64_t polls);
 
 /* ufp4_status_string -- static, human-readable name of a status code. */
 const char* ufp4_status_string(ufp4_status status);

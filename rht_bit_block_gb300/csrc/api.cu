@@ -55,6 +55,19 @@ void make_sign_bits(uint64_t seed, int n, uint32_t bits[8]) {
         if (base[i % n]) bits[i / 32] |= 1u << (i % 32);
 }
 
+// The ten round keys of Philox4x32-10 (Salmon et al., SC'11) for a seed.
+SrKeys sr_round_keys(uint64_t seed) {
+    SrKeys k;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int i = 0; i < 10; ++i) {
+        k.k[2 * i] = k0;
+        k.k[2 * i + 1] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    return k;
+}
+
 bool is_pow2(int64_t v) { return v >= 1 && (v & (v - 1)) == 0; }
 
 float inv_sqrt_n(int n) { return (float)(1.0 / std::sqrt((double)n)); }
@@ -175,6 +188,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     p.inv_sqrt_n = inv_sqrt_n(n);
     make_sign_bits(desc->sign_seed, n, p.sign_bits);
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
+    p.sr_keys = sr_round_keys(p.sr_seed);
     p.group = desc->group;
     if (desc->scale_fmt == UFP4_SCALE_E4M3)  // two-level: the tensor amax pre-pass first
         for (int i = 0; i < k; ++i) {
@@ -262,7 +276,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     p.col_seg_lanes = seg_lanes;
     p.amax_slots = bs.is2d ? (tr / bs.b2d) * (tc / bs.b2d) : 0;
     p.tile_rows = tr;
-    p.stages = std::max(2, std::min(6, (64 * 1024) / (tr * tc * 2)));  // about 64 KB of tiles per CTA, 3 CTAs per SM
+    p.stages = std::max(2, std::min(6, (96 * 1024) / (tr * tc * 2)));  // about 96 KB of tiles per CTA, 2 CTAs per SM
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
     p.lbw_row = ilog2(bs.bw);
     p.lbw_col = ilog2(bs.bw);
@@ -272,6 +286,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     while ((1 << (2 * p.log4n)) < n) ++p.log4n;
     p.pow4 = (1 << (2 * p.log4n)) == n;
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
+    p.sr_keys = sr_round_keys(p.sr_seed);
     p.do_row = do_row;
     p.do_col = do_col;
     p.vec256 = aligned(x, 32) && (ld % 16 == 0);
@@ -374,6 +389,13 @@ const char* ufp4_status_string(ufp4_status s) {
         case UFP4_ERR_TIMEOUT: return "UFP4_ERR_TIMEOUT";
     }
     return "UFP4_ERR_UNKNOWN";
+}
+
+ufp4_status ufp4_set_quantize_wait_limit(int64_t polls) {
+    if (polls > (int64_t)0xFFFFFFFF) return UFP4_ERR_INVALID_ARG;
+    ensure_loaded();
+    if (cudaDeviceSynchronize() != cudaSuccess) return UFP4_ERR_CUDA;
+    return cuda_status(set_quant_wait_limit(polls < 0 ? quant_wait_limit_default() : (uint32_t)polls));
 }
 
 ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host) {

@@ -1633,5 +1633,5 @@ extern "C" ufp4_status ufp4_device_error(int32_t* code) {
     int q = 0;
     if (ufp4::quant_error_read_clear(&q) != cudaSuccess) return UFP4_ERR_CUDA;
     *code = v ? v : q;
-    return UFP4_OK;
+    return *code ? UFP4_ERR_TIMEOUT : UFP4_OK;
 }

@@ -43,6 +43,14 @@ struct SignBits {
     uint32_t bits[8];  // bit i set <=> eps_{i mod n} = -1, for i in 0..255
 };
 
+// Round keys of Philox4x32-10 for one SR seed, computed on the host:
+// k[2i] = seed lo + i * 0x9E3779B9, k[2i + 1] = seed hi + i * 0xBB67AE85
+// (i = 0..9).  As kernel parameters they sit in the constant bank, where the
+// XOR of each round reads them directly.
+struct SrKeys {
+    uint32_t k[20];
+};
+
 struct QOut {
     void* codes;
     void* scales;
@@ -66,6 +74,7 @@ struct QuantParams {
     int lbw_row, lbw_col, lb2d, lseg;  // log2 of block widths, 2-D side and col_seg_lanes
     int pow4, log4n;    // n = 4^log4n: 1/sqrt(n) is a power of two
     uint64_t sr_seed;
+    SrKeys sr_keys;
     int do_row, do_col, vec256, col_grouped;
     QOut row, col;
     int col_tiles;
@@ -101,6 +110,7 @@ struct RowsParams {
     float inv_sqrt_n;
     uint32_t sign_bits[8];
     uint64_t sr_seed;
+    SrKeys sr_keys;
     int group;
 };
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st);
@@ -108,6 +118,10 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int n
 cudaError_t launch_tensor_amax(const uint16_t* x, int64_t rows, int64_t cols, int64_t ld, int n, float inv_sqrt_n,
                                const uint32_t sign_bits[8], float* amax, int num_sms, cudaStream_t st);
 cudaError_t quant_error_read_clear(int* value);
+// Polls of a tile barrier before the quantizer kernels give up (device-wide;
+// the default is restored by passing quant_wait_limit_default()).
+cudaError_t set_quant_wait_limit(uint32_t polls);
+uint32_t quant_wait_limit_default();
 
 // 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,
 // pitch bytes between rows, boxes of box_inner x box_outer elements.

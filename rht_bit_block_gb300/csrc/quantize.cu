@@ -30,7 +30,7 @@ __device__ int g_quant_error;
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kMaxStages = 6;               // TMA ring depth
-constexpr int kCtasPerSm = 3;               // 24 warps per SM; the ring holds about 64 KB per CTA
+constexpr int kCtasPerSm = 2;               // 16 warps per SM, up to 128 registers a thread; about 96 KB of ring per CTA
 constexpr uint32_t kWaitLimit = 1u << 24;   // bounded mbarrier polling
 
 __device__ __forceinline__ int find_group(const QuantParams& p, int row_tile) {
@@ -55,8 +55,13 @@ __device__ __forceinline__ uint32_t smem_addr(const void* ptr) {
     return (uint32_t)__cvta_generic_to_shared(ptr);
 }
 
-__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i) {
+// Polls of a tile's barrier before a quantizer kernel gives up (a failure-
+// detection hook can lower it; the drain of copies in flight always uses
+// kWaitLimit).
+__device__ uint32_t g_quant_wait_limit = kWaitLimit;
+
+__device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i) {
         uint32_t ok;
         asm volatile(
             "{ .reg .pred q; mbarrier.try_wait.parity.shared::cta.b64 q, [%1], %2; selp.u32 %0, 1, 0, q; }"
@@ -75,6 +80,37 @@ struct Fold {
     bool pow4;     // n = 4^j: 1/sqrt n = 2^-j folds exactly into the block reciprocal
     int j;         // log4 n when pow4
 };
+
+// The UE8M0 byte e + 127 of a block amax M: e is the smallest integer with
+// M <= qmax * 2^e (exact form of the truncation-free scale).  With M = m 2^E
+// (m in [1,2)) and qmax = mq 2^Eq: e = E - Eq + (m > mq), and the comparison
+// is the carry of M's mantissa + (2^23 - 1 - mq) into the exponent field, so
+// the byte is one add and one shift of M's bits; a zero block gives 0.
+// MXFP8 (GRID 4) takes e = floor(log2 M) - 8 instead: the same formula with
+// Eq = 8 and mq = 2^23 - 1 (no carry).  Blocks whose amax is nonzero but
+// below 2^-120 or above 2^120 are outside the input contract and are not
+// special-cased.
+template <int GRID>
+__device__ __forceinline__ int po2_byte(float M) {
+    constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : (GRID == 4 ? 8 : 2));
+    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : (GRID == 4 ? 0x7FFFFFu : 0x600000u));
+    constexpr uint32_t add = (0x7FFFFFu - mq) - ((uint32_t)Eq << 23);
+    return max((int)(__float_as_uint(M) + add) >> 23, 0);
+}
+
+// Eight level offsets o_i = k_i + 8 (the low nibbles of v_i = bits of
+// fp32(1.5 * 2^23 + 8 + k_i)) packed into one word, element i in bits 4i..4i+3.
+// Every v_i is E + o_i with E = 0x4B400000 and o_i < 16, so a tree of
+// multiply-adds (x16, x256, x65536) lines the nibbles up and leaves the
+// constant E (17 * 257 * ...) in bits 22 and up, removed at the end.
+__device__ __forceinline__ uint32_t pack_offsets8(const uint32_t* v) {
+    constexpr uint32_t E = 0x4B400000u;
+    constexpr uint32_t bias = E * 17u * 257u;  // mod 2^32; the low 22 bits are zero
+    const uint32_t p0 = v[1] * 16u + v[0], p1 = v[3] * 16u + v[2];
+    const uint32_t p2 = v[5] * 16u + v[4], p3 = v[7] * 16u + v[6];
+    const uint32_t q0 = p1 * 256u + p0, q1 = p3 * 256u + p2;
+    return q1 * 65536u + q0 - bias;
+}
 
 // Scale, round, pack and store two 16-element vectors a and b held as pairs
 // e[i] = (a_i, b_i) of transformed values before the 1/sqrt(n) multiply
@@ -105,12 +141,11 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
         const float r = s == 0.0f ? 0.0f : __frcp_rn(s);
         return __fmul_rn(r, pow2_exact(lf + lj));
     } else if (SF == 1) {
-        const int eb = scale_po2_byte<GRID>(Mz);  // e + 127
+        const int eb = po2_byte<GRID>(Mz);  // e + 127
         if (write) *sptr = (uint8_t)eb;
-        // 2^(-e + lf + lj) from its biased exponent (a subnormal below 1;
-        // capped at 2^127, reached only by blocks outside the input contract)
-        const int kb = min(254 - eb + lf + lj, 254);
-        return __uint_as_float(kb >= 1 ? (uint32_t)kb << 23 : 1u << (kb + 22));
+        // 2^(-e + lf + lj) from its biased exponent: a normal number for every
+        // block inside the input contract (|lf + lj| <= 6, eb <= 248)
+        return __uint_as_float((uint32_t)(254 + lf + lj - eb) << 23);
     } else {
         float sc, r;
         scale_fp32(Mz, qmax, sc, r);
@@ -126,35 +161,44 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
 // floor(v) * 2^16, so the level index is k = (ceil(v * 2^16) + 2^16 - 1 - u)
 // >> 16 (floor(v) or floor(v) + 1), and ceil(v * 2^16) is the low mantissa
 // bits of one fma rounded upward, v * 2^16 + 2^23 (exact: v * 2^16 < 2^23).
-template <int GRID>
-__device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uint64_t lin0, uint32_t stream,
+// Each nibble is sign * 8 + k (sign-magnitude), the nibbles line up through a
+// tree of multiply-adds, and a zero level loses its sign word-wise.  CLAMP:
+// |t| may exceed the largest level by an ulp (fp32 and two-level scales);
+// with UE8M0 scales |t| <= qmax holds exactly.
+template <int GRID, bool CLAMP>
+__device__ __forceinline__ uint2 sr_vec(const float t[16], const SrKeys& keys, uint64_t lin0, uint32_t stream,
                                         uint32_t group) {
     constexpr float qmax = grid_qmax(GRID);
     uint32_t w[8];
-    sr_draws16(sr_seed, lin0, stream, group, w);
-    uint32_t out[2] = {0u, 0u};
+    sr_draws16(keys, lin0, stream, group, w);
+    uint32_t nib[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
         const float ti = t[i];
-        // E2M1 values are in level units (largest qmax), uniform ones in steps (largest 7)
-        const float a = fminf(fabsf(ti), GRID >= 2 ? qmax : 7.0f);
         uint32_t idx;
         if (GRID >= 2) {
             // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
+            const float a = fminf(fabsf(ti), qmax);
             const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
             const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
             const uint32_t vb = __float_as_uint(__fmaf_ru(__fmul_rn(a, inv), 65536.0f, 8388608.0f));
             const uint32_t k = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
             idx = cvt_e2m1x2(0.0f, __fmul_rn((float)k, gap)) & 7u;
         } else {
-            // uniform grids: t is already in units of the step
+            // uniform grids: t is already in units of the step (largest level 7)
+            const float a = CLAMP ? fminf(fabsf(ti), 7.0f) : fabsf(ti);
             const uint32_t vb = __float_as_uint(__fmaf_ru(a, 65536.0f, 8388608.0f));
             idx = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
         }
-        const uint32_t neg = __float_as_uint(ti) >> 31;
-        out[i >> 3] |= (idx == 0 ? 0u : ((neg << 3) | idx)) << (4 * (i & 7));
+        nib[i] = (__float_as_uint(ti) >> 31) * 8u + idx;
     }
+    auto pack8 = [](const uint32_t* v) {
+        const uint32_t q0 = (v[3] * 16u + v[2]) * 256u + (v[1] * 16u + v[0]);
+        const uint32_t q1 = (v[7] * 16u + v[6]) * 256u + (v[5] * 16u + v[4]);
+        return q1 * 65536u + q0;
+    };
+    uint32_t out[2] = {clear_negative_zero(pack8(nib)), clear_negative_zero(pack8(nib + 8))};
     if (GRID == 1) {
         out[0] = signmag_to_twos(out[0]);
         out[1] = signmag_to_twos(out[1]);
@@ -165,7 +209,7 @@ __device__ __forceinline__ uint2 sr_vec(const float t[16], uint64_t sr_seed, uin
 template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B,
-                                          uint64_t sr_seed, uint32_t stream, uint32_t group) {
+                                          const SrKeys& sr_keys, uint32_t stream, uint32_t group) {
     // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
     // to the value in units of the grid step (below): INT4 k, E1M2 4 t
     constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
@@ -209,32 +253,29 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         // factor 4 = 1 / step), so one fma t + (1.5 * 2^23 + 8) rounds t to the
         // nearest integer k, ties to even (the addend is even and the result's
         // unit is 1), and its low nibble is o = k + 8 (|k| <= 7: the
-        // truncation-free scale keeps |t| <= 7).  Pairs of nibbles merge with
-        // one multiply-add (bits 4..7 of k + 8 are clear).  INT4: flipping
+        // truncation-free scale keeps |t| <= 7).  The offsets line up through
+        // a tree of multiply-adds (pack_offsets8).  INT4: flipping
         // bit 3 of o gives the two's complement nibble of k.  E1M2: o >= 8
         // (k >= 0) becomes o - 8 = k; o < 8 (k < 0) becomes (o ^ 15) + 1 =
         // 8 + |k|, the sign-magnitude nibble, and k = 0 is +0.
+        const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1), cc = pk2(12582920.0f, 12582920.0f);
         uint32_t va[16], vb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float a, b;
-            up2(e[i], a, b);
-            va[i] = __float_as_uint(__fmaf_rn(a, i < 8 ? ra0 : ra1, 12582920.0f));
-            vb[i] = __float_as_uint(__fmaf_rn(b, i < 8 ? rb0 : rb1, 12582920.0f));
+            up2(fma2(e[i], i < 8 ? q0 : q1, cc), a, b);
+            va[i] = __float_as_uint(a);
+            vb[i] = __float_as_uint(b);
         }
-        auto pack8 = [](const uint32_t* v) {
-            const uint32_t p0 = v[1] * 16u + v[0], p1 = v[3] * 16u + v[2];
-            const uint32_t p2 = v[5] * 16u + v[4], p3 = v[7] * 16u + v[6];
-            uint32_t x, y, w;
-            asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(x) : "r"(p0), "r"(p1));
-            asm("prmt.b32 %0, %1, %2, 0x0040;" : "=r"(y) : "r"(p2), "r"(p3));
-            asm("prmt.b32 %0, %1, %2, 0x5410;" : "=r"(w) : "r"(x), "r"(y));
+        auto finish = [](uint32_t w) {
             if (GRID == 1) return w ^ 0x88888888u;
             const uint32_t neg = ((w >> 3) & 0x11111111u) ^ 0x11111111u;  // per nibble: 1 iff o < 8
             return (w ^ (neg * 7u + 0x88888888u)) + neg;
         };
-        if (A.valid) *reinterpret_cast<uint2*>(A.codes) = make_uint2(pack8(va), pack8(va + 8));
-        if (B.valid) *reinterpret_cast<uint2*>(B.codes) = make_uint2(pack8(vb), pack8(vb + 8));
+        if (A.valid)
+            *reinterpret_cast<uint2*>(A.codes) = make_uint2(finish(pack_offsets8(va)), finish(pack_offsets8(va + 8)));
+        if (B.valid)
+            *reinterpret_cast<uint2*>(B.codes) = make_uint2(finish(pack_offsets8(vb)), finish(pack_offsets8(vb + 8)));
         return;
     }
     const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
@@ -243,8 +284,8 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
     for (int i = 0; i < 16; ++i) up2(mul2(e[i], i < 8 ? q0 : q1), ta[i], tb[i]);
     uint2 ca, cb;
     if (SR) {
-        ca = sr_vec<GRID>(ta, sr_seed, A.lin0, stream, group);
-        cb = sr_vec<GRID>(tb, sr_seed, B.lin0, stream, group);
+        ca = sr_vec<GRID, SF != 1>(ta, sr_keys, A.lin0, stream, group);
+        cb = sr_vec<GRID, SF != 1>(tb, sr_keys, B.lin0, stream, group);
     } else {
         ca = make_uint2(rtne8<GRID>(ta[0], ta[1], ta[2], ta[3], ta[4], ta[5], ta[6], ta[7]),
                         rtne8<GRID>(ta[8], ta[9], ta[10], ta[11], ta[12], ta[13], ta[14], ta[15]));
@@ -331,6 +372,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     // read buffers this one writes: wait for it before the first copy
     griddep_wait();
     griddep_launch();
+    const uint32_t wait_limit = g_quant_wait_limit;
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
@@ -355,6 +397,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     const int lncb = 1 + lS;                 // log2((TC/2) / (32/S)) for TC = 128
     const int ncb_mask = (1 << lncb) - 1;
     const int col_tasks = TR * TC / (kChunk * 64 * kWarps);  // per warp
+    // a thread's row chunks are all lane % S modulo S, and the signs repeat
+    // every n = 16 S elements (or every 16 when n <= 16): one mask set serves
+    SignMasks mc;
+    make_masks(chunk_signs(p, (lane & (S - 1)) * kChunk), mc);
     const int nslot = p.amax_slots;
     // tile coordinates advance by gridDim.x tiles per step, without division
     const int step_r = gridDim.x / p.col_tiles, step_c = gridDim.x - step_r * p.col_tiles;
@@ -376,7 +422,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             }
             if (p.num_groups > 1) g = find_group(p, row_tile);
         }
-        const bool landed = wait_phase(bars + 8u * s, phase);
+        const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
         if (!__syncthreads_and(landed)) {
             if (tid == 0) atomicExch(&g_quant_error, 1);
             break;
@@ -466,7 +512,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     B.w1 = (lbr & bmask) == 0 && lb == 3;
                     A.lin0 = (uint64_t)la * (uint64_t)p.cols + (uint64_t)col;
                     B.lin0 = (uint64_t)lbr * (uint64_t)p.cols + (uint64_t)col;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 0u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 0u, grp_id);
                 }
             } else {
                 const bool wsc = (col & ((1 << lbw) - 1)) == 0;
@@ -504,7 +550,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     A.w1 = B.w1 = false;
                     A.lin0 = lin + (uint64_t)(2 * it) * lstep;
                     B.lin0 = A.lin0 + lstep;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 0u, grp_id);
                 }
             }
         }
@@ -525,8 +571,6 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
                     const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    SignMasks mc;
-                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
                     uint32_t gw[16];
                     uint64_t e[16];
                     gather_pair<TC>(tile_s, tcol, rchunk, gw);
@@ -553,8 +597,6 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
                     const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    SignMasks mc;
-                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
                     uint32_t gw[16];
                     uint64_t e[16];
                     gather_pair<TC>(tile_s, tcol, rchunk, gw);
@@ -584,7 +626,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     B.w1 = (cb & bmask) == 0 && lb == 3;
                     A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
                     B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_seed, 1u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 1u, grp_id);
                 }
             } else {
                 const int bwc = 1 << lbwc;
@@ -592,8 +634,6 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
                     const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    SignMasks mc;
-                    make_masks(chunk_signs(p, rchunk * kChunk), mc);
                     uint32_t gw[16];
                     uint64_t e[16];
                     gather_pair<TC>(tile_s, tcol, rchunk, gw);
@@ -615,7 +655,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     A.w1 = B.w1 = false;
                     A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
                     B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 1u, grp_id);
+                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 1u, grp_id);
                 }
             }
         }
@@ -639,7 +679,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         for (int k = i; k < i + kStages; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
             if (tile >= num_tiles) break;
-            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1));
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
         }
 }
 
@@ -653,8 +693,10 @@ struct RowsMaps {
     CUtensorMap m[kMaxBatch];
 };
 
-template <int GRID, bool SR, int SF>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+// N16: n = 16 (the FPROP operands' case), with the four butterfly strides
+// fixed at compile time.
+template <int GRID, bool SR, int SF, bool N16, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
     constexpr int TC = 128, TR = 128;
     constexpr int kTileBytes = TR * TC * 2;
@@ -711,6 +753,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     __syncthreads();
     griddep_wait();
     griddep_launch();
+    const uint32_t wait_limit = g_quant_wait_limit;
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
@@ -739,7 +782,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             }
             if (rt >= p.t[t].row_tiles) relocate(tile);  // into the next tensor
         }
-        const bool landed = wait_phase(bars + 8u * s, phase);
+        const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
         if (!__syncthreads_and(landed)) {
             if (tid == 0) atomicExch(&g_quant_error, 1);
             break;
@@ -770,9 +813,18 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
             wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
             widen_rows(wa, wb, mrow, e);
-            fwht_pair(e, n, seg_row);
             float Ma, Mb;
-            amax_1d_pair(e, 1 << lbw, Ma, Mb);
+            if (N16) {
+                fwht_pair16(e);
+                amax_pair(e, 0, 16, Ma, Mb);
+                if (lbw == 5) {  // 1 x 32 blocks: the neighbouring lane holds the other half
+                    Ma = fmaxf(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, 1));
+                    Mb = fmaxf(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, 1));
+                }
+            } else {
+                fwht_pair(e, n, seg_row);
+                amax_1d_pair(e, 1 << lbw, Ma, Mb);
+            }
             Dest A, B;
             A.codes = cp + (2 * it) * cstep;
             B.codes = A.codes + cstep;
@@ -784,7 +836,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             A.w1 = B.w1 = false;
             A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
             B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
-            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_seed, 0u, (uint32_t)p.group);
+            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
         }
         // everyone is done with stage s: refill it
         __syncthreads();
@@ -805,7 +857,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
         for (int k = i; k < i + kStages; ++k) {
             const int tile = blockIdx.x + k * gridDim.x;
             if (tile >= p.num_tiles) break;
-            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1));
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
         }
 }
 
@@ -884,14 +936,28 @@ cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, i
     return cudaErrorInvalidValue;
 }
 
-template <int GRID, bool SR, int SF>
-static cudaError_t launch_rows(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
+// CTAs per SM and ring depth of the row kernel (128 x 128 tiles): two CTAs
+// of up to 128 registers a thread, each with three 32 KB stages (measured on
+// the 16384 x 7168 + 7168 x 7168 batch: 6.13 TB/s, against 5.87 TB/s for
+// three CTAs of two stages, whose 80-register cap costs 1.6 instructions per
+// element in register moves).
+constexpr int kRowsCtas = 2, kRowsStages = 3;
+
+template <int GRID, bool SR, int SF, bool N16, int CTAS>
+static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
     const size_t smem = (size_t)p.stages * 128 * 128 * 2 + 8 * p.stages + 128;
-    auto k = quantize_rows_kernel<GRID, SR, SF>;
+    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_tiles < kCtasPerSm * num_sms ? p.num_tiles : kCtasPerSm * num_sms;
+    const int grid = p.num_tiles < CTAS * num_sms ? p.num_tiles : CTAS * num_sms;
     return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
+}
+
+template <int GRID, bool SR, int SF>
+static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
+    p.stages = kRowsStages;
+    if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas>(maps, p, num_sms, st);
+    return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas>(maps, p, num_sms, st);
 }
 
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
@@ -919,6 +985,12 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int n
 #undef UFP4_R
     if (grid == 4 && !sr && sf == 1) return launch_rows<4, false, 1>(maps, p, num_sms, st);  // MXFP8
     return cudaErrorInvalidValue;
+}
+
+uint32_t quant_wait_limit_default() { return kWaitLimit; }
+
+cudaError_t set_quant_wait_limit(uint32_t polls) {
+    return cudaMemcpyToSymbol(g_quant_wait_limit, &polls, sizeof(polls));
 }
 
 cudaError_t quant_error_read_clear(int* value) {
@@ -954,9 +1026,12 @@ static void preload_q(cudaFuncAttributes* a) {
 }
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, true, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas>);
 }
 template <int G>
 static void preload_grid(cudaFuncAttributes* a) {
@@ -973,7 +1048,8 @@ cudaError_t preload_quantize_kernels() {
     preload_grid<1>(&a);
     preload_grid<2>(&a);
     preload_grid<3>(&a);
-    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas>);
     return cudaFuncGetAttributes(&a, rht_kernel);
 }
 

@@ -53,19 +53,17 @@ __device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
 
 // ------------------------------------------------------------- Philox4x32-10
 // Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
-// bumped by 0x9E3779B9 / 0xBB67AE85 between rounds.  Each product is one
-// 32 x 32 -> 64-bit multiply (both halves at once).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// bumped by 0x9E3779B9 / 0xBB67AE85 between rounds (the round keys come
+// precomputed, see SrKeys).  Each product is one 32 x 32 -> 64-bit multiply
+// (both halves at once).
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const SrKeys& k) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        if (i) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
         uint64_t p0, p1;
         asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
         asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1, (uint32_t)p0);
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k[2 * i], (uint32_t)p1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ k.k[2 * i + 1], (uint32_t)p0);
     }
     return c;
 }
@@ -73,13 +71,12 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
 // Sixteen 16-bit SR draws for output elements lin0 .. lin0+15 (lin0 % 8 == 0):
 // counter (g lo, g hi, stream, group) with g = lin / 8; element j of a group
 // of eight takes the low half of word j/2 when j is even, the high half when odd.
-__device__ __forceinline__ void sr_draws16(uint64_t seed, uint64_t lin0, uint32_t stream,
-                                           uint32_t group, uint32_t w[8]) {
+__device__ __forceinline__ void sr_draws16(const SrKeys& k, uint64_t lin0, uint32_t stream, uint32_t group,
+                                           uint32_t w[8]) {
     const uint64_t g = lin0 >> 3;
-    const uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-    const uint4 a = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, group), k0, k1);
+    const uint4 a = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, group), k);
     const uint64_t g1 = g + 1;
-    const uint4 b = philox4x32_10(make_uint4((uint32_t)g1, (uint32_t)(g1 >> 32), stream, group), k0, k1);
+    const uint4 b = philox4x32_10(make_uint4((uint32_t)g1, (uint32_t)(g1 >> 32), stream, group), k);
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
     w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
 }
@@ -132,23 +129,6 @@ __device__ __forceinline__ void fwht16(float v[16], int n, int seg_lane) {
 __device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float& r) {
     s = __fdiv_rn(M, qmax);
     r = (s == 0.0f) ? 0.0f : __frcp_rn(s);
-}
-
-// Power-of-two scale: smallest e with M <= qmax * 2^e, clamped to
-// [-127, 127], returned as its UE8M0 byte e + 127.  With M = m * 2^E (m in
-// [1,2)) and qmax = mq * 2^Eq: e = E - Eq + (m > mq).  The comparison is the
-// carry of M's mantissa + (2^23 - 1 - mq) into the exponent field, so the
-// byte is one add and one shift of M's bits.  Zero (and a subnormal M,
-// outside the contract) gives byte 0.
-// MXFP8 (GRID 4) takes e = floor(log2 M) - 8 instead: the same formula with
-// Eq = 8 and mq = 2^23 - 1 (no carry).
-template <int GRID>
-__device__ __forceinline__ int scale_po2_byte(float M) {
-    constexpr int Eq = (GRID == 0) ? 0 : (GRID == 3 ? 1 : (GRID == 4 ? 8 : 2));
-    constexpr uint32_t mq = (GRID == 2) ? 0x400000u : (GRID == 3 ? 0u : (GRID == 4 ? 0x7FFFFFu : 0x600000u));
-    const uint32_t b = __float_as_uint(M);
-    const int eb = (int)((b + (0x7FFFFFu - mq)) >> 23) - Eq;
-    return b < 0x00800000u ? 0 : min(max(eb, 0), 254);
 }
 
 __device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
@@ -334,6 +314,26 @@ __device__ __forceinline__ void fwht_pair(uint64_t e[16], int n, int seg_lane) {
             e[i] = upper ? sub2(o, e[i]) : add2(e[i], o);
         }
     }
+}
+
+// The same for n = 16: strides 1, 2, 4, 8, all inside the thread.
+__device__ __forceinline__ void fwht_pair16(uint64_t e[16]) {
+#pragma unroll
+    for (int h = 1; h < kChunk; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < kChunk; ++i) {
+            if (i & h) continue;
+            const uint64_t a = e[i], b = e[i + h];
+            e[i] = add2(a, b);
+            e[i + h] = sub2(a, b);
+        }
+    }
+}
+
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
 }
 
 // Tree amax of |a_i| and |b_i| over i in [lo, hi) (lo, hi multiples of 8).

@@ -14,6 +14,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libufp4.so")
 
 UFP4_OK = 0
+UFP4_ERR_TIMEOUT = 5
 STATUS_NAMES = {0: "UFP4_OK", 1: "UFP4_ERR_INVALID_ARG", 2: "UFP4_ERR_UNSUPPORTED",
                 3: "UFP4_ERR_ALIGNMENT", 4: "UFP4_ERR_CUDA", 5: "UFP4_ERR_TIMEOUT"}
 GRID_E1M2, GRID_INT4, GRID_E2M1 = 0, 1, 2
@@ -30,7 +31,7 @@ EXPORTED = (
     "ufp4_rht_transform", "ufp4_dequantize", "ufp4_gemm_workspace_size", "ufp4_gemm",
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
     "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
-    "ufp4_rht_quantize_batch", "ufp4_quant_error_stats", "ufp4_error_stats",
+    "ufp4_rht_quantize_batch", "ufp4_quant_error_stats", "ufp4_error_stats", "ufp4_set_quantize_wait_limit",
 )
 MAX_BATCH = 4
 
@@ -86,6 +87,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_gemm_grouped.argtypes = [i32, QT, QT, QD, ctypes.POINTER(P), ctypes.POINTER(i64), P, ctypes.c_size_t, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
     L.ufp4_device_error.argtypes = [ctypes.POINTER(i32)]
+    L.ufp4_set_quantize_wait_limit.argtypes = [i64]
+    L.ufp4_set_quantize_wait_limit.restype = ctypes.c_int
     L.ufp4_status_string.argtypes = [ctypes.c_int]
     L.ufp4_status_string.restype = ctypes.c_char_p
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
@@ -247,9 +250,25 @@ def ufp4_sign_vector(sign_seed: int, n: int):
 
 
 def ufp4_device_error() -> int:
+    """The device error code (0: no bounded wait gave up since the last read);
+    the C call returns UFP4_ERR_TIMEOUT exactly when the code is nonzero."""
     code = ctypes.c_int32(0)
-    _check(load().ufp4_device_error(ctypes.byref(code)), "ufp4_device_error")
+    st = load().ufp4_device_error(ctypes.byref(code))
+    if st not in (UFP4_OK, UFP4_ERR_TIMEOUT) or (st == UFP4_ERR_TIMEOUT) != (code.value != 0):
+        raise Ufp4Error(st, "ufp4_device_error")
     return int(code.value)
+
+
+def ufp4_device_error_status() -> int:
+    """The status ufp4_device_error returns (UFP4_OK or UFP4_ERR_TIMEOUT)."""
+    code = ctypes.c_int32(0)
+    return int(load().ufp4_device_error(ctypes.byref(code)))
+
+
+def ufp4_set_quantize_wait_limit(polls: int):
+    """Failure-detection hook: polls of a tile barrier before the quantizer
+    kernels give up (negative: the default)."""
+    _check(load().ufp4_set_quantize_wait_limit(polls), "ufp4_set_quantize_wait_limit")
 
 
 def ufp4_status_string(status: int) -> str:

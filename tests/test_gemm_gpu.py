@@ -93,8 +93,11 @@ def test_gemm_random_scales(grid, block, shape):
 
 @pytest.mark.parametrize("grid", FP8_GRIDS)
 def test_gemm_wide_scale_gap(grid):
-    """Neighbouring 1 x 16 blocks 20-30 binades apart: the smaller block's
-    elements fall below E5M2's range and round; the error stays far below the bar."""
+    """Neighbouring 1 x 16 blocks 27 binades apart: the smaller block's
+    elements fall below E5M2's range and round.  Besides the relative bar, each
+    output stays within the stated bound: per product term at most 2^-17 of
+    the pair's hardware scale (2^(e_max - 2) for E1M2, 2^e_max for INT4) times
+    |B|, plus the fp32 accumulation."""
     M, N, K = 256, 256, 512
     rng = np.random.default_rng(5)
     ac, asc = _rand_operand(rng, M, K, grid, (1, 16), lo=127, hi=127)
@@ -103,6 +106,16 @@ def test_gemm_wide_scale_gap(grid):
     D = _gemm(ac, asc, bc, bsc, M, N, K, grid, (1, 16))
     ref = orc.gemm_reference(ac, asc, bc, bsc, grid=grid, block=(1, 16))
     assert _rel(D, ref) <= TOL
+    da = orc.dequantize_f64(ac, asc, grid=grid, block=(1, 16))
+    db = orc.dequantize_f64(bc, bsc, grid=grid, block=(1, 16))
+    e = asc.astype(np.int64) - 127
+    e_pair = np.maximum(e[:, 0::2], e[:, 1::2])                       # per 32 elements
+    gap = np.repeat(e_pair, 2, axis=1) - e                            # binades below the pair's max
+    hw = 2.0 ** (np.repeat(e_pair, 2, axis=1) - (2 if grid == "e1m2" else 0))
+    term = np.where(gap > 16, 2.0 ** -17 * hw, 0.0)  # per 16-element block: exact up to 16 binades
+    bound = np.repeat(term, 16, axis=1) @ np.abs(db).T
+    slack = 2.0 ** -20 * (np.abs(da) @ np.abs(db).T)
+    assert (np.abs(D - ref) <= bound + slack).all()
 
 
 def _quantized(x, grid, block, colwise=False, rounding=orc.RTNE):

@@ -229,27 +229,31 @@ def test_dy_sr_row_and_col_full_size():
     assert_bitwise(got["col"][1], s, "W column-wise scales")
 
 
+SWEEP_CELLS = [(grid, block, fmt, rnd) for grid in ("e1m2", "int4", "e2m1")
+               for block, fmt in (((1, 16), FP32), ((1, 32), FP32), ((32, 32), PO2))
+               for rnd in (RTNE, SR)]
+
+
 @pytest.mark.parametrize("n", [16, 64, 256])
 def test_large_sweep_sampled_rows(n):
-    """MoE-124B-like X 16384 x 7168: a sample of the quantizer sweep, checked on
-    seeded bands of 64 rows (1-D blocks depend on their own row only; 2-D
-    32 x 32 blocks on their 32-row band)."""
+    """MoE-124B-like X 16384 x 7168, every cell of the quantizer sweep (grid x
+    block x rounding, here for one n): each checked on two seeded bands of 64
+    rows (1-D blocks depend on their own row only; 2-D 32 x 32 blocks on
+    their 32-row band)."""
     x, _ = inputs.large_sweep(k=7168, m=16384, n=7168)
     xd = to_dev(x)
     rng = np.random.default_rng(n)
-    bands = sorted(rng.choice(16384 // 64, size=4, replace=False))
-    combos = [("e1m2", (1, 16), FP32, RTNE), ("int4", (1, 32), FP32, SR), ("e2m1", (32, 32), PO2, RTNE),
-              ("e1m2", (32, 32), PO2, SR)]
-    for grid, block, fmt, rnd in combos:
+    for grid, block, fmt, rnd in SWEEP_CELLS:
         kw = dict(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, rounding=rnd,
                   sr_seed=inputs.SR_SEED, scale_fmt=fmt)
         got = gpu_quantize(xd, out_mask=ufp4.OUT_ROWWISE, **kw)
-        for b in bands:
+        for b in sorted(rng.choice(16384 // 64, size=2, replace=False)):
             r0 = int(b) * 64
             c, s = orc.quantize(x[r0:r0 + 64], row0=r0, **kw)
-            assert_bitwise(got["row"][0][r0:r0 + 64], c, f"{grid} {block} band {b} codes")
+            what = f"{grid} {block} {'SR' if rnd else 'RTNE'} n={n} band {b}"
+            assert_bitwise(got["row"][0][r0:r0 + 64], c, what + " codes")
             br = block[0]
-            assert_bitwise(got["row"][1][r0 // br:(r0 + 64) // br], s, f"{grid} {block} band {b} scales")
+            assert_bitwise(got["row"][1][r0 // br:(r0 + 64) // br], s, what + " scales")
 
 
 # ----------------------------------------- row-wise kernel and batched calls

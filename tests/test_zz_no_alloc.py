@@ -1,8 +1,11 @@
 """ufp4_gemm_noalloc, the GEMM entry point for callers that cannot allocate
-device memory (for example code under CUDA-graph capture or inside a host
-framework that owns all allocations): it must give the same result as
-ufp4_gemm with a caller-allocated workspace, on two calls in a row, through
-the C ABI.  This file is collected last on purpose."""
+device memory (for example a plugin or custom op whose host framework owns
+every device allocation, or a loop that must not risk the device-wide
+synchronization an allocation can cause): through the C ABI it must give
+exactly what ufp4_gemm gives with a caller-allocated workspace, call after
+call.  The first call has the largest footprint, so the later, smaller calls
+(other K and N) run over scratch bytes left behind by the earlier ones.  This
+file is collected last on purpose."""
 import numpy as np
 import pytest
 import torch
@@ -10,8 +13,6 @@ import torch
 from rht_bit_block_gb300 import inputs, ufp4
 
 pytestmark = pytest.mark.gpu
-
-TOL = 1e-5  # the relative Frobenius bar the GEMM tests use
 
 
 def _operands(seed, m, n, k, grid):
@@ -26,9 +27,10 @@ def _operands(seed, m, n, k, grid):
 
 
 @pytest.mark.parametrize("grid", ["e1m2", "e2m1"])
-def test_noalloc_matches_workspace_gemm_twice(grid):
+def test_noalloc_matches_workspace_gemm_call_after_call(grid):
     torch.cuda.init()
-    for call, (seed, m, n, k) in enumerate([(11, 640, 768, 1024), (12, 384, 512, 2048)]):
+    shapes = [(11, 1024, 1280, 4096), (12, 384, 512, 2048), (13, 256, 448, 1024)]
+    for call, (seed, m, n, k) in enumerate(shapes):
         desc, A, B, keep = _operands(seed, m, n, k, grid)
         ref = torch.empty((m, n), dtype=torch.float32, device="cuda")
         ws = torch.empty(max(1, ufp4.ufp4_gemm_workspace_size(m, n, k, desc)), dtype=torch.uint8, device="cuda")
@@ -37,10 +39,8 @@ def test_noalloc_matches_workspace_gemm_twice(grid):
         ufp4.ufp4_gemm_noalloc(A, B, desc, got)
         torch.cuda.synchronize()
         assert ufp4.ufp4_device_error() == 0
-        r = ref.double().cpu().numpy()
-        g = got.double().cpu().numpy()
-        rel = np.linalg.norm(g - r) / np.linalg.norm(r)
-        assert rel <= TOL, f"call {call}: relative error {rel}"
+        # the same kernels on the same operands: the results must agree bit for bit
+        assert torch.equal(got, ref), f"call {call}: noalloc result differs from ufp4_gemm"
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch():
