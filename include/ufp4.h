@@ -205,8 +205,9 @@ ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t
  * each host array describes tensor i exactly as the arguments of
  * ufp4_rht_quantize do (x: device bf16 rows[i] x cols[i], leading dimension
  * ld[i]; rowwise[i]: its row-wise output).  Requirements: 0 <= count <=
- * UFP4_MAX_BATCH, desc->out_mask == UFP4_OUT_ROWWISE, 1-D blocks, hadamard_n
- * <= 128 (UFP4_ERR_UNSUPPORTED otherwise), and per tensor the shape and
+ * UFP4_MAX_BATCH, desc->out_mask == UFP4_OUT_ROWWISE, 1-D blocks, and
+ * hadamard_n <= 128 for the two-level scale and MXFP8 (UFP4_ERR_UNSUPPORTED
+ * otherwise), and per tensor the shape and
  * alignment rules of ufp4_rht_quantize.  The results are bit-identical to
  * `count` separate ufp4_rht_quantize calls.  Nothing is written when any
  * argument is rejected. */

@@ -156,6 +156,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     std::memset(&p, 0, sizeof(p));
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
     const int n = desc->hadamard_n;
+    const int tc = n == 256 ? 256 : 128, tr = 16384 / tc;  // tile columns and rows
     int64_t tiles = 0;
     int k = 0;
     for (int i = 0; i < count; ++i) {
@@ -169,8 +170,8 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
         T.scales_ld = rowwise[i].scales_ld;
         T.rows = (int)rows[i];
         T.cols = (int)cols[i];
-        T.col_tiles = (int)((cols[i] + 127) / 128);
-        T.row_tiles = (int)((rows[i] + 127) / 128);
+        T.col_tiles = (int)((cols[i] + tc - 1) / tc);
+        T.row_tiles = (int)((rows[i] + tr - 1) / tr);
         T.tile0 = (int)tiles;
         T.amax = rowwise[i].tensor_amax;
         tiles += (int64_t)T.col_tiles * T.row_tiles;
@@ -179,6 +180,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     if (tiles > 0x7FFFFFFF) return UFP4_ERR_UNSUPPORTED;
     p.count = k;
     p.num_tiles = (int)tiles;
+    p.tc = tc;
     p.n = n;
     p.lbw = ilog2(bs.bw);
     p.log4n = 0;
@@ -251,7 +253,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if ((desc->scale_fmt == UFP4_SCALE_E4M3 || desc->grid == UFP4_GRID_MXFP8) &&
         (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) || cols >= (1LL << 31)))
         return UFP4_ERR_UNSUPPORTED;  // two-level scale and MXFP8: row-wise, 1-D blocks, n <= 128
-    if (do_row && !do_col && !bs.is2d && !grouped && n <= 128 && total_rows < (1LL << 31) && cols < (1LL << 31)) {
+    if (do_row && !do_col && !bs.is2d && !grouped && total_rows < (1LL << 31) && cols < (1LL << 31)) {
         const ufp4_qtensor* rw = rowwise;
         return quantize_rows_batch(1, &x, &total_rows, &cols, &ld, desc, bs, rw, stream);
     }
@@ -262,7 +264,10 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     const int seg_lanes = (bs.is2d ? std::max(n, 16) : std::max(std::max(n, bs.bw), 16)) / 16;
     // row-only work takes 128-row tiles (more elements per thread per tile);
     // the column pass takes 64-row tiles unless a segment spans 8 row chunks
-    const int tr = (do_col && seg_lanes < 8) ? 64 : (n == 256 ? 64 : 128);
+    // 2-D blocks take 64-row tiles where they can: one row pair (and one
+    // column task) per thread, whose values stay in registers across the
+    // block-amax barrier
+    const int tr = (do_col && seg_lanes < 8) ? 64 : ((n == 256 || (bs.is2d && !do_col)) ? 64 : 128);
     p.x = (const uint16_t*)x;
     p.cols = cols;
     p.ld = ld;
@@ -422,7 +427,9 @@ extern "C" ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const*
     if (count == 0) return UFP4_OK;
     if (!x || !rows || !cols || !ld || !rowwise) return UFP4_ERR_INVALID_ARG;
     if (desc->out_mask != UFP4_OUT_ROWWISE) return UFP4_ERR_INVALID_ARG;
-    if (bs.is2d || desc->hadamard_n > 128) return UFP4_ERR_UNSUPPORTED;
+    if (bs.is2d) return UFP4_ERR_UNSUPPORTED;
+    if (desc->hadamard_n > 128 && (desc->scale_fmt == UFP4_SCALE_E4M3 || desc->grid == UFP4_GRID_MXFP8))
+        return UFP4_ERR_UNSUPPORTED;  // two-level scale and MXFP8: n <= 128
     const int n = desc->hadamard_n;
     for (int i = 0; i < count; ++i) {
         if (rows[i] < 0 || cols[i] < 0) return UFP4_ERR_INVALID_ARG;

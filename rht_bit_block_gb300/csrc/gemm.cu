@@ -68,6 +68,10 @@ constexpr int kPairStagesFp4x2 = 5, kPairStagesFp4x4 = 4;
 // with one .32x128b.warpx4 per 512-byte chunk (false), or stored four times
 // and copied two chunks per .128x256b (true, the FP8 layout)
 constexpr bool kFp4Replicated = true;
+// Pair rows per tile group (see pair_tile_coords).  With 16 on the
+// 16384 x 7168 x 7168 FPROP, the tiles in flight touch about 16 A panels
+// (29 MB of FP8) and 5 B panels, A is read from DRAM once and B four times.
+constexpr int kPairGroupM = 16;
 __host__ __device__ constexpr bool pair_replicated(int kind) { return kind == 0 || kFp4Replicated; }
 
 // ------------------------------------------------------------ PTX wrappers
@@ -352,6 +356,7 @@ struct PairCfg {
 // one GEMM after the other.
 struct PairGroup {
     int M, N, k_tiles, m_pairs, n_tiles;
+    int group_m;          // tile order: groups of group_m pair rows, n fastest inside a group
     int tile0;            // index of this GEMM's first tile in the launch
     int64_t sf_chunks_k;  // chunks along K per 128-row block
     float* D;
@@ -373,6 +378,22 @@ struct PairKParams {
     float den;
     int two_level;
 };
+
+// Output tile (pair row mp, column block nb) of the GEMM's local tile index.
+// Tiles run in groups of group_m pair rows, the column block advancing
+// fastest inside a group: the 76 or so tiles in flight at a time then touch
+// about group_m A panels and a few B panels, which stay in L2 while the group
+// sweeps N, so A comes from DRAM once and B once per group (in plain
+// column-major order every column block re-read all of A).
+__device__ __forceinline__ void pair_tile_coords(const PairGroup& pg, int local, int& mp, int& nb) {
+    const int span = pg.group_m * pg.n_tiles;
+    const int g = local / span;
+    const int first = g * pg.group_m;
+    const int rows = min(pg.group_m, pg.m_pairs - first);
+    const int l = local - g * span;
+    nb = l / rows;
+    mp = first + (l - nb * rows);
+}
 
 template <int KIND, int STAGES, int KPS, int G>
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -448,7 +469,8 @@ gemm_pair_kernel(const __grid_constant__ PairMaps<G> maps, const __grid_constant
             const int gi = locate(tile, local);
             const PairGroup& q = p.g[gi];
             const CUtensorMap* tm = maps.m[gi];
-            const int mp = local % q.m_pairs, nb = local / q.m_pairs;
+            int mp, nb;
+            pair_tile_coords(q, local, mp, nb);
             const int k_stages = (q.k_tiles + KPS - 1) / KPS;
             const int ablk = 2 * mp + (int)peer;            // this CTA's 128-row block of A
             const int arow = ablk * kBM;
@@ -557,7 +579,8 @@ gemm_pair_kernel(const __grid_constant__ PairMaps<G> maps, const __grid_constant
             tc_fence_after();
             int local;
             const PairGroup& pg = p.g[locate(tile, local)];
-            const int mp = local % pg.m_pairs, nb = local / pg.m_pairs;
+            int mp, nb;
+            pair_tile_coords(pg, local, mp, nb);
             const int row = (2 * mp + (int)peer) * kBM + q * 32 + lane;
             // two-level scale: the product of the tensor scales (written by the quantizer before this launch)
             const float gab =
@@ -1390,6 +1413,7 @@ cudaError_t fill_pair_group(const GemmArgs& g, const Plan& pl, CUtensorMap* maps
     pg.N = (int)g.N;
     pg.k_tiles = (int)pl.k_tiles;
     pg.m_pairs = (int)((g.M + 2 * kBM - 1) / (2 * kBM));
+    pg.group_m = std::min(pg.m_pairs, kPairGroupM);
     pg.n_tiles = (int)((g.N + pl.bn - 1) / pl.bn);
     pg.sf_chunks_k = pl.chunks_k;
     pg.D = g.D;

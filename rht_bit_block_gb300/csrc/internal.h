@@ -88,7 +88,7 @@ struct QuantParams {
 cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
                             int64_t total_rows, int num_sms, cudaStream_t st);
 
-// Row-wise only, 1-D blocks, n <= 128: the lean kernel, over up to
+// Row-wise only, 1-D blocks, n <= 256: the lean kernel, over up to
 // kMaxBatch independent tensors in one launch.
 constexpr int kMaxBatch = 4;
 struct RowsTensor {
@@ -106,6 +106,7 @@ struct RowsTensor {
 struct RowsParams {
     RowsTensor t[kMaxBatch];
     int count, num_tiles;
+    int tc;             // tile columns: 128, or 256 for n = 256 (tiles of 16384 elements)
     int n, lbw, pow4, log4n, stages;
     float inv_sqrt_n;
     uint32_t sign_bits[8];

@@ -455,6 +455,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 const int bmask = (1 << lb) - 1;
                 for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
                 __syncthreads();
+                // with one row pair per thread (64-row tiles) the transformed values
+                // stay in registers while the block amax settles in shared memory;
+                // with two, the second pass transforms them again
+                uint64_t keep[16];
                 for (int it = 0; it < pairs; ++it) {
                     const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
                     uint32_t wa[8], wb[8];
@@ -463,6 +467,9 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     load_row_chunk<TC>(tile_s, rb, cchunk, wb);
                     widen_rows(wa, wb, mrow, e);
                     fwht_pair(e, n, seg_row);
+                    if (pairs == 1)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) keep[i] = e[i];
                     const int sa = (ra >> lb) << lnbc, sb = (rb >> lb) << lnbc;
                     if (lb == 3) {
                         float a0, b0, a1, b1;
@@ -482,12 +489,17 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 __syncthreads();
                 for (int it = 0; it < pairs; ++it) {
                     const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
-                    uint32_t wa[8], wb[8];
                     uint64_t e[16];
-                    load_row_chunk<TC>(tile_s, ra, cchunk, wa);
-                    load_row_chunk<TC>(tile_s, rb, cchunk, wb);
-                    widen_rows(wa, wb, mrow, e);
-                    fwht_pair(e, n, seg_row);
+                    if (pairs == 1) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) e[i] = keep[i];
+                    } else {
+                        uint32_t wa[8], wb[8];
+                        load_row_chunk<TC>(tile_s, ra, cchunk, wa);
+                        load_row_chunk<TC>(tile_s, rb, cchunk, wb);
+                        widen_rows(wa, wb, mrow, e);
+                        fwht_pair(e, n, seg_row);
+                    }
                     const int off = lb == 3 ? 2 * cchunk : ((cchunk * kChunk) >> lb);
                     const int sa = ((ra >> lb) << lnbc) + off, sb = ((rb >> lb) << lnbc) + off;
                     const float MA0 = __uint_as_float(amax2d[sa]);
@@ -567,6 +579,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 const int bmask = (1 << lb) - 1;
                 for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
                 __syncthreads();
+                uint64_t keep[16];
                 for (int k = 0; k < col_tasks; ++k) {
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
@@ -576,6 +589,9 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     gather_pair<TC>(tile_s, tcol, rchunk, gw);
                     widen_cols(gw, mc, e);
                     fwht_pair(e, n, rchunk & (S - 1));
+                    if (col_tasks == 1)
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) keep[i] = e[i];
                     const int sa = (tcol >> lb) << lnbq, sb = ((tcol + 1) >> lb) << lnbq;
                     if (lb == 3) {
                         float a0, b0, a1, b1;
@@ -597,11 +613,16 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
                     const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    uint32_t gw[16];
                     uint64_t e[16];
-                    gather_pair<TC>(tile_s, tcol, rchunk, gw);
-                    widen_cols(gw, mc, e);
-                    fwht_pair(e, n, rchunk & (S - 1));
+                    if (col_tasks == 1) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) e[i] = keep[i];
+                    } else {
+                        uint32_t gw[16];
+                        gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                        widen_cols(gw, mc, e);
+                        fwht_pair(e, n, rchunk & (S - 1));
+                    }
                     const int off = lb == 3 ? 2 * rchunk : ((rchunk * kChunk) >> lb);
                     const int sa = ((tcol >> lb) << lnbq) + off, sb = (((tcol + 1) >> lb) << lnbq) + off;
                     const float MA0 = __uint_as_float(amax2d[sa]);
@@ -695,10 +716,12 @@ struct RowsMaps {
 
 // N16: n = 16 (the FPROP operands' case), with the four butterfly strides
 // fixed at compile time.
-template <int GRID, bool SR, int SF, bool N16, int CTAS>
+// TC: tile columns, 128, or 256 for n = 256 (whose segments span 16 chunks);
+// the tiles hold 16 K elements either way.
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
-    constexpr int TC = 128, TR = 128;
+    constexpr int TR = 16384 / TC;
     constexpr int kTileBytes = TR * TC * 2;
     constexpr int SZ = SF == 0 ? 4 : 1;
     constexpr int kCPR = TC / kChunk;      // 16-element chunks per tile row
@@ -943,10 +966,10 @@ cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, i
 // element in register moves).
 constexpr int kRowsCtas = 2, kRowsStages = 3;
 
-template <int GRID, bool SR, int SF, bool N16, int CTAS>
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC>
 static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
-    const size_t smem = (size_t)p.stages * 128 * 128 * 2 + 8 * p.stages + 128;
-    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS>;
+    const size_t smem = (size_t)p.stages * 16384 * 2 + 8 * p.stages + 128;
+    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS, TC>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < CTAS * num_sms ? p.num_tiles : CTAS * num_sms;
@@ -956,8 +979,9 @@ static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, in
 template <int GRID, bool SR, int SF>
 static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
     p.stages = kRowsStages;
-    if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas>(maps, p, num_sms, st);
-    return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas>(maps, p, num_sms, st);
+    if (p.tc == 256) return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 256>(maps, p, num_sms, st);
+    if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128>(maps, p, num_sms, st);
+    return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128>(maps, p, num_sms, st);
 }
 
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
@@ -966,7 +990,7 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int n
     for (int t = 0; t < p.count; ++t) {
         const RowsTensor& T = p.t[t];
         if (!encode_map_2d(&maps.m[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, T.x, (uint64_t)T.cols, (uint64_t)T.rows,
-                           (uint64_t)T.ld * 2, 128, 128, CU_TENSOR_MAP_SWIZZLE_NONE))
+                           (uint64_t)T.ld * 2, (uint32_t)p.tc, (uint32_t)(16384 / p.tc), CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
 #define UFP4_R(G)                                                                              \
@@ -1026,12 +1050,15 @@ static void preload_q(cudaFuncAttributes* a) {
 }
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, true, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, true, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas, 128>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 256>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 256>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 256>);
 }
 template <int G>
 static void preload_grid(cudaFuncAttributes* a) {
@@ -1048,8 +1075,9 @@ cudaError_t preload_quantize_kernels() {
     preload_grid<1>(&a);
     preload_grid<2>(&a);
     preload_grid<3>(&a);
-    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas>);
-    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 128>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas, 128>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 256>);
     return cudaFuncGetAttributes(&a, rht_kernel);
 }
 

@@ -190,6 +190,12 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return r;
 }
 
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+
 // Sign masks of a 16-element chunk: bit j of sgn set <=> eps_j = -1.
 struct SignMasks {
     uint32_t lo[8], hi[8];  // 0 or 0x80000000 for elements 2k and 2k+1
@@ -305,13 +311,17 @@ __device__ __forceinline__ void fwht_pair(uint64_t e[16], int n, int seg_lane) {
             }
         }
     }
+    // across lanes: the lower lane of a pair forms a + b, the upper one a - b,
+    // i.e. o + s e with s = +1 or -1, one fma each (the product is exact, so
+    // the single rounding equals that of the add or subtract)
     for (int h = kChunk; h < n; h <<= 1) {
         const int lm = h / kChunk;
-        const bool upper = (seg_lane & lm) != 0;
+        const float sgn = (seg_lane & lm) != 0 ? -1.0f : 1.0f;
+        const uint64_t s2 = pk2(sgn, sgn);
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
             const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)e[i], lm);
-            e[i] = upper ? sub2(o, e[i]) : add2(e[i], o);
+            e[i] = fma2(s2, e[i], o);
         }
     }
 }
@@ -330,11 +340,6 @@ __device__ __forceinline__ void fwht_pair16(uint64_t e[16]) {
     }
 }
 
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t r;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
-    return r;
-}
 
 // Tree amax of |a_i| and |b_i| over i in [lo, hi) (lo, hi multiples of 8).
 __device__ __forceinline__ float max3(float a, float b, float c) {

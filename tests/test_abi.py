@@ -92,7 +92,9 @@ def test_batch_validation_rejects_bad_arguments(lib):
     assert call(ok, count=0) == 0                                          # nothing to do
     assert call(ok, count=ufp4.MAX_BATCH + 1) == 1                          # too many tensors
     assert call(ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)) == 1  # row-wise only
-    assert call(ufp4.make_desc(n=256, out_mask=ufp4.OUT_ROWWISE)) == 2     # n > 128
+    assert call(ufp4.make_desc(n=256, out_mask=ufp4.OUT_ROWWISE)) == 1     # cols not a multiple of n
+    mx256 = ufp4.make_desc(grid="mxfp8", block=(1, 32), n=256, scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+    assert call(mx256, cols=(256, 256), lds=(256, 256)) == 2                 # MXFP8 keeps n <= 128
     assert call(ufp4.make_desc(block=(32, 32), scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)) == 2
     assert call(ok, xs=(0x1000, 0x9001)) == 3                              # second input misaligned
     assert call(ok, cols=(64, 72), lds=(64, 72)) == 1                      # cols not a multiple of 16
