@@ -616,22 +616,27 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
         emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
              2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
         del A, B, ws, D
-        # the large-sweep FPROP GEMM
+        # the large-sweep FPROP GEMMs: 16384 x 7168 x 7168 per grid, 1x16 and 32x32 UE8M0 operands
         M5, N5, K5 = 16384, 7168, 7168
-        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_UE8M0)
-        A = (torch.randint(0, 256, (M5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-             torch.randint(120, 132, (M5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
-        B = (torch.randint(0, 256, (N5, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-             torch.randint(120, 132, (N5, K5 // 16), generator=g, dtype=torch.uint8).to(dev))
-        qa, qb = ufp4.qtensor(*A, M5, K5), ufp4.qtensor(*B, N5, K5)
-        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M5, N5, K5, desc), dtype=torch.uint8, device=dev)
-        D = torch.empty((M5, N5), dtype=torch.float32, device=dev)
-        ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream)
-        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream), reps=10)
-        tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
-        emit("gemm", f"{M5}x{N5}x{K5} e1m2 1x16 UE8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
-             kernel_ms=kms)
-        del A, B, ws, D
+        for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 16), 2.0), ("e2m1", (1, 16), 6.0),
+                                       ("e1m2", (32, 32), 2.0), ("int4", (32, 32), 2.0), ("e2m1", (32, 32), 6.0)):
+            desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
+            def operand(rows):
+                c = torch.randint(0, 256, (rows, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev)
+                srows = rows // block[0] if block[0] > 1 else rows
+                sc = torch.randint(120, 132, (srows, K5 // block[1]), generator=g, dtype=torch.uint8).to(dev)
+                return c, sc
+            A, B = operand(M5), operand(N5)
+            qa, qb = ufp4.qtensor(*A, M5, K5), ufp4.qtensor(*B, N5, K5)
+            ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M5, N5, K5, desc), dtype=torch.uint8, device=dev)
+            D = torch.empty((M5, N5), dtype=torch.float32, device=dev)
+            pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream), reps=10)
+            kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream), reps=10)
+            tf = 2.0 * M5 * N5 * K5 / (kms / 1e3) / 1e12
+            peak = kind_peak * pk["bf16"]
+            emit("gemm", f"{M5}x{N5}x{K5} {grid} {block[0]}x{block[1]} UE8M0", tf, "TFLOP/s", tf / peak, peak,
+                 kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
+            del A, B, ws, D
 
     if "moe" in sections:
         # 5. MoE-7.9B-like expert FFN step: seeded top-2 routing of 16384 tokens

@@ -156,7 +156,8 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     std::memset(&p, 0, sizeof(p));
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
     const int n = desc->hadamard_n;
-    const int tc = n == 256 ? 256 : 128, tr = 16384 / tc;  // tile columns and rows
+    // tile columns and rows: 16 K elements, or 8 K (one row pair per thread) with 2-D blocks
+    const int tc = n == 256 ? 256 : 128, tr = bs.is2d ? 2 * (256 / (tc / 16)) : 16384 / tc;
     int64_t tiles = 0;
     int k = 0;
     for (int i = 0; i < count; ++i) {
@@ -181,6 +182,10 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     p.count = k;
     p.num_tiles = (int)tiles;
     p.tc = tc;
+    p.tr = tr;
+    p.lb2d = 0;
+    if (bs.is2d)
+        while ((1 << p.lb2d) < bs.b2d) ++p.lb2d;
     p.n = n;
     p.lbw = ilog2(bs.bw);
     p.log4n = 0;
@@ -253,7 +258,11 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if ((desc->scale_fmt == UFP4_SCALE_E4M3 || desc->grid == UFP4_GRID_MXFP8) &&
         (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) || cols >= (1LL << 31)))
         return UFP4_ERR_UNSUPPORTED;  // two-level scale and MXFP8: row-wise, 1-D blocks, n <= 128
-    if (do_row && !do_col && !bs.is2d && !grouped && total_rows < (1LL << 31) && cols < (1LL << 31)) {
+    // the row kernel: row-wise, not grouped; 1-D blocks, or b x b blocks with b = 16, 32 or 64 (b <= 32 when
+    // n = 256: its tiles have 32 rows)
+    const bool rows_2d = bs.is2d && bs.b2d >= 16 && (n < 256 || bs.b2d <= 32);
+    if (do_row && !do_col && (!bs.is2d || rows_2d) && !grouped && total_rows < (1LL << 31) &&
+        cols < (1LL << 31)) {
         const ufp4_qtensor* rw = rowwise;
         return quantize_rows_batch(1, &x, &total_rows, &cols, &ld, desc, bs, rw, stream);
     }

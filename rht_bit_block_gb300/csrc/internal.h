@@ -88,7 +88,7 @@ struct QuantParams {
 cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
                             int64_t total_rows, int num_sms, cudaStream_t st);
 
-// Row-wise only, 1-D blocks, n <= 256: the lean kernel, over up to
+// Row-wise only, 1-D blocks (or b x b blocks, b = 16, 32, 64), n <= 256: the lean kernel, over up to
 // kMaxBatch independent tensors in one launch.
 constexpr int kMaxBatch = 4;
 struct RowsTensor {
@@ -106,7 +106,8 @@ struct RowsTensor {
 struct RowsParams {
     RowsTensor t[kMaxBatch];
     int count, num_tiles;
-    int tc;             // tile columns: 128, or 256 for n = 256 (tiles of 16384 elements)
+    int tc, tr;         // tile columns (128, or 256 for n = 256) and rows
+    int lb2d;           // log2 b of b x b blocks, 0 for 1-D blocks
     int n, lbw, pow4, log4n, stages;
     float inv_sqrt_n;
     uint32_t sign_bits[8];
@@ -123,6 +124,11 @@ cudaError_t quant_error_read_clear(int* value);
 // the default is restored by passing quant_wait_limit_default()).
 cudaError_t set_quant_wait_limit(uint32_t polls);
 uint32_t quant_wait_limit_default();
+// The row kernel's unit (quantize_rows.cu) keeps its own error word and wait
+// limit; the two functions above read and set both units'.
+cudaError_t rows_error_read_clear(int* value);
+cudaError_t set_rows_wait_limit(uint32_t polls);
+cudaError_t preload_rows_kernels();
 
 // 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,
 // pitch bytes between rows, boxes of box_inner x box_outer elements.

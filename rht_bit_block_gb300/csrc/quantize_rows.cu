@@ -1,0 +1,375 @@
+// Row-wise fused RHT + block-scaled 4-bit quantizer for sm_103a: the FPROP
+// operands' case (RHT and 1-D blocks along the rows), over up to four
+// tensors in one launch.
+//
+// Pages: UFP4 summary (hyper.ai, arXiv 2606.20381), sections 数据集 (codebooks,
+// blocks, s_B = amax / largest level, RTNE, SR) and 方法 (Sylvester H_2n,
+// H'_n = S_n H_n, the quantized GEMM's operands quantized along K);
+// "Stable FP4 Training via Transposition-Invariant Block Quantization",
+// truncation-free scale.
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "internal.h"
+#include "quantize_common.cuh"
+#include "ufp4_device.cuh"
+
+namespace ufp4 {
+
+__device__ int g_rows_error;
+
+// Polls of a tile's barrier before a row-kernel CTA gives up (see
+// set_quant_wait_limit; the drain of copies in flight always uses kWaitLimit).
+__device__ uint32_t g_rows_wait_limit = kWaitLimit;
+
+// ------------------------------------------------------ row-wise (lean)
+// Row-wise quantization with 1-D blocks and n <= 128, the FPROP operands'
+// case, over up to kMaxBatch independent tensors in one launch (their tiles
+// are numbered one after the other).  Same steps as the row pass above, with
+// 128 x 128 tiles fixed at compile time, tile coordinates and output pointers
+// advanced without division, and per-row bounds checks only on ragged tiles.
+struct RowsMaps {
+    CUtensorMap m[kMaxBatch];
+};
+
+// N16: n = 16 (the FPROP operands' case), with the four butterfly strides
+// fixed at compile time.
+// TC: tile columns, 128, or 256 for n = 256 (whose segments span 16 chunks);
+// the tiles hold 16 K elements either way.
+//
+// TWO_D: b x b blocks (b = 16, 32 or 64; with 256-column tiles b <= 32,
+// UE8M0 scales).  The tile then has 2 kRPI rows, so each thread holds one
+// row pair; the block amax is reduced across the lanes of a warp that share
+// the block, then across warps with a shared-memory atomicMax, while the
+// transformed values wait in registers.  The amax slots come in two sets
+// used by alternate tiles, so a set is cleared during the tile before its use.
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
+__global__ void __launch_bounds__(kThreads, CTAS)
+quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
+    constexpr int kCPR = TC / kChunk;      // 16-element chunks per tile row
+    constexpr int kRPI = kThreads / kCPR;  // tile rows per thread step
+    constexpr int TR = TWO_D ? 2 * kRPI : 16384 / TC;
+    constexpr int kTileBytes = TR * TC * 2;
+    constexpr int SZ = SF == 0 ? 4 : 1;
+    constexpr int kSlots = TWO_D ? (TR / 16) * (TC / 16) : 0;  // amax slots per set (b = 16 at most)
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 127u) & ~127u) - raw;
+    uint8_t* base = smem_raw + pad;
+    const int kStages = p.stages;
+    uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes);  // 2 sets of kSlots
+    const uint32_t bars = smem_addr(base + kStages * kTileBytes + 8 * kSlots);
+    const int tid = threadIdx.x;
+    const int cchunk = tid % kCPR;
+    const int r0 = tid / kCPR;
+    const int n = p.n;
+    Fold fd;
+    fd.inv_s = p.inv_sqrt_n;
+    fd.pow4 = p.pow4;
+    fd.j = p.log4n;
+    fd.g = 0.0f;
+    const int seg_row = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
+    SignMasks mrow;
+    {
+        const int pos = (cchunk * kChunk) & 255;
+        make_masks((p.sign_bits[pos >> 5] >> (pos & 31)) & 0xFFFFu, mrow);
+    }
+    const int lbw = p.lbw;
+
+    // tensor and tile coordinates of a tile index
+    auto locate = [&](int tile, int& t, int& rt, int& ct) {
+        t = 0;
+        while (t + 1 < p.count && tile >= p.t[t + 1].tile0) ++t;
+        const int local = tile - p.t[t].tile0;
+        rt = local / p.t[t].col_tiles;
+        ct = local - rt * p.t[t].col_tiles;
+    };
+    auto issue = [&](int tile, int s) {
+        int t, rt, ct;
+        locate(tile, t, rt, ct);
+        const uint32_t bar = bars + 8u * s;
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+            ::"r"(smem_addr(base + s * kTileBytes)), "l"((uint64_t)&maps.m[t]), "r"(ct * TC), "r"(rt * TR), "r"(bar)
+            : "memory");
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (TWO_D)
+        for (int q = tid; q < 2 * kSlots; q += kThreads) amax2d[q] = 0u;
+    const int lb = p.lb2d;  // log2 b (2-D blocks)
+    __syncthreads();
+    griddep_wait();
+    griddep_launch();
+    const uint32_t wait_limit = g_rows_wait_limit;
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int tile = blockIdx.x + s * gridDim.x;
+            if (tile < p.num_tiles) issue(tile, s);
+        }
+
+    int t = 0, rt = 0, ct = 0, step_r = 0, step_c = 0;
+    auto relocate = [&](int tile) {
+        locate(tile, t, rt, ct);
+        step_r = (int)gridDim.x / p.t[t].col_tiles;
+        step_c = (int)gridDim.x - step_r * p.t[t].col_tiles;
+        // two-level scale: the tensor amax was written by the pre-pass (before this launch)
+        if (SF == 2) fd.g = __fdiv_rn(*p.t[t].amax, grid_qmax(GRID) * 448.0f);
+    };
+    if ((int)blockIdx.x < p.num_tiles) relocate(blockIdx.x);
+    int s = 0;
+    uint32_t phase = 0;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++i) {
+        if (i) {
+            ct += step_c;
+            rt += step_r;
+            if (ct >= p.t[t].col_tiles) {
+                ct -= p.t[t].col_tiles;
+                ++rt;
+            }
+            if (rt >= p.t[t].row_tiles) relocate(tile);  // into the next tensor
+        }
+        const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
+        if (!__syncthreads_and(landed)) {
+            if (tid == 0) atomicExch(&g_rows_error, 1);
+            break;
+        }
+        const RowsTensor& T = p.t[t];
+        const uint16_t* tile_s = reinterpret_cast<const uint16_t*>(base + s * kTileBytes);
+        const int row0 = rt * TR;
+        const int col = ct * TC + cchunk * kChunk;
+        const bool col_ok = col < T.cols;
+        const int left = T.rows - row0 - r0;  // rows of this thread's first row onward
+        const bool full = T.rows - row0 >= TR;
+        uint8_t* cp = T.codes + (int64_t)(row0 + r0) * T.codes_ld + (GRID == 4 ? col : col >> 1);
+        uint8_t* sp = T.scales + ((int64_t)(row0 + r0) * T.scales_ld + (col >> lbw)) * SZ;
+        const int64_t cstep = (int64_t)kRPI * T.codes_ld;
+        const int64_t sstep = (int64_t)kRPI * T.scales_ld * SZ;
+        const bool wsc = (col & ((1 << lbw) - 1)) == 0;
+        const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
+#pragma unroll
+        for (int it = 0; it < TR / (2 * kRPI); ++it) {
+            const int ra = 2 * kRPI * it;
+            uint32_t wa[8], wb[8];
+            uint64_t e[16];
+            const uint4* pa = reinterpret_cast<const uint4*>(src + ra * TC);
+            const uint4* pb = reinterpret_cast<const uint4*>(src + (ra + kRPI) * TC);
+            const uint4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
+            wa[0] = a0.x; wa[1] = a0.y; wa[2] = a0.z; wa[3] = a0.w;
+            wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
+            wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
+            wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
+            widen_rows(wa, wb, mrow, e);
+            float Ma, Mb;
+            if (TWO_D) {
+                if (N16) fwht_pair16(e);
+                else fwht_pair(e, n, seg_row);
+                amax_pair(e, 0, 16, Ma, Mb);
+                // the lanes of this warp in the same block: the b/16 neighbouring
+                // chunks (lane bits below log2 kCPR) and the warp's 32/kCPR rows
+                // (the lane bits above); when b > kRPI the thread's two rows
+                // share the block as well
+                for (int k = 1; k < (1 << lb) / kChunk; k <<= 1) {
+                    Ma = fmaxf(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, k));
+                    Mb = fmaxf(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, k));
+                }
+                const bool shared_rows = (1 << lb) > kRPI;
+                if (shared_rows) Ma = Mb = fmaxf(Ma, Mb);
+#pragma unroll
+                for (int k = kCPR; k < 32; k <<= 1) {
+                    Ma = fmaxf(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, k));
+                    Mb = fmaxf(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, k));
+                }
+                uint32_t* set = amax2d + (i & 1) * kSlots;
+                const int lnbc = (TC == 256 ? 8 : 7) - lb;  // log2(TC / b): block columns per tile
+                const int bc = (cchunk * kChunk) >> lb;
+                const int sa = ((r0 >> lb) << lnbc) + bc, sb = (((r0 + kRPI) >> lb) << lnbc) + bc;
+                if ((r0 & (32 / kCPR - 1)) == 0 && ((cchunk * kChunk) & ((1 << lb) - 1)) == 0) {
+                    atomicMax(&set[sa], __float_as_uint(Ma));
+                    if (!shared_rows) atomicMax(&set[sb], __float_as_uint(Mb));
+                }
+                __syncthreads();
+                Ma = __uint_as_float(set[sa]);
+                Mb = __uint_as_float(set[sb]);
+                // the other set serves the next tile: every read of it (the
+                // previous tile's) happened before this tile's first barrier
+                uint32_t* other = amax2d + ((i & 1) ^ 1) * kSlots;
+                for (int q = tid; q < kSlots; q += kThreads) other[q] = 0u;
+            } else if (N16) {
+                fwht_pair16(e);
+                amax_pair(e, 0, 16, Ma, Mb);
+                if (lbw == 5) {  // 1 x 32 blocks: the neighbouring lane holds the other half
+                    Ma = fmaxf(Ma, __shfl_xor_sync(0xFFFFFFFFu, Ma, 1));
+                    Mb = fmaxf(Mb, __shfl_xor_sync(0xFFFFFFFFu, Mb, 1));
+                }
+            } else {
+                fwht_pair(e, n, seg_row);
+                amax_1d_pair(e, 1 << lbw, Ma, Mb);
+            }
+            Dest A, B;
+            A.codes = cp + (2 * it) * cstep;
+            B.codes = A.codes + cstep;
+            if (TWO_D) {
+                // one UE8M0 byte per b x b block, written by its top-left thread
+                const int rA = row0 + r0, rB = rA + kRPI;
+                A.s0 = A.s1 = T.scales + (int64_t)(rA >> lb) * T.scales_ld + (col >> lb);
+                B.s0 = B.s1 = T.scales + (int64_t)(rB >> lb) * T.scales_ld + (col >> lb);
+                const bool cfirst = (col & ((1 << lb) - 1)) == 0;
+                A.w0 = cfirst && (rA & ((1 << lb) - 1)) == 0;
+                B.w0 = cfirst && (rB & ((1 << lb) - 1)) == 0;
+            } else {
+                A.s0 = A.s1 = sp + (2 * it) * sstep;
+                B.s0 = B.s1 = A.s0 + sstep;
+                A.w0 = B.w0 = wsc;
+            }
+            A.valid = col_ok && (full || ra < left);
+            B.valid = col_ok && (full || ra + kRPI < left);
+            A.w1 = B.w1 = false;
+            A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
+            B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
+            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+        }
+        // everyone is done with stage s: refill it
+        __syncthreads();
+        if (tid == 0) {
+            const int next = tile + kStages * gridDim.x;
+            if (next < p.num_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, s);
+            }
+        }
+        if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+    // a broken-off loop leaves copies in flight: let them land (bounded)
+    if (tid == 0)
+        for (int k = i; k < i + kStages; ++k) {
+            const int tile = blockIdx.x + k * gridDim.x;
+            if (tile >= p.num_tiles) break;
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
+        }
+}
+
+// CTAs per SM and ring depth of the row kernel (128 x 128 tiles): two CTAs
+// of up to 128 registers a thread, each with three 32 KB stages (measured on
+// the 16384 x 7168 + 7168 x 7168 batch: 6.13 TB/s, against 5.87 TB/s for
+// three CTAs of two stages, whose 80-register cap costs 1.6 instructions per
+// element in register moves).
+constexpr int kRowsCtas = 2, kRowsStages = 3;
+
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
+static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
+    constexpr int kTileElems = TWO_D ? 2 * (kThreads / (TC / kChunk)) * TC : 16384;
+    constexpr int kSlots = TWO_D ? (kTileElems / TC / 16) * (TC / 16) : 0;
+    const size_t smem = (size_t)p.stages * kTileElems * 2 + 8 * kSlots + 8 * p.stages + 128;
+    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS, TC, TWO_D>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < CTAS * num_sms ? p.num_tiles : CTAS * num_sms;
+    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
+}
+
+template <int GRID, bool SR, int SF>
+static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
+    if constexpr (SF == 1 && GRID < 4) {
+        if (p.lb2d) {
+            // 2-D blocks: 8 K-element tiles (one row pair per thread), six stages
+            p.stages = 2 * kRowsStages;
+            if (p.tc == 256) return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 256, true>(maps, p, num_sms, st);
+            if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, true>(maps, p, num_sms, st);
+            return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128, true>(maps, p, num_sms, st);
+        }
+    }
+    p.stages = kRowsStages;
+    if (p.tc == 256) return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 256, false>(maps, p, num_sms, st);
+    if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, false>(maps, p, num_sms, st);
+    return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128, false>(maps, p, num_sms, st);
+}
+
+cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
+    RowsMaps maps;
+    memset(&maps, 0, sizeof(maps));
+    for (int t = 0; t < p.count; ++t) {
+        const RowsTensor& T = p.t[t];
+        if (!encode_map_2d(&maps.m[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, T.x, (uint64_t)T.cols, (uint64_t)T.rows,
+                           (uint64_t)T.ld * 2, (uint32_t)p.tc, (uint32_t)p.tr, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return cudaErrorInvalidValue;
+    }
+#define UFP4_R(G)                                                                              \
+    if (grid == G) {                                                                           \
+        if (sr) return sf == 2 ? launch_rows<G, true, 2>(maps, p, num_sms, st)                 \
+                     : sf == 1 ? launch_rows<G, true, 1>(maps, p, num_sms, st)                 \
+                               : launch_rows<G, true, 0>(maps, p, num_sms, st);                \
+        return sf == 2 ? launch_rows<G, false, 2>(maps, p, num_sms, st)                        \
+             : sf == 1 ? launch_rows<G, false, 1>(maps, p, num_sms, st)                        \
+                       : launch_rows<G, false, 0>(maps, p, num_sms, st);                       \
+    }
+    UFP4_R(0)
+    UFP4_R(1)
+    UFP4_R(2)
+    UFP4_R(3)
+#undef UFP4_R
+    if (grid == 4 && !sr && sf == 1) return launch_rows<4, false, 1>(maps, p, num_sms, st);  // MXFP8
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t rows_error_read_clear(int* value) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_rows_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbol(g_rows_error, &zero, sizeof(int));
+    }
+    *value = v;
+    return e;
+}
+
+cudaError_t set_rows_wait_limit(uint32_t polls) {
+    return cudaMemcpyToSymbol(g_rows_wait_limit, &polls, sizeof(polls));
+}
+
+// Loads every kernel of this unit (cudaFuncGetAttributes loads a function
+// that has not been loaded yet).
+template <int G, bool SR>
+static void preload_rows(cudaFuncAttributes* a) {
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, true, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 256, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 256, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 256, false>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, true>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, true>);
+    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 256, true>);
+}
+
+cudaError_t preload_rows_kernels() {
+    cudaFuncAttributes a;
+    preload_rows<0, false>(&a);
+    preload_rows<0, true>(&a);
+    preload_rows<1, false>(&a);
+    preload_rows<1, true>(&a);
+    preload_rows<2, false>(&a);
+    preload_rows<2, true>(&a);
+    preload_rows<3, false>(&a);
+    preload_rows<3, true>(&a);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas, 128, false>);
+    return cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 256, false>);
+}
+
+}  // namespace ufp4

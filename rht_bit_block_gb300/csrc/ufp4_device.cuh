@@ -55,30 +55,38 @@ __device__ __forceinline__ float decode_level(int grid, uint32_t nib) {
 // Salmon et al., SC'11: ten rounds, multipliers 0xD2511F53 / 0xCD9E8D57, key
 // bumped by 0x9E3779B9 / 0xBB67AE85 between rounds (the round keys come
 // precomputed, see SrKeys).  Each product is one 32 x 32 -> 64-bit multiply
-// (both halves at once).
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const SrKeys& k) {
+// (both halves at once).  Four independent blocks run round by round, so
+// that the four multiply chains overlap (ten dependent rounds each).
+__device__ __forceinline__ void philox4x32_10_x4(uint4 c[4], const SrKeys& k) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        uint64_t p0, p1;
-        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c.x), "r"(0xD2511F53u));
-        asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c.z), "r"(0xCD9E8D57u));
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k.k[2 * i], (uint32_t)p1,
-                       (uint32_t)(p0 >> 32) ^ c.w ^ k.k[2 * i + 1], (uint32_t)p0);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint64_t p0, p1;
+            asm("mul.wide.u32 %0, %1, %2;" : "=l"(p0) : "r"(c[j].x), "r"(0xD2511F53u));
+            asm("mul.wide.u32 %0, %1, %2;" : "=l"(p1) : "r"(c[j].z), "r"(0xCD9E8D57u));
+            c[j] = make_uint4((uint32_t)(p1 >> 32) ^ c[j].y ^ k.k[2 * i], (uint32_t)p1,
+                              (uint32_t)(p0 >> 32) ^ c[j].w ^ k.k[2 * i + 1], (uint32_t)p0);
+        }
     }
-    return c;
 }
 
-// Sixteen 16-bit SR draws for output elements lin0 .. lin0+15 (lin0 % 8 == 0):
-// counter (g lo, g hi, stream, group) with g = lin / 8; element j of a group
-// of eight takes the low half of word j/2 when j is even, the high half when odd.
-__device__ __forceinline__ void sr_draws16(const SrKeys& k, uint64_t lin0, uint32_t stream, uint32_t group,
-                                           uint32_t w[8]) {
-    const uint64_t g = lin0 >> 3;
-    const uint4 a = philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), stream, group), k);
-    const uint64_t g1 = g + 1;
-    const uint4 b = philox4x32_10(make_uint4((uint32_t)g1, (uint32_t)(g1 >> 32), stream, group), k);
-    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-    w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+// SR draws of 16 output elements lin0 .. lin0+15 (lin0 % 8 == 0): counter
+// (g lo, g hi, stream, group) with g = lin / 8; element j of a group of
+// eight takes the low half of word j/2 when j is even, the high half when odd.
+// Two vectors at once: elements la0 .. la0+15 into wa, lb0 .. lb0+15 into wb.
+__device__ __forceinline__ void sr_draws16x2(const SrKeys& k, uint64_t la0, uint64_t lb0, uint32_t stream,
+                                             uint32_t group, uint32_t wa[8], uint32_t wb[8]) {
+    const uint64_t ga = la0 >> 3, gb = lb0 >> 3;
+    uint4 c[4] = {make_uint4((uint32_t)ga, (uint32_t)(ga >> 32), stream, group),
+                  make_uint4((uint32_t)(ga + 1), (uint32_t)((ga + 1) >> 32), stream, group),
+                  make_uint4((uint32_t)gb, (uint32_t)(gb >> 32), stream, group),
+                  make_uint4((uint32_t)(gb + 1), (uint32_t)((gb + 1) >> 32), stream, group)};
+    philox4x32_10_x4(c, k);
+    wa[0] = c[0].x; wa[1] = c[0].y; wa[2] = c[0].z; wa[3] = c[0].w;
+    wa[4] = c[1].x; wa[5] = c[1].y; wa[6] = c[1].z; wa[7] = c[1].w;
+    wb[0] = c[2].x; wb[1] = c[2].y; wb[2] = c[2].z; wb[3] = c[2].w;
+    wb[4] = c[3].x; wb[5] = c[3].y; wb[6] = c[3].z; wb[7] = c[3].w;
 }
 
 // ------------------------------------------------------------------ loading

@@ -71,6 +71,23 @@ def test_block_shapes(block, n):
            sr_seed=2)
 
 
+@pytest.mark.parametrize("b", [16, 32, 64])
+@pytest.mark.parametrize("n", [1, 16, 32, 128, 256])
+@pytest.mark.parametrize("rounding", [RTNE, SR])
+def test_2d_blocks_rowwise_kernel(b, n, rounding):
+    """Row-wise b x b blocks run in the row kernel (one row pair per thread, the
+    block amax reduced across lanes and warps): ragged tiles (rows and columns
+    multiples of b but not of the tile), every grid."""
+    if n == 256 and b == 64:
+        pytest.skip("64 x 64 blocks with n = 256 take the general kernel")
+    rows = 3 * b + 2 * 64 if b < 64 else 320
+    cols = 768 if n == 256 else 384 + 2 * b
+    cols = -(-cols // max(n, b)) * max(n, b)
+    x = inputs.tiny_check(rows, cols)
+    for grid in GRIDS:
+        _check(x, grid=grid, block=(b, b), n=n, sign_seed=5, rounding=rounding, sr_seed=13, scale_fmt=PO2)
+
+
 @pytest.mark.parametrize("block", [(8, 8), (32, 32)])
 def test_2d_blocks_with_n256(block):
     x = inputs.tiny_check(128, 512)
