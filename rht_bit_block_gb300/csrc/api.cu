@@ -194,6 +194,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     p.stages = 2;  // 2 x 32 KB tiles per CTA, 3 CTAs per SM
     p.inv_sqrt_n = inv_sqrt_n(n);
     make_sign_bits(desc->sign_seed, n, p.sign_bits);
+    for (int j = 0; j < 64; ++j) p.smask[j] = ((p.sign_bits[j / 32] >> (j % 32)) & 1u) << 31;
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
     p.sr_keys = sr_round_keys(p.sr_seed);
     p.group = desc->group;

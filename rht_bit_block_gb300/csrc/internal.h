@@ -111,6 +111,7 @@ struct RowsParams {
     int n, lbw, pow4, log4n, stages;
     float inv_sqrt_n;
     uint32_t sign_bits[8];
+    uint32_t smask[64];  // n = 64: sign bit of element j of a segment (0x80000000 when eps_j = -1)
     uint64_t sr_seed;
     SrKeys sr_keys;
     int group;

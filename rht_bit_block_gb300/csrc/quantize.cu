@@ -157,103 +157,41 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             __syncthreads();
         }
 
-        // -------------------------------------------------------- row pass
-        if (p.do_row) {
+        if (!p.is2d) {
+            // ------------------------------------------ 1-D blocks, both passes
+            // the row pairs and the column tasks of this tile go through one
+            // emit site, so that the scale, rounding and packing code (long
+            // with SR) has one inlined copy
             const int64_t col = c0 + cchunk * kChunk;
             const bool col_ok = col < p.cols;
             // rows of this tile that exist, counted from this thread's first row
             const int64_t left = cnt - lr0 - r0;
             const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
-            if (p.is2d) {
-                const int lnbc = 7 + (TC == 256) - lb;  // log2(TC / b)
-                const int bmask = (1 << lb) - 1;
-                for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
-                __syncthreads();
-                // with one row pair per thread (64-row tiles) the transformed values
-                // stay in registers while the block amax settles in shared memory;
-                // with two, the second pass transforms them again
-                uint64_t keep[16];
-                for (int it = 0; it < pairs; ++it) {
-                    const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
-                    uint32_t wa[8], wb[8];
-                    uint64_t e[16];
-                    load_row_chunk<TC>(tile_s, ra, cchunk, wa);
-                    load_row_chunk<TC>(tile_s, rb, cchunk, wb);
-                    widen_rows(wa, wb, mrow, e);
-                    fwht_pair(e, n, seg_row);
-                    if (pairs == 1)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) keep[i] = e[i];
-                    const int sa = (ra >> lb) << lnbc, sb = (rb >> lb) << lnbc;
-                    if (lb == 3) {
-                        float a0, b0, a1, b1;
-                        amax_pair(e, 0, 8, a0, b0);
-                        amax_pair(e, 8, 16, a1, b1);
-                        post_amax(&amax2d[sa + 2 * cchunk], a0);
-                        post_amax(&amax2d[sa + 2 * cchunk + 1], a1);
-                        post_amax(&amax2d[sb + 2 * cchunk], b0);
-                        post_amax(&amax2d[sb + 2 * cchunk + 1], b1);
-                    } else {
-                        float a0, b0;
-                        amax_pair(e, 0, 16, a0, b0);
-                        post_amax(&amax2d[sa + ((cchunk * kChunk) >> lb)], a0);
-                        post_amax(&amax2d[sb + ((cchunk * kChunk) >> lb)], b0);
-                    }
-                }
-                __syncthreads();
-                for (int it = 0; it < pairs; ++it) {
-                    const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
-                    uint64_t e[16];
-                    if (pairs == 1) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) e[i] = keep[i];
-                    } else {
-                        uint32_t wa[8], wb[8];
-                        load_row_chunk<TC>(tile_s, ra, cchunk, wa);
-                        load_row_chunk<TC>(tile_s, rb, cchunk, wb);
-                        widen_rows(wa, wb, mrow, e);
-                        fwht_pair(e, n, seg_row);
-                    }
-                    const int off = lb == 3 ? 2 * cchunk : ((cchunk * kChunk) >> lb);
-                    const int sa = ((ra >> lb) << lnbc) + off, sb = ((rb >> lb) << lnbc) + off;
-                    const float MA0 = __uint_as_float(amax2d[sa]);
-                    const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
-                    const float MB0 = __uint_as_float(amax2d[sb]);
-                    const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
-                    Dest A, B;
-                    const int64_t la = lr0 + ra, lbr = lr0 + rb;
-                    const bool colfirst = lb == 3 || (col & bmask) == 0;
-                    uint8_t* sbase = (uint8_t*)p.row.scales;
-                    A.codes = (uint8_t*)p.row.codes + (grow0 + la) * p.row.codes_ld + (col >> 1);
-                    B.codes = (uint8_t*)p.row.codes + (grow0 + lbr) * p.row.codes_ld + (col >> 1);
-                    A.s0 = sbase + ((la >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
-                    B.s0 = sbase + ((lbr >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
-                    A.s1 = A.s0 + SZ;
-                    B.s1 = B.s0 + SZ;
-                    A.valid = la < cnt && col_ok;
-                    B.valid = lbr < cnt && col_ok;
-                    A.w0 = (la & bmask) == 0 && colfirst;
-                    B.w0 = (lbr & bmask) == 0 && colfirst;
-                    A.w1 = (la & bmask) == 0 && lb == 3;
-                    B.w1 = (lbr & bmask) == 0 && lb == 3;
-                    A.lin0 = (uint64_t)la * (uint64_t)p.cols + (uint64_t)col;
-                    B.lin0 = (uint64_t)lbr * (uint64_t)p.cols + (uint64_t)col;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 0u, grp_id);
-                }
-            } else {
-                const bool wsc = (col & ((1 << lbw) - 1)) == 0;
-                // output pointers of this thread's first row, stepped per pair
-                const int64_t orow0 = grow0 + lr0 + r0;  // row-wise output rows follow the input rows
-                uint8_t* cp = (uint8_t*)p.row.codes + orow0 * p.row.codes_ld + (col >> 1);
-                uint8_t* sp = (uint8_t*)p.row.scales + (orow0 * p.row.scales_ld + (col >> lbw)) * SZ;
-                const int64_t cstep = (int64_t)kRPI * p.row.codes_ld;
-                const int64_t sstep = (int64_t)kRPI * p.row.scales_ld * SZ;
-                uint64_t lin = (uint64_t)(lr0 + r0) * (uint64_t)p.cols + (uint64_t)col;
-                const uint64_t lstep = (uint64_t)kRPI * (uint64_t)p.cols;
-                for (int it = 0; it < pairs; ++it) {
+            const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
+            const int64_t sc_ld = p.col_grouped ? (padded >> lbwc) : p.col.scales_ld;
+            uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
+            uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lbwc) * SZ : 0);
+            const bool wsc = (col & ((1 << lbw) - 1)) == 0;
+            // output pointers of this thread's first row, stepped per pair
+            const int64_t orow0 = grow0 + lr0 + r0;  // row-wise output rows follow the input rows
+            uint8_t* cp = (uint8_t*)p.row.codes + orow0 * p.row.codes_ld + (col >> 1);
+            uint8_t* sp = (uint8_t*)p.row.scales + (orow0 * p.row.scales_ld + (col >> lbw)) * SZ;
+            const int64_t cstep = (int64_t)kRPI * p.row.codes_ld;
+            const int64_t sstep = (int64_t)kRPI * p.row.scales_ld * SZ;
+            uint64_t lin = (uint64_t)(lr0 + r0) * (uint64_t)p.cols + (uint64_t)col;
+            const uint64_t lstep = (uint64_t)kRPI * (uint64_t)p.cols;
+            const int bwc = 1 << lbwc;
+            const int nrow = p.do_row ? pairs : 0;
+            const int items = nrow + (p.do_col ? col_tasks : 0);
+            for (int w = 0; w < items; ++w) {
+                uint64_t e[16];
+                float Ma, Mb;
+                Dest A, B;
+                uint32_t stream;
+                if (w < nrow) {
+                    const int it = w;
                     const int ra = 2 * kRPI * it;
                     uint32_t wa[8], wb[8];
-                    uint64_t e[16];
                     const uint4* pa = reinterpret_cast<const uint4*>(src + ra * TC);
                     const uint4* pb = reinterpret_cast<const uint4*>(src + (ra + kRPI) * TC);
                     const uint4 a0 = pa[0], a1 = pa[1], b0 = pb[0], b1 = pb[1];
@@ -263,9 +201,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
                     widen_rows(wa, wb, mrow, e);
                     fwht_pair(e, n, seg_row);
-                    float Ma, Mb;
                     amax_1d_pair(e, 1 << lbw, Ma, Mb);
-                    Dest A, B;
                     A.codes = cp + (2 * it) * cstep;
                     B.codes = A.codes + cstep;
                     A.s0 = A.s1 = sp + (2 * it) * sstep;
@@ -276,121 +212,198 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                     A.w1 = B.w1 = false;
                     A.lin0 = lin + (uint64_t)(2 * it) * lstep;
                     B.lin0 = A.lin0 + lstep;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 0u, grp_id);
-                }
-            }
-        }
-
-        // ----------------------------------------------------- column pass
-        if (p.do_col) {
-            const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
-            const int lsd = p.is2d ? lb : lbwc;
-            const int64_t sc_ld = p.col_grouped ? (padded >> lsd) : p.col.scales_ld;
-            uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
-            uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lsd) * SZ : 0);
-            if (p.is2d) {
-                const int lnbq = (TR == 128 ? 7 : 6) - lb;  // log2(TR / b)
-                const int bmask = (1 << lb) - 1;
-                for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
-                __syncthreads();
-                uint64_t keep[16];
-                for (int k = 0; k < col_tasks; ++k) {
+                    stream = 0u;
+                } else {
+                    const int k = w - nrow;
                     const int t = warp + kWarps * k;
                     const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
                     const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
                     uint32_t gw[16];
-                    uint64_t e[16];
                     gather_pair<TC>(tile_s, tcol, rchunk, gw);
                     widen_cols(gw, mc, e);
                     fwht_pair(e, n, rchunk & (S - 1));
-                    if (col_tasks == 1)
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) keep[i] = e[i];
-                    const int sa = (tcol >> lb) << lnbq, sb = ((tcol + 1) >> lb) << lnbq;
-                    if (lb == 3) {
-                        float a0, b0, a1, b1;
-                        amax_pair(e, 0, 8, a0, b0);
-                        amax_pair(e, 8, 16, a1, b1);
-                        post_amax(&amax2d[sa + 2 * rchunk], a0);
-                        post_amax(&amax2d[sa + 2 * rchunk + 1], a1);
-                        post_amax(&amax2d[sb + 2 * rchunk], b0);
-                        post_amax(&amax2d[sb + 2 * rchunk + 1], b1);
-                    } else {
-                        float a0, b0;
-                        amax_pair(e, 0, 16, a0, b0);
-                        post_amax(&amax2d[sa + ((rchunk * kChunk) >> lb)], a0);
-                        post_amax(&amax2d[sb + ((rchunk * kChunk) >> lb)], b0);
-                    }
-                }
-                __syncthreads();
-                for (int k = 0; k < col_tasks; ++k) {
-                    const int t = warp + kWarps * k;
-                    const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
-                    const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    uint64_t e[16];
-                    if (col_tasks == 1) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) e[i] = keep[i];
-                    } else {
-                        uint32_t gw[16];
-                        gather_pair<TC>(tile_s, tcol, rchunk, gw);
-                        widen_cols(gw, mc, e);
-                        fwht_pair(e, n, rchunk & (S - 1));
-                    }
-                    const int off = lb == 3 ? 2 * rchunk : ((rchunk * kChunk) >> lb);
-                    const int sa = ((tcol >> lb) << lnbq) + off, sb = (((tcol + 1) >> lb) << lnbq) + off;
-                    const float MA0 = __uint_as_float(amax2d[sa]);
-                    const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
-                    const float MB0 = __uint_as_float(amax2d[sb]);
-                    const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
-                    const int64_t lrow = lr0 + rchunk * kChunk;
-                    const int64_t ca = c0 + tcol, cb = ca + 1;
-                    const bool rowfirst = lb == 3 || (lrow & bmask) == 0;
-                    Dest A, B;
-                    A.codes = gcodes + ca * out_ld + (lrow >> 1);
-                    B.codes = gcodes + cb * out_ld + (lrow >> 1);
-                    A.s0 = gscales + ((ca >> lb) * sc_ld + (lrow >> lb)) * SZ;
-                    B.s0 = gscales + ((cb >> lb) * sc_ld + (lrow >> lb)) * SZ;
-                    A.s1 = A.s0 + SZ;
-                    B.s1 = B.s0 + SZ;
-                    A.valid = lrow < padded && ca < p.cols;
-                    B.valid = lrow < padded && cb < p.cols;
-                    A.w0 = (ca & bmask) == 0 && rowfirst;
-                    B.w0 = (cb & bmask) == 0 && rowfirst;
-                    A.w1 = (ca & bmask) == 0 && lb == 3;
-                    B.w1 = (cb & bmask) == 0 && lb == 3;
-                    A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
-                    B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 1u, grp_id);
-                }
-            } else {
-                const int bwc = 1 << lbwc;
-                for (int k = 0; k < col_tasks; ++k) {
-                    const int t = warp + kWarps * k;
-                    const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
-                    const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
-                    uint32_t gw[16];
-                    uint64_t e[16];
-                    gather_pair<TC>(tile_s, tcol, rchunk, gw);
-                    widen_cols(gw, mc, e);
-                    fwht_pair(e, n, rchunk & (S - 1));
-                    float Ma, Mb;
                     amax_1d_pair(e, bwc, Ma, Mb);
                     const int64_t lrow = lr0 + rchunk * kChunk;
-                    const bool wsc = (lrow & (bwc - 1)) == 0;
+                    const bool wsc_col = (lrow & (bwc - 1)) == 0;
                     const int64_t ca = c0 + tcol, cb = ca + 1;
-                    Dest A, B;
                     A.codes = gcodes + ca * out_ld + (lrow >> 1);
                     B.codes = A.codes + out_ld;
                     A.s0 = A.s1 = gscales + (ca * sc_ld + (lrow >> lbwc)) * SZ;
                     B.s0 = B.s1 = A.s0 + sc_ld * SZ;
                     A.valid = lrow < padded && ca < p.cols;
                     B.valid = lrow < padded && cb < p.cols;
-                    A.w0 = B.w0 = wsc;
+                    A.w0 = B.w0 = wsc_col;
                     A.w1 = B.w1 = false;
                     A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
                     B.lin0 = A.lin0 + (uint64_t)padded;
-                    emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 1u, grp_id);
+                    stream = 1u;
+                }
+                emit_pair<GRID, SR, PO2 ? 1 : 0>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, stream, grp_id);
+            }
+        } else {
+            // ------------------------------------------------ 2-D blocks
+            if (p.do_row) {
+                const int64_t col = c0 + cchunk * kChunk;
+                const bool col_ok = col < p.cols;
+                {
+                    const int lnbc = 7 + (TC == 256) - lb;  // log2(TC / b)
+                    const int bmask = (1 << lb) - 1;
+                    for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
+                    __syncthreads();
+                    // with one row pair per thread (64-row tiles) the transformed values
+                    // stay in registers while the block amax settles in shared memory;
+                    // with two, the second pass transforms them again
+                    uint64_t keep[16];
+                    for (int it = 0; it < pairs; ++it) {
+                        const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
+                        uint32_t wa[8], wb[8];
+                        uint64_t e[16];
+                        load_row_chunk<TC>(tile_s, ra, cchunk, wa);
+                        load_row_chunk<TC>(tile_s, rb, cchunk, wb);
+                        widen_rows(wa, wb, mrow, e);
+                        fwht_pair(e, n, seg_row);
+                        if (pairs == 1)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) keep[i] = e[i];
+                        const int sa = (ra >> lb) << lnbc, sb = (rb >> lb) << lnbc;
+                        if (lb == 3) {
+                            float a0, b0, a1, b1;
+                            amax_pair(e, 0, 8, a0, b0);
+                            amax_pair(e, 8, 16, a1, b1);
+                            post_amax(&amax2d[sa + 2 * cchunk], a0);
+                            post_amax(&amax2d[sa + 2 * cchunk + 1], a1);
+                            post_amax(&amax2d[sb + 2 * cchunk], b0);
+                            post_amax(&amax2d[sb + 2 * cchunk + 1], b1);
+                        } else {
+                            float a0, b0;
+                            amax_pair(e, 0, 16, a0, b0);
+                            post_amax(&amax2d[sa + ((cchunk * kChunk) >> lb)], a0);
+                            post_amax(&amax2d[sb + ((cchunk * kChunk) >> lb)], b0);
+                        }
+                    }
+                    __syncthreads();
+                    for (int it = 0; it < pairs; ++it) {
+                        const int ra = r0 + 2 * kRPI * it, rb = ra + kRPI;
+                        uint64_t e[16];
+                        if (pairs == 1) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) e[i] = keep[i];
+                        } else {
+                            uint32_t wa[8], wb[8];
+                            load_row_chunk<TC>(tile_s, ra, cchunk, wa);
+                            load_row_chunk<TC>(tile_s, rb, cchunk, wb);
+                            widen_rows(wa, wb, mrow, e);
+                            fwht_pair(e, n, seg_row);
+                        }
+                        const int off = lb == 3 ? 2 * cchunk : ((cchunk * kChunk) >> lb);
+                        const int sa = ((ra >> lb) << lnbc) + off, sb = ((rb >> lb) << lnbc) + off;
+                        const float MA0 = __uint_as_float(amax2d[sa]);
+                        const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
+                        const float MB0 = __uint_as_float(amax2d[sb]);
+                        const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                        Dest A, B;
+                        const int64_t la = lr0 + ra, lbr = lr0 + rb;
+                        const bool colfirst = lb == 3 || (col & bmask) == 0;
+                        uint8_t* sbase = (uint8_t*)p.row.scales;
+                        A.codes = (uint8_t*)p.row.codes + (grow0 + la) * p.row.codes_ld + (col >> 1);
+                        B.codes = (uint8_t*)p.row.codes + (grow0 + lbr) * p.row.codes_ld + (col >> 1);
+                        A.s0 = sbase + ((la >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
+                        B.s0 = sbase + ((lbr >> lb) * p.row.scales_ld + (col >> lb)) * SZ;
+                        A.s1 = A.s0 + SZ;
+                        B.s1 = B.s0 + SZ;
+                        A.valid = la < cnt && col_ok;
+                        B.valid = lbr < cnt && col_ok;
+                        A.w0 = (la & bmask) == 0 && colfirst;
+                        B.w0 = (lbr & bmask) == 0 && colfirst;
+                        A.w1 = (la & bmask) == 0 && lb == 3;
+                        B.w1 = (lbr & bmask) == 0 && lb == 3;
+                        A.lin0 = (uint64_t)la * (uint64_t)p.cols + (uint64_t)col;
+                        B.lin0 = (uint64_t)lbr * (uint64_t)p.cols + (uint64_t)col;
+                        emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 0u, grp_id);
+                    }
+                }
+            }
+            if (p.do_col) {
+                const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
+                const int lsd = p.is2d ? lb : lbwc;
+                const int64_t sc_ld = p.col_grouped ? (padded >> lsd) : p.col.scales_ld;
+                uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
+                uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lsd) * SZ : 0);
+                {
+                    const int lnbq = (TR == 128 ? 7 : 6) - lb;  // log2(TR / b)
+                    const int bmask = (1 << lb) - 1;
+                    for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
+                    __syncthreads();
+                    uint64_t keep[16];
+                    for (int k = 0; k < col_tasks; ++k) {
+                        const int t = warp + kWarps * k;
+                        const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
+                        const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
+                        uint32_t gw[16];
+                        uint64_t e[16];
+                        gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                        widen_cols(gw, mc, e);
+                        fwht_pair(e, n, rchunk & (S - 1));
+                        if (col_tasks == 1)
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) keep[i] = e[i];
+                        const int sa = (tcol >> lb) << lnbq, sb = ((tcol + 1) >> lb) << lnbq;
+                        if (lb == 3) {
+                            float a0, b0, a1, b1;
+                            amax_pair(e, 0, 8, a0, b0);
+                            amax_pair(e, 8, 16, a1, b1);
+                            post_amax(&amax2d[sa + 2 * rchunk], a0);
+                            post_amax(&amax2d[sa + 2 * rchunk + 1], a1);
+                            post_amax(&amax2d[sb + 2 * rchunk], b0);
+                            post_amax(&amax2d[sb + 2 * rchunk + 1], b1);
+                        } else {
+                            float a0, b0;
+                            amax_pair(e, 0, 16, a0, b0);
+                            post_amax(&amax2d[sa + ((rchunk * kChunk) >> lb)], a0);
+                            post_amax(&amax2d[sb + ((rchunk * kChunk) >> lb)], b0);
+                        }
+                    }
+                    __syncthreads();
+                    for (int k = 0; k < col_tasks; ++k) {
+                        const int t = warp + kWarps * k;
+                        const int tcol = 2 * (((t & ncb_mask) << (5 - lS)) + (lane >> lS));
+                        const int rchunk = ((t >> lncb) << lS) + (lane & (S - 1));
+                        uint64_t e[16];
+                        if (col_tasks == 1) {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) e[i] = keep[i];
+                        } else {
+                            uint32_t gw[16];
+                            gather_pair<TC>(tile_s, tcol, rchunk, gw);
+                            widen_cols(gw, mc, e);
+                            fwht_pair(e, n, rchunk & (S - 1));
+                        }
+                        const int off = lb == 3 ? 2 * rchunk : ((rchunk * kChunk) >> lb);
+                        const int sa = ((tcol >> lb) << lnbq) + off, sb = (((tcol + 1) >> lb) << lnbq) + off;
+                        const float MA0 = __uint_as_float(amax2d[sa]);
+                        const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
+                        const float MB0 = __uint_as_float(amax2d[sb]);
+                        const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                        const int64_t lrow = lr0 + rchunk * kChunk;
+                        const int64_t ca = c0 + tcol, cb = ca + 1;
+                        const bool rowfirst = lb == 3 || (lrow & bmask) == 0;
+                        Dest A, B;
+                        A.codes = gcodes + ca * out_ld + (lrow >> 1);
+                        B.codes = gcodes + cb * out_ld + (lrow >> 1);
+                        A.s0 = gscales + ((ca >> lb) * sc_ld + (lrow >> lb)) * SZ;
+                        B.s0 = gscales + ((cb >> lb) * sc_ld + (lrow >> lb)) * SZ;
+                        A.s1 = A.s0 + SZ;
+                        B.s1 = B.s0 + SZ;
+                        A.valid = lrow < padded && ca < p.cols;
+                        B.valid = lrow < padded && cb < p.cols;
+                        A.w0 = (ca & bmask) == 0 && rowfirst;
+                        B.w0 = (cb & bmask) == 0 && rowfirst;
+                        A.w1 = (ca & bmask) == 0 && lb == 3;
+                        B.w1 = (cb & bmask) == 0 && lb == 3;
+                        A.lin0 = (uint64_t)ca * (uint64_t)padded + (uint64_t)lrow;
+                        B.lin0 = A.lin0 + (uint64_t)padded;
+                        emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, p.sr_keys, 1u, grp_id);
+                    }
                 }
             }
         }

@@ -25,10 +25,10 @@ __device__ int g_rows_error;
 __device__ uint32_t g_rows_wait_limit = kWaitLimit;
 
 // ------------------------------------------------------ row-wise (lean)
-// Row-wise quantization with 1-D blocks and n <= 128, the FPROP operands'
-// case, over up to kMaxBatch independent tensors in one launch (their tiles
-// are numbered one after the other).  Same steps as the row pass above, with
-// 128 x 128 tiles fixed at compile time, tile coordinates and output pointers
+// Row-wise quantization (1-D blocks, or row-wise b x b blocks), over up to
+// kMaxBatch independent tensors in one launch (their tiles are numbered one
+// after the other).  The same steps as the general kernel's row pass, with the
+// tile shape fixed at compile time, tile coordinates and output pointers
 // advanced without division, and per-row bounds checks only on ragged tiles.
 struct RowsMaps {
     CUtensorMap m[kMaxBatch];
@@ -155,7 +155,9 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
         const int64_t sstep = (int64_t)kRPI * T.scales_ld * SZ;
         const bool wsc = (col & ((1 << lbw) - 1)) == 0;
         const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
-#pragma unroll
+        // one copy of the step for SR (its Philox rounds make the step long;
+        // two copies crowd the instruction cache), two otherwise
+#pragma unroll(SR ? 1 : 2)
         for (int it = 0; it < TR / (2 * kRPI); ++it) {
             const int ra = 2 * kRPI * it;
             uint32_t wa[8], wb[8];
@@ -267,6 +269,205 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
 // element in register moves).
 constexpr int kRowsCtas = 2, kRowsStages = 3;
 
+// n = 64 with 1-D blocks: a thread owns one 64-element segment of a row, so
+// the whole transform runs inside the thread and no lane exchanges data.  The
+// tile (128 rows x 128 columns) arrives as two 64-column TMA boxes with the
+// 128-byte swizzle (16-byte unit u of row r at u ^ (r % 8)), which spreads
+// the 16-byte loads of neighbouring rows over the banks.  The 64 values are
+// held as pairs (v_i, v_i+32): strides 1 .. 16 are paired adds, stride 32
+// adds the two halves of each pair.  The random signs come from a per-element
+// mask table in the kernel parameters (the same for every segment).
+template <int GRID, bool SR, int SF, int CTAS>
+__global__ void __launch_bounds__(kThreads, CTAS)
+quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
+    constexpr int TC = 128, TR = 128;
+    constexpr int kTileBytes = TR * TC * 2;
+    constexpr int SZ = SF == 0 ? 4 : 1;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;  // 128-byte swizzle: 1024-byte aligned stages
+    uint8_t* base = smem_raw + pad;
+    const int kStages = p.stages;
+    const uint32_t bars = smem_addr(base + kStages * kTileBytes);
+    const int tid = threadIdx.x;
+    const int r = tid >> 1, seg = tid & 1;
+    Fold fd;
+    fd.inv_s = p.inv_sqrt_n;
+    fd.pow4 = p.pow4;
+    fd.j = p.log4n;
+    fd.g = 0.0f;
+    const int lbw = p.lbw;
+
+    auto locate = [&](int tile, int& t, int& rt, int& ct) {
+        t = 0;
+        while (t + 1 < p.count && tile >= p.t[t + 1].tile0) ++t;
+        const int local = tile - p.t[t].tile0;
+        rt = local / p.t[t].col_tiles;
+        ct = local - rt * p.t[t].col_tiles;
+    };
+    auto issue = [&](int tile, int s) {
+        int t, rt, ct;
+        locate(tile, t, rt, ct);
+        const uint32_t bar = bars + 8u * s;
+        const uint32_t dst = smem_addr(base + s * kTileBytes);
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                ::"r"(dst + h * (kTileBytes / 2)), "l"((uint64_t)&maps.m[t]), "r"(ct * TC + 64 * h), "r"(rt * TR),
+                "r"(bar)
+                : "memory");
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kStages; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    griddep_wait();
+    griddep_launch();
+    const uint32_t wait_limit = g_rows_wait_limit;
+    if (tid == 0)
+        for (int s = 0; s < kStages; ++s) {
+            const int tile = blockIdx.x + s * gridDim.x;
+            if (tile < p.num_tiles) issue(tile, s);
+        }
+
+    int t = 0, rt = 0, ct = 0, step_r = 0, step_c = 0;
+    auto relocate = [&](int tile) {
+        locate(tile, t, rt, ct);
+        step_r = (int)gridDim.x / p.t[t].col_tiles;
+        step_c = (int)gridDim.x - step_r * p.t[t].col_tiles;
+        if (SF == 2) fd.g = __fdiv_rn(*p.t[t].amax, grid_qmax(GRID) * 448.0f);
+    };
+    if ((int)blockIdx.x < p.num_tiles) relocate(blockIdx.x);
+    int s = 0;
+    uint32_t phase = 0;
+    int i = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++i) {
+        if (i) {
+            ct += step_c;
+            rt += step_r;
+            if (ct >= p.t[t].col_tiles) {
+                ct -= p.t[t].col_tiles;
+                ++rt;
+            }
+            if (rt >= p.t[t].row_tiles) relocate(tile);
+        }
+        const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
+        if (!__syncthreads_and(landed)) {
+            if (tid == 0) atomicExch(&g_rows_error, 1);
+            break;
+        }
+        const RowsTensor& T = p.t[t];
+        const int row = rt * TR + r;
+        const int col = ct * TC + 64 * seg;
+        const bool valid = col < T.cols && row < T.rows;
+        // the segment: eight 16-byte units of row r in this half of the tile
+        const uint8_t* half = base + s * kTileBytes + seg * (kTileBytes / 2) + r * 128;
+        uint32_t w[32];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const uint4 u = *reinterpret_cast<const uint4*>(half + ((k ^ (r & 7)) << 4));
+            w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
+        }
+        // pairs (v_i, v_i+32) with the signs folded into the widening
+        uint64_t e[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {
+            const uint32_t wl = w[q >> 1], wh = w[(q + 32) >> 1];
+            const float lo = (q & 1) ? __uint_as_float((wl & 0xFFFF0000u) ^ p.smask[q])
+                                     : __uint_as_float(wl * 65536u + p.smask[q]);
+            const float hi = (q & 1) ? __uint_as_float((wh & 0xFFFF0000u) ^ p.smask[q + 32])
+                                     : __uint_as_float(wh * 65536u + p.smask[q + 32]);
+            e[q] = pk2(lo, hi);
+        }
+#pragma unroll
+        for (int h = 1; h < 32; h <<= 1) {
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+                if (q & h) continue;
+                const uint64_t a = e[q], b = e[q + h];
+                e[q] = add2(a, b);
+                e[q + h] = sub2(a, b);
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < 32; ++q) {  // stride 32: the two halves of each pair
+            float a, b;
+            up2(e[q], a, b);
+            e[q] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+        // block amax: (chunk 0, chunk 2) from pairs 0..15, (chunk 1, chunk 3) from pairs 16..31
+        float M0, M2, M1, M3;
+        amax_pair(e, 0, 16, M0, M2);
+        amax_pair(e + 16, 0, 16, M1, M3);
+        const bool b32 = lbw == 5;
+        if (b32) {
+            M0 = M1 = fmaxf(M0, M1);
+            M2 = M3 = fmaxf(M2, M3);
+        }
+        uint8_t* cp = T.codes + (int64_t)row * T.codes_ld + (GRID == 4 ? col : col >> 1);
+        uint8_t* sp = T.scales + ((int64_t)row * T.scales_ld + (col >> lbw)) * SZ;
+        const int cstride = GRID == 4 ? 16 : 8;  // code bytes per 16 elements
+        const uint64_t lin0 = (uint64_t)row * (uint64_t)T.cols + (uint64_t)col;
+        Dest A, B;
+        // chunks 0 and 2
+        A.codes = cp;
+        B.codes = cp + 2 * cstride;
+        A.s0 = A.s1 = sp;
+        B.s0 = B.s1 = sp + (b32 ? 1 : 2) * SZ;
+        A.valid = B.valid = valid;
+        A.w0 = B.w0 = true;
+        A.w1 = B.w1 = false;
+        A.lin0 = lin0;
+        B.lin0 = lin0 + 32;
+        emit_pair<GRID, SR, SF>(e, M0, M0, M2, M2, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+        // chunks 1 and 3 (their 1 x 32 scales were written with chunks 0 and 2)
+        A.codes = cp + cstride;
+        B.codes = cp + 3 * cstride;
+        A.s0 = A.s1 = sp + SZ;
+        B.s0 = B.s1 = sp + 3 * SZ;
+        A.w0 = B.w0 = !b32;
+        A.lin0 = lin0 + 16;
+        B.lin0 = lin0 + 48;
+        emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+        // everyone is done with stage s: refill it
+        __syncthreads();
+        if (tid == 0) {
+            const int next = tile + kStages * gridDim.x;
+            if (next < p.num_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, s);
+            }
+        }
+        if (++s == kStages) {
+            s = 0;
+            phase ^= 1u;
+        }
+    }
+    if (tid == 0)
+        for (int k = i; k < i + kStages; ++k) {
+            const int tile = blockIdx.x + k * gridDim.x;
+            if (tile >= p.num_tiles) break;
+            wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
+        }
+}
+
+template <int GRID, bool SR, int SF>
+static cudaError_t launch_rows64(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
+    p.stages = kRowsStages;
+    const size_t smem = (size_t)p.stages * 16384 * 2 + 8 * p.stages + 1024;
+    auto k = quantize_rows64_kernel<GRID, SR, SF, kRowsCtas>;
+    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    const int grid = p.num_tiles < kRowsCtas * num_sms ? p.num_tiles : kRowsCtas * num_sms;
+    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
+}
+
+
 template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
 static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
     constexpr int kTileElems = TWO_D ? 2 * (kThreads / (TC / kChunk)) * TC : 16384;
@@ -297,27 +498,38 @@ static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms,
 }
 
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
+    // n = 64 with 1-D blocks: the in-thread kernel, fed by two 64-column boxes with the 128-byte swizzle
+    const bool n64 = p.n == 64 && p.lb2d == 0 && p.tc == 128;
     RowsMaps maps;
     memset(&maps, 0, sizeof(maps));
     for (int t = 0; t < p.count; ++t) {
         const RowsTensor& T = p.t[t];
         if (!encode_map_2d(&maps.m[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, T.x, (uint64_t)T.cols, (uint64_t)T.rows,
-                           (uint64_t)T.ld * 2, (uint32_t)p.tc, (uint32_t)p.tr, CU_TENSOR_MAP_SWIZZLE_NONE))
+                           (uint64_t)T.ld * 2, n64 ? 64u : (uint32_t)p.tc, (uint32_t)p.tr,
+                           n64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
-#define UFP4_R(G)                                                                              \
+#define UFP4_R(G, FN)                                                                          \
     if (grid == G) {                                                                           \
-        if (sr) return sf == 2 ? launch_rows<G, true, 2>(maps, p, num_sms, st)                 \
-                     : sf == 1 ? launch_rows<G, true, 1>(maps, p, num_sms, st)                 \
-                               : launch_rows<G, true, 0>(maps, p, num_sms, st);                \
-        return sf == 2 ? launch_rows<G, false, 2>(maps, p, num_sms, st)                        \
-             : sf == 1 ? launch_rows<G, false, 1>(maps, p, num_sms, st)                        \
-                       : launch_rows<G, false, 0>(maps, p, num_sms, st);                       \
+        if (sr) return sf == 2 ? FN<G, true, 2>(maps, p, num_sms, st)                          \
+                     : sf == 1 ? FN<G, true, 1>(maps, p, num_sms, st)                          \
+                               : FN<G, true, 0>(maps, p, num_sms, st);                         \
+        return sf == 2 ? FN<G, false, 2>(maps, p, num_sms, st)                                 \
+             : sf == 1 ? FN<G, false, 1>(maps, p, num_sms, st)                                 \
+                       : FN<G, false, 0>(maps, p, num_sms, st);                                \
     }
-    UFP4_R(0)
-    UFP4_R(1)
-    UFP4_R(2)
-    UFP4_R(3)
+    if (n64) {
+        UFP4_R(0, launch_rows64)
+        UFP4_R(1, launch_rows64)
+        UFP4_R(2, launch_rows64)
+        UFP4_R(3, launch_rows64)
+        if (grid == 4 && !sr && sf == 1) return launch_rows64<4, false, 1>(maps, p, num_sms, st);  // MXFP8
+        return cudaErrorInvalidValue;
+    }
+    UFP4_R(0, launch_rows)
+    UFP4_R(1, launch_rows)
+    UFP4_R(2, launch_rows)
+    UFP4_R(3, launch_rows)
 #undef UFP4_R
     if (grid == 4 && !sr && sf == 1) return launch_rows<4, false, 1>(maps, p, num_sms, st);  // MXFP8
     return cudaErrorInvalidValue;
@@ -343,6 +555,9 @@ cudaError_t set_rows_wait_limit(uint32_t polls) {
 // that has not been loaded yet).
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
+    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 0, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 1, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 2, kRowsCtas>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128, false>);
@@ -369,6 +584,7 @@ cudaError_t preload_rows_kernels() {
     preload_rows<3, true>(&a);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas, 128, false>);
+    cudaFuncGetAttributes(&a, quantize_rows64_kernel<4, false, 1, kRowsCtas>);
     return cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 256, false>);
 }
 
