@@ -284,6 +284,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     p.n = n;
     p.inv_sqrt_n = inv_sqrt_n(n);
     make_sign_bits(desc->sign_seed, n, p.sign_bits);
+    for (int j = 0; j < 16; ++j) p.smask16[j] = ((p.sign_bits[0] >> j) & 1u) << 31;
     p.is2d = bs.is2d;
     p.b2d = bs.b2d;
     p.bw_row = bs.bw;

@@ -65,6 +65,7 @@ struct QuantParams {
     int n;
     float inv_sqrt_n;
     uint32_t sign_bits[8];
+    uint32_t smask16[16];  // n = 16: sign bit of element j of a segment (0x80000000 when eps_j = -1)
     int is2d, b2d;      // 2-D square blocks of side b2d
     int bw_row, bw_col; // 1-D block widths (or b2d)
     int col_seg_lanes;  // lanes sharing one column segment in the column pass
@@ -126,10 +127,17 @@ cudaError_t quant_error_read_clear(int* value);
 cudaError_t set_quant_wait_limit(uint32_t polls);
 uint32_t quant_wait_limit_default();
 // The row kernel's unit (quantize_rows.cu) keeps its own error word and wait
-// limit; the two functions above read and set both units'.
+// limit; the two functions above read and set every quantizer unit's.
 cudaError_t rows_error_read_clear(int* value);
 cudaError_t set_rows_wait_limit(uint32_t polls);
 cudaError_t preload_rows_kernels();
+// The general kernel's SR instantiations (quantize_sr.cu), with their own
+// error word and wait limit.
+cudaError_t launch_quantize_sr(const CUtensorMap& map, const QuantParams& p, int grid, bool po2, int tc,
+                               int num_tiles, int num_sms, cudaStream_t st);
+cudaError_t sr_error_read_clear(int* value);
+cudaError_t set_sr_wait_limit(uint32_t polls);
+cudaError_t preload_quantize_sr_kernels();
 
 // 2-D tiled tensor map (TMA) over a row-major matrix: inner x outer elements,
 // pitch bytes between rows, boxes of box_inner x box_outer elements.

@@ -83,13 +83,25 @@ __device__ __forceinline__ int po2_byte(float M) {
 // Every v_i is E + o_i with E = 0x4B400000 and o_i < 16, so a tree of
 // multiply-adds (x16, x256, x65536) lines the nibbles up and leaves the
 // constant E (17 * 257 * ...) in bits 22 and up, removed at the end.
+template <uint32_t E = 0x4B400000u>
 __device__ __forceinline__ uint32_t pack_offsets8(const uint32_t* v) {
-    constexpr uint32_t E = 0x4B400000u;
     constexpr uint32_t bias = E * 17u * 257u;  // mod 2^32; the low 22 bits are zero
     const uint32_t p0 = v[1] * 16u + v[0], p1 = v[3] * 16u + v[2];
     const uint32_t p2 = v[5] * 16u + v[4], p3 = v[7] * 16u + v[6];
     const uint32_t q0 = p1 * 256u + p0, q1 = p3 * 256u + p2;
     return q1 * 65536u + q0 - bias;
+}
+
+// Paired subtractions with directed rounding (round up / round down).
+__device__ __forceinline__ uint64_t sub2_rp(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rp.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+__device__ __forceinline__ uint64_t sub2_rm(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("sub.rm.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
 }
 
 // Scale, round, pack and store two 16-element vectors a and b held as pairs
@@ -134,40 +146,32 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
     }
 }
 
-// Stochastic rounding of 16 scaled values to packed codes.  With a =
-// min(|t|, qmax) in units of the local level gap g (v = a / g, between the
-// levels floor(v) and floor(v) + 1), round up iff u < (v - floor(v)) * 2^16,
-// u the element's 16 random bits.  For integer u that is u < ceil(v * 2^16) -
-// floor(v) * 2^16, so the level index is k = (ceil(v * 2^16) + 2^16 - 1 - u)
-// >> 16 (floor(v) or floor(v) + 1), and ceil(v * 2^16) is the low mantissa
-// bits of one fma rounded upward, v * 2^16 + 2^23 (exact: v * 2^16 < 2^23).
-// Each nibble is sign * 8 + k (sign-magnitude), the nibbles line up through a
-// tree of multiply-adds, and a zero level loses its sign word-wise.  CLAMP:
-// |t| may exceed the largest level by an ulp (fp32 and two-level scales);
-// with UE8M0 scales |t| <= qmax holds exactly.
-template <int GRID, bool CLAMP>
+// Stochastic rounding of 16 scaled values to packed E2M1 codes (the uniform
+// grids take the fma path in emit_pair).  With a = min(|t|, qmax) in units of
+// the local level gap g (v = a / g, between the levels floor(v) and
+// floor(v) + 1), round up iff u < (v - floor(v)) * 2^16, u the element's 16
+// random bits.  For integer u that is u < ceil(v * 2^16) - floor(v) * 2^16, so
+// the level index is k = (ceil(v * 2^16) + 2^16 - 1 - u) >> 16 (floor(v) or
+// floor(v) + 1), and ceil(v * 2^16) is the low mantissa bits of one fma
+// rounded upward, v * 2^16 + 2^23 (exact: v * 2^16 < 2^23).  Each nibble is
+// sign * 8 + k (sign-magnitude), the nibbles line up through a tree of
+// multiply-adds, and a zero level loses its sign word-wise.
+template <int GRID>
 __device__ __forceinline__ uint2 sr_vec(const float t[16], const uint32_t w[8]) {
+    static_assert(GRID == 2 || GRID == 3, "E2M1 grids only");
     constexpr float qmax = grid_qmax(GRID);
     uint32_t nib[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         const uint32_t u = (i & 1) ? (w[i >> 1] >> 16) : (w[i >> 1] & 0xFFFFu);
         const float ti = t[i];
-        uint32_t idx;
-        if (GRID >= 2) {
-            // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
-            const float a = fminf(fabsf(ti), qmax);
-            const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-            const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-            const uint32_t vb = __float_as_uint(__fmaf_ru(__fmul_rn(a, inv), 65536.0f, 8388608.0f));
-            const uint32_t k = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
-            idx = cvt_e2m1x2(0.0f, __fmul_rn((float)k, gap)) & 7u;
-        } else {
-            // uniform grids: t is already in units of the step (largest level 7)
-            const float a = CLAMP ? fminf(fabsf(ti), 7.0f) : fabsf(ti);
-            const uint32_t vb = __float_as_uint(__fmaf_ru(a, 65536.0f, 8388608.0f));
-            idx = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
-        }
+        // E2M1 gaps: 0.5 below 2, 1 on [2,4), 2 on [4,6]
+        const float a = fminf(fabsf(ti), qmax);
+        const float gap = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+        const float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+        const uint32_t vb = __float_as_uint(__fmaf_ru(__fmul_rn(a, inv), 65536.0f, 8388608.0f));
+        const uint32_t k = (vb - 0x4B000000u + 0xFFFFu - u) >> 16;
+        const uint32_t idx = cvt_e2m1x2(0.0f, __fmul_rn((float)k, gap)) & 7u;
         nib[i] = (__float_as_uint(ti) >> 31) * 8u + idx;
     }
     auto pack8 = [](const uint32_t* v) {
@@ -175,18 +179,24 @@ __device__ __forceinline__ uint2 sr_vec(const float t[16], const uint32_t w[8]) 
         const uint32_t q1 = (v[7] * 16u + v[6]) * 256u + (v[5] * 16u + v[4]);
         return q1 * 65536u + q0;
     };
-    uint32_t out[2] = {clear_negative_zero(pack8(nib)), clear_negative_zero(pack8(nib + 8))};
-    if (GRID == 1) {
-        out[0] = signmag_to_twos(out[0]);
-        out[1] = signmag_to_twos(out[1]);
-    }
-    return make_uint2(out[0], out[1]);
+    return make_uint2(clear_negative_zero(pack8(nib)), clear_negative_zero(pack8(nib + 8)));
+}
+
+// SR draws of the two vectors of one emit_pair call (16 elements each).  The
+// caller draws them before it widens and transforms the input: they depend
+// only on the output positions, and the generator's registers are then free
+// again when the transformed values are live.
+struct SrDraws {
+    uint32_t a[8], b[8];
+};
+__device__ __forceinline__ void draw_pair(SrDraws& d, const SrKeys& keys, const Dest& A, const Dest& B,
+                                          uint32_t stream, uint32_t group) {
+    sr_draws16x2(keys, A.lin0, B.lin0, stream, group, d.a, d.b);
 }
 
 template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
-                                          const Fold& fd, const Dest& A, const Dest& B,
-                                          const SrKeys& sr_keys, uint32_t stream, uint32_t group) {
+                                          const Fold& fd, const Dest& A, const Dest& B, const SrDraws& dr) {
     // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
     // to the value in units of the grid step (below): INT4 k, E1M2 4 t
     constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
@@ -250,9 +260,63 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
             return (w ^ (neg * 7u + 0x88888888u)) + neg;
         };
         if (A.valid)
-            *reinterpret_cast<uint2*>(A.codes) = make_uint2(finish(pack_offsets8(va)), finish(pack_offsets8(va + 8)));
+            *reinterpret_cast<uint2*>(A.codes) = make_uint2(finish(pack_offsets8<>(va)), finish(pack_offsets8<>(va + 8)));
         if (B.valid)
-            *reinterpret_cast<uint2*>(B.codes) = make_uint2(finish(pack_offsets8(vb)), finish(pack_offsets8(vb + 8)));
+            *reinterpret_cast<uint2*>(B.codes) = make_uint2(finish(pack_offsets8<>(vb)), finish(pack_offsets8<>(vb + 8)));
+        return;
+    }
+    if (SR && GRID <= 1) {
+        // SR on the uniform grids (t in units of the step, largest level 7),
+        // on the fma pipe.  With C = ceil(|t| 2^16) and u the element's 16-bit
+        // draw, the level index is k = ceil((C - u) / 2^16) (u < the fraction
+        // of |t| above floor(|t|), times 2^16, rounds up; see sr_vec).
+        //  X = rm(192 + u 2^-16 - |t|) = 192 + (u - C) 2^-16: the addend's
+        //      bits are 0x4340 above u, and its unit 2^-16 sets the grid;
+        //  K = rp(2^23 + 196 - X) = 2^23 + 4 + k;
+        //  V = K - copysign(4, t) = 2^23 + 8 s + k, s the sign bit.
+        // The low nibbles of V are sign-magnitude codes (a zero level with
+        // s = 1 is cleared below).  With UE8M0 scales t = y r is exact, so
+        // the first step is one fma on y; otherwise t = fp32(y r) is formed
+        // and clamped to 7 first, as in the definition.
+        const uint32_t* wa = dr.a;
+        const uint32_t* wb = dr.b;
+        const uint64_t c196 = pk2(8388804.0f, 8388804.0f);
+        const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
+        uint32_t va[16], vb[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t sel = (i & 1) ? 0x7632u : 0x7610u;
+            const float ua = __uint_as_float(__byte_perm(wa[i >> 1], 0x43400000u, sel));
+            const float ub = __uint_as_float(__byte_perm(wb[i >> 1], 0x43400000u, sel));
+            float ya, yb;
+            uint64_t x;
+            if (SF == 1) {
+                up2(e[i], ya, yb);
+                x = pk2(__fmaf_rd(-fabsf(ya), i < 8 ? ra0 : ra1, ua), __fmaf_rd(-fabsf(yb), i < 8 ? rb0 : rb1, ub));
+            } else {
+                up2(mul2(e[i], i < 8 ? q0 : q1), ya, yb);
+                x = sub2_rm(pk2(ua, ub), pk2(fminf(fabsf(ya), 7.0f), fminf(fabsf(yb), 7.0f)));
+            }
+            const uint64_t cs = pk2(__uint_as_float((__float_as_uint(ya) & 0x80000000u) | 0x40800000u),
+                                    __uint_as_float((__float_as_uint(yb) & 0x80000000u) | 0x40800000u));
+            float a, b;
+            up2(sub2(sub2_rp(c196, x), cs), a, b);
+            va[i] = __float_as_uint(a);
+            vb[i] = __float_as_uint(b);
+        }
+        uint32_t oa[2] = {clear_negative_zero(pack_offsets8<0x4B000000u>(va)),
+                          clear_negative_zero(pack_offsets8<0x4B000000u>(va + 8))};
+        uint32_t ob[2] = {clear_negative_zero(pack_offsets8<0x4B000000u>(vb)),
+                          clear_negative_zero(pack_offsets8<0x4B000000u>(vb + 8))};
+        if (GRID == 1) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                oa[h] = signmag_to_twos(oa[h]);
+                ob[h] = signmag_to_twos(ob[h]);
+            }
+        }
+        if (A.valid) *reinterpret_cast<uint2*>(A.codes) = make_uint2(oa[0], oa[1]);
+        if (B.valid) *reinterpret_cast<uint2*>(B.codes) = make_uint2(ob[0], ob[1]);
         return;
     }
     const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
@@ -260,11 +324,9 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
 #pragma unroll
     for (int i = 0; i < 16; ++i) up2(mul2(e[i], i < 8 ? q0 : q1), ta[i], tb[i]);
     uint2 ca, cb;
-    if (SR) {
-        uint32_t wa[8], wb[8];
-        sr_draws16x2(sr_keys, A.lin0, B.lin0, stream, group, wa, wb);
-        ca = sr_vec<GRID, SF != 1>(ta, wa);
-        cb = sr_vec<GRID, SF != 1>(tb, wb);
+    if constexpr (SR && (GRID == 2 || GRID == 3)) {
+        ca = sr_vec<GRID>(ta, dr.a);
+        cb = sr_vec<GRID>(tb, dr.b);
     } else {
         ca = make_uint2(rtne8<GRID>(ta[0], ta[1], ta[2], ta[3], ta[4], ta[5], ta[6], ta[7]),
                         rtne8<GRID>(ta[8], ta[9], ta[10], ta[11], ta[12], ta[13], ta[14], ta[15]));

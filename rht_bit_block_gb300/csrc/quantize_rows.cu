@@ -71,8 +71,8 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     fd.j = p.log4n;
     fd.g = 0.0f;
     const int seg_row = (cchunk * kChunk % (n > kChunk ? n : kChunk)) / kChunk;
-    SignMasks mrow;
-    {
+    SignMasks mrow;  // n = 16 reads its masks from the kernel parameters (p.smask)
+    if (!N16) {
         const int pos = (cchunk * kChunk) & 255;
         make_masks((p.sign_bits[pos >> 5] >> (pos & 31)) & 0xFFFFu, mrow);
     }
@@ -160,6 +160,29 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
 #pragma unroll(SR ? 1 : 2)
         for (int it = 0; it < TR / (2 * kRPI); ++it) {
             const int ra = 2 * kRPI * it;
+            Dest A, B;
+            A.codes = cp + (2 * it) * cstep;
+            B.codes = A.codes + cstep;
+            if (TWO_D) {
+                // one UE8M0 byte per b x b block, written by its top-left thread
+                const int rA = row0 + r0, rB = rA + kRPI;
+                A.s0 = A.s1 = T.scales + (int64_t)(rA >> lb) * T.scales_ld + (col >> lb);
+                B.s0 = B.s1 = T.scales + (int64_t)(rB >> lb) * T.scales_ld + (col >> lb);
+                const bool cfirst = (col & ((1 << lb) - 1)) == 0;
+                A.w0 = cfirst && (rA & ((1 << lb) - 1)) == 0;
+                B.w0 = cfirst && (rB & ((1 << lb) - 1)) == 0;
+            } else {
+                A.s0 = A.s1 = sp + (2 * it) * sstep;
+                B.s0 = B.s1 = A.s0 + sstep;
+                A.w0 = B.w0 = wsc;
+            }
+            A.valid = col_ok && (full || ra < left);
+            B.valid = col_ok && (full || ra + kRPI < left);
+            A.w1 = B.w1 = false;
+            A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
+            B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
+            SrDraws dr;
+            if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
             uint32_t wa[8], wb[8];
             uint64_t e[16];
             const uint4* pa = reinterpret_cast<const uint4*>(src + ra * TC);
@@ -169,7 +192,8 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             wa[4] = a1.x; wa[5] = a1.y; wa[6] = a1.z; wa[7] = a1.w;
             wb[0] = b0.x; wb[1] = b0.y; wb[2] = b0.z; wb[3] = b0.w;
             wb[4] = b1.x; wb[5] = b1.y; wb[6] = b1.z; wb[7] = b1.w;
-            widen_rows(wa, wb, mrow, e);
+            if (N16) widen_rows_c(wa, wb, p.smask, e);
+            else widen_rows(wa, wb, mrow, e);
             float Ma, Mb;
             if (TWO_D) {
                 if (N16) fwht_pair16(e);
@@ -216,28 +240,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
                 fwht_pair(e, n, seg_row);
                 amax_1d_pair(e, 1 << lbw, Ma, Mb);
             }
-            Dest A, B;
-            A.codes = cp + (2 * it) * cstep;
-            B.codes = A.codes + cstep;
-            if (TWO_D) {
-                // one UE8M0 byte per b x b block, written by its top-left thread
-                const int rA = row0 + r0, rB = rA + kRPI;
-                A.s0 = A.s1 = T.scales + (int64_t)(rA >> lb) * T.scales_ld + (col >> lb);
-                B.s0 = B.s1 = T.scales + (int64_t)(rB >> lb) * T.scales_ld + (col >> lb);
-                const bool cfirst = (col & ((1 << lb) - 1)) == 0;
-                A.w0 = cfirst && (rA & ((1 << lb) - 1)) == 0;
-                B.w0 = cfirst && (rB & ((1 << lb) - 1)) == 0;
-            } else {
-                A.s0 = A.s1 = sp + (2 * it) * sstep;
-                B.s0 = B.s1 = A.s0 + sstep;
-                A.w0 = B.w0 = wsc;
-            }
-            A.valid = col_ok && (full || ra < left);
-            B.valid = col_ok && (full || ra + kRPI < left);
-            A.w1 = B.w1 = false;
-            A.lin0 = (uint64_t)(row0 + r0 + ra) * (uint64_t)T.cols + (uint64_t)col;
-            B.lin0 = A.lin0 + (uint64_t)kRPI * (uint64_t)T.cols;
-            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, dr);
         }
         // everyone is done with stage s: refill it
         __syncthreads();
@@ -424,7 +427,11 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
         A.w1 = B.w1 = false;
         A.lin0 = lin0;
         B.lin0 = lin0 + 32;
-        emit_pair<GRID, SR, SF>(e, M0, M0, M2, M2, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+        {
+            SrDraws dr;
+            if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+            emit_pair<GRID, SR, SF>(e, M0, M0, M2, M2, false, fd, A, B, dr);
+        }
         // chunks 1 and 3 (their 1 x 32 scales were written with chunks 0 and 2)
         A.codes = cp + cstride;
         B.codes = cp + 3 * cstride;
@@ -433,7 +440,11 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
         A.w0 = B.w0 = !b32;
         A.lin0 = lin0 + 16;
         B.lin0 = lin0 + 48;
-        emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, p.sr_keys, 0u, (uint32_t)p.group);
+        {
+            SrDraws dr;
+            if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+            emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, dr);
+        }
         // everyone is done with stage s: refill it
         __syncthreads();
         if (tid == 0) {

@@ -295,6 +295,23 @@ __device__ __forceinline__ void widen_rows(const uint32_t wa[8], const uint32_t 
     }
 }
 
+// The same with the masks of the 16 elements read from kernel parameters
+// (constant bank) instead of registers: mask[j] is 0x80000000 when eps_j = -1.
+__device__ __forceinline__ void widen_rows_c(const uint32_t wa[8], const uint32_t wb[8], const uint32_t* mask,
+                                             uint64_t e[16]) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        e[2 * k] = pk2(__uint_as_float(wa[k] * 65536u + mask[2 * k]), __uint_as_float(wb[k] * 65536u + mask[2 * k]));
+        e[2 * k + 1] = pk2(__uint_as_float((wa[k] & 0xFFFF0000u) ^ mask[2 * k + 1]),
+                           __uint_as_float((wb[k] & 0xFFFF0000u) ^ mask[2 * k + 1]));
+    }
+}
+__device__ __forceinline__ void widen_cols_c(const uint32_t g[16], const uint32_t* mask, uint64_t e[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        e[i] = pk2(__uint_as_float(g[i] * 65536u + mask[i]), __uint_as_float((g[i] & 0xFFFF0000u) ^ mask[i]));
+}
+
 // Columns: word g[i] holds row i of column a (low half) and column b (high half).
 __device__ __forceinline__ void widen_cols(const uint32_t g[16], const SignMasks& m, uint64_t e[16]) {
 #pragma unroll
