@@ -272,19 +272,26 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
 // element in register moves).
 constexpr int kRowsCtas = 2, kRowsStages = 3;
 
-// n = 64 with 1-D blocks: a thread owns one 64-element segment of a row, so
-// the whole transform runs inside the thread and no lane exchanges data.  The
-// tile (128 rows x 128 columns) arrives as two 64-column TMA boxes with the
-// 128-byte swizzle (16-byte unit u of row r at u ^ (r % 8)), which spreads
-// the 16-byte loads of neighbouring rows over the banks.  The 64 values are
-// held as pairs (v_i, v_i+32): strides 1 .. 16 are paired adds, stride 32
-// adds the two halves of each pair.  The random signs come from a per-element
-// mask table in the kernel parameters (the same for every segment).
-template <int GRID, bool SR, int SF, int CTAS>
+// n = 64 and n = 256 with 1-D blocks: a thread owns one 64-element segment of
+// a row.  QN segments make one tile row (QN = 2: 128 columns, n = 64; QN = 4:
+// 256 columns, n = 256), so the tile is 128 x 128 or 64 x 256.  It arrives as
+// QN 64-column TMA boxes with the 128-byte swizzle (16-byte unit u of row r at
+// u ^ (r % 8)).  The eight threads of a quarter-warp take the same segment of
+// eight consecutive rows, so their 16-byte loads fall on eight different bank
+// groups.  The 64 values are held as pairs (v_i, v_i+32): strides 1 .. 16 are
+// paired adds, stride 32 adds the two halves of each pair, and for n = 256
+// strides 64 and 128 pair the thread with the lanes holding the neighbouring
+// segments (lane ^ 8, lane ^ 16).  The random signs: n = 64 reads a per-
+// element mask table from the kernel parameters (the same for every segment);
+// n = 256 from a table in shared memory, one 64-entry set per segment.
+template <int GRID, bool SR, int SF, int CTAS, int QN>
 __global__ void __launch_bounds__(kThreads, CTAS)
-quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
-    constexpr int TC = 128, TR = 128;
+quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
+    static_assert(QN == 2 || QN == 4, "two or four segments per tile row");
+    constexpr int TC = 64 * QN, TR = 16384 / TC;
+    constexpr int kLQ = QN == 2 ? 1 : 2;
     constexpr int kTileBytes = TR * TC * 2;
+    constexpr int kBoxBytes = TR * 128;
     constexpr int SZ = SF == 0 ? 4 : 1;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_addr(smem_raw);
@@ -292,8 +299,10 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
     uint8_t* base = smem_raw + pad;
     const int kStages = p.stages;
     const uint32_t bars = smem_addr(base + kStages * kTileBytes);
+    uint32_t* sgn_tab = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes + 64);  // n = 256: [segment][j]
     const int tid = threadIdx.x;
-    const int r = tid >> 1, seg = tid & 1;
+    const int seg = (tid >> 3) & (QN - 1);
+    const int r = (tid & 7) + 8 * (tid >> (3 + kLQ));
     Fold fd;
     fd.inv_s = p.inv_sqrt_n;
     fd.pow4 = p.pow4;
@@ -315,10 +324,10 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
         const uint32_t dst = smem_addr(base + s * kTileBytes);
         asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(kTileBytes) : "memory");
 #pragma unroll
-        for (int h = 0; h < 2; ++h)
+        for (int h = 0; h < QN; ++h)
             asm volatile(
                 "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-                ::"r"(dst + h * (kTileBytes / 2)), "l"((uint64_t)&maps.m[t]), "r"(ct * TC + 64 * h), "r"(rt * TR),
+                ::"r"(dst + h * kBoxBytes), "l"((uint64_t)&maps.m[t]), "r"(ct * TC + 64 * h), "r"(rt * TR),
                 "r"(bar)
                 : "memory");
     };
@@ -328,6 +337,8 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    if (QN == 4)  // mask of element j of segment q: 0x80000000 when eps_(64 q + j) = -1
+        sgn_tab[tid] = ((p.sign_bits[tid >> 5] >> (tid & 31)) & 1u) << 31;
     __syncthreads();
     griddep_wait();
     griddep_launch();
@@ -368,23 +379,23 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
         const int row = rt * TR + r;
         const int col = ct * TC + 64 * seg;
         const bool valid = col < T.cols && row < T.rows;
-        // the segment: eight 16-byte units of row r in this half of the tile
-        const uint8_t* half = base + s * kTileBytes + seg * (kTileBytes / 2) + r * 128;
+        // the segment: eight 16-byte units of row r in box seg
+        const uint8_t* box = base + s * kTileBytes + seg * kBoxBytes + r * 128;
         uint32_t w[32];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-            const uint4 u = *reinterpret_cast<const uint4*>(half + ((k ^ (r & 7)) << 4));
+            const uint4 u = *reinterpret_cast<const uint4*>(box + ((k ^ (r & 7)) << 4));
             w[4 * k] = u.x; w[4 * k + 1] = u.y; w[4 * k + 2] = u.z; w[4 * k + 3] = u.w;
         }
         // pairs (v_i, v_i+32) with the signs folded into the widening
         uint64_t e[32];
+        const uint32_t* sm = QN == 4 ? sgn_tab + 64 * seg : p.smask;
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
             const uint32_t wl = w[q >> 1], wh = w[(q + 32) >> 1];
-            const float lo = (q & 1) ? __uint_as_float((wl & 0xFFFF0000u) ^ p.smask[q])
-                                     : __uint_as_float(wl * 65536u + p.smask[q]);
-            const float hi = (q & 1) ? __uint_as_float((wh & 0xFFFF0000u) ^ p.smask[q + 32])
-                                     : __uint_as_float(wh * 65536u + p.smask[q + 32]);
+            const uint32_t ml = sm[q], mh = sm[q + 32];
+            const float lo = (q & 1) ? __uint_as_float((wl & 0xFFFF0000u) ^ ml) : __uint_as_float(wl * 65536u + ml);
+            const float hi = (q & 1) ? __uint_as_float((wh & 0xFFFF0000u) ^ mh) : __uint_as_float(wh * 65536u + mh);
             e[q] = pk2(lo, hi);
         }
 #pragma unroll
@@ -402,6 +413,20 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
             float a, b;
             up2(e[q], a, b);
             e[q] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
+        }
+        if (QN == 4) {
+            // strides 64 and 128: the lower segment of a pair forms a + b, the
+            // upper one a - b, i.e. o + s e with s = +1 or -1 (exact product)
+#pragma unroll
+            for (int lm = 1; lm <= 2; lm <<= 1) {
+                const float sg = (seg & lm) ? -1.0f : 1.0f;
+                const uint64_t s2 = pk2(sg, sg);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) {
+                    const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)e[q], 8 * lm);
+                    e[q] = fma2(s2, e[q], o);
+                }
+            }
         }
         // block amax: (chunk 0, chunk 2) from pairs 0..15, (chunk 1, chunk 3) from pairs 16..31
         float M0, M2, M1, M3;
@@ -468,10 +493,11 @@ quantize_rows64_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p
 }
 
 template <int GRID, bool SR, int SF>
-static cudaError_t launch_rows64(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
+static cudaError_t launch_rows_seg(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
     p.stages = kRowsStages;
-    const size_t smem = (size_t)p.stages * 16384 * 2 + 8 * p.stages + 1024;
-    auto k = quantize_rows64_kernel<GRID, SR, SF, kRowsCtas>;
+    const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 1024;  // ring, barriers, sign table, alignment
+    auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kRowsCtas, 4>
+                        : quantize_rows_seg_kernel<GRID, SR, SF, kRowsCtas, 2>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < kRowsCtas * num_sms ? p.num_tiles : kRowsCtas * num_sms;
@@ -509,15 +535,15 @@ static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms,
 }
 
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
-    // n = 64 with 1-D blocks: the in-thread kernel, fed by two 64-column boxes with the 128-byte swizzle
-    const bool n64 = p.n == 64 && p.lb2d == 0 && p.tc == 128;
+    // n = 64 and n = 256 with 1-D blocks: the segment kernel, fed by 64-column boxes with the 128-byte swizzle
+    const bool seg_kernel = p.lb2d == 0 && ((p.n == 64 && p.tc == 128) || (p.n == 256 && p.tc == 256));
     RowsMaps maps;
     memset(&maps, 0, sizeof(maps));
     for (int t = 0; t < p.count; ++t) {
         const RowsTensor& T = p.t[t];
         if (!encode_map_2d(&maps.m[t], CU_TENSOR_MAP_DATA_TYPE_UINT16, T.x, (uint64_t)T.cols, (uint64_t)T.rows,
-                           (uint64_t)T.ld * 2, n64 ? 64u : (uint32_t)p.tc, (uint32_t)p.tr,
-                           n64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
+                           (uint64_t)T.ld * 2, seg_kernel ? 64u : (uint32_t)p.tc, seg_kernel ? (p.n == 256 ? 64u : 128u) : (uint32_t)p.tr,
+                           seg_kernel ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
             return cudaErrorInvalidValue;
     }
 #define UFP4_R(G, FN)                                                                          \
@@ -529,12 +555,12 @@ cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int n
              : sf == 1 ? FN<G, false, 1>(maps, p, num_sms, st)                                 \
                        : FN<G, false, 0>(maps, p, num_sms, st);                                \
     }
-    if (n64) {
-        UFP4_R(0, launch_rows64)
-        UFP4_R(1, launch_rows64)
-        UFP4_R(2, launch_rows64)
-        UFP4_R(3, launch_rows64)
-        if (grid == 4 && !sr && sf == 1) return launch_rows64<4, false, 1>(maps, p, num_sms, st);  // MXFP8
+    if (seg_kernel) {
+        UFP4_R(0, launch_rows_seg)
+        UFP4_R(1, launch_rows_seg)
+        UFP4_R(2, launch_rows_seg)
+        UFP4_R(3, launch_rows_seg)
+        if (grid == 4 && !sr && sf == 1) return launch_rows_seg<4, false, 1>(maps, p, num_sms, st);  // MXFP8
         return cudaErrorInvalidValue;
     }
     UFP4_R(0, launch_rows)
@@ -566,9 +592,12 @@ cudaError_t set_rows_wait_limit(uint32_t polls) {
 // that has not been loaded yet).
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
-    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 0, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 1, kRowsCtas>);
-    cudaFuncGetAttributes(a, quantize_rows64_kernel<G, SR, 2, kRowsCtas>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kRowsCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kRowsCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kRowsCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kRowsCtas, 4>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kRowsCtas, 4>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kRowsCtas, 4>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128, false>);
@@ -595,7 +624,8 @@ cudaError_t preload_rows_kernels() {
     preload_rows<3, true>(&a);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas, 128, false>);
-    cudaFuncGetAttributes(&a, quantize_rows64_kernel<4, false, 1, kRowsCtas>);
+    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 2>);
+    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 4>);
     return cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 256, false>);
 }
 

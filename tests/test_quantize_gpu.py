@@ -274,13 +274,15 @@ def test_large_sweep_sampled_rows(n):
 
 
 # ----------------------------------------- row-wise kernel and batched calls
-# Row-wise calls with 1-D blocks and n <= 128 run the lean row kernel; these
-# cover its ragged row and column tiles, padded leading dimensions and every
-# rounding and scale mode.
+# Row-wise calls with 1-D blocks run the row kernels (n = 64 and n = 256: the
+# segment kernel, 128 x 128 and 64 x 256 tiles); these cover their ragged row
+# and column tiles, padded leading dimensions and every rounding and scale
+# mode.
 @pytest.mark.parametrize("grid", GRIDS)
 @pytest.mark.parametrize("rounding", [RTNE, SR])
 @pytest.mark.parametrize("block,n,cols", [((1, 16), 16, 576), ((1, 32), 64, 576), ((1, 16), 128, 640),
-                                          ((1, 32), 1, 544)])
+                                          ((1, 32), 1, 544), ((1, 16), 64, 704), ((1, 16), 256, 768),
+                                          ((1, 32), 256, 512)])
 def test_rowwise_ragged_tiles(grid, rounding, block, n, cols):
     x = inputs.tiny_check(300, cols)
     fmt = PO2 if grid.startswith("e2m1") else FP32
