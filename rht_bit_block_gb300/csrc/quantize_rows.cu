@@ -284,6 +284,9 @@ constexpr int kRowsCtas = 2, kRowsStages = 3;
 // segments (lane ^ 8, lane ^ 16).  The random signs: n = 64 reads a per-
 // element mask table from the kernel parameters (the same for every segment);
 // n = 256 from a table in shared memory, one 64-entry set per segment.
+// No CTA barrier per tile: each warp waits on the stage's TMA barrier itself
+// and, when done with the stage, arrives on the stage's "empty" barrier;
+// thread 0 waits on that one before it refills the stage.
 template <int GRID, bool SR, int SF, int CTAS, int QN>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
@@ -298,8 +301,11 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;  // 128-byte swizzle: 1024-byte aligned stages
     uint8_t* base = smem_raw + pad;
     const int kStages = p.stages;
+    // full barriers (TMA landed) at bars + 8 s, empty barriers (every warp
+    // done with the stage) at bars + 32 + 8 s, s < kStages <= 4
     const uint32_t bars = smem_addr(base + kStages * kTileBytes);
-    uint32_t* sgn_tab = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes + 64);  // n = 256: [segment][j]
+    const uint32_t empties = bars + 32u;
+    uint32_t* sgn_tab = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes + 64);  // n = 256: [segment][j], 16-byte aligned
     const int tid = threadIdx.x;
     const int seg = (tid >> 3) & (QN - 1);
     const int r = (tid & 7) + 8 * (tid >> (3 + kLQ));
@@ -333,8 +339,10 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (QN == 4)  // mask of element j of segment q: 0x80000000 when eps_(64 q + j) = -1
@@ -343,10 +351,15 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     griddep_wait();
     griddep_launch();
     const uint32_t wait_limit = g_rows_wait_limit;
+    const int lane = tid & 31;
+    int issued = 0;  // tiles of this CTA issued so far (thread 0)
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
-            if (tile < p.num_tiles) issue(tile, s);
+            if (tile < p.num_tiles) {
+                issue(tile, s);
+                issued = s + 1;
+            }
         }
 
     int t = 0, rt = 0, ct = 0, step_r = 0, step_c = 0;
@@ -370,9 +383,12 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
             }
             if (rt >= p.t[t].row_tiles) relocate(tile);
         }
+        // no CTA barrier per tile: each warp waits for the copy itself, and
+        // a warp whose wait gave up leaves the loop (the others then give up
+        // on the stages it no longer releases)
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (!__syncthreads_and(landed)) {
-            if (tid == 0) atomicExch(&g_rows_error, 1);
+        if (!__all_sync(0xFFFFFFFFu, landed)) {
+            if (lane == 0) atomicExch(&g_rows_error, 1);
             break;
         }
         const RowsTensor& T = p.t[t];
@@ -389,11 +405,21 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
         }
         // pairs (v_i, v_i+32) with the signs folded into the widening
         uint64_t e[32];
-        const uint32_t* sm = QN == 4 ? sgn_tab + 64 * seg : p.smask;
+        uint32_t msk[QN == 4 ? 64 : 1];
+        if (QN == 4) {
+            const uint4* sm4 = reinterpret_cast<const uint4*>(sgn_tab + 64 * seg);
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const uint4 v = sm4[k];
+                msk[4 * k] = v.x; msk[4 * k + 1] = v.y; msk[4 * k + 2] = v.z; msk[4 * k + 3] = v.w;
+            }
+        }
 #pragma unroll
         for (int q = 0; q < 32; ++q) {
             const uint32_t wl = w[q >> 1], wh = w[(q + 32) >> 1];
-            const uint32_t ml = sm[q], mh = sm[q + 32];
+            // n = 64: the parameter array indexed directly (constant-bank operands)
+            const uint32_t ml = QN == 4 ? msk[q] : p.smask[q];
+            const uint32_t mh = QN == 4 ? msk[q + 32] : p.smask[q + 32];
             const float lo = (q & 1) ? __uint_as_float((wl & 0xFFFF0000u) ^ ml) : __uint_as_float(wl * 65536u + ml);
             const float hi = (q & 1) ? __uint_as_float((wh & 0xFFFF0000u) ^ mh) : __uint_as_float(wh * 65536u + mh);
             e[q] = pk2(lo, hi);
@@ -470,37 +496,49 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
             if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
             emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, dr);
         }
-        // everyone is done with stage s: refill it
-        __syncthreads();
+        // this warp is done with stage s; thread 0 refills it once all are
+        __syncwarp();
+        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
+        bool refill_failed = false;
         if (tid == 0) {
             const int next = tile + kStages * gridDim.x;
             if (next < p.num_tiles) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(next, s);
+                if (wait_phase(empties + 8u * s, phase, kWaitLimit)) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(next, s);
+                    issued = i + kStages + 1;
+                } else {
+                    atomicExch(&g_rows_error, 1);
+                    refill_failed = true;
+                }
             }
+        }
+        if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
+            ++i;
+            break;
         }
         if (++s == kStages) {
             s = 0;
             phase ^= 1u;
         }
     }
+    // copies this CTA issued and thread 0 has not seen land (a broken-off
+    // loop): let them land before the CTA exits (bounded)
     if (tid == 0)
-        for (int k = i; k < i + kStages; ++k) {
-            const int tile = blockIdx.x + k * gridDim.x;
-            if (tile >= p.num_tiles) break;
+        for (int k = i; k < issued; ++k)
             wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
-        }
 }
 
 template <int GRID, bool SR, int SF>
 static cudaError_t launch_rows_seg(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
+    constexpr int kCtas = kRowsCtas;
     p.stages = kRowsStages;
     const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 1024;  // ring, barriers, sign table, alignment
-    auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kRowsCtas, 4>
-                        : quantize_rows_seg_kernel<GRID, SR, SF, kRowsCtas, 2>;
+    auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 4>
+                        : quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 2>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int grid = p.num_tiles < kRowsCtas * num_sms ? p.num_tiles : kRowsCtas * num_sms;
+    const int grid = p.num_tiles < kCtas * num_sms ? p.num_tiles : kCtas * num_sms;
     return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, maps, p);
 }
 
@@ -592,12 +630,13 @@ cudaError_t set_rows_wait_limit(uint32_t polls) {
 // that has not been loaded yet).
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kRowsCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kRowsCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kRowsCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kRowsCtas, 4>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kRowsCtas, 4>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kRowsCtas, 4>);
+    constexpr int kSegCtas = kRowsCtas;
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 2>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 4>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 4>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 4>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128, false>);

@@ -17,16 +17,18 @@ from tests.gpu_util import assert_bitwise, gpu_quantize, to_dev
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("mask", [ufp4.OUT_ROWWISE, ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE])
-def test_quantizer_wait_timeout_is_reported_and_recovers(mask):
+# row-only n = 16: the row kernel; row + column: the general kernel; row-only
+# n = 64 and n = 256: the segment kernel (per-warp waits, empty barriers)
+@pytest.mark.parametrize("mask,n", [(ufp4.OUT_ROWWISE, 16), (ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE, 16),
+                                    (ufp4.OUT_ROWWISE, 64), (ufp4.OUT_ROWWISE, 256)])
+def test_quantizer_wait_timeout_is_reported_and_recovers(mask, n):
     x = inputs.tiny_check(256, 1024)
-    kw = dict(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0)
+    kw = dict(grid="e1m2", block=(1, 16), n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0)
     xd = to_dev(x)
     torch.cuda.synchronize()
     assert ufp4.ufp4_device_error() == 0
     ufp4.ufp4_set_quantize_wait_limit(0)
     try:
-        # the row-only mask runs the row kernel, row + column the general one
         ufp4.quantize(xd, ufp4.make_desc(out_mask=mask, **kw))
         torch.cuda.synchronize()
         assert ufp4.ufp4_device_error_status() == ufp4.UFP4_ERR_TIMEOUT
@@ -35,7 +37,7 @@ def test_quantizer_wait_timeout_is_reported_and_recovers(mask):
         ufp4.ufp4_set_quantize_wait_limit(-1)
     got = gpu_quantize(xd, out_mask=mask, **kw)
     assert ufp4.ufp4_device_error_status() == ufp4.UFP4_OK
-    c, s = orc.quantize(x, grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED,
+    c, s = orc.quantize(x, grid="e1m2", block=(1, 16), n=n, sign_seed=inputs.SIGN_SEED,
                         scale_fmt=orc.SCALE_UE8M0)
     assert_bitwise(got["row"][0], c, "row-wise codes after the timeout")
     assert_bitwise(got["row"][1], s, "row-wise scales after the timeout")
