@@ -39,6 +39,10 @@ struct RowsMaps {
 // TC: tile columns, 128, or 256 for n = 256 (whose segments span 16 chunks);
 // the tiles hold 16 K elements either way.
 //
+// With 1-D blocks no CTA barrier separates the tiles: each warp waits on the
+// stage's TMA barrier itself and arrives on the stage's "empty" barrier when
+// it is done with it; thread 0 waits on that one before it refills the stage.
+//
 // TWO_D: b x b blocks (b = 16, 32 or 64; with 256-column tiles b <= 32,
 // UE8M0 scales).  The tile then has 2 kRPI rows, so each thread holds one
 // row pair; the block amax is reduced across the lanes of a warp that share
@@ -61,6 +65,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     const int kStages = p.stages;
     uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes);  // 2 sets of kSlots
     const uint32_t bars = smem_addr(base + kStages * kTileBytes + 8 * kSlots);
+    const uint32_t empties = bars + 8u * kStages;  // 1-D blocks: every warp done with the stage
     const int tid = threadIdx.x;
     const int cchunk = tid % kCPR;
     const int r0 = tid / kCPR;
@@ -98,8 +103,10 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+            if (!TWO_D) asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (TWO_D)
@@ -109,10 +116,15 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
     griddep_wait();
     griddep_launch();
     const uint32_t wait_limit = g_rows_wait_limit;
+    const int lane = tid & 31;
+    int issued = 0;  // tiles of this CTA issued so far (thread 0)
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
-            if (tile < p.num_tiles) issue(tile, s);
+            if (tile < p.num_tiles) {
+                issue(tile, s);
+                issued = s + 1;
+            }
         }
 
     int t = 0, rt = 0, ct = 0, step_r = 0, step_c = 0;
@@ -138,8 +150,16 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             if (rt >= p.t[t].row_tiles) relocate(tile);  // into the next tensor
         }
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (!__syncthreads_and(landed)) {
-            if (tid == 0) atomicExch(&g_rows_error, 1);
+        if (TWO_D) {
+            if (!__syncthreads_and(landed)) {
+                if (tid == 0) atomicExch(&g_rows_error, 1);
+                break;
+            }
+        } else if (!__all_sync(0xFFFFFFFFu, landed)) {
+            // 1-D blocks: no CTA barrier per tile; a warp whose wait gave up
+            // leaves the loop (the others then give up on the stages it no
+            // longer releases)
+            if (lane == 0) atomicExch(&g_rows_error, 1);
             break;
         }
         const RowsTensor& T = p.t[t];
@@ -242,13 +262,33 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             }
             emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, dr);
         }
-        // everyone is done with stage s: refill it
-        __syncthreads();
-        if (tid == 0) {
-            const int next = tile + kStages * gridDim.x;
-            if (next < p.num_tiles) {
+        const int next = tile + kStages * gridDim.x;
+        if (TWO_D) {
+            // everyone is done with stage s: refill it
+            __syncthreads();
+            if (tid == 0 && next < p.num_tiles) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue(next, s);
+                issued = i + kStages + 1;
+            }
+        } else {
+            // this warp is done with stage s; thread 0 refills it once all are
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
+            bool refill_failed = false;
+            if (tid == 0 && next < p.num_tiles) {
+                if (wait_phase(empties + 8u * s, phase, kWaitLimit)) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(next, s);
+                    issued = i + kStages + 1;
+                } else {
+                    atomicExch(&g_rows_error, 1);
+                    refill_failed = true;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
+                ++i;
+                break;
             }
         }
         if (++s == kStages) {
@@ -256,13 +296,11 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
             phase ^= 1u;
         }
     }
-    // a broken-off loop leaves copies in flight: let them land (bounded)
+    // copies this CTA issued and thread 0 has not seen land (a broken-off
+    // loop): let them land before the CTA exits (bounded)
     if (tid == 0)
-        for (int k = i; k < i + kStages; ++k) {
-            const int tile = blockIdx.x + k * gridDim.x;
-            if (tile >= p.num_tiles) break;
+        for (int k = i; k < issued; ++k)
             wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
-        }
 }
 
 // CTAs per SM and ring depth of the row kernel (128 x 128 tiles): two CTAs
@@ -547,7 +585,7 @@ template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
 static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
     constexpr int kTileElems = TWO_D ? 2 * (kThreads / (TC / kChunk)) * TC : 16384;
     constexpr int kSlots = TWO_D ? (kTileElems / TC / 16) * (TC / 16) : 0;
-    const size_t smem = (size_t)p.stages * kTileElems * 2 + 8 * kSlots + 8 * p.stages + 128;
+    const size_t smem = (size_t)p.stages * kTileElems * 2 + 8 * kSlots + 16 * p.stages + 128;
     auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS, TC, TWO_D>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
