@@ -156,8 +156,10 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     std::memset(&p, 0, sizeof(p));
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
     const int n = desc->hadamard_n;
-    // tile columns and rows: 16 K elements, or 8 K (one row pair per thread) with 2-D blocks
-    const int tc = n == 256 ? 256 : 128, tr = bs.is2d ? 2 * (256 / (tc / 16)) : 16384 / tc;
+    // tile columns and rows: 16 K elements, or 8 K (one row pair per thread) with 2-D blocks in the
+    // row kernel; n = 64 and n = 256 run the segment kernel, 16 K-element tiles either way
+    const bool seg = n == 64 || n == 256;
+    const int tc = n == 256 ? 256 : 128, tr = bs.is2d && !seg ? 2 * (256 / (tc / 16)) : 16384 / tc;
     int64_t tiles = 0;
     int k = 0;
     for (int i = 0; i < count; ++i) {
@@ -259,9 +261,8 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     if ((desc->scale_fmt == UFP4_SCALE_E4M3 || desc->grid == UFP4_GRID_MXFP8) &&
         (do_col || grouped || bs.is2d || n > 128 || total_rows >= (1LL << 31) || cols >= (1LL << 31)))
         return UFP4_ERR_UNSUPPORTED;  // two-level scale and MXFP8: row-wise, 1-D blocks, n <= 128
-    // the row kernel: row-wise, not grouped; 1-D blocks, or b x b blocks with b = 16, 32 or 64 (b <= 32 when
-    // n = 256: its tiles have 32 rows)
-    const bool rows_2d = bs.is2d && bs.b2d >= 16 && (n < 256 || bs.b2d <= 32);
+    // the row kernels: row-wise, not grouped; 1-D blocks, or b x b blocks with b = 16, 32 or 64
+    const bool rows_2d = bs.is2d && bs.b2d >= 16;
     if (do_row && !do_col && (!bs.is2d || rows_2d) && !grouped && total_rows < (1LL << 31) &&
         cols < (1LL << 31)) {
         const ufp4_qtensor* rw = rowwise;

@@ -36,15 +36,14 @@ struct RowsMaps {
 
 // N16: n = 16 (the FPROP operands' case), with the four butterfly strides
 // fixed at compile time.
-// TC: tile columns, 128, or 256 for n = 256 (whose segments span 16 chunks);
-// the tiles hold 16 K elements either way.
+// TC: tile columns, 128 (n = 256 and n = 64 take the segment kernel below;
+// the template also takes 256 for segments of 16 chunks).
 //
 // With 1-D blocks no CTA barrier separates the tiles: each warp waits on the
 // stage's TMA barrier itself and arrives on the stage's "empty" barrier when
 // it is done with it; thread 0 waits on that one before it refills the stage.
 //
-// TWO_D: b x b blocks (b = 16, 32 or 64; with 256-column tiles b <= 32,
-// UE8M0 scales).  The tile then has 2 kRPI rows, so each thread holds one
+// TWO_D: b x b blocks (b = 16, 32 or 64, UE8M0 scales).  The tile then has 2 kRPI rows, so each thread holds one
 // row pair; the block amax is reduced across the lanes of a warp that share
 // the block, then across warps with a shared-memory atomicMax, while the
 // transformed values wait in registers.  The amax slots come in two sets
@@ -310,7 +309,7 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
 // element in register moves).
 constexpr int kRowsCtas = 2, kRowsStages = 3;
 
-// n = 64 and n = 256 with 1-D blocks: a thread owns one 64-element segment of
+// n = 64 and n = 256, 1-D or b x b blocks: a thread owns one 64-element segment of
 // a row.  QN segments make one tile row (QN = 2: 128 columns, n = 64; QN = 4:
 // 256 columns, n = 256), so the tile is 128 x 128 or 64 x 256.  It arrives as
 // QN 64-column TMA boxes with the 128-byte swizzle (16-byte unit u of row r at
@@ -322,13 +321,19 @@ constexpr int kRowsCtas = 2, kRowsStages = 3;
 // segments (lane ^ 8, lane ^ 16).  The random signs: n = 64 reads a per-
 // element mask table from the kernel parameters (the same for every segment);
 // n = 256 from a table in shared memory, one 64-entry set per segment.
-// No CTA barrier per tile: each warp waits on the stage's TMA barrier itself
-// and, when done with the stage, arrives on the stage's "empty" barrier;
-// thread 0 waits on that one before it refills the stage.
-template <int GRID, bool SR, int SF, int CTAS, int QN>
+// 1-D blocks: no CTA barrier per tile; each warp waits on the stage's TMA
+// barrier itself and, when done with the stage, arrives on the stage's
+// "empty" barrier; thread 0 waits on that one before it refills the stage.
+// TWO_D (b = 16, 32, 64; UE8M0): the block amax is reduced over the rows a
+// warp holds (lanes ^ 1, 2, 4, and ^ 16 for two segments a row), then across
+// warps with a shared-memory atomicMax, with the CTA barrier per tile; the
+// amax slots come in two sets used by alternate tiles (a set is cleared
+// during the tile before its use).
+template <int GRID, bool SR, int SF, int CTAS, int QN, bool TWO_D>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
     static_assert(QN == 2 || QN == 4, "two or four segments per tile row");
+    constexpr int kSlots = 64;  // amax slots per set: (TR / b) x (TC / b) <= 64 for b >= 16
     constexpr int TC = 64 * QN, TR = 16384 / TC;
     constexpr int kLQ = QN == 2 ? 1 : 2;
     constexpr int kTileBytes = TR * TC * 2;
@@ -344,6 +349,7 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     const uint32_t bars = smem_addr(base + kStages * kTileBytes);
     const uint32_t empties = bars + 32u;
     uint32_t* sgn_tab = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes + 64);  // n = 256: [segment][j], 16-byte aligned
+    uint32_t* amax2d = sgn_tab + 256;  // 2-D blocks: two sets of kSlots
     const int tid = threadIdx.x;
     const int seg = (tid >> 3) & (QN - 1);
     const int r = (tid & 7) + 8 * (tid >> (3 + kLQ));
@@ -379,12 +385,14 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
-            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
+            if (!TWO_D) asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (QN == 4)  // mask of element j of segment q: 0x80000000 when eps_(64 q + j) = -1
         sgn_tab[tid] = ((p.sign_bits[tid >> 5] >> (tid & 31)) & 1u) << 31;
+    if (TWO_D && tid < 2 * kSlots) amax2d[tid] = 0u;
+    const int lb = p.lb2d;  // log2 b (2-D blocks)
     __syncthreads();
     griddep_wait();
     griddep_launch();
@@ -425,7 +433,12 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
         // a warp whose wait gave up leaves the loop (the others then give up
         // on the stages it no longer releases)
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (!__all_sync(0xFFFFFFFFu, landed)) {
+        if (TWO_D) {
+            if (!__syncthreads_and(landed)) {
+                if (tid == 0) atomicExch(&g_rows_error, 1);
+                break;
+            }
+        } else if (!__all_sync(0xFFFFFFFFu, landed)) {
             if (lane == 0) atomicExch(&g_rows_error, 1);
             break;
         }
@@ -496,23 +509,71 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
         float M0, M2, M1, M3;
         amax_pair(e, 0, 16, M0, M2);
         amax_pair(e + 16, 0, 16, M1, M3);
-        const bool b32 = lbw == 5;
+        const bool b32 = TWO_D ? lb >= 5 : lbw == 5;
         if (b32) {
             M0 = M1 = fmaxf(M0, M1);
             M2 = M3 = fmaxf(M2, M3);
+        }
+        if (TWO_D) {
+            if (lb == 6) M0 = M1 = M2 = M3 = fmaxf(M0, M2);
+            // the rows of this warp in the same b-row band: lanes ^ 1, 2, 4 (and
+            // ^ 16: rows + 8 with two segments a row); b >= 16 covers them all
+#pragma unroll
+            for (int k = 1; k <= (QN == 2 ? 16 : 4); k <<= 1) {
+                if (k == 8) continue;
+                M0 = fmaxf(M0, __shfl_xor_sync(0xFFFFFFFFu, M0, k));
+                M1 = fmaxf(M1, __shfl_xor_sync(0xFFFFFFFFu, M1, k));
+                M2 = fmaxf(M2, __shfl_xor_sync(0xFFFFFFFFu, M2, k));
+                M3 = fmaxf(M3, __shfl_xor_sync(0xFFFFFFFFu, M3, k));
+            }
+            // then across the warps of the band: slot (row block, column block)
+            uint32_t* set = amax2d + (i & 1) * kSlots;
+            const int lnbc = (QN == 2 ? 7 : 8) - lb;  // log2(TC / b)
+            const int slot0 = ((r >> lb) << lnbc) + ((64 * seg) >> lb);
+            const int cpb = (1 << lb) >> 4;  // chunks per block column
+            if ((lane & (QN == 2 ? 0x17 : 0x7)) == 0) {
+                atomicMax(&set[slot0], __float_as_uint(M0));
+                if (cpb == 1) atomicMax(&set[slot0 + 1], __float_as_uint(M1));
+                if (cpb <= 2) atomicMax(&set[slot0 + (cpb == 1 ? 2 : 1)], __float_as_uint(M2));
+                if (cpb == 1) atomicMax(&set[slot0 + 3], __float_as_uint(M3));
+            }
+            __syncthreads();
+            M0 = __uint_as_float(set[slot0]);
+            M1 = __uint_as_float(set[slot0 + (cpb == 1 ? 1 : 0)]);
+            M2 = __uint_as_float(set[slot0 + (cpb == 1 ? 2 : (cpb == 2 ? 1 : 0))]);
+            M3 = __uint_as_float(set[slot0 + (cpb == 1 ? 3 : (cpb == 2 ? 1 : 0))]);
+            // the other set serves the next tile: every read of it (the
+            // previous tile's) happened before this tile's first barrier
+            uint32_t* other = amax2d + ((i & 1) ^ 1) * kSlots;
+            if (tid < kSlots) other[tid] = 0u;
         }
         uint8_t* cp = T.codes + (int64_t)row * T.codes_ld + (GRID == 4 ? col : col >> 1);
         uint8_t* sp = T.scales + ((int64_t)row * T.scales_ld + (col >> lbw)) * SZ;
         const int cstride = GRID == 4 ? 16 : 8;  // code bytes per 16 elements
         const uint64_t lin0 = (uint64_t)row * (uint64_t)T.cols + (uint64_t)col;
         Dest A, B;
+        // 2-D: one UE8M0 byte per b x b block at (row / b, column / b), written
+        // by the thread holding its top-left chunk
+        uint8_t* sp2 = T.scales + (int64_t)(row >> lb) * T.scales_ld;
+        const bool rfirst = (row & ((1 << lb) - 1)) == 0;
+        auto chunk_scale = [&](int c, uint8_t*& sptr, bool& w) {
+            const int cc = col + 16 * c;
+            if (TWO_D) {
+                sptr = sp2 + (cc >> lb);
+                w = rfirst && (cc & ((1 << lb) - 1)) == 0;
+            } else {
+                sptr = sp + (cc - col) / (b32 ? 32 : 16) * SZ;
+                w = !b32 || (c & 1) == 0;
+            }
+        };
         // chunks 0 and 2
         A.codes = cp;
         B.codes = cp + 2 * cstride;
-        A.s0 = A.s1 = sp;
-        B.s0 = B.s1 = sp + (b32 ? 1 : 2) * SZ;
+        chunk_scale(0, A.s0, A.w0);
+        chunk_scale(2, B.s0, B.w0);
+        A.s1 = A.s0;
+        B.s1 = B.s0;
         A.valid = B.valid = valid;
-        A.w0 = B.w0 = true;
         A.w1 = B.w1 = false;
         A.lin0 = lin0;
         B.lin0 = lin0 + 32;
@@ -524,9 +585,10 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
         // chunks 1 and 3 (their 1 x 32 scales were written with chunks 0 and 2)
         A.codes = cp + cstride;
         B.codes = cp + 3 * cstride;
-        A.s0 = A.s1 = sp + SZ;
-        B.s0 = B.s1 = sp + 3 * SZ;
-        A.w0 = B.w0 = !b32;
+        chunk_scale(1, A.s0, A.w0);
+        chunk_scale(3, B.s0, B.w0);
+        A.s1 = A.s0;
+        B.s1 = B.s0;
         A.lin0 = lin0 + 16;
         B.lin0 = lin0 + 48;
         {
@@ -534,13 +596,21 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
             if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
             emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, dr);
         }
-        // this warp is done with stage s; thread 0 refills it once all are
-        __syncwarp();
-        if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
-        bool refill_failed = false;
-        if (tid == 0) {
-            const int next = tile + kStages * gridDim.x;
-            if (next < p.num_tiles) {
+        const int next = tile + kStages * gridDim.x;
+        if (TWO_D) {
+            // everyone is done with stage s: refill it
+            __syncthreads();
+            if (tid == 0 && next < p.num_tiles) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                issue(next, s);
+                issued = i + kStages + 1;
+            }
+        } else {
+            // this warp is done with stage s; thread 0 refills it once all are
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
+            bool refill_failed = false;
+            if (tid == 0 && next < p.num_tiles) {
                 if (wait_phase(empties + 8u * s, phase, kWaitLimit)) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     issue(next, s);
@@ -550,10 +620,10 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                     refill_failed = true;
                 }
             }
-        }
-        if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
-            ++i;
-            break;
+            if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
+                ++i;
+                break;
+            }
         }
         if (++s == kStages) {
             s = 0;
@@ -571,9 +641,15 @@ template <int GRID, bool SR, int SF>
 static cudaError_t launch_rows_seg(const RowsMaps& maps, RowsParams& p, int num_sms, cudaStream_t st) {
     constexpr int kCtas = kRowsCtas;
     p.stages = kRowsStages;
-    const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 1024;  // ring, barriers, sign table, alignment
-    auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 4>
-                        : quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 2>;
+    // ring, barriers, sign table, 2-D amax slots, alignment
+    const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 512 + 1024;
+    auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 4, false>
+                        : quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 2, false>;
+    if constexpr (SF == 1 && GRID < 4) {
+        if (p.lb2d)
+            k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 4, true>
+                           : quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 2, true>;
+    }
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < kCtas * num_sms ? p.num_tiles : kCtas * num_sms;
@@ -599,20 +675,18 @@ static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms,
         if (p.lb2d) {
             // 2-D blocks: 8 K-element tiles (one row pair per thread), six stages
             p.stages = 2 * kRowsStages;
-            if (p.tc == 256) return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 256, true>(maps, p, num_sms, st);
             if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, true>(maps, p, num_sms, st);
             return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128, true>(maps, p, num_sms, st);
         }
     }
     p.stages = kRowsStages;
-    if (p.tc == 256) return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 256, false>(maps, p, num_sms, st);
     if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, false>(maps, p, num_sms, st);
     return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128, false>(maps, p, num_sms, st);
 }
 
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
-    // n = 64 and n = 256 with 1-D blocks: the segment kernel, fed by 64-column boxes with the 128-byte swizzle
-    const bool seg_kernel = p.lb2d == 0 && ((p.n == 64 && p.tc == 128) || (p.n == 256 && p.tc == 256));
+    // n = 64 and n = 256: the segment kernel, fed by 64-column boxes with the 128-byte swizzle
+    const bool seg_kernel = (p.n == 64 && p.tc == 128) || (p.n == 256 && p.tc == 256);
     RowsMaps maps;
     memset(&maps, 0, sizeof(maps));
     for (int t = 0; t < p.count; ++t) {
@@ -669,24 +743,22 @@ cudaError_t set_rows_wait_limit(uint32_t polls) {
 template <int G, bool SR>
 static void preload_rows(cudaFuncAttributes* a) {
     constexpr int kSegCtas = kRowsCtas;
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 2>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 4>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 4>);
-    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 4>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 2, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 2, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 2, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 0, kSegCtas, 4, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 4, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 2, kSegCtas, 4, false>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 2, true>);
+    cudaFuncGetAttributes(a, quantize_rows_seg_kernel<G, SR, 1, kSegCtas, 4, true>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, true, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas, 128, false>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 0, false, kRowsCtas, 256, false>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 256, false>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, false, kRowsCtas, 256, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, true>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, true>);
-    cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 256, true>);
 }
 
 cudaError_t preload_rows_kernels() {
@@ -701,9 +773,9 @@ cudaError_t preload_rows_kernels() {
     preload_rows<3, true>(&a);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, true, kRowsCtas, 128, false>);
-    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 2>);
-    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 4>);
-    return cudaFuncGetAttributes(&a, quantize_rows_kernel<4, false, 1, false, kRowsCtas, 256, false>);
+    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 2, false>);
+    cudaFuncGetAttributes(&a, quantize_rows_seg_kernel<4, false, 1, kRowsCtas, 4, false>);
+    return cudaGetLastError();
 }
 
 }  // namespace ufp4

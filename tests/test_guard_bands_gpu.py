@@ -55,6 +55,7 @@ def _quant_out(rows, cols, desc, pad_codes=16, pad_scales=8):
     dict(grid="int4", block=(1, 32), n=64, scale_fmt=ufp4.SCALE_FP32, rounding=ufp4.ROUND_SR, sr_seed=3),
     dict(grid="e2m1", block=(1, 16), n=256, scale_fmt=ufp4.SCALE_UE8M0),
     dict(grid="e1m2", block=(32, 32), n=16, scale_fmt=ufp4.SCALE_UE8M0),
+    dict(grid="int4", block=(16, 16), n=64, scale_fmt=ufp4.SCALE_UE8M0, rounding=ufp4.ROUND_SR, sr_seed=4),
     dict(grid="mxfp8", block=(1, 32), n=16, scale_fmt=ufp4.SCALE_UE8M0),
 ])
 @pytest.mark.parametrize("colwise", [False, True])

@@ -72,14 +72,13 @@ def test_block_shapes(block, n):
 
 
 @pytest.mark.parametrize("b", [16, 32, 64])
-@pytest.mark.parametrize("n", [1, 16, 32, 128, 256])
+@pytest.mark.parametrize("n", [1, 16, 32, 64, 128, 256])
 @pytest.mark.parametrize("rounding", [RTNE, SR])
 def test_2d_blocks_rowwise_kernel(b, n, rounding):
-    """Row-wise b x b blocks run in the row kernel (one row pair per thread, the
-    block amax reduced across lanes and warps): ragged tiles (rows and columns
-    multiples of b but not of the tile), every grid."""
-    if n == 256 and b == 64:
-        pytest.skip("64 x 64 blocks with n = 256 take the general kernel")
+    """Row-wise b x b blocks run in the row kernels (n = 64 and 256: the segment
+    kernel; otherwise the row kernel, one row pair per thread; the block amax
+    reduced across lanes and warps): ragged tiles (rows and columns multiples
+    of b but not of the tile), every grid."""
     rows = 3 * b + 2 * 64 if b < 64 else 320
     cols = 768 if n == 256 else 384 + 2 * b
     cols = -(-cols // max(n, b)) * max(n, b)
