@@ -315,34 +315,64 @@ def run_gpu(args):
     kernel_tflops = g_units / k_time / 1e12
 
     # ------------------------------------------------------- e2e (host buffers)
+    # Every step copies X and W in from pinned host memory, runs
+    # ufp4_rht_quantize_batch and ufp4_gemm, and copies the codes, scales and
+    # Y out.  Steps are pipelined over three streams with two sets of device
+    # and host buffers: the copy-in of step i + 1 and the copy-out of step i - 1
+    # run while step i computes, so the two directions of the host link
+    # overlap.  The timed region spans the first copy-in to the last copy-out.
     xh = to_t(x_np).pin_memory()
     whh = to_t(w_np).pin_memory()
-    xd, wd = xs[0], wsrc[0]
-    codes_h = [torch.empty_like(qx[0], device="cpu").pin_memory(), torch.empty_like(qx[1], device="cpu").pin_memory(),
-               torch.empty_like(qw[0], device="cpu").pin_memory(), torch.empty_like(qw[1], device="cpu").pin_memory()]
-    Dh = torch.empty((M, N), dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
+    xin = [xs[0], xs[1 % ROTATE] if ROTATE > 1 else to_t(x_np).to(dev)]
+    win = [wsrc[0], wsrc[1 % ROTATE] if ROTATE > 1 else to_t(w_np).to(dev)]
+    qxs = [qx, ufp4.alloc_quantized(M, K, desc, dev)]
+    qws = [qw, ufp4.alloc_quantized(N, K, desc, dev)]
+    txs = [tx, ufp4.qtensor(*qxs[1], M, K)]
+    tws = [tw, ufp4.qtensor(*qws[1], N, K)]
+    Ds = [D, torch.empty((M, N), dtype=torch.float32, device=dev)]
+    wss = [wsb, torch.empty_like(wsb)]
+    codes_h = [[torch.empty_like(t, device="cpu").pin_memory() for t in (*qxs[k], *qws[k])] for k in range(2)]
+    Dh = [torch.empty((M, N), dtype=torch.float32).pin_memory() for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    e_in = [torch.cuda.Event() for _ in range(2)]    # copy-in of buffer set k done
+    e_comp = [torch.cuda.Event() for _ in range(2)]  # compute on set k done (its inputs free)
+    e_out = [torch.cuda.Event() for _ in range(2)]   # copy-out of set k done (its outputs free)
+    e2e_steps = max(4, min(args.steps, 20))
 
-    def e2e_step():
-        xd.copy_(xh, non_blocking=True)
-        wd.copy_(whh, non_blocking=True)
-        ufp4.ufp4_rht_quantize_batch([xd, wd], desc, [tx, tw], stream.cuda_stream)
-        ufp4.ufp4_gemm(tx, tw, desc, D, wsb, stream.cuda_stream)
-        for hbuf, dbuf in zip(codes_h, (qx[0], qx[1], qw[0], qw[1])):
-            hbuf.copy_(dbuf, non_blocking=True)
-        Dh.copy_(D, non_blocking=True)
+    def e2e_pass(n_steps, t_start=None, t_end=None):
+        for i in range(n_steps):
+            k = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(e_comp[k])
+                if i == 0 and t_start is not None:
+                    t_start.record(s_in)
+                xin[k].copy_(xh, non_blocking=True)
+                win[k].copy_(whh, non_blocking=True)
+                e_in[k].record(s_in)
+            stream.wait_event(e_in[k])
+            if i >= 2:
+                stream.wait_event(e_out[k])
+            ufp4.ufp4_rht_quantize_batch([xin[k], win[k]], desc, [txs[k], tws[k]], stream.cuda_stream)
+            ufp4.ufp4_gemm(txs[k], tws[k], desc, Ds[k], wss[k], stream.cuda_stream)
+            e_comp[k].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(e_comp[k])
+                for hbuf, dbuf in zip(codes_h[k], (*qxs[k], *qws[k])):
+                    hbuf.copy_(dbuf, non_blocking=True)
+                Dh[k].copy_(Ds[k], non_blocking=True)
+                e_out[k].record(s_out)
+        if t_end is not None:
+            t_end.record(s_out)
 
-    e2e_step()
+    e2e_pass(2)
     barrier()
     a, b = ev(), ev()
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    e2e_pass(e2e_steps, a, b)
     barrier()
     e2e_s, e2e_units = aggregate(a.elapsed_time(b) / 1e3, QUANT_BYTES * e2e_steps, world, dev)
     h2d = (xh.numel() + whh.numel()) * 2
-    d2h = sum(t.numel() * t.element_size() for t in codes_h) + Dh.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in codes_h[0]) + Dh[0].numel() * 4
 
     pk = peaks()
     q_launch_ms = statistics.mean(q_ms)  # one batched quantizer launch per step (X and W)
