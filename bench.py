@@ -544,16 +544,19 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
         dy, _ = inputs.dy_sr()
         dys = [to_t(dy).to(dev) for _ in range(5)]
         r3, c3 = dy.shape
-        for fmt in (ufp4.SCALE_FP32, ufp4.SCALE_UE8M0):
+        # then the same shape rounded to nearest (the X and W operands' row + column pass)
+        for rnd, fmt in ((ufp4.ROUND_SR, ufp4.SCALE_FP32), (ufp4.ROUND_SR, ufp4.SCALE_UE8M0),
+                         (ufp4.ROUND_RTNE, ufp4.SCALE_FP32), (ufp4.ROUND_RTNE, ufp4.SCALE_UE8M0)):
             desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
-                                  rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED,
+                                  rounding=rnd, sr_seed=inputs.SR_SEED,
                                   out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
             ro = ufp4.alloc_quantized(r3, c3, desc, dev)
             co = ufp4.alloc_quantized(c3, r3, desc, dev)
             rq, cq = ufp4.qtensor(*ro, r3, c3), ufp4.qtensor(*co, c3, r3)
             ms = timed(lambda i: ufp4.ufp4_rht_quantize(dys[i % 5], desc, rq, cq, stream.cuda_stream))
             gbs = r3 * c3 * (2 + 2 * (0.5 + scale_bytes(desc))) / (ms / 1e3) / 1e9
-            emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 SR row+col", gbs,
+            tag = "SR" if rnd == ufp4.ROUND_SR else "RTNE"
+            emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 {tag} row+col", gbs,
                  "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
 
     if "diag" in sections:

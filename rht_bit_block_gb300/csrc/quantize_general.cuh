@@ -190,6 +190,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             const int bwc = 1 << lbwc;
             const int nrow = p.do_row ? pairs : 0;
             const int items = nrow + (p.do_col ? col_tasks : 0);
+#pragma unroll(SR ? 1 : 2)
             for (int w = 0; w < items; ++w) {
                 const bool is_row = w < nrow;
                 // output positions first: the SR draws depend on them only
