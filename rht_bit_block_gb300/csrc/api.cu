@@ -193,7 +193,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     p.log4n = 0;
     while ((1 << (2 * p.log4n)) < n) ++p.log4n;
     p.pow4 = (1 << (2 * p.log4n)) == n;
-    p.stages = 2;  // 2 x 32 KB tiles per CTA, 3 CTAs per SM
+    p.stages = 0;  // set by the launcher (the ring depth depends on the kernel it picks)
     p.inv_sqrt_n = inv_sqrt_n(n);
     make_sign_bits(desc->sign_seed, n, p.sign_bits);
     for (int j = 0; j < 64; ++j) p.smask[j] = ((p.sign_bits[j / 32] >> (j % 32)) & 1u) << 31;
