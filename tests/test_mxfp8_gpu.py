@@ -24,7 +24,7 @@ def _outliers(rows, cols, seed):
     return inputs.with_element_outliers(inputs.normal_bf16(rows, cols, seed), 0.001, 50.0, seed + 1)
 
 
-@pytest.mark.parametrize("n", [1, 16, 32, 128])
+@pytest.mark.parametrize("n", [1, 16, 32, 64, 128])
 @pytest.mark.parametrize("shape", [(256, 1024), (200, 96), (130, 4096)])
 def test_mxfp8_quantize_matches_oracle(n, shape):
     """Full and ragged 128 x 128 tiles (200 rows, 96 columns), n from none to 128."""

@@ -291,12 +291,15 @@ def test_rowwise_ragged_tiles(grid, rounding, block, n, cols):
 
 @pytest.mark.parametrize("rounding", [RTNE, SR])
 @pytest.mark.parametrize("grid", ["e1m2", "e2m1"])
-def test_batch_matches_oracle_and_single_calls(rounding, grid):
+@pytest.mark.parametrize("n", [16, 64, 256])
+def test_batch_matches_oracle_and_single_calls(rounding, grid, n):
     """ufp4_rht_quantize_batch over tensors of different shapes (one empty)
-    equals the oracle per tensor and the separate single calls, bit for bit."""
-    shapes = [(300, 576), (128, 1024), (0, 64), (1000, 192)]
+    equals the oracle per tensor and the separate single calls, bit for bit
+    (n = 16: the row kernel; n = 64, 256: the segment kernel)."""
+    shapes = [(300, 576), (128, 1024), (0, 64), (1000, 192)] if n < 256 else [(300, 768), (64, 512), (0, 256),
+                                                                             (200, 256)]
     xs = [inputs.tiny_check(r, c) if r else np.zeros((0, c), np.uint16) for r, c in shapes]
-    kw = dict(grid=grid, block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, rounding=rounding,
+    kw = dict(grid=grid, block=(1, 16), n=n, sign_seed=inputs.SIGN_SEED, rounding=rounding,
               sr_seed=inputs.SR_SEED, scale_fmt=PO2, group=3)
     desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE, **kw)
     devs = [to_dev(x) for x in xs]
