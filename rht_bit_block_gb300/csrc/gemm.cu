@@ -57,9 +57,13 @@ constexpr int kErrTimeout = 1;
 // Output tile widths.  Both paths run on CTA pairs.  FP8: 256 x 224 tiles, two
 // 224-column accumulators plus two sets of scale columns fit the 512
 // tensor-memory columns, and the wider tile gives each MMA instruction more
-// work (issuing a tcgen05 instruction costs a fixed time).  FP4 needs two to
-// four times the scale columns per K tile, so its tiles are 256 x 192.
+// work (issuing a tcgen05 instruction costs a fixed time).  FP4 needs two
+// (2X kind) to four (4X kind) times the scale columns per K tile: the 2X
+// kind's two scale sets still fit beside two 224-column accumulators
+// (448 + 48 <= 512), the 4X kind's do not, so its tiles are 256 x 192.
 constexpr int kBnFp8 = 224, kBnFp4 = 192;
+constexpr int kBnFp4x2 = 224;
+__host__ __device__ constexpr int pair_bn(int kind) { return kind == 0 ? kBnFp8 : (kind == 1 ? kBnFp4x2 : kBnFp4); }
 // CTA-pair rings: stages of KPS K tiles each (FP4 stages hold one K tile of
 // 256 elements, as much MMA work as two FP8 K tiles of 128)
 constexpr int kPairKps = 2, kPairStages = 3;          // FP8
@@ -318,7 +322,7 @@ __device__ __forceinline__ uint64_t sf256_desc(uint32_t saddr) {
 template <int KIND, int STAGES, int KPS>
 struct PairCfg {
     static constexpr int CPK = KIND == 0 ? 1 : (KIND == 1 ? 2 : 4);
-    static constexpr int BN = KIND == 0 ? kBnFp8 : kBnFp4;  // output columns of a pair tile
+    static constexpr int BN = pair_bn(KIND);  // output columns of a pair tile
     static constexpr int kBRows = BN / 2;                // B rows held per CTA
     static constexpr int kAAtom = kBM * kBKBytes;        // 16 KB
     static constexpr int kBAtom = kBRows * kBKBytes;
@@ -1236,7 +1240,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
     }
     pl.kind = (grid == 2 || grid == 3) ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
     pl.native = grid == 4;                                          // MXFP8: E4M3 bytes
-    pl.bn = pl.kind == 0 ? kBnFp8 : kBnFp4;
+    pl.bn = pair_bn(pl.kind);
     pl.k_bytes = (grid == 2 || grid == 3) ? K / 2 : K;
     pl.k_tiles = (pl.k_bytes + kBKBytes - 1) / kBKBytes;
     const int cps = pl.kind == 0 ? 1 : (pl.kind == 1 ? 2 : 4);
@@ -1451,7 +1455,7 @@ cudaError_t launch_main_pair_g(const GemmArgs* gs, int n, cudaStream_t st) {
         return run_gemm_pair<0, kPairStages, kPairKps, G>(maps, kp, st);
     }
     if (pl.kind == 1) {
-        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, (j % 2) * 2);  // E2M1
+        for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4x2, (j % 2) * 2);  // E2M1
         return run_gemm_pair<1, kPairStagesFp4x2, 1, G>(maps, kp, st);
     }
     // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
