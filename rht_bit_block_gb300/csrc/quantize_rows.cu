@@ -429,9 +429,10 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
             }
             if (rt >= p.t[t].row_tiles) relocate(tile);
         }
-        // no CTA barrier per tile: each warp waits for the copy itself, and
-        // a warp whose wait gave up leaves the loop (the others then give up
-        // on the stages it no longer releases)
+        // 1-D blocks: no CTA barrier per tile; each warp waits for the copy
+        // itself, and a warp whose wait gave up leaves the loop (the others
+        // then give up on the stages it no longer releases).  2-D blocks keep
+        // the CTA barrier, which their block amax needs anyway.
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
         if (TWO_D) {
             if (!__syncthreads_and(landed)) {
