@@ -55,6 +55,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     uint8_t* base = smem_raw + pad;
     uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * tile_bytes);
     const uint32_t bars = smem_addr(base + kStages * tile_bytes + 4 * p.amax_slots);  // 8-byte aligned
+    const uint32_t empties = bars + 8u * kStages;  // 1-D blocks: every warp done with the stage
 
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -82,8 +83,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     };
 
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s)
+        for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
@@ -92,10 +95,14 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     griddep_wait();
     griddep_launch();
     const uint32_t wait_limit = g_quant_wait_limit;
+    int issued = 0;  // tiles of this CTA issued so far (thread 0)
     if (tid == 0)
         for (int s = 0; s < kStages; ++s) {
             const int tile = blockIdx.x + s * gridDim.x;
-            if (tile < num_tiles) issue(tile, s);
+            if (tile < num_tiles) {
+                issue(tile, s);
+                issued = s + 1;
+            }
         }
 
     // row pass: a thread owns chunk column cchunk of the row pairs
@@ -143,9 +150,18 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             }
             if (p.num_groups > 1) g = find_group(p, row_tile);
         }
+        // 1-D blocks: no CTA barrier per tile; each warp waits for the copy
+        // itself, and a warp whose wait gave up leaves the loop (the others
+        // then give up on the stages it no longer releases).  2-D blocks keep
+        // the CTA barrier, which their block amax needs anyway.
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (!__syncthreads_and(landed)) {
-            if (tid == 0) atomicExch(&g_quant_error, 1);
+        if (p.is2d) {
+            if (!__syncthreads_and(landed)) {
+                if (tid == 0) atomicExch(&g_quant_error, 1);
+                break;
+            }
+        } else if (!__all_sync(0xFFFFFFFFu, landed)) {
+            if (lane == 0) atomicExch(&g_quant_error, 1);
             break;
         }
         const int64_t lr0 = (int64_t)(row_tile - p.grp_tile0[g]) * TR;
@@ -436,14 +452,35 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 }
             }
         }
-        // everyone is done with stage s: refill it (the fence orders this
-        // CTA's generic shared-memory accesses before the async-proxy write)
-        __syncthreads();
-        if (tid == 0) {
-            const int next = tile + kStages * gridDim.x;
-            if (next < num_tiles) {
+        // the fence orders this CTA's generic shared-memory accesses (reads,
+        // and the zero rows of a group's end) before the async-proxy refill
+        const int next = tile + kStages * gridDim.x;
+        if (p.is2d) {
+            // everyone is done with stage s: refill it
+            __syncthreads();
+            if (tid == 0 && next < num_tiles) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 issue(next, s);
+                issued = i + kStages + 1;
+            }
+        } else {
+            // this warp is done with stage s; thread 0 refills it once all are
+            __syncwarp();
+            if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
+            bool refill_failed = false;
+            if (tid == 0 && next < num_tiles) {
+                if (wait_phase(empties + 8u * s, phase, kWaitLimit)) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue(next, s);
+                    issued = i + kStages + 1;
+                } else {
+                    atomicExch(&g_quant_error, 1);
+                    refill_failed = true;
+                }
+            }
+            if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
+                ++i;
+                break;
             }
         }
         if (++s == kStages) {
@@ -451,20 +488,18 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             phase ^= 1u;
         }
     }
-    // a broken-off loop leaves copies in flight: let them land (bounded)
+    // copies this CTA issued and thread 0 has not seen land (a broken-off
+    // loop): let them land before the CTA exits (bounded)
     if (tid == 0)
-        for (int k = i; k < i + kStages; ++k) {
-            const int tile = blockIdx.x + k * gridDim.x;
-            if (tile >= num_tiles) break;
+        for (int k = i; k < issued; ++k)
             wait_phase(bars + 8u * (k % kStages), (uint32_t)((k / kStages) & 1), kWaitLimit);
-        }
 }
 
 // ------------------------------------------------------------- launchers
 template <int GRID, bool SR, bool PO2, int TC, bool N16>
 static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int num_tiles, int num_sms,
                             cudaStream_t st) {
-    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 4 * (size_t)p.amax_slots + 8 * p.stages + 128;
+    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 4 * (size_t)p.amax_slots + 16 * p.stages + 128;
     auto k = quantize_kernel<GRID, SR, PO2, TC, N16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
