@@ -558,6 +558,20 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
             tag = "SR" if rnd == ufp4.ROUND_SR else "RTNE"
             emit("quantize_rowcol", f"dY {r3}x{c3} e1m2 1x16 {'UE8M0' if fmt else 'fp32'} n=16 {tag} row+col", gbs,
                  "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
+        # 2-D 32 x 32 blocks, row-wise and column-wise from one read, on the large operand
+        xl, _ = inputs.large_sweep(k=7168, n=128)
+        xls = [to_t(xl).to(dev)]
+        rl, cl = xl.shape
+        for n2 in (1, 16):
+            desc = ufp4.make_desc(grid="e1m2", block=(32, 32), n=n2, sign_seed=inputs.SIGN_SEED,
+                                  scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)
+            ro = ufp4.alloc_quantized(rl, cl, desc, dev)
+            co = ufp4.alloc_quantized(cl, rl, desc, dev)
+            rq, cq = ufp4.qtensor(*ro, rl, cl), ufp4.qtensor(*co, cl, rl)
+            ms = timed(lambda i: ufp4.ufp4_rht_quantize(xls[0], desc, rq, cq, stream.cuda_stream))
+            gbs = rl * cl * (2 + 2 * (0.5 + scale_bytes(desc))) / (ms / 1e3) / 1e9
+            emit("quantize_rowcol", f"X {rl}x{cl} e1m2 32x32 UE8M0 n={n2} RTNE row+col", gbs, "GB/s",
+                 gbs / pk["hbm"], pk["hbm"], ms=ms)
 
     if "diag" in sections:
         # 3. diagnostics on the dense FPROP X

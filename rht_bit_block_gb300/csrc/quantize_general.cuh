@@ -53,8 +53,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t pad = ((raw + 127u) & ~127u) - raw;
     uint8_t* base = smem_raw + pad;
-    uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * tile_bytes);
-    const uint32_t bars = smem_addr(base + kStages * tile_bytes + 4 * p.amax_slots);  // 8-byte aligned
+    uint32_t* amax2d = reinterpret_cast<uint32_t*>(base + kStages * tile_bytes);  // 2-D: 4 sets of amax_slots
+    const uint32_t bars = smem_addr(base + kStages * tile_bytes + 16 * p.amax_slots);  // 8-byte aligned
     const uint32_t empties = bars + 8u * kStages;  // 1-D blocks: every warp done with the stage
 
     const int tid = threadIdx.x;
@@ -89,6 +89,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    for (int q = tid; q < 4 * p.amax_slots; q += kThreads) amax2d[q] = 0u;
     __syncthreads();
     // the input may come from the previous kernel, and that kernel may still
     // read buffers this one writes: wait for it before the first copy
@@ -281,8 +282,9 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 {
                     const int lnbc = 7 + (TC == 256) - lb;  // log2(TC / b)
                     const int bmask = (1 << lb) - 1;
-                    for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
-                    __syncthreads();
+                    // two slot sets per pass, used by alternate tiles: the set of
+                    // this tile was cleared during the previous one
+                    uint32_t* slots = amax2d + (i & 1) * nslot;
                     // with one row pair per thread (64-row tiles) the transformed values
                     // stay in registers while the block amax settles in shared memory;
                     // with two, the second pass transforms them again
@@ -305,15 +307,15 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                             float a0, b0, a1, b1;
                             amax_pair(e, 0, 8, a0, b0);
                             amax_pair(e, 8, 16, a1, b1);
-                            post_amax(&amax2d[sa + 2 * cchunk], a0);
-                            post_amax(&amax2d[sa + 2 * cchunk + 1], a1);
-                            post_amax(&amax2d[sb + 2 * cchunk], b0);
-                            post_amax(&amax2d[sb + 2 * cchunk + 1], b1);
+                            post_amax(&slots[sa + 2 * cchunk], a0);
+                            post_amax(&slots[sa + 2 * cchunk + 1], a1);
+                            post_amax(&slots[sb + 2 * cchunk], b0);
+                            post_amax(&slots[sb + 2 * cchunk + 1], b1);
                         } else {
                             float a0, b0;
                             amax_pair(e, 0, 16, a0, b0);
-                            post_amax(&amax2d[sa + ((cchunk * kChunk) >> lb)], a0);
-                            post_amax(&amax2d[sb + ((cchunk * kChunk) >> lb)], b0);
+                            post_amax(&slots[sa + ((cchunk * kChunk) >> lb)], a0);
+                            post_amax(&slots[sb + ((cchunk * kChunk) >> lb)], b0);
                         }
                     }
                     __syncthreads();
@@ -334,10 +336,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                         }
                         const int off = lb == 3 ? 2 * cchunk : ((cchunk * kChunk) >> lb);
                         const int sa = ((ra >> lb) << lnbc) + off, sb = ((rb >> lb) << lnbc) + off;
-                        const float MA0 = __uint_as_float(amax2d[sa]);
-                        const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
-                        const float MB0 = __uint_as_float(amax2d[sb]);
-                        const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                        const float MA0 = __uint_as_float(slots[sa]);
+                        const float MA1 = __uint_as_float(slots[lb == 3 ? sa + 1 : sa]);
+                        const float MB0 = __uint_as_float(slots[sb]);
+                        const float MB1 = __uint_as_float(slots[lb == 3 ? sb + 1 : sb]);
                         Dest A, B;
                         const int64_t la = lr0 + ra, lbr = lr0 + rb;
                         const bool colfirst = lb == 3 || (col & bmask) == 0;
@@ -360,6 +362,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                         if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, grp_id);
                         emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, dr);
                     }
+                    // the other set serves the next tile: every read of it (the
+                    // previous tile's) happened before this tile's first barrier
+                    uint32_t* other = amax2d + ((i & 1) ^ 1) * nslot;
+                    for (int q = tid; q < nslot; q += kThreads) other[q] = 0u;
                 }
             }
             if (p.do_col) {
@@ -371,8 +377,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 {
                     const int lnbq = (TR == 128 ? 7 : 6) - lb;  // log2(TR / b)
                     const int bmask = (1 << lb) - 1;
-                    for (int q = tid; q < nslot; q += kThreads) amax2d[q] = 0u;
-                    __syncthreads();
+                    uint32_t* slots = amax2d + (2 + (i & 1)) * nslot;  // the column pass's two sets
                     uint64_t keep[16];
                     for (int k = 0; k < col_tasks; ++k) {
                         const int t = warp + kWarps * k;
@@ -393,15 +398,15 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                             float a0, b0, a1, b1;
                             amax_pair(e, 0, 8, a0, b0);
                             amax_pair(e, 8, 16, a1, b1);
-                            post_amax(&amax2d[sa + 2 * rchunk], a0);
-                            post_amax(&amax2d[sa + 2 * rchunk + 1], a1);
-                            post_amax(&amax2d[sb + 2 * rchunk], b0);
-                            post_amax(&amax2d[sb + 2 * rchunk + 1], b1);
+                            post_amax(&slots[sa + 2 * rchunk], a0);
+                            post_amax(&slots[sa + 2 * rchunk + 1], a1);
+                            post_amax(&slots[sb + 2 * rchunk], b0);
+                            post_amax(&slots[sb + 2 * rchunk + 1], b1);
                         } else {
                             float a0, b0;
                             amax_pair(e, 0, 16, a0, b0);
-                            post_amax(&amax2d[sa + ((rchunk * kChunk) >> lb)], a0);
-                            post_amax(&amax2d[sb + ((rchunk * kChunk) >> lb)], b0);
+                            post_amax(&slots[sa + ((rchunk * kChunk) >> lb)], a0);
+                            post_amax(&slots[sb + ((rchunk * kChunk) >> lb)], b0);
                         }
                     }
                     __syncthreads();
@@ -423,10 +428,10 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                         }
                         const int off = lb == 3 ? 2 * rchunk : ((rchunk * kChunk) >> lb);
                         const int sa = ((tcol >> lb) << lnbq) + off, sb = (((tcol + 1) >> lb) << lnbq) + off;
-                        const float MA0 = __uint_as_float(amax2d[sa]);
-                        const float MA1 = __uint_as_float(amax2d[lb == 3 ? sa + 1 : sa]);
-                        const float MB0 = __uint_as_float(amax2d[sb]);
-                        const float MB1 = __uint_as_float(amax2d[lb == 3 ? sb + 1 : sb]);
+                        const float MA0 = __uint_as_float(slots[sa]);
+                        const float MA1 = __uint_as_float(slots[lb == 3 ? sa + 1 : sa]);
+                        const float MB0 = __uint_as_float(slots[sb]);
+                        const float MB1 = __uint_as_float(slots[lb == 3 ? sb + 1 : sb]);
                         const int64_t lrow = lr0 + rchunk * kChunk;
                         const int64_t ca = c0 + tcol, cb = ca + 1;
                         const bool rowfirst = lb == 3 || (lrow & bmask) == 0;
@@ -449,6 +454,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                         if (SR) draw_pair(dr, p.sr_keys, A, B, 1u, grp_id);
                         emit_pair<GRID, SR, PO2 ? 1 : 0>(e, MA0, MA1, MB0, MB1, lb == 3, fd, A, B, dr);
                     }
+                    uint32_t* other = amax2d + (2 + ((i & 1) ^ 1)) * nslot;
+                    for (int q = tid; q < nslot; q += kThreads) other[q] = 0u;
                 }
             }
         }
@@ -499,7 +506,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
 template <int GRID, bool SR, bool PO2, int TC, bool N16>
 static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int num_tiles, int num_sms,
                             cudaStream_t st) {
-    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 4 * (size_t)p.amax_slots + 16 * p.stages + 128;
+    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 16 * (size_t)p.amax_slots + 16 * p.stages + 128;
     auto k = quantize_kernel<GRID, SR, PO2, TC, N16>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
