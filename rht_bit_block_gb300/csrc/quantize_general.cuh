@@ -42,7 +42,9 @@ constexpr int kCtasPerSm = 2;               // 16 warps per SM, up to 128 regist
 // kWaitLimit).
 static __device__ uint32_t g_quant_wait_limit = kWaitLimit;
 
-template <int GRID, bool SR, bool PO2, int TC, bool N16>
+// TWO_D: b x b blocks (compile-time, so that each instantiation carries only
+// its own block path); they need power-of-two scales (PO2).
+template <int GRID, bool SR, bool PO2, int TC, bool N16, bool TWO_D>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, const int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
@@ -89,7 +91,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
-    for (int q = tid; q < 4 * p.amax_slots; q += kThreads) amax2d[q] = 0u;
+    if (TWO_D)
+        for (int q = tid; q < 4 * p.amax_slots; q += kThreads) amax2d[q] = 0u;
     __syncthreads();
     // the input may come from the previous kernel, and that kernel may still
     // read buffers this one writes: wait for it before the first copy
@@ -156,7 +159,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         // then give up on the stages it no longer releases).  2-D blocks keep
         // the CTA barrier, which their block amax needs anyway.
         const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (p.is2d) {
+        if (TWO_D) {
             if (!__syncthreads_and(landed)) {
                 if (tid == 0) atomicExch(&g_quant_error, 1);
                 break;
@@ -181,7 +184,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             __syncthreads();
         }
 
-        if (!p.is2d) {
+        if (!TWO_D) {
             // ------------------------------------------ 1-D blocks, both passes
             // the row pairs and the column tasks of this tile go through one
             // emit site, so that the scale, rounding and packing code (long
@@ -370,7 +373,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             }
             if (p.do_col) {
                 const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
-                const int lsd = p.is2d ? lb : lbwc;
+                const int lsd = TWO_D ? lb : lbwc;
                 const int64_t sc_ld = p.col_grouped ? (padded >> lsd) : p.col.scales_ld;
                 uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
                 uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lsd) * SZ : 0);
@@ -462,7 +465,7 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
         // the fence orders this CTA's generic shared-memory accesses (reads,
         // and the zero rows of a group's end) before the async-proxy refill
         const int next = tile + kStages * gridDim.x;
-        if (p.is2d) {
+        if (TWO_D) {
             // everyone is done with stage s: refill it
             __syncthreads();
             if (tid == 0 && next < num_tiles) {
@@ -507,7 +510,10 @@ template <int GRID, bool SR, bool PO2, int TC, bool N16>
 static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int num_tiles, int num_sms,
                             cudaStream_t st) {
     const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 16 * (size_t)p.amax_slots + 16 * p.stages + 128;
-    auto k = quantize_kernel<GRID, SR, PO2, TC, N16>;
+    auto k = quantize_kernel<GRID, SR, PO2, TC, N16, false>;
+    if constexpr (PO2) {
+        if (p.is2d) k = quantize_kernel<GRID, SR, PO2, TC, N16, true>;
+    }
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = num_tiles < kCtasPerSm * num_sms ? num_tiles : kCtasPerSm * num_sms;
@@ -560,9 +566,14 @@ static cudaError_t general_set_wait_limit(uint32_t polls) {
 // function that has not been loaded yet).
 template <int G, bool SR, bool PO2>
 static void preload_q(cudaFuncAttributes* a) {
-    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, true>);
-    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, false>);
-    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 256, false>);
+    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, true, false>);
+    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, false, false>);
+    cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 256, false, false>);
+    if constexpr (PO2) {
+        cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, true, true>);
+        cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 128, false, true>);
+        cudaFuncGetAttributes(a, quantize_kernel<G, SR, PO2, 256, false, true>);
+    }
 }
 template <bool SR>
 static cudaError_t preload_general() {
