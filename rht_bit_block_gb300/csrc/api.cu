@@ -293,7 +293,7 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     p.col_seg_lanes = seg_lanes;
     p.amax_slots = bs.is2d ? (tr / bs.b2d) * (tc / bs.b2d) : 0;
     p.tile_rows = tr;
-    p.stages = std::max(2, std::min(6, (96 * 1024) / (tr * tc * 2)));  // about 96 KB of tiles per CTA, 2 CTAs per SM
+    p.stages = 0;  // set by the launcher (the ring depth depends on the block shape)
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
     p.lbw_row = ilog2(bs.bw);
     p.lbw_col = ilog2(bs.bw);

@@ -21,6 +21,7 @@
 // kernels and quantize_sr.cu the SR ones, so the two compile in parallel.
 #pragma once
 
+#include <algorithm>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -35,7 +36,10 @@ namespace ufp4 {
 // instantiates it (quantize.cu: RTNE, quantize_sr.cu: SR).
 static __device__ int g_quant_error;
 
-constexpr int kCtasPerSm = 2;               // 16 warps per SM, up to 128 registers a thread; about 96 KB of ring per CTA
+// CTAs per SM: 2-D blocks 2 (16 warps, up to 128 registers a thread, about
+// 96 KB of ring each); 1-D blocks 3 (24 warps, up to 80 registers, about
+// 64 KB of ring each)
+__host__ __device__ constexpr int general_ctas(bool two_d) { return two_d ? 2 : 3; }
 
 // Polls of a tile's barrier before a general-kernel CTA gives up (a failure-
 // detection hook can lower it; the drain of copies in flight always uses
@@ -45,7 +49,7 @@ static __device__ uint32_t g_quant_wait_limit = kWaitLimit;
 // TWO_D: b x b blocks (compile-time, so that each instantiation carries only
 // its own block path); they need power-of-two scales (PO2).
 template <int GRID, bool SR, bool PO2, int TC, bool N16, bool TWO_D>
-__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+__global__ void __launch_bounds__(kThreads, general_ctas(TWO_D))
 quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, const int num_tiles) {
     extern __shared__ uint8_t smem_raw[];
     constexpr int SZ = PO2 ? 1 : 4;         // bytes per scale
@@ -509,15 +513,19 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
 template <int GRID, bool SR, bool PO2, int TC, bool N16>
 static cudaError_t launch_q(const CUtensorMap& map, const QuantParams& p, int num_tiles, int num_sms,
                             cudaStream_t st) {
-    const size_t smem = (size_t)p.stages * p.tile_rows * TC * 2 + 16 * (size_t)p.amax_slots + 16 * p.stages + 128;
+    // ring: about 96 KB of tiles per CTA with 2-D blocks (2 CTAs per SM), 64 KB with 1-D ones (3)
+    const int ctas = general_ctas(p.is2d);
+    QuantParams q = p;
+    q.stages = std::max(2, std::min(kMaxStages, (p.is2d ? 96 : 64) * 1024 / (p.tile_rows * TC * 2)));
+    const size_t smem = (size_t)q.stages * q.tile_rows * TC * 2 + 16 * (size_t)q.amax_slots + 16 * q.stages + 128;
     auto k = quantize_kernel<GRID, SR, PO2, TC, N16, false>;
     if constexpr (PO2) {
         if (p.is2d) k = quantize_kernel<GRID, SR, PO2, TC, N16, true>;
     }
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int grid = num_tiles < kCtasPerSm * num_sms ? num_tiles : kCtasPerSm * num_sms;
-    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, map, p, num_tiles);
+    const int grid = num_tiles < ctas * num_sms ? num_tiles : ctas * num_sms;
+    return launch_pdl(k, dim3(grid), dim3(kThreads), smem, st, map, q, num_tiles);
 }
 
 // Tile shapes: 128 columns with the n = 16 butterflies fixed at compile
