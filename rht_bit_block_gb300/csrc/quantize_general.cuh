@@ -142,6 +142,26 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
     const int step_r = gridDim.x / p.col_tiles, step_c = gridDim.x - step_r * p.col_tiles;
     int row_tile = blockIdx.x / p.col_tiles, col_tile = blockIdx.x - row_tile * p.col_tiles;
     int g = p.num_groups > 1 ? find_group(p, row_tile) : 0;
+    // values of the current group, reloaded only when the group changes
+    int gt0;                 // first row tile of the group
+    int64_t grow0, cnt;      // first input row and row count
+    int64_t padded;          // padded row count (column-wise output)
+    uint32_t grp_id;         // SR counter group id
+    int64_t out_ld1, sc_ld1; // 1-D column-wise output: code and scale leading dimensions
+    uint8_t* gcodes1;        // 1-D column-wise output: the group's codes and scales
+    uint8_t* gscales1;
+    auto load_group = [&](int gg) {
+        gt0 = p.grp_tile0[gg];
+        grow0 = p.grp_row0[gg];
+        cnt = p.grp_row0[gg + 1] - grow0;
+        padded = p.grp_pad0[gg + 1] - p.grp_pad0[gg];
+        grp_id = (uint32_t)(p.group_base + gg);
+        out_ld1 = p.col_grouped ? padded / 2 : p.col.codes_ld;
+        sc_ld1 = p.col_grouped ? (padded >> p.lbw_col) : p.col.scales_ld;
+        gcodes1 = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[gg] / 2) : 0);
+        gscales1 = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[gg] >> p.lbw_col) * SZ : 0);
+    };
+    load_group(g);
 
     int i = 0;
     int s = 0;            // ring stage of tile i
@@ -156,7 +176,13 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
                 col_tile -= p.col_tiles;
                 ++row_tile;
             }
-            if (p.num_groups > 1) g = find_group(p, row_tile);
+            if (p.num_groups > 1) {
+                const int ng = find_group(p, row_tile);
+                if (ng != g) {
+                    g = ng;
+                    load_group(g);
+                }
+            }
         }
         // 1-D blocks: no CTA barrier per tile; each warp waits for the copy
         // itself, and a warp whose wait gave up leaves the loop (the others
@@ -172,12 +198,8 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             if (lane == 0) atomicExch(&g_quant_error, 1);
             break;
         }
-        const int64_t lr0 = (int64_t)(row_tile - p.grp_tile0[g]) * TR;
+        const int64_t lr0 = (int64_t)(row_tile - gt0) * TR;
         const int64_t c0 = (int64_t)col_tile * TC;
-        const int64_t grow0 = p.grp_row0[g];
-        const int64_t cnt = p.grp_row0[g + 1] - grow0;
-        const int64_t padded = p.grp_pad0[g + 1] - p.grp_pad0[g];
-        const uint32_t grp_id = (uint32_t)(p.group_base + g);
         uint16_t* tile_s = reinterpret_cast<uint16_t*>(base + s * tile_bytes);
         if (p.do_col && lr0 + TR > cnt) {
             // rows past the group's end belong to the next group (or the
@@ -198,10 +220,9 @@ quantize_kernel(const __grid_constant__ CUtensorMap tmap, const QuantParams p, c
             // rows of this tile that exist, counted from this thread's first row
             const int64_t left = cnt - lr0 - r0;
             const uint16_t* src = tile_s + r0 * TC + cchunk * kChunk;
-            const int64_t out_ld = p.col_grouped ? padded / 2 : p.col.codes_ld;
-            const int64_t sc_ld = p.col_grouped ? (padded >> lbwc) : p.col.scales_ld;
-            uint8_t* gcodes = (uint8_t*)p.col.codes + (p.col_grouped ? p.cols * (p.grp_pad0[g] / 2) : 0);
-            uint8_t* gscales = (uint8_t*)p.col.scales + (p.col_grouped ? p.cols * (p.grp_pad0[g] >> lbwc) * SZ : 0);
+            const int64_t out_ld = out_ld1, sc_ld = sc_ld1;
+            uint8_t* gcodes = gcodes1;
+            uint8_t* gscales = gscales1;
             const bool wsc = (col & ((1 << lbw) - 1)) == 0;
             // output pointers of this thread's first row, stepped per pair
             const int64_t orow0 = grow0 + lr0 + r0;  // row-wise output rows follow the input rows
