@@ -194,9 +194,15 @@ __device__ __forceinline__ void draw_pair(SrDraws& d, const SrKeys& keys, const 
     sr_draws16x2(keys, A.lin0, B.lin0, stream, group, d.a, d.b);
 }
 
+// nega / negb: the sign bit (0 or 0x80000000) of a vector held negated; its
+// reciprocal then carries that sign, so that t = y r is the value of the
+// unnegated vector (exact: IEEE products are sign-symmetric).  join: B's codes
+// follow A's (A.codes + 8, 16-byte aligned, A.valid == B.valid), stored as one
+// 16-byte word.
 template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
-                                          const Fold& fd, const Dest& A, const Dest& B, const SrDraws& dr) {
+                                          const Fold& fd, const Dest& A, const Dest& B, const SrDraws& dr,
+                                          uint32_t nega = 0u, uint32_t negb = 0u, bool join = false) {
     // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
     // to the value in units of the grid step (below): INT4 k, E1M2 4 t
     constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
@@ -210,6 +216,16 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         ra1 = block_recip<GRID, SF>(MA1, fd, lf, A.valid && A.w1, A.s1);
         rb1 = block_recip<GRID, SF>(MB1, fd, lf, B.valid && B.w1, B.s1);
     }
+    const float sa0 = __uint_as_float(__float_as_uint(ra0) ^ nega), sa1 = __uint_as_float(__float_as_uint(ra1) ^ nega);
+    const float sb0 = __uint_as_float(__float_as_uint(rb0) ^ negb), sb1 = __uint_as_float(__float_as_uint(rb1) ^ negb);
+    auto store_pair = [&](uint2 ca, uint2 cb) {
+        if (join) {
+            if (A.valid) *reinterpret_cast<uint4*>(A.codes) = make_uint4(ca.x, ca.y, cb.x, cb.y);
+        } else {
+            if (A.valid) *reinterpret_cast<uint2*>(A.codes) = ca;
+            if (B.valid) *reinterpret_cast<uint2*>(B.codes) = cb;
+        }
+    };
     if (!fd.pow4) {
         const uint64_t is2 = pk2(fd.inv_s, fd.inv_s);
 #pragma unroll
@@ -218,7 +234,7 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
     if (GRID == 4) {
         // MXFP8: t = z * 2^-e (exact), one E4M3 byte per element, nearest
         // even, saturated at 448; a zero byte keeps no sign
-        const uint64_t q = pk2(ra0, rb0);
+        const uint64_t q = pk2(sa0, sb0);
         float ta[16], tb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) up2(mul2(e[i], q), ta[i], tb[i]);
@@ -245,7 +261,7 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         // bit 3 of o gives the two's complement nibble of k.  E1M2: o >= 8
         // (k >= 0) becomes o - 8 = k; o < 8 (k < 0) becomes (o ^ 15) + 1 =
         // 8 + |k|, the sign-magnitude nibble, and k = 0 is +0.
-        const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1), cc = pk2(12582920.0f, 12582920.0f);
+        const uint64_t q0 = pk2(sa0, sb0), q1 = pk2(sa1, sb1), cc = pk2(12582920.0f, 12582920.0f);
         uint32_t va[16], vb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -259,10 +275,8 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
             const uint32_t neg = ((w >> 3) & 0x11111111u) ^ 0x11111111u;  // per nibble: 1 iff o < 8
             return (w ^ (neg * 7u + 0x88888888u)) + neg;
         };
-        if (A.valid)
-            *reinterpret_cast<uint2*>(A.codes) = make_uint2(finish(pack_offsets8<>(va)), finish(pack_offsets8<>(va + 8)));
-        if (B.valid)
-            *reinterpret_cast<uint2*>(B.codes) = make_uint2(finish(pack_offsets8<>(vb)), finish(pack_offsets8<>(vb + 8)));
+        store_pair(make_uint2(finish(pack_offsets8<>(va)), finish(pack_offsets8<>(va + 8))),
+                   make_uint2(finish(pack_offsets8<>(vb)), finish(pack_offsets8<>(vb + 8))));
         return;
     }
     if (SR && GRID <= 1) {
@@ -281,7 +295,10 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         const uint32_t* wa = dr.a;
         const uint32_t* wb = dr.b;
         const uint64_t c196 = pk2(8388804.0f, 8388804.0f);
-        const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
+        const uint64_t q0 = pk2(sa0, sb0), q1 = pk2(sa1, sb1);
+        // the sign of t: y's sign bit flipped for a negated vector (the
+        // SF == 1 form takes |y| times the unsigned reciprocal)
+        const uint32_t csa = (SF == 1 ? nega : 0u) | 0x40800000u, csb = (SF == 1 ? negb : 0u) | 0x40800000u;
         uint32_t va[16], vb[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -297,8 +314,8 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
                 up2(mul2(e[i], i < 8 ? q0 : q1), ya, yb);
                 x = sub2_rm(pk2(ua, ub), pk2(fminf(fabsf(ya), 7.0f), fminf(fabsf(yb), 7.0f)));
             }
-            const uint64_t cs = pk2(__uint_as_float((__float_as_uint(ya) & 0x80000000u) | 0x40800000u),
-                                    __uint_as_float((__float_as_uint(yb) & 0x80000000u) | 0x40800000u));
+            const uint64_t cs = pk2(__uint_as_float((__float_as_uint(ya) & 0x80000000u) ^ csa),
+                                    __uint_as_float((__float_as_uint(yb) & 0x80000000u) ^ csb));
             float a, b;
             up2(sub2(sub2_rp(c196, x), cs), a, b);
             va[i] = __float_as_uint(a);
@@ -315,11 +332,10 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
                 ob[h] = signmag_to_twos(ob[h]);
             }
         }
-        if (A.valid) *reinterpret_cast<uint2*>(A.codes) = make_uint2(oa[0], oa[1]);
-        if (B.valid) *reinterpret_cast<uint2*>(B.codes) = make_uint2(ob[0], ob[1]);
+        store_pair(make_uint2(oa[0], oa[1]), make_uint2(ob[0], ob[1]));
         return;
     }
-    const uint64_t q0 = pk2(ra0, rb0), q1 = pk2(ra1, rb1);
+    const uint64_t q0 = pk2(sa0, sb0), q1 = pk2(sa1, sb1);
     float ta[16], tb[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) up2(mul2(e[i], i < 8 ? q0 : q1), ta[i], tb[i]);
@@ -333,8 +349,7 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         cb = make_uint2(rtne8<GRID>(tb[0], tb[1], tb[2], tb[3], tb[4], tb[5], tb[6], tb[7]),
                         rtne8<GRID>(tb[8], tb[9], tb[10], tb[11], tb[12], tb[13], tb[14], tb[15]));
     }
-    if (A.valid) *reinterpret_cast<uint2*>(A.codes) = ca;
-    if (B.valid) *reinterpret_cast<uint2*>(B.codes) = cb;
+    store_pair(ca, cb);
 }
 
 // 1-D block amax over bw/16 neighbouring lanes (bw >= 16), for both vectors.

@@ -318,17 +318,21 @@ constexpr int kRowsCtas = 2, kRowsStages = 3;
 // groups.  The 64 values are held as pairs (v_i, v_i+32): strides 1 .. 16 are
 // paired adds, stride 32 adds the two halves of each pair, and for n = 256
 // strides 64 and 128 pair the thread with the lanes holding the neighbouring
-// segments (lane ^ 8, lane ^ 16).  The random signs: n = 64 reads a per-
-// element mask table from the kernel parameters (the same for every segment);
-// n = 256 from a table in shared memory, one 64-entry set per segment.
+// segments (lane ^ 8, lane ^ 16), each lane keeping half of the values.  The
+// random signs: n = 64 reads a per-element mask table from the kernel
+// parameters (the same for every segment); n = 256 from a table in shared
+// memory, one 64-entry set per segment.
 // 1-D blocks: no CTA barrier per tile; each warp waits on the stage's TMA
 // barrier itself and, when done with the stage, arrives on the stage's
 // "empty" barrier; thread 0 waits on that one before it refills the stage.
 // TWO_D (b = 16, 32, 64; UE8M0): the block amax is reduced over the rows a
 // warp holds (lanes ^ 1, 2, 4, and ^ 16 for two segments a row), then across
-// warps with a shared-memory atomicMax, with the CTA barrier per tile; the
-// amax slots come in two sets used by alternate tiles (a set is cleared
-// during the tile before its use).
+// warps with a shared-memory atomicMax and one CTA barrier per tile; the ring
+// runs as for 1-D blocks.  The amax slots come in three sets used in turn:
+// after tile i's barrier the set of tile i + 2 is cleared.  Its last reads
+// (tile i - 1) precede tile i's barrier in every warp, and its next
+// atomicMax (tile i + 2) follows tile i + 1's barrier, which the clearing
+// threads reach only after the clear.
 template <int GRID, bool SR, int SF, int CTAS, int QN, bool TWO_D>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
@@ -349,7 +353,7 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     const uint32_t bars = smem_addr(base + kStages * kTileBytes);
     const uint32_t empties = bars + 32u;
     uint32_t* sgn_tab = reinterpret_cast<uint32_t*>(base + kStages * kTileBytes + 64);  // n = 256: [segment][j], 16-byte aligned
-    uint32_t* amax2d = sgn_tab + 256;  // 2-D blocks: two sets of kSlots
+    uint32_t* amax2d = sgn_tab + 256;  // 2-D blocks: three sets of kSlots
     const int tid = threadIdx.x;
     const int seg = (tid >> 3) & (QN - 1);
     const int r = (tid & 7) + 8 * (tid >> (3 + kLQ));
@@ -385,13 +389,13 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
             asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bars + 8u * s));
-            if (!TWO_D) asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(empties + 8u * s), "r"(kWarps));
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (QN == 4)  // mask of element j of segment q: 0x80000000 when eps_(64 q + j) = -1
         sgn_tab[tid] = ((p.sign_bits[tid >> 5] >> (tid & 31)) & 1u) << 31;
-    if (TWO_D && tid < 2 * kSlots) amax2d[tid] = 0u;
+    if (TWO_D && tid < 3 * kSlots) amax2d[tid] = 0u;
     const int lb = p.lb2d;  // log2 b (2-D blocks)
     __syncthreads();
     griddep_wait();
@@ -419,6 +423,7 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
     int s = 0;
     uint32_t phase = 0;
     int i = 0;
+    bool refill_failed = false;  // 2-D: thread 0 could not refill a stage (carried to the next barrier)
     for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x, ++i) {
         if (i) {
             ct += step_c;
@@ -429,17 +434,14 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
             }
             if (rt >= p.t[t].row_tiles) relocate(tile);
         }
-        // 1-D blocks: no CTA barrier per tile; each warp waits for the copy
-        // itself, and a warp whose wait gave up leaves the loop (the others
-        // then give up on the stages it no longer releases).  2-D blocks keep
-        // the CTA barrier, which their block amax needs anyway.
-        const bool landed = wait_phase(bars + 8u * s, phase, wait_limit);
-        if (TWO_D) {
-            if (!__syncthreads_and(landed)) {
-                if (tid == 0) atomicExch(&g_rows_error, 1);
-                break;
-            }
-        } else if (!__all_sync(0xFFFFFFFFu, landed)) {
+        // Each warp waits for the copy itself.  1-D blocks: a warp whose
+        // wait gave up leaves the loop (the others then give up on the stages
+        // it no longer releases).  2-D blocks: it goes on to the tile's CTA
+        // barrier (reading a stage that may not have landed, writing nothing
+        // global before it), where every warp learns of it and leaves.
+        const bool ok = __all_sync(0xFFFFFFFFu, wait_phase(bars + 8u * s, phase, wait_limit)) &&
+                        !(TWO_D && __shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0));
+        if (!TWO_D && !ok) {
             if (lane == 0) atomicExch(&g_rows_error, 1);
             break;
         }
@@ -486,132 +488,234 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                 e[q + h] = sub2(a, b);
             }
         }
+        if constexpr (QN == 4) {
+            // Strides 32, 64 and 128 with half exchanges.  Lane (b1, b0) of a
+            // row's four (segment S = 2 b1 + b0) keeps half of what it holds at
+            // each step and sends the other half, one shuffle per kept value:
+            //  * stride 32 (in the pair): keep position q + 32 b0 of S, send
+            //    q + 32 (1 - b0): a + s b and a - s b with s = +1 (b0 = 0) or -1;
+            //  * stride 64 (lane ^ 8, segments 2 b1 and 2 b1 + 1, same positions):
+            //    keep = mine + t recv, send = mine - t recv, t = +1 (b1 = 0) or -1,
+            //    so b1 = 0 keeps the sums and b1 = 1 the differences (negated
+            //    where b0 = 1, as is the sent difference of b0 = 1, b1 = 0);
+            //  * stride 128 (lane ^ 16): out1 = keep + recv, out2 = keep - recv.
+            // Lane (b1, b0) ends with segments b1 (out1) and 2 + b1 (out2) at
+            // positions 32 b0 + j (.x) and 32 b0 + 16 + j (.y), j < 16: chunks
+            // 2 b0 and 2 b0 + 1 of each.  Every value equals the butterfly's
+            // up to its sign (RN(a - b) = -RN(b - a)): out1 is negated on lane
+            // (1, 1) and out2 on lane (1, 0), which the reciprocal's sign undoes.
+            const int b0 = seg & 1, b1 = seg >> 1;
+            const float s0 = b0 ? -1.0f : 1.0f;
+            uint64_t K[16], S[16];
 #pragma unroll
-        for (int q = 0; q < 32; ++q) {  // stride 32: the two halves of each pair
-            float a, b;
-            up2(e[q], a, b);
-            e[q] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
-        }
-        if (QN == 4) {
-            // strides 64 and 128: the lower segment of a pair forms a + b, the
-            // upper one a - b, i.e. o + s e with s = +1 or -1 (exact product)
-#pragma unroll
-            for (int lm = 1; lm <= 2; lm <<= 1) {
-                const float sg = (seg & lm) ? -1.0f : 1.0f;
-                const uint64_t s2 = pk2(sg, sg);
-#pragma unroll
-                for (int q = 0; q < 32; ++q) {
-                    const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)e[q], 8 * lm);
-                    e[q] = fma2(s2, e[q], o);
-                }
+            for (int j = 0; j < 16; ++j) {
+                float a0, c0, a1, c1;
+                up2(e[j], a0, c0);
+                up2(e[j + 16], a1, c1);
+                K[j] = pk2(__fmaf_rn(s0, c0, a0), __fmaf_rn(s0, c1, a1));
+                S[j] = pk2(__fmaf_rn(-s0, c0, a0), __fmaf_rn(-s0, c1, a1));
             }
-        }
-        // block amax: (chunk 0, chunk 2) from pairs 0..15, (chunk 1, chunk 3) from pairs 16..31
-        float M0, M2, M1, M3;
-        amax_pair(e, 0, 16, M0, M2);
-        amax_pair(e + 16, 0, 16, M1, M3);
-        const bool b32 = TWO_D ? lb >= 5 : lbw == 5;
-        if (b32) {
-            M0 = M1 = fmaxf(M0, M1);
-            M2 = M3 = fmaxf(M2, M3);
-        }
-        if (TWO_D) {
-            if (lb == 6) M0 = M1 = M2 = M3 = fmaxf(M0, M2);
-            // the rows of this warp in the same b-row band: lanes ^ 1, 2, 4 (and
-            // ^ 16: rows + 8 with two segments a row); b >= 16 covers them all
+            const float tau = b1 ? -1.0f : 1.0f;
+            const uint64_t t2 = pk2(tau, tau), nt2 = pk2(-tau, -tau);
 #pragma unroll
-            for (int k = 1; k <= (QN == 2 ? 16 : 4); k <<= 1) {
-                if (k == 8) continue;
-                M0 = fmaxf(M0, __shfl_xor_sync(0xFFFFFFFFu, M0, k));
-                M1 = fmaxf(M1, __shfl_xor_sync(0xFFFFFFFFu, M1, k));
-                M2 = fmaxf(M2, __shfl_xor_sync(0xFFFFFFFFu, M2, k));
-                M3 = fmaxf(M3, __shfl_xor_sync(0xFFFFFFFFu, M3, k));
+            for (int j = 0; j < 16; ++j) {
+                const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)S[j], 8);
+                S[j] = fma2(nt2, o, K[j]);
+                K[j] = fma2(t2, o, K[j]);
             }
-            // then across the warps of the band: slot (row block, column block)
-            uint32_t* set = amax2d + (i & 1) * kSlots;
-            const int lnbc = (QN == 2 ? 7 : 8) - lb;  // log2(TC / b)
-            const int slot0 = ((r >> lb) << lnbc) + ((64 * seg) >> lb);
-            const int cpb = (1 << lb) >> 4;  // chunks per block column
-            if ((lane & (QN == 2 ? 0x17 : 0x7)) == 0) {
-                atomicMax(&set[slot0], __float_as_uint(M0));
-                if (cpb == 1) atomicMax(&set[slot0 + 1], __float_as_uint(M1));
-                if (cpb <= 2) atomicMax(&set[slot0 + (cpb == 1 ? 2 : 1)], __float_as_uint(M2));
-                if (cpb == 1) atomicMax(&set[slot0 + 3], __float_as_uint(M3));
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const uint64_t o = (uint64_t)__shfl_xor_sync(0xFFFFFFFFu, (unsigned long long)S[j], 16);
+                S[j] = sub2(K[j], o);
+                K[j] = add2(K[j], o);
             }
-            __syncthreads();
-            M0 = __uint_as_float(set[slot0]);
-            M1 = __uint_as_float(set[slot0 + (cpb == 1 ? 1 : 0)]);
-            M2 = __uint_as_float(set[slot0 + (cpb == 1 ? 2 : (cpb == 2 ? 1 : 0))]);
-            M3 = __uint_as_float(set[slot0 + (cpb == 1 ? 3 : (cpb == 2 ? 1 : 0))]);
-            // the other set serves the next tile: every read of it (the
-            // previous tile's) happened before this tile's first barrier
-            uint32_t* other = amax2d + ((i & 1) ^ 1) * kSlots;
-            if (tid < kSlots) other[tid] = 0u;
-        }
-        uint8_t* cp = T.codes + (int64_t)row * T.codes_ld + (GRID == 4 ? col : col >> 1);
-        uint8_t* sp = T.scales + ((int64_t)row * T.scales_ld + (col >> lbw)) * SZ;
-        const int cstride = GRID == 4 ? 16 : 8;  // code bytes per 16 elements
-        const uint64_t lin0 = (uint64_t)row * (uint64_t)T.cols + (uint64_t)col;
-        Dest A, B;
-        // 2-D: one UE8M0 byte per b x b block at (row / b, column / b), written
-        // by the thread holding its top-left chunk
-        uint8_t* sp2 = T.scales + (int64_t)(row >> lb) * T.scales_ld;
-        const bool rfirst = (row & ((1 << lb) - 1)) == 0;
-        auto chunk_scale = [&](int c, uint8_t*& sptr, bool& w) {
-            const int cc = col + 16 * c;
+            const uint32_t neg1 = (b1 & b0) ? 0x80000000u : 0u;
+            const uint32_t neg2 = (b1 & (b0 ^ 1)) ? 0x80000000u : 0u;
+            // chunk amax: (2 b0, 2 b0 + 1) of segment b1 (MA1, MB1) and of 2 + b1 (MA2, MB2)
+            float MA1, MB1, MA2, MB2;
+            amax_pair(K, 0, 16, MA1, MB1);
+            amax_pair(S, 0, 16, MA2, MB2);
+            const bool b32 = TWO_D ? lb >= 5 : lbw == 5;
+            if (b32) {
+                MA1 = MB1 = fmaxf(MA1, MB1);
+                MA2 = MB2 = fmaxf(MA2, MB2);
+            }
+            const int c1 = 64 * b1 + 32 * b0;  // tile column of chunk 2 b0 of segment b1 (+128: of 2 + b1)
             if (TWO_D) {
-                sptr = sp2 + (cc >> lb);
-                w = rfirst && (cc & ((1 << lb) - 1)) == 0;
-            } else {
-                sptr = sp + (cc - col) / (b32 ? 32 : 16) * SZ;
-                w = !b32 || (c & 1) == 0;
+                if (lb == 6) {  // a 64-wide block: both halves of the segment (lane ^ 8)
+                    MA1 = MB1 = fmaxf(MA1, __shfl_xor_sync(0xFFFFFFFFu, MA1, 8));
+                    MA2 = MB2 = fmaxf(MA2, __shfl_xor_sync(0xFFFFFFFFu, MA2, 8));
+                }
+                // the eight rows of this warp (lanes ^ 1, 2, 4): one b-row band for b >= 16
+#pragma unroll
+                for (int k = 1; k <= 4; k <<= 1) {
+                    MA1 = fmaxf(MA1, __shfl_xor_sync(0xFFFFFFFFu, MA1, k));
+                    MB1 = fmaxf(MB1, __shfl_xor_sync(0xFFFFFFFFu, MB1, k));
+                    MA2 = fmaxf(MA2, __shfl_xor_sync(0xFFFFFFFFu, MA2, k));
+                    MB2 = fmaxf(MB2, __shfl_xor_sync(0xFFFFFFFFu, MB2, k));
+                }
+                // then across the warps of the band: slot (row block, column block)
+                uint32_t* set = amax2d + (i % 3) * kSlots;
+                const int rs = (r >> lb) << (8 - lb);
+                const int sA1 = rs + (c1 >> lb), sB1 = rs + ((c1 + 16) >> lb);
+                const int sA2 = rs + ((c1 + 128) >> lb), sB2 = rs + ((c1 + 144) >> lb);
+                if ((lane & 7) == 0 && (lb < 6 || b0 == 0)) {
+                    atomicMax(&set[sA1], __float_as_uint(MA1));
+                    atomicMax(&set[sA2], __float_as_uint(MA2));
+                    if (lb == 4) {
+                        atomicMax(&set[sB1], __float_as_uint(MB1));
+                        atomicMax(&set[sB2], __float_as_uint(MB2));
+                    }
+                }
+                if (!__syncthreads_and(ok)) {
+                    if (tid == 0) atomicExch(&g_rows_error, 1);
+                    break;
+                }
+                MA1 = __uint_as_float(set[sA1]);
+                MB1 = __uint_as_float(set[sB1]);
+                MA2 = __uint_as_float(set[sA2]);
+                MB2 = __uint_as_float(set[sB2]);
+                // the set of tile i + 2 (last read in tile i - 1)
+                if (tid < kSlots) amax2d[((i + 2) % 3) * kSlots + tid] = 0u;
             }
-        };
-        // chunks 0 and 2
-        A.codes = cp;
-        B.codes = cp + 2 * cstride;
-        chunk_scale(0, A.s0, A.w0);
-        chunk_scale(2, B.s0, B.w0);
-        A.s1 = A.s0;
-        B.s1 = B.s0;
-        A.valid = B.valid = valid;
-        A.w1 = B.w1 = false;
-        A.lin0 = lin0;
-        B.lin0 = lin0 + 32;
-        {
-            SrDraws dr;
-            if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
-            emit_pair<GRID, SR, SF>(e, M0, M0, M2, M2, false, fd, A, B, dr);
-        }
-        // chunks 1 and 3 (their 1 x 32 scales were written with chunks 0 and 2)
-        A.codes = cp + cstride;
-        B.codes = cp + 3 * cstride;
-        chunk_scale(1, A.s0, A.w0);
-        chunk_scale(3, B.s0, B.w0);
-        A.s1 = A.s0;
-        B.s1 = B.s0;
-        A.lin0 = lin0 + 16;
-        B.lin0 = lin0 + 48;
-        {
-            SrDraws dr;
-            if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
-            emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, dr);
-        }
-        const int next = tile + kStages * gridDim.x;
-        if (TWO_D) {
-            // everyone is done with stage s: refill it
-            __syncthreads();
-            if (tid == 0 && next < p.num_tiles) {
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                issue(next, s);
-                issued = i + kStages + 1;
+            const bool join = GRID != 4 && (T.codes_ld & 15) == 0;
+            const int64_t rowlin = (int64_t)row * T.cols;
+            uint8_t* const crow = T.codes + (int64_t)row * T.codes_ld;
+            uint8_t* const sp2 = T.scales + (int64_t)(row >> lb) * T.scales_ld;
+            const bool rfirst = (row & ((1 << lb) - 1)) == 0;
+            auto dest = [&](int cc, Dest& D) {  // cc: column of the chunk
+                D.codes = crow + (GRID == 4 ? cc : cc >> 1);
+                if (TWO_D) {
+                    D.s0 = sp2 + (cc >> lb);
+                    D.w0 = rfirst && (cc & ((1 << lb) - 1)) == 0;
+                } else {
+                    D.s0 = T.scales + ((int64_t)row * T.scales_ld + (cc >> lbw)) * SZ;
+                    D.w0 = !b32 || (cc & 31) == 0;
+                }
+                D.s1 = D.s0;
+                D.w1 = false;
+                D.lin0 = (uint64_t)(rowlin + cc);
+            };
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int cc = ct * TC + c1 + 128 * h;
+                Dest A, B;
+                dest(cc, A);
+                dest(cc + 16, B);
+                A.valid = B.valid = row < T.rows && cc < T.cols;
+                SrDraws dr;
+                if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+                if (h == 0)
+                    emit_pair<GRID, SR, SF>(K, MA1, MA1, MB1, MB1, false, fd, A, B, dr, neg1, neg1, join);
+                else
+                    emit_pair<GRID, SR, SF>(S, MA2, MA2, MB2, MB2, false, fd, A, B, dr, neg2, neg2, join);
             }
         } else {
+    #pragma unroll
+            for (int q = 0; q < 32; ++q) {  // stride 32: the two halves of each pair
+                float a, b;
+                up2(e[q], a, b);
+                e[q] = pk2(__fadd_rn(a, b), __fsub_rn(a, b));
+            }
+            // block amax: (chunk 0, chunk 2) from pairs 0..15, (chunk 1, chunk 3) from pairs 16..31
+            float M0, M2, M1, M3;
+            amax_pair(e, 0, 16, M0, M2);
+            amax_pair(e + 16, 0, 16, M1, M3);
+            const bool b32 = TWO_D ? lb >= 5 : lbw == 5;
+            if (b32) {
+                M0 = M1 = fmaxf(M0, M1);
+                M2 = M3 = fmaxf(M2, M3);
+            }
+            if (TWO_D) {
+                if (lb == 6) M0 = M1 = M2 = M3 = fmaxf(M0, M2);
+                // the rows of this warp in the same b-row band: lanes ^ 1, 2, 4 (and
+                // ^ 16: rows + 8 with two segments a row); b >= 16 covers them all
+    #pragma unroll
+                for (int k = 1; k <= (QN == 2 ? 16 : 4); k <<= 1) {
+                    if (k == 8) continue;
+                    M0 = fmaxf(M0, __shfl_xor_sync(0xFFFFFFFFu, M0, k));
+                    M1 = fmaxf(M1, __shfl_xor_sync(0xFFFFFFFFu, M1, k));
+                    M2 = fmaxf(M2, __shfl_xor_sync(0xFFFFFFFFu, M2, k));
+                    M3 = fmaxf(M3, __shfl_xor_sync(0xFFFFFFFFu, M3, k));
+                }
+                // then across the warps of the band: slot (row block, column block)
+                uint32_t* set = amax2d + (i % 3) * kSlots;
+                const int lnbc = (QN == 2 ? 7 : 8) - lb;  // log2(TC / b)
+                const int slot0 = ((r >> lb) << lnbc) + ((64 * seg) >> lb);
+                const int cpb = (1 << lb) >> 4;  // chunks per block column
+                if ((lane & (QN == 2 ? 0x17 : 0x7)) == 0) {
+                    atomicMax(&set[slot0], __float_as_uint(M0));
+                    if (cpb == 1) atomicMax(&set[slot0 + 1], __float_as_uint(M1));
+                    if (cpb <= 2) atomicMax(&set[slot0 + (cpb == 1 ? 2 : 1)], __float_as_uint(M2));
+                    if (cpb == 1) atomicMax(&set[slot0 + 3], __float_as_uint(M3));
+                }
+                if (!__syncthreads_and(ok)) {
+                    if (tid == 0) atomicExch(&g_rows_error, 1);
+                    break;
+                }
+                M0 = __uint_as_float(set[slot0]);
+                M1 = __uint_as_float(set[slot0 + (cpb == 1 ? 1 : 0)]);
+                M2 = __uint_as_float(set[slot0 + (cpb == 1 ? 2 : (cpb == 2 ? 1 : 0))]);
+                M3 = __uint_as_float(set[slot0 + (cpb == 1 ? 3 : (cpb == 2 ? 1 : 0))]);
+                // the set of tile i + 2 (last read in tile i - 1)
+                if (tid < kSlots) amax2d[((i + 2) % 3) * kSlots + tid] = 0u;
+            }
+            uint8_t* cp = T.codes + (int64_t)row * T.codes_ld + (GRID == 4 ? col : col >> 1);
+            uint8_t* sp = T.scales + ((int64_t)row * T.scales_ld + (col >> lbw)) * SZ;
+            const int cstride = GRID == 4 ? 16 : 8;  // code bytes per 16 elements
+            const uint64_t lin0 = (uint64_t)row * (uint64_t)T.cols + (uint64_t)col;
+            Dest A, B;
+            // 2-D: one UE8M0 byte per b x b block at (row / b, column / b), written
+            // by the thread holding its top-left chunk
+            uint8_t* sp2 = T.scales + (int64_t)(row >> lb) * T.scales_ld;
+            const bool rfirst = (row & ((1 << lb) - 1)) == 0;
+            auto chunk_scale = [&](int c, uint8_t*& sptr, bool& w) {
+                const int cc = col + 16 * c;
+                if (TWO_D) {
+                    sptr = sp2 + (cc >> lb);
+                    w = rfirst && (cc & ((1 << lb) - 1)) == 0;
+                } else {
+                    sptr = sp + (cc - col) / (b32 ? 32 : 16) * SZ;
+                    w = !b32 || (c & 1) == 0;
+                }
+            };
+            // chunks 0 and 2
+            A.codes = cp;
+            B.codes = cp + 2 * cstride;
+            chunk_scale(0, A.s0, A.w0);
+            chunk_scale(2, B.s0, B.w0);
+            A.s1 = A.s0;
+            B.s1 = B.s0;
+            A.valid = B.valid = valid;
+            A.w1 = B.w1 = false;
+            A.lin0 = lin0;
+            B.lin0 = lin0 + 32;
+            {
+                SrDraws dr;
+                if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+                emit_pair<GRID, SR, SF>(e, M0, M0, M2, M2, false, fd, A, B, dr);
+            }
+            // chunks 1 and 3 (their 1 x 32 scales were written with chunks 0 and 2)
+            A.codes = cp + cstride;
+            B.codes = cp + 3 * cstride;
+            chunk_scale(1, A.s0, A.w0);
+            chunk_scale(3, B.s0, B.w0);
+            A.s1 = A.s0;
+            B.s1 = B.s0;
+            A.lin0 = lin0 + 16;
+            B.lin0 = lin0 + 48;
+            {
+                SrDraws dr;
+                if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+                emit_pair<GRID, SR, SF>(e + 16, M1, M1, M3, M3, false, fd, A, B, dr);
+            }
+        }
+        const int next = tile + kStages * gridDim.x;
+        {
             // this warp is done with stage s; thread 0 refills it once all are
             __syncwarp();
             if (lane == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empties + 8u * s) : "memory");
-            bool refill_failed = false;
-            if (tid == 0 && next < p.num_tiles) {
+            if (tid == 0 && next < p.num_tiles && !refill_failed) {
                 if (wait_phase(empties + 8u * s, phase, kWaitLimit)) {
                     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                     issue(next, s);
@@ -621,7 +725,8 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                     refill_failed = true;
                 }
             }
-            if (__shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {  // warp 0 stops with its producer
+            // 1-D: warp 0 stops with its producer; 2-D: every warp stops at the next barrier
+            if (!TWO_D && __shfl_sync(0xFFFFFFFFu, (int)refill_failed, 0)) {
                 ++i;
                 break;
             }
@@ -643,7 +748,7 @@ static cudaError_t launch_rows_seg(const RowsMaps& maps, RowsParams& p, int num_
     constexpr int kCtas = kRowsCtas;
     p.stages = kRowsStages;
     // ring, barriers, sign table, 2-D amax slots, alignment
-    const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 512 + 1024;
+    const size_t smem = (size_t)p.stages * 16384 * 2 + 64 + 1024 + 768 + 1024;
     auto k = p.n == 256 ? quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 4, false>
                         : quantize_rows_seg_kernel<GRID, SR, SF, kCtas, 2, false>;
     if constexpr (SF == 1 && GRID < 4) {

@@ -18,12 +18,15 @@ pytestmark = pytest.mark.gpu
 
 
 # row-only n = 16: the row kernel; row + column: the general kernel; row-only
-# n = 64 and n = 256: the segment kernel (per-warp waits, empty barriers)
-@pytest.mark.parametrize("mask,n", [(ufp4.OUT_ROWWISE, 16), (ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE, 16),
-                                    (ufp4.OUT_ROWWISE, 64), (ufp4.OUT_ROWWISE, 256)])
-def test_quantizer_wait_timeout_is_reported_and_recovers(mask, n):
+# n = 64 and n = 256: the segment kernel (per-warp waits, empty barriers; with
+# 32 x 32 blocks the failed waits meet the other warps at the tile's barrier)
+@pytest.mark.parametrize("mask,n,block", [(ufp4.OUT_ROWWISE, 16, (1, 16)),
+                                          (ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE, 16, (1, 16)),
+                                          (ufp4.OUT_ROWWISE, 64, (1, 16)), (ufp4.OUT_ROWWISE, 256, (1, 16)),
+                                          (ufp4.OUT_ROWWISE, 64, (32, 32)), (ufp4.OUT_ROWWISE, 256, (32, 32))])
+def test_quantizer_wait_timeout_is_reported_and_recovers(mask, n, block):
     x = inputs.tiny_check(256, 1024)
-    kw = dict(grid="e1m2", block=(1, 16), n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0)
+    kw = dict(grid="e1m2", block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0)
     xd = to_dev(x)
     torch.cuda.synchronize()
     assert ufp4.ufp4_device_error() == 0
@@ -37,7 +40,7 @@ def test_quantizer_wait_timeout_is_reported_and_recovers(mask, n):
         ufp4.ufp4_set_quantize_wait_limit(-1)
     got = gpu_quantize(xd, out_mask=mask, **kw)
     assert ufp4.ufp4_device_error_status() == ufp4.UFP4_OK
-    c, s = orc.quantize(x, grid="e1m2", block=(1, 16), n=n, sign_seed=inputs.SIGN_SEED,
+    c, s = orc.quantize(x, grid="e1m2", block=block, n=n, sign_seed=inputs.SIGN_SEED,
                         scale_fmt=orc.SCALE_UE8M0)
     assert_bitwise(got["row"][0], c, "row-wise codes after the timeout")
     assert_bitwise(got["row"][1], s, "row-wise scales after the timeout")
