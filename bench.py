@@ -6,14 +6,20 @@ workload (the largest single-GPU configuration): fused RHT + E1M2 4-bit
 quantization (n = 16, 1 x 16 blocks, UE8M0 scales, RTNE) of X (16384 x 7168
 bf16) and W (7168 x 7168 bf16), both N(0,1) with 0.1 % element outliers x50,
 then the quantized GEMM Y = Q(X H') Q(W H')^T (16384 x 7168 x 7168, fp32 out).
+The quantizer launch (ufp4_rht_quantize_prepare) also writes the GEMM's
+operands (E5M2 copies of the levels and the hardware scales in the
+tensor-memory copy layout), so the step is two launches: that one and the
+tensor-core GEMM (ufp4_gemm_prepared).
 
 value  = fused quantizer throughput in GB/s of algorithmic bytes (bf16 read
-         + packed codes + scales written), from CUDA events around the
-         quantizer launch inside the timed steps.
-gemm   = quantized GEMM TFLOP/s (2 M N K per step, operand prep included).
+         + packed codes + scales + the E5M2 operand + its scale cells
+         written), from CUDA events around the quantizer launch inside the
+         timed steps.
+gemm   = quantized GEMM TFLOP/s (2 M N K per step; the tensor-core kernel,
+         its operands prepared by the quantizer launch).
 e2e    = the same quantizer metric through the C ABI with host buffers:
-         pinned H2D of X and W, quantize, GEMM and D2H of the codes, scales
-         and Y inside the timed region.
+         pinned H2D of X and W, quantize + prepare, GEMM and D2H of the
+         codes, scales and Y inside the timed region.
 Inputs rotate over 2 copies (each copy 322 MiB > 2 x L2), so every step reads
 cold data.
 
@@ -42,10 +48,14 @@ import numpy as np  # noqa: E402
 METRIC = "fused RHT+4-bit quantize GB/s (% of HBM peak); quantized GEMM TFLOP/s (% peak)"
 M, N, K = 16384, 7168, 7168
 BLOCK = 16
-# algorithmic bytes per element: 2 (bf16 in) + 0.5 (codes) + 1/16 (UE8M0 scale)
+# algorithmic bytes per element of the row-wise quantization alone: 2 (bf16
+# in) + 0.5 (codes) + 1/16 (UE8M0 scale)
 BYTES_PER_ELEM = 2.0 + 0.5 + 1.0 / BLOCK
+# of the fused quantize + prepare launch: also 1 (E5M2 operand) + 4/32 (one
+# hardware-scale cell per 32 elements, stored four times)
+BYTES_PER_ELEM_PREP = BYTES_PER_ELEM + 1.0 + 4.0 / 32
 QUANT_ELEMS = (M + N) * K
-QUANT_BYTES = QUANT_ELEMS * BYTES_PER_ELEM
+QUANT_BYTES = QUANT_ELEMS * BYTES_PER_ELEM_PREP
 GEMM_FLOPS = 2.0 * M * N * K
 ROTATE = 2
 WORKLOAD = ("MoE-124B-like FPROP operands: X 16384x7168, W 7168x7168 bf16 (N(0,1), 0.1% element outliers x50); "
@@ -53,9 +63,9 @@ WORKLOAD = ("MoE-124B-like FPROP operands: X 16384x7168, W 7168x7168 bf16 (N(0,1
 L2_NOTE = "inputs rotate over 2 copies (each 322 MiB > 2x L2); the 470 MB fp32 Y is written every step"
 
 
-# library kernel launches per step: quantize X and W (one batched launch),
-# operand prep (both operands in one launch), tensor-core GEMM
-LAUNCHES_PER_STEP = 3
+# library kernel launches per step: quantize and prepare X and W (one
+# launch), tensor-core GEMM
+LAUNCHES_PER_STEP = 2
 
 
 def sources_hash(files) -> str:
@@ -184,7 +194,10 @@ def oracle_sample(rows_x: int, rows_w: int):
 
 def cpu_oracle_rate(sample, min_seconds: float, max_reps: int):
     """Oracle (single-threaded C) on a bounded row sample of X and W; returns
-    (GB/s of algorithmic bytes, elements, seconds, reps)."""
+    (GB/s, elements, seconds, reps).  The GB/s count the GPU arm's bytes per
+    element (BYTES_PER_ELEM_PREP), so that both arms' values are elements per
+    second times the same constant; the oracle itself computes the row-wise
+    quantization only."""
     import oracle as orc
     xs, ws, kw = sample
     elems = 0
@@ -198,7 +211,7 @@ def cpu_oracle_rate(sample, min_seconds: float, max_reps: int):
         if time.perf_counter() - t0 >= min_seconds:
             break
     dt = time.perf_counter() - t0
-    return elems * BYTES_PER_ELEM / dt / 1e9, elems, dt, reps
+    return elems * BYTES_PER_ELEM_PREP / dt / 1e9, elems, dt, reps
 
 
 def run_reference(args):
@@ -215,8 +228,9 @@ def run_reference(args):
         _, e, _, _ = cpu_oracle_rate(sample, 0.0, 1)
         elems += e
     dt = time.perf_counter() - t0
-    value = elems * BYTES_PER_ELEM / dt / 1e9
-    sample_desc = f"each step: the first {rows} rows of X and of W ({2 * rows * K} elements), oracle quantizer only"
+    value = elems * BYTES_PER_ELEM_PREP / dt / 1e9
+    sample_desc = (f"each step: the first {rows} rows of X and of W ({2 * rows * K} elements), oracle quantizer only; "
+                   f"GB/s = elements x {BYTES_PER_ELEM_PREP} B, the GPU arm's bytes per element")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
@@ -264,20 +278,17 @@ def run_gpu(args):
     ev = lambda: torch.cuda.Event(enable_timing=True)
     n_ev = args.steps
     e_q0, e_q1 = [ev() for _ in range(n_ev)], [ev() for _ in range(n_ev)]
-    e_p1, e_g1 = [ev() for _ in range(n_ev)], [ev() for _ in range(n_ev)]
+    e_g1 = [ev() for _ in range(n_ev)]
 
     def step(i, timed):
         xi, wi = xs[i % ROTATE], wsrc[i % ROTATE]
         if timed:
             e_q0[i].record(stream)
-        # X and W share the descriptor: one launch quantizes both
-        ufp4.ufp4_rht_quantize_batch([xi, wi], desc, [tx, tw], stream.cuda_stream)
+        # X and W share the descriptor: one launch quantizes both and writes
+        # the GEMM's prepared operands into the workspace
+        ufp4.ufp4_rht_quantize_prepare(xi, wi, desc, tx, tw, wsb, stream.cuda_stream)
         if timed:
             e_q1[i].record(stream)
-        # ufp4_gemm in its two stages, so that the tensor-core kernel is timed alone
-        ufp4.ufp4_gemm_prepare(tx, tw, desc, wsb, stream.cuda_stream)
-        if timed:
-            e_p1[i].record(stream)
         ufp4.ufp4_gemm_prepared(tx, tw, desc, D, wsb, stream.cuda_stream)
         if timed:
             e_g1[i].record(stream)
@@ -301,8 +312,8 @@ def run_gpu(args):
     clocks = sampler.stop()
     assert ufp4.ufp4_device_error() == 0, "a bounded device wait gave up"
     q_ms = [e_q0[i].elapsed_time(e_q1[i]) for i in range(args.steps)]
-    g_ms = [e_q1[i].elapsed_time(e_g1[i]) for i in range(args.steps)]  # operand prep + tensor-core kernel
-    k_ms = [e_p1[i].elapsed_time(e_g1[i]) for i in range(args.steps)]  # tensor-core kernel alone
+    g_ms = [e_q1[i].elapsed_time(e_g1[i]) for i in range(args.steps)]  # the tensor-core kernel
+    k_ms = g_ms
     total_ms = start_all.elapsed_time(end_all)
     q_s = sum(q_ms) / 1e3
     g_s = sum(g_ms) / 1e3
@@ -316,8 +327,8 @@ def run_gpu(args):
 
     # ------------------------------------------------------- e2e (host buffers)
     # Every step copies X and W in from pinned host memory, runs
-    # ufp4_rht_quantize_batch and ufp4_gemm, and copies the codes, scales and
-    # Y out.  Steps are pipelined over three streams with two sets of device
+    # ufp4_rht_quantize_prepare and ufp4_gemm_prepared, and copies the codes,
+    # scales and Y out.  Steps are pipelined over three streams with two sets of device
     # and host buffers: the copy-in of step i + 1 and the copy-out of step i - 1
     # run while step i computes, so the two directions of the host link
     # overlap.  The timed region spans the first copy-in to the last copy-out.
@@ -353,8 +364,8 @@ def run_gpu(args):
             stream.wait_event(e_in[k])
             if i >= 2:
                 stream.wait_event(e_out[k])
-            ufp4.ufp4_rht_quantize_batch([xin[k], win[k]], desc, [txs[k], tws[k]], stream.cuda_stream)
-            ufp4.ufp4_gemm(txs[k], tws[k], desc, Ds[k], wss[k], stream.cuda_stream)
+            ufp4.ufp4_rht_quantize_prepare(xin[k], win[k], desc, txs[k], tws[k], wss[k], stream.cuda_stream)
+            ufp4.ufp4_gemm_prepared(txs[k], tws[k], desc, Ds[k], wss[k], stream.cuda_stream)
             e_comp[k].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(e_comp[k])
@@ -380,11 +391,13 @@ def run_gpu(args):
     fp8_peak = 2.0 * pk["bf16"]  # dense FP8 = 2 x bf16 (nominal ratio)
     gemm_frac = gemm_tflops / fp8_peak
     rl_q = {"bound": "hbm", "achieved": q_gbs, "peak": pk["hbm"], "unit": "GB/s", "frac": q_gbs / pk["hbm"],
-            "traffic": recorded_traffic("quantize_rows_kernel<E1M2,RTNE,UE8M0>"),
-            "kernel": "quantize_rows_kernel<E1M2,RTNE,UE8M0> (X and W in one launch)", "peak_src": pk["src"] + " hbm_gbs (burst)"}
+            "traffic": recorded_traffic("quantize_rows_kernel<E1M2,RTNE,UE8M0,PREP>"),
+            "kernel": "quantize_rows_kernel<E1M2,RTNE,UE8M0,PREP> (X and W in one launch, with their prepared "
+                      "GEMM operands)", "bytes_per_elem": BYTES_PER_ELEM_PREP,
+            "peak_src": pk["src"] + " hbm_gbs (burst)"}
     rl_g = {"bound": "tensor", "achieved": kernel_tflops, "peak": fp8_peak, "unit": "TFLOP/s",
             "frac": kernel_tflops / fp8_peak, "traffic": recorded_traffic("gemm_pair_kernel<FP8>"),
-            "kernel": "gemm_pair_kernel<FP8> (CTA-pair tensor-core kernel; operand prep timed apart)",
+            "kernel": "gemm_pair_kernel<FP8> (CTA-pair tensor-core kernel)",
             "peak_src": pk["src"] + " bf16_tflops (burst) x2, the FP8/bf16 nominal ratio"}
     dominant = rl_g if statistics.mean(k_ms) >= statistics.mean(q_ms) else rl_q
 
@@ -392,7 +405,8 @@ def run_gpu(args):
     if rank == 0 and not args.no_cpu_baseline:
         rate, elems, dt, reps = cpu_oracle_rate(oracle_sample(1024, 1024), args.cpu_seconds, 64)
         cpu = {"value": rate, "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first 1024 rows of X and of W ({2 * 1024 * K} elements) per rep, {reps} reps, {dt:.1f} s"}
+               "sample": f"first 1024 rows of X and of W ({2 * 1024 * K} elements) per rep, {reps} reps, {dt:.1f} s; "
+                         f"row-wise quantization only, GB/s = elements x {BYTES_PER_ELEM_PREP} B as for value"}
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
@@ -402,8 +416,8 @@ def run_gpu(args):
                        "parallelism": f"replicas x{world}"},
             "quant_frac_of_hbm": value / pk["hbm"],
             "gemm": {"value": gemm_tflops, "unit": "TFLOP/s", "frac": gemm_frac, "peak": fp8_peak,
-                     "includes": "FP8 operand prep + tensor-core kernel",
-                     "kernel_only": kernel_tflops, "prep_ms": (sum(g_ms) - sum(k_ms)) / args.steps},
+                     "includes": "the tensor-core kernel; its FP8 operands are written by the quantizer launch "
+                                 "(no separate prep pass)"},
             "roofline": dominant, "roofline_quantize": rl_q, "roofline_gemm": rl_g,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_units / e2e_s / 1e9, "unit": "GB/s", "h2d_bytes_per_step": h2d,
@@ -475,6 +489,12 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
         emit("dense_step", f"Dense-1.5B-like FPROP operands X {m2}x{k2} + W {n2}x{k2}, e1m2 1x16 UE8M0 n=16 RTNE, "
              "one batched launch", qb / (qms / 1e3) / 1e9, "GB/s", qb / (qms / 1e3) / 1e9 / pk["hbm"], pk["hbm"],
              ms=qms)
+        fms = timed(lambda i: ufp4.ufp4_rht_quantize_prepare(xs2[i % 5], ws2[i % 5], desc, tx2, tw2, wsb2,
+                                                             stream.cuda_stream))
+        fb = (m2 + n2) * k2 * BYTES_PER_ELEM_PREP
+        emit("dense_step", f"Dense-1.5B-like FPROP operands, quantized and prepared for the GEMM in one launch "
+             "(ufp4_rht_quantize_prepare; replaces the batched launch + the prep pass)", fb / (fms / 1e3) / 1e9, "GB/s",
+             fb / (fms / 1e3) / 1e9 / pk["hbm"], pk["hbm"], ms=fms, unfused_ms=qms + pms)
         tf = 2.0 * m2 * n2 * k2 / (kms / 1e3) / 1e12
         emit("dense_step", f"Dense-1.5B-like FPROP GEMM {m2}x{n2}x{k2} e1m2 1x16 UE8M0 (tensor-core kernel; "
              "prep timed apart)", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"], kernel_ms=kms, prep_ms=pms)

@@ -317,6 +317,27 @@ ufp4_status ufp4_gemm_prepare(const ufp4_qtensor* A, const ufp4_qtensor* B, cons
 ufp4_status ufp4_gemm_prepared(const ufp4_qtensor* A, const ufp4_qtensor* B, const ufp4_quant_desc* desc, float* D,
                                int64_t ldd, void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
+/* ufp4_rht_quantize_prepare -- the two operands of one FPROP-style GEMM
+ * quantized and prepared in one launch: ufp4_rht_quantize_batch of a (the
+ * A operand, A->rows x A->cols) and b (B->rows x B->cols) fused with
+ * ufp4_gemm_prepare(A, B, desc, workspace) [UFP4-method: both operands of the
+ * quantized GEMM Y^ = Q_G(XH') Q_G(WH')^T are quantized along K, and E1M2 /
+ * INT4 levels widen exactly into FP8 for the tensor cores].  A and B receive
+ * exactly what ufp4_rht_quantize_batch writes, and the workspace exactly what
+ * ufp4_gemm_prepare writes, so ufp4_gemm_prepared(A, B, desc, D, ...) follows
+ * directly, with no separate prep pass over the codes.
+ *   a, b     device bf16, leading dimensions lda, ldb elements (the rules of
+ *            ufp4_rht_quantize)
+ *   A, B     their row-wise outputs; A->cols == B->cols == K
+ *   workspace, workspace_bytes  as for ufp4_gemm_prepare
+ * Requirements: desc->out_mask == UFP4_OUT_ROWWISE, grid E1M2 or INT4,
+ * UFP4_SCALE_UE8M0, 1 x 16 or 1 x 32 blocks and hadamard_n == 16
+ * (UFP4_ERR_UNSUPPORTED otherwise), and the rules of ufp4_rht_quantize_batch
+ * and ufp4_gemm_prepare.  Nothing is written when any argument is rejected. */
+ufp4_status ufp4_rht_quantize_prepare(const void* a, int64_t lda, const void* b, int64_t ldb,
+                                      const ufp4_quant_desc* desc, const ufp4_qtensor* A, const ufp4_qtensor* B,
+                                      void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /* ufp4_gemm_grouped_workspace_size -- scratch bytes ufp4_gemm_grouped needs:
  * the sum over the groups of ufp4_gemm_workspace_size, each rounded up to 256
  * bytes (0 for a group with an empty product); A, B: HOST arrays of

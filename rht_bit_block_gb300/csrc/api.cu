@@ -149,9 +149,12 @@ ufp4_status cuda_status(cudaError_t e) { return e == cudaSuccess ? UFP4_OK : UFP
 // Shared body of the plain and grouped quantizer calls.
 // Row-wise quantization of `count` tensors in one launch of the lean kernel
 // (arguments already validated).
+// prep (optional, one per tensor): also write each tensor's prepared GEMM
+// operand there; its tiles then run over the rows of whole GEMM tiles.
 ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* rows, const int64_t* cols,
                                 const int64_t* ld, const ufp4_quant_desc* desc, const BlockShape& bs,
-                                const ufp4_qtensor* rowwise, cudaStream_t stream) {
+                                const ufp4_qtensor* rowwise, cudaStream_t stream,
+                                const PrepTarget* prep = nullptr) {
     RowsParams p;
     std::memset(&p, 0, sizeof(p));
     auto ilog2 = [](int v) { int l = 0; while ((1 << l) < v) ++l; return l; };
@@ -175,6 +178,10 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
         T.cols = (int)cols[i];
         T.col_tiles = (int)((cols[i] + tc - 1) / tc);
         T.row_tiles = (int)((rows[i] + tr - 1) / tr);
+        if (prep) {
+            T.prep = prep[i];
+            T.row_tiles = (int)((std::max<int64_t>(rows[i], prep[i].rows_cover) + tr - 1) / tr);
+        }
         T.tile0 = (int)tiles;
         T.amax = rowwise[i].tensor_amax;
         tiles += (int64_t)T.col_tiles * T.row_tiles;
@@ -200,6 +207,7 @@ ufp4_status quantize_rows_batch(int count, const void* const* x, const int64_t* 
     p.sr_seed = desc->round == UFP4_ROUND_SR ? desc->sr_seed : 0;
     p.sr_keys = sr_round_keys(p.sr_seed);
     p.group = desc->group;
+    p.prep = prep ? 1 : 0;
     if (desc->scale_fmt == UFP4_SCALE_E4M3)  // two-level: the tensor amax pre-pass first
         for (int i = 0; i < k; ++i) {
             const RowsTensor& T = p.t[i];
@@ -455,6 +463,42 @@ extern "C" ufp4_status ufp4_rht_quantize_batch(int32_t count, const void* const*
         if (st != UFP4_OK) return st;
     }
     return quantize_rows_batch(count, x, rows, cols, ld, desc, bs, rowwise, stream);
+}
+
+extern "C" ufp4_status ufp4_rht_quantize_prepare(const void* a, int64_t lda, const void* b, int64_t ldb,
+                                                 const ufp4_quant_desc* desc, const ufp4_qtensor* A,
+                                                 const ufp4_qtensor* B, void* workspace, size_t workspace_bytes,
+                                                 cudaStream_t stream) {
+    BlockShape bs;
+    ufp4_status st = check_desc(desc, &bs);
+    if (st != UFP4_OK) return st;
+    if (!A || !B) return UFP4_ERR_INVALID_ARG;
+    if (desc->out_mask != UFP4_OUT_ROWWISE) return UFP4_ERR_INVALID_ARG;
+    if ((desc->grid != UFP4_GRID_E1M2 && desc->grid != UFP4_GRID_INT4) || desc->scale_fmt != UFP4_SCALE_UE8M0 ||
+        bs.is2d || desc->hadamard_n != 16)
+        return UFP4_ERR_UNSUPPORTED;
+    // the GEMM's rules (shapes, alignment, workspace); D is not touched here
+    GemmArgs g;
+    float dummy_d[4] __attribute__((aligned(16)));
+    st = prepare_gemm(A, B, desc, dummy_d, B->rows, workspace, workspace_bytes, &g);
+    if (st != UFP4_OK) return st;
+    // the quantizer's rules, as ufp4_rht_quantize_batch checks them
+    const void* const xs[2] = {a, b};
+    const int64_t rows[2] = {A->rows, B->rows}, cols[2] = {A->cols, B->cols}, lds[2] = {lda, ldb};
+    const ufp4_qtensor outs[2] = {*A, *B};
+    for (int i = 0; i < 2; ++i) {
+        if (rows[i] == 0 || cols[i] == 0) continue;
+        if (lds[i] < cols[i] || !xs[i]) return UFP4_ERR_INVALID_ARG;
+        if (!aligned(xs[i], 16) || lds[i] % 8) return UFP4_ERR_ALIGNMENT;
+        if (cols[i] % 16 || cols[i] % bs.bw) return UFP4_ERR_INVALID_ARG;
+    }
+    if (g.M == 0 || g.N == 0 || g.K == 0)  // no GEMM operand to prepare
+        return quantize_rows_batch(2, xs, rows, cols, lds, desc, bs, outs, stream);
+    PrepTarget targets[2];
+    const cudaError_t e = gemm_prep_targets(g, targets);
+    if (e == cudaErrorNotSupported) return UFP4_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return UFP4_ERR_INVALID_ARG;
+    return quantize_rows_batch(2, xs, rows, cols, lds, desc, bs, outs, stream, targets);
 }
 
 int64_t ufp4_grouped_padded_rows(int64_t rows, const ufp4_quant_desc* desc) {

@@ -39,6 +39,7 @@
 
 #include "../../include/ufp4.h"
 #include "internal.h"
+#include "widen_e5m2.cuh"
 
 namespace ufp4 {
 
@@ -873,18 +874,6 @@ gemm_f32s_kernel(const __grid_constant__ CUtensorMap tmap_a, const __grid_consta
 }
 
 // ------------------------------------------------------------- prep kernels
-__device__ __forceinline__ uint32_t cvt_e5m2x2(float hi, float lo) {
-    uint16_t r;
-    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-
-__device__ __forceinline__ float pow2f(int e) {  // 2^e for e in [-149, 127]
-    if (e >= -126) return __uint_as_float((uint32_t)(e + 127) << 23);
-    if (e < -149) return 0.0f;
-    return __uint_as_float(1u << (e + 149));
-}
 
 // One operand of the prep launch.
 struct PrepSide {
@@ -917,33 +906,6 @@ struct PrepParams {
 // ((((t * chunks_k + g) * parts + h) * 4 + copy) * 512, with row w of the part
 // and scale cell byte j at (w % 32) * 16 + (w / 32) * 4 + j in each copy
 // (the tcgen05.cp 32x128b chunk layout).
-
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t r;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-    return r;
-}
-
-// Eight sign-magnitude codes (one 32-bit word) -> eight E5M2 bytes of
-// k * 2^-d, d <= 14 (two words).  lo and hi hold the E5M2 bytes of 0, 1, ..., 7
-// with d already subtracted from the exponent field of the nonzero ones
-// (e5m2_tables); the magnitudes select from them and the sign bits select
-// 0x80 or 0 (byte permutes).  Exact: every k * 2^-d with |k| <= 7, d <= 14 is
-// an E5M2 normal number.
-__device__ __forceinline__ void e5m2x8(uint32_t w, uint32_t lo, uint32_t hi, uint32_t& o0, uint32_t& o1) {
-    const uint32_t mw = w & 0x77777777u;
-    const uint32_t sw = (w >> 3) & 0x11111111u;  // each nibble: its sign bit
-    o0 = prmt(lo, hi, mw) | prmt(0x00008000u, 0u, sw);
-    o1 = prmt(lo, hi, mw >> 16) | prmt(0x00008000u, 0u, sw >> 16);
-}
-
-// E5M2 bytes of 0, 1.0, 2.0, 3.0 (lo) and 4.0 .. 7.0 (hi), each nonzero one
-// scaled by 2^-d (d <= 14: every byte stays >= 4 d, so no borrow crosses bytes).
-__device__ __forceinline__ void e5m2_tables(int d, uint32_t& lo, uint32_t& hi) {
-    const uint32_t sub = (uint32_t)d * 0x04040404u;
-    lo = 0x42403C00u - (sub & 0xFFFFFF00u);
-    hi = 0x47464544u - sub;
-}
 
 // Widen E1M2 / INT4 codes into FP8 E5M2 with one UE8M0 hardware scale per 32
 // elements (replicated chunk layout above).  A CTA is 32 x 8 threads and
@@ -1006,41 +968,13 @@ __global__ void __launch_bounds__(256) prep_widen_kernel(const PrepParams p) {
         if (!ok[q]) continue;
         const int d0 = hw[q] - step_log2 - e0[q], d1 = hw[q] - step_log2 - e1[q];  // >= 0
         uint32_t words[4] = {cw[q].x, cw[q].y, cw[q].z, cw[q].w};
-        if (p.grid == 1) {
+        if (p.grid == 1)
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {  // two's complement -> sign-magnitude (no -8 code occurs)
-                const uint32_t v = words[k];
-                const uint32_t neg = (v >> 3) & 0x11111111u;
-                const uint32_t mag = ((v ^ (neg * 15u)) + neg) & 0x77777777u;
-                words[k] = mag | (neg << 3);
-            }
-        }
-        uint32_t outw[8];
-        if (d0 <= 14 && d1 <= 14) {
-            uint32_t lo0, hi0, lo1, hi1;
-            e5m2_tables(d0, lo0, hi0);
-            e5m2_tables(d1, lo1, hi1);
-            e5m2x8(words[0], lo0, hi0, outw[0], outw[1]);  // elements 0-15: the first 16-element block
-            e5m2x8(words[1], lo0, hi0, outw[2], outw[3]);
-            e5m2x8(words[2], lo1, hi1, outw[4], outw[5]);
-            e5m2x8(words[3], lo1, hi1, outw[6], outw[7]);
-        } else {
-            // shifts beyond E5M2's normal range: exact float path, rounding to
-            // nearest only below E5M2's smallest subnormal
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float mult = pow2f(-(k < 4 ? d0 : d1));
-                const uint32_t v = (words[k >> 1] >> (16 * (k & 1))) & 0xFFFFu;
-                float f[4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t nib = (v >> (4 * u)) & 0xFu;
-                    const float m = (float)(int)(nib & 7u);
-                    f[u] = ((nib & 8u) ? -m : m) * mult;
-                }
-                outw[k] = cvt_e5m2x2(f[1], f[0]) | (cvt_e5m2x2(f[3], f[2]) << 16);
-            }
-        }
+            for (int k = 0; k < 4; ++k) words[k] = twos_to_signmag8(words[k]);
+        // elements 0-15: the first 16-element block, 16-31: the second
+        const uint4 lo16 = widen16_e5m2(words[0], words[1], d0);
+        const uint4 hi16 = widen16_e5m2(words[2], words[3], d1);
+        const uint32_t outw[8] = {lo16.x, lo16.y, lo16.z, lo16.w, hi16.x, hi16.y, hi16.z, hi16.w};
         uint4* dst = reinterpret_cast<uint4*>(s.out_fp8 + (int64_t)row * s.K + (g0 + q) * 32);
         dst[0] = make_uint4(outw[0], outw[1], outw[2], outw[3]);
         dst[1] = make_uint4(outw[4], outw[5], outw[6], outw[7]);
@@ -1330,6 +1264,29 @@ cudaError_t pair_plan(const GemmArgs& g, Plan& pl) {
     if (g.K % 64 && fp4) return cudaErrorNotSupported;  // FP4 rows must be 32-byte multiples
     pl = make_plan(g.M, g.N, g.K, g.grid, g.br, g.bc, g.sf);
     if (g.workspace_bytes < pl.total) return cudaErrorInvalidValue;
+    return cudaSuccess;
+}
+
+cudaError_t gemm_prep_targets(const GemmArgs& g, PrepTarget out[2]) {
+    Plan pl{};
+    const cudaError_t e = pair_plan(g, pl);
+    if (e != cudaSuccess) return e;
+    if (pl.kind != 0 || pl.native) return cudaErrorNotSupported;
+    // the quantizer zeroes the cells past a tile's short last part from that
+    // part's first rows, so that part must hold at least half of its 128
+    if (pl.bn % 128 != 0 && pl.bn % 128 < 64) return cudaErrorNotSupported;
+    uint8_t* ws = (uint8_t*)g.workspace;
+    for (int side = 0; side < 2; ++side) {
+        PrepTarget& t = out[side];
+        const int64_t rows = side ? g.N : g.M;
+        t.fp8 = ws + (side ? pl.fp8_b : pl.fp8_a);
+        t.chunks = ws + (side ? pl.sfb : pl.sfa);
+        t.K = g.K;
+        t.tile_rows = side ? pl.bn : kBM;
+        t.parts = (t.tile_rows + 127) / 128;
+        t.chunks_k = (int)pl.chunks_k;
+        t.rows_cover = (int)((rows + t.tile_rows - 1) / t.tile_rows) * t.tile_rows;
+    }
     return cudaSuccess;
 }
 

@@ -89,6 +89,20 @@ struct QuantParams {
 cudaError_t launch_quantize(const QuantParams& p, int grid, bool sr, bool po2, int tc, int tr, int num_tiles,
                             int64_t total_rows, int num_sms, cudaStream_t st);
 
+// The prepared form of one FP8-path GEMM operand (E1M2 / INT4, UE8M0, 1-D
+// blocks) in the GEMM workspace: E5M2 copies of the levels with one hardware
+// scale per 32 elements, and those scales in the replicated chunk layout of
+// the CTA-pair kernel (widen_e5m2.cuh).
+struct PrepTarget {
+    uint8_t* fp8;     // rows x K bytes, row pitch K
+    uint8_t* chunks;  // replicated scale chunks
+    int64_t K;
+    int tile_rows;    // rows of one GEMM tile of the operand (128 for A, the tile width for B)
+    int parts;        // 128-row parts of a GEMM tile
+    int chunks_k;     // chunks along K per 128 rows
+    int rows_cover;   // rows with scale cells: rows rounded up to whole GEMM tiles
+};
+
 // Row-wise only, 1-D blocks (or b x b blocks, b = 16, 32, 64), n <= 256: the lean kernel, over up to
 // kMaxBatch independent tensors in one launch.
 constexpr int kMaxBatch = 4;
@@ -103,6 +117,7 @@ struct RowsTensor {
     int col_tiles, row_tiles;
     int tile0;          // first tile of this tensor in the launch
     const float* amax;  // two-level scale: the tensor amax T (device)
+    PrepTarget prep;    // with RowsParams::prep: where the prepared GEMM operand goes
 };
 struct RowsParams {
     RowsTensor t[kMaxBatch];
@@ -116,6 +131,7 @@ struct RowsParams {
     uint64_t sr_seed;
     SrKeys sr_keys;
     int group;
+    int prep;           // also write each tensor's prepared GEMM operand (n = 16, E1M2 / INT4, UE8M0, 1-D)
 };
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st);
 // Two-level scale pre-pass: *amax = max |RHT(x)| over the tensor (zeroed first).
@@ -199,6 +215,9 @@ struct GemmArgs {
     size_t workspace_bytes;
 };
 size_t gemm_workspace_bytes(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf);
+// The workspace targets of A (out[0]) and B (out[1]) for ufp4_gemm_prepared;
+// cudaErrorNotSupported unless the GEMM takes the widened FP8 path.
+cudaError_t gemm_prep_targets(const GemmArgs& g, PrepTarget out[2]);
 cudaError_t launch_gemm(const GemmArgs& g, int num_sms, cudaStream_t st);
 cudaError_t launch_gemm_prep(const GemmArgs& g, cudaStream_t st);
 cudaError_t launch_gemm_main(const GemmArgs& g, int num_sms, cudaStream_t st);

@@ -120,7 +120,8 @@ __device__ __forceinline__ uint64_t sub2_rm(uint64_t a, uint64_t b) {
 // is formed first, as in the definition.
 // SF: 0 fp32 scale, 1 UE8M0, 2 two-level (E4M3 block byte x tensor scale g).
 template <int GRID, int SF>
-__device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, bool write, uint8_t* sptr) {
+__device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, bool write, uint8_t* sptr,
+                                             int* byte_out = nullptr) {
     constexpr float qmax = grid_qmax(GRID);
     const float Mz = __fmul_rn(My, fd.inv_s);
     const int lj = fd.pow4 ? -fd.j : 0;
@@ -135,6 +136,7 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
     } else if (SF == 1) {
         const int eb = po2_byte<GRID>(Mz);  // e + 127
         if (write) *sptr = (uint8_t)eb;
+        if (byte_out) *byte_out = eb;
         // 2^(-e + lf + lj) from its biased exponent: a normal number for every
         // block inside the input contract (|lf + lj| <= 6, eb <= 248)
         return __uint_as_float((uint32_t)(254 + lf + lj - eb) << 23);
@@ -194,23 +196,32 @@ __device__ __forceinline__ void draw_pair(SrDraws& d, const SrKeys& keys, const 
     sr_draws16x2(keys, A.lin0, B.lin0, stream, group, d.a, d.b);
 }
 
+// What one emit_pair call stored, for callers that derive more from it:
+// the packed code words of A and B and (UE8M0 scales) their scale bytes.
+struct EmitOut {
+    uint2 ca, cb;
+    int sa, sb;
+};
+
 // nega / negb: the sign bit (0 or 0x80000000) of a vector held negated; its
 // reciprocal then carries that sign, so that t = y r is the value of the
 // unnegated vector (exact: IEEE products are sign-symmetric).  join: B's codes
 // follow A's (A.codes + 8, 16-byte aligned, A.valid == B.valid), stored as one
-// 16-byte word.
+// 16-byte word.  out: if given, receives the codes and scale bytes (1-D
+// blocks of 16 or 32, split false).
 template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B, const SrDraws& dr,
-                                          uint32_t nega = 0u, uint32_t negb = 0u, bool join = false) {
+                                          uint32_t nega = 0u, uint32_t negb = 0u, bool join = false,
+                                          EmitOut* out = nullptr) {
     // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
     // to the value in units of the grid step (below): INT4 k, E1M2 4 t
     constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
     constexpr int lf = GRID == 4 ? 0
                      : kMagic    ? (GRID == 0 ? 2 : 0)
                                  : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
-    const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0);
-    const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0);
+    const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0, out ? &out->sa : nullptr);
+    const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0, out ? &out->sb : nullptr);
     float ra1 = ra0, rb1 = rb0;
     if (split) {
         ra1 = block_recip<GRID, SF>(MA1, fd, lf, A.valid && A.w1, A.s1);
@@ -219,6 +230,10 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
     const float sa0 = __uint_as_float(__float_as_uint(ra0) ^ nega), sa1 = __uint_as_float(__float_as_uint(ra1) ^ nega);
     const float sb0 = __uint_as_float(__float_as_uint(rb0) ^ negb), sb1 = __uint_as_float(__float_as_uint(rb1) ^ negb);
     auto store_pair = [&](uint2 ca, uint2 cb) {
+        if (out) {
+            out->ca = ca;
+            out->cb = cb;
+        }
         if (join) {
             if (A.valid) *reinterpret_cast<uint4*>(A.codes) = make_uint4(ca.x, ca.y, cb.x, cb.y);
         } else {

@@ -15,6 +15,7 @@
 #include "internal.h"
 #include "quantize_common.cuh"
 #include "ufp4_device.cuh"
+#include "widen_e5m2.cuh"
 
 namespace ufp4 {
 
@@ -48,9 +49,20 @@ struct RowsMaps {
 // the block, then across warps with a shared-memory atomicMax, while the
 // transformed values wait in registers.  The amax slots come in two sets
 // used by alternate tiles, so a set is cleared during the tile before its use.
-template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
+//
+// PREP (E1M2 / INT4, UE8M0, 1-D blocks, n = 16): each tensor is also written
+// in the prepared form ufp4_gemm_prepared reads (widen_e5m2.cuh): every chunk
+// of 16 codes as 16 E5M2 bytes, shifted by its block's distance d to the
+// hardware scale of its 32-element group (the other block of the group is in
+// lane ^ 1), and the hardware scales as cells of the replicated chunk array.
+// A tile's 128 columns are one chunk along K, so lane 0 of each row gathers
+// its four cells (lanes 0, 2, 4, 6) into one word per copy.  The launch runs
+// over the tensor's rows rounded up to whole GEMM tiles (rows_cover): the
+// rows past the tensor read zeros and get zero cells.
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D, bool PREP = false>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
+    static_assert(!PREP || (GRID <= 1 && SF == 1 && N16 && TC == 128 && !TWO_D), "prepared FP8 operands");
     constexpr int kCPR = TC / kChunk;      // 16-element chunks per tile row
     constexpr int kRPI = kThreads / kCPR;  // tile rows per thread step
     constexpr int TR = TWO_D ? 2 * kRPI : 16384 / TC;
@@ -165,6 +177,8 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
         const uint16_t* tile_s = reinterpret_cast<const uint16_t*>(base + s * kTileBytes);
         const int row0 = rt * TR;
         const int col = ct * TC + cchunk * kChunk;
+        // PREP: the GEMM tile holding the quantizer tile's first row, and its first row
+        const int ptile = PREP ? row0 / T.prep.tile_rows : 0, prow0 = PREP ? ptile * T.prep.tile_rows : 0;
         const bool col_ok = col < T.cols;
         const int left = T.rows - row0 - r0;  // rows of this thread's first row onward
         const bool full = T.rows - row0 >= TR;
@@ -259,7 +273,60 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
                 fwht_pair(e, n, seg_row);
                 amax_1d_pair(e, 1 << lbw, Ma, Mb);
             }
-            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, dr);
+            EmitOut eo;
+            emit_pair<GRID, SR, SF>(e, Ma, Ma, Mb, Mb, false, fd, A, B, dr, 0u, 0u, false, PREP ? &eo : nullptr);
+            if constexpr (PREP) {
+                const PrepTarget& P = T.prep;
+                constexpr int kStep = GRID == 0 ? -2 : 0;  // log2 of the level step in scale units: E1M2 k/4, INT4 k
+                const int pa = __shfl_xor_sync(0xFFFFFFFFu, eo.sa, 1), pb = __shfl_xor_sync(0xFFFFFFFFu, eo.sb, 1);
+                const int hwa = max(max(eo.sa, pa) + kStep, 0), hwb = max(max(eo.sb, pb) + kStep, 0);
+                const int rA = row0 + r0 + ra, rB = rA + kRPI;
+                uint32_t wa0 = eo.ca.x, wa1 = eo.ca.y, wb0 = eo.cb.x, wb1 = eo.cb.y;
+                if (GRID == 1) {
+                    wa0 = twos_to_signmag8(wa0);
+                    wa1 = twos_to_signmag8(wa1);
+                    wb0 = twos_to_signmag8(wb0);
+                    wb1 = twos_to_signmag8(wb1);
+                }
+                if (A.valid)
+                    *reinterpret_cast<uint4*>(P.fp8 + (int64_t)rA * P.K + col) =
+                        widen16_e5m2(wa0, wa1, hwa - kStep - eo.sa);
+                if (B.valid)
+                    *reinterpret_cast<uint4*>(P.fp8 + (int64_t)rB * P.K + col) =
+                        widen16_e5m2(wb0, wb1, hwb - kStep - eo.sb);
+                // cells of the groups (col / 32): lanes with an even chunk index
+                // hold them; every lane of the row's eight gets both rows' words
+                const uint32_t ca = A.valid ? (uint32_t)hwa : 0u, cb = B.valid ? (uint32_t)hwb : 0u;
+                uint32_t wa = 0u, wb = 0u;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    wa |= __shfl_sync(0xFFFFFFFFu, ca, (lane & ~7) + 2 * k) << (8 * k);
+                    wb |= __shfl_sync(0xFFFFFFFFu, cb, (lane & ~7) + 2 * k) << (8 * k);
+                }
+                // lane c of the eight stores copy c % 4 of row A (c < 4) or B; when
+                // the row's part is a tile's short last part (part_rows < 128),
+                // row w also stores the zero cells of the part's row w + part_rows
+                // if that row lies past the part's end
+                const int r = cchunk < 4 ? rA : rB;
+                if (r < P.rows_cover) {
+                    // the GEMM tile of r from that of the quantizer tile's first row
+                    // (tiles are at least 128 rows, so r is in it or the next)
+                    int tt = ptile, rr = r - prow0;
+                    if (rr >= P.tile_rows) {
+                        ++tt;
+                        rr -= P.tile_rows;
+                    }
+                    const int h = rr >> 7, w = rr & 127;
+                    const int part_rows = min(128, P.tile_rows - 128 * h);
+                    const int g0 = (col >> 5) & ~3;  // the first group of the chunk (the tile's 128 columns)
+                    uint8_t* c = P.chunks + (cchunk & 3) * 512;
+                    *reinterpret_cast<uint32_t*>(c + chunk_cell_offset_twh(tt, h, w, g0, P.parts, P.chunks_k)) =
+                        cchunk < 4 ? wa : wb;
+                    if (w + part_rows < 128)
+                        *reinterpret_cast<uint32_t*>(
+                            c + chunk_cell_offset_twh(tt, h, w + part_rows, g0, P.parts, P.chunks_k)) = 0u;
+                }
+            }
         }
         const int next = tile + kStages * gridDim.x;
         if (TWO_D) {
@@ -763,12 +830,12 @@ static cudaError_t launch_rows_seg(const RowsMaps& maps, RowsParams& p, int num_
 }
 
 
-template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D>
+template <int GRID, bool SR, int SF, bool N16, int CTAS, int TC, bool TWO_D, bool PREP = false>
 static cudaError_t launch_rows_cfg(const RowsMaps& maps, const RowsParams& p, int num_sms, cudaStream_t st) {
     constexpr int kTileElems = TWO_D ? 2 * (kThreads / (TC / kChunk)) * TC : 16384;
     constexpr int kSlots = TWO_D ? (kTileElems / TC / 16) * (TC / 16) : 0;
     const size_t smem = (size_t)p.stages * kTileElems * 2 + 8 * kSlots + 16 * p.stages + 128;
-    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS, TC, TWO_D>;
+    auto k = quantize_rows_kernel<GRID, SR, SF, N16, CTAS, TC, TWO_D, PREP>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int grid = p.num_tiles < CTAS * num_sms ? p.num_tiles : CTAS * num_sms;
@@ -786,6 +853,13 @@ static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms,
         }
     }
     p.stages = kRowsStages;
+    if constexpr (SF == 1 && GRID <= 1) {
+        if (p.prep) {
+            if (p.n != 16) return cudaErrorNotSupported;
+            return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, false, true>(maps, p, num_sms, st);
+        }
+    }
+    if (p.prep) return cudaErrorNotSupported;
     if (p.n == 16) return launch_rows_cfg<GRID, SR, SF, true, kRowsCtas, 128, false>(maps, p, num_sms, st);
     return launch_rows_cfg<GRID, SR, SF, false, kRowsCtas, 128, false>(maps, p, num_sms, st);
 }
@@ -793,6 +867,7 @@ static cudaError_t launch_rows(const RowsMaps& maps, RowsParams& p, int num_sms,
 cudaError_t launch_quantize_rows(RowsParams& p, int grid, bool sr, int sf, int num_sms, cudaStream_t st) {
     // n = 64 and n = 256: the segment kernel, fed by 64-column boxes with the 128-byte swizzle
     const bool seg_kernel = (p.n == 64 && p.tc == 128) || (p.n == 256 && p.tc == 256);
+    if (p.prep && (seg_kernel || p.lb2d || sf != 1 || grid > 1)) return cudaErrorNotSupported;
     RowsMaps maps;
     memset(&maps, 0, sizeof(maps));
     for (int t = 0; t < p.count; ++t) {
@@ -865,6 +940,7 @@ static void preload_rows(cudaFuncAttributes* a) {
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 2, true, kRowsCtas, 128, false>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, false, kRowsCtas, 128, true>);
     cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, true>);
+    if constexpr (G <= 1) cudaFuncGetAttributes(a, quantize_rows_kernel<G, SR, 1, true, kRowsCtas, 128, false, true>);
 }
 
 cudaError_t preload_rows_kernels() {

@@ -32,6 +32,7 @@ EXPORTED = (
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
     "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
     "ufp4_rht_quantize_batch", "ufp4_quant_error_stats", "ufp4_error_stats", "ufp4_set_quantize_wait_limit",
+    "ufp4_rht_quantize_prepare",
 )
 MAX_BATCH = 4
 
@@ -83,6 +84,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_gemm_noalloc.argtypes = [QT, QT, QD, P, i64, P]
     L.ufp4_gemm_prepare.argtypes = [QT, QT, QD, P, ctypes.c_size_t, P]
     L.ufp4_gemm_prepared.argtypes = [QT, QT, QD, P, i64, P, ctypes.c_size_t, P]
+    L.ufp4_rht_quantize_prepare.argtypes = [P, i64, P, i64, QD, QT, QT, P, ctypes.c_size_t, P]
     L.ufp4_gemm_grouped_workspace_size.argtypes = [i32, QT, QT, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm_grouped.argtypes = [i32, QT, QT, QD, ctypes.POINTER(P), ctypes.POINTER(i64), P, ctypes.c_size_t, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
@@ -94,7 +96,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
                  "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error",
                  "ufp4_gemm_noalloc", "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped",
-                 "ufp4_gemm_prepare", "ufp4_gemm_prepared"):
+                 "ufp4_gemm_prepare", "ufp4_gemm_prepared", "ufp4_rht_quantize_prepare"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -207,6 +209,15 @@ def ufp4_gemm_prepare(A: QTensor, B: QTensor, desc: QuantDesc, workspace, stream
     _check(load().ufp4_gemm_prepare(ctypes.byref(A), ctypes.byref(B), ctypes.byref(desc), workspace.data_ptr(),
                                     workspace.numel() * workspace.element_size(), _stream(stream)),
            "ufp4_gemm_prepare")
+
+
+def ufp4_rht_quantize_prepare(a, b, desc: QuantDesc, A: QTensor, B: QTensor, workspace, stream=None):
+    """Row-wise quantization of the GEMM operands a and b into A and B, and their prepared form in
+    `workspace` (what ufp4_gemm_prepare writes), in one launch."""
+    _check(load().ufp4_rht_quantize_prepare(a.data_ptr(), a.stride(0), b.data_ptr(), b.stride(0), ctypes.byref(desc),
+                                            ctypes.byref(A), ctypes.byref(B), workspace.data_ptr(),
+                                            workspace.numel() * workspace.element_size(), _stream(stream)),
+           "ufp4_rht_quantize_prepare")
 
 
 def ufp4_gemm_prepared(A: QTensor, B: QTensor, desc: QuantDesc, D, workspace, stream=None):

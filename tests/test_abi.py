@@ -103,6 +103,26 @@ def test_batch_validation_rejects_bad_arguments(lib):
     assert call(ok, count=1, xs=(0, 0), rows=(0, 0), lds=(1, 1)) == 0
 
 
+def test_quantize_prepare_validation(lib):
+    """ufp4_rht_quantize_prepare takes only what it fuses (E1M2 / INT4, UE8M0,
+    1-D blocks, n = 16) and checks the GEMM's rules, before anything is launched."""
+    P = ctypes.c_void_p
+    def call(desc, M=256, N=256, K=256, ws_bytes=1 << 20, a=0x1000, lda=256):
+        A = ufp4.QTensor(0x20000, 0x30000, M, K, K // 2, K // 16)
+        B = ufp4.QTensor(0x40000, 0x50000, N, K, K // 2, K // 16)
+        return lib.ufp4_rht_quantize_prepare(P(a), lda, P(0x9000), K, ctypes.byref(desc), ctypes.byref(A),
+                                             ctypes.byref(B), P(0x100000), ws_bytes, None)
+    ue8 = dict(scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE)
+    assert call(ufp4.make_desc(grid="e2m1", **ue8)) == 2                  # native FP4: nothing to widen
+    assert call(ufp4.make_desc(n=64, **ue8)) == 2                         # n = 16 only
+    assert call(ufp4.make_desc(block=(32, 32), **ue8)) == 2               # 1-D blocks only
+    assert call(ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)) == 2           # fp32 scales
+    assert call(ufp4.make_desc(scale_fmt=ufp4.SCALE_UE8M0, out_mask=ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE)) == 1
+    assert call(ufp4.make_desc(**ue8), ws_bytes=256) == 1                 # workspace too small
+    assert call(ufp4.make_desc(**ue8), a=0x1001) == 3                     # a misaligned
+    assert call(ufp4.make_desc(**ue8), lda=128) == 1                      # lda < K
+
+
 def test_diagnostics_validation(lib):
     desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)
     q = ufp4.QTensor(0x2000, 0x3000, 64, 64, 32, 4)
