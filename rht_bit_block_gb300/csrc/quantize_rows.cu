@@ -376,6 +376,18 @@ quantize_rows_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) 
 // element in register moves).
 constexpr int kRowsCtas = 2, kRowsStages = 3;
 
+// Barrier of the nthreads threads (a multiple of 32) of the warps that use
+// named barrier id (1..15); returns the AND of v over them.  Barrier
+// semantics order the shared-memory accesses of those threads.
+__device__ __forceinline__ bool band_sync_and(uint32_t id, uint32_t nthreads, bool v) {
+    uint32_t r;
+    asm volatile("{ .reg .pred p, q; setp.ne.u32 p, %1, 0; bar.red.and.pred q, %2, %3, p; selp.u32 %0, 1, 0, q; }"
+                 : "=r"(r)
+                 : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+                 : "memory");
+    return r != 0;
+}
+
 // n = 64 and n = 256, 1-D or b x b blocks: a thread owns one 64-element segment of
 // a row.  QN segments make one tile row (QN = 2: 128 columns, n = 64; QN = 4:
 // 256 columns, n = 256), so the tile is 128 x 128 or 64 x 256.  It arrives as
@@ -394,12 +406,14 @@ constexpr int kRowsCtas = 2, kRowsStages = 3;
 // "empty" barrier; thread 0 waits on that one before it refills the stage.
 // TWO_D (b = 16, 32, 64; UE8M0): the block amax is reduced over the rows a
 // warp holds (lanes ^ 1, 2, 4, and ^ 16 for two segments a row), then across
-// warps with a shared-memory atomicMax and one CTA barrier per tile; the ring
-// runs as for 1-D blocks.  The amax slots come in three sets used in turn:
-// after tile i's barrier the set of tile i + 2 is cleared.  Its last reads
-// (tile i - 1) precede tile i's barrier in every warp, and its next
-// atomicMax (tile i + 2) follows tile i + 1's barrier, which the clearing
-// threads reach only after the clear.
+// the warps of its b-row band (the b / 16 or b / 8 warps holding those rows)
+// with a shared-memory atomicMax and one named barrier of the band per tile;
+// a band of one warp (n = 64, b = 16) needs neither.  The ring runs as for
+// 1-D blocks.  The amax slots come in three sets used in turn: after tile
+// i's barrier the band clears its slots of the set of tile i + 2.  Their
+// last reads (tile i - 1) precede tile i's barrier in every warp of the
+// band, and their next atomicMax (tile i + 2) follows tile i + 1's barrier,
+// which the clearing threads reach only after the clear.
 template <int GRID, bool SR, int SF, int CTAS, int QN, bool TWO_D>
 __global__ void __launch_bounds__(kThreads, CTAS)
 quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams p) {
@@ -621,9 +635,12 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                     MA2 = fmaxf(MA2, __shfl_xor_sync(0xFFFFFFFFu, MA2, k));
                     MB2 = fmaxf(MB2, __shfl_xor_sync(0xFFFFFFFFu, MB2, k));
                 }
-                // then across the warps of the band: slot (row block, column block)
+                // then across the warps of the band (b / 8 warps of eight rows):
+                // slot (row block = band, column block)
                 uint32_t* set = amax2d + (i % 3) * kSlots;
-                const int rs = (r >> lb) << (8 - lb);
+                const int band = (tid >> 5) >> (lb - 3);
+                const int bthreads = 32 << (lb - 3);
+                const int rs = band << (8 - lb);
                 const int sA1 = rs + (c1 >> lb), sB1 = rs + ((c1 + 16) >> lb);
                 const int sA2 = rs + ((c1 + 128) >> lb), sB2 = rs + ((c1 + 144) >> lb);
                 if ((lane & 7) == 0 && (lb < 6 || b0 == 0)) {
@@ -634,16 +651,17 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                         atomicMax(&set[sB2], __float_as_uint(MB2));
                     }
                 }
-                if (!__syncthreads_and(ok)) {
-                    if (tid == 0) atomicExch(&g_rows_error, 1);
+                if (!band_sync_and(1 + band, bthreads, ok)) {
+                    if (lane == 0) atomicExch(&g_rows_error, 1);
                     break;
                 }
                 MA1 = __uint_as_float(set[sA1]);
                 MB1 = __uint_as_float(set[sB1]);
                 MA2 = __uint_as_float(set[sA2]);
                 MB2 = __uint_as_float(set[sB2]);
-                // the set of tile i + 2 (last read in tile i - 1)
-                if (tid < kSlots) amax2d[((i + 2) % 3) * kSlots + tid] = 0u;
+                // the band's slots of the set of tile i + 2 (last read in tile i - 1)
+                const int bl = tid - band * bthreads;
+                if (bl < (256 >> lb)) amax2d[((i + 2) % 3) * kSlots + rs + bl] = 0u;
             }
             const bool join = GRID != 4 && (T.codes_ld & 15) == 0;
             const int64_t rowlin = (int64_t)row * T.cols;
@@ -705,27 +723,36 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                     M2 = fmaxf(M2, __shfl_xor_sync(0xFFFFFFFFu, M2, k));
                     M3 = fmaxf(M3, __shfl_xor_sync(0xFFFFFFFFu, M3, k));
                 }
-                // then across the warps of the band: slot (row block, column block)
-                uint32_t* set = amax2d + (i % 3) * kSlots;
-                const int lnbc = (QN == 2 ? 7 : 8) - lb;  // log2(TC / b)
-                const int slot0 = ((r >> lb) << lnbc) + ((64 * seg) >> lb);
-                const int cpb = (1 << lb) >> 4;  // chunks per block column
-                if ((lane & (QN == 2 ? 0x17 : 0x7)) == 0) {
-                    atomicMax(&set[slot0], __float_as_uint(M0));
-                    if (cpb == 1) atomicMax(&set[slot0 + 1], __float_as_uint(M1));
-                    if (cpb <= 2) atomicMax(&set[slot0 + (cpb == 1 ? 2 : 1)], __float_as_uint(M2));
-                    if (cpb == 1) atomicMax(&set[slot0 + 3], __float_as_uint(M3));
+                // then across the warps of the band (b / 16 warps of sixteen rows):
+                // slot (row block = band, column block); a band of one warp
+                // (b = 16) has its block amax already
+                static_assert(QN == 2, "n = 64 here");
+                if (lb == 4) {
+                    if (!ok) {
+                        if (lane == 0) atomicExch(&g_rows_error, 1);
+                        break;
+                    }
+                } else {
+                    uint32_t* set = amax2d + (i % 3) * kSlots;
+                    const int band = (tid >> 5) >> (lb - 4);
+                    const int bthreads = 32 << (lb - 4);
+                    const int lnbc = 7 - lb;  // log2(TC / b)
+                    const int slot0 = (band << lnbc) + ((64 * seg) >> lb);
+                    const int cpb = (1 << lb) >> 4;  // chunks per block column
+                    if ((lane & 0x17) == 0) {
+                        atomicMax(&set[slot0], __float_as_uint(M0));
+                        if (cpb <= 2) atomicMax(&set[slot0 + 1], __float_as_uint(M2));
+                    }
+                    if (!band_sync_and(1 + band, bthreads, ok)) {
+                        if (lane == 0) atomicExch(&g_rows_error, 1);
+                        break;
+                    }
+                    M0 = M1 = __uint_as_float(set[slot0]);
+                    M2 = M3 = __uint_as_float(set[slot0 + (cpb == 2 ? 1 : 0)]);
+                    // the band's slots of the set of tile i + 2 (last read in tile i - 1)
+                    const int bl = tid - band * bthreads;
+                    if (bl < (128 >> lb)) amax2d[((i + 2) % 3) * kSlots + (band << lnbc) + bl] = 0u;
                 }
-                if (!__syncthreads_and(ok)) {
-                    if (tid == 0) atomicExch(&g_rows_error, 1);
-                    break;
-                }
-                M0 = __uint_as_float(set[slot0]);
-                M1 = __uint_as_float(set[slot0 + (cpb == 1 ? 1 : 0)]);
-                M2 = __uint_as_float(set[slot0 + (cpb == 1 ? 2 : (cpb == 2 ? 1 : 0))]);
-                M3 = __uint_as_float(set[slot0 + (cpb == 1 ? 3 : (cpb == 2 ? 1 : 0))]);
-                // the set of tile i + 2 (last read in tile i - 1)
-                if (tid < kSlots) amax2d[((i + 2) % 3) * kSlots + tid] = 0u;
             }
             uint8_t* cp = T.codes + (int64_t)row * T.codes_ld + (GRID == 4 ? col : col >> 1);
             uint8_t* sp = T.scales + ((int64_t)row * T.scales_ld + (col >> lbw)) * SZ;

@@ -19,11 +19,13 @@ pytestmark = pytest.mark.gpu
 
 # row-only n = 16: the row kernel; row + column: the general kernel; row-only
 # n = 64 and n = 256: the segment kernel (per-warp waits, empty barriers; with
-# 32 x 32 blocks the failed waits meet the other warps at the tile's barrier)
+# b x b blocks the failed waits meet the band's other warps at its barrier, and
+# n = 64 with 16 x 16 blocks, a band of one warp, leaves like 1-D blocks)
 @pytest.mark.parametrize("mask,n,block", [(ufp4.OUT_ROWWISE, 16, (1, 16)),
                                           (ufp4.OUT_ROWWISE | ufp4.OUT_COLWISE, 16, (1, 16)),
                                           (ufp4.OUT_ROWWISE, 64, (1, 16)), (ufp4.OUT_ROWWISE, 256, (1, 16)),
-                                          (ufp4.OUT_ROWWISE, 64, (32, 32)), (ufp4.OUT_ROWWISE, 256, (32, 32))])
+                                          (ufp4.OUT_ROWWISE, 64, (32, 32)), (ufp4.OUT_ROWWISE, 256, (32, 32)),
+                                          (ufp4.OUT_ROWWISE, 64, (16, 16)), (ufp4.OUT_ROWWISE, 256, (64, 64))])
 def test_quantizer_wait_timeout_is_reported_and_recovers(mask, n, block):
     x = inputs.tiny_check(256, 1024)
     kw = dict(grid="e1m2", block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0)
