@@ -286,7 +286,15 @@ ufp4_status quantize_common(const void* x, int64_t cols, int64_t ld, const int64
     // 2-D blocks take 64-row tiles where they can: one row pair (and one
     // column task) per thread, whose values stay in registers across the
     // block-amax barrier
-    const int tr = (do_col && seg_lanes < 8) ? 64 : ((n == 256 || (bs.is2d && !do_col)) ? 64 : 128);
+    int tr = (do_col && seg_lanes < 8) ? 64 : ((n == 256 || (bs.is2d && !do_col)) ? 64 : 128);
+    if (do_col && seg_lanes < 8 && !bs.is2d) {
+        // 1-D blocks: 128-row tiles give each warp two column tasks per tile
+        // (more work per tile barrier) where the walk still has about four
+        // waves of tiles for the three CTAs per SM; small tensors keep 64
+        int64_t t128 = 0;
+        for (int g = 0; g < ngroups; ++g) t128 += (pad0[g + 1] - pad0[g] + 127) / 128;
+        if (t128 * ((cols + tc - 1) / tc) >= 12LL * num_sms_current()) tr = 128;
+    }
     p.x = (const uint16_t*)x;
     p.cols = cols;
     p.ld = ld;
