@@ -61,10 +61,21 @@ constexpr int kErrTimeout = 1;
 // work (issuing a tcgen05 instruction costs a fixed time).  FP4 needs two
 // (2X kind) to four (4X kind) times the scale columns per K tile: the 2X
 // kind's two scale sets still fit beside two 224-column accumulators
-// (448 + 48 <= 512), the 4X kind's do not, so its tiles are 256 x 192.
-constexpr int kBnFp8 = 224, kBnFp4 = 192;
+// (448 + 48 <= 512).  The 4X kind's do not: kind 2 runs 256 x 192 tiles
+// with two accumulators (384 + 96), kind 4 256 x 256 tiles with one (256 +
+// 96).  Each stage's six scale copies and its hand-off cost the same time
+// whatever the tile width, so the wide tile does a third more MMA work per
+// stage, but a tile's epilogue then holds up the next tile's first MMA:
+// the plan takes kind 4 for long K (16 or more K tiles per output tile).
+constexpr int kBnFp8 = 224, kBnFp4 = 192, kBnFp4Wide = 256;
 constexpr int kBnFp4x2 = 224;
-__host__ __device__ constexpr int pair_bn(int kind) { return kind == 0 ? kBnFp8 : (kind == 1 ? kBnFp4x2 : kBnFp4); }
+__host__ __device__ constexpr int pair_bn(int kind) {
+    return kind == 0 ? kBnFp8 : (kind == 1 ? kBnFp4x2 : (kind == 4 ? kBnFp4Wide : kBnFp4));
+}
+// accumulator buffers in tensor memory: two (a tile's epilogue overlaps the
+// next tile's main loop), or one for kind 4's 256-wide tiles
+__host__ __device__ constexpr int pair_nacc(int kind) { return kind == 4 ? 1 : 2; }
+constexpr int kWideFp4MinKTiles = 16;
 // CTA-pair rings: stages of KPS K tiles each (FP4 stages hold one K tile of
 // 256 elements, as much MMA work as two FP8 K tiles of 128)
 constexpr int kPairKps = 2, kPairStages = 3;          // FP8
@@ -241,7 +252,7 @@ __device__ __forceinline__ void tma_load_pair(uint32_t dst, const CUtensorMap* m
         : "memory");
 }
 
-template <int KIND>  // 0: mxf8f6f4 scale_vec::1X, 1: mxf4 scale_vec::2X, 2: mxf4nvf4 scale_vec::4X
+template <int KIND>  // 0: mxf8f6f4 scale_vec::1X, 1: mxf4 scale_vec::2X, 2 and 4: mxf4nvf4 scale_vec::4X
 __device__ __forceinline__ void mma_pair(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                          uint32_t sfb, uint32_t accumulate) {
     if (KIND == 0) {
@@ -346,8 +357,9 @@ struct PairCfg {
     static constexpr int kTmemCols = 512;
     static constexpr int kASet = 4 * kChunks;            // scale columns of A per set
     static constexpr int kBSet = 8 * kChunks;            // scale columns of B per set
-    static constexpr int kSfaCol = 2 * BN;
-    static constexpr int kSfbCol = 2 * BN + 2 * kASet;
+    static constexpr int NACC = pair_nacc(KIND);
+    static constexpr int kSfaCol = NACC * BN;
+    static constexpr int kSfbCol = kSfaCol + 2 * kASet;
     static_assert(kSfbCol + 2 * kBSet <= kTmemCols, "tensor memory overflow");
     static_assert(kSmem <= 232448, "shared memory overflow");
     static_assert(kOffA % 1024 == 0 && kAAtom % 1024 == 0 && kBAtom % 1024 == 0,
@@ -513,8 +525,10 @@ gemm_pair_kernel(const __grid_constant__ PairMaps<G> maps, const __grid_constant
         int sc = 0;  // stages issued so far (alternates the scale sets)
         bool ok = true;
         for (int tile = cluster_id; tile < num_tiles && ok; tile += num_clusters, ++tc) {
-            const int buf = tc & 1;
-            if (!mbar_wait(acce_bar(buf), ((tc >> 1) & 1) ^ 1)) {
+            // buffer buf of NACC, in its (tc / NACC)-th use
+            const int buf = C::NACC == 2 ? (tc & 1) : 0;
+            const uint32_t use_par = C::NACC == 2 ? ((tc >> 1) & 1) : (tc & 1);
+            if (!mbar_wait(acce_bar(buf), use_par ^ 1)) {
                 ok = false;
                 break;
             }
@@ -578,8 +592,9 @@ gemm_pair_kernel(const __grid_constant__ PairMaps<G> maps, const __grid_constant
         const uint64_t stream_out = policy_evict_first();
         int tc = 0;
         for (int tile = cluster_id; tile < num_tiles; tile += num_clusters, ++tc) {
-            const int buf = tc & 1;
-            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), (tc >> 1) & 1));
+            const int buf = C::NACC == 2 ? (tc & 1) : 0;
+            const uint32_t use_par = C::NACC == 2 ? ((tc >> 1) & 1) : (tc & 1);
+            const bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(accf_bar(buf), use_par));
             if (!ok || *abort_flag) break;
             tc_fence_after();
             int local;
@@ -1127,7 +1142,7 @@ bool make_map(CUtensorMap* map, const void* ptr, int64_t rows, int64_t row_bytes
 }
 
 struct Plan {
-    int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X, 3 fp32 block scales (bf16 partials rescaled)
+    int kind;          // 0 fp8, 1 fp4 2X, 2 fp4 4X, 3 fp32 block scales (bf16 partials rescaled), 4 fp4 4X wide tiles
     bool native;       // kind 0 on MXFP8 codes: E4M3 operands used in place (no widening)
     int bn;            // B tile rows (output tile columns)
     int64_t k_bytes;   // bytes of K per row in the MMA operand
@@ -1173,6 +1188,7 @@ Plan make_plan(int64_t M, int64_t N, int64_t K, int grid, int br, int bc, int sf
         return pl;
     }
     pl.kind = (grid == 2 || grid == 3) ? (bc == 16 ? 2 : 1) : 0;  // E2M1 codes (grids 2, 3): native FP4
+    if (pl.kind == 2 && (K / 2 + kBKBytes - 1) / kBKBytes >= kWideFp4MinKTiles) pl.kind = 4;
     pl.native = grid == 4;                                          // MXFP8: E4M3 bytes
     pl.bn = pair_bn(pl.kind);
     pl.k_bytes = (grid == 2 || grid == 3) ? K / 2 : K;
@@ -1328,7 +1344,7 @@ cudaError_t launch_prep_pair(const GemmArgs* gs, int n, cudaStream_t st) {
     pp.grid = gs[0].grid;
     pp.lbr = ilog2(gs[0].br);
     pp.lbc = ilog2(gs[0].bc);
-    pp.lhw = pl.kind == 2 ? 4 : 5;
+    pp.lhw = (pl.kind == 2 || pl.kind == 4) ? 4 : 5;
     pp.copies = pair_replicated(pl.kind) ? 4 : 1;
     if (pl.kind == 0 && !pl.native) {
         // 64 groups of 32 elements per CTA along K; 16 CTAs per 128-row part of a GEMM tile
@@ -1417,9 +1433,10 @@ cudaError_t launch_main_pair_g(const GemmArgs* gs, int n, cudaStream_t st) {
     }
     // scale_vec::4X: UE8M0 scales, or E4M3 ones (scale type bit 0) for the two-level format
     const bool two_level = g.sf == 2;
-    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, kBnFp4, 0, !two_level);
+    for (int j = 0; j < 4; ++j) kp.idesc[j] = make_idesc(1, 1, 2 * kBM, pair_bn(pl.kind), 0, !two_level);
     kp.two_level = two_level;
     kp.den = grid_qmax_host(g.grid) * 448.0f;
+    if (pl.kind == 4) return run_gemm_pair<4, kPairStagesFp4x4, 1, G>(maps, kp, st);
     return run_gemm_pair<2, kPairStagesFp4x4, 1, G>(maps, kp, st);
 }
 
@@ -1594,6 +1611,7 @@ cudaError_t preload_gemm_kernels() {
     cudaFuncGetAttributes(&a, gemm_pair_kernel<0, kPairStages, kPairKps, 1>);
     cudaFuncGetAttributes(&a, gemm_pair_kernel<1, kPairStagesFp4x2, 1, 1>);
     cudaFuncGetAttributes(&a, gemm_pair_kernel<2, kPairStagesFp4x4, 1, 1>);
+    cudaFuncGetAttributes(&a, gemm_pair_kernel<4, kPairStagesFp4x4, 1, 1>);
     cudaFuncGetAttributes(&a, gemm_f32s_kernel);
     cudaFuncGetAttributes(&a, prep_widen_kernel);
     cudaFuncGetAttributes(&a, prep_scales_kernel);

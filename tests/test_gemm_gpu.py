@@ -50,6 +50,21 @@ def _rel(D, ref):
 FP8_GRIDS = ("e1m2", "int4")
 
 
+@pytest.mark.parametrize("shape", [(2560, 2304, 4096), (2500, 2200, 4160)])
+def test_gemm_exact_integer_wide_fp4_tiles(shape):
+    """E2M1 1 x 16 with 16 or more K tiles takes the 256 x 256 tiles with one
+    accumulator: more output tiles than CTA pairs (ragged in the second shape),
+    so each pair hands its accumulator from one tile's epilogue to the next
+    tile's MMAs.  Unit scales: exact."""
+    rng = np.random.default_rng(23)
+    M, N, K = shape
+    ac, asc = _rand_operand(rng, M, K, "e2m1", (1, 16))
+    bc, bsc = _rand_operand(rng, N, K, "e2m1", (1, 16))
+    D = _gemm(ac, asc, bc, bsc, M, N, K, "e2m1", (1, 16))
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid="e2m1", block=(1, 16))
+    np.testing.assert_array_equal(D, ref)
+
+
 @pytest.mark.parametrize("grid", FP8_GRIDS + ("e2m1", "e2m1r2"))
 @pytest.mark.parametrize("block", BLOCKS)
 @pytest.mark.parametrize("shape", [(128, 256, 128), (256, 512, 512), (200, 300, 384), (200, 300, 160)])
