@@ -50,18 +50,22 @@ def _rel(D, ref):
 FP8_GRIDS = ("e1m2", "int4")
 
 
+@pytest.mark.parametrize("block", [(1, 16), (1, 32), (32, 32)])
 @pytest.mark.parametrize("shape", [(2560, 2304, 4096), (2500, 2200, 4160)])
-def test_gemm_exact_integer_wide_fp4_tiles(shape):
-    """E2M1 1 x 16 with 16 or more K tiles takes the 256 x 256 tiles with one
-    accumulator: more output tiles than CTA pairs (ragged in the second shape),
-    so each pair hands its accumulator from one tile's epilogue to the next
+def test_gemm_exact_integer_wide_fp4_tiles(shape, block):
+    """Long K (16 or more K tiles): E2M1 1 x 16 takes the 256 x 256 tiles with
+    one accumulator, 1 x 32 and 32 x 32 the 2X kind's double-buffered 256 x 224
+    tiles.  More output tiles than CTA pairs (ragged in the second shape), so
+    each pair hands its accumulators from one tile's epilogue to the next
     tile's MMAs.  Unit scales: exact."""
     rng = np.random.default_rng(23)
     M, N, K = shape
-    ac, asc = _rand_operand(rng, M, K, "e2m1", (1, 16))
-    bc, bsc = _rand_operand(rng, N, K, "e2m1", (1, 16))
-    D = _gemm(ac, asc, bc, bsc, M, N, K, "e2m1", (1, 16))
-    ref = orc.gemm_reference(ac, asc, bc, bsc, grid="e2m1", block=(1, 16))
+    if block[0] > 1:
+        M, N = (M + 31) // 32 * 32, (N + 31) // 32 * 32
+    ac, asc = _rand_operand(rng, M, K, "e2m1", block)
+    bc, bsc = _rand_operand(rng, N, K, "e2m1", block)
+    D = _gemm(ac, asc, bc, bsc, M, N, K, "e2m1", block)
+    ref = orc.gemm_reference(ac, asc, bc, bsc, grid="e2m1", block=block)
     np.testing.assert_array_equal(D, ref)
 
 
