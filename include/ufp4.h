@@ -367,9 +367,7 @@ ufp4_status ufp4_gemm_grouped_workspace_size(int32_t num_groups, const ufp4_qten
  * that small groups run side by side.  The internal streams start after the
  * work already enqueued on `stream`, and `stream` waits for them before any
  * later work, so the call is ordered on `stream` like a single launch.  The
- * enqueue sequence is serialized by a lock (safe from several host threads).
- * Inside a CUDA-graph capture of `stream` the internal streams join the
- * capture and are joined back before the call returns. */
+ * enqueue sequence is serialized by a lock (safe from several host threads). */
 ufp4_status ufp4_gemm_grouped(int32_t num_groups, const ufp4_qtensor* A, const ufp4_qtensor* B,
                               const ufp4_quant_desc* desc, float* const* D, const int64_t* ldd, void* workspace,
                               size_t workspace_bytes, cudaStream_t stream);
