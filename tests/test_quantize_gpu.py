@@ -317,3 +317,34 @@ def test_batch_matches_oracle_and_single_calls(rounding, grid, n):
         single = gpu_quantize(dv, out_mask=ufp4.OUT_ROWWISE, **kw)["row"]
         assert_bitwise(cb.cpu().numpy(), single[0], "batch vs single codes")
         assert_bitwise(sb.cpu().numpy(), single[1], "batch vs single scales")
+
+
+@pytest.mark.parametrize("block,fmt", [((1, 16), FP32), ((1, 32), PO2), ((32, 32), PO2)])
+@pytest.mark.parametrize("rounding", [RTNE, SR])
+def test_hadamard_256_code_rows_8_byte_aligned(block, fmt, rounding):
+    """n = 256 stores each segment's two chunks of codes as one 16-byte word
+    when the code rows are 16-byte aligned, else as two 8-byte words: a code
+    leading dimension of 8 mod 16 bytes takes the second form.  The padding
+    bytes of each code row stay untouched."""
+    rows, cols = 128, 768
+    x = inputs.tiny_check(rows, cols)
+    kw = dict(grid="e1m2", block=block, n=256, sign_seed=4, rounding=rounding, sr_seed=6, scale_fmt=fmt)
+    desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE, **ufp4_kw(kw))
+    dev = torch.device("cuda", 0)
+    codes_full = torch.full((rows, cols // 2 + 8), 0x5A, dtype=torch.uint8, device=dev)
+    codes = codes_full[:, : cols // 2]
+    _, scales = ufp4.alloc_quantized(rows, cols, desc, dev)
+    q = ufp4.qtensor(codes, scales, rows, cols)
+    assert q.codes_ld % 16 == 8
+    ufp4.ufp4_rht_quantize(to_dev(x), desc, q, None)
+    torch.cuda.synchronize()
+    c, s = orc.quantize(x, **kw)
+    assert_bitwise(codes.cpu().numpy(), c, "row-wise codes")
+    assert_bitwise(scales.cpu().numpy(), s, "row-wise scales")
+    assert torch.all(codes_full[:, cols // 2:] == 0x5A), "a code row's padding was written"
+
+
+def ufp4_kw(kw):
+    """The oracle's keyword names mapped to ufp4.make_desc's."""
+    return dict(grid=kw["grid"], block=kw["block"], n=kw["n"], sign_seed=kw["sign_seed"], rounding=kw["rounding"],
+                sr_seed=kw["sr_seed"], scale_fmt=kw["scale_fmt"])

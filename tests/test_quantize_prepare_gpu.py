@@ -5,7 +5,6 @@ reads the workspace must then give the same D bit for bit.  The quantized
 codes and scales are checked against the oracle through the batch call
 (tests/test_quantize_gpu.py); the GEMM on such a workspace against the
 oracle's fp64 product (tests/test_gemm_gpu.py)."""
-import numpy as np
 import pytest
 import torch
 
@@ -80,11 +79,12 @@ def test_fused_prepare_wide_scale_gaps_and_strided_input():
         _assert_same(_two_routes(x, w, desc, x_ld=K + 64))
 
 
-def test_fused_prepare_stochastic_rounding():
+@pytest.mark.parametrize("grid", ["e1m2", "int4"])
+def test_fused_prepare_stochastic_rounding(grid):
     M, N, K = 384, 224, 1024
     x = inputs.student_t_bf16(M, K, 621)
     w = inputs.normal_bf16(N, K, 622, std=0.02)
-    desc = ufp4.make_desc(grid="e1m2", block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0,
+    desc = ufp4.make_desc(grid=grid, block=(1, 16), n=16, sign_seed=inputs.SIGN_SEED, scale_fmt=ufp4.SCALE_UE8M0,
                           rounding=ufp4.ROUND_SR, sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
     _assert_same(_two_routes(x, w, desc))
 
