@@ -208,12 +208,14 @@ struct EmitOut {
 // unnegated vector (exact: IEEE products are sign-symmetric).  join: B's codes
 // follow A's (A.codes + 8, 16-byte aligned, A.valid == B.valid), stored as one
 // 16-byte word.  out: if given, receives the codes and scale bytes (1-D
-// blocks of 16 or 32, split false).
+// blocks of 16 or 32, split false).  b_in_a: B is the second half of A's
+// block (a 32-wide block over both vectors: MB0 == MA0, split false, B writes
+// no scale), so B takes A's reciprocal instead of computing it again.
 template <int GRID, bool SR, int SF>
 __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, float MB0, float MB1, bool split,
                                           const Fold& fd, const Dest& A, const Dest& B, const SrDraws& dr,
                                           uint32_t nega = 0u, uint32_t negb = 0u, bool join = false,
-                                          EmitOut* out = nullptr) {
+                                          EmitOut* out = nullptr, bool b_in_a = false) {
     // the uniform grids with power-of-two scales round by adding 1.5 * 2^23 + 8
     // to the value in units of the grid step (below): INT4 k, E1M2 4 t
     constexpr bool kMagic = GRID <= 1 && !SR && SF == 1;
@@ -221,7 +223,8 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
                      : kMagic    ? (GRID == 0 ? 2 : 0)
                                  : (SR ? (GRID == 0 ? 2 : 0) : (GRID == 0 ? -7 : (GRID == 1 ? -9 : 0)));  // log2 f
     const float ra0 = block_recip<GRID, SF>(MA0, fd, lf, A.valid && A.w0, A.s0, out ? &out->sa : nullptr);
-    const float rb0 = block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0, out ? &out->sb : nullptr);
+    const float rb0 = b_in_a ? ra0 : block_recip<GRID, SF>(MB0, fd, lf, B.valid && B.w0, B.s0, out ? &out->sb : nullptr);
+    if (b_in_a && out) out->sb = out->sa;
     float ra1 = ra0, rb1 = rb0;
     if (split) {
         ra1 = block_recip<GRID, SF>(MA1, fd, lf, A.valid && A.w1, A.s1);
@@ -343,8 +346,8 @@ __device__ __forceinline__ void emit_pair(uint64_t e[16], float MA0, float MA1, 
         if (GRID == 1) {
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                oa[h] = signmag_to_twos(oa[h]);
-                ob[h] = signmag_to_twos(ob[h]);
+                oa[h] = signmag_nz_to_twos(oa[h]);
+                ob[h] = signmag_nz_to_twos(ob[h]);
             }
         }
         store_pair(make_uint2(oa[0], oa[1]), make_uint2(ob[0], ob[1]));

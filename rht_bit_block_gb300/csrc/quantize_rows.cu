@@ -690,10 +690,11 @@ quantize_rows_seg_kernel(const __grid_constant__ RowsMaps maps, const RowsParams
                 A.valid = B.valid = row < T.rows && cc < T.cols;
                 SrDraws dr;
                 if (SR) draw_pair(dr, p.sr_keys, A, B, 0u, (uint32_t)p.group);
+                // a 32-wide block (b32) covers both chunks: B (chunk + 16) writes no scale
                 if (h == 0)
-                    emit_pair<GRID, SR, SF>(K, MA1, MA1, MB1, MB1, false, fd, A, B, dr, neg1, neg1, join);
+                    emit_pair<GRID, SR, SF>(K, MA1, MA1, MB1, MB1, false, fd, A, B, dr, neg1, neg1, join, nullptr, b32);
                 else
-                    emit_pair<GRID, SR, SF>(S, MA2, MA2, MB2, MB2, false, fd, A, B, dr, neg2, neg2, join);
+                    emit_pair<GRID, SR, SF>(S, MA2, MA2, MB2, MB2, false, fd, A, B, dr, neg2, neg2, join, nullptr, b32);
             }
         } else {
     #pragma unroll

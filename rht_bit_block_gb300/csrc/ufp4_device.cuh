@@ -155,14 +155,24 @@ __device__ __forceinline__ uint32_t clear_negative_zero(uint32_t w) {
     return w & (y | 0x77777777u);
 }
 
-// Sign-magnitude nibbles -> two's complement (INT4): for a negative nibble
-// s|k with k > 0 the result is 8 | ((8 - k) & 7); -0 becomes 0.
-__device__ __forceinline__ uint32_t signmag_to_twos(uint32_t w) {
+// Sign-magnitude nibbles with no -0 (clear_negative_zero first) -> INT4
+// two's complement: a negative nibble 8 + k (k >= 1) becomes
+// ((8 + k) ^ 7) + 1 = 16 - k, which stays inside the nibble.
+__device__ __forceinline__ uint32_t signmag_nz_to_twos(uint32_t w) {
     const uint32_t neg = (w >> 3) & 0x11111111u;
-    const uint32_t mag = w & 0x77777777u;
-    const uint32_t negm = ((mag ^ (neg * 7u)) + neg) & 0x77777777u;
-    const uint32_t nz = (negm + 0x77777777u) & 0x88888888u;
-    return negm | ((neg << 3) & nz);
+    return (w ^ (neg * 7u)) + neg;
+}
+
+// Four E4M3 bytes s000 0kkk (levels k on the subnormal grid, k <= 7) -> the
+// INT4 two's complement of (-1)^s k in the low nibble of each byte: 16 - k
+// for s = 1, formed within the byte (16 - 0 sets bit 4, which the caller
+// masks off, so -0 gives 0).  The sign mask is a byte permute that replicates
+// each byte's top bit.
+__device__ __forceinline__ uint32_t int4_from_e4m3_bytes(uint32_t v) {
+    const uint32_t k = v & 0x07070707u;
+    uint32_t m;
+    asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(m) : "r"(v));
+    return (k & ~m) | ((0x10101010u - k) & m);
 }
 
 }  // namespace ufp4
@@ -251,7 +261,8 @@ __device__ __forceinline__ uint32_t cvt_e2m1x8(float t0, float t1, float t2, flo
 // word of packed sign-magnitude codes.  Uniform grids: the values are k * 2^-9
 // with |k| <= 7 exactly on e4m3's subnormals, so an e4m3 conversion rounds to
 // nearest with ties to even k; the even-indexed elements land in word E and
-// the odd ones in word O, and each byte of E | O becomes one packed byte.
+// the odd ones in word O, and each byte of E | O becomes one packed byte
+// (INT4: two's complement codes, formed per byte before packing).
 template <int GRID>
 __device__ __forceinline__ uint32_t rtne8(float t0, float t1, float t2, float t3, float t4, float t5, float t6,
                                           float t7) {
@@ -261,11 +272,11 @@ __device__ __forceinline__ uint32_t rtne8(float t0, float t1, float t2, float t3
     } else {
         const uint32_t E = cvt_e4m3x4(t0, t2, t4, t6);  // bytes: s000 0kkk
         const uint32_t O = cvt_e4m3x4(t1, t3, t5, t7);
+        if (GRID == 1)
+            return (int4_from_e4m3_bytes(E) & 0x0F0F0F0Fu) | ((int4_from_e4m3_bytes(O) << 4) & 0xF0F0F0F0u);
         w = ((E | (E >> 4)) & 0x0F0F0F0Fu) | ((O | (O << 4)) & 0xF0F0F0F0u);
     }
-    w = clear_negative_zero(w);
-    if (GRID == 1) w = signmag_to_twos(w);
-    return w;
+    return clear_negative_zero(w);
 }
 
 }  // namespace ufp4
