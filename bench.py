@@ -34,6 +34,7 @@ from __future__ import annotations
 import argparse
 import json
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -547,15 +548,17 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
                 for block, fmt in (((1, 16), ufp4.SCALE_FP32), ((1, 32), ufp4.SCALE_FP32),
                                    ((32, 32), ufp4.SCALE_UE8M0)):
                     for rnd in (ufp4.ROUND_RTNE, ufp4.ROUND_SR):
+                        name = (f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
+                                f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}")
+                        if args.suite_match and not re.search(args.suite_match, name):
+                            continue
                         desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
                                               rounding=rnd, sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
                         out = ufp4.alloc_quantized(rows, cols, desc, dev)
                         q = ufp4.qtensor(*out, rows, cols)
                         ms = timed(lambda i: ufp4.ufp4_rht_quantize(xs5[i % 2], desc, q, None, stream.cuda_stream))
                         gbs = rows * cols * (2 + 0.5 + scale_bytes(desc)) / (ms / 1e3) / 1e9
-                        emit("quantize_sweep", f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
-                             f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}", gbs, "GB/s",
-                             gbs / pk["hbm"], pk["hbm"], ms=ms)
+                        emit("quantize_sweep", name, gbs, "GB/s", gbs / pk["hbm"], pk["hbm"], ms=ms)
                         del out, q
         del xs5
 
@@ -792,6 +795,8 @@ def main():
                     help="further measurements (other workloads, widened rows), one JSON line each")
     ap.add_argument("--suite-sections", default="dense,rowwise,sweep,rowcol,diag,gemm,moe",
                     help="comma-separated subset of the suite: dense, rowwise, sweep, rowcol, diag, gemm, moe")
+    ap.add_argument("--suite-match", default=None,
+                    help="sweep section: run only the cells whose workload name matches this regular expression")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
