@@ -179,9 +179,9 @@ __device__ __forceinline__ uint32_t int4_from_e4m3_bytes(uint32_t v) {
 
 // ======================================================================
 // Paired-lane helpers (PTX add/sub/mul.rn.f32x2: two independent IEEE
-// binary32 operations, round to nearest even).  On sm_103a each issues as two
-// scalar operations (instruction counters); the pairing keeps two vectors in
-// step through the same code.
+// binary32 operations, round to nearest even).  On sm_103a each issues as one
+// instruction: the fp32 instruction counts of the quantizers match one per
+// pair.  The pairing keeps two vectors in step through the same code.
 namespace ufp4 {
 
 __device__ __forceinline__ uint64_t pk2(float a, float b) {
