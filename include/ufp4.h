@@ -401,6 +401,31 @@ ufp4_status ufp4_gemm_noalloc(const ufp4_qtensor* A, const ufp4_qtensor* B, cons
  * for consumers that apply the rotation themselves. */
 ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host);
 
+/* ufp4_round_levels -- the rounding and packing step of ufp4_rht_quantize on
+ * given scaled values, for checking it against a reference on any fp32 input
+ * (UFP4 summary, section 数据集: RTNE and SR to the codebook levels and the
+ * 4-bit encodings; 2D-block tutorial, 2D 方块量化: E[roundS(x)] = x).
+ * It runs the quantizer's own code on blocks whose amax is the grid's largest
+ * level qmax (n = 1), so the block reciprocal is 1 and each value t is
+ * rounded as the quantizer rounds t = z * r.
+ *   grid       UFP4_GRID_E1M2 .. UFP4_GRID_E2M1_R2 (not MXFP8).
+ *   rounding   UFP4_ROUND_RTNE or UFP4_ROUND_SR.
+ *   scale_fmt  UFP4_SCALE_FP32 or UFP4_SCALE_UE8M0: which of the quantizer's
+ *              two arithmetic paths rounds (they agree wherever both apply).
+ *   t          DEVICE, count fp32 values, |t| <= qmax (the values a block
+ *              can hold; larger ones are outside the quantizer's domain),
+ *              16-byte aligned.
+ *   u16        DEVICE, count 16-bit draws for SR (element i uses u16[i]), 4-byte
+ *              aligned; ignored (may be NULL) for RTNE.
+ *   count      a multiple of 32 (0 does nothing).
+ *   codes      DEVICE, count / 2 bytes, 8-byte aligned: packed as the
+ *              quantizer packs them (element i in the low nibble of byte i/2
+ *              when i is even), a zero level as +0.
+ * Errors: UFP4_ERR_INVALID_ARG (enum values, count, NULL pointers),
+ * UFP4_ERR_ALIGNMENT, UFP4_ERR_CUDA (launch). */
+ufp4_status ufp4_round_levels(int32_t grid, int32_t rounding, int32_t scale_fmt, const float* t, const uint16_t* u16,
+                              int64_t count, uint8_t* codes, cudaStream_t stream);
+
 /* ufp4_device_error -- reads and clears the library's device error words on
  * the current device (synchronizes the device first).  Every device-side wait
  * of the library is bounded: a kernel whose wait gives up records the event,

@@ -81,6 +81,7 @@ def lib():
         L.orc_round_sr_array.argtypes = [i32, P, P, i64, P]
         L.orc_round_sr_array.restype = None
         L.orc_round_sr_philox.argtypes = [i32, ctypes.c_float, u64, u64, i64, u32, u32, P]
+        L.orc_round_encode_array.argtypes = [i32, i32, P, P, i64, P]
         L.orc_round_sr_philox.restype = None
         L.orc_quantize_rows_mxfp8.argtypes = [P, i64, i64, i64, i32, u64, P, P]
         L.orc_quantize_rows_mxfp8.restype = i32
@@ -146,6 +147,22 @@ def round_sr_array(grid, a: np.ndarray, u16: np.ndarray) -> np.ndarray:
     idx = np.empty(a.shape, dtype=np.uint8)
     lib().orc_round_sr_array(_grid(grid), _ptr(a), _ptr(u), a.size, _ptr(idx))
     return idx
+
+
+def round_encode_array(grid, rounding, t: np.ndarray, u16: np.ndarray | None = None) -> np.ndarray:
+    """The quantizer's element step (clamp to qmax, round, encode with the sign)
+    over given scaled values t, packed two per byte like the codes."""
+    t = np.ascontiguousarray(t, dtype=np.float32).ravel()
+    assert t.size % 2 == 0
+    if rounding == SR:
+        u = np.ascontiguousarray(u16, dtype=np.uint16).ravel()
+        assert u.size == t.size
+        up = _ptr(u)
+    else:
+        up = None
+    codes = np.empty(t.size // 2, dtype=np.uint8)
+    lib().orc_round_encode_array(_grid(grid), int(rounding), _ptr(t), up, t.size, _ptr(codes))
+    return codes
 
 
 def round_sr_philox(grid, a: float, sr_seed: int, lin0: int, count: int, stream: int = 0,

@@ -294,6 +294,18 @@ static uint32_t sr_draw(uint64_t sr_seed, uint64_t lin, uint32_t stream, uint32_
     return (j % 2 == 0) ? (word & 0xFFFFu) : (word >> 16);
 }
 
+/* [UFP4-data]: the element step of the quantizer.  The scaled value t = z * r
+ * of an element is clamped to qmax in magnitude, rounded to a level index
+ * (RTNE, or SR with the element's 16-bit draw u16) and encoded with t's sign
+ * (a zero level is +0). */
+static uint8_t element_code(int grid, int round, float t, uint32_t u16) {
+    float qmax = (float)orc_qmax(grid);
+    float a = fabsf(t);
+    if (a > qmax) a = qmax;
+    int idx = (round == ORC_RTNE) ? orc_round_rtne(grid, a) : orc_round_sr(grid, a, u16);
+    return encode(grid, signbit(t) ? 1 : 0, idx);
+}
+
 /* Test entries of the SR rule above, over many draws at once.
  *  orc_round_sr_array:  idx[i] = orc_round_sr(grid, a[i], u16[i]);
  *  orc_round_sr_philox: idx[i] = orc_round_sr(grid, a, draw of output element
@@ -306,6 +318,19 @@ void orc_round_sr_philox(int grid, float a, uint64_t sr_seed, uint64_t lin0, int
                          uint32_t group, uint8_t* idx) {
     for (int64_t i = 0; i < count; ++i)
         idx[i] = (uint8_t)orc_round_sr(grid, a, sr_draw(sr_seed, lin0 + (uint64_t)i, stream, group));
+}
+
+/* Test entry: the element step above over given scaled values t[0..count),
+ * packed two per byte as the quantizer packs them (element i in the low
+ * nibble of byte i/2 when i is even, the high nibble when odd).  u16 holds
+ * the draws for SR and may be NULL for RTNE; count is even. */
+void orc_round_encode_array(int grid, int round, const float* t, const uint16_t* u16, int64_t count,
+                            uint8_t* codes) {
+    for (int64_t i = 0; i < count; i += 2) {
+        uint8_t lo = element_code(grid, round, t[i], round == ORC_RTNE ? 0u : u16[i]);
+        uint8_t hi = element_code(grid, round, t[i + 1], round == ORC_RTNE ? 0u : u16[i + 1]);
+        codes[i / 2] = (uint8_t)(lo | (hi << 4));
+    }
 }
 
 /* --------------------------------------------------------- the quantizer
@@ -377,16 +402,12 @@ static int quantize_rows_impl(const uint16_t* x, int64_t rows, int64_t cols, int
             for (int64_t r = bi * block_rows; r < (bi + 1) * block_rows; ++r)
                 for (int64_t c = bj * block_cols; c < (bj + 1) * block_cols; ++c) {
                     float t = z[r * cols + c] * rcp;
-                    float a = fabsf(t);
-                    if (a > qmax) a = qmax;
-                    int idx;
-                    if (round == ORC_RTNE) {
-                        idx = orc_round_rtne(grid, a);
-                    } else {
+                    uint32_t u = 0;
+                    if (round != ORC_RTNE) {
                         uint64_t lin = (row0 + (uint64_t)r) * (uint64_t)cols + (uint64_t)c;
-                        idx = orc_round_sr(grid, a, sr_draw(sr_seed, lin, stream, group));
+                        u = sr_draw(sr_seed, lin, stream, group);
                     }
-                    uint8_t nib = encode(grid, signbit(t) ? 1 : 0, idx);
+                    uint8_t nib = element_code(grid, round, t, u);
                     codes[r * (cols / 2) + c / 2] |= (uint8_t)(nib << (4 * (c % 2)));
                 }
         }

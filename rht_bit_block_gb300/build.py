@@ -13,7 +13,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libufp4.so")
-SOURCES = ["api.cu", "quantize.cu", "quantize_sr.cu", "quantize_rows.cu", "dequant.cu", "gemm.cu", "noalloc.cu", "stats.cu"]
+SOURCES = ["api.cu", "quantize.cu", "quantize_sr.cu", "quantize_rows.cu", "dequant.cu", "gemm.cu", "noalloc.cu", "stats.cu",
+           "round_levels.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--fmad=false",
           "-I", os.path.join(HERE, "..", "include")]

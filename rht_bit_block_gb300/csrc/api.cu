@@ -85,6 +85,7 @@ void ensure_loaded() {
     preload_gemm_kernels();
     preload_dequant_kernels();
     preload_stats_kernels();
+    preload_round_levels_kernels();
     cudaGetLastError();  // a failed query shows up again at the launch
     done[dev] = true;
 }
@@ -435,6 +436,20 @@ ufp4_status ufp4_sign_vector(uint64_t sign_seed, int32_t n, int8_t* out_host) {
     if (!out_host || !is_pow2(n) || n > 256) return UFP4_ERR_INVALID_ARG;
     for (int i = 0; i < n; ++i) out_host[i] = (n == 1) ? 1 : (int8_t)(1 - 2 * sign_bit(sign_seed, i));
     return UFP4_OK;
+}
+
+ufp4_status ufp4_round_levels(int32_t grid, int32_t rounding, int32_t scale_fmt, const float* t,
+                              const uint16_t* u16, int64_t count, uint8_t* codes, cudaStream_t stream) {
+    if (grid < UFP4_GRID_E1M2 || grid > UFP4_GRID_E2M1_R2) return UFP4_ERR_INVALID_ARG;
+    if (rounding != UFP4_ROUND_RTNE && rounding != UFP4_ROUND_SR) return UFP4_ERR_INVALID_ARG;
+    if (scale_fmt != UFP4_SCALE_FP32 && scale_fmt != UFP4_SCALE_UE8M0) return UFP4_ERR_INVALID_ARG;
+    if (count < 0 || count % 32 != 0) return UFP4_ERR_INVALID_ARG;
+    if (count == 0) return UFP4_OK;
+    const bool sr = rounding == UFP4_ROUND_SR;
+    if (!t || !codes || (sr && !u16)) return UFP4_ERR_INVALID_ARG;
+    if ((uintptr_t)t % 16 || (uintptr_t)codes % 8 || (sr && (uintptr_t)u16 % 4)) return UFP4_ERR_ALIGNMENT;
+    ensure_loaded();
+    return cuda_status(launch_round_levels(grid, sr, scale_fmt, t, sr ? u16 : nullptr, count, codes, stream));
 }
 
 ufp4_status ufp4_rht_quantize(const void* x, int64_t rows, int64_t cols, int64_t ld, const ufp4_quant_desc* desc,

@@ -229,6 +229,11 @@ cudaError_t preload_quantize_kernels();
 cudaError_t preload_gemm_kernels();
 cudaError_t preload_dequant_kernels();
 cudaError_t preload_stats_kernels();
+cudaError_t preload_round_levels_kernels();
+// The quantizer's rounding and packing step on count given scaled values
+// (count a multiple of 32; u16: SR draws), round_levels.cu.
+cudaError_t launch_round_levels(int grid, bool sr, int sf, const float* t, const uint16_t* u16, int64_t count,
+                                uint8_t* codes, cudaStream_t st);
 // n GEMMs sharing a descriptor, each with its own workspace (the grouped call)
 cudaError_t launch_gemm_groups(const GemmArgs* gs, int n, int num_sms, cudaStream_t st);
 

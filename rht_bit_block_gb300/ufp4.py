@@ -32,7 +32,7 @@ EXPORTED = (
     "ufp4_sign_vector", "ufp4_device_error", "ufp4_status_string", "ufp4_gemm_noalloc",
     "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped", "ufp4_gemm_prepare", "ufp4_gemm_prepared",
     "ufp4_rht_quantize_batch", "ufp4_quant_error_stats", "ufp4_error_stats", "ufp4_set_quantize_wait_limit",
-    "ufp4_rht_quantize_prepare",
+    "ufp4_rht_quantize_prepare", "ufp4_round_levels",
 )
 MAX_BATCH = 4
 
@@ -88,6 +88,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     L.ufp4_gemm_grouped_workspace_size.argtypes = [i32, QT, QT, QD, ctypes.POINTER(ctypes.c_size_t)]
     L.ufp4_gemm_grouped.argtypes = [i32, QT, QT, QD, ctypes.POINTER(P), ctypes.POINTER(i64), P, ctypes.c_size_t, P]
     L.ufp4_sign_vector.argtypes = [u64, i32, P]
+    L.ufp4_round_levels.argtypes = [i32, i32, i32, P, P, i64, P, P]
     L.ufp4_device_error.argtypes = [ctypes.POINTER(i32)]
     L.ufp4_set_quantize_wait_limit.argtypes = [i64]
     L.ufp4_set_quantize_wait_limit.restype = ctypes.c_int
@@ -96,7 +97,7 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     for name in ("ufp4_rht_quantize", "ufp4_rht_quantize_grouped", "ufp4_rht_transform", "ufp4_dequantize",
                  "ufp4_gemm_workspace_size", "ufp4_gemm", "ufp4_sign_vector", "ufp4_device_error",
                  "ufp4_gemm_noalloc", "ufp4_gemm_grouped_workspace_size", "ufp4_gemm_grouped",
-                 "ufp4_gemm_prepare", "ufp4_gemm_prepared", "ufp4_rht_quantize_prepare"):
+                 "ufp4_gemm_prepare", "ufp4_gemm_prepared", "ufp4_rht_quantize_prepare", "ufp4_round_levels"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -258,6 +259,15 @@ def ufp4_sign_vector(sign_seed: int, n: int):
     buf = (ctypes.c_int8 * n)()
     _check(load().ufp4_sign_vector(sign_seed, n, buf), "ufp4_sign_vector")
     return list(buf)
+
+
+def ufp4_round_levels(grid, rounding: int, scale_fmt: int, t, codes, u16=None, stream=None):
+    """The quantizer's rounding and packing step on the scaled values t (device
+    float32, |t| <= qmax, numel a multiple of 32) into codes (device uint8,
+    numel / 2); u16: device draws for SR."""
+    g = GRIDS[grid] if isinstance(grid, str) else int(grid)
+    _check(load().ufp4_round_levels(g, rounding, scale_fmt, t.data_ptr(), None if u16 is None else u16.data_ptr(),
+                                    t.numel(), codes.data_ptr(), _stream(stream)), "ufp4_round_levels")
 
 
 def ufp4_device_error() -> int:

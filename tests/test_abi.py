@@ -123,6 +123,26 @@ def test_quantize_prepare_validation(lib):
     assert call(ufp4.make_desc(**ue8), lda=128) == 1                      # lda < K
 
 
+def test_round_levels_validation(lib):
+    """ufp4_round_levels checks its arguments before anything is launched."""
+    P = ctypes.c_void_p
+    def call(grid=0, rnd=0, fmt=0, t=0x1000, u=0x2000, count=64, codes=0x3000):
+        return lib.ufp4_round_levels(grid, rnd, fmt, P(t), P(u), count, P(codes), None)
+    assert call(count=0) == 0                   # nothing to do
+    assert call(grid=4) == 1                    # MXFP8 codes are bytes, not levels
+    assert call(grid=-1) == 1
+    assert call(rnd=2) == 1
+    assert call(fmt=2) == 1                     # two-level scales: not a rounding path of their own
+    assert call(count=48) == 1                  # a multiple of 32
+    assert call(count=-32) == 1
+    assert call(t=0) == 1
+    assert call(codes=0) == 1
+    assert call(rnd=1, u=0) == 1                # SR needs draws
+    assert call(t=0x1004) == 3                  # t 16-byte aligned
+    assert call(codes=0x3004) == 3              # codes 8-byte aligned
+    assert call(rnd=1, u=0x2002) == 3           # draws 4-byte aligned
+
+
 def test_diagnostics_validation(lib):
     desc = ufp4.make_desc(out_mask=ufp4.OUT_ROWWISE)
     q = ufp4.QTensor(0x2000, 0x3000, 64, 64, 32, 4)

@@ -346,6 +346,42 @@ def test_e1m2_and_int4_codes_are_identical():
             np.testing.assert_array_equal(se, si * np.float32(4))
 
 
+def _quantizer_draws(sr_seed, count, stream=0, group=0):
+    """16-bit SR draws of output elements 0 .. count - 1 (row-major), in the
+    quantizer's counter layout: Philox4x32-10 with key = sr_seed and counter
+    (g lo, g hi, stream, group), g = element / 8; element j of the eight takes
+    the low half of word j/2 when j is even, the high half when odd."""
+    key = np.array([sr_seed & 0xFFFFFFFF, sr_seed >> 32], dtype=np.uint32)
+    out = np.empty(count, dtype=np.uint16)
+    for g in range(count // 8):
+        w = orc.philox4x32_10(np.array([g, 0, stream, group], dtype=np.uint32), key)
+        for j in range(8):
+            out[8 * g + j] = (int(w[j // 2]) >> (16 * (j % 2))) & 0xFFFF
+    return out
+
+
+@pytest.mark.parametrize("grid", GRIDS)
+def test_round_encode_array_is_the_quantizer_element_step(grid):
+    """round_encode_array applies the quantizer's own element step.  With n = 1
+    (z = x) and every 1 x 16 block holding +-qmax, the block reciprocal is 1 in
+    both scale formats (fp32: s = qmax / qmax; UE8M0: e = 0), so the
+    quantizer's codes are the element step of x itself; for SR with the draws
+    the quantizer takes for each element."""
+    q = np.float32(orc.qmax(grid))
+    x = np.random.default_rng(11).uniform(-q, q, size=(32, 64)).astype(np.float32)
+    x[:, 0::16] = q
+    x[:, 1::16] = -q
+    x[:, 2::16] = np.float32(-1e-30)  # rounds to the zero level, written as +0
+    xb = inputs.f32_to_bf16_bits(x)
+    t = inputs.bf16_bits_to_f32(xb).ravel()
+    for fmt in (orc.SCALE_FP32, orc.SCALE_UE8M0):
+        c, _ = orc.quantize(xb, grid=grid, n=1, scale_fmt=fmt)
+        np.testing.assert_array_equal(c.ravel(), orc.round_encode_array(grid, orc.RTNE, t))
+        c, _ = orc.quantize(xb, grid=grid, n=1, scale_fmt=fmt, rounding=orc.SR, sr_seed=inputs.SR_SEED)
+        u = _quantizer_draws(inputs.SR_SEED, t.size)
+        np.testing.assert_array_equal(c.ravel(), orc.round_encode_array(grid, orc.SR, t, u))
+
+
 @pytest.mark.parametrize("grid", GRIDS)
 def test_zero_block_has_zero_scale_and_codes(grid):
     x = np.zeros((16, 64), dtype=np.uint16)
