@@ -465,6 +465,9 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
         line.update(extra)
         print(json.dumps(line), flush=True)
 
+    def want(name):  # --suite-match: the sweep cells and GEMM lines to run
+        return not args.suite_match or re.search(args.suite_match, name) is not None
+
     def scale_bytes(desc):
         per = 1 if desc.scale_fmt == ufp4.SCALE_UE8M0 else 4
         return per / (desc.block_rows * desc.block_cols)
@@ -550,7 +553,7 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
                     for rnd in (ufp4.ROUND_RTNE, ufp4.ROUND_SR):
                         name = (f"X {rows}x{cols} {grid} {block[0]}x{block[1]} "
                                 f"{'UE8M0' if fmt else 'fp32'} n={n} {'SR' if rnd else 'RTNE'}")
-                        if args.suite_match and not re.search(args.suite_match, name):
+                        if not want(name):
                             continue
                         desc = ufp4.make_desc(grid=grid, block=block, n=n, sign_seed=inputs.SIGN_SEED, scale_fmt=fmt,
                                               rounding=rnd, sr_seed=inputs.SR_SEED, out_mask=ufp4.OUT_ROWWISE)
@@ -621,6 +624,8 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
         g = torch.Generator().manual_seed(7)
         for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 32), 2.0), ("e2m1", (1, 16), 6.0),
                                        ("e2m1", (1, 32), 6.0), ("e2m1r2", (1, 16), 6.0)):
+            if not want(f"{M}x{N}x{K} {grid} {block[0]}x{block[1]} UE8M0"):
+                continue
             desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
             def operand(rows):
                 c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8)
@@ -639,57 +644,62 @@ def run_suite(args, sections=("dense", "rowwise", "sweep", "rowcol", "diag", "ge
                  kernel_ms=kms, prep_ms=pms, peak_src=f"measured bf16 burst x{kind_peak:g} (nominal ratio)")
             del A, B, ws, D
         # two-level scales: UE4M3 block bytes on the native FP4 kind, g_A g_B in the epilogue
-        desc = ufp4.make_desc(grid="e2m1", block=(1, 16), scale_fmt=ufp4.SCALE_E4M3)
-        def two_level_operand(rows):
-            c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8) & 0x77
-            sc = torch.randint(0x30, 0x48, (rows, K // 16), generator=g, dtype=torch.uint8)  # E4M3 0.5 .. 4
-            return c.to(dev), sc.to(dev), torch.full((1,), 100.0, dtype=torch.float32, device=dev)
-        A, B = two_level_operand(M), two_level_operand(N)
-        qa, qb = ufp4.qtensor(A[0], A[1], M, K, A[2]), ufp4.qtensor(B[0], B[1], N, K, B[2])
-        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
-        D = torch.empty((M, N), dtype=torch.float32, device=dev)
-        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
-        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
-        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-        emit("gemm", f"{M}x{N}x{K} e2m1 1x16 two-level (UE4M3 x fp32)", tf, "TFLOP/s", tf / (6 * pk["bf16"]),
-             6 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x6 (nominal ratio)")
-        del A, B, ws, D
+        if want(f"{M}x{N}x{K} e2m1 1x16 two-level (UE4M3 x fp32)"):
+            desc = ufp4.make_desc(grid="e2m1", block=(1, 16), scale_fmt=ufp4.SCALE_E4M3)
+            def two_level_operand(rows):
+                c = torch.randint(0, 256, (rows, K // 2), generator=g, dtype=torch.uint8) & 0x77
+                sc = torch.randint(0x30, 0x48, (rows, K // 16), generator=g, dtype=torch.uint8)  # E4M3 0.5 .. 4
+                return c.to(dev), sc.to(dev), torch.full((1,), 100.0, dtype=torch.float32, device=dev)
+            A, B = two_level_operand(M), two_level_operand(N)
+            qa, qb = ufp4.qtensor(A[0], A[1], M, K, A[2]), ufp4.qtensor(B[0], B[1], N, K, B[2])
+            ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+            D = torch.empty((M, N), dtype=torch.float32, device=dev)
+            pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+            kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+            tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+            emit("gemm", f"{M}x{N}x{K} e2m1 1x16 two-level (UE4M3 x fp32)", tf, "TFLOP/s", tf / (6 * pk["bf16"]),
+                 6 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x6 (nominal ratio)")
+            del A, B, ws, D
         # MXFP8 operands (E4M3 codes read in place by the FP8 kernel)
-        desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
-        def e4m3_operand(rows):
-            c = torch.randint(0, 0x7F, (rows, K), generator=g, dtype=torch.uint8)  # finite magnitudes
-            c = c | (torch.randint(0, 2, (rows, K), generator=g, dtype=torch.uint8) << 7)
-            sc = torch.randint(120, 132, (rows, K // 32), generator=g, dtype=torch.uint8)
-            return c.to(dev), sc.to(dev)
-        A, B = e4m3_operand(M), e4m3_operand(N)
-        qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
-        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
-        D = torch.empty((M, N), dtype=torch.float32, device=dev)
-        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
-        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
-        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-        emit("gemm", f"{M}x{N}x{K} mxfp8 1x32 E8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
-             kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (nominal ratio)")
-        del A, B, ws, D
+        if want(f"{M}x{N}x{K} mxfp8 1x32 E8M0"):
+            desc = ufp4.make_desc(grid="mxfp8", block=(1, 32), scale_fmt=ufp4.SCALE_UE8M0)
+            def e4m3_operand(rows):
+                c = torch.randint(0, 0x7F, (rows, K), generator=g, dtype=torch.uint8)  # finite magnitudes
+                c = c | (torch.randint(0, 2, (rows, K), generator=g, dtype=torch.uint8) << 7)
+                sc = torch.randint(120, 132, (rows, K // 32), generator=g, dtype=torch.uint8)
+                return c.to(dev), sc.to(dev)
+            A, B = e4m3_operand(M), e4m3_operand(N)
+            qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+            ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+            D = torch.empty((M, N), dtype=torch.float32, device=dev)
+            pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+            kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+            tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+            emit("gemm", f"{M}x{N}x{K} mxfp8 1x32 E8M0", tf, "TFLOP/s", tf / (2 * pk["bf16"]), 2 * pk["bf16"],
+                 kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (nominal ratio)")
+            del A, B, ws, D
         # fp32 block scales (the two-scale path: bf16 partials rescaled on the CUDA cores)
-        desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
-        A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-             torch.rand((M, K // 16), generator=g).add(0.5).to(dev))
-        B = (torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
-             torch.rand((N, K // 16), generator=g).add(0.5).to(dev))
-        qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
-        ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
-        D = torch.empty((M, N), dtype=torch.float32, device=dev)
-        pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
-        kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
-        tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
-        emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
-             2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
-        del A, B, ws, D
+        if want(f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)"):
+            desc = ufp4.make_desc(grid="e1m2", block=(1, 16), scale_fmt=ufp4.SCALE_FP32)
+            A = (torch.randint(0, 256, (M, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+                 torch.rand((M, K // 16), generator=g).add(0.5).to(dev))
+            B = (torch.randint(0, 256, (N, K // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev),
+                 torch.rand((N, K // 16), generator=g).add(0.5).to(dev))
+            qa, qb = ufp4.qtensor(*A, M, K), ufp4.qtensor(*B, N, K)
+            ws = torch.empty(ufp4.ufp4_gemm_workspace_size(M, N, K, desc), dtype=torch.uint8, device=dev)
+            D = torch.empty((M, N), dtype=torch.float32, device=dev)
+            pms = timed(lambda i: ufp4.ufp4_gemm_prepare(qa, qb, desc, ws, stream.cuda_stream))
+            kms = timed(lambda i: ufp4.ufp4_gemm_prepared(qa, qb, desc, D, ws, stream.cuda_stream))
+            tf = 2.0 * M * N * K / (kms / 1e3) / 1e12
+            emit("gemm", f"{M}x{N}x{K} e1m2 1x16 fp32 scales (two-scale path)", tf, "TFLOP/s", tf / (2 * pk["bf16"]),
+                 2 * pk["bf16"], kernel_ms=kms, prep_ms=pms, peak_src="measured bf16 burst x2 (FP8 peak, for comparison)")
+            del A, B, ws, D
         # the large-sweep FPROP GEMMs: 16384 x 7168 x 7168 per grid, 1x16 and 32x32 UE8M0 operands
         M5, N5, K5 = 16384, 7168, 7168
         for grid, block, kind_peak in (("e1m2", (1, 16), 2.0), ("int4", (1, 16), 2.0), ("e2m1", (1, 16), 6.0),
                                        ("e1m2", (32, 32), 2.0), ("int4", (32, 32), 2.0), ("e2m1", (32, 32), 6.0)):
+            if not want(f"{M5}x{N5}x{K5} {grid} {block[0]}x{block[1]} UE8M0"):
+                continue
             desc = ufp4.make_desc(grid=grid, block=block, scale_fmt=ufp4.SCALE_UE8M0)
             def operand(rows):
                 c = torch.randint(0, 256, (rows, K5 // 2), generator=g, dtype=torch.uint8).__and__(0x77).to(dev)
@@ -796,7 +806,8 @@ def main():
     ap.add_argument("--suite-sections", default="dense,rowwise,sweep,rowcol,diag,gemm,moe",
                     help="comma-separated subset of the suite: dense, rowwise, sweep, rowcol, diag, gemm, moe")
     ap.add_argument("--suite-match", default=None,
-                    help="sweep section: run only the cells whose workload name matches this regular expression")
+                    help="sweep and gemm sections: run only the cells and lines whose workload name matches "
+                         "this regular expression")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
