@@ -127,7 +127,7 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
     const int lj = fd.pow4 ? -fd.j : 0;
     if (SF == 2) {
         // b = E4M3(fp32(fp32(M / qmax) / g)), s = fp32(e4m3(b) * g), r = fp32(1 / s)
-        const float sb = __fdiv_rn(Mz, qmax);
+        const float sb = div_qmax_rn<GRID>(Mz);
         const uint32_t b8 = fd.g == 0.0f ? 0u : e4m3_byte(__fdiv_rn(sb, fd.g));
         const float s = __fmul_rn(e4m3_value(b8), fd.g);
         if (write) *sptr = (uint8_t)b8;
@@ -142,7 +142,7 @@ __device__ __forceinline__ float block_recip(float My, const Fold& fd, int lf, b
         return __uint_as_float((uint32_t)(254 + lf + lj - eb) << 23);
     } else {
         float sc, r;
-        scale_fp32(Mz, qmax, sc, r);
+        scale_fp32<GRID>(Mz, sc, r);
         if (write) *reinterpret_cast<float*>(sptr) = sc;
         return __fmul_rn(r, pow2_exact(lf + lj));
     }

@@ -133,9 +133,34 @@ __device__ __forceinline__ void fwht16(float v[16], int n, int seg_lane) {
 }
 
 // ------------------------------------------------------------------- scales
+// fp32(x / q) for the grid's largest level q, x >= 0, correctly rounded.  For
+// q = 1.75, 7 and 6 it uses division by a constant known in advance (P.
+// Markstein's correction step, as analysed for constant divisors by N.
+// Brisebarre and J.-M. Muller, "Accelerating correctly rounded floating-point
+// division when the divisor is known in advance", IEEE Trans. Computers 53(8),
+// 2004): q0 = RN(x z) with z = RN(1/q), the remainder x - q0 q exact in one
+// fma, then RN(q0 + rem z).  Compared with IEEE x / q on every non-negative
+// finite fp32 x: equal for every x with q = 7, and for every x >= 2^-123 with
+// q = 1.75 and q = 6 (block amaxes below 2^-120 are outside the quantizer's
+// input contract).  q = 2 is a multiplication by 0.5.
+__device__ __forceinline__ float div_known_rn(float x, float q, float z) {
+    const float q0 = __fmul_rn(x, z);
+    const float rem = __fmaf_rn(-q0, q, x);
+    return __fmaf_rn(rem, z, q0);
+}
+template <int GRID>
+__device__ __forceinline__ float div_qmax_rn(float x) {
+    if (GRID == 0) return div_known_rn(x, 1.75f, 0x1.24924ap-1f);  // z = RN(1 / 1.75)
+    if (GRID == 1) return div_known_rn(x, 7.0f, 0x1.24924ap-3f);   // z = RN(1 / 7)
+    if (GRID == 2) return div_known_rn(x, 6.0f, 0x1.555556p-3f);   // z = RN(1 / 6)
+    if (GRID == 3) return __fmul_rn(x, 0.5f);
+    return __fdiv_rn(x, grid_qmax(GRID));
+}
+
 // fp32 scale s = fp32(M / qmax); reciprocal r = fp32(1/s), 0 for s = 0.
-__device__ __forceinline__ void scale_fp32(float M, float qmax, float& s, float& r) {
-    s = __fdiv_rn(M, qmax);
+template <int GRID>
+__device__ __forceinline__ void scale_fp32(float M, float& s, float& r) {
+    s = div_qmax_rn<GRID>(M);
     r = (s == 0.0f) ? 0.0f : __frcp_rn(s);
 }
 
